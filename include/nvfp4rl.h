@@ -1,0 +1,227 @@
+/*
+ * nvfp4rl — C ABI of the NVFP4 FP4-explore hot path (GB300, sm_103a).
+ *
+ * Five calls implement the data path of Sol-RL's "FP4 Explore, BF16 Train"
+ * iteration:
+ *   nvfp4_requant       LoRA-merge the DiT weights and re-quantize them to NVFP4
+ *                       after a policy update (Sol-RL project page, "Two-Stage
+ *                       Pipeline", Stage 2: "re-quantize weights to NVFP4 for the
+ *                       next iteration"; AI Trends summary, paragraph on training
+ *                       stability: LoRA rank 32, re-quantized in real time with
+ *                       no compile step).
+ *   nvfp4_act_quant     quantize BF16 activations to NVFP4, one scale per token,
+ *                       for the NVFP4-quantized solver (Sol-RL project page,
+ *                       "Two-Stage Pipeline", Stage 1).
+ *   nvfp4_gemm          the block-scaled FP4 linear layer of that solver (same
+ *                       section: "up to 4x TFLOPs vs. BF16").
+ *   bf16_gemm           the BF16 linear layer of Stage 2 (regeneration of the
+ *                       selected seeds), used for the FP4 / BF16 ratio.
+ *   select_contrastive  keep the top K/2 and bottom K/2 seeds of N proxy rewards
+ *                       per prompt (Sol-RL project page, "Two-Stage Pipeline",
+ *                       Stage 1; AI Trends summary, paragraph on the pipeline)
+ *                       and apply the DiffusionNFT reward transform ("DiffusionNFT",
+ *                       VeRL-Omni documentation, "Algorithm").
+ *
+ * NVFP4 convention.  The pages name NVFP4 without defining its encoding; this
+ * library uses the two-level scheme
+ *     s    = amax / (6 * 448)                      fp32; per tensor for weights,
+ *                                                  per row ("per token") for
+ *                                                  activations
+ *     sf   = RNE_E4M3_sat(block_amax / (6 * s))    one E4M3 scale per 16
+ *                                                  consecutive K-elements
+ *     code = RNE_E2M1_sat(x / (sf * s))            E2M1, sign kept, saturating
+ * with every scale operation an IEEE fp32 operation (round to nearest even):
+ * d = 6*s; v = block_amax / d (a true division); den = sf*s; q = x / den.  A
+ * zero s gives sf = 0 everywhere; a block whose den is 0 emits code 0x0.
+ *
+ * Data layouts (all row-major, K innermost).
+ *   codes  [rows, K/2] bytes: byte k/2 holds the code of element k (even) in
+ *          bits 0..3 and of element k+1 in bits 4..7.  E2M1 code: bit 3 sign,
+ *          bits 2..1 exponent (bias 1), bit 0 mantissa.
+ *   sf     nvfp4_sf_bytes(rows, K) bytes in the 128x4 blocked layout that the
+ *          tensor cores read: tile (R, C) covers rows 128R..128R+127 and 16-element
+ *          K-blocks 4C..4C+3 and is 512 contiguous bytes; tiles are stored
+ *          R-major (tile index R * K/64 + C); inside a tile the byte of (row, kblk)
+ *          is at (row % 32) * 16 + ((row / 32) % 4) * 4 + kblk % 4.  Rows from
+ *          `rows` up to the next multiple of 128 are padding and are written as 0.
+ *          E4M3 scale byte: sign 0, bits 6..3 exponent (bias 7), bits 2..0 mantissa.
+ *   s      fp32: one value (weights) or one per row (activations).
+ *
+ * Conventions shared by every call.
+ *   - Pointers marked "device" are CUDA device (or managed) memory owned by the
+ *     caller; the library never allocates, frees or retains them.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *     stream).  Every call only enqueues work on it and returns; outputs are
+ *     valid once the stream reaches that point.  No call synchronizes.
+ *   - Arguments are validated before any CUDA call: NULL required pointers give
+ *     NVFP4_ERR_NULL, bad sizes NVFP4_ERR_SHAPE, device pointers not 16-byte
+ *     aligned NVFP4_ERR_ALIGN (4-byte for fp32 scalars and vectors).  A current
+ *     device that is not compute capability 10.3 gives NVFP4_ERR_ARCH; a failed
+ *     CUDA call or launch gives NVFP4_ERR_CUDA.  Nothing is launched on error.
+ *   - Device-side failures never trap: every wait inside a kernel is bounded, and
+ *     a kernel that gives up records NVFP4_ERR_TIMEOUT in a device status word
+ *     read by nvfp4_device_status().
+ *   - No C++ exception crosses this interface.
+ *   - Sizes: 1 <= K, K % 64 == 0 for the NVFP4 calls; rows (M, N) may be 0 (the
+ *     call is then a no-op) and need not be multiples of anything except where
+ *     stated.
+ */
+#ifndef NVFP4RL_H
+#define NVFP4RL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_NULL = 1,
+    NVFP4_ERR_SHAPE = 2,
+    NVFP4_ERR_ALIGN = 3,
+    NVFP4_ERR_ARCH = 4,
+    NVFP4_ERR_CUDA = 5,
+    NVFP4_ERR_TIMEOUT = 6
+} nvfp4_status;
+
+enum { NVFP4_W_BF16 = 0, NVFP4_W_FP32 = 1 };
+
+/* Size in bytes of a scale-factor buffer for a [rows, K] NVFP4 tensor. */
+static inline size_t nvfp4_sf_bytes(int64_t rows, int64_t K) {
+    return (size_t)((rows + 127) / 128) * 128u * (size_t)(K / 16);
+}
+
+/* Byte offset of the scale of (row, kblk) in that buffer (kblk = k / 16). */
+static inline size_t nvfp4_sf_offset(int64_t row, int64_t kblk, int64_t K) {
+    return (size_t)(((row / 128) * (K / 64) + kblk / 4) * 512 + (row % 32) * 16 +
+                    ((row / 32) % 4) * 4 + kblk % 4);
+}
+
+/*
+ * nvfp4_requant — W' = W + (alpha / r) * B * A, then per-tensor NVFP4.
+ *   W      device, [N, K], bf16 (w_dtype NVFP4_W_BF16) or fp32 (NVFP4_W_FP32).
+ *   A      device, [r, K] fp32, or NULL;  B  device, [N, r] fp32, or NULL.
+ *          r == 0 or A == NULL or B == NULL quantizes W without a merge.
+ *          0 <= r <= 64.  The merge is, per element, acc = +0 followed by
+ *          acc = fma(B[n,j], A[j,k], acc) for j = 0..r-1 in order, then
+ *          w' = fma(alpha / r, acc, W[n,k]) (fp32, alpha / r rounded once).
+ *   codes  device, [N, K/2] bytes (out).
+ *   sf     device, nvfp4_sf_bytes(N, K) bytes (out, padding rows written 0).
+ *   s_t    device, one fp32 (out): amax(|W'|) / 2688.  Also used as the amax
+ *          accumulator while the call runs, so it must not alias other buffers.
+ *   K % 64 == 0, K <= 1 << 20, N < 2^31.
+ * Enqueues a memset and three kernels (merge + amax; merge + quantize; finalize s_t).
+ */
+nvfp4_status nvfp4_requant(const void* W, int w_dtype, const float* A, const float* B, int r,
+                           float alpha, int64_t N, int64_t K, uint8_t* codes, uint8_t* sf,
+                           float* s_t, void* stream);
+
+/*
+ * nvfp4_act_quant — per-row ("per token") NVFP4 of BF16 activations.
+ *   X      device, [M, K] bf16.
+ *   codes  device, [M, K/2] bytes (out).
+ *   sf     device, nvfp4_sf_bytes(M, K) bytes (out, padding rows written 0).
+ *   s_row  device, [M] fp32 (out): amax(|X[m,:]|) / 2688.
+ *   K % 64 == 0, K <= 32768, M < 2^31.  One kernel, one pass over X.
+ */
+nvfp4_status nvfp4_act_quant(const void* X, int64_t M, int64_t K, uint8_t* codes, uint8_t* sf,
+                             float* s_row, void* stream);
+
+/*
+ * nvfp4_gemm — Y = bf16_RNE( s_a[m] * s_w * sum_k a_hat[m,k] * w_hat[n,k] + bias[n] ),
+ * where a_hat = e2m1(code) * e4m3(sf) of the activations and w_hat likewise of
+ * the weights; the sum runs on the tensor cores (tcgen05 block-scaled FP4 MMA)
+ * with fp32 accumulation.
+ *   a_codes, a_sf, a_srow   device, activations as written by nvfp4_act_quant:
+ *                           [M, K/2], nvfp4_sf_bytes(M, K), [M] fp32.
+ *   w_codes, w_sf, w_st     device, weights as written by nvfp4_requant:
+ *                           [N, K/2], nvfp4_sf_bytes(N, K), one fp32.
+ *   bias                    device, [N] bf16, or NULL for none.
+ *   Y                       device, [M, N] bf16 (out).
+ *   K % 64 == 0, N % 8 == 0, M, N < 2^31.
+ */
+nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_srow,
+                        const uint8_t* w_codes, const uint8_t* w_sf, const float* w_st,
+                        const void* bias, void* Y, int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * bf16_gemm — Y = bf16_RNE( X * W^T + bias ), bf16 operands, fp32 accumulation on
+ * the tensor cores (tcgen05 kind::f16).
+ *   X [M, K] bf16, W [N, K] bf16, bias [N] bf16 or NULL, Y [M, N] bf16 (out); device.
+ *   K % 8 == 0, N % 8 == 0, M, N < 2^31.
+ */
+nvfp4_status bf16_gemm(const void* X, const void* W, const void* bias, void* Y, int64_t M,
+                       int64_t N, int64_t K, void* stream);
+
+/*
+ * select_contrastive — contrastive filter plus the DiffusionNFT reward transform.
+ *   rewards  device, [P, N] fp32 proxy rewards (finite).
+ *   idx      device, [P, K] int32 (out): slots 0..K/2-1 hold the seeds of the K/2
+ *            largest rewards ordered by (reward descending, seed ascending); slots
+ *            K/2..K-1 the seeds of the K/2 smallest, by (reward ascending, seed
+ *            ascending).  -0 and +0 compare equal.
+ *   r_out    device, [P, K] fp32 (out), or NULL to skip the transform:
+ *            r = 1/2 + 1/2 clip((x - mean_p) / Z, -1, 1) where x is the selected
+ *            raw reward, mean_p the mean of prompt p's K selected rewards, and Z the
+ *            population standard deviation of all P*K selected rewards
+ *            (global_std = 1, the default of the page) or of prompt p's K
+ *            (global_std = 0); Z == 0 gives r = 1/2.  Accumulated in fp64.
+ *   0 < K <= N, K even, N <= 4096, 0 <= P < 2^31.  One kernel (one CTA).
+ */
+nvfp4_status select_contrastive(const float* rewards, int P, int N, int K, int global_std,
+                                int32_t* idx, float* r_out, void* stream);
+
+/* ---------------------------------------------------------------- diagnostics */
+
+/* Human-readable name of a status code (static storage). */
+const char* nvfp4_status_string(nvfp4_status s);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int nvfp4_version(void);
+
+/*
+ * Reads the device status word of the current device (NVFP4_OK, or
+ * NVFP4_ERR_TIMEOUT if some kernel gave up on a bounded wait since the last
+ * clear) into *out (host).  clear != 0 resets it afterwards.  Synchronizes the
+ * device.  Returns NVFP4_ERR_CUDA if the device cannot be read.
+ */
+nvfp4_status nvfp4_device_status(int* out, int clear);
+
+/* ---------------------------------------------------------------- test hooks
+ * Exported for the test-suite: each runs, over n independent elements, the very
+ * device function the quantizers use, so that their rounding can be checked
+ * exhaustively.  All buffers are device memory; n >= 0.
+ */
+
+/* codes[i] = RNE_E2M1_sat(q[i]) (sign kept), one code per byte. */
+nvfp4_status nvfp4_test_e2m1(const float* q, uint8_t* codes, int64_t n, void* stream);
+
+/* codes[i] = RNE_E4M3_sat(v[i]) for v[i] >= 0. */
+nvfp4_status nvfp4_test_e4m3(const float* v, uint8_t* codes, int64_t n, void* stream);
+
+/* codes[i] = RNE_E2M1_sat(fl32(x[i] / den[i])) for den[i] > 0, through the
+ * quantizers' reciprocal fast path with its exact-division fallback. */
+nvfp4_status nvfp4_test_e2m1_quotient(const float* x, const float* den, uint8_t* codes,
+                                      int64_t n, void* stream);
+
+/* codes[i] = RNE_E4M3_sat(fl32(v[i] / d[i])) for v[i] >= 0, d[i] > 0, through the
+ * quantizers' reciprocal fast path with its exact-division fallback. */
+nvfp4_status nvfp4_test_e4m3_quotient(const float* v, const float* d, uint8_t* codes, int64_t n,
+                                      void* stream);
+
+/*
+ * Launches one CTA that waits on a shared-memory barrier nothing will ever
+ * complete, through the same bounded wait the GEMM pipelines use, with a limit
+ * of timeout_ns (1e3 .. 1e10).  The kernel must give up, record
+ * NVFP4_ERR_TIMEOUT in the device status word and exit; the context stays
+ * usable.
+ */
+nvfp4_status nvfp4_test_wait_timeout(int64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4RL_H */

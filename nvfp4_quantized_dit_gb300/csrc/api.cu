@@ -1,0 +1,295 @@
+// extern "C" entry points of libnvfp4rl (declared and documented in nvfp4rl.h).
+//
+// Every call validates its arguments before touching CUDA, resolves the current
+// device (cached: compute capability, SM count, the address of the device status
+// word), encodes TMA tensor maps where a GEMM needs them, and enqueues kernels on
+// the caller's stream.  No call allocates, frees or synchronizes (except
+// nvfp4_device_status, documented as synchronizing).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace nvfp4rl {
+
+// Device status word: 0, or the first failure a kernel recorded (NVFP4_ERR_TIMEOUT).
+__device__ int g_status_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceInfo {
+    bool checked = false;
+    bool arch_ok = false;
+    int num_sms = 0;
+    int* status = nullptr;
+};
+
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_mutex;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool misaligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) != 0; }
+
+nvfp4_status resolve(void* stream, LaunchCtx* ctx) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return NVFP4_ERR_CUDA;
+    }
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceInfo& d = g_devices[dev];
+    if (!d.checked) {
+        int major = 0, minor = 0, sms = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return NVFP4_ERR_CUDA;
+        }
+        d.arch_ok = (major == 10 && minor == 3);
+        d.num_sms = sms;
+        if (d.arch_ok) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_status_word) != cudaSuccess) {
+                cudaGetLastError();
+                return NVFP4_ERR_CUDA;
+            }
+            d.status = static_cast<int*>(p);
+        }
+        d.checked = true;
+    }
+    if (!d.arch_ok) return NVFP4_ERR_ARCH;
+    ctx->stream = static_cast<cudaStream_t>(stream);
+    ctx->status = d.status;
+    ctx->num_sms = d.num_sms;
+    cudaGetLastError();  // start from a clean error state
+    return NVFP4_OK;
+}
+
+nvfp4_status from_cuda(cudaError_t e) { return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA; }
+
+bool encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr) {
+            cudaGetLastError();
+            return false;
+        }
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    *out = g_encode;
+    return true;
+}
+
+// 2-D K-major tensor [rows, inner] with a (box_inner x box_rows) box, 128-byte swizzle.
+bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
+               uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    if (!encoder(&enc)) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
+
+}  // namespace
+}  // namespace nvfp4rl
+
+using namespace nvfp4rl;
+
+extern "C" {
+
+const char* nvfp4_status_string(nvfp4_status s) {
+    switch (s) {
+        case NVFP4_OK: return "NVFP4_OK";
+        case NVFP4_ERR_NULL: return "NVFP4_ERR_NULL";
+        case NVFP4_ERR_SHAPE: return "NVFP4_ERR_SHAPE";
+        case NVFP4_ERR_ALIGN: return "NVFP4_ERR_ALIGN";
+        case NVFP4_ERR_ARCH: return "NVFP4_ERR_ARCH";
+        case NVFP4_ERR_CUDA: return "NVFP4_ERR_CUDA";
+        case NVFP4_ERR_TIMEOUT: return "NVFP4_ERR_TIMEOUT";
+    }
+    return "NVFP4_ERR_UNKNOWN";
+}
+
+int nvfp4_version(void) { return 100; }
+
+nvfp4_status nvfp4_requant(const void* W, int w_dtype, const float* A, const float* B, int r,
+                           float alpha, int64_t N, int64_t K, uint8_t* codes, uint8_t* sf,
+                           float* s_t, void* stream) {
+    if (w_dtype != NVFP4_W_BF16 && w_dtype != NVFP4_W_FP32) return NVFP4_ERR_SHAPE;
+    if (r < 0 || r > 64 || N < 0 || N > kMaxRows || K <= 0 || K % 64 != 0 || K > (1 << 20))
+        return NVFP4_ERR_SHAPE;
+    if (s_t == nullptr) return NVFP4_ERR_NULL;
+    if (misaligned(s_t, 4)) return NVFP4_ERR_ALIGN;
+    const bool merge = r > 0 && A != nullptr && B != nullptr;
+    if (N > 0) {
+        if (W == nullptr || codes == nullptr || sf == nullptr) return NVFP4_ERR_NULL;
+        if (misaligned(W, 16) || misaligned(codes, 16) || misaligned(sf, 16)) return NVFP4_ERR_ALIGN;
+        if (merge && (misaligned(A, 16) || misaligned(B, 4))) return NVFP4_ERR_ALIGN;
+    }
+    LaunchCtx ctx;
+    nvfp4_status st = resolve(stream, &ctx);
+    if (st != NVFP4_OK) return st;
+    if (N == 0) return from_cuda(cudaMemsetAsync(s_t, 0, sizeof(float), ctx.stream));
+    const float c = merge ? alpha / static_cast<float>(r) : 0.0f;
+    return from_cuda(launch_requant(ctx, W, w_dtype, merge ? A : nullptr, merge ? B : nullptr,
+                                    merge ? r : 0, c, N, K, codes, sf, s_t));
+}
+
+nvfp4_status nvfp4_act_quant(const void* X, int64_t M, int64_t K, uint8_t* codes, uint8_t* sf,
+                             float* s_row, void* stream) {
+    if (M < 0 || M > kMaxRows || K <= 0 || K % 64 != 0 || K > 32768) return NVFP4_ERR_SHAPE;
+    if (M == 0) return NVFP4_OK;
+    if (X == nullptr || codes == nullptr || sf == nullptr || s_row == nullptr) return NVFP4_ERR_NULL;
+    if (misaligned(X, 16) || misaligned(codes, 16) || misaligned(sf, 16) || misaligned(s_row, 4))
+        return NVFP4_ERR_ALIGN;
+    LaunchCtx ctx;
+    nvfp4_status st = resolve(stream, &ctx);
+    if (st != NVFP4_OK) return st;
+    return from_cuda(launch_act_quant(ctx, static_cast<const __nv_bfloat16*>(X), M, K, codes, sf,
+                                      s_row));
+}
+
+nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_srow,
+                        const uint8_t* w_codes, const uint8_t* w_sf, const float* w_st,
+                        const void* bias, void* Y, int64_t M, int64_t N, int64_t K, void* stream) {
+    if (M < 0 || N < 0 || M > kMaxRows || N > kMaxRows || K <= 0 || K % 64 != 0 ||
+        K > (1 << 24) || N % 8 != 0)
+        return NVFP4_ERR_SHAPE;
+    if (M == 0 || N == 0) return NVFP4_OK;
+    if (!a_codes || !a_sf || !a_srow || !w_codes || !w_sf || !w_st || !Y) return NVFP4_ERR_NULL;
+    if (misaligned(a_codes, 16) || misaligned(a_sf, 16) || misaligned(w_codes, 16) ||
+        misaligned(w_sf, 16) || misaligned(Y, 16) || misaligned(a_srow, 4) ||
+        misaligned(w_st, 4) || (bias && misaligned(bias, 16)))
+        return NVFP4_ERR_ALIGN;
+    LaunchCtx ctx;
+    nvfp4_status st = resolve(stream, &ctx);
+    if (st != NVFP4_OK) return st;
+    CUtensorMap ta, tb;
+    if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, (uint64_t)K / 2, (uint64_t)M,
+                   (uint64_t)K / 2, 128, 128) ||
+        !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_codes, (uint64_t)K / 2, (uint64_t)N,
+                   (uint64_t)K / 2, 128, 256))
+        return NVFP4_ERR_CUDA;
+    return from_cuda(launch_gemm_nvfp4(ctx, ta, tb, a_sf, w_sf, a_srow, w_st,
+                                       static_cast<const __nv_bfloat16*>(bias),
+                                       static_cast<__nv_bfloat16*>(Y), M, N, K));
+}
+
+nvfp4_status bf16_gemm(const void* X, const void* W, const void* bias, void* Y, int64_t M,
+                       int64_t N, int64_t K, void* stream) {
+    if (M < 0 || N < 0 || M > kMaxRows || N > kMaxRows || K <= 0 || K % 8 != 0 ||
+        K > (1 << 24) || N % 8 != 0)
+        return NVFP4_ERR_SHAPE;
+    if (M == 0 || N == 0) return NVFP4_OK;
+    if (!X || !W || !Y) return NVFP4_ERR_NULL;
+    if (misaligned(X, 16) || misaligned(W, 16) || misaligned(Y, 16) || (bias && misaligned(bias, 16)))
+        return NVFP4_ERR_ALIGN;
+    LaunchCtx ctx;
+    nvfp4_status st = resolve(stream, &ctx);
+    if (st != NVFP4_OK) return st;
+    CUtensorMap ta, tb;
+    if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)K, (uint64_t)M,
+                   (uint64_t)K * 2, 64, 128) ||
+        !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)K, (uint64_t)N,
+                   (uint64_t)K * 2, 64, 256))
+        return NVFP4_ERR_CUDA;
+    return from_cuda(launch_gemm_bf16(ctx, ta, tb, static_cast<const __nv_bfloat16*>(bias),
+                                      static_cast<__nv_bfloat16*>(Y), M, N, K));
+}
+
+nvfp4_status select_contrastive(const float* rewards, int P, int N, int K, int global_std,
+                                int32_t* idx, float* r_out, void* stream) {
+    if (P < 0 || N < 1 || N > 1024 || K <= 0 || K % 2 != 0 || K > N) return NVFP4_ERR_SHAPE;
+    if (P == 0) return NVFP4_OK;
+    if (rewards == nullptr || idx == nullptr) return NVFP4_ERR_NULL;
+    if (misaligned(rewards, 4) || misaligned(idx, 4) || (r_out && misaligned(r_out, 4)))
+        return NVFP4_ERR_ALIGN;
+    LaunchCtx ctx;
+    nvfp4_status st = resolve(stream, &ctx);
+    if (st != NVFP4_OK) return st;
+    return from_cuda(launch_select(ctx, rewards, P, N, K, global_std ? 1 : 0, idx, r_out));
+}
+
+nvfp4_status nvfp4_device_status(int* out, int clear) {
+    if (out == nullptr) return NVFP4_ERR_NULL;
+    LaunchCtx ctx;
+    nvfp4_status st = resolve(nullptr, &ctx);
+    if (st != NVFP4_OK) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) {
+        cudaGetLastError();
+        return NVFP4_ERR_CUDA;
+    }
+    if (cudaMemcpyFromSymbol(out, g_status_word, sizeof(int)) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (clear) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_status_word, &zero, sizeof(int)) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+    }
+    return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_test_e2m1(const float* q, uint8_t* codes, int64_t n, void* stream) {
+    if (n < 0) return NVFP4_ERR_SHAPE;
+    if (n == 0) return NVFP4_OK;
+    if (!q || !codes) return NVFP4_ERR_NULL;
+    if (misaligned(q, 4)) return NVFP4_ERR_ALIGN;
+    LaunchCtx ctx;
+    nvfp4_status st = resolve(stream, &ctx);
+    return st != NVFP4_OK ? st : from_cuda(launch_test_e2m1(ctx, q, codes, n));
+}
+
+nvfp4_status nvfp4_test_e4m3(const float* v, uint8_t* codes, int64_t n, void* stream) {
+    if (n < 0) return NVFP4_ERR_SHAPE;
+    if (n == 0) return NVFP4_OK;
+    if (!v || !codes) return NVFP4_ERR_NULL;
+    if (misaligned(v, 4)) return NVFP4_ERR_ALIGN;
+    LaunchCtx ctx;
+    nvfp4_status st = resolve(stream, &ctx);
+    return st != NVFP4_OK ? st : from_cuda(launch_test_e4m3(ctx, v, codes, n));
+}
+
+nvfp4_status nvfp4_test_e2m1_quotient(const float* x, const float* den, uint8_t* codes, int64_t n,
+                                      void* stream) {
+    if (n < 0) return NVFP4_ERR_SHAPE;
+    if (n == 0) return NVFP4_OK;
+    if (!x || !den || !codes) return NVFP4_ERR_NULL;
+    if (misaligned(x, 4) || misaligned(den, 4)) return NVFP4_ERR_ALIGN;
+    LaunchCtx ctx;
+    nvfp4_status st = resolve(stream, &ctx);
+    return st != NVFP4_OK ? st : from_cuda(launch_test_e2m1_quotient(ctx, x, den, codes, n));
+}
+
+nvfp4_status nvfp4_test_e4m3_quotient(const float* v, const float* d, uint8_t* codes, int64_t n,
+                                      void* stream) {
+    if (n < 0) return NVFP4_ERR_SHAPE;
+    if (n == 0) return NVFP4_OK;
+    if (!v || !d || !codes) return NVFP4_ERR_NULL;
+    if (misaligned(v, 4) || misaligned(d, 4)) return NVFP4_ERR_ALIGN;
+    LaunchCtx ctx;
+    nvfp4_status st = resolve(stream, &ctx);
+    return st != NVFP4_OK ? st : from_cuda(launch_test_e4m3_quotient(ctx, v, d, codes, n));
+}
+
+nvfp4_status nvfp4_test_wait_timeout(int64_t timeout_ns, void* stream) {
+    if (timeout_ns < 1000 || timeout_ns > 10000000000LL) return NVFP4_ERR_SHAPE;
+    LaunchCtx ctx;
+    nvfp4_status st = resolve(stream, &ctx);
+    return st != NVFP4_OK ? st : from_cuda(launch_test_wait_timeout(ctx, timeout_ns));
+}
+
+}  // extern "C"

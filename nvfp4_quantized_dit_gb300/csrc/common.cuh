@@ -1,0 +1,338 @@
+// Shared device helpers of the nvfp4rl library (sm_103a).
+//
+// Contents: the NVFP4 element/scale conversions used by both quantizers, the
+// bounded mbarrier wait every pipelined kernel uses, and thin inline-PTX
+// wrappers for TMA, mbarrier and the tcgen05 tensor-core instructions.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "nvfp4rl.h"
+
+namespace nvfp4rl {
+
+// ----------------------------------------------------------------- host side
+
+struct LaunchCtx {
+    cudaStream_t stream;
+    int* status;      // device status word (NVFP4_ERR_TIMEOUT is recorded here)
+    int num_sms;
+};
+
+// Implemented per translation unit; each returns cudaSuccess or the launch error.
+cudaError_t launch_act_quant(const LaunchCtx&, const __nv_bfloat16* X, int64_t M, int64_t K,
+                             uint8_t* codes, uint8_t* sf, float* s_row);
+cudaError_t launch_requant(const LaunchCtx&, const void* W, int w_dtype, const float* A,
+                           const float* B, int r, float c, int64_t N, int64_t K, uint8_t* codes,
+                           uint8_t* sf, float* s_t);
+cudaError_t launch_select(const LaunchCtx&, const float* rewards, int P, int N, int K,
+                          int global_std, int32_t* idx, float* r_out);
+cudaError_t launch_test_e2m1(const LaunchCtx&, const float* q, uint8_t* codes, int64_t n);
+cudaError_t launch_test_e4m3(const LaunchCtx&, const float* v, uint8_t* codes, int64_t n);
+cudaError_t launch_test_e2m1_quotient(const LaunchCtx&, const float* x, const float* den,
+                                      uint8_t* codes, int64_t n);
+cudaError_t launch_test_e4m3_quotient(const LaunchCtx&, const float* v, const float* d,
+                                      uint8_t* codes, int64_t n);
+// GEMMs: tensor maps are encoded by the caller (host) and passed by value.
+cudaError_t launch_gemm_nvfp4(const LaunchCtx&, const CUtensorMap& tmap_a,
+                              const CUtensorMap& tmap_b, const uint8_t* a_sf,
+                              const uint8_t* w_sf, const float* a_srow, const float* w_st,
+                              const __nv_bfloat16* bias, __nv_bfloat16* Y, int64_t M, int64_t N,
+                              int64_t K);
+cudaError_t launch_gemm_bf16(const LaunchCtx&, const CUtensorMap& tmap_a,
+                             const CUtensorMap& tmap_b, const __nv_bfloat16* bias,
+                             __nv_bfloat16* Y, int64_t M, int64_t N, int64_t K);
+cudaError_t launch_test_wait_timeout(const LaunchCtx&, int64_t timeout_ns);
+
+// ----------------------------------------------------------------- device side
+
+#if defined(__CUDACC__)
+
+// NVFP4 / E4M3 constants of the two-level scale convention.
+constexpr float kE2M1Max = 6.0f;
+constexpr float kE4M3Max = 448.0f;
+constexpr float kAmaxDiv = 2688.0f;  // 6 * 448
+
+// E2M1 codes of 8 fp32 values, round to nearest even, saturating, sign kept.
+// Element i lands in bits 4i..4i+3 of the result (element 0 in the low nibble).
+__device__ __forceinline__ uint32_t cvt_e2m1x8(float q0, float q1, float q2, float q3, float q4,
+                                               float q5, float q6, float q7) {
+    uint32_t out;
+    // cvt ...e2m1x2.f32 d, a, b puts a in the high nibble and b in the low one.
+    asm("{\n\t"
+        ".reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t"
+        "}"
+        : "=r"(out)
+        : "f"(q0), "f"(q1), "f"(q2), "f"(q3), "f"(q4), "f"(q5), "f"(q6), "f"(q7));
+    return out;
+}
+
+// E4M3 code (round to nearest even, saturating at 448) of v >= 0.
+__device__ __forceinline__ uint32_t cvt_e4m3(float v) {
+    unsigned short out;
+    // cvt ...e4m3x2.f32 d, a, b puts a in the high byte and b in the low one.
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(out) : "f"(0.0f), "f"(v));
+    return (uint32_t)out & 0xFFu;
+}
+
+// Value of a non-negative E4M3 code: exponent bits 6..3 (bias 7), mantissa 2..0.
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+    const uint32_t e = (code >> 3) & 15u, m = code & 7u;
+    if (e == 0) return (float)m * 0.001953125f;           // m * 2^-9 (subnormal), exact
+    return __uint_as_float(((e + 120u) << 23) | (m << 20)); // (1 + m/8) * 2^(e-7)
+}
+
+// True when the fp32 value with bit pattern u lies within 8 ulps of a number
+// with at most (23 - lowbits + 1) significant bits, i.e. when its low `lowbits`
+// mantissa bits are within 8 of 0 modulo 2^lowbits.  Every E2M1 rounding
+// boundary (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5) has 3 significant bits
+// (lowbits = 20); every E4M3 boundary (midpoints of adjacent codes) has at most
+// 5 (lowbits = 18).
+template <int kLowBits>
+__device__ __forceinline__ bool near_boundary(uint32_t u) {
+    constexpr uint32_t mask = (1u << kLowBits) - 1u;
+    return ((u + 8u) & mask) < 16u;
+}
+
+// RNE_E2M1_sat(fl(x / den)) for 8 values sharing den > 0, with r = fl(1/den).
+//
+// Fast path: q' = fl(x * r).  With r correctly rounded, |q' - x/den| <= 2^-23|x/den|
+// and |fl(x/den) - x/den| <= 2^-24|x/den|, so q' and the exact quotient fl(x/den)
+// are within about 3 ulps of each other.  E2M1 rounding is a step function whose
+// steps sit at 3-significant-bit numbers; if q' is more than 8 ulps away from every
+// such number, q' and fl(x/den) round to the same code.  Otherwise (and whenever
+// r is not a normal number) the value is recomputed with a true IEEE division.
+__device__ __forceinline__ uint32_t e2m1_quotient8(const float (&x)[8], float den, float r,
+                                                   bool fast_ok) {
+    float q[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(x[i], r);
+    bool any = !fast_ok;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) any |= near_boundary<20>(__float_as_uint(q[i]));
+    if (any) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            if (!fast_ok || near_boundary<20>(__float_as_uint(q[i]))) q[i] = __fdiv_rn(x[i], den);
+    }
+    return cvt_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
+}
+
+// RNE_E4M3_sat(fl(v / d)) for v >= 0, d > 0, with inv_d = fl(1/d): same argument
+// as above with the E4M3 boundaries (<= 5 significant bits).
+__device__ __forceinline__ uint32_t e4m3_quotient(float v, float d, float inv_d, bool fast_ok) {
+    float q = __fmul_rn(v, inv_d);
+    if (!fast_ok || near_boundary<18>(__float_as_uint(q))) q = __fdiv_rn(v, d);
+    return cvt_e4m3(q);
+}
+
+// A reciprocal usable by the fast paths: den in the normal range, so that 1/den is
+// a normal number too (den <= 448 * FLT_MAX / 2688 keeps 1/den >= 2^-126).
+__device__ __forceinline__ bool fast_recip_ok(float den) {
+    return den >= 1.17549435e-38f && den <= 8.5e37f;
+}
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for the phase of `bar` with the given parity to complete, for at most
+// limit_ns of device time.  On expiry it records NVFP4_ERR_TIMEOUT in *status,
+// raises the CTA's abort flag (so the CTA's other waits give up at once) and
+// returns false.  It also returns false as soon as another thread of the CTA
+// has raised the abort flag.  An iteration cap backs up the clock.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
+                                          volatile int* abort_flag, uint64_t limit_ns) {
+    const uint32_t a = smem_u32(bar);
+    if (mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 1; it < (1u << 30); ++it) {
+        if (mbar_try_wait(a, parity)) return true;
+        if ((it & 31u) == 0u) {
+            if (*abort_flag) return false;
+            if (globaltimer_ns() - t0 > limit_ns) break;
+        }
+    }
+    atomicCAS(status, 0, (int)NVFP4_ERR_TIMEOUT);
+    *abort_flag = 1;
+    return false;
+}
+
+// --- TMA (bulk tensor / bulk copies into shared memory, completion on an mbarrier)
+
+__device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                            int32_t x, int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+// --- tcgen05 (5th-generation tensor cores, accumulators in tensor memory)
+
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before_sync() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after_sync() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T, bf16 inputs, fp32 accumulation.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// D[tmem] (+)= (A * SFA)[smem] * (B * SFB)[smem]^T: E2M1 inputs with one E4M3
+// scale per 16 K-elements read from tensor memory, fp32 accumulation.
+__device__ __forceinline__ void mma_nvfp4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive (once) on `bar` when every tcgen05 operation this thread issued so far
+// has completed.
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+// Copy a 32-row x 16-byte block from shared memory into tensor memory, replicated
+// into all four 32-lane quarters.
+__device__ __forceinline__ void tmem_cp_32x128b_x4(uint32_t taddr, uint64_t src_desc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc)
+                 : "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns -> 32 registers per thread (thread i
+// reads lane base+i).
+__device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15,"
+        " %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31},"
+        " [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
+          "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+          "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
+          "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() {
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format): start address, leading and
+// stride byte offsets (all >> 4), descriptor version 1 at bits 46..47, layout
+// (swizzle) mode at bits 61..63.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo,
+                                              uint32_t layout) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+    d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)(layout & 7u) << 61;
+    return d;
+}
+constexpr uint32_t kLayoutNone = 0;
+constexpr uint32_t kLayoutSw128 = 2;
+
+#endif  // __CUDACC__
+
+}  // namespace nvfp4rl

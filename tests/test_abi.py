@@ -1,0 +1,134 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load, export every entry point include/nvfp4rl.h declares, and
+reject bad arguments with the documented status codes before any CUDA call.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "nvfp4rl.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from nvfp4_quantized_dit_gb300 import build as b
+    b.build()
+    import nvfp4_quantized_dit_gb300 as pkg
+    return pkg.library()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^(?:nvfp4_status|const char\*|int)\s+(\w+)\s*\(", text, flags=re.M)
+    return names
+
+
+def test_header_declares_the_five_calls():
+    names = _declared_functions()
+    for n in ["nvfp4_requant", "nvfp4_act_quant", "nvfp4_gemm", "bf16_gemm", "select_contrastive"]:
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    import nvfp4_quantized_dit_gb300 as pkg
+    for code, name in pkg.STATUS.items():
+        assert pkg.nvfp4_status_string(code) == name
+    assert pkg.nvfp4_version() >= 100
+
+
+def test_sf_helpers_match_header_layout():
+    import nvfp4_quantized_dit_gb300 as pkg
+    K = 256
+    assert pkg.sf_bytes(1, K) == 128 * 16 and pkg.sf_bytes(129, K) == 256 * 16
+    seen = set()
+    for row in range(256):
+        for kb in range(K // 16):
+            off = pkg.sf_offset(row, kb, K)
+            assert off not in seen
+            seen.add(off)
+    assert seen == set(range(pkg.sf_bytes(256, K)))
+    # tile (R, C) is 512 contiguous bytes; inside: (row%32)*16 + ((row/32)%4)*4 + kb%4
+    assert pkg.sf_offset(0, 0, K) == 0 and pkg.sf_offset(1, 0, K) == 16
+    assert pkg.sf_offset(32, 0, K) == 4 and pkg.sf_offset(0, 3, K) == 3
+    assert pkg.sf_offset(0, 4, K) == 512 and pkg.sf_offset(128, 0, K) == (K // 64) * 512
+
+
+A16 = 0x10000  # aligned fake addresses: never dereferenced, validation fails first
+BAD = 0x10001
+
+
+def test_act_quant_validation(lib):
+    P = ctypes.c_void_p
+    assert lib.nvfp4_act_quant(P(A16), 4, 100, P(A16), P(A16), P(A16), None) == 2  # K % 64
+    assert lib.nvfp4_act_quant(P(A16), -1, 64, P(A16), P(A16), P(A16), None) == 2
+    assert lib.nvfp4_act_quant(P(A16), 4, 64 * 1024, P(A16), P(A16), P(A16), None) == 2
+    assert lib.nvfp4_act_quant(None, 4, 64, P(A16), P(A16), P(A16), None) == 1
+    assert lib.nvfp4_act_quant(P(BAD), 4, 64, P(A16), P(A16), P(A16), None) == 3
+    assert lib.nvfp4_act_quant(None, 0, 64, None, None, None, None) == 0  # empty: no-op
+
+
+def test_requant_validation(lib):
+    P = ctypes.c_void_p
+    f = ctypes.c_float(32.0)
+    assert lib.nvfp4_requant(P(A16), 2, None, None, 0, f, 8, 64, P(A16), P(A16), P(A16), None) == 2
+    assert lib.nvfp4_requant(P(A16), 0, P(A16), P(A16), 65, f, 8, 64, P(A16), P(A16), P(A16), None) == 2
+    assert lib.nvfp4_requant(P(A16), 0, None, None, 0, f, 8, 96, P(A16), P(A16), P(A16), None) == 2
+    assert lib.nvfp4_requant(P(A16), 0, None, None, 0, f, 8, 64, P(A16), P(A16), None, None) == 1
+    assert lib.nvfp4_requant(None, 0, None, None, 0, f, 8, 64, P(A16), P(A16), P(A16), None) == 1
+    assert lib.nvfp4_requant(P(A16), 0, P(BAD), P(A16), 32, f, 8, 64, P(A16), P(A16), P(A16), None) == 3
+    assert lib.nvfp4_requant(P(A16), 0, None, None, 0, f, 8, 64, P(BAD), P(A16), P(A16), None) == 3
+
+
+def test_gemm_validation(lib):
+    P = ctypes.c_void_p
+    a = [P(A16)] * 6
+    assert lib.nvfp4_gemm(*a, None, P(A16), 16, 12, 64, None) == 2   # N % 8
+    assert lib.nvfp4_gemm(*a, None, P(A16), 16, 16, 96, None) == 2   # K % 64
+    assert lib.nvfp4_gemm(*a, None, None, 16, 16, 64, None) == 1
+    assert lib.nvfp4_gemm(*a, P(BAD), P(A16), 16, 16, 64, None) == 3  # bias alignment
+    assert lib.nvfp4_gemm(*a, None, P(A16), 0, 16, 64, None) == 0     # empty
+    assert lib.bf16_gemm(P(A16), P(A16), None, P(A16), 16, 16, 12, None) == 2
+    assert lib.bf16_gemm(P(A16), None, None, P(A16), 16, 16, 64, None) == 1
+    assert lib.bf16_gemm(P(BAD), P(A16), None, P(A16), 16, 16, 64, None) == 3
+    assert lib.bf16_gemm(P(A16), P(A16), None, P(A16), 16, 0, 64, None) == 0
+
+
+def test_select_validation(lib):
+    P = ctypes.c_void_p
+    assert lib.select_contrastive(P(A16), 1, 96, 23, 1, P(A16), None, None) == 2
+    assert lib.select_contrastive(P(A16), 1, 96, 98, 1, P(A16), None, None) == 2
+    assert lib.select_contrastive(P(A16), 1, 2000, 24, 1, P(A16), None, None) == 2
+    assert lib.select_contrastive(None, 1, 96, 24, 1, P(A16), None, None) == 1
+    assert lib.select_contrastive(P(BAD + 1), 1, 96, 24, 1, P(A16), None, None) == 3
+    assert lib.select_contrastive(None, 0, 96, 24, 1, None, None, None) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="needs a machine without a usable GPU")
+def test_well_formed_call_without_gpu_reports_cuda_error(lib):
+    P = ctypes.c_void_p
+    rc = lib.nvfp4_act_quant(P(A16), 4, 64, P(A16), P(A16), P(A16), None)
+    assert rc in (4, 5)
+    out = ctypes.c_int(-1)
+    assert lib.nvfp4_device_status(ctypes.byref(out), 0) in (4, 5)
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import nvfp4_quantized_dit_gb300 as pkg
+    with pytest.raises(ValueError):
+        pkg.nvfp4_act_quant(torch.zeros(4, 64, dtype=torch.bfloat16),
+                            codes=torch.zeros(4, 32, dtype=torch.uint8),
+                            sf=torch.zeros(pkg.sf_bytes(4, 64), dtype=torch.uint8),
+                            s_row=torch.zeros(4))
