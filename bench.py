@@ -1,0 +1,499 @@
+"""Benchmark of the NVFP4 FP4-explore hot path on one GB300 (or N replicas).
+
+One step = one pass of the whole hot path over one batch of synthetic input of
+the FLUX.1-shaped MLP up-projection (M = 8 images x 4608 tokens = 36864, K = 3072,
+N = 12288), all calls through the library's C ABI:
+  1. nvfp4_requant       LoRA (r = 32) merge of W [12288, 3072] bf16 + per-tensor NVFP4
+  2. nvfp4_act_quant     per-row NVFP4 of X [36864, 3072] bf16
+  3. nvfp4_gemm          Y = X W'^T + bias, block-scaled FP4 on the tensor cores
+  4. bf16_gemm           the BF16 counterpart (Stage 2), for the FP4 / BF16 ratio
+  5. select_contrastive  32 prompts x 96 proxy rewards -> top/bottom 12 + reward transform
+
+Prints one JSON line.  `value` is the NVFP4 GEMM throughput in TFLOP/s (2MNK per
+launch / mean CUDA-event duration of the launch over the timed steps, summed over
+ranks); the re-quantization GB/s and every other kernel's roofline are reported
+beside it.  `--impl reference` times the CPU oracle on a bounded sample of the
+same workload instead (no GPU work).
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WORKLOAD = "flux_up"
+REWARD_CFG = "iter"
+NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25  # dense NVFP4 / dense BF16 tensor rates, GB300 nominal
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash(*rel):
+    h = hashlib.sha256()
+    for r in rel:
+        with open(os.path.join(ROOT, r), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+KERNEL_SOURCES = {
+    "nvfp4_gemm": ["nvfp4_quantized_dit_gb300/csrc/gemm.cu", "nvfp4_quantized_dit_gb300/csrc/common.cuh"],
+    "bf16_gemm": ["nvfp4_quantized_dit_gb300/csrc/gemm.cu", "nvfp4_quantized_dit_gb300/csrc/common.cuh"],
+    "nvfp4_act_quant": ["nvfp4_quantized_dit_gb300/csrc/quant.cu", "nvfp4_quantized_dit_gb300/csrc/common.cuh"],
+    "nvfp4_requant": ["nvfp4_quantized_dit_gb300/csrc/quant.cu", "nvfp4_quantized_dit_gb300/csrc/common.cuh"],
+}
+
+
+def dram_traffic(kernel, workload):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel's
+    sources are unchanged since it was captured (else None)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    cur = source_hash(*KERNEL_SOURCES[kernel])
+    with open(path) as f:
+        for ln in f:
+            parts = ln.split()
+            if len(parts) >= 4 and not ln.startswith("#") and parts[0] == kernel and parts[1] == workload:
+                return float(parts[3]) if parts[2] == cur else None
+    return None
+
+
+class ClockSampler:
+    """Samples nvidia-smi clocks and throttle reasons during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=5)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and device.type == "cuda":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+# ----------------------------------------------------------------------------- workload
+
+def algorithmic_bytes(cfg, rcfg):
+    M, K, N = cfg.M, cfg.K, cfg.N
+    sf_w = (N + 127) // 128 * 128 * (K // 16)
+    sf_a = (M + 127) // 128 * 128 * (K // 16)
+    return {
+        # single read of W, A, B; write of codes, scales and s_t
+        "nvfp4_requant": N * K * 2 + 32 * K * 4 + N * 32 * 4 + N * K // 2 + sf_w + 4,
+        # read X once; write codes, scales, one fp32 per row
+        "nvfp4_act_quant": M * K * 2 + M * K // 2 + sf_a + 4 * M,
+    }
+
+
+def make_inputs(device, seed=0, rows=None):
+    import dataclasses
+    import workloads
+    cfg = workloads.LINEARS[WORKLOAD]
+    if rows:
+        cfg = dataclasses.replace(cfg, M=int(rows))
+    rcfg = workloads.REWARDS[REWARD_CFG]
+    host = {
+        "X": workloads.activations(cfg, seed),
+        "W": workloads.weight(cfg, seed),
+        "bias": workloads.bias(cfg, seed),
+        "rewards": workloads.rewards(rcfg, seed),
+    }
+    host["A"], host["B"] = workloads.lora(cfg, seed)
+    dev = {k: v.to(device) for k, v in host.items()}
+    return cfg, rcfg, host, dev
+
+
+def run_ours(args):
+    import torch
+    import nvfp4_quantized_dit_gb300 as nv
+    import workloads
+
+    world, rank, local = dist_setup()
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    nv.library()
+
+    cfg, rcfg, host, dev = make_inputs(device, rows=args.rows)
+    M, K, N = cfg.M, cfg.K, cfg.N
+    Kr = rcfg.K
+    # outputs, allocated once
+    w_codes = torch.empty(N, K // 2, dtype=torch.uint8, device=device)
+    w_sf = torch.empty(nv.sf_bytes(N, K), dtype=torch.uint8, device=device)
+    w_st = torch.empty(1, dtype=torch.float32, device=device)
+    a_codes = torch.empty(M, K // 2, dtype=torch.uint8, device=device)
+    a_sf = torch.empty(nv.sf_bytes(M, K), dtype=torch.uint8, device=device)
+    a_s = torch.empty(M, dtype=torch.float32, device=device)
+    Y4 = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+    Y16 = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+    idx = torch.empty(rcfg.P, Kr, dtype=torch.int32, device=device)
+    rr = torch.empty(rcfg.P, Kr, dtype=torch.float32, device=device)
+    names = ["nvfp4_requant", "nvfp4_act_quant", "nvfp4_gemm", "bf16_gemm", "select_contrastive"]
+    launches_per_step = {"nvfp4_requant": 3, "nvfp4_act_quant": 1, "nvfp4_gemm": 1, "bf16_gemm": 1,
+                         "select_contrastive": 1}
+
+    def step(d, events=None):
+        def mark(i):
+            if events is not None:
+                events[i].record()
+        mark(0)
+        nv.nvfp4_requant(d["W"], d["A"], d["B"], workloads.LORA_ALPHA, w_codes, w_sf, w_st)
+        mark(1)
+        nv.nvfp4_act_quant(d["X"], a_codes, a_sf, a_s)
+        mark(2)
+        nv.nvfp4_gemm((a_codes, a_sf, a_s), (w_codes, w_sf, w_st), d["bias"], out=Y4)
+        mark(3)
+        nv.bf16_gemm(d["X"], d["W"], d["bias"], out=Y16)
+        mark(4)
+        nv.select_contrastive(d["rewards"], Kr, True, True, idx, rr)
+        mark(5)
+
+    # ---- device-resident timing
+    for _ in range(args.warmup):
+        step(dev)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    clocks = ClockSampler(device.index)
+    clocks.start()
+    barrier(world, device)
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record()
+    for s in range(args.steps):
+        step(dev, ev[s])
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world, device)
+    clk = clocks.stop()
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, device)
+    per = {n: statistics.mean(ev[s][i].elapsed_time(ev[s][i + 1]) for s in range(args.steps))
+           for i, n in enumerate(names)}
+    per = {n: max_over_ranks(v, world, device) for n, v in per.items()}
+
+    # ---- end to end: pinned host inputs in, result out, every step
+    if args.no_e2e:
+        e2e_ms = float("nan")
+        h2d = d2h = 0
+    else:
+        e2e_ms, h2d, d2h = run_e2e(args, host, dev, step, Y4, idx, rr, M, N, rcfg, Kr, world, device)
+    status = nv.nvfp4_device_status()
+    return report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk, world, rank,
+                  launches_per_step)
+
+
+def run_e2e(args, host, dev, step, Y4, idx, rr, M, N, rcfg, Kr, world, device):
+    import torch
+    pinned = {k: v.pin_memory() for k, v in host.items()}
+    y_host = torch.empty(M, N, dtype=torch.bfloat16, pin_memory=True)
+    idx_host = torch.empty(rcfg.P, Kr, dtype=torch.int32, pin_memory=True)
+    r_host = torch.empty(rcfg.P, Kr, dtype=torch.float32, pin_memory=True)
+    dev2 = {k: torch.empty_like(v) for k, v in dev.items()}
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = y_host.numel() * 2 + idx_host.numel() * 4 + r_host.numel() * 4
+
+    def e2e_step():
+        for k, v in pinned.items():
+            dev2[k].copy_(v, non_blocking=True)
+        step(dev2)
+        y_host.copy_(Y4, non_blocking=True)
+        idx_host.copy_(idx, non_blocking=True)
+        r_host.copy_(rr, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world, device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    barrier(world, device)
+    return max_over_ranks(e0.elapsed_time(e1), world, device), h2d, d2h
+
+
+def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk, world, rank,
+           launches_per_step):
+    if rank != 0:
+        return None
+    M, K, N = cfg.M, cfg.K, cfg.N
+    Kr = rcfg.K
+
+    pk, pk_kind = peaks()
+    fp4_peak = pk["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
+    gemm_flops = 2.0 * M * N * K
+    ab = algorithmic_bytes(cfg, rcfg)
+    tflops4 = gemm_flops / (per["nvfp4_gemm"] * 1e-3) / 1e12
+    tflops16 = gemm_flops / (per["bf16_gemm"] * 1e-3) / 1e12
+    rq_gbs = ab["nvfp4_requant"] / (per["nvfp4_requant"] * 1e-3) / 1e9
+    aq_gbs = ab["nvfp4_act_quant"] / (per["nvfp4_act_quant"] * 1e-3) / 1e9
+    ms_per_step = elapsed_ms / args.steps
+    e2e_ms_step = e2e_ms / args.steps
+
+    def roof(bound, achieved, peak, unit, kernel):
+        return {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
+                "frac": round(achieved / peak, 4), "traffic": dram_traffic(kernel, WORKLOAD)}
+
+    out = {
+        "metric": "NVFP4 GEMM TFLOP/s (FLUX.1-shaped linears) & re-quant GB/s, % of roofline",
+        "value": round(tflops4 * world, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "nvfp4 (e2m1 x e4m3 block scale) -> fp32 accumulate -> bf16",
+        "data": "synthetic (seeded; FLUX.1-shaped weights, activations, LoRA r=32, rewards)",
+        "config": {"workload": f"FLUX.1-shaped MLP up-projection M={M} K={K} N={N} + LoRA r=32 "
+                               "requant + 32x96 reward selection (K=24)",
+                   "M": M, "K": K, "N": N, "lora_rank": 32, "prompts": rcfg.P, "seeds": rcfg.N,
+                   "selected": Kr, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (X 226 MB read, Y 906 MB written per step)"},
+        "value_basis": "mean CUDA-event duration of the nvfp4_gemm launch inside the timed steps",
+        "requant_gbs": round(rq_gbs, 1),
+        "act_quant_gbs": round(aq_gbs, 1),
+        "bf16_gemm_tflops": round(tflops16, 1),
+        "fp4_over_bf16": round(tflops4 / tflops16, 3),
+        "select_us": round(per["select_contrastive"] * 1e3, 2),
+        "kernel_ms": {n: round(v, 4) for n, v in per.items()},
+        "roofline": roof("tensor", tflops4, fp4_peak, "TFLOP/s", "nvfp4_gemm"),
+        "rooflines": {
+            "nvfp4_gemm": roof("tensor", tflops4, fp4_peak, "TFLOP/s", "nvfp4_gemm"),
+            "bf16_gemm": roof("tensor", tflops16, pk["bf16_tflops"], "TFLOP/s", "bf16_gemm"),
+            "nvfp4_requant": roof("hbm", rq_gbs, pk["hbm_gbs"], "GB/s", "nvfp4_requant"),
+            "nvfp4_act_quant": roof("hbm", aq_gbs, pk["hbm_gbs"], "GB/s", "nvfp4_act_quant"),
+        },
+        "peak_source": f"{pk_kind}: bf16 {pk['bf16_tflops']} TFLOP/s x {NOMINAL_FP4_OVER_BF16:g} "
+                       f"(nominal dense NVFP4/BF16) for NVFP4; HBM {pk['hbm_gbs']} GB/s",
+        "e2e": None if args.no_e2e else {
+            "value": round(gemm_flops / (e2e_ms_step * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
+            "ms_per_step": round(e2e_ms_step, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": sum(launches_per_step.values()) * args.steps,
+        "device_status": status,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(cfg, host, budget_s=args.cpu_budget)
+    return out
+
+
+# ----------------------------------------------------------------------------- oracle legs
+
+def _oracle_inputs(cfg, host, rows):
+    import workloads
+    xb = workloads.bf16_bits(host["X"])[rows]
+    wb = workloads.bf16_bits(host["W"])
+    return xb, wb
+
+
+def cpu_baseline(cfg, host, budget_s=12.0):
+    """The oracle, as it stands, on the host cores: NVFP4 GEMM over a row sample
+    sized to about `budget_s` seconds (the weights quantized by the oracle)."""
+    import numpy as np
+    import oracle
+    import workloads
+    oracle.build()
+    wb = workloads.bf16_bits(host["W"])
+    wc, wsf, ws = oracle.requant(wb, host["A"].numpy(), host["B"].numpy(), workloads.LORA_ALPHA)
+    rng = np.random.default_rng(0)
+    probe = np.sort(rng.choice(cfg.M, 16, replace=False))
+    ac, asf, a_s = oracle.act_quant(workloads.bf16_bits(host["X"])[probe])
+    t = time.perf_counter()
+    oracle.gemm_nvfp4(ac, asf, a_s, wc, wsf, ws, workloads.bf16_bits(host["bias"]))
+    per_row = (time.perf_counter() - t) / len(probe)
+    nrows = int(max(16, min(4096, budget_s / max(per_row, 1e-6))))
+    rows = np.sort(rng.choice(cfg.M, nrows, replace=False))
+    ac, asf, a_s = oracle.act_quant(workloads.bf16_bits(host["X"])[rows])
+    t = time.perf_counter()
+    oracle.gemm_nvfp4(ac, asf, a_s, wc, wsf, ws, workloads.bf16_bits(host["bias"]))
+    dt = time.perf_counter() - t
+    flops = 2.0 * nrows * cfg.N * cfg.K
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": f"fp64 NVFP4 GEMM oracle on {nrows} sampled rows x N={cfg.N} x K={cfg.K} "
+                      f"({dt:.1f} s), weights re-quantized by the oracle"}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step is a bounded sample of the
+    workload (requant of the full weight, act_quant + GEMM of 32 rows, selection)."""
+    import numpy as np
+    import torch
+    import oracle
+    import workloads
+    world, rank, _ = dist_setup()
+    if rank != 0:
+        return None
+    oracle.build()
+    cfg = workloads.LINEARS[WORKLOAD]
+    rcfg = workloads.REWARDS[REWARD_CFG]
+    host = {"X": workloads.activations(cfg), "W": workloads.weight(cfg), "bias": workloads.bias(cfg),
+            "rewards": workloads.rewards(rcfg)}
+    host["A"], host["B"] = workloads.lora(cfg)
+    wb = workloads.bf16_bits(host["W"])
+    xb_all = workloads.bf16_bits(host["X"])
+    bias = workloads.bf16_bits(host["bias"])
+    rows_per_step = 32
+    rng = np.random.default_rng(0)
+
+    def step():
+        wc, wsf, ws = oracle.requant(wb, host["A"].numpy(), host["B"].numpy(), workloads.LORA_ALPHA)
+        rows = np.sort(rng.choice(cfg.M, rows_per_step, replace=False))
+        ac, asf, a_s = oracle.act_quant(xb_all[rows])
+        t = time.perf_counter()
+        oracle.gemm_nvfp4(ac, asf, a_s, wc, wsf, ws, bias)
+        g = time.perf_counter() - t
+        oracle.select_contrastive(host["rewards"].numpy(), rcfg.K)
+        return g
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    gemm_s = sum(step() for _ in range(args.steps))
+    total = time.perf_counter() - t0
+    flops = 2.0 * rows_per_step * cfg.N * cfg.K * args.steps
+    v = flops / gemm_s / 1e12
+    return {
+        "impl": "reference",
+        "metric": "NVFP4 GEMM TFLOP/s (FLUX.1-shaped linears) & re-quant GB/s, % of roofline",
+        "value": round(v, 6), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp64 over NVFP4 values (oracle)", "data": "synthetic (seeded)",
+        "config": {"workload": "FLUX.1-shaped MLP up-projection M=36864 K=3072 N=12288 + LoRA r=32 "
+                               "requant + 32x96 reward selection (K=24)",
+                   "parallelism": "replicas x1 (oracle on host cores)"},
+        "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+                         "kind": "oracle",
+                         "sample": f"per step: full-weight requant, act_quant + fp64 GEMM of "
+                                   f"{rows_per_step} sampled rows, selection"},
+        "e2e": {"value": round(v, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end phase")
+    ap.add_argument("--rows", type=int, default=None,
+                    help="override M (a smaller case for profiling; the default is the full 36864)")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
+    out = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+    world, _, _ = dist_setup()
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
