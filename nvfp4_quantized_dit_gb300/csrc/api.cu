@@ -103,6 +103,22 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, ui
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Scale-factor buffer of a [rows, K] NVFP4 tensor viewed as 4-D bytes
+// {256, 2, K/64, ceil(rows/128)}: one 512-byte tile per (K-chunk of 64, 128-row
+// tile), loaded four K-chunks (2 KB) at a time; tiles or chunks past the end arrive
+// as zeros.
+bool encode_sf(CUtensorMap* map, const void* base, int64_t rows, int64_t K) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc;
+    if (!encoder(&enc)) return false;
+    const cuuint64_t dims[4] = {256, 2, (cuuint64_t)(K / 64), (cuuint64_t)((rows + 127) / 128)};
+    const cuuint64_t strides[3] = {256, 512, (cuuint64_t)(K / 64) * 512};
+    const cuuint32_t box[4] = {256, 2, 4, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
 
 }  // namespace
@@ -179,13 +195,14 @@ nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const float
     LaunchCtx ctx;
     nvfp4_status st = resolve(stream, &ctx);
     if (st != NVFP4_OK) return st;
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, tsa, tsb;
     if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, (uint64_t)K / 2, (uint64_t)M,
                    (uint64_t)K / 2, 128, 128) ||
         !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_codes, (uint64_t)K / 2, (uint64_t)N,
-                   (uint64_t)K / 2, 128, 256))
+                   (uint64_t)K / 2, 128, 128) ||
+        !encode_sf(&tsa, a_sf, M, K) || !encode_sf(&tsb, w_sf, N, K))
         return NVFP4_ERR_CUDA;
-    return from_cuda(launch_gemm_nvfp4(ctx, ta, tb, a_sf, w_sf, a_srow, w_st,
+    return from_cuda(launch_gemm_nvfp4(ctx, ta, tb, tsa, tsb, a_srow, w_st,
                                        static_cast<const __nv_bfloat16*>(bias),
                                        static_cast<__nv_bfloat16*>(Y), M, N, K));
 }
@@ -206,7 +223,7 @@ nvfp4_status bf16_gemm(const void* X, const void* W, const void* bias, void* Y, 
     if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)K, (uint64_t)M,
                    (uint64_t)K * 2, 64, 128) ||
         !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)K, (uint64_t)N,
-                   (uint64_t)K * 2, 64, 256))
+                   (uint64_t)K * 2, 64, 128))
         return NVFP4_ERR_CUDA;
     return from_cuda(launch_gemm_bf16(ctx, ta, tb, static_cast<const __nv_bfloat16*>(bias),
                                       static_cast<__nv_bfloat16*>(Y), M, N, K));

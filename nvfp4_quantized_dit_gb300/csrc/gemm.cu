@@ -8,16 +8,25 @@
 //            Stage 1: "up to 4x TFLOPs vs. BF16").
 //  * BF16:   Y = bf16( X W^T + bias ) with kind::f16 (Stage 2's BF16 layers).
 //
-// One persistent CTA per SM, 192 threads:
-//   warp 0       TMA producer: A/B tiles (128-byte swizzle) and, for NVFP4, the
-//                scale tiles (bulk copies) into a 4-stage shared-memory ring;
-//   warp 1       allocates 512 tensor-memory columns; lane 0 issues the MMAs
-//                (scale tiles first go shared -> tensor memory with tcgen05.cp);
-//   warps 2..5   epilogue: tensor memory -> registers (tcgen05.ld), scale, bias,
-//                bf16, staged through shared memory into coalesced global stores.
-// Tile 128 x 256 (M x N), 128 bytes of K per stage row (256 E2M1 or 64 BF16
-// elements), fp32 accumulator in tensor-memory columns 0..255.  NVFP4 scale
-// tiles for stage s live in columns 256 + 48 s (A: 4 per MMA, B: 8 per MMA).
+// Persistent kernel on CTA pairs (clusters of two): each pair computes a 256 x 256
+// tile with 2-CTA MMAs (tcgen05 cta_group::2, M = 256).  Each CTA loads its own 128
+// rows of A and one half of B's 256 rows, so each SM stores and reads only half of
+// the B tile; the even CTA issues the MMAs for both.  224 threads per CTA:
+//   warp 0       TMA producer (both CTAs): A, half of B and, for NVFP4, the scale
+//                tiles into a shared-memory ring whose completion is counted on the
+//                even CTA's barriers;
+//   warp 1       allocates 512 tensor-memory columns in both CTAs (collectively);
+//                lane 0 of the even CTA issues the MMAs and releases each stage
+//                to both CTAs;
+//   warps 2..9   epilogue (both CTAs), two warps per tensor-memory lane quarter,
+//                128 columns each: tensor memory -> registers (tcgen05.ld, all
+//                issued before one wait), release of the accumulator, then scale,
+//                bias, bf16, staged through shared memory into coalesced stores;
+//   warp 10      NVFP4, even CTA: copies each stage's scale tiles shared -> tensor
+//                memory in both CTAs (tcgen05.cp) and hands the stage to the MMAs.
+// Per CTA: fp32 accumulator in tensor-memory columns 0..255 (its 128 rows x 256);
+// NVFP4 scale tiles for stage s in columns 256 + 48 s (A: 4 per MMA for its 128
+// rows, B: 8 per MMA for all 256 rows).
 //
 // Every mbarrier wait is bounded (common.cuh: mbar_wait); on expiry the kernel
 // records NVFP4_ERR_TIMEOUT, drains its own copies and MMAs (again bounded),
@@ -27,44 +36,52 @@
 namespace nvfp4rl {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int kStages = 4;
-constexpr int kThreads = 192;
-constexpr uint32_t kATileBytes = BM * 128;    // 16 KB
-constexpr uint32_t kBTileBytes = BN * 128;    // 32 KB
-constexpr uint32_t kSFAStageBytes = 4 * 512;  // 128 rows x 4 K-chunks of 64
-constexpr uint32_t kSFBStageBytes = 8 * 512;  // 256 rows x 4 K-chunks of 64
-constexpr uint32_t kEpiWarpBytes = 32 * 64;   // 32 rows x 32 bf16
-constexpr uint32_t kEpiBytes = 4 * kEpiWarpBytes;
+constexpr int BM = 128;        // rows of A / D per CTA
+constexpr int BN = 256;        // columns of D per pair (rows of B)
+constexpr int kPair = 2;       // CTAs per cluster (one 2-CTA MMA)
+constexpr int kEpiWarps = 8;
+constexpr int kThreads = (2 + kEpiWarps + 1) * 32;
+constexpr int kCopierWarp = 2 + kEpiWarps;
+constexpr uint32_t kATileBytes = BM * 128;            // 16 KB: 128 rows x 128 B
+constexpr uint32_t kBHalfBytes = (BN / kPair) * 128;  // 16 KB: this CTA's 128 rows of B
+constexpr uint32_t kSFAStageBytes = 4 * 512;          // 128 rows x 4 K-chunks of 64
+constexpr uint32_t kSFBStageBytes = 8 * 512;          // 256 rows x 4 K-chunks of 64
+constexpr uint32_t kEpiWarpBytes = 32 * 64;           // 32 rows x 32 bf16
+constexpr uint32_t kEpiBytes = kEpiWarps * kEpiWarpBytes;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemBase = 256;
 constexpr uint32_t kSfTmemPerStage = 48;
+constexpr uint16_t kBothCtas = 0x3;
+constexpr uint16_t kEvenCta = 0x1;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;  // 4 s: far beyond any legitimate wait
 constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for copies already in flight
 
 template <bool kFP4>
 struct Cfg {
-    static constexpr uint32_t kStageBytes =
-        kATileBytes + kBTileBytes + (kFP4 ? kSFAStageBytes + kSFBStageBytes : 0u);
+    static constexpr int kStages = kFP4 ? 5 : 6;
+    // Bytes this CTA loads per stage (the even CTA expects twice as many).
+    static constexpr uint32_t kLoadBytes =
+        kATileBytes + kBHalfBytes + (kFP4 ? kSFAStageBytes + kSFBStageBytes : 0u);
+    static constexpr uint32_t kStageBytes = kLoadBytes;
     static constexpr uint32_t kBarrierBytes = 256;
     static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarrierBytes;
 };
-static_assert(Cfg<true>::kSmemBytes <= 232448, "shared memory budget");
+static_assert(Cfg<true>::kSmemBytes <= 232448 && Cfg<false>::kSmemBytes <= 232448,
+              "shared memory budget");
 static_assert(Cfg<true>::kStageBytes % 1024 == 0 && Cfg<false>::kStageBytes % 1024 == 0,
               "stages must keep 1024-byte alignment for the 128-byte swizzle");
+static_assert(kSfTmemBase + Cfg<true>::kStages * kSfTmemPerStage <= kTmemCols, "tensor memory");
 
 // Instruction descriptors (tcgen05, 32 bits): bits 4-5 accumulator format
 // (1 = f32), 7-9 A format, 10-12 B format, 15/16 A/B major (0 = K-major),
-// 17-22 N >> 3, 24-28 M >> 4.  For the block-scaled kinds bit 23 selects the
-// scale type (0 = UE4M3) and the E2M1 format code is 1.
+// 17-22 N >> 3, 24-28 M >> 4 (M = 256 for the pair).  For the block-scaled kinds
+// bit 23 selects the scale type (0 = UE4M3) and the E2M1 format code is 1.
+constexpr uint32_t kMmaM = BM * kPair;
 constexpr uint32_t idesc_bf16() {
-    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-           ((uint32_t)(BM >> 4) << 24);
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((kMmaM >> 4) << 24);
 }
 constexpr uint32_t idesc_nvfp4() {
-    return (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | (0u << 23) |
-           ((uint32_t)(BM >> 4) << 24);
+    return (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | (0u << 23) | ((kMmaM >> 4) << 24);
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
@@ -73,8 +90,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 struct GemmArgs {
-    const uint8_t* a_sf;
-    const uint8_t* b_sf;
     const float* a_srow;
     const float* w_st;
     const __nv_bfloat16* bias;
@@ -83,42 +98,58 @@ struct GemmArgs {
     int* status;
 };
 
+// Pair tiles: tile t covers m-blocks 2*(t % num_mp) + {0, 1} (one per CTA) and
+// n-block t / num_mp; cluster c walks t = c, c + num_clusters, ...
+struct Sched {
+    int num_m, num_mp, total, first, step;
+    __device__ Sched(int M, int N) {
+        num_m = (M + BM - 1) / BM;
+        num_mp = (num_m + kPair - 1) / kPair;
+        total = num_mp * ((N + BN - 1) / BN);
+        first = (int)(blockIdx.x / kPair);
+        step = (int)(gridDim.x / kPair);
+    }
+};
+
 template <bool kFP4>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
-                const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args) {
+                const __grid_constant__ CUtensorMap tmap_b,
+                const __grid_constant__ CUtensorMap tmap_sfa,
+                const __grid_constant__ CUtensorMap tmap_sfb, const GemmArgs args) {
     using C = Cfg<kFP4>;
+    constexpr int S = C::kStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* epi = smem + kStages * C::kStageBytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(epi + kEpiBytes);
-    uint64_t* empty = full + kStages;
-    uint64_t* tmem_full = empty + kStages;
-    uint64_t* tmem_empty = tmem_full + 1;
+    uint8_t* epi = smem + S * C::kStageBytes;
+    uint64_t* full = reinterpret_cast<uint64_t*>(epi + kEpiBytes);  // used in the even CTA
+    uint64_t* empty = full + S;
+    uint64_t* sfready = empty + S;
+    uint64_t* tmem_full = sfready + S;
+    uint64_t* tmem_empty = tmem_full + 1;  // used in the even CTA
     uint64_t* drain = tmem_empty + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0 (even, issues the MMAs) or 1
+    const bool leader = rank == 0;
     const int M = args.M, N = args.N, K = args.K;
-    const int num_m = (M + BM - 1) / BM;
-    const int num_n = (N + BN - 1) / BN;
-    const int num_tiles = num_m * num_n;
+    const Sched sch(M, N);
     // MMA steps along K: 64 E2M1 (32 bytes) or 16 BF16 (32 bytes) each; 4 per stage.
     const int k_steps = kFP4 ? K / 64 : (K + 15) / 16;
     const int num_kb = (k_steps + 3) / 4;
-    const int sf_row_tiles_b = (N + 127) / 128;
-    const int k_chunks = K / 64;  // 512-byte scale tiles per 128-row tile (NVFP4)
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            mbar_init(&sfready[s], 1);
         }
         mbar_init(tmem_full, 1);
-        mbar_init(tmem_empty, 4);
+        mbar_init(tmem_empty, kEpiWarps * kPair);  // the epilogue warps of both CTAs
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -126,85 +157,92 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmap_a);
         prefetch_tmap(&tmap_b);
+        if (kFP4) {
+            prefetch_tmap(&tmap_sfa);
+            prefetch_tmap(&tmap_sfb);
+        }
     }
     if (warp == 1) {
-        tmem_alloc(tmem_slot, kTmemCols);
-        tmem_relinquish();
+        tmem_alloc_pair(tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
     }
     tc_fence_before_sync();
     __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers and tensor memory exist from here on
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp == 0) {
         if (lane == 0) {
-            // ------------------------------------------------ TMA producer
+            // ------------------------------------------------ TMA producer (both CTAs)
+            const uint32_t full_even = map_to_rank(smem_u32(full), 0);
             int stage = 0;
             uint32_t phase = 0;
-            uint32_t issued = 0, last_parity = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const int m_blk = tile % num_m;
-                const int n_blk = tile / num_m;
+            for (int t = sch.first; ok && t < sch.total; t += sch.step) {
+                const int m_blk = (t % sch.num_mp) * kPair + (int)rank;
+                const int n_blk = t / sch.num_mp;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, args.status, abort_flag,
                                    kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
+                    if (leader) mbar_arrive_expect_tx(&full[stage], kPair * C::kLoadBytes);
+                    const uint32_t bar = full_even + 8u * (uint32_t)stage;
                     uint8_t* sa = smem + stage * C::kStageBytes;
                     uint8_t* sb = sa + kATileBytes;
-                    uint32_t bytes = kATileBytes + kBTileBytes;
-                    const int nk = min(4, k_steps - kb * 4);
-                    int nb = 0;
-                    if (kFP4) {
-                        nb = (2 * n_blk + 1 < sf_row_tiles_b) ? 2 : 1;
-                        bytes += (uint32_t)nk * 512u * (uint32_t)(1 + nb);
-                    }
-                    mbar_arrive_expect_tx(&full[stage], bytes);
                     const int x = kFP4 ? kb * 128 : kb * 64;
-                    tma_load_2d(&tmap_a, &full[stage], sa, x, m_blk * BM);
-                    tma_load_2d(&tmap_b, &full[stage], sb, x, n_blk * BN);
+                    tma_load_2d_pair(&tmap_a, bar, sa, x, m_blk * BM);
+                    tma_load_2d_pair(&tmap_b, bar, sb, x, n_blk * BN + (int)rank * (BN / kPair));
                     if (kFP4) {
-                        uint8_t* sfa = sb + kBTileBytes;
+                        // Scale tiles: 4 chunks of 512 bytes along K per 128-row tile; chunks
+                        // or tiles past the end arrive as zeros.
+                        uint8_t* sfa = sb + kBHalfBytes;
                         uint8_t* sfb = sfa + kSFAStageBytes;
-                        const uint8_t* src_a =
-                            args.a_sf + ((size_t)m_blk * k_chunks + (size_t)kb * 4) * 512;
-                        bulk_load(sfa, src_a, (uint32_t)nk * 512u, &full[stage]);
-                        for (int h = 0; h < nb; ++h) {
-                            const uint8_t* src_b =
-                                args.b_sf +
-                                ((size_t)(2 * n_blk + h) * k_chunks + (size_t)kb * 4) * 512;
-                            bulk_load(sfb + h * 2048, src_b, (uint32_t)nk * 512u, &full[stage]);
-                        }
+                        tma_load_4d_pair(&tmap_sfa, bar, sfa, 0, 0, kb * 4, m_blk);
+                        tma_load_4d_pair(&tmap_sfb, bar, sfb, 0, 0, kb * 4, 2 * n_blk);
+                        tma_load_4d_pair(&tmap_sfb, bar, sfb + 2048, 0, 0, kb * 4, 2 * n_blk + 1);
                     }
-                    issued |= 1u << stage;
-                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == kStages) {
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (ok && !*abort_flag) {
+                // Tail: wait until the last fill of every stage has been released, so no
+                // release from the pair's MMAs is still in flight towards this CTA at exit.
+                for (int i = 0; i < S; ++i) {
+                    if (!mbar_wait(&empty[stage], phase ^ 1u, args.status, abort_flag,
+                                   kWaitLimitNs))
+                        break;
+                    if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
             }
             if (*abort_flag) {
-                // Let every copy this thread started land before the CTA exits.
-                for (int s = 0; s < kStages; ++s)
-                    if (issued & (1u << s)) {
-                        int dummy_flag = 0;
-                        mbar_wait(&full[s], (last_parity >> s) & 1u, args.status, &dummy_flag,
-                                  kDrainLimitNs);
-                    }
+                // Give copies already issued time to land before the pair tears down.
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ------------------------------------------------ MMA issuer
+        if (lane == 0 && leader) {
+            // ------------------------------------------------ MMA issuer (even CTA)
             const uint32_t idesc = kFP4 ? idesc_nvfp4() : idesc_bf16();
+            // Descriptors of stage 0, K-step 0; stage s adds kStageBytes >> 4 and K-step kk
+            // adds 32 >> 4 = 2 to the start-address field (never carries: < 256 KB).
+            const uint64_t a_desc0 = smem_desc(smem_u32(smem), 16, 1024, kLayoutSw128);
+            const uint64_t b_desc0 = smem_desc(smem_u32(smem) + kATileBytes, 16, 1024, kLayoutSw128);
+            uint64_t* ready = kFP4 ? sfready : full;
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
             bool any_mma = false;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            for (int t = sch.first; ok && t < sch.total; t += sch.step) {
                 if (!mbar_wait(tmem_empty, acc_phase ^ 1u, args.status, abort_flag,
                                kWaitLimitNs)) {
                     ok = false;
@@ -212,80 +250,120 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after_sync();
                 for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&ready[stage], phase, args.status, abort_flag, kWaitLimitNs)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const int nk = min(4, k_steps - kb * 4);
+                    const uint64_t soff = (uint64_t)((stage * C::kStageBytes) >> 4);
+                    const uint32_t sf_col = tmem_base + kSfTmemBase + (uint32_t)stage * kSfTmemPerStage;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if (kk < nk) {
+                            const uint64_t ad = a_desc0 + soff + 2 * kk;
+                            const uint64_t bd = b_desc0 + soff + 2 * kk;
+                            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                            if (kFP4)
+                                mma_nvfp4_pair(tmem_base, ad, bd, idesc, sf_col + 4 * kk,
+                                               sf_col + 16 + 8 * kk, acc);
+                            else
+                                mma_bf16_pair(tmem_base, ad, bd, idesc, acc);
+                        }
+                    }
+                    any_mma = true;
+                    mma_commit_pair_multicast(&empty[stage], kBothCtas);  // release to both CTAs
+                    if (++stage == S) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit_pair_multicast(tmem_full, kBothCtas);
+                acc_phase ^= 1u;
+            }
+            if (*abort_flag && any_mma) {
+                // Let every MMA this thread issued finish before tensor memory is freed.
+                mma_commit_pair_multicast(drain, kEvenCta);
+                int dummy_flag = 0;
+                mbar_wait(drain, 0, args.status, &dummy_flag, kDrainLimitNs);
+            }
+        }
+    } else if (warp == kCopierWarp) {
+        if (kFP4 && lane == 0 && leader) {
+            // ------------------------------------------------ scale copier (NVFP4, even CTA)
+            const uint64_t sf_desc0 =
+                smem_desc(smem_u32(smem) + kATileBytes + kBHalfBytes, 128, 128, kLayoutNone);
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            bool any_cp = false;
+            for (int t = sch.first; ok && t < sch.total; t += sch.step) {
+                for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(&full[stage], phase, args.status, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after_sync();
                     const int nk = min(4, k_steps - kb * 4);
-                    const uint32_t sa = smem_u32(smem + stage * C::kStageBytes);
-                    const uint32_t sb = sa + kATileBytes;
-                    const uint32_t sf_col = kSfTmemBase + (uint32_t)stage * kSfTmemPerStage;
-                    if (kFP4) {
-                        const uint32_t sfa = sb + kBTileBytes;
-                        const uint32_t sfb = sfa + kSFAStageBytes;
-                        for (int kk = 0; kk < nk; ++kk) {
-                            tmem_cp_32x128b_x4(tmem_base + sf_col + 4 * kk,
-                                               smem_desc(sfa + kk * 512, 128, 128, kLayoutNone));
-                            tmem_cp_32x128b_x4(tmem_base + sf_col + 16 + 8 * kk,
-                                               smem_desc(sfb + kk * 512, 128, 128, kLayoutNone));
-                            tmem_cp_32x128b_x4(
-                                tmem_base + sf_col + 16 + 8 * kk + 4,
-                                smem_desc(sfb + 2048 + kk * 512, 128, 128, kLayoutNone));
+                    const uint64_t soff = (uint64_t)((stage * C::kStageBytes) >> 4);
+                    const uint32_t sf_col = tmem_base + kSfTmemBase + (uint32_t)stage * kSfTmemPerStage;
+                    // SFA chunk kk at +512 kk; SFB rows 0-127 at +2048 + 512 kk, rows
+                    // 128-255 at +4096 + 512 kk (descriptor units of 16 bytes).
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if (kk < nk) {
+                            tmem_cp_32x128b_x4_pair(sf_col + 4 * kk, sf_desc0 + soff + 32 * kk);
+                            tmem_cp_32x128b_x4_pair(sf_col + 16 + 8 * kk, sf_desc0 + soff + 128 + 32 * kk);
+                            tmem_cp_32x128b_x4_pair(sf_col + 20 + 8 * kk, sf_desc0 + soff + 256 + 32 * kk);
                         }
                     }
-                    for (int kk = 0; kk < nk; ++kk) {
-                        const uint64_t ad = smem_desc(sa + kk * 32, 16, 1024, kLayoutSw128);
-                        const uint64_t bd = smem_desc(sb + kk * 32, 16, 1024, kLayoutSw128);
-                        const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-                        if (kFP4)
-                            mma_nvfp4(tmem_base, ad, bd, idesc, tmem_base + sf_col + 4 * kk,
-                                      tmem_base + sf_col + 16 + 8 * kk, acc);
-                        else
-                            mma_bf16(tmem_base, ad, bd, idesc, acc);
-                    }
-                    any_mma = true;
-                    mma_commit(&empty[stage]);
-                    if (++stage == kStages) {
+                    any_cp = true;
+                    mma_commit_pair_multicast(&sfready[stage], kEvenCta);
+                    if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
-                if (!ok) break;
-                mma_commit(tmem_full);
-                acc_phase ^= 1u;
             }
-            if (*abort_flag && any_mma) {
-                // Let every MMA this thread issued finish before tensor memory is freed.
-                mma_commit(drain);
+            if (*abort_flag && any_cp) {
+                mma_commit_pair_multicast(drain, kEvenCta);
                 int dummy_flag = 0;
                 mbar_wait(drain, 0, args.status, &dummy_flag, kDrainLimitNs);
             }
         }
-    } else {
-        // ------------------------------------------------ epilogue (warps 2..5)
-        const int quarter = warp & 3;  // tensor-memory lanes 32*quarter .. +31
+    } else if (warp >= 2 && warp < 2 + kEpiWarps) {
+        // ------------------------------------------------ epilogue (warps 2..9, both CTAs)
+        const int quarter = warp & 3;                // tensor-memory lanes 32*quarter .. +31
+        const int half = (warp - 2) / 4;             // columns 128*half .. +127
         uint8_t* stg = epi + (warp - 2) * kEpiWarpBytes;
+        const uint32_t tmem_empty_even = map_to_rank(smem_u32(tmem_empty), 0);
         uint32_t acc_phase = 0;
         const float w_scale = kFP4 ? *args.w_st : 1.0f;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-            const int m_blk = tile % num_m;
-            const int n_blk = tile / num_m;
+        for (int t = sch.first; t < sch.total; t += sch.step) {
+            const int m_blk = (t % sch.num_mp) * kPair + (int)rank;
+            const int n_blk = t / sch.num_mp;
             bool ok = mbar_wait(tmem_full, acc_phase, args.status, abort_flag, kWaitLimitNs);
             // tcgen05.ld is .sync.aligned: reconverge the warp and agree on the outcome.
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             tc_fence_after_sync();
             const int row = m_blk * BM + quarter * 32 + lane;
-            const int n0 = n_blk * BN;
+            const int n0 = n_blk * BN + half * 128;
             float scale = 1.0f;
             if (kFP4) scale = (row < M ? args.a_srow[row] : 0.0f) * w_scale;
-            uint32_t packed[128];
+            // All four 32-column loads in flight, one wait, then the accumulator is free.
+            uint32_t v[4][32];
+            const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + half * 128;
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(quarter * 32) << 16) + c * 32, v);
-                tmem_ld_wait();
+            for (int c = 0; c < 4; ++c) tmem_ld_32x32b_x32(taddr + c * 32, v[c]);
+            tmem_ld_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tmem_empty_even);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t packed[16];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     // 8 bias values (one 16-byte load, warp-uniform address) per 8 columns.
@@ -297,28 +375,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int i = q * 4 + u;
-                        packed[c * 16 + i] = pack_bf16x2(
-                            fmaf(__uint_as_float(v[2 * i]), scale, __uint_as_float(bw[u] << 16)),
-                            fmaf(__uint_as_float(v[2 * i + 1]), scale,
+                        packed[i] = pack_bf16x2(
+                            fmaf(__uint_as_float(v[c][2 * i]), scale, __uint_as_float(bw[u] << 16)),
+                            fmaf(__uint_as_float(v[c][2 * i + 1]), scale,
                                  __uint_as_float(bw[u] & 0xFFFF0000u)));
                     }
                 }
-            }
-            // The accumulator is in registers: hand tensor memory back to the MMA warp.
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tmem_empty);
-#pragma unroll
-            for (int c = 0; c < 8; ++c) {
                 // Row `lane` of the 32x32 bf16 chunk -> staging (16-byte pieces XOR-swizzled
                 // by row), then 8 rows x 64 bytes per store instruction.
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint4 val = make_uint4(packed[c * 16 + 4 * j], packed[c * 16 + 4 * j + 1],
-                                                 packed[c * 16 + 4 * j + 2],
-                                                 packed[c * 16 + 4 * j + 3]);
-                    *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ (lane & 3)) * 16)) = val;
-                }
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ (lane & 3)) * 16)) =
+                        make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
+                                   packed[4 * j + 3]);
                 __syncwarp();
 #pragma unroll
                 for (int it = 0; it < 4; ++it) {
@@ -341,9 +410,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_before_sync();
     __syncthreads();
+    cluster_sync_all();  // no CTA leaves while its peer may still signal or load towards it
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, kTmemCols);
+        tmem_dealloc_pair(tmem_base, kTmemCols);
     }
 }
 
@@ -362,32 +432,51 @@ __global__ void wait_timeout_kernel(int* status, uint64_t limit_ns) {
 
 template <bool kFP4>
 cudaError_t run_gemm(const LaunchCtx& ctx, const CUtensorMap& ta, const CUtensorMap& tb,
-                     const GemmArgs& args) {
+                     const CUtensorMap& tsfa, const CUtensorMap& tsfb, const GemmArgs& args) {
     // Set on every call: the attribute belongs to the current device's context.
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Cfg<kFP4>::kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int64_t tiles = (int64_t)((args.M + BM - 1) / BM) * ((args.N + BN - 1) / BN);
-    const int grid = (int)(tiles < ctx.num_sms ? tiles : ctx.num_sms);
-    gemm_kernel<kFP4><<<grid, kThreads, Cfg<kFP4>::kSmemBytes, ctx.stream>>>(ta, tb, args);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kPair;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = Cfg<kFP4>::kSmemBytes;
+    cfg.stream = ctx.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // Co-resident pairs (one CTA per SM), capped by the work available.
+    cfg.gridDim = dim3((unsigned)(ctx.num_sms / kPair * kPair), 1, 1);
+    int max_clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&max_clusters, gemm_kernel<kFP4>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (max_clusters < 1) return cudaErrorInvalidConfiguration;
+    const int64_t num_m = (args.M + BM - 1) / BM;
+    const int64_t pairs = (num_m + kPair - 1) / kPair * ((args.N + BN - 1) / BN);
+    const int64_t clusters = pairs < max_clusters ? pairs : max_clusters;
+    cfg.gridDim = dim3((unsigned)(clusters * kPair), 1, 1);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<kFP4>, ta, tb, tsfa, tsfb, args);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_nvfp4(const LaunchCtx& ctx, const CUtensorMap& tmap_a,
-                              const CUtensorMap& tmap_b, const uint8_t* a_sf, const uint8_t* w_sf,
-                              const float* a_srow, const float* w_st, const __nv_bfloat16* bias,
-                              __nv_bfloat16* Y, int64_t M, int64_t N, int64_t K) {
-    GemmArgs a{a_sf, w_sf, a_srow, w_st, bias, Y, (int)M, (int)N, (int)K, ctx.status};
-    return run_gemm<true>(ctx, tmap_a, tmap_b, a);
+                              const CUtensorMap& tmap_b, const CUtensorMap& tmap_sfa,
+                              const CUtensorMap& tmap_sfb, const float* a_srow, const float* w_st,
+                              const __nv_bfloat16* bias, __nv_bfloat16* Y, int64_t M, int64_t N,
+                              int64_t K) {
+    GemmArgs a{a_srow, w_st, bias, Y, (int)M, (int)N, (int)K, ctx.status};
+    return run_gemm<true>(ctx, tmap_a, tmap_b, tmap_sfa, tmap_sfb, a);
 }
 
 cudaError_t launch_gemm_bf16(const LaunchCtx& ctx, const CUtensorMap& tmap_a,
                              const CUtensorMap& tmap_b, const __nv_bfloat16* bias,
                              __nv_bfloat16* Y, int64_t M, int64_t N, int64_t K) {
-    GemmArgs a{nullptr, nullptr, nullptr, nullptr, bias, Y, (int)M, (int)N, (int)K, ctx.status};
-    return run_gemm<false>(ctx, tmap_a, tmap_b, a);
+    GemmArgs a{nullptr, nullptr, bias, Y, (int)M, (int)N, (int)K, ctx.status};
+    return run_gemm<false>(ctx, tmap_a, tmap_b, tmap_a, tmap_b, a);
 }
 
 cudaError_t launch_test_wait_timeout(const LaunchCtx& ctx, int64_t timeout_ns) {
