@@ -88,9 +88,10 @@ bool encoder(PFN_cuTensorMapEncodeTiled_v12000* out) {
     return true;
 }
 
-// 2-D K-major tensor [rows, inner] with a (box_inner x box_rows) box, 128-byte swizzle.
+// 2-D row-major tensor [rows, inner] with a (box_inner x box_rows) box.
 bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, uint64_t inner,
-               uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
+               uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
+               CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
     PFN_cuTensorMapEncodeTiled_v12000 enc;
     if (!encoder(&enc)) return false;
     const cuuint64_t dims[2] = {inner, rows};
@@ -98,9 +99,14 @@ bool encode_2d(CUtensorMap* map, CUtensorMapDataType dtype, const void* base, ui
     const cuuint32_t box[2] = {box_inner, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, dtype, 2, const_cast<void*>(base), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// The bf16 output Y [M, N] as 32 x 32 store boxes with the 64-byte swizzle.
+bool encode_out(CUtensorMap* map, void* Y, int64_t M, int64_t N) {
+    return encode_2d(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Y, (uint64_t)N, (uint64_t)M,
+                     (uint64_t)N * 2, 32, 32, CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 // Scale-factor buffer of a [rows, K] NVFP4 tensor viewed as 4-D bytes
@@ -195,16 +201,15 @@ nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const float
     LaunchCtx ctx;
     nvfp4_status st = resolve(stream, &ctx);
     if (st != NVFP4_OK) return st;
-    CUtensorMap ta, tb, tsa, tsb;
+    CUtensorMap ta, tb, tsa, tsb, ty;
     if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, (uint64_t)K / 2, (uint64_t)M,
                    (uint64_t)K / 2, 128, 128) ||
         !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, w_codes, (uint64_t)K / 2, (uint64_t)N,
                    (uint64_t)K / 2, 128, 128) ||
-        !encode_sf(&tsa, a_sf, M, K) || !encode_sf(&tsb, w_sf, N, K))
+        !encode_sf(&tsa, a_sf, M, K) || !encode_sf(&tsb, w_sf, N, K) || !encode_out(&ty, Y, M, N))
         return NVFP4_ERR_CUDA;
-    return from_cuda(launch_gemm_nvfp4(ctx, ta, tb, tsa, tsb, a_srow, w_st,
-                                       static_cast<const __nv_bfloat16*>(bias),
-                                       static_cast<__nv_bfloat16*>(Y), M, N, K));
+    return from_cuda(launch_gemm_nvfp4(ctx, ta, tb, tsa, tsb, ty, a_srow, w_st,
+                                       static_cast<const __nv_bfloat16*>(bias), M, N, K));
 }
 
 nvfp4_status bf16_gemm(const void* X, const void* W, const void* bias, void* Y, int64_t M,
@@ -219,14 +224,15 @@ nvfp4_status bf16_gemm(const void* X, const void* W, const void* bias, void* Y, 
     LaunchCtx ctx;
     nvfp4_status st = resolve(stream, &ctx);
     if (st != NVFP4_OK) return st;
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, ty;
     if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, X, (uint64_t)K, (uint64_t)M,
                    (uint64_t)K * 2, 64, 128) ||
         !encode_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)K, (uint64_t)N,
-                   (uint64_t)K * 2, 64, 128))
+                   (uint64_t)K * 2, 64, 128) ||
+        !encode_out(&ty, Y, M, N))
         return NVFP4_ERR_CUDA;
-    return from_cuda(launch_gemm_bf16(ctx, ta, tb, static_cast<const __nv_bfloat16*>(bias),
-                                      static_cast<__nv_bfloat16*>(Y), M, N, K));
+    return from_cuda(launch_gemm_bf16(ctx, ta, tb, ty, static_cast<const __nv_bfloat16*>(bias), M,
+                                      N, K));
 }
 
 nvfp4_status select_contrastive(const float* rewards, int P, int N, int K, int global_std,

@@ -39,12 +39,12 @@ cudaError_t launch_test_e4m3_quotient(const LaunchCtx&, const float* v, const fl
 // GEMMs: tensor maps are encoded by the caller (host) and passed by value.
 cudaError_t launch_gemm_nvfp4(const LaunchCtx&, const CUtensorMap& tmap_a,
                               const CUtensorMap& tmap_b, const CUtensorMap& tmap_sfa,
-                              const CUtensorMap& tmap_sfb, const float* a_srow, const float* w_st,
-                              const __nv_bfloat16* bias, __nv_bfloat16* Y, int64_t M, int64_t N,
-                              int64_t K);
+                              const CUtensorMap& tmap_sfb, const CUtensorMap& tmap_y,
+                              const float* a_srow, const float* w_st, const __nv_bfloat16* bias,
+                              int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_bf16(const LaunchCtx&, const CUtensorMap& tmap_a,
-                             const CUtensorMap& tmap_b, const __nv_bfloat16* bias,
-                             __nv_bfloat16* Y, int64_t M, int64_t N, int64_t K);
+                             const CUtensorMap& tmap_b, const CUtensorMap& tmap_y,
+                             const __nv_bfloat16* bias, int64_t M, int64_t N, int64_t K);
 cudaError_t launch_test_wait_timeout(const LaunchCtx&, int64_t timeout_ns);
 
 // ----------------------------------------------------------------- device side
@@ -326,6 +326,38 @@ __device__ __forceinline__ void tmem_cp_32x128b_x4_pair(uint32_t taddr, uint64_t
                  : "memory");
 }
 
+// --- TMA stores (shared -> global), tracked per thread in bulk groups
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int32_t x,
+                                             int32_t y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(src)), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until at most kPending bulk groups of this thread still read shared memory.
+template <int kPending>
+__device__ __forceinline__ void bulk_wait_group_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(kPending) : "memory");
+}
+
+template <int kPending>
+__device__ __forceinline__ void bulk_wait_group() {
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(kPending) : "memory");
+}
+
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy
+// (TMA) reads of them.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
@@ -444,6 +476,58 @@ __device__ __forceinline__ void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)
           "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
           "=r"(r[31])
         : "r"(taddr));
+}
+
+// 32 registers per thread -> 32 lanes x 32 consecutive 32-bit columns (thread i
+// writes lane base+i); and the 16-column form.
+__device__ __forceinline__ void tmem_st_32x32b_x32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0],"
+        " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16,"
+        " %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+        "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+        "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0],"
+        " {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Tile load into this CTA's shared memory, completion on this CTA's own mbarrier.
+__device__ __forceinline__ void tma_load_4d(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                            int32_t c0, int32_t c1, int32_t c2, int32_t c3) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4, %5, %6}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+        : "memory");
+}
+
+// Warp-group register rebalancing.  The four warp groups of a 512-thread CTA are
+// launched with 128 registers per thread; the counts requested below must add up
+// to at most 4 x 128 per lane, or an increase would wait forever.
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_decrease() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <uint32_t kRegs>
+__device__ __forceinline__ void regs_increase() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 
 __device__ __forceinline__ void tmem_ld_wait() {

@@ -21,7 +21,8 @@
 //   warps 2..9   epilogue (both CTAs), two warps per tensor-memory lane quarter,
 //                128 columns each: tensor memory -> registers (tcgen05.ld, all
 //                issued before one wait), release of the accumulator, then scale,
-//                bias, bf16, staged through shared memory into coalesced stores;
+//                bias, bf16, and 32x32 chunks stored by TMA from a swizzled
+//                shared-memory staging ring (asynchronous, clipped at M and N);
 //   warp 10      NVFP4, even CTA: copies each stage's scale tiles shared -> tensor
 //                memory in both CTAs (tcgen05.cp) and hands the stage to the MMAs.
 // Per CTA: fp32 accumulator in tensor-memory columns 0..255 (its 128 rows x 256);
@@ -46,8 +47,8 @@ constexpr uint32_t kATileBytes = BM * 128;            // 16 KB: 128 rows x 128 B
 constexpr uint32_t kBHalfBytes = (BN / kPair) * 128;  // 16 KB: this CTA's 128 rows of B
 constexpr uint32_t kSFAStageBytes = 4 * 512;          // 128 rows x 4 K-chunks of 64
 constexpr uint32_t kSFBStageBytes = 8 * 512;          // 256 rows x 4 K-chunks of 64
-constexpr uint32_t kEpiWarpBytes = 32 * 64;           // 32 rows x 32 bf16
-constexpr uint32_t kEpiBytes = kEpiWarps * kEpiWarpBytes;
+constexpr uint32_t kChunkBytes = 32 * 64;             // 32 rows x 32 bf16, one TMA store
+constexpr uint32_t kBiasBytes = 256;                   // 128 bias values per epilogue warp
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kSfTmemBase = 256;
 constexpr uint32_t kSfTmemPerStage = 48;
@@ -59,10 +60,13 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for copies already in
 template <bool kFP4>
 struct Cfg {
     static constexpr int kStages = kFP4 ? 5 : 6;
-    // Bytes this CTA loads per stage (the even CTA expects twice as many).
-    static constexpr uint32_t kLoadBytes =
-        kATileBytes + kBHalfBytes + (kFP4 ? kSFAStageBytes + kSFBStageBytes : 0u);
-    static constexpr uint32_t kStageBytes = kLoadBytes;
+    // A and B bytes this CTA loads per stage, and for NVFP4 its scale-tile bytes (the
+    // even CTA expects twice each, on separate barriers).
+    static constexpr uint32_t kABBytes = kATileBytes + kBHalfBytes;
+    static constexpr uint32_t kSFBytes = kFP4 ? kSFAStageBytes + kSFBStageBytes : 0u;
+    static constexpr uint32_t kStageBytes = kABBytes + kSFBytes;
+    static constexpr int kEpiBufs = kFP4 ? 2 : 1;  // staging chunks per epilogue warp
+    static constexpr uint32_t kEpiBytes = kEpiWarps * (kEpiBufs * kChunkBytes + kBiasBytes);
     static constexpr uint32_t kBarrierBytes = 256;
     static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarrierBytes;
 };
@@ -93,7 +97,6 @@ struct GemmArgs {
     const float* a_srow;
     const float* w_st;
     const __nv_bfloat16* bias;
-    __nv_bfloat16* Y;
     int M, N, K;
     int* status;
 };
@@ -116,17 +119,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 const __grid_constant__ CUtensorMap tmap_b,
                 const __grid_constant__ CUtensorMap tmap_sfa,
-                const __grid_constant__ CUtensorMap tmap_sfb, const GemmArgs args) {
+                const __grid_constant__ CUtensorMap tmap_sfb,
+                const __grid_constant__ CUtensorMap tmap_y, const GemmArgs args) {
     using C = Cfg<kFP4>;
     constexpr int S = C::kStages;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* epi = smem + S * C::kStageBytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(epi + kEpiBytes);  // used in the even CTA
+    uint64_t* full = reinterpret_cast<uint64_t*>(epi + C::kEpiBytes);  // used in the even CTA
     uint64_t* empty = full + S;
     uint64_t* sfready = empty + S;
-    uint64_t* tmem_full = sfready + S;
+    uint64_t* sf_full = sfready + S;  // scale tiles of both CTAs landed (even CTA)
+    uint64_t* tmem_full = sf_full + S;
     uint64_t* tmem_empty = tmem_full + 1;  // used in the even CTA
     uint64_t* drain = tmem_empty + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -147,6 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
             mbar_init(&sfready[s], 1);
+            mbar_init(&sf_full[s], 1);
         }
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, kEpiWarps * kPair);  // the epilogue warps of both CTAs
@@ -176,6 +182,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // ------------------------------------------------ TMA producer (both CTAs)
             const uint32_t full_even = map_to_rank(smem_u32(full), 0);
+            const uint32_t sf_full_even = map_to_rank(smem_u32(sf_full), 0);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -188,22 +195,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    if (leader) mbar_arrive_expect_tx(&full[stage], kPair * C::kLoadBytes);
                     const uint32_t bar = full_even + 8u * (uint32_t)stage;
                     uint8_t* sa = smem + stage * C::kStageBytes;
                     uint8_t* sb = sa + kATileBytes;
+                    if (kFP4) {
+                        // Scale tiles first (small; the copier can start on them while A and B
+                        // are in flight): 4 chunks of 512 bytes along K per 128-row tile;
+                        // chunks or tiles past the end arrive as zeros.
+                        if (leader) mbar_arrive_expect_tx(&sf_full[stage], kPair * C::kSFBytes);
+                        const uint32_t sbar = sf_full_even + 8u * (uint32_t)stage;
+                        uint8_t* sfa = sb + kBHalfBytes;
+                        uint8_t* sfb = sfa + kSFAStageBytes;
+                        tma_load_4d_pair(&tmap_sfa, sbar, sfa, 0, 0, kb * 4, m_blk);
+                        tma_load_4d_pair(&tmap_sfb, sbar, sfb, 0, 0, kb * 4, 2 * n_blk);
+                        tma_load_4d_pair(&tmap_sfb, sbar, sfb + 2048, 0, 0, kb * 4, 2 * n_blk + 1);
+                    }
+                    if (leader) mbar_arrive_expect_tx(&full[stage], kPair * C::kABBytes);
                     const int x = kFP4 ? kb * 128 : kb * 64;
                     tma_load_2d_pair(&tmap_a, bar, sa, x, m_blk * BM);
                     tma_load_2d_pair(&tmap_b, bar, sb, x, n_blk * BN + (int)rank * (BN / kPair));
-                    if (kFP4) {
-                        // Scale tiles: 4 chunks of 512 bytes along K per 128-row tile; chunks
-                        // or tiles past the end arrive as zeros.
-                        uint8_t* sfa = sb + kBHalfBytes;
-                        uint8_t* sfb = sfa + kSFAStageBytes;
-                        tma_load_4d_pair(&tmap_sfa, bar, sfa, 0, 0, kb * 4, m_blk);
-                        tma_load_4d_pair(&tmap_sfb, bar, sfb, 0, 0, kb * 4, 2 * n_blk);
-                        tma_load_4d_pair(&tmap_sfb, bar, sfb + 2048, 0, 0, kb * 4, 2 * n_blk + 1);
-                    }
                     if (++stage == S) {
                         stage = 0;
                         phase ^= 1u;
@@ -237,7 +247,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // adds 32 >> 4 = 2 to the start-address field (never carries: < 256 KB).
             const uint64_t a_desc0 = smem_desc(smem_u32(smem), 16, 1024, kLayoutSw128);
             const uint64_t b_desc0 = smem_desc(smem_u32(smem) + kATileBytes, 16, 1024, kLayoutSw128);
-            uint64_t* ready = kFP4 ? sfready : full;
             int stage = 0;
             uint32_t phase = 0, acc_phase = 0;
             bool ok = true;
@@ -250,7 +259,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after_sync();
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&ready[stage], phase, args.status, abort_flag, kWaitLimitNs)) {
+                    if (!mbar_wait(&full[stage], phase, args.status, abort_flag, kWaitLimitNs) ||
+                        (kFP4 &&
+                         !mbar_wait(&sfready[stage], phase, args.status, abort_flag, kWaitLimitNs))) {
                         ok = false;
                         break;
                     }
@@ -300,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool any_cp = false;
             for (int t = sch.first; ok && t < sch.total; t += sch.step) {
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, args.status, abort_flag, kWaitLimitNs)) {
+                    if (!mbar_wait(&sf_full[stage], phase, args.status, abort_flag, kWaitLimitNs)) {
                         ok = false;
                         break;
                     }
@@ -336,22 +347,34 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------ epilogue (warps 2..9, both CTAs)
         const int quarter = warp & 3;                // tensor-memory lanes 32*quarter .. +31
         const int half = (warp - 2) / 4;             // columns 128*half .. +127
-        uint8_t* stg = epi + (warp - 2) * kEpiWarpBytes;
+        const int ew = warp - 2;
+        uint8_t* stg = epi + ew * C::kEpiBufs * kChunkBytes;  // 2048-byte aligned chunks
+        uint8_t* sbias = epi + kEpiWarps * C::kEpiBufs * kChunkBytes + ew * kBiasBytes;
+        uint32_t chunk_seq = 0;
         const uint32_t tmem_empty_even = map_to_rank(smem_u32(tmem_empty), 0);
         uint32_t acc_phase = 0;
         const float w_scale = kFP4 ? *args.w_st : 1.0f;
         for (int t = sch.first; t < sch.total; t += sch.step) {
             const int m_blk = (t % sch.num_mp) * kPair + (int)rank;
             const int n_blk = t / sch.num_mp;
+            const int row = m_blk * BM + quarter * 32 + lane;
+            const int n0 = n_blk * BN + half * 128;
+            // Fetch this tile's per-row scale and the warp's 128 bias values while the
+            // MMAs run, so no global load sits between the accumulator and the stores.
+            float scale = 1.0f;
+            if (kFP4) scale = (row < M ? args.a_srow[row] : 0.0f) * w_scale;
+            {
+                uint2 b2 = make_uint2(0, 0);
+                if (args.bias != nullptr && n0 + lane * 4 < N)
+                    b2 = __ldg(reinterpret_cast<const uint2*>(args.bias + n0 + lane * 4));
+                *reinterpret_cast<uint2*>(sbias + lane * 8) = b2;
+            }
+            __syncwarp();
             bool ok = mbar_wait(tmem_full, acc_phase, args.status, abort_flag, kWaitLimitNs);
             // tcgen05.ld is .sync.aligned: reconverge the warp and agree on the outcome.
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
             tc_fence_after_sync();
-            const int row = m_blk * BM + quarter * 32 + lane;
-            const int n0 = n_blk * BN + half * 128;
-            float scale = 1.0f;
-            if (kFP4) scale = (row < M ? args.a_srow[row] : 0.0f) * w_scale;
             // All four 32-column loads in flight, one wait, then the accumulator is free.
             uint32_t v[4][32];
             const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + half * 128;
@@ -366,11 +389,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t packed[16];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
-                    // 8 bias values (one 16-byte load, warp-uniform address) per 8 columns.
-                    uint4 braw = make_uint4(0, 0, 0, 0);
-                    const int col = n0 + c * 32 + q * 8;
-                    if (args.bias != nullptr && col < N)
-                        braw = __ldg(reinterpret_cast<const uint4*>(args.bias + col));
+                    // 8 bias values per 8 columns (shared memory, broadcast to the warp).
+                    const uint4 braw = *reinterpret_cast<const uint4*>(sbias + (c * 32 + q * 8) * 2);
                     const uint32_t bw[4] = {braw.x, braw.y, braw.z, braw.w};
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
@@ -381,29 +401,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                                  __uint_as_float(bw[u] & 0xFFFF0000u)));
                     }
                 }
-                // Row `lane` of the 32x32 bf16 chunk -> staging (16-byte pieces XOR-swizzled
-                // by row), then 8 rows x 64 bytes per store instruction.
+                // Row `lane` of the 32x32 bf16 chunk -> staging chunk, 16-byte pieces placed
+                // by the 64-byte swizzle of the Y tensor map (piece j of row r at
+                // j ^ ((r >> 1) & 3)), then one TMA store of the chunk.
+                uint8_t* buf = stg + (chunk_seq % C::kEpiBufs) * kChunkBytes;
+                if (chunk_seq >= (uint32_t)C::kEpiBufs) {
+                    if (lane == 0) bulk_wait_group_read<C::kEpiBufs - 1>();
+                    __syncwarp();
+                }
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4*>(stg + lane * 64 + ((j ^ (lane & 3)) * 16)) =
+                    *reinterpret_cast<uint4*>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) * 16)) =
                         make_uint4(packed[4 * j], packed[4 * j + 1], packed[4 * j + 2],
                                    packed[4 * j + 3]);
+                fence_proxy_async_smem();
                 __syncwarp();
-#pragma unroll
-                for (int it = 0; it < 4; ++it) {
-                    const int rr = it * 8 + (lane >> 2);
-                    const int ch = lane & 3;
-                    const uint4 val =
-                        *reinterpret_cast<const uint4*>(stg + rr * 64 + ((ch ^ (rr & 3)) * 16));
-                    const int grow = m_blk * BM + quarter * 32 + rr;
-                    const int gcol = n0 + c * 32 + ch * 8;
-                    if (grow < M && gcol < N)
-                        *reinterpret_cast<uint4*>(args.Y + (size_t)grow * N + gcol) = val;
+                const int sx = n0 + c * 32, sy = m_blk * BM + quarter * 32;
+                if (lane == 0 && sx < N && sy < M) {  // partial boxes are clipped by TMA
+                    tma_store_2d(&tmap_y, buf, sx, sy);
+                    bulk_commit_group();
                 }
-                __syncwarp();
+                ++chunk_seq;
             }
             acc_phase ^= 1u;
         }
+        if (lane == 0) bulk_wait_group<0>();  // every store of this warp has completed
+        __syncwarp();
     }
 
     // ------------------------------------------------ teardown
@@ -432,7 +455,8 @@ __global__ void wait_timeout_kernel(int* status, uint64_t limit_ns) {
 
 template <bool kFP4>
 cudaError_t run_gemm(const LaunchCtx& ctx, const CUtensorMap& ta, const CUtensorMap& tb,
-                     const CUtensorMap& tsfa, const CUtensorMap& tsfb, const GemmArgs& args) {
+                     const CUtensorMap& tsfa, const CUtensorMap& tsfb, const CUtensorMap& ty,
+                     const GemmArgs& args) {
     // Set on every call: the attribute belongs to the current device's context.
     cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Cfg<kFP4>::kSmemBytes);
@@ -458,25 +482,25 @@ cudaError_t run_gemm(const LaunchCtx& ctx, const CUtensorMap& ta, const CUtensor
     const int64_t pairs = (num_m + kPair - 1) / kPair * ((args.N + BN - 1) / BN);
     const int64_t clusters = pairs < max_clusters ? pairs : max_clusters;
     cfg.gridDim = dim3((unsigned)(clusters * kPair), 1, 1);
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<kFP4>, ta, tb, tsfa, tsfb, args);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<kFP4>, ta, tb, tsfa, tsfb, ty, args);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_nvfp4(const LaunchCtx& ctx, const CUtensorMap& tmap_a,
                               const CUtensorMap& tmap_b, const CUtensorMap& tmap_sfa,
-                              const CUtensorMap& tmap_sfb, const float* a_srow, const float* w_st,
-                              const __nv_bfloat16* bias, __nv_bfloat16* Y, int64_t M, int64_t N,
-                              int64_t K) {
-    GemmArgs a{a_srow, w_st, bias, Y, (int)M, (int)N, (int)K, ctx.status};
-    return run_gemm<true>(ctx, tmap_a, tmap_b, tmap_sfa, tmap_sfb, a);
+                              const CUtensorMap& tmap_sfb, const CUtensorMap& tmap_y,
+                              const float* a_srow, const float* w_st, const __nv_bfloat16* bias,
+                              int64_t M, int64_t N, int64_t K) {
+    GemmArgs a{a_srow, w_st, bias, (int)M, (int)N, (int)K, ctx.status};
+    return run_gemm<true>(ctx, tmap_a, tmap_b, tmap_sfa, tmap_sfb, tmap_y, a);
 }
 
 cudaError_t launch_gemm_bf16(const LaunchCtx& ctx, const CUtensorMap& tmap_a,
-                             const CUtensorMap& tmap_b, const __nv_bfloat16* bias,
-                             __nv_bfloat16* Y, int64_t M, int64_t N, int64_t K) {
-    GemmArgs a{nullptr, nullptr, bias, Y, (int)M, (int)N, (int)K, ctx.status};
-    return run_gemm<false>(ctx, tmap_a, tmap_b, tmap_a, tmap_b, a);
+                             const CUtensorMap& tmap_b, const CUtensorMap& tmap_y,
+                             const __nv_bfloat16* bias, int64_t M, int64_t N, int64_t K) {
+    GemmArgs a{nullptr, nullptr, bias, (int)M, (int)N, (int)K, ctx.status};
+    return run_gemm<false>(ctx, tmap_a, tmap_b, tmap_a, tmap_b, tmap_y, a);
 }
 
 cudaError_t launch_test_wait_timeout(const LaunchCtx& ctx, int64_t timeout_ns) {
