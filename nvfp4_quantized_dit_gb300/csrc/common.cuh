@@ -90,48 +90,23 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
     return __uint_as_float(((e + 120u) << 23) | (m << 20)); // (1 + m/8) * 2^(e-7)
 }
 
-// True when the fp32 value with bit pattern u lies within 8 ulps of a number
-// with at most (23 - lowbits + 1) significant bits, i.e. when its low `lowbits`
-// mantissa bits are within 8 of 0 modulo 2^lowbits.  Every E2M1 rounding
-// boundary (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5) has 3 significant bits
-// (lowbits = 20); every E4M3 boundary (midpoints of adjacent codes) has at most
-// 5 (lowbits = 18).
+// True when the fp32 value with bit pattern u lies within 16 ulps of a number with
+// at most (23 - kLowBits + 1) significant bits, i.e. when its low kLowBits mantissa
+// bits are within 16 of 0 modulo 2^kLowBits.  Every E2M1 rounding boundary (0.25,
+// 0.75, 1.25, 1.75, 2.5, 3.5, 5) has 3 significant bits (kLowBits = 20); every E4M3
+// boundary (midpoints of adjacent codes) has at most 5 (kLowBits = 18).
 template <int kLowBits>
 __device__ __forceinline__ bool near_boundary(uint32_t u) {
     constexpr uint32_t mask = (1u << kLowBits) - 1u;
-    return ((u + 8u) & mask) < 16u;
+    return ((u + 16u) & mask) < 32u;
 }
 
-// RNE_E2M1_sat(fl(x / den)) for 8 values sharing den > 0, with r = fl(1/den).
-//
-// Fast path: q' = fl(x * r).  With r correctly rounded, |q' - x/den| <= 2^-23|x/den|
-// and |fl(x/den) - x/den| <= 2^-24|x/den|, so q' and the exact quotient fl(x/den)
-// are within about 3 ulps of each other.  E2M1 rounding is a step function whose
-// steps sit at 3-significant-bit numbers; if q' is more than 8 ulps away from every
-// such number, q' and fl(x/den) round to the same code.  Otherwise (and whenever
-// r is not a normal number) the value is recomputed with a true IEEE division.
-__device__ __forceinline__ uint32_t e2m1_quotient8(const float (&x)[8], float den, float r,
-                                                   bool fast_ok) {
-    float q[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) q[i] = __fmul_rn(x[i], r);
-    bool any = !fast_ok;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) any |= near_boundary<20>(__float_as_uint(q[i]));
-    if (any) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i)
-            if (!fast_ok || near_boundary<20>(__float_as_uint(q[i]))) q[i] = __fdiv_rn(x[i], den);
-    }
-    return cvt_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]);
-}
-
-// RNE_E4M3_sat(fl(v / d)) for v >= 0, d > 0, with inv_d = fl(1/d): same argument
-// as above with the E4M3 boundaries (<= 5 significant bits).
-__device__ __forceinline__ uint32_t e4m3_quotient(float v, float d, float inv_d, bool fast_ok) {
-    float q = __fmul_rn(v, inv_d);
-    if (!fast_ok || near_boundary<18>(__float_as_uint(q))) q = __fdiv_rn(v, d);
-    return cvt_e4m3(q);
+// Approximate reciprocal, at most 1 ulp from 1/d for normal d whose reciprocal is
+// normal (the hardware's documented bound for rcp.approx.f32).
+__device__ __forceinline__ float recip_approx(float d) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+    return r;
 }
 
 // A reciprocal usable by the fast paths: den in the normal range, so that 1/den is
@@ -140,10 +115,64 @@ __device__ __forceinline__ bool fast_recip_ok(float den) {
     return den >= 1.17549435e-38f && den <= 8.5e37f;
 }
 
+struct F8 {
+    float v[8];
+};
+
+// Slow path of e2m1_quotient8 (rare): true IEEE divisions where the fast quotient
+// is within the window of a rounding boundary, or everywhere when !fast_ok.
+static __device__ __noinline__ F8 e2m1_fix8(F8 x, F8 q, float den, bool fast_ok) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        if (!fast_ok || near_boundary<20>(__float_as_uint(q.v[i]))) q.v[i] = __fdiv_rn(x.v[i], den);
+    return q;
+}
+
+static __device__ __noinline__ float exact_quotient(float v, float d) { return __fdiv_rn(v, d); }
+
+// RNE_E2M1_sat(fl(x / den)) for 8 values sharing den > 0, with r an approximation of
+// 1/den within 1 ulp (valid when fast_ok).
+//
+// Fast path: q' = fl(x * r).  Then |q' - x/den| <= 1.5 * 2^-23 |x/den| and
+// |fl(x/den) - x/den| <= 2^-24 |x/den|, so q' and the exact quotient fl(x/den) are
+// less than 4 ulps apart.  E2M1 rounding is a step function whose steps sit at
+// 3-significant-bit numbers; if q' is more than 16 ulps away from every such number,
+// q' and fl(x/den) round to the same code.  Otherwise (and whenever den or 1/den is
+// not a normal number) the value is recomputed with a true IEEE division.
+__device__ __forceinline__ uint32_t e2m1_quotient8(const float (&x)[8], float den, float r,
+                                                   bool fast_ok) {
+    F8 q;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) q.v[i] = __fmul_rn(x[i], r);
+    bool any = !fast_ok;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) any |= near_boundary<20>(__float_as_uint(q.v[i]));
+    if (any) {
+        F8 xv;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) xv.v[i] = x[i];
+        q = e2m1_fix8(xv, q, den, fast_ok);
+    }
+    return cvt_e2m1x8(q.v[0], q.v[1], q.v[2], q.v[3], q.v[4], q.v[5], q.v[6], q.v[7]);
+}
+
+// RNE_E4M3_sat(fl(v / d)) for v >= 0, d > 0, with inv_d within 1 ulp of 1/d: same
+// argument as above with the E4M3 boundaries (<= 5 significant bits).
+__device__ __forceinline__ uint32_t e4m3_quotient(float v, float d, float inv_d, bool fast_ok) {
+    float q = __fmul_rn(v, inv_d);
+    if (!fast_ok || near_boundary<18>(__float_as_uint(q))) q = exact_quotient(v, d);
+    return cvt_e4m3(q);
+}
+
 // ------------------------------------------------------------------ PTX helpers
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Barrier `id` (1..15) among `nthreads` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {

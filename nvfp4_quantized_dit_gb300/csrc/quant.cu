@@ -59,7 +59,7 @@ __device__ __forceinline__ int64_t sf_word_offset(int64_t row, int64_t kb, int64
 
 // Quantizes 8 consecutive elements x of a 16-element block whose other half is
 // held by the partner lane (lane ^ 1).  s is the second-level scale, d = 6*s and
-// inv_d = fl(1/d) (when d_fast).  Returns the 8 packed codes; *sfc gets the
+// inv_d within 1 ulp of 1/d (when d_fast).  Returns the 8 packed codes; *sfc gets the
 // block's E4M3 scale code.  Every lane of the warp must call it (shuffle).
 __device__ __forceinline__ uint32_t quant_half_block(const float (&x)[8], float s, float d,
                                                      float inv_d, bool d_fast, uint32_t* sfc) {
@@ -71,8 +71,7 @@ __device__ __forceinline__ uint32_t quant_half_block(const float (&x)[8], float 
     const float den = __fmul_rn(e4m3_value(code), s);
     if (!(den > 0.0f)) return 0u;
     const bool fast = fast_recip_ok(den);
-    const float r = fast ? __frcp_rn(den) : 0.0f;
-    return e2m1_quotient8(x, den, r, fast);
+    return e2m1_quotient8(x, den, fast ? recip_approx(den) : 0.0f, fast);
 }
 
 // Gathers the scale codes of 4 consecutive blocks held by lanes l, l+2, l+4, l+6
@@ -86,88 +85,183 @@ __device__ __forceinline__ uint32_t gather_sf_word(uint32_t sfc) {
 
 // ------------------------------------------------------------------ act_quant
 
-// TPR threads per row (a multiple of 32 dividing 256), up to VPT 8-element
-// vectors per thread.  Thread t of a row holds vectors t, t+TPR, ...; two lanes
-// share each 16-element block.  Rows M..rows_pad-1 are scale padding: their scale
-// words are written as 0, nothing else.
-template <int TPR, int VPT>
-__global__ void __launch_bounds__(256) act_quant_kernel(const __nv_bfloat16* __restrict__ X,
-                                                        int64_t M, int64_t K, int64_t rows_pad,
-                                                        uint8_t* __restrict__ codes,
-                                                        uint8_t* __restrict__ sf,
-                                                        float* __restrict__ s_row) {
-    constexpr int kRowsPerCta = 256 / TPR;
-    constexpr int kWarpsPerRow = TPR / 32;
-    __shared__ float red[8];
+// Persistent, several 8-warp CTAs per SM.  Warps form groups of G (32 G threads per
+// row); each group owns a ring of kAqRing row buffers in shared memory that one lane
+// fills with bulk copies (kAqRing rows ahead; a shallow ring keeps more CTAs per SM,
+// which measured faster than a deeper one), so HBM streams while the group
+// quantizes earlier rows from shared memory.  One lane per 16-element block:
+//   pass 1: block maxima on packed bf16 pairs (kept in registers), row amax (warp
+//           shuffles, then shared memory across the group's warps);
+//   pass 2: the block's E4M3 scale, its 16 E2M1 codes (8 bytes), and one scale
+//           word per 4 blocks.
+// Rows M..rows_pad-1 are scale padding: their scale words are written as 0.
+constexpr int kAqWarps = 8;
+constexpr int kAqRing = 2;
+constexpr int kAqMaxBpt = 8;  // 16-element blocks per thread (K <= 4096 * G)
 
-    const int tid = threadIdx.x;
-    const int t = tid % TPR;
-    const int64_t m = (int64_t)blockIdx.x * kRowsPerCta + tid / TPR;
-    const bool valid = m < M;
-    const bool exists = m < rows_pad;
-    const int nvec = (int)(K >> 3);
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t m, uint32_t w) {
+    // Max of magnitudes, lane-wise on two bf16 values: clearing the sign bits makes the
+    // bit patterns order like the magnitudes, so an unsigned 16-bit max is exact.
+    return __vmaxu2(m, w & 0x7FFF7FFFu);
+}
 
-    const uint4* xr = reinterpret_cast<const uint4*>(X + (valid ? m : 0) * K);
-    uint4 v[VPT];
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-        const int vi = t + i * TPR;
-        v[i] = (valid && vi < nvec) ? ld_stream_v4(xr + vi) : make_uint4(0, 0, 0, 0);
-        float x[8];
-        unpack8(v[i], x);
-        amax = fmaxf(amax, absmax8(x));
-    }
-    amax = warp_max(amax);
-    if (kWarpsPerRow > 1) {
-        if ((tid & 31) == 0) red[tid >> 5] = amax;
-        __syncthreads();
-        const int w0 = (tid / TPR) * kWarpsPerRow;
-#pragma unroll
-        for (int w = 0; w < kWarpsPerRow; ++w) amax = fmaxf(amax, red[w0 + w]);
-    }
+template <int G>
+__global__ void __launch_bounds__(kAqWarps * 32)
+    act_quant_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t K, int64_t rows_pad,
+                     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                     float* __restrict__ s_row, int* status) {
+    constexpr int kGroups = kAqWarps / G;
+    constexpr int kThreadsPerRow = 32 * G;
+    extern __shared__ __align__(128) uint8_t aq_smem[];
+    __shared__ uint64_t full[kGroups][kAqRing];
+    __shared__ float red[kAqWarps];
+    __shared__ int abort_flag;
 
-    const float s = __fdiv_rn(amax, kAmaxDiv);
-    if (valid && t == 0) s_row[m] = s;
-    const float d = __fmul_rn(6.0f, s);
-    const bool d_fast = fast_recip_ok(d);
-    const float inv_d = d_fast ? __frcp_rn(d) : 0.0f;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int group = warp / G;
+    const int t = threadIdx.x % kThreadsPerRow;  // thread within the row group
+    const int nblk = (int)(K >> 4);
+    const uint32_t row_bytes = (uint32_t)(K * 2);
+    uint8_t* ring = aq_smem + (size_t)group * kAqRing * row_bytes;
+    const int64_t first = (int64_t)blockIdx.x * kGroups + group;
+    const int64_t step = (int64_t)gridDim.x * kGroups;
 
-    uint32_t* crow = reinterpret_cast<uint32_t*>(codes + (valid ? m : 0) * (K >> 1));
-#pragma unroll
-    for (int i = 0; i < VPT; ++i) {
-        const int vi = t + i * TPR;
-        float x[8];
-        unpack8(v[i], x);
-        uint32_t sfc;
-        const uint32_t packed = quant_half_block(x, s, d, inv_d, d_fast, &sfc);
-        const uint32_t word = gather_sf_word(sfc);
-        if (vi < nvec) {
-            if (valid) crow[vi] = packed;
-            if (exists && (vi & 7) == 0)
-                *reinterpret_cast<uint32_t*>(sf + sf_word_offset(m, vi >> 1, K)) = word;
+    if (threadIdx.x == 0) abort_flag = 0;
+    if (t == 0)
+        for (int s = 0; s < kAqRing; ++s) mbar_init(&full[group][s], 1);
+    fence_barrier_init();
+    __syncthreads();
+
+    // Prologue: the first kAqRing rows of this group.
+    if (t == 0) {
+        for (int s = 0; s < kAqRing; ++s) {
+            const int64_t m = first + s * step;
+            if (m < M) {
+                mbar_arrive_expect_tx(&full[group][s], row_bytes);
+                bulk_load(ring + s * row_bytes, X + m * K, row_bytes, &full[group][s]);
+            }
         }
     }
+
+    int slot = 0;
+    uint32_t phase = 0;
+    for (int64_t m = first; m < rows_pad; m += step) {
+        const bool valid = m < M;
+        const uint4* srow = reinterpret_cast<const uint4*>(ring + slot * row_bytes);
+        if (valid) {
+            bool ok = mbar_wait(&full[group][slot], phase, status, &abort_flag, 4000000000ull);
+            ok = __all_sync(kFull, ok);
+            if (!ok) break;
+        }
+        // Pass 1: block maxima and the row amax.
+        float bmax[kAqMaxBpt];
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kAqMaxBpt; ++i) {
+            const int b = t + i * kThreadsPerRow;
+            float bm = 0.0f;
+            if (valid && b < nblk) {
+                const uint4 u0 = srow[2 * b], u1 = srow[2 * b + 1];
+                uint32_t mm = bf16x2_absmax(0u, u0.x);
+                mm = bf16x2_absmax(mm, u0.y);
+                mm = bf16x2_absmax(mm, u0.z);
+                mm = bf16x2_absmax(mm, u0.w);
+                mm = bf16x2_absmax(mm, u1.x);
+                mm = bf16x2_absmax(mm, u1.y);
+                mm = bf16x2_absmax(mm, u1.z);
+                mm = bf16x2_absmax(mm, u1.w);
+                bm = fmaxf(bf16_lo(mm), bf16_hi(mm));
+            }
+            bmax[i] = bm;
+            amax = fmaxf(amax, bm);
+        }
+        amax = warp_max(amax);
+        if (G > 1) {
+            if (lane == 0) red[warp] = amax;
+            named_barrier_sync(1 + group, kThreadsPerRow);
+#pragma unroll
+            for (int w = 0; w < G; ++w) amax = fmaxf(amax, red[group * G + w]);
+        }
+        const float s = __fdiv_rn(amax, kAmaxDiv);
+        if (valid && t == 0) s_row[m] = s;
+        const float d = __fmul_rn(6.0f, s);
+        const bool d_fast = fast_recip_ok(d);
+        const float inv_d = d_fast ? recip_approx(d) : 0.0f;
+
+        // Pass 2: one block per lane.
+        uint2* crow = reinterpret_cast<uint2*>(codes + (valid ? m : 0) * (K >> 1));
+#pragma unroll
+        for (int i = 0; i < kAqMaxBpt; ++i) {
+            if (i * kThreadsPerRow >= nblk) break;  // uniform across the warp
+            const int b = t + i * kThreadsPerRow;
+            const bool have = b < nblk;
+            uint32_t sfc = 0;
+            if (d > 0.0f) sfc = e4m3_quotient(bmax[i], d, inv_d, d_fast);
+            const float den = __fmul_rn(e4m3_value(sfc), s);
+            uint2 packed = make_uint2(0u, 0u);
+            if (valid && have && den > 0.0f) {
+                const bool fast = fast_recip_ok(den);
+                const float r = fast ? recip_approx(den) : 0.0f;
+                float x[8];
+                unpack8(srow[2 * b], x);
+                packed.x = e2m1_quotient8(x, den, r, fast);
+                unpack8(srow[2 * b + 1], x);
+                packed.y = e2m1_quotient8(x, den, r, fast);
+            }
+            // Scale codes of blocks b..b+3 (lanes l..l+3, l % 4 == 0) -> one word.
+            const uint32_t s1 = __shfl_down_sync(kFull, sfc, 1);
+            const uint32_t s2 = __shfl_down_sync(kFull, sfc, 2);
+            const uint32_t s3 = __shfl_down_sync(kFull, sfc, 3);
+            if (have) {
+                if (valid) crow[b] = packed;
+                if ((b & 3) == 0)
+                    *reinterpret_cast<uint32_t*>(sf + sf_word_offset(m, b, K)) =
+                        sfc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+            }
+        }
+
+        // Every thread of the group is done with this slot: refill it kAqRing rows ahead.
+        if (G > 1) named_barrier_sync(1 + group, kThreadsPerRow);
+        else __syncwarp();
+        if (t == 0) {
+            const int64_t next = m + kAqRing * step;
+            if (next < M) {
+                mbar_arrive_expect_tx(&full[group][slot], row_bytes);
+                bulk_load(ring + slot * row_bytes, X + next * K, row_bytes, &full[group][slot]);
+            }
+        }
+        if (valid) {
+            if (++slot == kAqRing) {
+                slot = 0;
+                phase ^= 1u;
+            }
+        }
+    }
+    // After an abort, give copies already issued time to land before the CTA exits.
+    if (abort_flag && t == 0) {
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
+    }
 }
 
-template <int TPR, int VPT>
+template <int G>
 cudaError_t run_act_quant(const LaunchCtx& ctx, const __nv_bfloat16* X, int64_t M, int64_t K,
                           int64_t rows_pad, uint8_t* codes, uint8_t* sf, float* s_row) {
-    const int64_t grid = (rows_pad + (256 / TPR) - 1) / (256 / TPR);
-    act_quant_kernel<TPR, VPT><<<(unsigned)grid, 256, 0, ctx.stream>>>(X, M, K, rows_pad, codes, sf,
-                                                                        s_row);
+    const size_t smem = (size_t)(kAqWarps / G) * kAqRing * (size_t)K * 2;
+    cudaError_t e = cudaFuncSetAttribute(act_quant_kernel<G>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, act_quant_kernel<G>, kAqWarps * 32,
+                                                      smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) per_sm = 1;
+    int64_t grid = (rows_pad + (kAqWarps / G) - 1) / (kAqWarps / G);
+    if (grid > (int64_t)ctx.num_sms * per_sm) grid = (int64_t)ctx.num_sms * per_sm;
+    act_quant_kernel<G><<<(unsigned)grid, kAqWarps * 32, smem, ctx.stream>>>(X, M, K, rows_pad, codes,
+                                                                          sf, s_row, ctx.status);
     return cudaGetLastError();
-}
-
-template <int TPR>
-cudaError_t dispatch_vpt(const LaunchCtx& ctx, const __nv_bfloat16* X, int64_t M, int64_t K,
-                         int64_t rows_pad, uint8_t* codes, uint8_t* sf, float* s_row) {
-    const int64_t nvec = K >> 3;
-    const int64_t per = (nvec + TPR - 1) / TPR;
-    if (per <= 4) return run_act_quant<TPR, 4>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-    if (per <= 8) return run_act_quant<TPR, 8>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-    if (per <= 12) return run_act_quant<TPR, 12>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-    return run_act_quant<TPR, 16>(ctx, X, M, K, rows_pad, codes, sf, s_row);
 }
 
 // ------------------------------------------------------------------ requant
@@ -314,7 +408,7 @@ __global__ void __launch_bounds__(256) requant_quant_kernel(RqArgs a) {
     const float s = __fdiv_rn(amax, kAmaxDiv);
     const float d = __fmul_rn(6.0f, s);
     const bool d_fast = fast_recip_ok(d);
-    const float inv_d = d_fast ? __frcp_rn(d) : 0.0f;
+    const float inv_d = d_fast ? recip_approx(d) : 0.0f;
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int64_t n = n0 + rg * 4 + i;
@@ -377,7 +471,7 @@ __global__ void test_e2m1_quotient_kernel(const float* x, const float* den, uint
          i += (int64_t)gridDim.x * blockDim.x) {
         const float dn = den[i];
         const bool fast = fast_recip_ok(dn);
-        const float r = fast ? __frcp_rn(dn) : 0.0f;
+        const float r = fast ? recip_approx(dn) : 0.0f;
         const float xs[8] = {x[i], 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         out[i] = (uint8_t)(e2m1_quotient8(xs, dn, r, fast) & 0xFu);
     }
@@ -389,7 +483,7 @@ __global__ void test_e4m3_quotient_kernel(const float* v, const float* d, uint8_
          i += (int64_t)gridDim.x * blockDim.x) {
         const float dd = d[i];
         const bool fast = fast_recip_ok(dd);
-        out[i] = (uint8_t)e4m3_quotient(v[i], dd, fast ? __frcp_rn(dd) : 0.0f, fast);
+        out[i] = (uint8_t)e4m3_quotient(v[i], dd, fast ? recip_approx(dd) : 0.0f, fast);
     }
 }
 
@@ -404,11 +498,12 @@ unsigned grid_for(int64_t n, const LaunchCtx& ctx) {
 cudaError_t launch_act_quant(const LaunchCtx& ctx, const __nv_bfloat16* X, int64_t M, int64_t K,
                              uint8_t* codes, uint8_t* sf, float* s_row) {
     const int64_t rows_pad = (M + 127) / 128 * 128;
-    const int64_t nvec = K >> 3;
-    if (nvec <= 32 * 16) return dispatch_vpt<32>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-    if (nvec <= 64 * 16) return dispatch_vpt<64>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-    if (nvec <= 128 * 16) return dispatch_vpt<128>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-    return dispatch_vpt<256>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+    // G warps per row: at most 4 blocks of 16 elements per thread up to K = 16384 (a
+    // smaller ring footprint per CTA, so more CTAs per SM), 8 beyond.
+    if (K <= 2048) return run_act_quant<1>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+    if (K <= 4096) return run_act_quant<2>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+    if (K <= 8192) return run_act_quant<4>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+    return run_act_quant<8>(ctx, X, M, K, rows_pad, codes, sf, s_row);
 }
 
 cudaError_t launch_requant(const LaunchCtx& ctx, const void* W, int w_dtype, const float* A,
