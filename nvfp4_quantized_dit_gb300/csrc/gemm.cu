@@ -101,16 +101,30 @@ struct GemmArgs {
     int* status;
 };
 
-// Pair tiles: tile t covers m-blocks 2*(t % num_mp) + {0, 1} (one per CTA) and
-// n-block t / num_mp; cluster c walks t = c, c + num_clusters, ...
+// Pair tiles, grouped for L2 reuse: tiles are ordered in bands of kBandMp m-pairs
+// (256 rows each); inside a band the m-pair varies fastest,
+// then the n-block.  The clusters walk t = c, c + num_clusters, ..., so the tiles in
+// flight at any time share a few m-pairs (their A rows are read from DRAM once) and
+// sweep B band by band (B is re-read once per band), instead of re-reading A for
+// every n-block.  Tile t covers m-blocks 2 mp + {0, 1} (one per CTA) and n-block nb.
+constexpr int kBandMp = 16;
+
 struct Sched {
-    int num_m, num_mp, total, first, step;
+    int num_m, num_mp, num_n, total, first, step;
     __device__ Sched(int M, int N) {
         num_m = (M + BM - 1) / BM;
         num_mp = (num_m + kPair - 1) / kPair;
-        total = num_mp * ((N + BN - 1) / BN);
+        num_n = (N + BN - 1) / BN;
+        total = num_mp * num_n;
         first = (int)(blockIdx.x / kPair);
         step = (int)(gridDim.x / kPair);
+    }
+    __device__ __forceinline__ void tile(int t, int& mp, int& nb) const {
+        const int band = t / (kBandMp * num_n);
+        const int within = t - band * (kBandMp * num_n);
+        const int rows = min(kBandMp, num_mp - band * kBandMp);  // m-pairs in this band
+        mp = band * kBandMp + within % rows;
+        nb = within / rows;
     }
 };
 
@@ -187,8 +201,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t phase = 0;
             bool ok = true;
             for (int t = sch.first; ok && t < sch.total; t += sch.step) {
-                const int m_blk = (t % sch.num_mp) * kPair + (int)rank;
-                const int n_blk = t / sch.num_mp;
+                int mp, n_blk;
+                sch.tile(t, mp, n_blk);
+                const int m_blk = mp * kPair + (int)rank;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, args.status, abort_flag,
                                    kWaitLimitNs)) {
@@ -355,8 +370,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t acc_phase = 0;
         const float w_scale = kFP4 ? *args.w_st : 1.0f;
         for (int t = sch.first; t < sch.total; t += sch.step) {
-            const int m_blk = (t % sch.num_mp) * kPair + (int)rank;
-            const int n_blk = t / sch.num_mp;
+            int mp, n_blk;
+            sch.tile(t, mp, n_blk);
+            const int m_blk = mp * kPair + (int)rank;
             const int row = m_blk * BM + quarter * 32 + lane;
             const int n0 = n_blk * BN + half * 128;
             // Fetch this tile's per-row scale and the warp's 128 bias values while the
