@@ -112,7 +112,10 @@ static inline size_t nvfp4_sf_offset(int64_t row, int64_t kblk, int64_t K) {
  *   s_t    device, one fp32 (out): amax(|W'|) / 2688.  Also used as the amax
  *          accumulator while the call runs, so it must not alias other buffers.
  *   K % 64 == 0, K <= 1 << 20, N < 2^31.
- * Enqueues a memset and three kernels (merge + amax; merge + quantize; finalize s_t).
+ * Enqueues a memset and three kernels: exact amax|W'| (W read once; only the
+ * elements whose |W| a Cauchy-Schwarz bound on the LoRA term leaves in reach of
+ * the maximum are merged), merge + quantize (every element merged once), and a
+ * one-thread finalize of s_t.  Inputs must be finite.
  */
 nvfp4_status nvfp4_requant(const void* W, int w_dtype, const float* A, const float* B, int r,
                            float alpha, int64_t N, int64_t K, uint8_t* codes, uint8_t* sf,
@@ -210,6 +213,15 @@ nvfp4_status nvfp4_test_e2m1_quotient(const float* x, const float* den, uint8_t*
  * quantizers' reciprocal fast path with its exact-division fallback. */
 nvfp4_status nvfp4_test_e4m3_quotient(const float* v, const float* d, uint8_t* codes, int64_t n,
                                       void* stream);
+
+/*
+ * out[n, k] = W'[n, k] (fp32, device, [N, K]): the merged weights exactly as
+ * nvfp4_requant computes them before quantizing (its second kernel, writing the
+ * merged values instead of codes).  Arguments and limits as nvfp4_requant;
+ * out must be 16-byte aligned.
+ */
+nvfp4_status nvfp4_test_merge(const void* W, int w_dtype, const float* A, const float* B, int r,
+                              float alpha, int64_t N, int64_t K, float* out, void* stream);
 
 /*
  * Launches one CTA that waits on a shared-memory barrier nothing will ever

@@ -22,7 +22,7 @@ __all__ = [
     "nvfp4_requant", "nvfp4_act_quant", "nvfp4_gemm", "bf16_gemm", "select_contrastive",
     "nvfp4_device_status", "nvfp4_status_string", "nvfp4_version",
     "nvfp4_test_e2m1", "nvfp4_test_e4m3", "nvfp4_test_e2m1_quotient", "nvfp4_test_e4m3_quotient",
-    "nvfp4_test_wait_timeout",
+    "nvfp4_test_merge", "nvfp4_test_wait_timeout",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnvfp4rl.so")
@@ -62,6 +62,7 @@ def library() -> ctypes.CDLL:
                 "nvfp4_test_e4m3": [P, P, I64, P],
                 "nvfp4_test_e2m1_quotient": [P, P, P, I64, P],
                 "nvfp4_test_e4m3_quotient": [P, P, P, I64, P],
+                "nvfp4_test_merge": [P, I, P, P, I, F, I64, I64, P, P],
                 "nvfp4_test_wait_timeout": [I64, P],
             }
             for name, args in sig.items():
@@ -234,6 +235,20 @@ def nvfp4_test_e4m3_quotient(v, d, out=None, stream=None):
     out = torch.empty(v.numel(), dtype=torch.uint8, device=v.device) if out is None else out
     _call("nvfp4_test_e4m3_quotient", _dev(v, "v", torch.float32), _dev(d, "d", torch.float32),
           _dev(out, "codes", torch.uint8), v.numel(), _stream(stream))
+    return out
+
+
+def nvfp4_test_merge(W, A=None, B=None, alpha: float = 32.0, out=None, stream=None):
+    """The merged weights W' [N, K] (fp32) exactly as nvfp4_requant forms them."""
+    N, K = W.shape
+    w_dtype = {torch.bfloat16: W_BF16, torch.float32: W_FP32}.get(W.dtype)
+    if w_dtype is None:
+        raise TypeError("W must be bfloat16 or float32")
+    r = 0 if (A is None or B is None) else A.shape[0]
+    out = torch.empty(N, K, dtype=torch.float32, device=W.device) if out is None else out
+    _call("nvfp4_test_merge", _dev(W, "W"), w_dtype, _opt(A, "A", torch.float32),
+          _opt(B, "B", torch.float32), r, ctypes.c_float(alpha), N, K,
+          _dev(out, "out", torch.float32), _stream(stream))
     return out
 
 

@@ -308,6 +308,24 @@ nvfp4_status nvfp4_test_e4m3_quotient(const float* v, const float* d, uint8_t* c
     return st != NVFP4_OK ? st : from_cuda(launch_test_e4m3_quotient(ctx, v, d, codes, n));
 }
 
+nvfp4_status nvfp4_test_merge(const void* W, int w_dtype, const float* A, const float* B, int r,
+                              float alpha, int64_t N, int64_t K, float* out, void* stream) {
+    if (w_dtype != NVFP4_W_BF16 && w_dtype != NVFP4_W_FP32) return NVFP4_ERR_SHAPE;
+    if (r < 0 || r > 64 || N < 0 || N > kMaxRows || K <= 0 || K % 64 != 0 || K > (1 << 20))
+        return NVFP4_ERR_SHAPE;
+    if (N == 0) return NVFP4_OK;
+    if (W == nullptr || out == nullptr) return NVFP4_ERR_NULL;
+    const bool merge = r > 0 && A != nullptr && B != nullptr;
+    if (misaligned(W, 16) || misaligned(out, 16)) return NVFP4_ERR_ALIGN;
+    if (merge && (misaligned(A, 16) || misaligned(B, 4))) return NVFP4_ERR_ALIGN;
+    LaunchCtx ctx;
+    nvfp4_status st = resolve(stream, &ctx);
+    if (st != NVFP4_OK) return st;
+    const float c = merge ? alpha / static_cast<float>(r) : 0.0f;
+    return from_cuda(launch_test_merge(ctx, W, w_dtype, merge ? A : nullptr, merge ? B : nullptr,
+                                       merge ? r : 0, c, N, K, out));
+}
+
 nvfp4_status nvfp4_test_wait_timeout(int64_t timeout_ns, void* stream) {
     if (timeout_ns < 1000 || timeout_ns > 10000000000LL) return NVFP4_ERR_SHAPE;
     LaunchCtx ctx;

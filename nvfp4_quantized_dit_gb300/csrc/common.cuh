@@ -28,6 +28,8 @@ cudaError_t launch_act_quant(const LaunchCtx&, const __nv_bfloat16* X, int64_t M
 cudaError_t launch_requant(const LaunchCtx&, const void* W, int w_dtype, const float* A,
                            const float* B, int r, float c, int64_t N, int64_t K, uint8_t* codes,
                            uint8_t* sf, float* s_t);
+cudaError_t launch_test_merge(const LaunchCtx&, const void* W, int w_dtype, const float* A,
+                              const float* B, int r, float c, int64_t N, int64_t K, float* out);
 cudaError_t launch_select(const LaunchCtx&, const float* rewards, int P, int N, int K,
                           int global_std, int32_t* idx, float* r_out);
 cudaError_t launch_test_e2m1(const LaunchCtx&, const float* q, uint8_t* codes, int64_t n);

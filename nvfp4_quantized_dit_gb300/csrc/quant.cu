@@ -265,11 +265,22 @@ cudaError_t run_act_quant(const LaunchCtx& ctx, const __nv_bfloat16* X, int64_t 
 }
 
 // ------------------------------------------------------------------ requant
-
-// CTA tile: 64 rows x 128 columns of W; thread tile 4 rows x 8 columns.  Lane
-// l of warp w owns column group cg = l % 16 and row group rg = 2w + l / 16.
+//
+// Both kernels walk the same tiles: kRqRows x kRqCols pieces of W in strip-major
+// order (a strip is kRqCols columns), each CTA a contiguous run of tiles, so a CTA
+// stages the r x kRqCols strip of A in shared memory about once.  Warp w owns rows
+// 16 (w / 2) .. +15 and columns 64 (w % 2) .. +63 of a tile; lane l owns the 4 rows
+// 4 i + l / 8 (i = 0..3) of that block and the 8 columns 8 (l % 8) .. +7, so the
+// 16-element scale block of a row lives in lanes l, l ^ 1 and one scale word (4
+// blocks) in 8 consecutive lanes.  Each warp copies the 16 rows of B it needs into
+// its own double-buffered slice of shared memory, one tile ahead (row stride rs = r
+// rounded up to 8, plus 4, which keeps the four rows a load instruction touches on
+// distinct banks).
 constexpr int kRqRows = 64;
 constexpr int kRqCols = 128;
+constexpr int kRqThreads = 256;
+constexpr int kRqWarps = kRqThreads / 32;
+constexpr int kRqMaxR = 64;
 
 struct RqArgs {
     const void* W;
@@ -281,173 +292,546 @@ struct RqArgs {
     uint8_t* codes;
     uint8_t* sf;
     float* s_t;
+    float* dump;  // test hook: merged values instead of codes
+    int64_t row_tiles, tiles;
+    int rs;     // row stride of B in shared memory (floats)
+    int inv_r;  // ceil(2^16 / r): x / r == (x * inv_r) >> 16 for 0 <= x < 16 r
+    int b_vec;  // B 16-byte aligned and r % 4 == 0: 16-byte copies
 };
 
-// Merged values w'[4][8] of this thread's tile, per the library's merge order:
-// acc = +0; acc = fma(B[n,j], A[j,k], acc) for j = 0..r-1; w' = fma(c, acc, W).
-template <int kWType>
-__device__ __forceinline__ void merge_tile(const RqArgs& a, const float* As, const float* Bs,
-                                           int64_t n0, int64_t k0, bool col_ok,
-                                           float (&w)[4][8]) {
-    float acc[4][8];
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
-    const int cg = threadIdx.x & 15;
-    const int rg = threadIdx.x >> 4;
-    if (a.r > 0) {
-#pragma unroll 4
-        for (int j = 0; j < a.r; ++j) {
-            const float4 a0 = *reinterpret_cast<const float4*>(As + j * kRqCols + cg * 8);
-            const float4 a1 = *reinterpret_cast<const float4*>(As + j * kRqCols + cg * 8 + 4);
-            const float4 b = *reinterpret_cast<const float4*>(Bs + j * kRqRows + rg * 4);
-            const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
-            const float bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-#pragma unroll
-                for (int q = 0; q < 8; ++q) acc[i][q] = __fmaf_rn(bv[i], av[q], acc[i][q]);
-        }
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int64_t n = n0 + rg * 4 + i;
-        float wv[8];
-        if (n < a.N && col_ok) {
-            if (kWType == NVFP4_W_BF16) {
-                const uint4 raw = ld_stream_v4(static_cast<const __nv_bfloat16*>(a.W) + n * a.K +
-                                               k0 + cg * 8);
-                unpack8(raw, wv);
-            } else {
-                const float* p = static_cast<const float*>(a.W) + n * a.K + k0 + cg * 8;
-                const uint4 r0 = ld_stream_v4(p);
-                const uint4 r1 = ld_stream_v4(p + 4);
-                wv[0] = __uint_as_float(r0.x); wv[1] = __uint_as_float(r0.y);
-                wv[2] = __uint_as_float(r0.z); wv[3] = __uint_as_float(r0.w);
-                wv[4] = __uint_as_float(r1.x); wv[5] = __uint_as_float(r1.y);
-                wv[6] = __uint_as_float(r1.z); wv[7] = __uint_as_float(r1.w);
-            }
-        } else {
-#pragma unroll
-            for (int q = 0; q < 8; ++q) wv[q] = 0.0f;
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q) w[i][q] = (a.r > 0) ? __fmaf_rn(a.c, acc[i][q], wv[q]) : wv[q];
-    }
+__host__ __device__ constexpr int rq_bstride(int r) { return ((r + 7) & ~7) + 4; }
+
+__host__ __device__ constexpr int rq_inv_r(int r) { return r > 0 ? (65536 + r - 1) / r : 0; }
+
+// The multiply-shift quotient is exact for every index a B copy uses.
+constexpr bool rq_inv_r_exact() {
+    for (int r = 1; r <= kRqMaxR; ++r)
+        for (int x = 0; x < 16 * r; ++x)
+            if (((x * rq_inv_r(r)) >> 16) != x / r) return false;
+    return true;
+}
+static_assert(rq_inv_r_exact(), "x * ceil(2^16 / r) >> 16 must equal x / r for x < 16 r");
+
+__host__ __device__ inline size_t rq_smem_bytes(int r) {
+    return ((size_t)r * kRqCols + (size_t)kRqWarps * 2 * 16 * rq_bstride(r)) * sizeof(float);
 }
 
-// Stages A[:, k0:k0+128] as As[j][col] and B[n0:n0+64, :]^T as Bs[j][row].
-__device__ __forceinline__ void stage_lora(const RqArgs& a, float* As, float* Bs, int64_t n0,
-                                           int64_t k0) {
-    const int tid = threadIdx.x;
-    for (int e = tid; e < a.r * (kRqCols / 4); e += 256) {
+struct RqLane {
+    int warp, lane, wr, wc, cg, rg;
+    __device__ __forceinline__ RqLane() {
+        warp = threadIdx.x >> 5;
+        lane = threadIdx.x & 31;
+        wr = warp >> 1;
+        wc = warp & 1;
+        cg = lane & 7;
+        rg = lane >> 3;
+    }
+    // Tile-local row of this lane's row i, and the warp-slice row of B it reads.
+    __device__ __forceinline__ int row(int i) const { return wr * 16 + i * 4 + rg; }
+    __device__ __forceinline__ int brow(int i) const { return i * 4 + rg; }
+    __device__ __forceinline__ int col() const { return wc * 64 + cg * 8; }
+};
+
+// Position in the strip-major tile order, advanced one tile at a time.
+struct RqCursor {
+    int64_t strip, rt;
+    __device__ __forceinline__ void init(const RqArgs& a, int64_t t) {
+        strip = t / a.row_tiles;
+        rt = t - strip * a.row_tiles;
+    }
+    __device__ __forceinline__ void next(const RqArgs& a) {
+        if (++rt == a.row_tiles) {
+            rt = 0;
+            ++strip;
+        }
+    }
+    __device__ __forceinline__ int64_t n0() const { return rt * kRqRows; }
+    __device__ __forceinline__ int64_t k0() const { return strip * kRqCols; }
+};
+
+// A[:, k0:k0+kRqCols] -> As[j][col], zero past K.  Called by the whole CTA.
+__device__ __forceinline__ void rq_stage_a(const RqArgs& a, float* As, int64_t k0) {
+    for (int e = threadIdx.x; e < a.r * (kRqCols / 4); e += kRqThreads) {
         const int j = e / (kRqCols / 4), c4 = e % (kRqCols / 4);
         const int64_t k = k0 + c4 * 4;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
         if (k < a.K) v = *reinterpret_cast<const float4*>(a.A + (int64_t)j * a.K + k);
         *reinterpret_cast<float4*>(As + j * kRqCols + c4 * 4) = v;
     }
-    for (int e = tid; e < a.r * kRqRows; e += 256) {
-        const int row = e % kRqRows, j = e / kRqRows;
-        const int64_t n = n0 + row;
-        Bs[j * kRqRows + row] = (n < a.N) ? a.B[n * a.r + j] : 0.0f;
+}
+
+// Asynchronous copies of B[row0 : row0+16, :] (the warp's rows; rows past N are
+// zero-filled) into the warp's slice Bw with row stride rs.  One commit group.
+__device__ __forceinline__ void rq_copy_b(const RqArgs& a, int lane, int64_t row0, float* Bw) {
+    if (a.b_vec) {
+        for (int c = lane; c < 4 * a.r; c += 32) {
+            const int x = 4 * c;
+            const int rl = (x * a.inv_r) >> 16, j = x - rl * a.r;
+            const bool valid = row0 + rl < a.N;
+            const float* src = a.B + (valid ? (row0 + rl) * a.r + j : 0);
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                             smem_u32(Bw + rl * a.rs + j)),
+                         "l"(src), "r"(valid ? 16 : 0)
+                         : "memory");
+        }
+    } else {
+        for (int x = lane; x < 16 * a.r; x += 32) {
+            const int rl = (x * a.inv_r) >> 16, j = x - rl * a.r;
+            const bool valid = row0 + rl < a.N;
+            const float* src = a.B + (valid ? (row0 + rl) * a.r + j : 0);
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                             smem_u32(Bw + rl * a.rs + j)),
+                         "l"(src), "r"(valid ? 4 : 0)
+                         : "memory");
+        }
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void rq_commit_empty() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Waits until at most one of this lane's copy groups is pending, then makes the
+// warp's copies visible to the whole warp.
+__device__ __forceinline__ void rq_wait_b() {
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+    __syncwarp();
+}
+
+// W rows of this lane for one tile, as raw 16-byte words (bf16: one per row; fp32: two).
+template <int kWType>
+struct RqW {
+    static constexpr int kWords = kWType == NVFP4_W_BF16 ? 1 : 2;
+    uint4 v[4][kWords];
+
+    __device__ __forceinline__ void load(const RqArgs& a, const RqLane& L, int64_t n0, int64_t k0) {
+        const int64_t k = k0 + L.col();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t n = n0 + L.row(i);
+            const bool ok = n < a.N && k < a.K;
+#pragma unroll
+            for (int w = 0; w < kWords; ++w) {
+                if (ok) {
+                    if (kWType == NVFP4_W_BF16)
+                        v[i][w] = ld_stream_v4(static_cast<const __nv_bfloat16*>(a.W) + n * a.K + k);
+                    else
+                        v[i][w] = ld_stream_v4(static_cast<const float*>(a.W) + n * a.K + k + 4 * w);
+                } else {
+                    v[i][w] = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+        }
+    }
+
+    __device__ __forceinline__ void row(int i, float (&x)[8]) const {
+        if (kWType == NVFP4_W_BF16) {
+            unpack8(v[i][0], x);
+        } else {
+            x[0] = __uint_as_float(v[i][0].x); x[1] = __uint_as_float(v[i][0].y);
+            x[2] = __uint_as_float(v[i][0].z); x[3] = __uint_as_float(v[i][0].w);
+            x[4] = __uint_as_float(v[i][kWords - 1].x); x[5] = __uint_as_float(v[i][kWords - 1].y);
+            x[6] = __uint_as_float(v[i][kWords - 1].z); x[7] = __uint_as_float(v[i][kWords - 1].w);
+        }
+    }
+
+    // Bit 8 i + q set where row i is in `rows` and |W[i][q]| >= t.
+    __device__ __forceinline__ unsigned mask_ge(unsigned rows, float t) const {
+        unsigned msk = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float x[8];
+            row(i, x);
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                msk |= (((rows >> i) & 1u) && fabsf(x[q]) >= t) ? 1u << (i * 8 + q) : 0u;
+        }
+        return msk;
+    }
+
+    // Element e = 8 i + q (selects from registers; no local-memory indexing).
+    __device__ __forceinline__ float at(int e) const {
+        const int i = e >> 3, q = e & 7;
+        uint4 lo = v[0][0], hi = v[0][kWords - 1];
+#pragma unroll
+        for (int k = 1; k < 4; ++k)
+            if (i == k) {
+                lo = v[k][0];
+                hi = v[k][kWords - 1];
+            }
+        if (kWType == NVFP4_W_BF16) {
+            const uint32_t w = (q >> 1) == 0 ? lo.x : (q >> 1) == 1 ? lo.y : (q >> 1) == 2 ? lo.z : lo.w;
+            return (q & 1) ? bf16_hi(w) : bf16_lo(w);
+        } else {
+            const uint4 h = q < 4 ? lo : hi;
+            const int qq = q & 3;
+            return __uint_as_float(qq == 0 ? h.x : qq == 1 ? h.y : qq == 2 ? h.z : h.w);
+        }
+    }
+
+    // max |W| over the rows whose bit is set in `rows` (-1 when none).
+    __device__ __forceinline__ float absmax(unsigned rows) const {
+        if (kWType == NVFP4_W_BF16) {
+            uint32_t m = 0;
+            bool any = false;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if ((rows >> i) & 1u) {
+                    any = true;
+                    m = bf16x2_absmax(m, v[i][0].x);
+                    m = bf16x2_absmax(m, v[i][0].y);
+                    m = bf16x2_absmax(m, v[i][0].z);
+                    m = bf16x2_absmax(m, v[i][0].w);
+                }
+            }
+            const uint32_t hi = m >> 16, lo = m & 0xFFFFu;
+            return any ? __uint_as_float((hi > lo ? hi : lo) << 16) : -1.0f;
+        } else {
+            float m = -1.0f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if ((rows >> i) & 1u) {
+                    float x[8];
+                    row(i, x);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) m = fmaxf(m, fabsf(x[q]));
+                }
+            }
+            return m;
+        }
+    }
+};
+
+// The merged value of one element, in the library's order: acc = +0;
+// acc = fma(B[n,j], A[j,k], acc) for j = 0..r-1; w' = fma(c, acc, W) (w' = W when r = 0).
+__device__ __forceinline__ float rq_merge_one(const RqArgs& a, const float* brow, const float* acol,
+                                              float w) {
+    if (a.r == 0) return w;
+    float acc = 0.0f;
+#pragma unroll 4
+    for (int j = 0; j < a.r; ++j) acc = __fmaf_rn(brow[j], acol[j * kRqCols], acc);
+    return __fmaf_rn(a.c, acc, w);
+}
+
+// ---- pass 1: exact amax|W'| without merging every element.
+//
+// For every element, |W'| <= (|W| + D) (1 + 2^-23) + 2^-140 with
+// D >= |c| (||B[n,:]||_2 ||A[:,k]||_2 (1 + 2^-17) + 2^-142): Cauchy-Schwarz bounds the
+// products' absolute sum, (1 + 2^-24)^r <= 1 + 2^-17 covers the r roundings of the
+// fma chain for r <= 64, and the absolute terms cover subnormal results.  A warp keeps
+// L, the largest |W'| it has evaluated exactly so far; an element can only raise it
+// if |W| >= tau(L, D), a round-down of (L - 2^-140) / (1 + 2^-23) - D, so only those
+// elements are merged (exactly, with the same fma chain as pass 2).  The norms are
+// upper bounds (sums of squares inflated for their own rounding, square roots
+// rounded up), D per warp and tile uses the largest row norm of its 16 rows and the
+// largest column norm of its 64 columns, every bound step rounds up (fp32 directed
+// rounding).  L is seeded from the exact value at the warp's largest |W| of the tile,
+// so typically a few elements per thousand are merged.
+__device__ __forceinline__ float rq_norm_ub(float sumsq) {
+    return __fsqrt_ru(__fmaf_ru(sumsq, 1.0f + 0x1p-17f, 0x1p-143f));
+}
+
+__device__ __forceinline__ float rq_tau(float L, float D) {
+    if (!(L > 0x1p-139f)) return -1.0f;
+    // (1 - 2^-22) <= 1 / (1 + 2^-23), and every step rounds down.
+    return __fsub_rd(__fmul_rd(__fsub_rd(L, 0x1p-140f), 1.0f - 0x1p-22f), D);
 }
 
 template <int kWType>
-__global__ void __launch_bounds__(256) requant_amax_kernel(RqArgs a) {
-    extern __shared__ float smem[];
-    float* As = smem;
-    float* Bs = smem + a.r * kRqCols;
-    __shared__ float red[8];
-    const int64_t n0 = (int64_t)blockIdx.x * kRqRows;
-    const int64_t k0 = (int64_t)blockIdx.y * kRqCols;
-    if (a.r > 0) {
-        stage_lora(a, As, Bs, n0, k0);
-        __syncthreads();
+__global__ void __launch_bounds__(kRqThreads, 2) requant_amax_kernel(RqArgs a) {
+    extern __shared__ __align__(16) float rq_smem[];
+    float* As = rq_smem;
+    const RqLane L;
+    float* Bw0 = rq_smem + a.r * kRqCols + L.warp * 2 * 16 * a.rs;
+
+    const int64_t t_begin = (int64_t)blockIdx.x * a.tiles / gridDim.x;
+    const int64_t t_end = (int64_t)(blockIdx.x + 1) * a.tiles / gridDim.x;
+    const float ac = fabsf(a.c);
+    int64_t staged = -1;
+    float amax_col = 0.0f;  // largest column norm of this warp's 64 columns (upper bound)
+    float Lw = 0.0f;        // warp-uniform: largest exact |W'| seen
+    RqW<kWType> wcur, wnext;
+    RqCursor cur;
+    cur.init(a, t_begin);
+    if (t_begin < t_end) {
+        wcur.load(a, L, cur.n0(), cur.k0());
+        rq_copy_b(a, L.lane, cur.n0() + L.wr * 16, Bw0);
     }
-    const bool col_ok = k0 + (threadIdx.x & 15) * 8 < a.K;
-    float w[4][8];
-    merge_tile<kWType>(a, As, Bs, n0, k0, col_ok, w);
-    float m = 0.0f;
+    int buf = 0;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        const int64_t n0 = cur.n0(), k0 = cur.k0();
+        if (cur.strip != staged) {
+            __syncthreads();
+            rq_stage_a(a, As, k0);
+            __syncthreads();
+            staged = cur.strip;
+            // Column norms: lane l covers columns 2l, 2l+1 of the warp's 64.
+            float m = 0.0f;
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
+            for (int h = 0; h < 2; ++h) {
+                const float* acol = As + L.wc * 64 + 2 * L.lane + h;
+                float s2 = 0.0f;
+#pragma unroll 4
+                for (int j = 0; j < a.r; ++j) s2 = __fmaf_rn(acol[j * kRqCols], acol[j * kRqCols], s2);
+                m = fmaxf(m, rq_norm_ub(s2));
+            }
+            amax_col = warp_max(m);
+        }
+        __syncwarp();
+        cur.next(a);
+        if (t + 1 < t_end) {
+            wnext.load(a, L, cur.n0(), cur.k0());
+            rq_copy_b(a, L.lane, cur.n0() + L.wr * 16, Bw0 + (buf ^ 1) * 16 * a.rs);
+        } else {
+            rq_commit_empty();
+        }
+        rq_wait_b();
+        const float* Bw = Bw0 + buf * 16 * a.rs;
+        buf ^= 1;
+
+        const bool col_ok = k0 + L.col() < a.K;
+        unsigned rows_ok = 0;
 #pragma unroll
-        for (int q = 0; q < 8; ++q) m = fmaxf(m, fabsf(w[i][q]));
-    m = warp_max(m);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        float b = 0.0f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) b = fmaxf(b, red[i]);
-        // |w'| >= 0, so the fp32 bit patterns order like the values.
-        atomicMax(reinterpret_cast<unsigned int*>(a.s_t), __float_as_uint(b));
+        for (int i = 0; i < 4; ++i) rows_ok |= (col_ok && n0 + L.row(i) < a.N) ? 1u << i : 0u;
+        const float m = wcur.absmax(rows_ok);
+        const float wm = warp_max(m);
+
+        float D = 0.0f;
+        if (a.r > 0) {
+            // Row norms: lanes 2m, 2m+1 share row m of the warp's 16 (halves of j).
+            float s2 = 0.0f;
+            const float* brow = Bw + (L.lane >> 1) * a.rs;
+#pragma unroll 4
+            for (int j = L.lane & 1; j < a.r; j += 2) s2 = __fmaf_rn(brow[j], brow[j], s2);
+            s2 += __shfl_xor_sync(kFull, s2, 1);  // two sums >= 0: one more rounding
+            const float bnorm = warp_max(rq_norm_ub(__fmul_ru(s2, 1.0f + 0x1p-22f)));
+            D = __fadd_ru(__fmul_ru(__fmul_ru(__fmul_ru(ac, bnorm), amax_col), 1.0f + 0x1p-16f),
+                          __fmul_ru(ac, 0x1p-140f));
+        }
+        // Only a tile whose largest |W| is within reach of L can raise it.
+        if (wm >= 0.0f && wm >= rq_tau(Lw, D)) {
+            // Seed: the exact value at the warp's largest |W| (lowest lane holding it).
+            const unsigned holders = __ballot_sync(kFull, m == wm);
+            int seed = -1;
+            float v = 0.0f;
+            if (L.lane == __ffs(holders) - 1) {
+                seed = __ffs(wcur.mask_ge(rows_ok, m)) - 1;
+                v = fabsf(rq_merge_one(a, Bw + L.brow(seed >> 3) * a.rs, As + L.col() + (seed & 7),
+                                       wcur.at(seed)));
+            }
+            Lw = fmaxf(Lw, warp_max(v));
+            // Then every element that could still exceed L, one merge call site.
+            const float tau = rq_tau(Lw, D);
+            float lm = 0.0f;
+            unsigned cand = m >= tau ? wcur.mask_ge(rows_ok, tau) : 0u;
+            if (seed >= 0) cand &= ~(1u << seed);
+            while (cand) {
+                const int e = __ffs(cand) - 1;
+                cand &= cand - 1;
+                lm = fmaxf(lm, fabsf(rq_merge_one(a, Bw + L.brow(e >> 3) * a.rs, As + L.col() + (e & 7),
+                                                  wcur.at(e))));
+            }
+            Lw = fmaxf(Lw, warp_max(lm));
+        }
+        wcur = wnext;
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
+    // |W'| >= 0, so the fp32 bit patterns order like the values.
+    if (L.lane == 0 && Lw > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(a.s_t), __float_as_uint(Lw));
 }
 
-template <int kWType>
-__global__ void __launch_bounds__(256) requant_quant_kernel(RqArgs a) {
-    extern __shared__ float smem[];
-    float* As = smem;
-    float* Bs = smem + a.r * kRqCols;
-    const int64_t n0 = (int64_t)blockIdx.x * kRqRows;
-    const int64_t k0 = (int64_t)blockIdx.y * kRqCols;
-    const float amax = *reinterpret_cast<volatile const float*>(a.s_t);
-    if (a.r > 0) {
-        stage_lora(a, As, Bs, n0, k0);
-        __syncthreads();
-    }
-    const int cg = threadIdx.x & 15;
-    const int rg = threadIdx.x >> 4;
-    const bool col_ok = k0 + cg * 8 < a.K;
-    float w[4][8];
-    merge_tile<kWType>(a, As, Bs, n0, k0, col_ok, w);
+// ---- pass 2: merge every element once and quantize it.
+template <int kWType, bool kDump>
+__global__ void __launch_bounds__(kRqThreads, 2) requant_quant_kernel(RqArgs a) {
+    extern __shared__ __align__(16) float rq_smem[];
+    float* As = rq_smem;
+    const RqLane L;
+    float* Bw0 = rq_smem + a.r * kRqCols + L.warp * 2 * 16 * a.rs;
 
+    const int64_t t_begin = (int64_t)blockIdx.x * a.tiles / gridDim.x;
+    const int64_t t_end = (int64_t)(blockIdx.x + 1) * a.tiles / gridDim.x;
+    // The dump variant (test hook) has no s_t: it writes merged values only.
+    const float amax = kDump ? 0.0f : *reinterpret_cast<volatile const float*>(a.s_t);
     const float s = __fdiv_rn(amax, kAmaxDiv);
     const float d = __fmul_rn(6.0f, s);
     const bool d_fast = fast_recip_ok(d);
     const float inv_d = d_fast ? recip_approx(d) : 0.0f;
+
+    int64_t staged = -1;
+    RqCursor cur;
+    cur.init(a, t_begin);
+    if (t_begin < t_end) rq_copy_b(a, L.lane, cur.n0() + L.wr * 16, Bw0);
+    int buf = 0;
+    for (int64_t t = t_begin; t < t_end; ++t) {
+        const int64_t n0 = cur.n0(), k0 = cur.k0();
+        if (cur.strip != staged) {
+            __syncthreads();
+            rq_stage_a(a, As, k0);
+            __syncthreads();
+            staged = cur.strip;
+        }
+        RqW<kWType> w;
+        w.load(a, L, n0, k0);
+        __syncwarp();
+        cur.next(a);
+        if (t + 1 < t_end)
+            rq_copy_b(a, L.lane, cur.n0() + L.wr * 16, Bw0 + (buf ^ 1) * 16 * a.rs);
+        else
+            rq_commit_empty();
+        rq_wait_b();
+        const float* Bw = Bw0 + buf * 16 * a.rs;
+        buf ^= 1;
+
+        // acc[i][p] holds columns 2p, 2p+1 of row i; fma.rn.f32x2 is an IEEE fma in
+        // each half, so every element follows the same chain as a scalar fmaf.
+        float2 acc[4][4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int64_t n = n0 + rg * 4 + i;
-        uint32_t sfc;
-        const uint32_t packed = quant_half_block(w[i], s, d, inv_d, d_fast, &sfc);
-        const uint32_t word = gather_sf_word(sfc);
-        if (col_ok) {
-            if (n < a.N)
-                *reinterpret_cast<uint32_t*>(a.codes + n * (a.K >> 1) + ((k0 + cg * 8) >> 1)) =
-                    packed;
-            if (n < a.rows_pad && (cg & 7) == 0)
-                *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(n, (k0 + cg * 8) >> 4, a.K)) =
-                    word;
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int p = 0; p < 4; ++p) acc[i][p] = make_float2(0.0f, 0.0f);
+        const float* ap = As + L.col();
+        const float* bq = Bw + L.rg * a.rs;
+        int j = 0;
+#pragma unroll 1
+        for (; j + 4 <= a.r; j += 4) {
+            float4 b4[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                b4[i] = *reinterpret_cast<const float4*>(bq + i * 4 * a.rs + j);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const float4 a0 = *reinterpret_cast<const float4*>(ap + (j + jj) * kRqCols);
+                const float4 a1 = *reinterpret_cast<const float4*>(ap + (j + jj) * kRqCols + 4);
+                const float2 av[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w),
+                                      make_float2(a1.x, a1.y), make_float2(a1.z, a1.w)};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float bv = jj == 0 ? b4[i].x : jj == 1 ? b4[i].y : jj == 2 ? b4[i].z : b4[i].w;
+                    const float2 bb = make_float2(bv, bv);
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) acc[i][p] = __ffma2_rn(bb, av[p], acc[i][p]);
+                }
+            }
+        }
+#pragma unroll 1
+        for (; j < a.r; ++j) {
+            const float4 a0 = *reinterpret_cast<const float4*>(ap + j * kRqCols);
+            const float4 a1 = *reinterpret_cast<const float4*>(ap + j * kRqCols + 4);
+            const float2 av[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w),
+                                  make_float2(a1.x, a1.y), make_float2(a1.z, a1.w)};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float bv = bq[i * 4 * a.rs + j];
+                const float2 bb = make_float2(bv, bv);
+#pragma unroll
+                for (int p = 0; p < 4; ++p) acc[i][p] = __ffma2_rn(bb, av[p], acc[i][p]);
+            }
+        }
+
+        const int64_t k = k0 + L.col();
+        const bool col_ok = k < a.K;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int64_t n = n0 + L.row(i);
+            float x[8];
+            w.row(i, x);
+            if (a.r > 0) {
+                const float2 cc = make_float2(a.c, a.c);
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    const float2 y = __ffma2_rn(cc, acc[i][p], make_float2(x[2 * p], x[2 * p + 1]));
+                    x[2 * p] = y.x;
+                    x[2 * p + 1] = y.y;
+                }
+            }
+            if (n >= a.N) {
+#pragma unroll
+                for (int q = 0; q < 8; ++q) x[q] = 0.0f;
+            }
+            if (kDump) {
+                if (col_ok && n < a.N) {
+                    float* p = a.dump + n * a.K + k;
+                    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
+                    *reinterpret_cast<float4*>(p + 4) = make_float4(x[4], x[5], x[6], x[7]);
+                }
+                continue;
+            }
+            uint32_t sfc;
+            const uint32_t packed = quant_half_block(x, s, d, inv_d, d_fast, &sfc);
+            const uint32_t word = gather_sf_word(sfc);
+            if (col_ok) {
+                if (n < a.N) *reinterpret_cast<uint32_t*>(a.codes + n * (a.K >> 1) + (k >> 1)) = packed;
+                if (n < a.rows_pad && L.cg == 0)
+                    *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(n, k >> 4, a.K)) = word;
+            }
         }
     }
+    asm volatile("cp.async.wait_group 0;" ::: "memory");
 }
 
 __global__ void requant_finalize_kernel(float* s_t) {
     if (threadIdx.x == 0 && blockIdx.x == 0) *s_t = __fdiv_rn(*s_t, kAmaxDiv);
 }
 
+template <typename Kern>
+cudaError_t rq_grid(const LaunchCtx& ctx, Kern kern, size_t smem, int64_t tiles, unsigned* grid) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRqThreads, smem);
+    if (e != cudaSuccess) return e;
+    const int64_t g = (int64_t)ctx.num_sms * (per_sm < 1 ? 1 : per_sm);
+    *grid = (unsigned)(tiles < g ? tiles : g);
+    return cudaSuccess;
+}
+
+RqArgs rq_args(const void* W, const float* A, const float* B, int r, float c, int64_t N, int64_t K,
+               uint8_t* codes, uint8_t* sf, float* s_t, float* dump) {
+    RqArgs a;
+    a.W = W;
+    a.A = A;
+    a.B = B;
+    a.r = r;
+    a.c = c;
+    a.N = N;
+    a.K = K;
+    a.rows_pad = (N + 127) / 128 * 128;
+    a.codes = codes;
+    a.sf = sf;
+    a.s_t = s_t;
+    a.dump = dump;
+    a.row_tiles = a.rows_pad / kRqRows;
+    a.tiles = a.row_tiles * ((K + kRqCols - 1) / kRqCols);
+    a.rs = rq_bstride(r);
+    a.inv_r = rq_inv_r(r);
+    a.b_vec = r > 0 && r % 4 == 0 && (reinterpret_cast<uintptr_t>(B) & 15u) == 0;
+    return a;
+}
+
 template <int kWType>
 cudaError_t run_requant(const LaunchCtx& ctx, const RqArgs& a) {
-    const dim3 grid((unsigned)((a.rows_pad + kRqRows - 1) / kRqRows),
-                    (unsigned)((a.K + kRqCols - 1) / kRqCols));
-    const size_t smem = (size_t)a.r * (kRqCols + kRqRows) * sizeof(float);
-    cudaError_t e = cudaFuncSetAttribute(requant_amax_kernel<kWType>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const size_t smem = rq_smem_bytes(a.r);
+    unsigned g1 = 0, g2 = 0;
+    cudaError_t e = rq_grid(ctx, requant_amax_kernel<kWType>, smem, a.tiles, &g1);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(requant_quant_kernel<kWType>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = rq_grid(ctx, requant_quant_kernel<kWType, false>, smem, a.tiles, &g2);
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(a.s_t, 0, sizeof(float), ctx.stream);
     if (e != cudaSuccess) return e;
-    requant_amax_kernel<kWType><<<grid, 256, smem, ctx.stream>>>(a);
+    requant_amax_kernel<kWType><<<g1, kRqThreads, smem, ctx.stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    requant_quant_kernel<kWType><<<grid, 256, smem, ctx.stream>>>(a);
+    requant_quant_kernel<kWType, false><<<g2, kRqThreads, smem, ctx.stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     requant_finalize_kernel<<<1, 32, 0, ctx.stream>>>(a.s_t);
+    return cudaGetLastError();
+}
+
+template <int kWType>
+cudaError_t run_merge_dump(const LaunchCtx& ctx, const RqArgs& a) {
+    const size_t smem = rq_smem_bytes(a.r);
+    unsigned g = 0;
+    cudaError_t e = rq_grid(ctx, requant_quant_kernel<kWType, true>, smem, a.tiles, &g);
+    if (e != cudaSuccess) return e;
+    requant_quant_kernel<kWType, true><<<g, kRqThreads, smem, ctx.stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -509,20 +893,16 @@ cudaError_t launch_act_quant(const LaunchCtx& ctx, const __nv_bfloat16* X, int64
 cudaError_t launch_requant(const LaunchCtx& ctx, const void* W, int w_dtype, const float* A,
                            const float* B, int r, float c, int64_t N, int64_t K, uint8_t* codes,
                            uint8_t* sf, float* s_t) {
-    RqArgs a;
-    a.W = W;
-    a.A = A;
-    a.B = B;
-    a.r = r;
-    a.c = c;
-    a.N = N;
-    a.K = K;
-    a.rows_pad = (N + 127) / 128 * 128;
-    a.codes = codes;
-    a.sf = sf;
-    a.s_t = s_t;
+    const RqArgs a = rq_args(W, A, B, r, c, N, K, codes, sf, s_t, nullptr);
     return w_dtype == NVFP4_W_BF16 ? run_requant<NVFP4_W_BF16>(ctx, a)
                                    : run_requant<NVFP4_W_FP32>(ctx, a);
+}
+
+cudaError_t launch_test_merge(const LaunchCtx& ctx, const void* W, int w_dtype, const float* A,
+                              const float* B, int r, float c, int64_t N, int64_t K, float* out) {
+    const RqArgs a = rq_args(W, A, B, r, c, N, K, nullptr, nullptr, nullptr, out);
+    return w_dtype == NVFP4_W_BF16 ? run_merge_dump<NVFP4_W_BF16>(ctx, a)
+                                   : run_merge_dump<NVFP4_W_FP32>(ctx, a);
 }
 
 cudaError_t launch_test_e2m1(const LaunchCtx& ctx, const float* q, uint8_t* codes, int64_t n) {

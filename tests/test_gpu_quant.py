@@ -174,3 +174,88 @@ def test_requant_repeated_calls_reset_amax(orc):
     nv.nvfp4_requant(W2.cuda(), codes=codes, sf=sf, s_t=s_t)
     _, _, os_ = orc.requant(W2.numpy(), None, None, 32.0)
     assert np_(s_t)[0] == os_[0]
+
+
+def _check_merge(orc, W, A, B, alpha):
+    """The GPU's merged weights (the values requant quantizes) against the
+    oracle's fma chain, bit for bit."""
+    got = np_(nv.nvfp4_test_merge(W.cuda(), None if A is None else A.cuda(),
+                                  None if B is None else B.cuda(), alpha))
+    Wn = workloads.bf16_bits(W) if W.dtype == torch.bfloat16 else W.numpy()
+    want = orc.merge(Wn, None if A is None else A.numpy(), None if B is None else B.numpy(), alpha)
+    bad = np.argwhere(got.view(np.uint32) != want.view(np.uint32))
+    assert bad.size == 0, f"{len(bad)} merged values differ, first at {bad[:3]}"
+
+
+@pytest.mark.parametrize("name", ["tiny", "sana", "flux_up"])
+def test_merge_configs_bit_exact(orc, name):
+    require_gpu()
+    cfg = workloads.LINEARS[name]
+    W = workloads.weight(cfg, seed=0)
+    A, B = workloads.lora(cfg, seed=0)
+    _check_merge(orc, W, A, B, workloads.LORA_ALPHA)
+
+
+@pytest.mark.parametrize("r", [0, 1, 7, 33, 64])
+@pytest.mark.parametrize("wdt", [torch.bfloat16, torch.float32])
+def test_merge_ranks_and_tails(orc, r, wdt):
+    """Ragged rows (200 = 3 row tiles + 8) and a half-width last strip (K = 320)."""
+    require_gpu()
+    g = torch.Generator().manual_seed(100 + r)
+    N, K = 200, 320
+    W = (torch.randn(N, K, generator=g) * 0.02).to(wdt)
+    A = torch.randn(r, K, generator=g) / 32 if r else None
+    B = torch.randn(N, r, generator=g) * 0.01 if r else None
+    _check_merge(orc, W, A, B, 3.0)
+
+
+def test_requant_amax_moved_by_lora(orc):
+    """The largest |W'| is not at the largest |W|: a rank-1 update lifts another
+    element of the same warp's rows above it, and, in a second case, one in a
+    different CTA's tile."""
+    require_gpu()
+    N, K = 256, 512
+    g = torch.Generator().manual_seed(21)
+    W = torch.randn(N, K, generator=g) * 0.01
+    W[5, 7] = 0.1
+    W[9, 3] = -0.099
+    A = torch.zeros(1, K)
+    B = torch.zeros(N, 1)
+    A[0, 3] = -0.005
+    B[9, 0] = 1.0
+    _check_requant(orc, W, A, B, 1.0)
+    W2 = W.clone()
+    W2[9, 3] = 0.0
+    W2[200, 400] = 0.0995
+    A2 = torch.zeros(1, K)
+    B2 = torch.zeros(N, 1)
+    A2[0, 400] = 0.001
+    B2[200, 0] = 1.0
+    _check_requant(orc, W2, A2, B2, 1.0)
+
+
+def test_requant_lora_dominated(orc):
+    """|B A| much larger than |W| everywhere (every element is a candidate for the
+    maximum), and W constant in magnitude with mixed signs."""
+    require_gpu()
+    g = torch.Generator().manual_seed(22)
+    N, K = 192, 256
+    W = torch.randn(N, K, generator=g) * 1e-6
+    A = torch.randn(32, K, generator=g)
+    B = torch.randn(N, 32, generator=g)
+    _check_requant(orc, W, A, B, 32.0)
+    Wc = torch.full((N, K), 0.05) * torch.sign(torch.randn(N, K, generator=g))
+    _check_requant(orc, Wc.to(torch.bfloat16), A / 32 * 0.01, B * 0.01, 32.0)
+
+
+def test_merge_subnormal_accumulator(orc):
+    """B A and W' in the fp32 subnormal range: the merge must not flush them."""
+    require_gpu()
+    g = torch.Generator().manual_seed(23)
+    N, K = 96, 192
+    W = torch.randn(N, K, generator=g) * 1e-39
+    A = torch.randn(32, K, generator=g) * 1e-20
+    B = torch.randn(N, 32, generator=g) * 1e-19
+    _check_merge(orc, W, A, B, 32.0)
+    _check_merge(orc, W * 0, A, B, 0.5)
+    _check_requant(orc, W, A, B, 32.0)
