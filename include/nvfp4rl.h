@@ -204,6 +204,10 @@ nvfp4_status nvfp4_test_e2m1(const float* q, uint8_t* codes, int64_t n, void* st
 /* codes[i] = RNE_E4M3_sat(v[i]) for v[i] >= 0. */
 nvfp4_status nvfp4_test_e4m3(const float* v, uint8_t* codes, int64_t n, void* stream);
 
+/* out[i] = the value of E4M3 code codes[i] (0 <= code <= 0x7E), as the
+ * quantizers decode a block scale before dividing by it. */
+nvfp4_status nvfp4_test_e4m3_decode(const uint8_t* codes, float* out, int64_t n, void* stream);
+
 /* codes[i] = RNE_E2M1_sat(fl32(x[i] / den[i])) for den[i] > 0, through the
  * quantizers' reciprocal fast path with its exact-division fallback. */
 nvfp4_status nvfp4_test_e2m1_quotient(const float* x, const float* den, uint8_t* codes,

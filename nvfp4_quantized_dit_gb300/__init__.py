@@ -22,7 +22,7 @@ __all__ = [
     "nvfp4_requant", "nvfp4_act_quant", "nvfp4_gemm", "bf16_gemm", "select_contrastive",
     "nvfp4_device_status", "nvfp4_status_string", "nvfp4_version",
     "nvfp4_test_e2m1", "nvfp4_test_e4m3", "nvfp4_test_e2m1_quotient", "nvfp4_test_e4m3_quotient",
-    "nvfp4_test_merge", "nvfp4_test_wait_timeout",
+    "nvfp4_test_e4m3_decode", "nvfp4_test_merge", "nvfp4_test_wait_timeout",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnvfp4rl.so")
@@ -62,6 +62,7 @@ def library() -> ctypes.CDLL:
                 "nvfp4_test_e4m3": [P, P, I64, P],
                 "nvfp4_test_e2m1_quotient": [P, P, P, I64, P],
                 "nvfp4_test_e4m3_quotient": [P, P, P, I64, P],
+                "nvfp4_test_e4m3_decode": [P, P, I64, P],
                 "nvfp4_test_merge": [P, I, P, P, I, F, I64, I64, P, P],
                 "nvfp4_test_wait_timeout": [I64, P],
             }
@@ -221,6 +222,13 @@ def nvfp4_test_e4m3(v, out=None, stream=None):
     out = torch.empty(v.numel(), dtype=torch.uint8, device=v.device) if out is None else out
     _call("nvfp4_test_e4m3", _dev(v, "v", torch.float32), _dev(out, "codes", torch.uint8), v.numel(),
           _stream(stream))
+    return out
+
+
+def nvfp4_test_e4m3_decode(codes, out=None, stream=None):
+    out = torch.empty(codes.numel(), dtype=torch.float32, device=codes.device) if out is None else out
+    _call("nvfp4_test_e4m3_decode", _dev(codes, "codes", torch.uint8), _dev(out, "out", torch.float32),
+          codes.numel(), _stream(stream))
     return out
 
 

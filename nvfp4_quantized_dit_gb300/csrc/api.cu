@@ -286,6 +286,16 @@ nvfp4_status nvfp4_test_e4m3(const float* v, uint8_t* codes, int64_t n, void* st
     return st != NVFP4_OK ? st : from_cuda(launch_test_e4m3(ctx, v, codes, n));
 }
 
+nvfp4_status nvfp4_test_e4m3_decode(const uint8_t* codes, float* out, int64_t n, void* stream) {
+    if (n < 0) return NVFP4_ERR_SHAPE;
+    if (n == 0) return NVFP4_OK;
+    if (!codes || !out) return NVFP4_ERR_NULL;
+    if (misaligned(out, 4)) return NVFP4_ERR_ALIGN;
+    LaunchCtx ctx;
+    nvfp4_status st = resolve(stream, &ctx);
+    return st != NVFP4_OK ? st : from_cuda(launch_test_e4m3_decode(ctx, codes, out, n));
+}
+
 nvfp4_status nvfp4_test_e2m1_quotient(const float* x, const float* den, uint8_t* codes, int64_t n,
                                       void* stream) {
     if (n < 0) return NVFP4_ERR_SHAPE;

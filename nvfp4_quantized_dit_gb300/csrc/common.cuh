@@ -7,6 +7,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -34,6 +35,7 @@ cudaError_t launch_select(const LaunchCtx&, const float* rewards, int P, int N, 
                           int global_std, int32_t* idx, float* r_out);
 cudaError_t launch_test_e2m1(const LaunchCtx&, const float* q, uint8_t* codes, int64_t n);
 cudaError_t launch_test_e4m3(const LaunchCtx&, const float* v, uint8_t* codes, int64_t n);
+cudaError_t launch_test_e4m3_decode(const LaunchCtx&, const uint8_t* codes, float* out, int64_t n);
 cudaError_t launch_test_e2m1_quotient(const LaunchCtx&, const float* x, const float* den,
                                       uint8_t* codes, int64_t n);
 cudaError_t launch_test_e4m3_quotient(const LaunchCtx&, const float* v, const float* d,
@@ -85,11 +87,14 @@ __device__ __forceinline__ uint32_t cvt_e4m3(float v) {
     return (uint32_t)out & 0xFFu;
 }
 
-// Value of a non-negative E4M3 code: exponent bits 6..3 (bias 7), mantissa 2..0.
+// Value of a non-negative E4M3 code, by the hardware conversion E4M3 -> f16 (every
+// E4M3 value is an f16 value) and f16 -> f32 (exact).
 __device__ __forceinline__ float e4m3_value(uint32_t code) {
-    const uint32_t e = (code >> 3) & 15u, m = code & 7u;
-    if (e == 0) return (float)m * 0.001953125f;           // m * 2^-9 (subnormal), exact
-    return __uint_as_float(((e + 120u) << 23) | (m << 20)); // (1 + m/8) * 2^(e-7)
+    uint32_t h2;
+    const unsigned short c = (unsigned short)(code & 0xFFu);
+    // cvt ...f16x2.e4m3x2 d, a: the low byte of a lands in the low half of d.
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(c));
+    return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
 }
 
 // True when the fp32 value with bit pattern u lies within 16 ulps of a number with
@@ -97,10 +102,16 @@ __device__ __forceinline__ float e4m3_value(uint32_t code) {
 // bits are within 16 of 0 modulo 2^kLowBits.  Every E2M1 rounding boundary (0.25,
 // 0.75, 1.25, 1.75, 2.5, 3.5, 5) has 3 significant bits (kLowBits = 20); every E4M3
 // boundary (midpoints of adjacent codes) has at most 5 (kLowBits = 18).
+//
+// Written as one shift-add and one compare: shifting out the top 32 - kLowBits bits
+// leaves ((u + 16) mod 2^kLowBits) * 2^(32 - kLowBits).
+template <int kLowBits>
+__device__ __forceinline__ uint32_t near_key(uint32_t u) {
+    return (u << (32 - kLowBits)) + (16u << (32 - kLowBits));
+}
 template <int kLowBits>
 __device__ __forceinline__ bool near_boundary(uint32_t u) {
-    constexpr uint32_t mask = (1u << kLowBits) - 1u;
-    return ((u + 16u) & mask) < 32u;
+    return near_key<kLowBits>(u) < (32u << (32 - kLowBits));
 }
 
 // Approximate reciprocal, at most 1 ulp from 1/d for normal d whose reciprocal is
@@ -146,10 +157,11 @@ __device__ __forceinline__ uint32_t e2m1_quotient8(const float (&x)[8], float de
     F8 q;
 #pragma unroll
     for (int i = 0; i < 8; ++i) q.v[i] = __fmul_rn(x[i], r);
-    bool any = !fast_ok;
+    // Any of the 8 near a boundary <=> the smallest key is.
+    uint32_t kmin = near_key<20>(__float_as_uint(q.v[0]));
 #pragma unroll
-    for (int i = 0; i < 8; ++i) any |= near_boundary<20>(__float_as_uint(q.v[i]));
-    if (any) {
+    for (int i = 1; i < 8; ++i) kmin = min(kmin, near_key<20>(__float_as_uint(q.v[i])));
+    if (!fast_ok || kmin < (32u << 12)) {
         F8 xv;
 #pragma unroll
         for (int i = 0; i < 8; ++i) xv.v[i] = x[i];

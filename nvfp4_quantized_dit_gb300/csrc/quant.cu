@@ -269,18 +269,26 @@ cudaError_t run_act_quant(const LaunchCtx& ctx, const __nv_bfloat16* X, int64_t 
 // Both kernels walk the same tiles: kRqRows x kRqCols pieces of W in strip-major
 // order (a strip is kRqCols columns), each CTA a contiguous run of tiles, so a CTA
 // stages the r x kRqCols strip of A in shared memory about once.  Warp w owns rows
-// 16 (w / 2) .. +15 and columns 64 (w % 2) .. +63 of a tile; lane l owns the 4 rows
-// 4 i + l / 8 (i = 0..3) of that block and the 8 columns 8 (l % 8) .. +7, so the
-// 16-element scale block of a row lives in lanes l, l ^ 1 and one scale word (4
-// blocks) in 8 consecutive lanes.  Each warp copies the 16 rows of B it needs into
-// its own double-buffered slice of shared memory, one tile ahead (row stride rs = r
-// rounded up to 8, plus 4, which keeps the four rows a load instruction touches on
-// distinct banks).
+// 16 (w / 2) .. +15 and columns 64 (w % 2) .. +63 of a tile; lane l owns the 4
+// consecutive rows 4 (l / 8) .. +3 of that block and the 8 columns 8 (l % 8) .. +7,
+// so the 16-element scale block of a row lives in lanes l, l ^ 1 and one scale word
+// (4 blocks) in 8 consecutive lanes.
+//
+// Shared memory holds the operands of the packed fp32 fma (fma.rn.f32x2, an IEEE fma
+// in each half) in the pairs it consumes, so that no register moves are needed:
+//   As2  A strip, each value twice: piece t of lane group g (4 floats) holds columns
+//        8 g + 2 t and 8 g + 2 t + 1 of its 64, as {a, a, a', a'}; the 8 pieces a load
+//        instruction touches (one per g) are contiguous (no bank conflicts).
+//   Bs   per warp, double-buffered one tile ahead: its 16 rows of B as copied
+//        (row-major, row stride rs = r rounded up to 4, plus 4);
+//   Bt   per warp (pass 2): the same rows transposed, Bt[j][row] with a stride of
+//        20 floats per j, so one 16-byte load gives a lane its 4 rows at step j.
 constexpr int kRqRows = 64;
 constexpr int kRqCols = 128;
 constexpr int kRqThreads = 256;
 constexpr int kRqWarps = kRqThreads / 32;
 constexpr int kRqMaxR = 64;
+constexpr int kRqA2 = 2 * kRqCols;  // floats per row of As2
 
 struct RqArgs {
     const void* W;
@@ -293,13 +301,16 @@ struct RqArgs {
     uint8_t* sf;
     float* s_t;
     float* dump;  // test hook: merged values instead of codes
-    int64_t row_tiles, tiles;
-    int rs;     // row stride of B in shared memory (floats)
+    int64_t row_tiles, tiles;    // pass 1: kRqRows-row tiles
+    int64_t row_tiles2, tiles2;  // pass 2: kQRows-row tiles
+    int rs;     // row stride of Bs (floats)
     int inv_r;  // ceil(2^16 / r): x / r == (x * inv_r) >> 16 for 0 <= x < 16 r
     int b_vec;  // B 16-byte aligned and r % 4 == 0: 16-byte copies
 };
 
-__host__ __device__ constexpr int rq_bstride(int r) { return ((r + 7) & ~7) + 4; }
+constexpr int kRqBtStride = 20;
+
+__host__ __device__ constexpr int rq_bstride(int r) { return ((r + 3) & ~3) + 4; }
 
 __host__ __device__ constexpr int rq_inv_r(int r) { return r > 0 ? (65536 + r - 1) / r : 0; }
 
@@ -312,8 +323,13 @@ constexpr bool rq_inv_r_exact() {
 }
 static_assert(rq_inv_r_exact(), "x * ceil(2^16 / r) >> 16 must equal x / r for x < 16 r");
 
+// Per warp: Bs double buffer, then Bt (rows of j rounded up to 8).
+__host__ __device__ constexpr int rq_warp_floats(int r) {
+    return 2 * 16 * rq_bstride(r) + ((r + 7) & ~7) * kRqBtStride;
+}
+
 __host__ __device__ inline size_t rq_smem_bytes(int r) {
-    return ((size_t)r * kRqCols + (size_t)kRqWarps * 2 * 16 * rq_bstride(r)) * sizeof(float);
+    return ((size_t)r * kRqA2 + (size_t)kRqWarps * rq_warp_floats(r)) * sizeof(float);
 }
 
 struct RqLane {
@@ -327,42 +343,55 @@ struct RqLane {
         rg = lane >> 3;
     }
     // Tile-local row of this lane's row i, and the warp-slice row of B it reads.
-    __device__ __forceinline__ int row(int i) const { return wr * 16 + i * 4 + rg; }
-    __device__ __forceinline__ int brow(int i) const { return i * 4 + rg; }
+    __device__ __forceinline__ int row(int i) const { return wr * 16 + rg * 4 + i; }
+    __device__ __forceinline__ int brow(int i) const { return rg * 4 + i; }
     __device__ __forceinline__ int col() const { return wc * 64 + cg * 8; }
 };
 
-// Position in the strip-major tile order, advanced one tile at a time.
+// Float index within an As2 row of column q (0..7) of lane group g in col-warp wc.
+__device__ __forceinline__ int rq_a2_index(int wc, int g, int q) {
+    return wc * 128 + ((q >> 1) * 8 + g) * 4 + 2 * (q & 1);
+}
+
+// Position in the strip-major tile order (tiles of `rows` rows, row_tiles per
+// strip), advanced one tile at a time.
 struct RqCursor {
-    int64_t strip, rt;
-    __device__ __forceinline__ void init(const RqArgs& a, int64_t t) {
-        strip = t / a.row_tiles;
-        rt = t - strip * a.row_tiles;
+    int64_t strip, rt, row_tiles;
+    int rows;
+    __device__ __forceinline__ void init(int64_t row_tiles_, int rows_, int64_t t) {
+        row_tiles = row_tiles_;
+        rows = rows_;
+        strip = t / row_tiles;
+        rt = t - strip * row_tiles;
     }
-    __device__ __forceinline__ void next(const RqArgs& a) {
-        if (++rt == a.row_tiles) {
+    __device__ __forceinline__ void next() {
+        if (++rt == row_tiles) {
             rt = 0;
             ++strip;
         }
     }
-    __device__ __forceinline__ int64_t n0() const { return rt * kRqRows; }
+    __device__ __forceinline__ int64_t n0() const { return rt * rows; }
     __device__ __forceinline__ int64_t k0() const { return strip * kRqCols; }
 };
 
-// A[:, k0:k0+kRqCols] -> As[j][col], zero past K.  Called by the whole CTA.
-__device__ __forceinline__ void rq_stage_a(const RqArgs& a, float* As, int64_t k0) {
-    for (int e = threadIdx.x; e < a.r * (kRqCols / 4); e += kRqThreads) {
-        const int j = e / (kRqCols / 4), c4 = e % (kRqCols / 4);
-        const int64_t k = k0 + c4 * 4;
-        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (k < a.K) v = *reinterpret_cast<const float4*>(a.A + (int64_t)j * a.K + k);
-        *reinterpret_cast<float4*>(As + j * kRqCols + c4 * 4) = v;
+// A[:, k0:k0+kRqCols] -> As2 (zero past K).  Called by the whole CTA.
+__device__ __forceinline__ void rq_stage_a(const RqArgs& a, float* As2, int64_t k0) {
+    // Thread e: row j, columns 8 g + 2 t, +1 of col-warp wc (one 4-float piece).
+    for (int e = threadIdx.x; e < a.r * (kRqCols / 2); e += kRqThreads) {
+        const int j = e / (kRqCols / 2), pc = e % (kRqCols / 2);
+        const int wc = pc >> 5, g = (pc >> 2) & 7, t = pc & 3;
+        const int64_t k = k0 + wc * 64 + g * 8 + 2 * t;
+        float2 v = make_float2(0.f, 0.f);
+        if (k < a.K) v = *reinterpret_cast<const float2*>(a.A + (int64_t)j * a.K + k);
+        *reinterpret_cast<float4*>(As2 + j * kRqA2 + wc * 128 + (t * 8 + g) * 4) =
+            make_float4(v.x, v.x, v.y, v.y);
     }
 }
 
 // Asynchronous copies of B[row0 : row0+16, :] (the warp's rows; rows past N are
-// zero-filled) into the warp's slice Bw with row stride rs.  One commit group.
-__device__ __forceinline__ void rq_copy_b(const RqArgs& a, int lane, int64_t row0, float* Bw) {
+// zero-filled) into Bs with row stride rs: 16-byte pieces when B allows, else 4-byte
+// ones.  One commit group.
+__device__ __forceinline__ void rq_copy_b(const RqArgs& a, int lane, int64_t row0, float* Bs) {
     if (a.b_vec) {
         for (int c = lane; c < 4 * a.r; c += 32) {
             const int x = 4 * c;
@@ -370,7 +399,7 @@ __device__ __forceinline__ void rq_copy_b(const RqArgs& a, int lane, int64_t row
             const bool valid = row0 + rl < a.N;
             const float* src = a.B + (valid ? (row0 + rl) * a.r + j : 0);
             asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
-                             smem_u32(Bw + rl * a.rs + j)),
+                             smem_u32(Bs + rl * a.rs + j)),
                          "l"(src), "r"(valid ? 16 : 0)
                          : "memory");
         }
@@ -380,12 +409,26 @@ __device__ __forceinline__ void rq_copy_b(const RqArgs& a, int lane, int64_t row
             const bool valid = row0 + rl < a.N;
             const float* src = a.B + (valid ? (row0 + rl) * a.r + j : 0);
             asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
-                             smem_u32(Bw + rl * a.rs + j)),
+                             smem_u32(Bs + rl * a.rs + j)),
                          "l"(src), "r"(valid ? 4 : 0)
                          : "memory");
         }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+// Bs (row-major) -> Bt[j][row].  Lane l moves row l % 16, steps j = 8 t + 4 (l / 16)
+// .. +3: one 16-byte load and four 4-byte stores, the stores of a warp instruction
+// covering 32 distinct banks.  Entries past r hold copies of the row padding.
+__device__ __forceinline__ void rq_transpose_b(const RqArgs& a, int lane, const float* Bs, float* Bt) {
+    const int rl = lane & 15, jq = (lane >> 4) * 4;
+    for (int j4 = jq; j4 < a.r; j4 += 8) {
+        const float4 v = *reinterpret_cast<const float4*>(Bs + rl * a.rs + j4);
+        Bt[(j4 + 0) * kRqBtStride + rl] = v.x;
+        Bt[(j4 + 1) * kRqBtStride + rl] = v.y;
+        Bt[(j4 + 2) * kRqBtStride + rl] = v.z;
+        Bt[(j4 + 3) * kRqBtStride + rl] = v.w;
+    }
 }
 
 __device__ __forceinline__ void rq_commit_empty() { asm volatile("cp.async.commit_group;" ::: "memory"); }
@@ -403,12 +446,13 @@ struct RqW {
     static constexpr int kWords = kWType == NVFP4_W_BF16 ? 1 : 2;
     uint4 v[4][kWords];
 
+    template <bool kEdge>
     __device__ __forceinline__ void load(const RqArgs& a, const RqLane& L, int64_t n0, int64_t k0) {
         const int64_t k = k0 + L.col();
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int64_t n = n0 + L.row(i);
-            const bool ok = n < a.N && k < a.K;
+            const bool ok = !kEdge || (n < a.N && k < a.K);
 #pragma unroll
             for (int w = 0; w < kWords; ++w) {
                 if (ok) {
@@ -503,12 +547,13 @@ struct RqW {
 
 // The merged value of one element, in the library's order: acc = +0;
 // acc = fma(B[n,j], A[j,k], acc) for j = 0..r-1; w' = fma(c, acc, W) (w' = W when r = 0).
+// brow walks a row of Bs, acol a column of As2 (stride kRqA2).
 __device__ __forceinline__ float rq_merge_one(const RqArgs& a, const float* brow, const float* acol,
                                               float w) {
     if (a.r == 0) return w;
     float acc = 0.0f;
 #pragma unroll 4
-    for (int j = 0; j < a.r; ++j) acc = __fmaf_rn(brow[j], acol[j * kRqCols], acc);
+    for (int j = 0; j < a.r; ++j) acc = __fmaf_rn(brow[j], acol[j * kRqA2], acc);
     return __fmaf_rn(a.c, acc, w);
 }
 
@@ -539,9 +584,9 @@ __device__ __forceinline__ float rq_tau(float L, float D) {
 template <int kWType>
 __global__ void __launch_bounds__(kRqThreads, 2) requant_amax_kernel(RqArgs a) {
     extern __shared__ __align__(16) float rq_smem[];
-    float* As = rq_smem;
+    float* As2 = rq_smem;
     const RqLane L;
-    float* Bw0 = rq_smem + a.r * kRqCols + L.warp * 2 * 16 * a.rs;
+    float* Bs0 = rq_smem + a.r * kRqA2 + L.warp * rq_warp_floats(a.r);
 
     const int64_t t_begin = (int64_t)blockIdx.x * a.tiles / gridDim.x;
     const int64_t t_end = (int64_t)(blockIdx.x + 1) * a.tiles / gridDim.x;
@@ -551,41 +596,43 @@ __global__ void __launch_bounds__(kRqThreads, 2) requant_amax_kernel(RqArgs a) {
     float Lw = 0.0f;        // warp-uniform: largest exact |W'| seen
     RqW<kWType> wcur, wnext;
     RqCursor cur;
-    cur.init(a, t_begin);
+    cur.init(a.row_tiles, kRqRows, t_begin);
     if (t_begin < t_end) {
-        wcur.load(a, L, cur.n0(), cur.k0());
-        rq_copy_b(a, L.lane, cur.n0() + L.wr * 16, Bw0);
+        wcur.template load<true>(a, L, cur.n0(), cur.k0());
+        if (a.r > 0) rq_copy_b(a, L.lane, cur.n0() + L.wr * 16, Bs0);
     }
     int buf = 0;
     for (int64_t t = t_begin; t < t_end; ++t) {
         const int64_t n0 = cur.n0(), k0 = cur.k0();
         if (cur.strip != staged) {
             __syncthreads();
-            rq_stage_a(a, As, k0);
+            rq_stage_a(a, As2, k0);
             __syncthreads();
             staged = cur.strip;
             // Column norms: lane l covers columns 2l, 2l+1 of the warp's 64.
             float m = 0.0f;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
-                const float* acol = As + L.wc * 64 + 2 * L.lane + h;
+                const int cl = 2 * L.lane + h;
+                const float* acol = As2 + rq_a2_index(L.wc, cl >> 3, cl & 7);
                 float s2 = 0.0f;
 #pragma unroll 4
-                for (int j = 0; j < a.r; ++j) s2 = __fmaf_rn(acol[j * kRqCols], acol[j * kRqCols], s2);
+                for (int j = 0; j < a.r; ++j) s2 = __fmaf_rn(acol[j * kRqA2], acol[j * kRqA2], s2);
                 m = fmaxf(m, rq_norm_ub(s2));
             }
             amax_col = warp_max(m);
         }
         __syncwarp();
-        cur.next(a);
+        cur.next();
         if (t + 1 < t_end) {
-            wnext.load(a, L, cur.n0(), cur.k0());
-            rq_copy_b(a, L.lane, cur.n0() + L.wr * 16, Bw0 + (buf ^ 1) * 16 * a.rs);
+            wnext.template load<true>(a, L, cur.n0(), cur.k0());
+            if (a.r > 0) rq_copy_b(a, L.lane, cur.n0() + L.wr * 16, Bs0 + (buf ^ 1) * 16 * a.rs);
+            else rq_commit_empty();
         } else {
             rq_commit_empty();
         }
         rq_wait_b();
-        const float* Bw = Bw0 + buf * 16 * a.rs;
+        const float* Bs = Bs0 + buf * 16 * a.rs;
         buf ^= 1;
 
         const bool col_ok = k0 + L.col() < a.K;
@@ -599,7 +646,7 @@ __global__ void __launch_bounds__(kRqThreads, 2) requant_amax_kernel(RqArgs a) {
         if (a.r > 0) {
             // Row norms: lanes 2m, 2m+1 share row m of the warp's 16 (halves of j).
             float s2 = 0.0f;
-            const float* brow = Bw + (L.lane >> 1) * a.rs;
+            const float* brow = Bs + (L.lane >> 1) * a.rs;
 #pragma unroll 4
             for (int j = L.lane & 1; j < a.r; j += 2) s2 = __fmaf_rn(brow[j], brow[j], s2);
             s2 += __shfl_xor_sync(kFull, s2, 1);  // two sums >= 0: one more rounding
@@ -615,8 +662,8 @@ __global__ void __launch_bounds__(kRqThreads, 2) requant_amax_kernel(RqArgs a) {
             float v = 0.0f;
             if (L.lane == __ffs(holders) - 1) {
                 seed = __ffs(wcur.mask_ge(rows_ok, m)) - 1;
-                v = fabsf(rq_merge_one(a, Bw + L.brow(seed >> 3) * a.rs, As + L.col() + (seed & 7),
-                                       wcur.at(seed)));
+                v = fabsf(rq_merge_one(a, Bs + L.brow(seed >> 3) * a.rs,
+                                       As2 + rq_a2_index(L.wc, L.cg, seed & 7), wcur.at(seed)));
             }
             Lw = fmaxf(Lw, warp_max(v));
             // Then every element that could still exceed L, one merge call site.
@@ -627,8 +674,8 @@ __global__ void __launch_bounds__(kRqThreads, 2) requant_amax_kernel(RqArgs a) {
             while (cand) {
                 const int e = __ffs(cand) - 1;
                 cand &= cand - 1;
-                lm = fmaxf(lm, fabsf(rq_merge_one(a, Bw + L.brow(e >> 3) * a.rs, As + L.col() + (e & 7),
-                                                  wcur.at(e))));
+                lm = fmaxf(lm, fabsf(rq_merge_one(a, Bs + L.brow(e >> 3) * a.rs,
+                                                  As2 + rq_a2_index(L.wc, L.cg, e & 7), wcur.at(e))));
             }
             Lw = fmaxf(Lw, warp_max(lm));
         }
@@ -640,72 +687,195 @@ __global__ void __launch_bounds__(kRqThreads, 2) requant_amax_kernel(RqArgs a) {
 }
 
 // ---- pass 2: merge every element once and quantize it.
+//
+// The merge is bound by how fast shared memory hands operands to the FMA pipe (a
+// lane receives 4 bytes per shared-memory wavefront), so each lane keeps an 8 x 8
+// block of accumulators: 16 operands per step j for 64 fmas.  Tiles are
+// kQRows x kRqCols; warp w owns rows 32 (w / 2) .. +31 and columns 64 (w % 2) .. +63,
+// lane l the rows 8 (l / 8) .. +7 and columns 8 (l % 8) .. +7 of that block.
+// Shared memory:
+//   As   the A strip, As[j][col] (staged by the whole CTA when the strip changes);
+//   Bt   per pair of warps sharing rows, double-buffered one tile ahead: their 32
+//        rows of B transposed, element (j, row) at 32 j + (row ^ (j % 32)).  Each
+//        copy instruction moves one row (lane = j, a coalesced 128-byte read) into
+//        32 distinct banks; a 16-byte load at 32 j + (4 m ^ (j & 28)) returns rows
+//        4 m .. 4 m + 3 in the order e ^ (j & 3);
+//   Ws   per warp: its 32 x 64 block of W, copied when the tile starts and read by
+//        the epilogue, so its latency hides behind the merge.
+constexpr int kQRows = 128;
+
+template <int kWType>
+struct Rq2Geom {
+    static constexpr int kWBytes = kWType == NVFP4_W_BF16 ? 2 : 4;
+    static constexpr int kWsFloats = 32 * 64 * kWBytes / 4;  // per warp
+};
+
+template <int kWType>
+__host__ __device__ inline size_t rq2_smem_bytes(int r) {
+    return ((size_t)r * kRqCols + 4 * 2 * (size_t)r * 32 + (size_t)kRqWarps * Rq2Geom<kWType>::kWsFloats) *
+           sizeof(float);
+}
+
+struct RqScale {
+    float s, d, inv_d;
+    bool d_fast;
+};
+
+// Copies this warp's half (16 rows) of the pair's 32 rows of B, starting at pair row
+// 16 h, transposed into Bt.  Lane j copies B[row][j] (and B[row][j + 32] for r > 32).
+__device__ __forceinline__ void rq2_copy_b(const RqArgs& a, int lane, int64_t pair_row0, int h,
+                                           float* Bt) {
+    for (int rr = 16 * h; rr < 16 * h + 16; ++rr) {
+        const int64_t n = pair_row0 + rr;
+        const bool valid = n < a.N;
+        for (int j = lane; j < a.r; j += 32) {
+            const float* src = a.B + (valid ? n * a.r + j : 0);
+            asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(
+                             smem_u32(Bt + j * 32 + (rr ^ (j & 31)))),
+                         "l"(src), "r"(valid ? 4 : 0)
+                         : "memory");
+        }
+    }
+}
+
+// Copies the warp's 32 x 64 block of W (rows n0w.., columns k0w..; zero outside W)
+// into Ws, row-major with 64 * kWBytes bytes per row.
+template <int kWType>
+__device__ __forceinline__ void rq2_copy_w(const RqArgs& a, int lane, int64_t n0w, int64_t k0w,
+                                           float* Ws) {
+    constexpr int kChunksPerRow = 64 * Rq2Geom<kWType>::kWBytes / 16;
+    for (int c = lane; c < 32 * kChunksPerRow; c += 32) {
+        const int row = c / kChunksPerRow, pc = c % kChunksPerRow;
+        const int64_t n = n0w + row;
+        const int64_t k = k0w + pc * (16 / Rq2Geom<kWType>::kWBytes);
+        const bool valid = n < a.N && k < a.K;
+        const char* src = static_cast<const char*>(a.W) +
+                          (valid ? (n * a.K + k) * Rq2Geom<kWType>::kWBytes : 0);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                         smem_u32(reinterpret_cast<char*>(Ws) + c * 16)),
+                     "l"(src), "r"(valid ? 16 : 0)
+                     : "memory");
+    }
+}
+
+template <int kWType>
+__device__ __forceinline__ void rq2_w_row(const float* Ws, int row, int cg, float (&x)[8]) {
+    if (kWType == NVFP4_W_BF16) {
+        const uint4 v = *reinterpret_cast<const uint4*>(reinterpret_cast<const char*>(Ws) + row * 128 + cg * 16);
+        unpack8(v, x);
+    } else {
+        const float4 v0 = *reinterpret_cast<const float4*>(Ws + row * 64 + cg * 8);
+        const float4 v1 = *reinterpret_cast<const float4*>(Ws + row * 64 + cg * 8 + 4);
+        x[0] = v0.x; x[1] = v0.y; x[2] = v0.z; x[3] = v0.w;
+        x[4] = v1.x; x[5] = v1.y; x[6] = v1.z; x[7] = v1.w;
+    }
+}
+
+// One merged row (8 columns) -> codes (at cp) and its scale word (at sp, written by
+// lane group 0 of the word), or the merged values (kDump, at dp).
+template <bool kEdge, bool kDump>
+__device__ __forceinline__ void rq2_emit_row(const RqScale& sc, int cg, bool row_ok, bool col_ok,
+                                             uint8_t* cp, uint8_t* sp, float* dp, float (&x)[8]) {
+    if (kDump) {
+        if (col_ok && row_ok) {
+            *reinterpret_cast<float4*>(dp) = make_float4(x[0], x[1], x[2], x[3]);
+            *reinterpret_cast<float4*>(dp + 4) = make_float4(x[4], x[5], x[6], x[7]);
+        }
+        return;
+    }
+    uint32_t sfc;
+    const uint32_t packed = quant_half_block(x, sc.s, sc.d, sc.inv_d, sc.d_fast, &sfc);
+    const uint32_t word = gather_sf_word(sfc);
+    if (!kEdge || col_ok) {
+        if (!kEdge || row_ok) *reinterpret_cast<uint32_t*>(cp) = packed;
+        if (cg == 0) *reinterpret_cast<uint32_t*>(sp) = word;
+    }
+}
+
 template <int kWType, bool kDump>
 __global__ void __launch_bounds__(kRqThreads, 2) requant_quant_kernel(RqArgs a) {
     extern __shared__ __align__(16) float rq_smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int wr = warp >> 1, wc = warp & 1, rg = lane >> 3, cg = lane & 7;
     float* As = rq_smem;
-    const RqLane L;
-    float* Bw0 = rq_smem + a.r * kRqCols + L.warp * 2 * 16 * a.rs;
+    float* Bt0 = As + a.r * kRqCols + wr * 2 * a.r * 32;
+    float* Ws = As + a.r * kRqCols + 4 * 2 * a.r * 32 + warp * Rq2Geom<kWType>::kWsFloats;
 
-    const int64_t t_begin = (int64_t)blockIdx.x * a.tiles / gridDim.x;
-    const int64_t t_end = (int64_t)(blockIdx.x + 1) * a.tiles / gridDim.x;
+    const int64_t t_begin = (int64_t)blockIdx.x * a.tiles2 / gridDim.x;
+    const int64_t t_end = (int64_t)(blockIdx.x + 1) * a.tiles2 / gridDim.x;
+    RqScale sc;
     // The dump variant (test hook) has no s_t: it writes merged values only.
     const float amax = kDump ? 0.0f : *reinterpret_cast<volatile const float*>(a.s_t);
-    const float s = __fdiv_rn(amax, kAmaxDiv);
-    const float d = __fmul_rn(6.0f, s);
-    const bool d_fast = fast_recip_ok(d);
-    const float inv_d = d_fast ? recip_approx(d) : 0.0f;
+    sc.s = __fdiv_rn(amax, kAmaxDiv);
+    sc.d = __fmul_rn(6.0f, sc.s);
+    sc.d_fast = fast_recip_ok(sc.d);
+    sc.inv_d = sc.d_fast ? recip_approx(sc.d) : 0.0f;
+    const float2 cc = make_float2(a.c, a.c);
+    const int pair_bar = 1 + wr;  // named barrier of the two warps sharing rows
 
     int64_t staged = -1;
     RqCursor cur;
-    cur.init(a, t_begin);
-    if (t_begin < t_end) rq_copy_b(a, L.lane, cur.n0() + L.wr * 16, Bw0);
+    cur.init(a.row_tiles2, kQRows, t_begin);
+    if (t_begin < t_end && a.r > 0) rq2_copy_b(a, lane, cur.n0() + wr * 32, wc, Bt0);
+    asm volatile("cp.async.commit_group;" ::: "memory");
     int buf = 0;
     for (int64_t t = t_begin; t < t_end; ++t) {
         const int64_t n0 = cur.n0(), k0 = cur.k0();
+        const bool edge = n0 + kQRows > a.N || k0 + kRqCols > a.K;  // CTA-uniform
         if (cur.strip != staged) {
             __syncthreads();
-            rq_stage_a(a, As, k0);
+            for (int e = threadIdx.x; e < a.r * (kRqCols / 4); e += kRqThreads) {
+                const int j = e / (kRqCols / 4), c4 = e % (kRqCols / 4);
+                const int64_t k = k0 + c4 * 4;
+                float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+                if (k < a.K) v = *reinterpret_cast<const float4*>(a.A + (int64_t)j * a.K + k);
+                *reinterpret_cast<float4*>(As + j * kRqCols + c4 * 4) = v;
+            }
             __syncthreads();
             staged = cur.strip;
         }
-        RqW<kWType> w;
-        w.load(a, L, n0, k0);
+        // This tile's W block, then the next tile's B rows (both asynchronous).
         __syncwarp();
-        cur.next(a);
-        if (t + 1 < t_end)
-            rq_copy_b(a, L.lane, cur.n0() + L.wr * 16, Bw0 + (buf ^ 1) * 16 * a.rs);
-        else
-            rq_commit_empty();
-        rq_wait_b();
-        const float* Bw = Bw0 + buf * 16 * a.rs;
+        rq2_copy_w<kWType>(a, lane, n0 + wr * 32, k0 + wc * 64, Ws);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        cur.next();
+        // The pair's other buffer was last read in the previous tile's merge.
+        named_barrier_sync(pair_bar, 64);
+        if (t + 1 < t_end && a.r > 0)
+            rq2_copy_b(a, lane, cur.n0() + wr * 32, wc, Bt0 + (buf ^ 1) * a.r * 32);
+        asm volatile("cp.async.commit_group;" ::: "memory");
+        // B of this tile (committed one tile ago) has landed, in both warps of the pair.
+        asm volatile("cp.async.wait_group 2;" ::: "memory");
+        named_barrier_sync(pair_bar, 64);
+        const float* Bt = Bt0 + buf * a.r * 32;
         buf ^= 1;
 
-        // acc[i][p] holds columns 2p, 2p+1 of row i; fma.rn.f32x2 is an IEEE fma in
-        // each half, so every element follows the same chain as a scalar fmaf.
-        float2 acc[4][4];
+        // acc[i][p]: row i of this lane's 8, columns 2p, 2p+1.
+        float2 acc[8][4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
             for (int p = 0; p < 4; ++p) acc[i][p] = make_float2(0.0f, 0.0f);
-        const float* ap = As + L.col();
-        const float* bq = Bw + L.rg * a.rs;
-        int j = 0;
+        const float* ap = As + wc * 64 + cg * 8;
+        int j4 = 0;
 #pragma unroll 1
-        for (; j + 4 <= a.r; j += 4) {
-            float4 b4[4];
+        for (; j4 + 4 <= a.r; j4 += 4) {
+            const int sw = j4 & 28;
+            const float* b0p = Bt + j4 * 32 + ((rg * 8) ^ sw);
+            const float* b1p = Bt + j4 * 32 + ((rg * 8 + 4) ^ sw);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                b4[i] = *reinterpret_cast<const float4*>(bq + i * 4 * a.rs + j);
-#pragma unroll
-            for (int jj = 0; jj < 4; ++jj) {
-                const float4 a0 = *reinterpret_cast<const float4*>(ap + (j + jj) * kRqCols);
-                const float4 a1 = *reinterpret_cast<const float4*>(ap + (j + jj) * kRqCols + 4);
+            for (int u = 0; u < 4; ++u) {
+                const float4 b0 = *reinterpret_cast<const float4*>(b0p + u * 32);
+                const float4 b1 = *reinterpret_cast<const float4*>(b1p + u * 32);
+                const float4 a0 = *reinterpret_cast<const float4*>(ap + (j4 + u) * kRqCols);
+                const float4 a1 = *reinterpret_cast<const float4*>(ap + (j4 + u) * kRqCols + 4);
+                const float bl[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
                 const float2 av[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w),
                                       make_float2(a1.x, a1.y), make_float2(a1.z, a1.w)};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const float bv = jj == 0 ? b4[i].x : jj == 1 ? b4[i].y : jj == 2 ? b4[i].z : b4[i].w;
+                for (int i = 0; i < 8; ++i) {
+                    // Row i sits at element (i % 4) ^ u of its 16-byte group.
+                    const float bv = bl[(i & 4) | ((i & 3) ^ u)];
                     const float2 bb = make_float2(bv, bv);
 #pragma unroll
                     for (int p = 0; p < 4; ++p) acc[i][p] = __ffma2_rn(bb, av[p], acc[i][p]);
@@ -713,29 +883,36 @@ __global__ void __launch_bounds__(kRqThreads, 2) requant_quant_kernel(RqArgs a) 
             }
         }
 #pragma unroll 1
-        for (; j < a.r; ++j) {
+        for (int j = j4; j < a.r; ++j) {
             const float4 a0 = *reinterpret_cast<const float4*>(ap + j * kRqCols);
             const float4 a1 = *reinterpret_cast<const float4*>(ap + j * kRqCols + 4);
             const float2 av[4] = {make_float2(a0.x, a0.y), make_float2(a0.z, a0.w),
                                   make_float2(a1.x, a1.y), make_float2(a1.z, a1.w)};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float bv = bq[i * 4 * a.rs + j];
+            for (int i = 0; i < 8; ++i) {
+                const float bv = Bt[j * 32 + ((rg * 8 + i) ^ (j & 31))];
                 const float2 bb = make_float2(bv, bv);
 #pragma unroll
                 for (int p = 0; p < 4; ++p) acc[i][p] = __ffma2_rn(bb, av[p], acc[i][p]);
             }
         }
 
-        const int64_t k = k0 + L.col();
+        // This tile's W block has landed (the next tile's B may still be in flight).
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+        __syncwarp();
+        // Row i of this lane: codes at cp + i K/2, its scale word at sp + 16 i (the 8
+        // rows share one 32-row group of the scale layout).
+        const int64_t k = k0 + wc * 64 + cg * 8;
+        const int64_t nb = n0 + wr * 32 + rg * 8;
         const bool col_ok = k < a.K;
+        uint8_t* cp = kDump ? nullptr : a.codes + nb * (a.K >> 1) + (k >> 1);
+        uint8_t* sp = kDump ? nullptr : a.sf + sf_word_offset(nb, k >> 4, a.K);
+        float* dp = kDump ? a.dump + nb * a.K + k : nullptr;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int64_t n = n0 + L.row(i);
+        for (int i = 0; i < 8; ++i) {
             float x[8];
-            w.row(i, x);
+            rq2_w_row<kWType>(Ws, rg * 8 + i, cg, x);
             if (a.r > 0) {
-                const float2 cc = make_float2(a.c, a.c);
 #pragma unroll
                 for (int p = 0; p < 4; ++p) {
                     const float2 y = __ffma2_rn(cc, acc[i][p], make_float2(x[2 * p], x[2 * p + 1]));
@@ -743,25 +920,21 @@ __global__ void __launch_bounds__(kRqThreads, 2) requant_quant_kernel(RqArgs a) 
                     x[2 * p + 1] = y.y;
                 }
             }
-            if (n >= a.N) {
+            if (edge) {
+                const bool row_ok = nb + i < a.N;
+                if (!row_ok) {
 #pragma unroll
-                for (int q = 0; q < 8; ++q) x[q] = 0.0f;
-            }
-            if (kDump) {
-                if (col_ok && n < a.N) {
-                    float* p = a.dump + n * a.K + k;
-                    *reinterpret_cast<float4*>(p) = make_float4(x[0], x[1], x[2], x[3]);
-                    *reinterpret_cast<float4*>(p + 4) = make_float4(x[4], x[5], x[6], x[7]);
+                    for (int q = 0; q < 8; ++q) x[q] = 0.0f;  // scale padding rows quantize zeros
                 }
-                continue;
+                rq2_emit_row<true, kDump>(sc, cg, row_ok, col_ok, cp, sp, dp, x);
+            } else {
+                rq2_emit_row<false, kDump>(sc, cg, true, true, cp, sp, dp, x);
             }
-            uint32_t sfc;
-            const uint32_t packed = quant_half_block(x, s, d, inv_d, d_fast, &sfc);
-            const uint32_t word = gather_sf_word(sfc);
-            if (col_ok) {
-                if (n < a.N) *reinterpret_cast<uint32_t*>(a.codes + n * (a.K >> 1) + (k >> 1)) = packed;
-                if (n < a.rows_pad && L.cg == 0)
-                    *reinterpret_cast<uint32_t*>(a.sf + sf_word_offset(n, k >> 4, a.K)) = word;
+            if (!kDump) {
+                cp += a.K >> 1;
+                sp += 16;
+            } else {
+                dp += a.K;
             }
         }
     }
@@ -801,6 +974,8 @@ RqArgs rq_args(const void* W, const float* A, const float* B, int r, float c, in
     a.dump = dump;
     a.row_tiles = a.rows_pad / kRqRows;
     a.tiles = a.row_tiles * ((K + kRqCols - 1) / kRqCols);
+    a.row_tiles2 = a.rows_pad / kQRows;
+    a.tiles2 = a.row_tiles2 * ((K + kRqCols - 1) / kRqCols);
     a.rs = rq_bstride(r);
     a.inv_r = rq_inv_r(r);
     a.b_vec = r > 0 && r % 4 == 0 && (reinterpret_cast<uintptr_t>(B) & 15u) == 0;
@@ -809,17 +984,17 @@ RqArgs rq_args(const void* W, const float* A, const float* B, int r, float c, in
 
 template <int kWType>
 cudaError_t run_requant(const LaunchCtx& ctx, const RqArgs& a) {
-    const size_t smem = rq_smem_bytes(a.r);
+    const size_t smem1 = rq_smem_bytes(a.r), smem2 = rq2_smem_bytes<kWType>(a.r);
     unsigned g1 = 0, g2 = 0;
-    cudaError_t e = rq_grid(ctx, requant_amax_kernel<kWType>, smem, a.tiles, &g1);
+    cudaError_t e = rq_grid(ctx, requant_amax_kernel<kWType>, smem1, a.tiles, &g1);
     if (e != cudaSuccess) return e;
-    e = rq_grid(ctx, requant_quant_kernel<kWType, false>, smem, a.tiles, &g2);
+    e = rq_grid(ctx, requant_quant_kernel<kWType, false>, smem2, a.tiles2, &g2);
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(a.s_t, 0, sizeof(float), ctx.stream);
     if (e != cudaSuccess) return e;
-    requant_amax_kernel<kWType><<<g1, kRqThreads, smem, ctx.stream>>>(a);
+    requant_amax_kernel<kWType><<<g1, kRqThreads, smem1, ctx.stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    requant_quant_kernel<kWType, false><<<g2, kRqThreads, smem, ctx.stream>>>(a);
+    requant_quant_kernel<kWType, false><<<g2, kRqThreads, smem2, ctx.stream>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     requant_finalize_kernel<<<1, 32, 0, ctx.stream>>>(a.s_t);
     return cudaGetLastError();
@@ -827,9 +1002,9 @@ cudaError_t run_requant(const LaunchCtx& ctx, const RqArgs& a) {
 
 template <int kWType>
 cudaError_t run_merge_dump(const LaunchCtx& ctx, const RqArgs& a) {
-    const size_t smem = rq_smem_bytes(a.r);
+    const size_t smem = rq2_smem_bytes<kWType>(a.r);
     unsigned g = 0;
-    cudaError_t e = rq_grid(ctx, requant_quant_kernel<kWType, true>, smem, a.tiles, &g);
+    cudaError_t e = rq_grid(ctx, requant_quant_kernel<kWType, true>, smem, a.tiles2, &g);
     if (e != cudaSuccess) return e;
     requant_quant_kernel<kWType, true><<<g, kRqThreads, smem, ctx.stream>>>(a);
     return cudaGetLastError();
@@ -847,6 +1022,12 @@ __global__ void test_e4m3_kernel(const float* v, uint8_t* out, int64_t n) {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x)
         out[i] = (uint8_t)cvt_e4m3(v[i]);
+}
+
+__global__ void test_e4m3_decode_kernel(const uint8_t* c, float* out, int64_t n) {
+    for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+         i += (int64_t)gridDim.x * blockDim.x)
+        out[i] = e4m3_value(c[i]);
 }
 
 __global__ void test_e2m1_quotient_kernel(const float* x, const float* den, uint8_t* out,
@@ -912,6 +1093,12 @@ cudaError_t launch_test_e2m1(const LaunchCtx& ctx, const float* q, uint8_t* code
 
 cudaError_t launch_test_e4m3(const LaunchCtx& ctx, const float* v, uint8_t* codes, int64_t n) {
     test_e4m3_kernel<<<grid_for(n, ctx), 256, 0, ctx.stream>>>(v, codes, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_test_e4m3_decode(const LaunchCtx& ctx, const uint8_t* codes, float* out,
+                                    int64_t n) {
+    test_e4m3_decode_kernel<<<grid_for(n, ctx), 256, 0, ctx.stream>>>(codes, out, n);
     return cudaGetLastError();
 }
 

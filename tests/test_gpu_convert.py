@@ -14,7 +14,7 @@ import pytest
 import torch
 
 import nvfp4_quantized_dit_gb300 as nv
-from gpu_util import require_gpu
+from gpu_util import np_, require_gpu
 
 pytestmark = pytest.mark.gpu
 
@@ -112,3 +112,13 @@ def test_e4m3_quotient_fast_path(orc):
     want = orc.e4m3_rne(q)
     got = nv.nvfp4_test_e4m3_quotient(torch.from_numpy(x).cuda(), torch.from_numpy(d).cuda()).cpu().numpy()
     assert np.array_equal(got, want), f"{int((got != want).sum())} mismatches"
+
+
+def test_e4m3_decode_every_scale_code(orc):
+    """Every non-negative finite E4M3 code decodes to the oracle's value, bit for bit
+    (the quantizers divide by this value)."""
+    require_gpu()
+    codes = torch.arange(0, 0x7F, dtype=torch.uint8)
+    got = np_(nv.nvfp4_test_e4m3_decode(codes.cuda()))
+    want = np.array([orc.e4m3_decode(int(c)) for c in codes], np.float32)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
