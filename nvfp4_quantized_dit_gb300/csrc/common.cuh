@@ -214,15 +214,28 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  : "memory");
 }
 
+// kCluster: acquire at cluster scope, for barriers that threads of the peer CTA
+// arrive on (their release.cluster arrivals then order their prior writes, including
+// tensor-memory stores fenced before the arrival, before the waiter's later work).
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t done;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(done)
-        : "r"(bar), "r"(parity)
-        : "memory");
+    if (kCluster)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity)
+            : "memory");
     return done != 0;
 }
 
@@ -231,13 +244,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // raises the CTA's abort flag (so the CTA's other waits give up at once) and
 // returns false.  It also returns false as soon as another thread of the CTA
 // has raised the abort flag.  An iteration cap backs up the clock.
+template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
                                           volatile int* abort_flag, uint64_t limit_ns) {
     const uint32_t a = smem_u32(bar);
-    if (mbar_try_wait(a, parity)) return true;
+    if (mbar_try_wait<kCluster>(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1; it < (1u << 30); ++it) {
-        if (mbar_try_wait(a, parity)) return true;
+        if (mbar_try_wait<kCluster>(a, parity)) return true;
         if ((it & 31u) == 0u) {
             if (*abort_flag) return false;
             if (globaltimer_ns() - t0 > limit_ns) break;
@@ -282,9 +296,15 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t local, uint32_t rank) {
 }
 
 // Arrive once on an mbarrier given by its shared::cluster address (possibly in a peer CTA).
+//
+// Default semantics (release at CTA scope).  The data these arrivals publish is
+// tensor memory whose tcgen05 loads or stores the arriving thread has already waited
+// for (tcgen05.wait, then tcgen05.fence::before_thread_sync), so no cluster-scope
+// release of ordinary memory is needed; a .release.cluster arrive measured ~1,250
+// cycles per arrive in the GEMM (it waits for the SM's outstanding memory traffic),
+// against ~100 for this form.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-                 : "memory");
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
 // Tile load into this CTA's shared memory whose completion is counted on an mbarrier

@@ -10,24 +10,38 @@
 //
 // Persistent kernel on CTA pairs (clusters of two): each pair computes a 256 x 256
 // tile with 2-CTA MMAs (tcgen05 cta_group::2, M = 256).  Each CTA loads its own 128
-// rows of A and one half of B's 256 rows, so each SM stores and reads only half of
-// the B tile; the even CTA issues the MMAs for both.  224 threads per CTA:
-//   warp 0       TMA producer (both CTAs): A, half of B and, for NVFP4, the scale
-//                tiles into a shared-memory ring whose completion is counted on the
-//                even CTA's barriers;
+// rows of A and one half of B's 256 rows; the even CTA issues the MMAs for both.
+//
+// The even CTA's first 128 rows of B are output columns 256 nb .. +127 and the odd
+// CTA's the next 128.  One accumulator of 256 columns per CTA: the MMAs of the next
+// tile wait until the epilogue has moved it to registers (it is released before the
+// conversion and the stores).
+//
+// Warps (NVFP4: 16 = four role-uniform warp groups, so that registers can be moved
+// to the epilogue with setmaxnreg; BF16: 10):
+//   warp 0       TMA producer (both CTAs): A, this CTA's half of B and, for NVFP4,
+//                the scale tiles of this stage into a shared-memory ring; A/B
+//                completion is counted on the even CTA's barriers, the scale tiles
+//                on this CTA's own;
 //   warp 1       allocates 512 tensor-memory columns in both CTAs (collectively);
 //                lane 0 of the even CTA issues the MMAs and releases each stage
 //                to both CTAs;
-//   warps 2..9   epilogue (both CTAs), two warps per tensor-memory lane quarter,
+//   epilogue     NVFP4 warps 8..15, BF16 warps 2..9 (both CTAs), two warps per
+//                tensor-memory lane quarter (quarter = warp % 4),
 //                128 columns each: tensor memory -> registers (tcgen05.ld, all
 //                issued before one wait), release of the accumulator, then scale,
 //                bias, bf16, and 32x32 chunks stored by TMA from a swizzled
 //                shared-memory staging ring (asynchronous, clipped at M and N);
-//   warp 10      NVFP4, even CTA: copies each stage's scale tiles shared -> tensor
-//                memory in both CTAs (tcgen05.cp) and hands the stage to the MMAs.
+//   warps 4..7   NVFP4 only (both CTAs), one per lane quarter: copy each stage's
+//                scale bytes from shared memory into registers and write them into
+//                this CTA's tensor memory with tcgen05.st (four warps writing their
+//                own lane quarters in parallel), then signal the even CTA.
 // Per CTA: fp32 accumulator in tensor-memory columns 0..255 (its 128 rows x 256);
-// NVFP4 scale tiles for stage s in columns 256 + 48 s (A: 4 per MMA for its 128
-// rows, B: 8 per MMA for all 256 rows).
+// NVFP4 scales for stage s in columns 256 + 48 s: A at +4 kk for K-step kk (4
+// columns: lane l, column c holds the 4 scales of row l + 32 c), B at +16 + 8 kk
+// (8 columns: lane l, column c holds the scales of B row l + 32 c).  Each lane
+// quarter holds the same scale data (the MMA reads its own quarter).  These are the
+// 512-byte chunks of the 128x4 blocked scale layout, row l of a chunk per lane.
 //
 // Every mbarrier wait is bounded (common.cuh: mbar_wait); on expiry the kernel
 // records NVFP4_ERR_TIMEOUT, drains its own copies and MMAs (again bounded),
@@ -41,8 +55,8 @@ constexpr int BM = 128;        // rows of A / D per CTA
 constexpr int BN = 256;        // columns of D per pair (rows of B)
 constexpr int kPair = 2;       // CTAs per cluster (one 2-CTA MMA)
 constexpr int kEpiWarps = 8;
-constexpr int kThreads = (2 + kEpiWarps + 1) * 32;
-constexpr int kCopierWarp = 2 + kEpiWarps;
+constexpr int kSfWarps = 4;
+constexpr int kSfWarp0 = 4;  // NVFP4: scale writers are warp group 1
 constexpr uint32_t kATileBytes = BM * 128;            // 16 KB: 128 rows x 128 B
 constexpr uint32_t kBHalfBytes = (BN / kPair) * 128;  // 16 KB: this CTA's 128 rows of B
 constexpr uint32_t kSFAStageBytes = 4 * 512;          // 128 rows x 4 K-chunks of 64
@@ -59,13 +73,15 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for copies already in
 
 template <bool kFP4>
 struct Cfg {
-    static constexpr int kStages = kFP4 ? 5 : 6;
-    // A and B bytes this CTA loads per stage, and for NVFP4 its scale-tile bytes (the
-    // even CTA expects twice each, on separate barriers).
+    static constexpr int kStages = 5;
+    static constexpr int kEpiWarp0 = kFP4 ? 8 : 2;  // first epilogue warp
+    static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+    // A and B bytes this CTA loads per stage (the even CTA expects twice that), and for
+    // NVFP4 its scale-tile bytes (expected on its own barrier).
     static constexpr uint32_t kABBytes = kATileBytes + kBHalfBytes;
     static constexpr uint32_t kSFBytes = kFP4 ? kSFAStageBytes + kSFBStageBytes : 0u;
     static constexpr uint32_t kStageBytes = kABBytes + kSFBytes;
-    static constexpr int kEpiBufs = kFP4 ? 2 : 1;  // staging chunks per epilogue warp
+    static constexpr int kEpiBufs = 2;  // staging chunks per epilogue warp
     static constexpr uint32_t kEpiBytes = kEpiWarps * (kEpiBufs * kChunkBytes + kBiasBytes);
     static constexpr uint32_t kBarrierBytes = 256;
     static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarrierBytes;
@@ -75,6 +91,12 @@ static_assert(Cfg<true>::kSmemBytes <= 232448 && Cfg<false>::kSmemBytes <= 23244
 static_assert(Cfg<true>::kStageBytes % 1024 == 0 && Cfg<false>::kStageBytes % 1024 == 0,
               "stages must keep 1024-byte alignment for the 128-byte swizzle");
 static_assert(kSfTmemBase + Cfg<true>::kStages * kSfTmemPerStage <= kTmemCols, "tensor memory");
+static_assert(kSfWarp0 % 4 == 0 && kSfWarps == 4 && Cfg<true>::kEpiWarp0 == kSfWarp0 + kSfWarps,
+              "scale warps are one whole warp group covering the four lane quarters");
+// NVFP4 register split (per thread; warp groups 0..3, launched with 65536 / 512 = 128):
+// producer/MMA group, scale writers, two epilogue groups.  Must not exceed 4 x 128.
+constexpr uint32_t kRegsCtl = 56, kRegsSf = 88, kRegsEpi = 184;
+static_assert(kRegsCtl + kRegsSf + 2 * kRegsEpi <= 4 * 128, "setmaxnreg split over budget");
 
 // Instruction descriptors (tcgen05, 32 bits): bits 4-5 accumulator format
 // (1 = f32), 7-9 A format, 10-12 B format, 15/16 A/B major (0 = K-major),
@@ -129,7 +151,7 @@ struct Sched {
 };
 
 template <bool kFP4>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(Cfg<kFP4>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 const __grid_constant__ CUtensorMap tmap_b,
                 const __grid_constant__ CUtensorMap tmap_sfa,
@@ -143,9 +165,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* epi = smem + S * C::kStageBytes;
     uint64_t* full = reinterpret_cast<uint64_t*>(epi + C::kEpiBytes);  // used in the even CTA
     uint64_t* empty = full + S;
-    uint64_t* sfready = empty + S;
-    uint64_t* sf_full = sfready + S;  // scale tiles of both CTAs landed (even CTA)
-    uint64_t* tmem_full = sf_full + S;
+    uint64_t* sf_full = empty + S;    // this CTA's scale tiles landed
+    uint64_t* sfready = sf_full + S;  // scales of both CTAs in tensor memory (even CTA)
+    uint64_t* tmem_full = sfready + S;
     uint64_t* tmem_empty = tmem_full + 1;  // used in the even CTA
     uint64_t* drain = tmem_empty + 1;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
@@ -165,8 +187,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
-            mbar_init(&sfready[s], 1);
             mbar_init(&sf_full[s], 1);
+            mbar_init(&sfready[s], kSfWarps * kPair);
         }
         mbar_init(tmem_full, 1);
         mbar_init(tmem_empty, kEpiWarps * kPair);  // the epilogue warps of both CTAs
@@ -191,12 +213,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     cluster_sync_all();  // both CTAs' barriers and tensor memory exist from here on
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // NVFP4: each role's branch starts with its warp group's setmaxnreg (every warp of a
+    // group executes the same one, converged).
 
     if (warp == 0) {
+        if (kFP4) regs_decrease<kRegsCtl>();
         if (lane == 0) {
             // ------------------------------------------------ TMA producer (both CTAs)
             const uint32_t full_even = map_to_rank(smem_u32(full), 0);
-            const uint32_t sf_full_even = map_to_rank(smem_u32(sf_full), 0);
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -214,16 +238,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* sa = smem + stage * C::kStageBytes;
                     uint8_t* sb = sa + kATileBytes;
                     if (kFP4) {
-                        // Scale tiles first (small; the copier can start on them while A and B
-                        // are in flight): 4 chunks of 512 bytes along K per 128-row tile;
+                        // Scale tiles first (small; the scale warps start on them while A and
+                        // B are in flight): 4 chunks of 512 bytes along K per 128-row tile;
                         // chunks or tiles past the end arrive as zeros.
-                        if (leader) mbar_arrive_expect_tx(&sf_full[stage], kPair * C::kSFBytes);
-                        const uint32_t sbar = sf_full_even + 8u * (uint32_t)stage;
+                        mbar_arrive_expect_tx(&sf_full[stage], C::kSFBytes);
                         uint8_t* sfa = sb + kBHalfBytes;
                         uint8_t* sfb = sfa + kSFAStageBytes;
-                        tma_load_4d_pair(&tmap_sfa, sbar, sfa, 0, 0, kb * 4, m_blk);
-                        tma_load_4d_pair(&tmap_sfb, sbar, sfb, 0, 0, kb * 4, 2 * n_blk);
-                        tma_load_4d_pair(&tmap_sfb, sbar, sfb + 2048, 0, 0, kb * 4, 2 * n_blk + 1);
+                        tma_load_4d(&tmap_sfa, &sf_full[stage], sfa, 0, 0, kb * 4, m_blk);
+                        tma_load_4d(&tmap_sfb, &sf_full[stage], sfb, 0, 0, kb * 4, 2 * n_blk);
+                        tma_load_4d(&tmap_sfb, &sf_full[stage], sfb + 2048, 0, 0, kb * 4,
+                                    2 * n_blk + 1);
                     }
                     if (leader) mbar_arrive_expect_tx(&full[stage], kPair * C::kABBytes);
                     const int x = kFP4 ? kb * 128 : kb * 64;
@@ -255,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == 1) {
+        if (kFP4) regs_decrease<kRegsCtl>();
         if (lane == 0 && leader) {
             // ------------------------------------------------ MMA issuer (even CTA)
             const uint32_t idesc = kFP4 ? idesc_nvfp4() : idesc_bf16();
@@ -267,16 +292,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             bool any_mma = false;
             for (int t = sch.first; ok && t < sch.total; t += sch.step) {
-                if (!mbar_wait(tmem_empty, acc_phase ^ 1u, args.status, abort_flag,
-                               kWaitLimitNs)) {
+                // The accumulator must have been drained by the epilogue of both CTAs.
+                if (!mbar_wait<true>(tmem_empty, acc_phase ^ 1u, args.status, abort_flag,
+                                     kWaitLimitNs)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(&full[stage], phase, args.status, abort_flag, kWaitLimitNs) ||
-                        (kFP4 &&
-                         !mbar_wait(&sfready[stage], phase, args.status, abort_flag, kWaitLimitNs))) {
+                        (kFP4 && !mbar_wait<true>(&sfready[stage], phase, args.status, abort_flag,
+                                                  kWaitLimitNs))) {
                         ok = false;
                         break;
                     }
@@ -315,54 +341,66 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(drain, 0, args.status, &dummy_flag, kDrainLimitNs);
             }
         }
-    } else if (warp == kCopierWarp) {
-        if (kFP4 && lane == 0 && leader) {
-            // ------------------------------------------------ scale copier (NVFP4, even CTA)
-            const uint64_t sf_desc0 =
-                smem_desc(smem_u32(smem) + kATileBytes + kBHalfBytes, 128, 128, kLayoutNone);
-            int stage = 0;
-            uint32_t phase = 0;
+    } else if (kFP4 && warp < kSfWarp0) {
+        regs_decrease<kRegsCtl>();  // warps 2, 3: no role
+    } else if (kFP4 && warp < C::kEpiWarp0) {
+        regs_decrease<kRegsSf>();
+        // ------------------------------------------------ scale writers (NVFP4, both CTAs)
+        // Warp w writes tensor-memory lanes 32 (w % 4) .. +31; lane l of every quarter
+        // takes row l of each 512-byte scale chunk (16 bytes: rows l + 32 c, c = 0..3).
+        const uint32_t quarter = (uint32_t)(warp & 3);
+        const uint32_t lane_base = tmem_base + ((quarter * 32u) << 16);
+        const uint32_t sfready_even = map_to_rank(smem_u32(sfready), 0);
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int t = sch.first; t < sch.total; t += sch.step) {
             bool ok = true;
-            bool any_cp = false;
-            for (int t = sch.first; ok && t < sch.total; t += sch.step) {
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&sf_full[stage], phase, args.status, abort_flag, kWaitLimitNs)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after_sync();
-                    const int nk = min(4, k_steps - kb * 4);
-                    const uint64_t soff = (uint64_t)((stage * C::kStageBytes) >> 4);
-                    const uint32_t sf_col = tmem_base + kSfTmemBase + (uint32_t)stage * kSfTmemPerStage;
-                    // SFA chunk kk at +512 kk; SFB rows 0-127 at +2048 + 512 kk, rows
-                    // 128-255 at +4096 + 512 kk (descriptor units of 16 bytes).
+            for (int kb = 0; kb < num_kb; ++kb) {
+                ok = mbar_wait(&sf_full[stage], phase, args.status, abort_flag, kWaitLimitNs);
+                ok = __all_sync(0xFFFFFFFFu, ok);  // tcgen05.st is .sync.aligned
+                if (!ok) break;
+                const uint8_t* sfa = smem + stage * C::kStageBytes + kATileBytes + kBHalfBytes;
+                const uint8_t* sfb = sfa + kSFAStageBytes;
+                uint32_t ra[16], rb[32];
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        if (kk < nk) {
-                            tmem_cp_32x128b_x4_pair(sf_col + 4 * kk, sf_desc0 + soff + 32 * kk);
-                            tmem_cp_32x128b_x4_pair(sf_col + 16 + 8 * kk, sf_desc0 + soff + 128 + 32 * kk);
-                            tmem_cp_32x128b_x4_pair(sf_col + 20 + 8 * kk, sf_desc0 + soff + 256 + 32 * kk);
-                        }
-                    }
-                    any_cp = true;
-                    mma_commit_pair_multicast(&sfready[stage], kEvenCta);
-                    if (++stage == S) {
-                        stage = 0;
-                        phase ^= 1u;
-                    }
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint4 a4 = *reinterpret_cast<const uint4*>(sfa + kk * 512 + lane * 16);
+                    const uint4 b0 = *reinterpret_cast<const uint4*>(sfb + kk * 512 + lane * 16);
+                    const uint4 b1 =
+                        *reinterpret_cast<const uint4*>(sfb + 2048 + kk * 512 + lane * 16);
+                    ra[4 * kk + 0] = a4.x;
+                    ra[4 * kk + 1] = a4.y;
+                    ra[4 * kk + 2] = a4.z;
+                    ra[4 * kk + 3] = a4.w;
+                    rb[8 * kk + 0] = b0.x;  // B rows 0..127 (the even CTA's half)
+                    rb[8 * kk + 1] = b0.y;
+                    rb[8 * kk + 2] = b0.z;
+                    rb[8 * kk + 3] = b0.w;
+                    rb[8 * kk + 4] = b1.x;  // B rows 128..255
+                    rb[8 * kk + 5] = b1.y;
+                    rb[8 * kk + 6] = b1.z;
+                    rb[8 * kk + 7] = b1.w;
+                }
+                const uint32_t col = lane_base + kSfTmemBase + (uint32_t)stage * kSfTmemPerStage;
+                tmem_st_32x32b_x16(col, ra);
+                tmem_st_32x32b_x32(col + 16, rb);
+                tmem_st_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(sfready_even + 8u * (uint32_t)stage);
+                if (++stage == S) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
-            if (*abort_flag && any_cp) {
-                mma_commit_pair_multicast(drain, kEvenCta);
-                int dummy_flag = 0;
-                mbar_wait(drain, 0, args.status, &dummy_flag, kDrainLimitNs);
-            }
+            if (!ok) break;
         }
-    } else if (warp >= 2 && warp < 2 + kEpiWarps) {
-        // ------------------------------------------------ epilogue (warps 2..9, both CTAs)
+    } else if (warp >= C::kEpiWarp0) {
+        if (kFP4) regs_increase<kRegsEpi>();
+        // ------------------------------------------------ epilogue (both CTAs)
         const int quarter = warp & 3;                // tensor-memory lanes 32*quarter .. +31
-        const int half = (warp - 2) / 4;             // columns 128*half .. +127
-        const int ew = warp - 2;
+        const int ew = warp - C::kEpiWarp0;
+        const int half = ew / 4;                     // columns 128*half .. +127
         uint8_t* stg = epi + ew * C::kEpiBufs * kChunkBytes;  // 2048-byte aligned chunks
         uint8_t* sbias = epi + kEpiWarps * C::kEpiBufs * kChunkBytes + ew * kBiasBytes;
         uint32_t chunk_seq = 0;
@@ -433,8 +471,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 __syncwarp();
                 const int sx = n0 + c * 32, sy = m_blk * BM + quarter * 32;
-                if (lane == 0 && sx < N && sy < M) {  // partial boxes are clipped by TMA
-                    tma_store_2d(&tmap_y, buf, sx, sy);
+                if (lane == 0) {
+                    // Partial boxes are clipped by TMA; a chunk wholly outside Y is not
+                    // stored but still commits its (empty) group, so that every ring slot
+                    // owns exactly one group and the wait above is exact.
+                    if (sx < N && sy < M) tma_store_2d(&tmap_y, buf, sx, sy);
                     bulk_commit_group();
                 }
                 ++chunk_seq;
@@ -483,7 +524,7 @@ cudaError_t run_gemm(const LaunchCtx& ctx, const CUtensorMap& ta, const CUtensor
     attr[0].val.clusterDim.x = kPair;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(Cfg<kFP4>::kThreads, 1, 1);
     cfg.dynamicSmemBytes = Cfg<kFP4>::kSmemBytes;
     cfg.stream = ctx.stream;
     cfg.attrs = attr;
