@@ -73,7 +73,9 @@ constexpr uint64_t kDrainLimitNs = 200000000ull;  // 0.2 s for copies already in
 
 template <bool kFP4>
 struct Cfg {
-    static constexpr int kStages = 5;
+    // NVFP4 stages carry A, B and the scale tiles (38 KB); BF16 stages A and B (32 KB),
+    // one more of them thanks to a single epilogue staging chunk per warp.
+    static constexpr int kStages = kFP4 ? 5 : 6;
     static constexpr int kEpiWarp0 = kFP4 ? 8 : 2;  // first epilogue warp
     static constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
     // A and B bytes this CTA loads per stage (the even CTA expects twice that), and for
@@ -81,7 +83,7 @@ struct Cfg {
     static constexpr uint32_t kABBytes = kATileBytes + kBHalfBytes;
     static constexpr uint32_t kSFBytes = kFP4 ? kSFAStageBytes + kSFBStageBytes : 0u;
     static constexpr uint32_t kStageBytes = kABBytes + kSFBytes;
-    static constexpr int kEpiBufs = 2;  // staging chunks per epilogue warp
+    static constexpr int kEpiBufs = kFP4 ? 2 : 1;  // staging chunks per epilogue warp
     static constexpr uint32_t kEpiBytes = kEpiWarps * (kEpiBufs * kChunkBytes + kBiasBytes);
     static constexpr uint32_t kBarrierBytes = 256;
     static constexpr uint32_t kSmemBytes = 1024 + kStages * kStageBytes + kEpiBytes + kBarrierBytes;
