@@ -132,42 +132,64 @@ struct F8 {
     float v[8];
 };
 
-// Slow path of e2m1_quotient8 (rare): true IEEE divisions where the fast quotient
-// is within the window of a rounding boundary, or everywhere when !fast_ok.
-static __device__ __noinline__ F8 e2m1_fix8(F8 x, F8 q, float den, bool fast_ok) {
+// Slow path of e2m1_quotient8 (rare): the 8 codes from true IEEE divisions.
+static __device__ __noinline__ uint32_t e2m1_exact8(F8 x, float den) {
+    F8 q;
 #pragma unroll
-    for (int i = 0; i < 8; ++i)
-        if (!fast_ok || near_boundary<20>(__float_as_uint(q.v[i]))) q.v[i] = __fdiv_rn(x.v[i], den);
-    return q;
+    for (int i = 0; i < 8; ++i) q.v[i] = __fdiv_rn(x.v[i], den);
+    return cvt_e2m1x8(q.v[0], q.v[1], q.v[2], q.v[3], q.v[4], q.v[5], q.v[6], q.v[7]);
 }
 
 static __device__ __noinline__ float exact_quotient(float v, float d) { return __fdiv_rn(v, d); }
 
-// RNE_E2M1_sat(fl(x / den)) for 8 values sharing den > 0, with r an approximation of
-// 1/den within 1 ulp (valid when fast_ok).
+// Bracketing reciprocals of a block's divisor den > 0 for e2m1_quotient8:
+// lo = RD(r (1 - 2^-20)), hi = RU(r (1 + 2^-20)) with r = rcp.approx(den), which is
+// within 1 ulp (< 2^-23 relative) of 1/den when den and 1/den are normal (`fast`).
+struct Recip {
+    float lo, hi;
+    bool fast;
+};
+__device__ __forceinline__ Recip make_recip(float den) {
+    Recip rc;
+    rc.fast = fast_recip_ok(den);
+    const float r = rc.fast ? recip_approx(den) : 0.0f;
+    rc.lo = __fmul_rd(r, 1.0f - 0x1p-20f);
+    rc.hi = __fmul_ru(r, 1.0f + 0x1p-20f);
+    return rc;
+}
+
+// RNE_E2M1_sat(fl(x / den)) for 8 values sharing den > 0.
 //
-// Fast path: q' = fl(x * r).  Then |q' - x/den| <= 1.5 * 2^-23 |x/den| and
-// |fl(x/den) - x/den| <= 2^-24 |x/den|, so q' and the exact quotient fl(x/den) are
-// less than 4 ulps apart.  E2M1 rounding is a step function whose steps sit at
-// 3-significant-bit numbers; if q' is more than 16 ulps away from every such number,
-// q' and fl(x/den) round to the same code.  Otherwise (and whenever den or 1/den is
-// not a normal number) the value is recomputed with a true IEEE division.
-__device__ __forceinline__ uint32_t e2m1_quotient8(const float (&x)[8], float den, float r,
-                                                   bool fast_ok) {
-    F8 q;
+// Fast path: the quotient is bracketed.  lo = fl(x * rc.lo) and hi = fl(x * rc.hi)
+// satisfy |lo| < |fl(x / den)| < |hi| with the same sign wherever a rounding decision
+// is made (rc.lo <= (1/den)(1 - 7 2^-23) and rc.hi >= (1/den)(1 + 7 2^-23); each
+// product and the quotient round by at most 2^-24 relatively; every E2M1 boundary is
+// a normal number, and below the smallest one all three give code 0 or 0x8).  E2M1
+// rounding is monotone in the magnitude, so if lo and hi give the same 8 codes so
+// does fl(x / den).  Otherwise (a quotient within about 2^-20 of a rounding boundary,
+// or an exact tie) and whenever den or 1/den is not a normal number, the 8 codes come
+// from true IEEE divisions.  Zero stays zero with its sign in both products.
+__device__ __forceinline__ uint32_t e2m1_quotient8(const float (&x)[8], float den, const Recip& rc) {
+    float lo[8], hi[8];
+    const float2 rl = make_float2(rc.lo, rc.lo), rh = make_float2(rc.hi, rc.hi);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q.v[i] = __fmul_rn(x[i], r);
-    // Any of the 8 near a boundary <=> the smallest key is.
-    uint32_t kmin = near_key<20>(__float_as_uint(q.v[0]));
-#pragma unroll
-    for (int i = 1; i < 8; ++i) kmin = min(kmin, near_key<20>(__float_as_uint(q.v[i])));
-    if (!fast_ok || kmin < (32u << 12)) {
+    for (int i = 0; i < 8; i += 2) {
+        const float2 xv = make_float2(x[i], x[i + 1]);
+        const float2 a = __fmul2_rn(xv, rl), b = __fmul2_rn(xv, rh);
+        lo[i] = a.x;
+        lo[i + 1] = a.y;
+        hi[i] = b.x;
+        hi[i + 1] = b.y;
+    }
+    const uint32_t c_lo = cvt_e2m1x8(lo[0], lo[1], lo[2], lo[3], lo[4], lo[5], lo[6], lo[7]);
+    const uint32_t c_hi = cvt_e2m1x8(hi[0], hi[1], hi[2], hi[3], hi[4], hi[5], hi[6], hi[7]);
+    if (!rc.fast || c_lo != c_hi) {
         F8 xv;
 #pragma unroll
         for (int i = 0; i < 8; ++i) xv.v[i] = x[i];
-        q = e2m1_fix8(xv, q, den, fast_ok);
+        return e2m1_exact8(xv, den);
     }
-    return cvt_e2m1x8(q.v[0], q.v[1], q.v[2], q.v[3], q.v[4], q.v[5], q.v[6], q.v[7]);
+    return c_hi;
 }
 
 // RNE_E4M3_sat(fl(v / d)) for v >= 0, d > 0, with inv_d within 1 ulp of 1/d: same

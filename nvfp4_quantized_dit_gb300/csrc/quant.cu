@@ -70,8 +70,7 @@ __device__ __forceinline__ uint32_t quant_half_block(const float (&x)[8], float 
     *sfc = code;
     const float den = __fmul_rn(e4m3_value(code), s);
     if (!(den > 0.0f)) return 0u;
-    const bool fast = fast_recip_ok(den);
-    return e2m1_quotient8(x, den, fast ? recip_approx(den) : 0.0f, fast);
+    return e2m1_quotient8(x, den, make_recip(den));
 }
 
 // Gathers the scale codes of 4 consecutive blocks held by lanes l, l+2, l+4, l+6
@@ -201,13 +200,12 @@ __global__ void __launch_bounds__(kAqWarps * 32)
             const float den = __fmul_rn(e4m3_value(sfc), s);
             uint2 packed = make_uint2(0u, 0u);
             if (valid && have && den > 0.0f) {
-                const bool fast = fast_recip_ok(den);
-                const float r = fast ? recip_approx(den) : 0.0f;
+                const Recip rc = make_recip(den);
                 float x[8];
                 unpack8(srow[2 * b], x);
-                packed.x = e2m1_quotient8(x, den, r, fast);
+                packed.x = e2m1_quotient8(x, den, rc);
                 unpack8(srow[2 * b + 1], x);
-                packed.y = e2m1_quotient8(x, den, r, fast);
+                packed.y = e2m1_quotient8(x, den, rc);
             }
             // Scale codes of blocks b..b+3 (lanes l..l+3, l % 4 == 0) -> one word.
             const uint32_t s1 = __shfl_down_sync(kFull, sfc, 1);
@@ -1035,10 +1033,8 @@ __global__ void test_e2m1_quotient_kernel(const float* x, const float* den, uint
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
          i += (int64_t)gridDim.x * blockDim.x) {
         const float dn = den[i];
-        const bool fast = fast_recip_ok(dn);
-        const float r = fast ? recip_approx(dn) : 0.0f;
         const float xs[8] = {x[i], 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        out[i] = (uint8_t)(e2m1_quotient8(xs, dn, r, fast) & 0xFu);
+        out[i] = (uint8_t)(e2m1_quotient8(xs, dn, make_recip(dn)) & 0xFu);
     }
 }
 
