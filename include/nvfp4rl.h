@@ -111,15 +111,32 @@ static inline size_t nvfp4_sf_offset(int64_t row, int64_t kblk, int64_t K) {
  *   sf     device, nvfp4_sf_bytes(N, K) bytes (out, padding rows written 0).
  *   s_t    device, one fp32 (out): amax(|W'|) / 2688.  Also used as the amax
  *          accumulator while the call runs, so it must not alias other buffers.
+ *   workspace, workspace_bytes
+ *          device scratch owned by the caller, or NULL / 0.  With bf16 W, r == 32
+ *          and a 16-byte aligned B, a 256-byte aligned workspace of at least
+ *          nvfp4_requant_workspace_bytes(...) bytes selects the tensor-core merge;
+ *          otherwise the merge runs on CUDA cores.  Both give identical results.
+ *          The workspace must not be used by anything else until the call's
+ *          work on `stream` has completed; its contents are not needed afterwards.
  *   K % 64 == 0, K <= 1 << 20, N < 2^31.
- * Enqueues a memset and three kernels: exact amax|W'| (W read once; only the
- * elements whose |W| a Cauchy-Schwarz bound on the LoRA term leaves in reach of
- * the maximum are merged), merge + quantize (every element merged once), and a
- * one-thread finalize of s_t.  Inputs must be finite.
+ * CUDA-core path: a memset and three kernels: exact amax|W'| (W read once; only the
+ * elements whose |W| a Cauchy-Schwarz bound on the LoRA term leaves in reach of the
+ * maximum are merged), merge + quantize (every element merged once), and a
+ * one-thread finalize of s_t.  Tensor-core path: a kernel that splits A and B into
+ * bf16 pairs (into the workspace), a memset, the merge as a bf16 GEMM with every
+ * decision certified against a rigorous bound or recomputed by the fp32 chain
+ * (amax pass, quantize pass), and the finalize.  Inputs must be finite.
  */
 nvfp4_status nvfp4_requant(const void* W, int w_dtype, const float* A, const float* B, int r,
                            float alpha, int64_t N, int64_t K, uint8_t* codes, uint8_t* sf,
-                           float* s_t, void* stream);
+                           float* s_t, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * nvfp4_requant_workspace_bytes — bytes of workspace that select nvfp4_requant's
+ * tensor-core merge for these arguments, or 0 when that path does not apply
+ * (w_dtype other than NVFP4_W_BF16, r != 32, or invalid sizes).  Host only.
+ */
+size_t nvfp4_requant_workspace_bytes(int w_dtype, int r, int64_t N, int64_t K);
 
 /*
  * nvfp4_act_quant — per-row ("per token") NVFP4 of BF16 activations.

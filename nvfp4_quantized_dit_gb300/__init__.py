@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "NVFP4Error", "library", "sf_bytes", "sf_offset",
-    "nvfp4_requant", "nvfp4_act_quant", "nvfp4_gemm", "bf16_gemm", "select_contrastive",
+    "nvfp4_requant", "requant_workspace_bytes", "nvfp4_act_quant", "nvfp4_gemm", "bf16_gemm", "select_contrastive",
     "nvfp4_device_status", "nvfp4_status_string", "nvfp4_version",
     "nvfp4_test_e2m1", "nvfp4_test_e4m3", "nvfp4_test_e2m1_quotient", "nvfp4_test_e4m3_quotient",
     "nvfp4_test_e4m3_decode", "nvfp4_test_merge", "nvfp4_test_wait_timeout",
@@ -52,7 +52,7 @@ def library() -> ctypes.CDLL:
             L = ctypes.CDLL(LIB_PATH)
             P, I64, I, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
             sig = {
-                "nvfp4_requant": [P, I, P, P, I, F, I64, I64, P, P, P, P],
+                "nvfp4_requant": [P, I, P, P, I, F, I64, I64, P, P, P, P, ctypes.c_size_t, P],
                 "nvfp4_act_quant": [P, I64, I64, P, P, P, P],
                 "nvfp4_gemm": [P, P, P, P, P, P, P, P, I64, I64, I64, P],
                 "bf16_gemm": [P, P, P, P, I64, I64, I64, P],
@@ -70,6 +70,8 @@ def library() -> ctypes.CDLL:
                 fn = getattr(L, name)
                 fn.argtypes = args
                 fn.restype = I
+            L.nvfp4_requant_workspace_bytes.argtypes = [I, I, I64, I64]
+            L.nvfp4_requant_workspace_bytes.restype = ctypes.c_size_t
             L.nvfp4_status_string.argtypes = [I]
             L.nvfp4_status_string.restype = ctypes.c_char_p
             L.nvfp4_version.argtypes = []
@@ -123,9 +125,17 @@ def nvfp4_version() -> int:
     return library().nvfp4_version()
 
 
+def requant_workspace_bytes(w_dtype: int, r: int, N: int, K: int) -> int:
+    """Workspace bytes that select the tensor-core merge of nvfp4_requant (0: n/a)."""
+    return int(library().nvfp4_requant_workspace_bytes(int(w_dtype), int(r), int(N), int(K)))
+
+
 def nvfp4_requant(W, A=None, B=None, alpha: float = 32.0, codes=None, sf=None, s_t=None,
-                  stream=None):
-    """W' = W + (alpha/r) B A, then per-tensor NVFP4.  Returns (codes, sf, s_t)."""
+                  stream=None, workspace=None):
+    """W' = W + (alpha/r) B A, then per-tensor NVFP4.  Returns (codes, sf, s_t).
+
+    ``workspace`` (uint8 CUDA tensor) is the call's scratch; when omitted and the
+    tensor-core merge applies, one of nvfp4_requant_workspace_bytes is allocated."""
     if W.dim() != 2:
         raise ValueError("W must be [N, K]")
     N, K = W.shape
@@ -139,9 +149,15 @@ def nvfp4_requant(W, A=None, B=None, alpha: float = 32.0, codes=None, sf=None, s
     codes = torch.empty(N, K // 2, dtype=torch.uint8, device=dev) if codes is None else codes
     sf = torch.empty(sf_bytes(N, K), dtype=torch.uint8, device=dev) if sf is None else sf
     s_t = torch.empty(1, dtype=torch.float32, device=dev) if s_t is None else s_t
+    if workspace is None and r:
+        need = requant_workspace_bytes(w_dtype, r, N, K)
+        if need:
+            workspace = torch.empty(need, dtype=torch.uint8, device=dev)
+    ws_ptr = _opt(workspace, "workspace", torch.uint8)
+    ws_bytes = 0 if workspace is None else workspace.numel()
     _call("nvfp4_requant", _dev(W, "W"), w_dtype, _opt(A, "A", torch.float32), _opt(B, "B", torch.float32),
           r, ctypes.c_float(alpha), N, K, _dev(codes, "codes", torch.uint8), _dev(sf, "sf", torch.uint8),
-          _dev(s_t, "s_t", torch.float32), _stream(stream))
+          _dev(s_t, "s_t", torch.float32), ws_ptr, ws_bytes, _stream(stream))
     return codes, sf, s_t
 
 

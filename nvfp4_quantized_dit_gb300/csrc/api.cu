@@ -18,8 +18,6 @@ __device__ int g_status_word = 0;
 
 namespace {
 
-constexpr int kMaxDevices = 64;
-
 struct DeviceInfo {
     bool checked = false;
     bool arch_ok = false;
@@ -65,6 +63,7 @@ nvfp4_status resolve(void* stream, LaunchCtx* ctx) {
     ctx->stream = static_cast<cudaStream_t>(stream);
     ctx->status = d.status;
     ctx->num_sms = d.num_sms;
+    ctx->device = dev;
     cudaGetLastError();  // start from a clean error state
     return NVFP4_OK;
 }
@@ -149,9 +148,14 @@ const char* nvfp4_status_string(nvfp4_status s) {
 
 int nvfp4_version(void) { return 100; }
 
+size_t nvfp4_requant_workspace_bytes(int w_dtype, int r, int64_t N, int64_t K) {
+    if (N < 0 || N > kMaxRows || K <= 0 || K % 64 != 0 || K > (1 << 20)) return 0;
+    return requant_tc_workspace_bytes(w_dtype, r, N, K);
+}
+
 nvfp4_status nvfp4_requant(const void* W, int w_dtype, const float* A, const float* B, int r,
                            float alpha, int64_t N, int64_t K, uint8_t* codes, uint8_t* sf,
-                           float* s_t, void* stream) {
+                           float* s_t, void* workspace, size_t workspace_bytes, void* stream) {
     if (w_dtype != NVFP4_W_BF16 && w_dtype != NVFP4_W_FP32) return NVFP4_ERR_SHAPE;
     if (r < 0 || r > 64 || N < 0 || N > kMaxRows || K <= 0 || K % 64 != 0 || K > (1 << 20))
         return NVFP4_ERR_SHAPE;
@@ -168,6 +172,20 @@ nvfp4_status nvfp4_requant(const void* W, int w_dtype, const float* A, const flo
     if (st != NVFP4_OK) return st;
     if (N == 0) return from_cuda(cudaMemsetAsync(s_t, 0, sizeof(float), ctx.stream));
     const float c = merge ? alpha / static_cast<float>(r) : 0.0f;
+    const size_t need = merge ? requant_tc_workspace_bytes(w_dtype, r, N, K) : 0;
+    if (need > 0 && workspace != nullptr && workspace_bytes >= need && !misaligned(workspace, 256) &&
+        !misaligned(B, 16)) {
+        const RequantTcLayout ws = requant_tc_layout(workspace, N, K);
+        RequantTcMaps m;
+        if (!encode_2d(&m.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)K, (uint64_t)N,
+                       (uint64_t)K * 2, 64, 128) ||
+            !encode_2d(&m.bp, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.bp, 128, (uint64_t)N, 256, 64, 128) ||
+            !encode_2d(&m.ap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.ap, 128, (uint64_t)K, 256, 64, 64) ||
+            !encode_2d(&m.af, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, (uint64_t)K, (uint64_t)r,
+                       (uint64_t)K * 4, 128, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return NVFP4_ERR_CUDA;
+        return from_cuda(launch_requant_tc(ctx, m, A, B, workspace, c, N, K, codes, sf, s_t));
+    }
     return from_cuda(launch_requant(ctx, W, w_dtype, merge ? A : nullptr, merge ? B : nullptr,
                                     merge ? r : 0, c, N, K, codes, sf, s_t));
 }

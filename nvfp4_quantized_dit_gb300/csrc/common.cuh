@@ -11,17 +11,74 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "nvfp4rl.h"
 
 namespace nvfp4rl {
 
 // ----------------------------------------------------------------- host side
 
+constexpr int kMaxDevices = 64;
+
 struct LaunchCtx {
     cudaStream_t stream;
     int* status;      // device status word (NVFP4_ERR_TIMEOUT is recorded here)
     int num_sms;
+    int device;       // current device ordinal, < kMaxDevices
 };
+
+// Launch-time occupancy of one kernel, cached per device: the count (co-resident CTAs
+// per SM, or clusters per device) for the dynamic shared-memory size it was last
+// computed for.  Filling an entry also raises the kernel's opt-in shared-memory limit
+// on that device, so a hit needs neither runtime call again.  The cache assumes the
+// device's primary context lives as long as the process.
+struct OccupancyCache {
+    std::atomic<uint64_t> entry[kMaxDevices];  // (smem bytes << 32) | count; 0 = empty
+    int lookup(int dev, size_t smem) const {
+        const uint64_t v = entry[dev].load(std::memory_order_acquire);
+        return (v >> 32) == (uint64_t)smem ? (int)(uint32_t)v : 0;
+    }
+    void store(int dev, size_t smem, int count) {
+        entry[dev].store(((uint64_t)smem << 32) | (uint32_t)count, std::memory_order_release);
+    }
+};
+
+// Co-resident CTAs per SM of `kern` (at least 1) with `threads` threads and `smem` bytes.
+template <typename Kern>
+cudaError_t blocks_per_sm(OccupancyCache& cache, const LaunchCtx& ctx, Kern kern, int threads,
+                          size_t smem, int* out) {
+    int n = cache.lookup(ctx.device, smem);
+    if (n == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem);
+        if (e != cudaSuccess) return e;
+        if (n < 1) n = 1;
+        cache.store(ctx.device, smem, n);
+    }
+    *out = n;
+    return cudaSuccess;
+}
+
+// Co-resident clusters of `kern` for the launch configuration `cfg` (its grid is
+// ignored by the query; block size, shared memory and cluster size count).
+template <typename Kern>
+cudaError_t clusters_per_device(OccupancyCache& cache, const LaunchCtx& ctx, Kern kern,
+                                const cudaLaunchConfig_t& cfg, int* out) {
+    int n = cache.lookup(ctx.device, cfg.dynamicSmemBytes);
+    if (n == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)cfg.dynamicSmemBytes);
+        if (e != cudaSuccess) return e;
+        e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+        if (e != cudaSuccess) return e;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        cache.store(ctx.device, cfg.dynamicSmemBytes, n);
+    }
+    *out = n;
+    return cudaSuccess;
+}
 
 // Implemented per translation unit; each returns cudaSuccess or the launch error.
 cudaError_t launch_act_quant(const LaunchCtx&, const __nv_bfloat16* X, int64_t M, int64_t K,
@@ -29,6 +86,43 @@ cudaError_t launch_act_quant(const LaunchCtx&, const __nv_bfloat16* X, int64_t M
 cudaError_t launch_requant(const LaunchCtx&, const void* W, int w_dtype, const float* A,
                            const float* B, int r, float c, int64_t N, int64_t K, uint8_t* codes,
                            uint8_t* sf, float* s_t);
+// Tensor-core merge (merge_tc.cu): bf16 W, rank 32, 16-byte aligned A and B, and a
+// workspace of requant_tc_workspace_bytes (0 when the path does not apply) laid out by
+// requant_tc_layout: B' [N, 128] bf16, A' [K, 128] bf16, rnorm [N rounded up to 256],
+// cnorm [K / 128 rounded up][4].
+struct RequantTcLayout {
+    uint8_t* bp;
+    uint8_t* ap;
+    float* rnorm;
+    float* cnorm;
+    size_t bytes;
+};
+inline RequantTcLayout requant_tc_layout(void* base, int64_t N, int64_t K) {
+    auto up = [](size_t x) { return (x + 255) & ~static_cast<size_t>(255); };
+    const uintptr_t p = reinterpret_cast<uintptr_t>(base);
+    RequantTcLayout l;
+    size_t off = 0;
+    l.bp = reinterpret_cast<uint8_t*>(p + off);
+    off += up((size_t)N * 256);
+    l.ap = reinterpret_cast<uint8_t*>(p + off);
+    off += up((size_t)K * 256);
+    l.rnorm = reinterpret_cast<float*>(p + off);
+    off += up((size_t)((N + 255) / 256 * 256) * 4);
+    l.cnorm = reinterpret_cast<float*>(p + off);
+    off += up((size_t)((K + 127) / 128) * 16);
+    l.bytes = off;
+    return l;
+}
+// Tensor maps of the merge kernels: W [N, K] bf16 (64 x 128 boxes), B' [N, 128] bf16
+// (64 x 128 boxes), A' [K, 128] bf16 (64 x 64 boxes), all with the 128-byte swizzle;
+// A [32, K] fp32 (128 x 32 boxes).
+struct RequantTcMaps {
+    CUtensorMap w, bp, ap, af;
+};
+size_t requant_tc_workspace_bytes(int w_dtype, int r, int64_t N, int64_t K);
+cudaError_t launch_requant_tc(const LaunchCtx&, const RequantTcMaps& maps, const float* A,
+                              const float* B, void* workspace, float c, int64_t N, int64_t K,
+                              uint8_t* codes, uint8_t* sf, float* s_t);
 cudaError_t launch_test_merge(const LaunchCtx&, const void* W, int w_dtype, const float* A,
                               const float* B, int r, float c, int64_t N, int64_t K, float* out);
 cudaError_t launch_select(const LaunchCtx&, const float* rewards, int P, int N, int K,
@@ -329,6 +423,14 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// As mbar_arrive_cluster, with release at cluster scope: for arrivals that publish
+// ordinary shared-memory writes (made visible to the async proxy by
+// fence_proxy_async_smem and gathered by a CTA barrier) to a waiter in the peer CTA.
+__device__ __forceinline__ void mbar_arrive_cluster_release(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
 // Tile load into this CTA's shared memory whose completion is counted on an mbarrier
 // of either CTA of the pair (`bar_cluster` is a shared::cluster address).
 __device__ __forceinline__ void tma_load_2d_pair(const CUtensorMap* map, uint32_t bar_cluster,
@@ -587,6 +689,13 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
         "r"(r[15])
         : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(
+                     taddr),
+                 "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_st_wait() {

@@ -516,10 +516,7 @@ template <bool kFP4>
 cudaError_t run_gemm(const LaunchCtx& ctx, const CUtensorMap& ta, const CUtensorMap& tb,
                      const CUtensorMap& tsfa, const CUtensorMap& tsfb, const CUtensorMap& ty,
                      const GemmArgs& args) {
-    // Set on every call: the attribute belongs to the current device's context.
-    cudaError_t e = cudaFuncSetAttribute(gemm_kernel<kFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)Cfg<kFP4>::kSmemBytes);
-    if (e != cudaSuccess) return e;
+    static OccupancyCache occupancy;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -534,9 +531,8 @@ cudaError_t run_gemm(const LaunchCtx& ctx, const CUtensorMap& ta, const CUtensor
     // Co-resident pairs (one CTA per SM), capped by the work available.
     cfg.gridDim = dim3((unsigned)(ctx.num_sms / kPair * kPair), 1, 1);
     int max_clusters = 0;
-    e = cudaOccupancyMaxActiveClusters(&max_clusters, gemm_kernel<kFP4>, &cfg);
+    const cudaError_t e = clusters_per_device(occupancy, ctx, gemm_kernel<kFP4>, cfg, &max_clusters);
     if (e != cudaSuccess) return e;
-    if (max_clusters < 1) return cudaErrorInvalidConfiguration;
     const int64_t num_m = (args.M + BM - 1) / BM;
     const int64_t pairs = (num_m + kPair - 1) / kPair * ((args.N + BN - 1) / BN);
     const int64_t clusters = pairs < max_clusters ? pairs : max_clusters;

@@ -1,0 +1,801 @@
+// LoRA merge on the tensor cores with certified-exact NVFP4 decisions.
+//
+// nvfp4_requant's result is defined by the fp32 fma chain of the merge
+// (acc = +0; acc = fma(B[n,j], A[j,k], acc), j = 0..r-1; w' = fma(c, acc, W[n,k]))
+// followed by the NVFP4 quantization of w' (Sol-RL project page, "Two-Stage
+// Pipeline", Stage 2: the updated weights are quantized again; AI Trends summary:
+// LoRA rank 32).  On CUDA cores the chain costs 32 fp32 FMAs per element and pass,
+// more than the weights' memory traffic.  Here the rank-32 product P = B A is taken
+// from the tensor cores instead, from two-part bf16 splits of both factors
+// (b = b0 + b1 and a = a0 + a1 with b0 = bf16(b), b1 = bf16(b - b0); b - b0 is exact),
+// as one bf16 GEMM with K' = 4 x 32 whose operands are [b0 b0 b1 b1] and [a0 a1 a0 a1]:
+//     P~[n,k] = sum_j (b0 a0 + b0 a1 + b1 a0 + b1 a1)[n,j,k],     w~ = fma(c, P~, W).
+//
+// The bound.  For a thread's row n and 64 columns, with b = ||B[n,:]||_2 and
+// a = max_k ||A[:,k]||_2 (upper bounds),
+//     E = |c| (2^-14 b a + 2^-120 (b + a) + 2^-117)      (rounded up, at least 2^-149)
+// covers |c| |P(chain) - P~|.  Relative part, by Cauchy-Schwarz relative to b a: the
+// chain's own rounding (r 2^-24 = 2^-19), the dropped split remainder (b1 and a1 are
+// bf16 roundings: 2 x 2^-9 x 2^-8 plus 2^-18, about 2^-16.4) and the tensor cores'
+// accumulation (8 MMAs of 16 exact bf16 products in fp32, at most 17 x 2^-23 of the
+// magnitudes each, 2^-15.9) sum to about 2^-15.1; the factor of two left covers the
+// roundings of the final fma (2^-23 relative, taken up by the 2^-19 nudges below) and
+// the second-order terms.  Absolute part, should the tensor cores flush subnormals:
+// a flushed split part (below 2^-126) loses at most 2^-124 sum_j |a_j| <= 2^-121.5 a
+// (or b), flushed products and partial sums at most 128 x 2^-126.  The chain's own
+// subnormal roundings are far below 2^-117.  Every decision is taken on the interval
+// [|w~| - E, |w~| + E] (with the final fma's own rounding covered by 2^-19 / 2^-21
+// nudges of the reciprocals and factors):
+//   * tensor amax (pass 1): a warp's maximum is among its elements whose upper bound
+//     reaches the largest lower bound of the warp; those are recomputed with the exact
+//     chain and the warp's maximum of them goes to the tensor amax;
+//   * block scale (pass 2): the E4M3 codes of both ends of [bam - E, bam + E] must agree,
+//     else the block's 16 values are recomputed exactly;
+//   * element code (pass 2): the E2M1 codes of both ends must agree (an interval that
+//     holds zero gives codes of both signs and never agrees), else that element alone
+//     is recomputed.
+// So codes, scales and s_t are bit-identical to the fp32 chain's.  The exact chain
+// reads the fp32 factors from shared memory.
+//
+// Kernels.  A split kernel writes the operands of the merge GEMM once per call into
+// the caller's workspace: B' = [b0 b0 b1 b1] per row of B, A' = [a0 a1 a0 a1] per
+// column of A (bf16, 256 bytes per row), an upper bound of every row norm of B and,
+// per 64 columns, the largest column norm of A.  Then both passes run as persistent
+// clusters of two CTAs; a pair tile is 256 weight rows (128 per CTA) x 128 columns,
+// walked k-strip first, so the rows of B usually stay the same from one tile to the
+// next.  Per CTA, 18 warps:
+//   warp 0      TMA into three rings: W tiles (128 x 128 bf16; 2 slots, freed as soon
+//               as every epilogue warp has copied its rows into registers), the MMA
+//               operands (2 slots: this CTA's 64 rows of A', and B' when the rows
+//               change; completing on the even CTA's barrier, freed by the MMAs) and
+//               the fp32 strip of A for the exact chain (4 slots);
+//   warp 1      tensor-memory allocation; lane 0 of the even CTA issues the 8 pair MMAs
+//               (kind::f16, M = 256, N = 128) into a double-buffered accumulator;
+//   warps 2-17  epilogue: four warps per tensor-memory lane quarter, 32 columns each (a
+//               thread owns one weight row): accumulator + W -> w~ -> pass 1 amax or
+//               pass 2 codes and scales, stored straight to global memory.  The fp32
+//               rows of B for the exact chain sit in tensor memory next to the
+//               accumulators (lane = row), written by the epilogue warps when the rows
+//               change; only the rare uncertain elements read them and the A strip.
+// Every mbarrier wait is bounded (mbar_wait).
+#include "common.cuh"
+
+namespace nvfp4rl {
+namespace {
+
+constexpr int kTM = 128;        // weight rows per CTA
+constexpr int kTK = 128;        // weight columns per pair tile (64 per CTA in the MMA's B)
+constexpr int kPair = 2;
+constexpr int kRank = 32;       // the rank this path serves (A [32, K], B [N, 32])
+constexpr int kJp = 4 * kRank;  // K' of the merge GEMM
+constexpr int kEpiWarp0 = 2, kEpiWarps = 16;
+constexpr int kCols = 32;       // columns per epilogue warp
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+constexpr uint32_t kOpABytes = kTM * kJp * 2;            // 32 KB: B' rows, two 64-column atoms
+constexpr uint32_t kOpBBytes = (kTK / kPair) * kJp * 2;  // 16 KB: A' rows, two 64-column atoms
+constexpr uint32_t kWBox = kTM * 128;                    // 16 KB: 128 rows x 64 bf16
+constexpr uint32_t kWBytes = 2 * kWBox;                  // 32 KB: 128 rows x 128 bf16
+constexpr uint32_t kBfBytes = kTM * kRank * 4;           // 16 KB: fp32 rows of B
+constexpr uint32_t kAfBytes = kRank * kTK * 4;           // 16 KB: fp32 strip of A
+constexpr int kXSlots = 4;                               // fp32 strips of A in flight
+constexpr uint32_t kMiscBytes = 256;
+constexpr uint32_t kSmemBytes =
+    1024 + 2 * (kOpABytes + kOpBBytes + kWBytes) + kXSlots * kAfBytes + kMiscBytes;
+// Tensor memory: two accumulators of 128 columns, then two buffers of 32 columns for
+// the fp32 rows of B (lane = row).
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kBrowCol = 2 * kTK;
+constexpr uint16_t kBothCtas = 0x3;
+constexpr uint16_t kEvenCta = 0x1;
+constexpr uint64_t kWaitLimitNs = 4000000000ull;
+constexpr uint64_t kDrainLimitNs = 200000000ull;
+constexpr int kModeAmax = 0, kModeQuant = 1;
+constexpr int kSplitThreads = 256;
+constexpr int kSplitRows = kSplitThreads / 4;  // rows of B per split block (4 threads a row)
+constexpr int kSplitCols = kSplitThreads / 4;  // columns of A per split block (4 threads a column)
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// kind::f16, bf16 A and B, fp32 accumulator, K-major, N = 128, M = 256 (pair).
+constexpr uint32_t idesc_merge() {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kTK >> 3) << 17) |
+           ((uint32_t)(kTM * kPair >> 4) << 24);
+}
+
+struct TcArgs {
+    float c;
+    int N, K, rows_pad;
+    uint8_t* codes;
+    uint8_t* sf;
+    float* s_t;  // pass 1: amax accumulator (fp32 bits, atomicMax); pass 2: reads it
+    const float* rnorm;  // [N padded to 256] upper bounds of ||B[n,:]||_2 (0 past N)
+    const float* B;      // [N, 32] fp32: the rows the exact chain reads
+    const float* cnorm;  // [K/128][4]: per 128-column strip, the largest ||A[:,k]||_2
+                         // of each 64-column half (upper bounds), then 2 unused
+    int* status;
+    int zero;    // 0 (a value the compiler cannot see; used for data dependencies)
+    int nks;     // 128-column strips
+    int tiles;   // 256-row blocks x nks, row block major
+};
+
+__device__ __forceinline__ float warp_max_f(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xFFFFFFFFu, v, o));
+    return v;
+}
+
+// Upper bound of the 2-norm from a sum of 32 squares accumulated with round-to-nearest
+// fmas (relative error below 2^-19; the absolute term covers underflow).
+__device__ __forceinline__ float norm_ub(float sumsq) {
+    return __fsqrt_ru(__fmaf_ru(sumsq, 1.0f + 0x1p-17f, 0x1p-143f));
+}
+
+__device__ __forceinline__ uint32_t bf16_pair(float lo, float hi) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Two-part bf16 split of 8 values: p0 = bf16(v), p1 = bf16(v - p0).
+__device__ __forceinline__ void split8(const float* v, uint4& p0, uint4& p1) {
+    float h[8], l[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        h[i] = __bfloat162float(__float2bfloat16_rn(v[i]));
+        l[i] = v[i] - h[i];
+    }
+    p0 = make_uint4(bf16_pair(h[0], h[1]), bf16_pair(h[2], h[3]), bf16_pair(h[4], h[5]),
+                    bf16_pair(h[6], h[7]));
+    p1 = make_uint4(bf16_pair(l[0], l[1]), bf16_pair(l[2], l[3]), bf16_pair(l[4], l[5]),
+                    bf16_pair(l[6], l[7]));
+}
+
+// Operands of the merge GEMM, four threads per row of B or column of A (8 values
+// each).  Blocks [0, nb_rows) take 64 rows of B: B'[n] = [b0 b0 b1 b1] and rnorm[n]
+// (rnorm is 0 for the padding rows up to rows_pad256).  The other blocks take 64
+// columns of A: A'[k] = [a0 a1 a0 a1] and the block's largest column norm.  Block 0
+// also clears the amax accumulator s_t.
+__global__ void __launch_bounds__(kSplitThreads)
+    merge_split_kernel(const float* __restrict__ A, const float* __restrict__ B, int N, int K,
+                       int rows_pad256, int nb_rows, uint8_t* __restrict__ Bp,
+                       uint8_t* __restrict__ Ap, float* __restrict__ rnorm,
+                       float* __restrict__ cnorm, float* __restrict__ s_t) {
+    __shared__ float red[kSplitThreads];
+    __shared__ float red2[kSplitCols / 32];
+    const int tid = (int)threadIdx.x;
+    if (blockIdx.x == 0 && tid == 0) *s_t = 0.0f;
+    float v[8];
+    if ((int)blockIdx.x < nb_rows) {
+        const int n = (int)blockIdx.x * kSplitRows + (tid >> 2), g = tid & 3;
+        float s2 = 0.0f;
+        if (n < N) {
+            const float4* src = reinterpret_cast<const float4*>(B + (int64_t)n * kRank + 8 * g);
+            const float4 x0 = src[0], x1 = src[1];
+            v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
+            v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s2 = __fmaf_rn(v[j], v[j], s2);
+            uint4 p0, p1;
+            split8(v, p0, p1);
+            uint4* dst = reinterpret_cast<uint4*>(Bp + (int64_t)n * (kJp * 2));
+            dst[g] = p0;
+            dst[4 + g] = p0;
+            dst[8 + g] = p1;
+            dst[12 + g] = p1;
+        }
+        // The four partial sums of the row (lanes 4r .. 4r + 3 of the warp).
+        s2 += __shfl_xor_sync(0xFFFFFFFFu, s2, 1);
+        s2 += __shfl_xor_sync(0xFFFFFFFFu, s2, 2);
+        if (g == 0 && n < rows_pad256) rnorm[n] = n < N ? norm_ub(s2) : 0.0f;
+    } else {
+        const int k0 = ((int)blockIdx.x - nb_rows) * kSplitCols;
+        const int kk = tid & (kSplitCols - 1), g = tid / kSplitCols;
+        const int k = k0 + kk;
+        float s2 = 0.0f;
+        if (k < K) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) v[j] = A[(int64_t)(8 * g + j) * K + k];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) s2 = __fmaf_rn(v[j], v[j], s2);
+            uint4 p0, p1;
+            split8(v, p0, p1);
+            uint4* dst = reinterpret_cast<uint4*>(Ap + (int64_t)k * (kJp * 2));
+            dst[g] = p0;
+            dst[4 + g] = p1;
+            dst[8 + g] = p0;
+            dst[12 + g] = p1;
+        }
+        red[tid] = s2;
+        __syncthreads();
+        if (tid < kSplitCols) {
+            const float t = (red[tid] + red[tid + kSplitCols]) + (red[tid + 2 * kSplitCols] + red[tid + 3 * kSplitCols]);
+            const float nrm = warp_max_f(k < K ? norm_ub(t) : 0.0f);
+            if ((tid & 31) == 0) red2[tid >> 5] = nrm;
+        }
+        __syncthreads();
+        if (tid == 0 && k0 < K) cnorm[(k0 >> 7) * 4 + ((k0 >> 6) & 1)] = fmaxf(red2[0], red2[1]);
+    }
+}
+
+// Element e (0..31) of 32 bf16 held as 16 packed pairs, as fp32.
+__device__ __forceinline__ float bf16_sel(const uint4 (&w)[4], int e) {
+    const uint4 v = (e >> 3) == 0 ? w[0] : (e >> 3) == 1 ? w[1] : (e >> 3) == 2 ? w[2] : w[3];
+    const int p = (e >> 1) & 3;
+    const uint32_t pr = p == 0 ? v.x : p == 1 ? v.y : p == 2 ? v.z : v.w;
+    return __uint_as_float((e & 1) ? (pr & 0xFFFF0000u) : (pr << 16));
+}
+
+// The library's merged value of one element (the fp32 fma chain, in order): b = the
+// element's row of B (fp32 bits), column kt of the fp32 strip of A (32 x kTK), weight w.
+__device__ __forceinline__ float exact_value(const uint32_t (&b)[kRank], const float* af, int kt,
+                                             float c, float w) {
+    float a[kRank];
+#pragma unroll
+    for (int j = 0; j < kRank; ++j) a[j] = af[j * kTK + kt];
+    float acc = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kRank; ++j) acc = __fmaf_rn(__uint_as_float(b[j]), a[j], acc);
+    return __fmaf_rn(c, acc, w);
+}
+
+template <int kMode>
+__global__ void __launch_bounds__(kThreads, 1)
+    merge_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                    const __grid_constant__ CUtensorMap tmap_bp,
+                    const __grid_constant__ CUtensorMap tmap_ap,
+                    const __grid_constant__ CUtensorMap tmap_af, const TcArgs args) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* opA = smem;                   // [2]: B' rows of this CTA
+    uint8_t* opB = opA + 2 * kOpABytes;    // [2]: A' rows of this CTA's 64 columns
+    uint8_t* wring = opB + 2 * kOpBBytes;  // [2]: W tiles
+    uint8_t* xring = wring + 2 * kWBytes;  // [kXSlots]: fp32 strips of A
+    uint64_t* bars = reinterpret_cast<uint64_t*>(xring + kXSlots * kAfBytes);
+    uint64_t* w_full = bars;           // [2]
+    uint64_t* w_empty = bars + 2;      // [2] the 16 epilogue warps have copied their rows
+    uint64_t* op_full = bars + 4;      // [2] even CTA: both CTAs' operands have landed
+    uint64_t* op_empty = bars + 6;     // [2] the pair's MMAs have read the operands
+    uint64_t* tmem_full = bars + 8;    // [2]
+    uint64_t* tmem_empty = bars + 10;  // [2] even CTA
+    uint64_t* brow_bar = bars + 12;    // [4] per lane quarter: its 4 warps stored B rows
+    uint64_t* x_full = bars + 16;      // [kXSlots]
+    uint64_t* x_empty = bars + 16 + kXSlots;  // [kXSlots] the 16 epilogue warps
+    uint64_t* drain = bars + 16 + 2 * kXSlots;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = (int)(blockIdx.x / kPair), npairs = (int)(gridDim.x / kPair);
+    const int t_begin = (int)((int64_t)pair * args.tiles / npairs);
+    const int t_end = (int)((int64_t)(pair + 1) * args.tiles / npairs);
+    // Tile t of the pair's range: row block t / nks, strip t % nks (walked strip first).
+    const int nks = args.nks;
+    const int nb_begin = t_begin / nks, ks_begin = t_begin - nb_begin * nks;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&w_full[i], 1);
+            mbar_init(&w_empty[i], kEpiWarps);
+            mbar_init(&op_full[i], 1);
+            mbar_init(&op_empty[i], 1);
+            mbar_init(&tmem_full[i], 1);
+            mbar_init(&tmem_empty[i], kEpiWarps * kPair);
+        }
+        for (int i = 0; i < 4; ++i) mbar_init(&brow_bar[i], kEpiWarps / 4);
+        for (int i = 0; i < kXSlots; ++i) {
+            mbar_init(&x_full[i], 1);
+            mbar_init(&x_empty[i], kEpiWarps);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmap_w);
+        prefetch_tmap(&tmap_bp);
+        prefetch_tmap(&tmap_ap);
+        prefetch_tmap(&tmap_af);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();
+    tc_fence_after_sync();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA (both CTAs)
+            const uint32_t op_full_even = map_to_rank(smem_u32(op_full), 0);
+            int nb = nb_begin, ks = ks_begin, nb_m1 = -1, nb_m2 = -1;  // row blocks of tiles i-1, i-2
+            int i = 0;
+            for (int t = t_begin; t < t_end; ++t, ++i) {
+                const int b = i & 1, xs = i % kXSlots;
+                const uint32_t ph = (uint32_t)((i >> 1) & 1) ^ 1u;
+                // Operand buffer b holds the B' rows of tile i - 2: reload if they differ.
+                const bool rows = nb != nb_m2;
+                const int row0 = nb * (kTM * kPair) + (int)rank * kTM;
+                // W (the stream from HBM).
+                if (!mbar_wait(&w_empty[b], ph, args.status, abort_flag, kWaitLimitNs)) break;
+                uint8_t* wt = wring + b * kWBytes;
+                mbar_arrive_expect_tx(&w_full[b], kWBytes);
+                tma_load_2d(&tmap_w, &w_full[b], wt, ks * kTK, row0);
+                tma_load_2d(&tmap_w, &w_full[b], wt + kWBox, ks * kTK + 64, row0);
+                // The MMA operands, counted on the even CTA's barrier.
+                if (!mbar_wait(&op_empty[b], ph, args.status, abort_flag, kWaitLimitNs)) break;
+                if (leader)
+                    mbar_arrive_expect_tx(&op_full[b], kPair * (kOpBBytes + (rows ? kOpABytes : 0u)));
+                const uint32_t bar = op_full_even + 8u * (uint32_t)b;
+                const int arow = ks * kTK + (int)rank * (kTK / kPair);
+                uint8_t* ob = opB + b * kOpBBytes;
+                tma_load_2d_pair(&tmap_ap, bar, ob, 0, arow);
+                tma_load_2d_pair(&tmap_ap, bar, ob + kOpBBytes / 2, 64, arow);
+                if (rows) {
+                    uint8_t* oa = opA + b * kOpABytes;
+                    tma_load_2d_pair(&tmap_bp, bar, oa, 0, row0);
+                    tma_load_2d_pair(&tmap_bp, bar, oa + kOpABytes / 2, 64, row0);
+                }
+                // The fp32 strip of A: the slot's previous strip has landed (its phase is
+                // complete) and the epilogue is done with it.
+                const uint32_t xph = (uint32_t)((i / kXSlots) & 1) ^ 1u;
+                if (!mbar_wait(&x_full[xs], xph, args.status, abort_flag, kWaitLimitNs) ||
+                    !mbar_wait(&x_empty[xs], xph, args.status, abort_flag, kWaitLimitNs))
+                    break;
+                mbar_arrive_expect_tx(&x_full[xs], kAfBytes);
+                tma_load_2d(&tmap_af, &x_full[xs], xring + xs * kAfBytes, ks * kTK, 0);
+                nb_m2 = nb_m1;
+                nb_m1 = nb;
+                if (++ks == nks) {
+                    ks = 0;
+                    ++nb;
+                }
+            }
+            if (!*abort_flag) {
+                // Tail: the last MMAs' releases of the operand buffers, and the last strips
+                // of A, land before exit.
+                for (int j = (i >= 2 ? i - 2 : 0); j < i; ++j)
+                    if (!mbar_wait(&op_empty[j & 1], (uint32_t)((j >> 1) & 1), args.status,
+                                   abort_flag, kWaitLimitNs))
+                        break;
+                for (int j = (i >= kXSlots ? i - kXSlots : 0); j < i; ++j)
+                    if (!mbar_wait(&x_full[j % kXSlots], (uint32_t)((j / kXSlots) & 1), args.status,
+                                   abort_flag, kWaitLimitNs))
+                        break;
+            }
+            if (*abort_flag) {
+                // Let copies already issued land before the pair tears down.
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && leader) {
+            // ------------------------------------------------ MMA issuer (even CTA)
+            const uint32_t idesc = idesc_merge();
+            bool any = false;
+            for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
+                const int b = i & 1;
+                if (!mbar_wait<true>(&op_full[b], (uint32_t)((i >> 1) & 1), args.status,
+                                     abort_flag, kWaitLimitNs) ||
+                    !mbar_wait<true>(&tmem_empty[b], ((i >> 1) & 1) ^ 1u, args.status,
+                                     abort_flag, kWaitLimitNs))
+                    break;
+                tc_fence_after_sync();
+                const uint64_t ad = smem_desc(smem_u32(opA + b * kOpABytes), 16, 1024, kLayoutSw128);
+                const uint64_t bd = smem_desc(smem_u32(opB + b * kOpBBytes), 16, 1024, kLayoutSw128);
+#pragma unroll
+                for (int kk = 0; kk < kJp / 16; ++kk) {
+                    // 16 bf16 (32 bytes) per step, 4 steps per 64-column atom.
+                    const uint64_t ao = (uint64_t)((kk >> 2) * ((kOpABytes / 2) >> 4) + (kk & 3) * 2);
+                    const uint64_t bo = (uint64_t)((kk >> 2) * ((kOpBBytes / 2) >> 4) + (kk & 3) * 2);
+                    mma_bf16_pair(tmem_base + (uint32_t)(b * kTK), ad + ao, bd + bo, idesc,
+                                  kk > 0 ? 1u : 0u);
+                }
+                any = true;
+                mma_commit_pair_multicast(&op_empty[b], kBothCtas);
+                mma_commit_pair_multicast(&tmem_full[b], kBothCtas);
+            }
+            if (*abort_flag && any) {
+                mma_commit_pair_multicast(drain, kEvenCta);
+                int dummy = 0;
+                mbar_wait(drain, 0, args.status, &dummy, kDrainLimitNs);
+            }
+        }
+    } else {
+        // ------------------------------------------------ epilogue (warps 2-17, both CTAs)
+        const int q = warp & 3;                             // tensor-memory lane quarter
+        const int chunk = (warp - kEpiWarp0) >> 2;          // 0..3
+        const int kt0 = chunk * kCols;                      // this warp's columns in the tile
+        const int rloc = q * 32 + lane;                     // this thread's row in the CTA's 128
+        const uint32_t tlane = (uint32_t)(q * 32) << 16;
+        const uint32_t tmem_empty_even = map_to_rank(smem_u32(tmem_empty), 0);
+        const float c = args.c, ac = fabsf(args.c);
+        float s = 0.0f, d = 0.0f, idlo = 0.0f, idhi = 0.0f;
+        bool d_fast = false;
+        if (kMode == kModeQuant) {
+            const float amax = *reinterpret_cast<volatile const float*>(args.s_t);
+            s = __fdiv_rn(amax, kAmaxDiv);
+            d = __fmul_rn(6.0f, s);
+            d_fast = fast_recip_ok(d);
+            const float rd = d_fast ? recip_approx(d) : 0.0f;
+            idlo = __fmul_rd(rd, 1.0f - 0x1p-19f);
+            idhi = __fmul_ru(rd, 1.0f + 0x1p-19f);
+        }
+        int nb = nb_begin, ks = ks_begin;
+        // The norms for E (global, read one tile ahead) and, in pass 1, the running lower
+        // bound of the tensor amax (any value s_t has held is one), read at the end of a
+        // tile for use in the next.
+        float rb_next = 0.0f, ra_next = 0.0f;
+        if (t_begin < t_end) {
+            const int k = ks * kTK + kt0;
+            rb_next = __ldg(args.rnorm + nb * (kTM * kPair) + (int)rank * kTM + rloc);
+            ra_next = k < args.K ? __ldg(args.cnorm + (k >> 7) * 4 + ((k >> 6) & 1)) : 0.0f;
+        }
+        float st_now = 0.0f, st_next = 0.0f;
+        int brow_nb = -1, brow_n = 0;  // row block whose B rows are in tensor memory; changes
+        for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
+            const int b = i & 1, xs = i % kXSlots;
+            const uint32_t ph = (uint32_t)((i >> 1) & 1);
+            const int n = nb * (kTM * kPair) + (int)rank * kTM + rloc;
+            const int k0 = ks * kTK + kt0;        // this warp's first column in W
+            const bool row_ok = n < args.N;
+            const bool col_ok = k0 < args.K;      // K is a multiple of 64: all 32 columns or none
+            const float rb = rb_next, ra = ra_next;
+            int nb1 = nb, ks1 = ks + 1;
+            if (ks1 == nks) {
+                ks1 = 0;
+                ++nb1;
+            }
+            if (t + 1 < t_end) {
+                const int k = ks1 * kTK + kt0;
+                rb_next = __ldg(args.rnorm + nb1 * (kTM * kPair) + (int)rank * kTM + rloc);
+                ra_next = k < args.K ? __ldg(args.cnorm + (k >> 7) * 4 + ((k >> 6) & 1)) : 0.0f;
+            }
+            // New rows: this warp's 8 of the 32 columns of the rows' fp32 B into the next
+            // tensor-memory buffer; the quarter's 4 warps meet on brow_bar.
+            if (nb != brow_nb) {
+                uint32_t bv[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+                if (row_ok) {
+                    const uint4* src = reinterpret_cast<const uint4*>(args.B + (int64_t)n * kRank + 8 * chunk);
+                    const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
+                    bv[0] = v0.x; bv[1] = v0.y; bv[2] = v0.z; bv[3] = v0.w;
+                    bv[4] = v1.x; bv[5] = v1.y; bv[6] = v1.z; bv[7] = v1.w;
+                }
+                tmem_st_32x32b_x8(tmem_base + tlane + kBrowCol + 32u * (uint32_t)(brow_n & 1) + 8u * (uint32_t)chunk, bv);
+                tmem_st_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&brow_bar[q]);
+                const bool ok = mbar_wait(&brow_bar[q], (uint32_t)(brow_n & 1), args.status, abort_flag,
+                                          kWaitLimitNs);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                tc_fence_after_sync();
+                brow_nb = nb;
+                ++brow_n;
+            }
+            const uint32_t tbrow = tmem_base + tlane + kBrowCol + 32u * (uint32_t)((brow_n - 1) & 1);
+            // The accumulator's 32 columns (released at once) and this thread's 32 weights.
+            bool ok = mbar_wait(&tmem_full[b], ph, args.status, abort_flag, kWaitLimitNs) &&
+                      mbar_wait(&w_full[b], ph, args.status, abort_flag, kWaitLimitNs);
+            if (!__all_sync(0xFFFFFFFFu, ok)) break;
+            tc_fence_after_sync();
+            uint32_t acc[32];
+            tmem_ld_32x32b_x32(tmem_base + tlane + (uint32_t)(b * kTK + kt0), acc);
+            uint4 wr[4];
+            {
+                const uint8_t* wb = wring + b * kWBytes + (kt0 >> 6) * kWBox + rloc * 128;
+                const int u0 = (kt0 & 63) >> 3;
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    wr[u] = *reinterpret_cast<const uint4*>(wb + (((u0 + u) ^ (rloc & 7)) << 4));
+            }
+            tmem_ld_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tmem_empty_even + 8u * (uint32_t)b);
+            // w~ = fma(c, P~, W) for the 32 columns.
+            float wv[kCols];
+            {
+                const float2 cc = make_float2(c, c);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const uint32_t rw[4] = {wr[u].x, wr[u].y, wr[u].z, wr[u].w};
+#pragma unroll
+                    for (int p = 0; p < 4; ++p) {
+                        const int e = 8 * u + 2 * p;
+                        const float2 y = __ffma2_rn(
+                            cc, make_float2(__uint_as_float(acc[e]), __uint_as_float(acc[e + 1])),
+                            make_float2(__uint_as_float(rw[p] << 16), __uint_as_float(rw[p] & 0xFFFF0000u)));
+                        wv[e] = y.x;
+                        wv[e + 1] = y.y;
+                    }
+                }
+            }
+            // The W slot goes back to the producer only after every lane's shared-memory
+            // reads of it have returned: the vote reads a value computed from all four
+            // loads in every lane, and the arrival's address depends on the vote (its
+            // offset is 0: args.zero == 0).  A proxy fence here would also wait for the
+            // previous tile's global stores.
+            {
+                const uint32_t dep = (__float_as_uint(wv[7]) ^ __float_as_uint(wv[15]) ^
+                                      __float_as_uint(wv[23]) ^ __float_as_uint(wv[31])) &
+                                     (uint32_t)args.zero;
+                const uint32_t off = __any_sync(0xFFFFFFFFu, dep != 0u) ? 1u : 0u;
+                if (lane == 0) mbar_arrive(&w_empty[b] + off);
+            }
+            // E for this row and these columns, every step rounded up.
+            float E;
+            {
+                const float rel = __fmul_ru(__fmul_ru(ac, 0x1p-14f), __fmul_ru(rb, ra));
+                const float abs_ = __fmul_ru(ac, __fmaf_ru(0x1p-120f, __fadd_ru(rb, ra), 0x1p-117f));
+                E = fmaxf(__fadd_ru(rel, abs_), 0x1p-149f);
+            }
+            const float* af = reinterpret_cast<const float*>(xring + xs * kAfBytes);
+            const uint32_t xph = (uint32_t)((i / kXSlots) & 1);
+            bool x_read = false;  // warp-uniform: the exact chain read the strip of A
+
+            if (kMode == kModeAmax) {
+                float m = 0.0f;
+#pragma unroll
+                for (int e = 0; e < kCols; ++e) m = fmaxf(m, fabsf(wv[e]));
+                const bool in = row_ok && col_ok;
+                // A lower bound of the tensor amax from this warp's elements.
+                const float lo = warp_max_f(in ? __fsub_rd(__fmul_rd(m, 1.0f - 0x1p-21f), E) : 0.0f);
+                st_now = fmaxf(st_now, st_next);
+                const float thr = fmaxf(lo, st_now);
+                // Only elements whose upper bound reaches thr can be the maximum.
+                const bool cand = in && __fadd_ru(__fmul_ru(m, 1.0f + 0x1p-21f), E) >= thr;
+                float em = 0.0f;
+                if (__any_sync(0xFFFFFFFFu, cand)) {
+                    uint32_t mask = 0u;
+#pragma unroll
+                    for (int e = 0; e < kCols; ++e)
+                        mask |= (__fadd_ru(__fmul_ru(fabsf(wv[e]), 1.0f + 0x1p-21f), E) >= thr ? 1u : 0u) << e;
+                    if (!cand) mask = 0u;
+                    ok = mbar_wait(&x_full[xs], xph, args.status, abort_flag, kWaitLimitNs);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                    x_read = true;
+                    uint32_t bq[kRank];
+                    tmem_ld_32x32b_x32(tbrow, bq);
+                    tmem_ld_wait();
+#pragma unroll 1
+                    while (mask != 0u) {
+                        const int e = __ffs((int)mask) - 1;
+                        mask &= mask - 1u;
+                        em = fmaxf(em, fabsf(exact_value(bq, af, kt0 + e, c, bf16_sel(wr, e))));
+                    }
+                    em = warp_max_f(em);
+                }
+                const float best = fmaxf(em, lo);
+                // |W'| >= 0: the fp32 bit patterns order like the values.
+                if (lane == 0 && best > st_now)
+                    atomicMax(reinterpret_cast<unsigned int*>(args.s_t), __float_as_uint(best));
+                st_next = *reinterpret_cast<volatile const float*>(args.s_t);
+            } else {
+                uint32_t cw[4], diff[4], sfc[2];
+                float den[2];
+                bool cert[2];
+#pragma unroll
+                for (int bk = 0; bk < 2; ++bk) {
+                    const float* x = wv + 16 * bk;
+                    float bam = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) bam = fmaxf(bam, fabsf(x[e]));
+                    // Block scale: both ends of [bam - E, bam + E] must give the same code.
+                    // Rows past N are scale padding (not part of W): scale 0, no codes.
+                    const bool scaled = d > 0.0f && row_ok;
+                    const uint32_t slo = cvt_e4m3(__fmul_rn(fmaxf(__fsub_rd(bam, E), 0.0f), idlo));
+                    const uint32_t shi = cvt_e4m3(__fmul_rn(__fadd_ru(bam, E), idhi));
+                    cert[bk] = !scaled || (d_fast && slo == shi);
+                    sfc[bk] = scaled ? shi : 0u;
+                    den[bk] = __fmul_rn(e4m3_value(sfc[bk]), s);
+                    const bool live = den[bk] > 0.0f;
+                    const bool fast = fast_recip_ok(den[bk]);
+                    const float rr = fast ? recip_approx(den[bk]) : 0.0f;
+                    const float2 rlo = make_float2(__fmul_rd(rr, 1.0f - 0x1p-19f), __fmul_rd(rr, 1.0f - 0x1p-19f));
+                    const float2 rhi = make_float2(__fmul_ru(rr, 1.0f + 0x1p-19f), __fmul_ru(rr, 1.0f + 0x1p-19f));
+                    // Element codes: both ends of [|w~| - E, |w~| + E], with w~'s sign.
+                    float lo16[16], hi16[16];
+#pragma unroll
+                    for (int e = 0; e < 16; e += 2) {
+                        const float2 xv = make_float2(x[e], x[e + 1]);
+                        const float2 sE = make_float2(copysignf(E, x[e]), copysignf(E, x[e + 1]));
+                        const float2 l = __fmul2_rn(__ffma2_rn(make_float2(-1.0f, -1.0f), sE, xv), rlo);
+                        const float2 h = __fmul2_rn(__fadd2_rn(xv, sE), rhi);
+                        lo16[e] = l.x;
+                        lo16[e + 1] = l.y;
+                        hi16[e] = h.x;
+                        hi16[e + 1] = h.y;
+                    }
+                    const uint32_t l0 = cvt_e2m1x8(lo16[0], lo16[1], lo16[2], lo16[3], lo16[4], lo16[5], lo16[6], lo16[7]);
+                    const uint32_t l1 = cvt_e2m1x8(lo16[8], lo16[9], lo16[10], lo16[11], lo16[12], lo16[13], lo16[14], lo16[15]);
+                    const uint32_t h0 = cvt_e2m1x8(hi16[0], hi16[1], hi16[2], hi16[3], hi16[4], hi16[5], hi16[6], hi16[7]);
+                    const uint32_t h1 = cvt_e2m1x8(hi16[8], hi16[9], hi16[10], hi16[11], hi16[12], hi16[13], hi16[14], hi16[15]);
+                    cw[2 * bk] = live ? h0 : 0u;
+                    cw[2 * bk + 1] = live ? h1 : 0u;
+                    diff[2 * bk] = !live ? 0u : fast ? (l0 ^ h0) : 0xFFFFFFFFu;
+                    diff[2 * bk + 1] = !live ? 0u : fast ? (l1 ^ h1) : 0xFFFFFFFFu;
+                }
+                const bool slow = row_ok && col_ok &&
+                                  (!cert[0] || !cert[1] || (diff[0] | diff[1] | diff[2] | diff[3]) != 0u);
+                if (__any_sync(0xFFFFFFFFu, slow)) {
+                    ok = mbar_wait(&x_full[xs], xph, args.status, abort_flag, kWaitLimitNs);
+                    if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                    x_read = true;
+                    uint32_t bq[kRank];
+                    tmem_ld_32x32b_x32(tbrow, bq);
+                    tmem_ld_wait();
+                    if (slow) {
+                        // Blocks whose scale is uncertain: the 16 values by the exact chain
+                        // (16 chains side by side), then the scale and codes by true divisions.
+#pragma unroll 1
+                        for (int bk = 0; bk < 2; ++bk) {
+                            if (bk == 0 ? cert[0] : cert[1]) continue;
+                            const int kt = kt0 + 16 * bk;
+                            float x16[16];
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) x16[e] = 0.0f;
+#pragma unroll 2
+                            for (int j = 0; j < kRank; ++j) {
+                                const float bj = __uint_as_float(bq[j]);
+                                const float4* ar = reinterpret_cast<const float4*>(af + j * kTK + kt);
+#pragma unroll
+                                for (int q4 = 0; q4 < 4; ++q4) {
+                                    const float4 v = ar[q4];
+                                    x16[4 * q4] = __fmaf_rn(bj, v.x, x16[4 * q4]);
+                                    x16[4 * q4 + 1] = __fmaf_rn(bj, v.y, x16[4 * q4 + 1]);
+                                    x16[4 * q4 + 2] = __fmaf_rn(bj, v.z, x16[4 * q4 + 2]);
+                                    x16[4 * q4 + 3] = __fmaf_rn(bj, v.w, x16[4 * q4 + 3]);
+                                }
+                            }
+                            float bam = 0.0f;
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) {
+                                x16[e] = __fmaf_rn(c, x16[e], bf16_sel(wr, 16 * bk + e));
+                                bam = fmaxf(bam, fabsf(x16[e]));
+                            }
+                            uint32_t sc = 0;
+                            if (d > 0.0f) sc = cvt_e4m3(__fdiv_rn(bam, d));
+                            const float dn = __fmul_rn(e4m3_value(sc), s);
+                            uint32_t c0 = 0u, c1 = 0u;
+                            if (dn > 0.0f) {
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) x16[e] = __fdiv_rn(x16[e], dn);
+                                c0 = cvt_e2m1x8(x16[0], x16[1], x16[2], x16[3], x16[4], x16[5], x16[6], x16[7]);
+                                c1 = cvt_e2m1x8(x16[8], x16[9], x16[10], x16[11], x16[12], x16[13], x16[14], x16[15]);
+                            }
+                            if (bk == 0) {
+                                cw[0] = c0; cw[1] = c1; sfc[0] = sc;
+                            } else {
+                                cw[2] = c0; cw[3] = c1; sfc[1] = sc;
+                            }
+                        }
+                        // Elements whose two ends disagree (in blocks with a certain scale).
+                        uint32_t um = 0u;
+#pragma unroll
+                        for (int w = 0; w < 4; ++w)
+#pragma unroll
+                            for (int j = 0; j < 8; ++j)
+                                um |= (((diff[w] >> (4 * j)) & 0xFu) != 0u ? 1u : 0u) << (8 * w + j);
+                        if (!cert[0]) um &= 0xFFFF0000u;
+                        if (!cert[1]) um &= 0x0000FFFFu;
+#pragma unroll 1
+                        while (um != 0u) {
+                            const int e = __ffs((int)um) - 1;
+                            um &= um - 1u;
+                            const float x = exact_value(bq, af, kt0 + e, c, bf16_sel(wr, e));
+                            const uint32_t code =
+                                cvt_e2m1x8(__fdiv_rn(x, e < 16 ? den[0] : den[1]), 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 0xFu;
+                            const uint32_t sh = 4u * (uint32_t)(e & 7), keep = ~(0xFu << sh);
+                            const int wi = e >> 3;
+                            if (wi == 0) cw[0] = (cw[0] & keep) | (code << sh);
+                            else if (wi == 1) cw[1] = (cw[1] & keep) | (code << sh);
+                            else if (wi == 2) cw[2] = (cw[2] & keep) | (code << sh);
+                            else cw[3] = (cw[3] & keep) | (code << sh);
+                        }
+                    }
+                }
+                if (col_ok) {
+                    if (row_ok)
+                        *reinterpret_cast<uint4*>(args.codes + (int64_t)n * (args.K >> 1) + (k0 >> 1)) =
+                            make_uint4(cw[0], cw[1], cw[2], cw[3]);
+                    if (n < args.rows_pad)
+                        *reinterpret_cast<uint16_t*>(
+                            args.sf + ((int64_t)(n >> 7) * (args.K >> 6) + (k0 >> 6)) * 512 +
+                            (n & 31) * 16 + ((n >> 5) & 3) * 4 + ((k0 >> 5) & 1) * 2) =
+                            (uint16_t)(sfc[0] | (sfc[1] << 8));
+                }
+            }
+            // Done with this tile's strip of A (reads, if any, were consumed by the exact
+            // chain, and fenced against the TMA that will overwrite the slot).
+            if (x_read) fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&x_empty[xs]);
+            nb = nb1;
+            ks = ks1;
+        }
+    }
+
+    __syncwarp();
+    tc_fence_before_sync();
+    __syncthreads();
+    cluster_sync_all();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
+    }
+}
+
+__global__ void merge_tc_finalize_kernel(float* s_t) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) *s_t = __fdiv_rn(*s_t, kAmaxDiv);
+}
+
+template <int kMode>
+cudaError_t run_merge_tc(const LaunchCtx& ctx, const RequantTcMaps& m, const TcArgs& a) {
+    static OccupancyCache occupancy;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kPair;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = ctx.stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3((unsigned)(ctx.num_sms / kPair * kPair), 1, 1);
+    int max_clusters = 0;
+    const cudaError_t e = clusters_per_device(occupancy, ctx, merge_tc_kernel<kMode>, cfg, &max_clusters);
+    if (e != cudaSuccess) return e;
+    const int clusters = a.tiles < max_clusters ? a.tiles : max_clusters;
+    cfg.gridDim = dim3((unsigned)(clusters * kPair), 1, 1);
+    return cudaLaunchKernelEx(&cfg, merge_tc_kernel<kMode>, m.w, m.bp, m.ap, m.af, a);
+}
+
+}  // namespace
+
+size_t requant_tc_workspace_bytes(int w_dtype, int r, int64_t N, int64_t K) {
+    const int64_t tiles = (N + kTM * kPair - 1) / (kTM * kPair) * ((K + kTK - 1) / kTK);
+    if (w_dtype != NVFP4_W_BF16 || r != kRank || N <= 0 || K <= 0 || tiles >= (int64_t(1) << 30))
+        return 0;
+    return requant_tc_layout(nullptr, N, K).bytes;
+}
+
+cudaError_t launch_requant_tc(const LaunchCtx& ctx, const RequantTcMaps& maps, const float* A,
+                              const float* B, void* workspace, float c, int64_t N, int64_t K,
+                              uint8_t* codes, uint8_t* sf, float* s_t) {
+    const RequantTcLayout ws = requant_tc_layout(workspace, N, K);
+    TcArgs a;
+    a.c = c;
+    a.N = (int)N;
+    a.K = (int)K;
+    a.rows_pad = (int)((N + 127) / 128 * 128);
+    a.codes = codes;
+    a.sf = sf;
+    a.s_t = s_t;
+    a.rnorm = ws.rnorm;
+    a.B = B;
+    a.cnorm = ws.cnorm;
+    a.status = ctx.status;
+    a.zero = 0;
+    a.nks = (int)((K + kTK - 1) / kTK);
+    a.tiles = (int)((N + kTM * kPair - 1) / (kTM * kPair)) * a.nks;
+    const int rows_pad256 = (int)((N + 255) / 256 * 256);
+    const int nb_rows = (rows_pad256 + kSplitRows - 1) / kSplitRows;
+    const int nb_cols = (int)((K + kSplitCols - 1) / kSplitCols);
+    merge_split_kernel<<<(unsigned)(nb_rows + nb_cols), kSplitThreads, 0, ctx.stream>>>(
+        A, B, (int)N, (int)K, rows_pad256, nb_rows, ws.bp, ws.ap, ws.rnorm, ws.cnorm, s_t);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if ((e = run_merge_tc<kModeAmax>(ctx, maps, a)) != cudaSuccess) return e;
+    if ((e = run_merge_tc<kModeQuant>(ctx, maps, a)) != cudaSuccess) return e;
+    merge_tc_finalize_kernel<<<1, 32, 0, ctx.stream>>>(s_t);
+    return cudaGetLastError();
+}
+
+}  // namespace nvfp4rl

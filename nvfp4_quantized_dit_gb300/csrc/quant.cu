@@ -247,14 +247,10 @@ template <int G>
 cudaError_t run_act_quant(const LaunchCtx& ctx, const __nv_bfloat16* X, int64_t M, int64_t K,
                           int64_t rows_pad, uint8_t* codes, uint8_t* sf, float* s_row) {
     const size_t smem = (size_t)(kAqWarps / G) * kAqRing * (size_t)K * 2;
-    cudaError_t e = cudaFuncSetAttribute(act_quant_kernel<G>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+    static OccupancyCache occupancy;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, act_quant_kernel<G>, kAqWarps * 32,
-                                                      smem);
+    const cudaError_t e = blocks_per_sm(occupancy, ctx, act_quant_kernel<G>, kAqWarps * 32, smem, &per_sm);
     if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
     int64_t grid = (rows_pad + (kAqWarps / G) - 1) / (kAqWarps / G);
     if (grid > (int64_t)ctx.num_sms * per_sm) grid = (int64_t)ctx.num_sms * per_sm;
     act_quant_kernel<G><<<(unsigned)grid, kAqWarps * 32, smem, ctx.stream>>>(X, M, K, rows_pad, codes,
@@ -944,13 +940,12 @@ __global__ void requant_finalize_kernel(float* s_t) {
 }
 
 template <typename Kern>
-cudaError_t rq_grid(const LaunchCtx& ctx, Kern kern, size_t smem, int64_t tiles, unsigned* grid) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
+cudaError_t rq_grid(OccupancyCache& occupancy, const LaunchCtx& ctx, Kern kern, size_t smem,
+                    int64_t tiles, unsigned* grid) {
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kRqThreads, smem);
+    const cudaError_t e = blocks_per_sm(occupancy, ctx, kern, kRqThreads, smem, &per_sm);
     if (e != cudaSuccess) return e;
-    const int64_t g = (int64_t)ctx.num_sms * (per_sm < 1 ? 1 : per_sm);
+    const int64_t g = (int64_t)ctx.num_sms * per_sm;
     *grid = (unsigned)(tiles < g ? tiles : g);
     return cudaSuccess;
 }
@@ -984,9 +979,10 @@ template <int kWType>
 cudaError_t run_requant(const LaunchCtx& ctx, const RqArgs& a) {
     const size_t smem1 = rq_smem_bytes(a.r), smem2 = rq2_smem_bytes<kWType>(a.r);
     unsigned g1 = 0, g2 = 0;
-    cudaError_t e = rq_grid(ctx, requant_amax_kernel<kWType>, smem1, a.tiles, &g1);
+    static OccupancyCache occ_amax, occ_quant;
+    cudaError_t e = rq_grid(occ_amax, ctx, requant_amax_kernel<kWType>, smem1, a.tiles, &g1);
     if (e != cudaSuccess) return e;
-    e = rq_grid(ctx, requant_quant_kernel<kWType, false>, smem2, a.tiles2, &g2);
+    e = rq_grid(occ_quant, ctx, requant_quant_kernel<kWType, false>, smem2, a.tiles2, &g2);
     if (e != cudaSuccess) return e;
     e = cudaMemsetAsync(a.s_t, 0, sizeof(float), ctx.stream);
     if (e != cudaSuccess) return e;
@@ -1002,7 +998,8 @@ template <int kWType>
 cudaError_t run_merge_dump(const LaunchCtx& ctx, const RqArgs& a) {
     const size_t smem = rq2_smem_bytes<kWType>(a.r);
     unsigned g = 0;
-    cudaError_t e = rq_grid(ctx, requant_quant_kernel<kWType, true>, smem, a.tiles2, &g);
+    static OccupancyCache occupancy;
+    cudaError_t e = rq_grid(occupancy, ctx, requant_quant_kernel<kWType, true>, smem, a.tiles2, &g);
     if (e != cudaSuccess) return e;
     requant_quant_kernel<kWType, true><<<g, kRqThreads, smem, ctx.stream>>>(a);
     return cudaGetLastError();

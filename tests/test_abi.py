@@ -27,7 +27,7 @@ def lib():
 def _declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    names = re.findall(r"^(?:nvfp4_status|const char\*|int)\s+(\w+)\s*\(", text, flags=re.M)
+    names = re.findall(r"^(?:nvfp4_status|const char\*|int|size_t)\s+(\w+)\s*\(", text, flags=re.M)
     return names
 
 
@@ -83,13 +83,30 @@ def test_act_quant_validation(lib):
 def test_requant_validation(lib):
     P = ctypes.c_void_p
     f = ctypes.c_float(32.0)
-    assert lib.nvfp4_requant(P(A16), 2, None, None, 0, f, 8, 64, P(A16), P(A16), P(A16), None) == 2
-    assert lib.nvfp4_requant(P(A16), 0, P(A16), P(A16), 65, f, 8, 64, P(A16), P(A16), P(A16), None) == 2
-    assert lib.nvfp4_requant(P(A16), 0, None, None, 0, f, 8, 96, P(A16), P(A16), P(A16), None) == 2
-    assert lib.nvfp4_requant(P(A16), 0, None, None, 0, f, 8, 64, P(A16), P(A16), None, None) == 1
-    assert lib.nvfp4_requant(None, 0, None, None, 0, f, 8, 64, P(A16), P(A16), P(A16), None) == 1
-    assert lib.nvfp4_requant(P(A16), 0, P(BAD), P(A16), 32, f, 8, 64, P(A16), P(A16), P(A16), None) == 3
-    assert lib.nvfp4_requant(P(A16), 0, None, None, 0, f, 8, 64, P(BAD), P(A16), P(A16), None) == 3
+    assert lib.nvfp4_requant(P(A16), 2, None, None, 0, f, 8, 64, P(A16), P(A16), P(A16), None, 0, None) == 2
+    assert lib.nvfp4_requant(P(A16), 0, P(A16), P(A16), 65, f, 8, 64, P(A16), P(A16), P(A16), None, 0, None) == 2
+    assert lib.nvfp4_requant(P(A16), 0, None, None, 0, f, 8, 96, P(A16), P(A16), P(A16), None, 0, None) == 2
+    assert lib.nvfp4_requant(P(A16), 0, None, None, 0, f, 8, 64, P(A16), P(A16), None, None, 0, None) == 1
+    assert lib.nvfp4_requant(None, 0, None, None, 0, f, 8, 64, P(A16), P(A16), P(A16), None, 0, None) == 1
+    assert lib.nvfp4_requant(P(A16), 0, P(BAD), P(A16), 32, f, 8, 64, P(A16), P(A16), P(A16), None, 0, None) == 3
+    assert lib.nvfp4_requant(P(A16), 0, None, None, 0, f, 8, 64, P(BAD), P(A16), P(A16), None, 0, None) == 3
+
+
+def test_requant_workspace_bytes(lib):
+    """The tensor-core merge's workspace: B' and A' (256 bytes per row of B and per
+    column of A), the row norms (rows padded to 256) and 16 bytes of column norms
+    per 128 columns, each piece rounded up to 256 bytes; 0 where that path does not
+    apply."""
+    ws = lib.nvfp4_requant_workspace_bytes
+    ws.restype = ctypes.c_size_t
+    ws.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64]
+    up = lambda x: (x + 255) // 256 * 256
+    assert ws(0, 32, 300, 192) == up(300 * 256) + up(192 * 256) + up(512 * 4) + up(2 * 16)
+    assert ws(0, 32, 12288, 3072) == 12288 * 256 + 3072 * 256 + 12288 * 4 + 512
+    assert ws(1, 32, 300, 192) == 0     # fp32 W: CUDA-core merge
+    assert ws(0, 16, 300, 192) == 0     # rank other than 32
+    assert ws(0, 32, 300, 100) == 0     # K % 64
+    assert ws(0, 32, 0, 64) == 0
 
 
 def test_gemm_validation(lib):

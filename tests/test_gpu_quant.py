@@ -160,6 +160,45 @@ def test_requant_edge_values(orc):
     _check_requant(orc, torch.zeros(N, K), A * 0, B * 0, 32.0)
 
 
+@pytest.mark.parametrize("N,K", [(1, 64), (100, 64), (257, 192), (640, 1088), (1024, 12288)])
+def test_requant_tensor_core_shapes(orc, N, K):
+    """bf16 weights with a rank-32 update take the tensor-core merge: one row, a
+    256-row block whose second half is empty, ragged rows with a half-width last
+    strip, and several row blocks per CTA pair (rows of B kept across strips)."""
+    require_gpu()
+    g = torch.Generator().manual_seed(N * 7 + K)
+    W = (torch.randn(N, K, generator=g) * 0.02).to(torch.bfloat16)
+    A = torch.randn(32, K, generator=g) / 32
+    B = torch.randn(N, 32, generator=g) * 0.01
+    _check_requant(orc, W, A, B, 32.0)
+
+
+def test_requant_tensor_core_degenerate(orc):
+    """The tensor-core merge's degenerate cases: alpha = 0 (W' = W up to the sign of
+    zero, which the chain's accumulator decides), zero rows of B and zero columns of
+    A, an update far larger than W (most decisions fall to the exact chain), and
+    factors whose products are fp32 subnormals."""
+    require_gpu()
+    g = torch.Generator().manual_seed(31)
+    N, K = 300, 256
+    W = torch.randn(N, K, generator=g) * 0.02
+    W[0] = -0.0
+    W[1, ::2] = -0.0
+    W[1, 1::2] = 0.0
+    W = W.to(torch.bfloat16)
+    A = torch.randn(32, K, generator=g) / 32
+    B = torch.randn(N, 32, generator=g) * 0.01
+    B[2] = 0.0
+    A[:, 5] = 0.0
+    _check_requant(orc, W, A, B, 0.0)
+    _check_requant(orc, W, A, B, 32.0)
+    Wt = (torch.randn(N, K, generator=g) * 1e-6).to(torch.bfloat16)
+    _check_requant(orc, Wt, torch.randn(32, K, generator=g), torch.randn(N, 32, generator=g), 32.0)
+    Ws = (torch.randn(N, K, generator=g) * 1e-39).to(torch.bfloat16)
+    _check_requant(orc, Ws, torch.randn(32, K, generator=g) * 1e-20,
+                   torch.randn(N, 32, generator=g) * 1e-19, 32.0)
+
+
 def test_requant_repeated_calls_reset_amax(orc):
     """s_t doubles as the amax accumulator: a second call on a smaller tensor must
     not see the first call's amax."""
