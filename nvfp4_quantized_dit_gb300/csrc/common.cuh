@@ -88,10 +88,9 @@ cudaError_t launch_requant(const LaunchCtx&, const void* W, int w_dtype, const f
                            uint8_t* sf, float* s_t);
 // Tensor-core merge (merge_tc.cu): bf16 W, rank 32, 16-byte aligned A and B, and a
 // workspace of requant_tc_workspace_bytes (0 when the path does not apply) laid out by
-// requant_tc_layout: B' [N, 128] bf16, A' [K, 128] bf16, rnorm [N rounded up to 256],
-// cnorm [K / 128 rounded up][4].
+// requant_tc_layout: A' [K, 128] bf16, rnorm [N rounded up to 256], cnorm [K / 128
+// rounded up][4].
 struct RequantTcLayout {
-    uint8_t* bp;
     uint8_t* ap;
     float* rnorm;
     float* cnorm;
@@ -102,8 +101,6 @@ inline RequantTcLayout requant_tc_layout(void* base, int64_t N, int64_t K) {
     const uintptr_t p = reinterpret_cast<uintptr_t>(base);
     RequantTcLayout l;
     size_t off = 0;
-    l.bp = reinterpret_cast<uint8_t*>(p + off);
-    off += up((size_t)N * 256);
     l.ap = reinterpret_cast<uint8_t*>(p + off);
     off += up((size_t)K * 256);
     l.rnorm = reinterpret_cast<float*>(p + off);
@@ -113,11 +110,10 @@ inline RequantTcLayout requant_tc_layout(void* base, int64_t N, int64_t K) {
     l.bytes = off;
     return l;
 }
-// Tensor maps of the merge kernels: W [N, K] bf16 (64 x 128 boxes), B' [N, 128] bf16
-// (64 x 128 boxes), A' [K, 128] bf16 (64 x 64 boxes), all with the 128-byte swizzle;
-// A [32, K] fp32 (128 x 32 boxes).
+// Tensor maps of the merge kernels: W [N, K] bf16 (64 x 128 boxes) and A' [K, 128] bf16
+// (64 x 64 boxes), both with the 128-byte swizzle; A [32, K] fp32 (128 x 32 boxes).
 struct RequantTcMaps {
-    CUtensorMap w, bp, ap, af;
+    CUtensorMap w, ap, af;
 };
 size_t requant_tc_workspace_bytes(int w_dtype, int r, int64_t N, int64_t K);
 cudaError_t launch_requant_tc(const LaunchCtx&, const RequantTcMaps& maps, const float* A,
@@ -484,6 +480,18 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, 
         : "memory");
 }
 
+// As mma_bf16_pair with the A operand in tensor memory: each CTA's 128 rows of A in
+// its own lanes 0..127 at column a_tmem, two bf16 per 32-bit column (K-major).
+__device__ __forceinline__ void mma_bf16_pair_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                 uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_nvfp4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                                uint32_t idesc, uint32_t sfa_tmem,
                                                uint32_t sfb_tmem, uint32_t accumulate) {
@@ -689,6 +697,12 @@ __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_
         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
         "r"(r[15])
         : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_32x32b_x4(uint32_t taddr, const uint32_t (&r)[4]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(r[0]),
+                 "r"(r[1]), "r"(r[2]), "r"(r[3])
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t (&r)[8]) {

@@ -37,26 +37,29 @@
 // So codes, scales and s_t are bit-identical to the fp32 chain's.  The exact chain
 // reads the fp32 factors from shared memory.
 //
-// Kernels.  A split kernel writes the operands of the merge GEMM once per call into
-// the caller's workspace: B' = [b0 b0 b1 b1] per row of B, A' = [a0 a1 a0 a1] per
-// column of A (bf16, 256 bytes per row), an upper bound of every row norm of B and,
-// per 64 columns, the largest column norm of A.  Then both passes run as persistent
+// Kernels.  A split kernel writes A' = [a0 a1 a0 a1] per column of A (bf16, 256 bytes
+// per row) into the caller's workspace, with upper bounds of every row norm of B and,
+// per 64 columns, of the largest column norm of A.  Then both passes run as persistent
 // clusters of two CTAs; a pair tile is 256 weight rows (128 per CTA) x 128 columns,
 // walked k-strip first, so the rows of B usually stay the same from one tile to the
-// next.  Per CTA, 18 warps:
-//   warp 0      TMA into three rings: W tiles (128 x 128 bf16; 2 slots, freed as soon
-//               as every epilogue warp has copied its rows into registers), the MMA
-//               operands (2 slots: this CTA's 64 rows of A', and B' when the rows
-//               change; completing on the even CTA's barrier, freed by the MMAs) and
-//               the fp32 strip of A for the exact chain (4 slots);
+// next.  Per CTA, 20 warps:
+//   warp 0      TMA: W tiles (128 x 128 bf16; 4 slots, freed as soon as every epilogue
+//               warp has copied its rows into registers) and the fp32 strip of A for the
+//               exact chain (3 slots);
 //   warp 1      tensor-memory allocation; lane 0 of the even CTA issues the 8 pair MMAs
-//               (kind::f16, M = 256, N = 128) into a double-buffered accumulator;
-//   warps 2-17  epilogue: four warps per tensor-memory lane quarter, 32 columns each (a
+//               (kind::f16, M = 256, N = 128, A from tensor memory) into a
+//               double-buffered accumulator;
+//   warp 2      TMA: this CTA's 64 rows of A' (the MMA's B operand; 3 slots),
+//               completing on the even CTA's barrier, freed by the MMAs;
+//   warp 3      idle;
+//   warps 4-19  epilogue: four warps per tensor-memory lane quarter, 32 columns each (a
 //               thread owns one weight row): accumulator + W -> w~ -> pass 1 amax or
-//               pass 2 codes and scales, stored straight to global memory.  The fp32
-//               rows of B for the exact chain sit in tensor memory next to the
-//               accumulators (lane = row), written by the epilogue warps when the rows
-//               change; only the rare uncertain elements read them and the A strip.
+//               pass 2 codes and scales, stored straight to global memory.
+// The rows of B live in tensor memory next to the accumulators (lane = row), in two
+// buffers for consecutive row blocks: [b0 b0 b1 b1] as bf16 pairs (the MMA's A
+// operand) and the fp32 values (for the exact chain).  The epilogue warps write the
+// next row block's buffer one tile ahead; only the rare uncertain elements read the
+// fp32 rows and the strip of A.
 // Every mbarrier wait is bounded (mbar_wait).
 #include "common.cuh"
 
@@ -68,23 +71,21 @@ constexpr int kTK = 128;        // weight columns per pair tile (64 per CTA in t
 constexpr int kPair = 2;
 constexpr int kRank = 32;       // the rank this path serves (A [32, K], B [N, 32])
 constexpr int kJp = 4 * kRank;  // K' of the merge GEMM
-constexpr int kEpiWarp0 = 2, kEpiWarps = 16;
+constexpr int kEpiWarp0 = 4, kEpiWarps = 16;  // warp groups: 0 control, 1-4 epilogue
 constexpr int kCols = 32;       // columns per epilogue warp
 constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
-constexpr uint32_t kOpABytes = kTM * kJp * 2;            // 32 KB: B' rows, two 64-column atoms
+constexpr int kWSlots = 4, kXSlots = 3, kOpSlots = 3;
 constexpr uint32_t kOpBBytes = (kTK / kPair) * kJp * 2;  // 16 KB: A' rows, two 64-column atoms
 constexpr uint32_t kWBox = kTM * 128;                    // 16 KB: 128 rows x 64 bf16
 constexpr uint32_t kWBytes = 2 * kWBox;                  // 32 KB: 128 rows x 128 bf16
-constexpr uint32_t kBfBytes = kTM * kRank * 4;           // 16 KB: fp32 rows of B
 constexpr uint32_t kAfBytes = kRank * kTK * 4;           // 16 KB: fp32 strip of A
-constexpr int kXSlots = 4;                               // fp32 strips of A in flight
-constexpr uint32_t kMiscBytes = 256;
+constexpr uint32_t kMiscBytes = 512;
 constexpr uint32_t kSmemBytes =
-    1024 + 2 * (kOpABytes + kOpBBytes + kWBytes) + kXSlots * kAfBytes + kMiscBytes;
-// Tensor memory: two accumulators of 128 columns, then two buffers of 32 columns for
-// the fp32 rows of B (lane = row).
+    1024 + kOpSlots * kOpBBytes + kWSlots * kWBytes + kXSlots * kAfBytes + kMiscBytes;
+// Tensor memory: two accumulators of 128 columns, then two row buffers of 96 columns:
+// 64 columns of [b0 b0 b1 b1] (bf16 pairs) and 32 columns of fp32 B.
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kBrowCol = 2 * kTK;
+constexpr uint32_t kRowBuf0 = 2 * kTK, kRowBufCols = 96, kRowBufF32 = 64;
 constexpr uint16_t kBothCtas = 0x3;
 constexpr uint16_t kEvenCta = 0x1;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
@@ -93,7 +94,13 @@ constexpr int kModeAmax = 0, kModeQuant = 1;
 constexpr int kSplitThreads = 256;
 constexpr int kSplitRows = kSplitThreads / 4;  // rows of B per split block (4 threads a row)
 constexpr int kSplitCols = kSplitThreads / 4;  // columns of A per split block (4 threads a column)
+// Registers: launched at 96 per thread (20 warps, 5 per scheduler); the control warp
+// group drops to 32 and the epilogue warp groups rise to 112 (4 x 32 + 16 x 112 <=
+// 20 x 96).
+constexpr uint32_t kRegsCtl = 32, kRegsEpi = 112;
+static_assert(4 * kRegsCtl + kEpiWarps * kRegsEpi <= (uint32_t)(kThreads / 32) * 96, "register split");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kRowBuf0 + 2 * kRowBufCols <= kTmemCols, "tensor memory budget");
 
 // kind::f16, bf16 A and B, fp32 accumulator, K-major, N = 128, M = 256 (pair).
 constexpr uint32_t idesc_merge() {
@@ -108,7 +115,7 @@ struct TcArgs {
     uint8_t* sf;
     float* s_t;  // pass 1: amax accumulator (fp32 bits, atomicMax); pass 2: reads it
     const float* rnorm;  // [N padded to 256] upper bounds of ||B[n,:]||_2 (0 past N)
-    const float* B;      // [N, 32] fp32: the rows the exact chain reads
+    const float* B;      // [N, 32] fp32
     const float* cnorm;  // [K/128][4]: per 128-column strip, the largest ||A[:,k]||_2
                          // of each 64-column half (upper bounds), then 2 unused
     int* status;
@@ -148,16 +155,15 @@ __device__ __forceinline__ void split8(const float* v, uint4& p0, uint4& p1) {
                     bf16_pair(l[6], l[7]));
 }
 
-// Operands of the merge GEMM, four threads per row of B or column of A (8 values
-// each).  Blocks [0, nb_rows) take 64 rows of B: B'[n] = [b0 b0 b1 b1] and rnorm[n]
-// (rnorm is 0 for the padding rows up to rows_pad256).  The other blocks take 64
-// columns of A: A'[k] = [a0 a1 a0 a1] and the block's largest column norm.  Block 0
-// also clears the amax accumulator s_t.
+// Four threads per row of B or column of A (8 values each).  Blocks [0, nb_rows) take
+// 64 rows of B: rnorm[n] (0 for the padding rows up to rows_pad256).  The other blocks
+// take 64 columns of A: A'[k] = [a0 a1 a0 a1] and the block's largest column norm.
+// Block 0 also clears the amax accumulator s_t.
 __global__ void __launch_bounds__(kSplitThreads)
     merge_split_kernel(const float* __restrict__ A, const float* __restrict__ B, int N, int K,
-                       int rows_pad256, int nb_rows, uint8_t* __restrict__ Bp,
-                       uint8_t* __restrict__ Ap, float* __restrict__ rnorm,
-                       float* __restrict__ cnorm, float* __restrict__ s_t) {
+                       int rows_pad256, int nb_rows, uint8_t* __restrict__ Ap,
+                       float* __restrict__ rnorm, float* __restrict__ cnorm,
+                       float* __restrict__ s_t) {
     __shared__ float red[kSplitThreads];
     __shared__ float red2[kSplitCols / 32];
     const int tid = (int)threadIdx.x;
@@ -169,17 +175,14 @@ __global__ void __launch_bounds__(kSplitThreads)
         if (n < N) {
             const float4* src = reinterpret_cast<const float4*>(B + (int64_t)n * kRank + 8 * g);
             const float4 x0 = src[0], x1 = src[1];
-            v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
-            v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) s2 = __fmaf_rn(v[j], v[j], s2);
-            uint4 p0, p1;
-            split8(v, p0, p1);
-            uint4* dst = reinterpret_cast<uint4*>(Bp + (int64_t)n * (kJp * 2));
-            dst[g] = p0;
-            dst[4 + g] = p0;
-            dst[8 + g] = p1;
-            dst[12 + g] = p1;
+            s2 = __fmaf_rn(x0.x, x0.x, s2);
+            s2 = __fmaf_rn(x0.y, x0.y, s2);
+            s2 = __fmaf_rn(x0.z, x0.z, s2);
+            s2 = __fmaf_rn(x0.w, x0.w, s2);
+            s2 = __fmaf_rn(x1.x, x1.x, s2);
+            s2 = __fmaf_rn(x1.y, x1.y, s2);
+            s2 = __fmaf_rn(x1.z, x1.z, s2);
+            s2 = __fmaf_rn(x1.w, x1.w, s2);
         }
         // The four partial sums of the row (lanes 4r .. 4r + 3 of the warp).
         s2 += __shfl_xor_sync(0xFFFFFFFFu, s2, 1);
@@ -236,30 +239,167 @@ __device__ __forceinline__ float exact_value(const uint32_t (&b)[kRank], const f
     return __fmaf_rn(c, acc, w);
 }
 
+// Pass 2's rare path for one thread's 32 columns (called by the whole warp; `slow`
+// says whether this thread has work): blocks whose scale is uncertain get their 16
+// values from the exact chain (16 chains side by side), then the scale and codes by
+// true divisions; elements whose interval ends disagree (diff) get their code from
+// the exact chain.  tbrow is the tensor-memory address of the fp32 rows of B, af the
+// fp32 strip of A, w the 32 weights.
+struct Codes32 {
+    uint32_t cw[4];
+    uint32_t sfc[2];
+};
+__device__ __noinline__ Codes32 quant_fix(uint32_t tbrow, const float* af, int kt0, float c, float s,
+                                          float d, Codes32 r, uint4 diff, float den0, float den1,
+                                          bool cert0, bool cert1, bool slow, uint4 w0, uint4 w1, uint4 w2,
+                                          uint4 w3) {
+    uint32_t bq[kRank];
+    tmem_ld_32x32b_x32(tbrow, bq);
+    tmem_ld_wait();
+    if (!slow) return r;
+    const uint4 wr[4] = {w0, w1, w2, w3};
+#pragma unroll 1
+    for (int bk = 0; bk < 2; ++bk) {
+        if (bk == 0 ? cert0 : cert1) continue;
+        const int kt = kt0 + 16 * bk;
+        float x16[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) x16[e] = 0.0f;
+#pragma unroll 2
+        for (int j = 0; j < kRank; ++j) {
+            const float bj = __uint_as_float(bq[j]);
+            const float4* ar = reinterpret_cast<const float4*>(af + j * kTK + kt);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                const float4 v = ar[q4];
+                x16[4 * q4] = __fmaf_rn(bj, v.x, x16[4 * q4]);
+                x16[4 * q4 + 1] = __fmaf_rn(bj, v.y, x16[4 * q4 + 1]);
+                x16[4 * q4 + 2] = __fmaf_rn(bj, v.z, x16[4 * q4 + 2]);
+                x16[4 * q4 + 3] = __fmaf_rn(bj, v.w, x16[4 * q4 + 3]);
+            }
+        }
+        float bam = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            x16[e] = __fmaf_rn(c, x16[e], bf16_sel(wr, 16 * bk + e));
+            bam = fmaxf(bam, fabsf(x16[e]));
+        }
+        uint32_t sc = 0;
+        if (d > 0.0f) sc = cvt_e4m3(__fdiv_rn(bam, d));
+        const float dn = __fmul_rn(e4m3_value(sc), s);
+        uint32_t c0 = 0u, c1 = 0u;
+        if (dn > 0.0f) {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) x16[e] = __fdiv_rn(x16[e], dn);
+            c0 = cvt_e2m1x8(x16[0], x16[1], x16[2], x16[3], x16[4], x16[5], x16[6], x16[7]);
+            c1 = cvt_e2m1x8(x16[8], x16[9], x16[10], x16[11], x16[12], x16[13], x16[14], x16[15]);
+        }
+        if (bk == 0) {
+            r.cw[0] = c0; r.cw[1] = c1; r.sfc[0] = sc;
+        } else {
+            r.cw[2] = c0; r.cw[3] = c1; r.sfc[1] = sc;
+        }
+    }
+    // Elements whose two ends disagree (in blocks with a certain scale).
+    const uint32_t dw[4] = {diff.x, diff.y, diff.z, diff.w};
+    uint32_t um = 0u;
+#pragma unroll
+    for (int w = 0; w < 4; ++w)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) um |= (((dw[w] >> (4 * j)) & 0xFu) != 0u ? 1u : 0u) << (8 * w + j);
+    if (!cert0) um &= 0xFFFF0000u;
+    if (!cert1) um &= 0x0000FFFFu;
+#pragma unroll 1
+    while (um != 0u) {
+        const int e = __ffs((int)um) - 1;
+        um &= um - 1u;
+        const float x = exact_value(bq, af, kt0 + e, c, bf16_sel(wr, e));
+        const uint32_t code = cvt_e2m1x8(__fdiv_rn(x, e < 16 ? den0 : den1), 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 0xFu;
+        const uint32_t sh = 4u * (uint32_t)(e & 7), keep = ~(0xFu << sh);
+        const int wi = e >> 3;
+        if (wi == 0) r.cw[0] = (r.cw[0] & keep) | (code << sh);
+        else if (wi == 1) r.cw[1] = (r.cw[1] & keep) | (code << sh);
+        else if (wi == 2) r.cw[2] = (r.cw[2] & keep) | (code << sh);
+        else r.cw[3] = (r.cw[3] & keep) | (code << sh);
+    }
+    return r;
+}
+
+// Writes the rows of row block nbw into row buffer nrb & 1 of tensor memory (this
+// warp's 8 of the 32 columns of B for its 32 rows: the bf16 parts for the MMA, fp32
+// for the exact chain), once the lane quarter's 4 warps are all past the tiles that
+// used the buffer, and publishes them to the quarter (qbar) and to the MMA (rows_ready,
+// on the even CTA).  Returns false if a wait gave up.
+__device__ __forceinline__ bool write_rows(const TcArgs& args, uint32_t tmem_base, uint32_t tlane,
+                                           uint64_t* qbar, uint32_t rows_ready_even, int nbw,
+                                           uint32_t rank, int rloc, int chunk, int lane, int& nrb,
+                                           int& nqb, volatile int* abort_flag) {
+    if (lane == 0) mbar_arrive(qbar);
+    bool ok = mbar_wait(qbar, (uint32_t)(nqb & 1), args.status, abort_flag, kWaitLimitNs);
+    ++nqb;
+    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+    tc_fence_after_sync();
+    const int n = nbw * (kTM * kPair) + (int)rank * kTM + rloc;
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (n < args.N) {
+        const float4* src = reinterpret_cast<const float4*>(args.B + (int64_t)n * kRank + 8 * chunk);
+        const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
+        v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
+        v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+    }
+    uint4 p0, p1;
+    split8(v, p0, p1);
+    const uint32_t base = tmem_base + tlane + kRowBuf0 + kRowBufCols * (uint32_t)(nrb & 1);
+    // [b0 b0 b1 b1]: K' index 32 g + j (g = part, j = column of B) sits in column
+    // (32 g + j) / 2 as the low (j even) or high half.
+    const uint32_t r0[4] = {p0.x, p0.y, p0.z, p0.w}, r1[4] = {p1.x, p1.y, p1.z, p1.w};
+    const uint32_t col = 4u * (uint32_t)chunk;
+    tmem_st_32x32b_x4(base + col, r0);
+    tmem_st_32x32b_x4(base + 16u + col, r0);
+    tmem_st_32x32b_x4(base + 32u + col, r1);
+    tmem_st_32x32b_x4(base + 48u + col, r1);
+    uint32_t f[8];
+#pragma unroll
+    for (int z = 0; z < 8; ++z) f[z] = __float_as_uint(v[z]);
+    tmem_st_32x32b_x8(base + kRowBufF32 + 8u * (uint32_t)chunk, f);
+    tmem_st_wait();
+    tc_fence_before_sync();
+    __syncwarp();
+    if (lane == 0) {
+        mbar_arrive_cluster(rows_ready_even + 8u * (uint32_t)(nrb & 1));
+        mbar_arrive(qbar);
+    }
+    ok = mbar_wait(qbar, (uint32_t)(nqb & 1), args.status, abort_flag, kWaitLimitNs);
+    ++nqb;
+    ++nrb;
+    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
+    tc_fence_after_sync();
+    return true;
+}
+
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     merge_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                    const __grid_constant__ CUtensorMap tmap_bp,
                     const __grid_constant__ CUtensorMap tmap_ap,
                     const __grid_constant__ CUtensorMap tmap_af, const TcArgs args) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t* opA = smem;                   // [2]: B' rows of this CTA
-    uint8_t* opB = opA + 2 * kOpABytes;    // [2]: A' rows of this CTA's 64 columns
-    uint8_t* wring = opB + 2 * kOpBBytes;  // [2]: W tiles
-    uint8_t* xring = wring + 2 * kWBytes;  // [kXSlots]: fp32 strips of A
+    uint8_t* opB = smem;                          // [kOpSlots]: A' rows of this CTA's 64 columns
+    uint8_t* wring = opB + kOpSlots * kOpBBytes;  // [kWSlots]: W tiles
+    uint8_t* xring = wring + kWSlots * kWBytes;   // [kXSlots]: fp32 strips of A
     uint64_t* bars = reinterpret_cast<uint64_t*>(xring + kXSlots * kAfBytes);
-    uint64_t* w_full = bars;           // [2]
-    uint64_t* w_empty = bars + 2;      // [2] the 16 epilogue warps have copied their rows
-    uint64_t* op_full = bars + 4;      // [2] even CTA: both CTAs' operands have landed
-    uint64_t* op_empty = bars + 6;     // [2] the pair's MMAs have read the operands
-    uint64_t* tmem_full = bars + 8;    // [2]
-    uint64_t* tmem_empty = bars + 10;  // [2] even CTA
-    uint64_t* brow_bar = bars + 12;    // [4] per lane quarter: its 4 warps stored B rows
-    uint64_t* x_full = bars + 16;      // [kXSlots]
-    uint64_t* x_empty = bars + 16 + kXSlots;  // [kXSlots] the 16 epilogue warps
-    uint64_t* drain = bars + 16 + 2 * kXSlots;
+    uint64_t* w_full = bars;                         // [kWSlots]
+    uint64_t* w_empty = w_full + kWSlots;            // [kWSlots] the 16 epilogue warps
+    uint64_t* op_full = w_empty + kWSlots;           // [kOpSlots] even CTA: both CTAs' A'
+    uint64_t* op_empty = op_full + kOpSlots;         // [kOpSlots] the pair's MMAs are done
+    uint64_t* x_full = op_empty + kOpSlots;          // [kXSlots]
+    uint64_t* x_empty = x_full + kXSlots;            // [kXSlots] the 16 epilogue warps
+    uint64_t* tmem_full = x_empty + kXSlots;         // [2]
+    uint64_t* tmem_empty = tmem_full + 2;            // [2] even CTA
+    uint64_t* rows_ready = tmem_empty + 2;           // [2] even CTA: a row buffer is written
+    uint64_t* quarter_bar = rows_ready + 2;          // [4] the 4 warps of a lane quarter
+    uint64_t* drain = quarter_bar + 4;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -274,29 +414,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int nb_begin = t_begin / nks, ks_begin = t_begin - nb_begin * nks;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kWSlots; ++i) {
             mbar_init(&w_full[i], 1);
             mbar_init(&w_empty[i], kEpiWarps);
+        }
+        for (int i = 0; i < kOpSlots; ++i) {
             mbar_init(&op_full[i], 1);
             mbar_init(&op_empty[i], 1);
-            mbar_init(&tmem_full[i], 1);
-            mbar_init(&tmem_empty[i], kEpiWarps * kPair);
         }
-        for (int i = 0; i < 4; ++i) mbar_init(&brow_bar[i], kEpiWarps / 4);
         for (int i = 0; i < kXSlots; ++i) {
             mbar_init(&x_full[i], 1);
             mbar_init(&x_empty[i], kEpiWarps);
         }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&tmem_full[i], 1);
+            mbar_init(&tmem_empty[i], kEpiWarps * kPair);
+            mbar_init(&rows_ready[i], kEpiWarps * kPair);
+        }
+        for (int i = 0; i < 4; ++i) mbar_init(&quarter_bar[i], kEpiWarps / 4);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
         prefetch_tmap(&tmap_w);
-        prefetch_tmap(&tmap_bp);
-        prefetch_tmap(&tmap_ap);
         prefetch_tmap(&tmap_af);
     }
+    if (warp == 2 && lane == 0) prefetch_tmap(&tmap_ap);
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, kTmemCols);
         tmem_relinquish_pair();
@@ -307,38 +451,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
+    if (warp < kEpiWarp0) {
+        regs_decrease<kRegsCtl>();
     if (warp == 0) {
         if (lane == 0) {
-            // ------------------------------------------------ TMA (both CTAs)
-            const uint32_t op_full_even = map_to_rank(smem_u32(op_full), 0);
-            int nb = nb_begin, ks = ks_begin, nb_m1 = -1, nb_m2 = -1;  // row blocks of tiles i-1, i-2
-            int i = 0;
+            // ------------------------------------------------ TMA: W and strips of A
+            int nb = nb_begin, ks = ks_begin, i = 0;
             for (int t = t_begin; t < t_end; ++t, ++i) {
-                const int b = i & 1, xs = i % kXSlots;
-                const uint32_t ph = (uint32_t)((i >> 1) & 1) ^ 1u;
-                // Operand buffer b holds the B' rows of tile i - 2: reload if they differ.
-                const bool rows = nb != nb_m2;
+                const int ws = i % kWSlots, xs = i % kXSlots;
                 const int row0 = nb * (kTM * kPair) + (int)rank * kTM;
                 // W (the stream from HBM).
-                if (!mbar_wait(&w_empty[b], ph, args.status, abort_flag, kWaitLimitNs)) break;
-                uint8_t* wt = wring + b * kWBytes;
-                mbar_arrive_expect_tx(&w_full[b], kWBytes);
-                tma_load_2d(&tmap_w, &w_full[b], wt, ks * kTK, row0);
-                tma_load_2d(&tmap_w, &w_full[b], wt + kWBox, ks * kTK + 64, row0);
-                // The MMA operands, counted on the even CTA's barrier.
-                if (!mbar_wait(&op_empty[b], ph, args.status, abort_flag, kWaitLimitNs)) break;
-                if (leader)
-                    mbar_arrive_expect_tx(&op_full[b], kPair * (kOpBBytes + (rows ? kOpABytes : 0u)));
-                const uint32_t bar = op_full_even + 8u * (uint32_t)b;
-                const int arow = ks * kTK + (int)rank * (kTK / kPair);
-                uint8_t* ob = opB + b * kOpBBytes;
-                tma_load_2d_pair(&tmap_ap, bar, ob, 0, arow);
-                tma_load_2d_pair(&tmap_ap, bar, ob + kOpBBytes / 2, 64, arow);
-                if (rows) {
-                    uint8_t* oa = opA + b * kOpABytes;
-                    tma_load_2d_pair(&tmap_bp, bar, oa, 0, row0);
-                    tma_load_2d_pair(&tmap_bp, bar, oa + kOpABytes / 2, 64, row0);
-                }
+                if (!mbar_wait(&w_empty[ws], (uint32_t)((i / kWSlots) & 1) ^ 1u, args.status,
+                               abort_flag, kWaitLimitNs))
+                    break;
+                uint8_t* wt = wring + ws * kWBytes;
+                mbar_arrive_expect_tx(&w_full[ws], kWBytes);
+                tma_load_2d(&tmap_w, &w_full[ws], wt, ks * kTK, row0);
+                tma_load_2d(&tmap_w, &w_full[ws], wt + kWBox, ks * kTK + 64, row0);
                 // The fp32 strip of A: the slot's previous strip has landed (its phase is
                 // complete) and the epilogue is done with it.
                 const uint32_t xph = (uint32_t)((i / kXSlots) & 1) ^ 1u;
@@ -347,20 +476,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 mbar_arrive_expect_tx(&x_full[xs], kAfBytes);
                 tma_load_2d(&tmap_af, &x_full[xs], xring + xs * kAfBytes, ks * kTK, 0);
-                nb_m2 = nb_m1;
-                nb_m1 = nb;
                 if (++ks == nks) {
                     ks = 0;
                     ++nb;
                 }
             }
             if (!*abort_flag) {
-                // Tail: the last MMAs' releases of the operand buffers, and the last strips
-                // of A, land before exit.
-                for (int j = (i >= 2 ? i - 2 : 0); j < i; ++j)
-                    if (!mbar_wait(&op_empty[j & 1], (uint32_t)((j >> 1) & 1), args.status,
-                                   abort_flag, kWaitLimitNs))
-                        break;
+                // Tail: the last strips of A land before exit.
                 for (int j = (i >= kXSlots ? i - kXSlots : 0); j < i; ++j)
                     if (!mbar_wait(&x_full[j % kXSlots], (uint32_t)((j / kXSlots) & 1), args.status,
                                    abort_flag, kWaitLimitNs))
@@ -372,32 +494,75 @@ __global__ void __launch_bounds__(kThreads, 1)
                 while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
             }
         }
+    } else if (warp == 2) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA: A' (the MMA's B operand)
+            const uint32_t op_full_even = map_to_rank(smem_u32(op_full), 0);
+            int ks = ks_begin, i = 0;
+            for (int t = t_begin; t < t_end; ++t, ++i) {
+                const int os = i % kOpSlots;
+                if (!mbar_wait(&op_empty[os], (uint32_t)((i / kOpSlots) & 1) ^ 1u, args.status,
+                               abort_flag, kWaitLimitNs))
+                    break;
+                if (leader) mbar_arrive_expect_tx(&op_full[os], kPair * kOpBBytes);
+                const uint32_t bar = op_full_even + 8u * (uint32_t)os;
+                const int arow = ks * kTK + (int)rank * (kTK / kPair);
+                uint8_t* ob = opB + os * kOpBBytes;
+                tma_load_2d_pair(&tmap_ap, bar, ob, 0, arow);
+                tma_load_2d_pair(&tmap_ap, bar, ob + kOpBBytes / 2, 64, arow);
+                if (++ks == nks) ks = 0;
+            }
+            if (!*abort_flag) {
+                // Tail: the last MMAs' releases of the operand slots land before exit.
+                for (int j = (i >= kOpSlots ? i - kOpSlots : 0); j < i; ++j)
+                    if (!mbar_wait(&op_empty[j % kOpSlots], (uint32_t)((j / kOpSlots) & 1), args.status,
+                                   abort_flag, kWaitLimitNs))
+                        break;
+            }
+            if (*abort_flag) {
+                const uint64_t t0 = globaltimer_ns();
+                while (globaltimer_ns() - t0 < 2000000ull) __nanosleep(1000);
+            }
+        }
     } else if (warp == 1) {
         if (lane == 0 && leader) {
             // ------------------------------------------------ MMA issuer (even CTA)
             const uint32_t idesc = idesc_merge();
             bool any = false;
+            int nb = nb_begin, ks = ks_begin, rb = -1, nrb = 0;  // row block in use, buffers filled
             for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
-                const int b = i & 1;
-                if (!mbar_wait<true>(&op_full[b], (uint32_t)((i >> 1) & 1), args.status,
+                const int b = i & 1, os = i % kOpSlots;
+                if (nb != rb) {
+                    // A new row block: its [b0 b0 b1 b1] rows are written by the epilogue.
+                    if (!mbar_wait<true>(&rows_ready[nrb & 1], (uint32_t)((nrb >> 1) & 1), args.status,
+                                         abort_flag, kWaitLimitNs))
+                        break;
+                    rb = nb;
+                    ++nrb;
+                }
+                if (!mbar_wait<true>(&op_full[os], (uint32_t)((i / kOpSlots) & 1), args.status,
                                      abort_flag, kWaitLimitNs) ||
                     !mbar_wait<true>(&tmem_empty[b], ((i >> 1) & 1) ^ 1u, args.status,
                                      abort_flag, kWaitLimitNs))
                     break;
                 tc_fence_after_sync();
-                const uint64_t ad = smem_desc(smem_u32(opA + b * kOpABytes), 16, 1024, kLayoutSw128);
-                const uint64_t bd = smem_desc(smem_u32(opB + b * kOpBBytes), 16, 1024, kLayoutSw128);
+                const uint32_t a_col = tmem_base + kRowBuf0 + kRowBufCols * (uint32_t)((nrb - 1) & 1);
+                const uint64_t bd = smem_desc(smem_u32(opB + os * kOpBBytes), 16, 1024, kLayoutSw128);
 #pragma unroll
                 for (int kk = 0; kk < kJp / 16; ++kk) {
-                    // 16 bf16 (32 bytes) per step, 4 steps per 64-column atom.
-                    const uint64_t ao = (uint64_t)((kk >> 2) * ((kOpABytes / 2) >> 4) + (kk & 3) * 2);
+                    // 16 bf16 per step: 8 tensor-memory columns of A; 32 bytes of B, 4 steps
+                    // per 64-column atom.
                     const uint64_t bo = (uint64_t)((kk >> 2) * ((kOpBBytes / 2) >> 4) + (kk & 3) * 2);
-                    mma_bf16_pair(tmem_base + (uint32_t)(b * kTK), ad + ao, bd + bo, idesc,
-                                  kk > 0 ? 1u : 0u);
+                    mma_bf16_pair_ta(tmem_base + (uint32_t)(b * kTK), a_col + 8u * (uint32_t)kk, bd + bo,
+                                     idesc, kk > 0 ? 1u : 0u);
                 }
                 any = true;
-                mma_commit_pair_multicast(&op_empty[b], kBothCtas);
+                mma_commit_pair_multicast(&op_empty[os], kBothCtas);
                 mma_commit_pair_multicast(&tmem_full[b], kBothCtas);
+                if (++ks == nks) {
+                    ks = 0;
+                    ++nb;
+                }
             }
             if (*abort_flag && any) {
                 mma_commit_pair_multicast(drain, kEvenCta);
@@ -405,13 +570,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_wait(drain, 0, args.status, &dummy, kDrainLimitNs);
             }
         }
+    }
     } else {
-        // ------------------------------------------------ epilogue (warps 2-17, both CTAs)
+        regs_increase<kRegsEpi>();
+        // ------------------------------------------------ epilogue (warps 4-19, both CTAs)
         const int q = warp & 3;                             // tensor-memory lane quarter
         const int chunk = (warp - kEpiWarp0) >> 2;          // 0..3
         const int kt0 = chunk * kCols;                      // this warp's columns in the tile
         const int rloc = q * 32 + lane;                     // this thread's row in the CTA's 128
         const uint32_t tlane = (uint32_t)(q * 32) << 16;
+        const uint32_t rows_ready_even = map_to_rank(smem_u32(rows_ready), 0);
         const uint32_t tmem_empty_even = map_to_rank(smem_u32(tmem_empty), 0);
         const float c = args.c, ac = fabsf(args.c);
         float s = 0.0f, d = 0.0f, idlo = 0.0f, idhi = 0.0f;
@@ -425,7 +593,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             idlo = __fmul_rd(rd, 1.0f - 0x1p-19f);
             idhi = __fmul_ru(rd, 1.0f + 0x1p-19f);
         }
+        int nrb = 0, nqb = 0;  // row buffers written, quarter_bar phases
         int nb = nb_begin, ks = ks_begin;
+        bool alive = t_begin >= t_end ||
+                     write_rows(args, tmem_base, tlane, quarter_bar + q, rows_ready_even, nb_begin, rank, rloc,
+                                chunk, lane, nrb, nqb, abort_flag);
         // The norms for E (global, read one tile ahead) and, in pass 1, the running lower
         // bound of the tensor amax (any value s_t has held is one), read at the end of a
         // tile for use in the next.
@@ -436,9 +608,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             ra_next = k < args.K ? __ldg(args.cnorm + (k >> 7) * 4 + ((k >> 6) & 1)) : 0.0f;
         }
         float st_now = 0.0f, st_next = 0.0f;
-        int brow_nb = -1, brow_n = 0;  // row block whose B rows are in tensor memory; changes
-        for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
-            const int b = i & 1, xs = i % kXSlots;
+        int cur_buf = 0;  // row buffer of the current tile's row block
+        for (int t = t_begin, i = 0; alive && t < t_end; ++t, ++i) {
+            const int b = i & 1, ws = i % kWSlots, xs = i % kXSlots;
             const uint32_t ph = (uint32_t)((i >> 1) & 1);
             const int n = nb * (kTM * kPair) + (int)rank * kTM + rloc;
             const int k0 = ks * kTK + kt0;        // this warp's first column in W
@@ -454,40 +626,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int k = ks1 * kTK + kt0;
                 rb_next = __ldg(args.rnorm + nb1 * (kTM * kPair) + (int)rank * kTM + rloc);
                 ra_next = k < args.K ? __ldg(args.cnorm + (k >> 7) * 4 + ((k >> 6) & 1)) : 0.0f;
+                // The next tile starts a new row block: write its rows one tile ahead.
+                if (nb1 != nb && !write_rows(args, tmem_base, tlane, quarter_bar + q, rows_ready_even, nb1, rank,
+                                             rloc, chunk, lane, nrb, nqb, abort_flag))
+                    break;
             }
-            // New rows: this warp's 8 of the 32 columns of the rows' fp32 B into the next
-            // tensor-memory buffer; the quarter's 4 warps meet on brow_bar.
-            if (nb != brow_nb) {
-                uint32_t bv[8] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-                if (row_ok) {
-                    const uint4* src = reinterpret_cast<const uint4*>(args.B + (int64_t)n * kRank + 8 * chunk);
-                    const uint4 v0 = __ldg(src), v1 = __ldg(src + 1);
-                    bv[0] = v0.x; bv[1] = v0.y; bv[2] = v0.z; bv[3] = v0.w;
-                    bv[4] = v1.x; bv[5] = v1.y; bv[6] = v1.z; bv[7] = v1.w;
-                }
-                tmem_st_32x32b_x8(tmem_base + tlane + kBrowCol + 32u * (uint32_t)(brow_n & 1) + 8u * (uint32_t)chunk, bv);
-                tmem_st_wait();
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&brow_bar[q]);
-                const bool ok = mbar_wait(&brow_bar[q], (uint32_t)(brow_n & 1), args.status, abort_flag,
-                                          kWaitLimitNs);
-                if (!__all_sync(0xFFFFFFFFu, ok)) break;
-                tc_fence_after_sync();
-                brow_nb = nb;
-                ++brow_n;
-            }
-            const uint32_t tbrow = tmem_base + tlane + kBrowCol + 32u * (uint32_t)((brow_n - 1) & 1);
+            const uint32_t tbrow = tmem_base + tlane + kRowBuf0 + kRowBufCols * (uint32_t)cur_buf + kRowBufF32;
+            if (t + 1 < t_end && nb1 != nb) cur_buf ^= 1;  // from the next tile on
             // The accumulator's 32 columns (released at once) and this thread's 32 weights.
             bool ok = mbar_wait(&tmem_full[b], ph, args.status, abort_flag, kWaitLimitNs) &&
-                      mbar_wait(&w_full[b], ph, args.status, abort_flag, kWaitLimitNs);
+                      mbar_wait(&w_full[ws], (uint32_t)((i / kWSlots) & 1), args.status, abort_flag,
+                                kWaitLimitNs);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             tc_fence_after_sync();
             uint32_t acc[32];
             tmem_ld_32x32b_x32(tmem_base + tlane + (uint32_t)(b * kTK + kt0), acc);
             uint4 wr[4];
             {
-                const uint8_t* wb = wring + b * kWBytes + (kt0 >> 6) * kWBox + rloc * 128;
+                const uint8_t* wb = wring + ws * kWBytes + (kt0 >> 6) * kWBox + rloc * 128;
                 const int u0 = (kt0 & 63) >> 3;
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
@@ -525,7 +681,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                       __float_as_uint(wv[23]) ^ __float_as_uint(wv[31])) &
                                      (uint32_t)args.zero;
                 const uint32_t off = __any_sync(0xFFFFFFFFu, dep != 0u) ? 1u : 0u;
-                if (lane == 0) mbar_arrive(&w_empty[b] + off);
+                if (lane == 0) mbar_arrive(&w_empty[ws] + off);
             }
             // E for this row and these columns, every step rounded up.
             float E;
@@ -626,78 +782,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = mbar_wait(&x_full[xs], xph, args.status, abort_flag, kWaitLimitNs);
                     if (!__all_sync(0xFFFFFFFFu, ok)) break;
                     x_read = true;
-                    uint32_t bq[kRank];
-                    tmem_ld_32x32b_x32(tbrow, bq);
-                    tmem_ld_wait();
-                    if (slow) {
-                        // Blocks whose scale is uncertain: the 16 values by the exact chain
-                        // (16 chains side by side), then the scale and codes by true divisions.
-#pragma unroll 1
-                        for (int bk = 0; bk < 2; ++bk) {
-                            if (bk == 0 ? cert[0] : cert[1]) continue;
-                            const int kt = kt0 + 16 * bk;
-                            float x16[16];
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) x16[e] = 0.0f;
-#pragma unroll 2
-                            for (int j = 0; j < kRank; ++j) {
-                                const float bj = __uint_as_float(bq[j]);
-                                const float4* ar = reinterpret_cast<const float4*>(af + j * kTK + kt);
-#pragma unroll
-                                for (int q4 = 0; q4 < 4; ++q4) {
-                                    const float4 v = ar[q4];
-                                    x16[4 * q4] = __fmaf_rn(bj, v.x, x16[4 * q4]);
-                                    x16[4 * q4 + 1] = __fmaf_rn(bj, v.y, x16[4 * q4 + 1]);
-                                    x16[4 * q4 + 2] = __fmaf_rn(bj, v.z, x16[4 * q4 + 2]);
-                                    x16[4 * q4 + 3] = __fmaf_rn(bj, v.w, x16[4 * q4 + 3]);
-                                }
-                            }
-                            float bam = 0.0f;
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                x16[e] = __fmaf_rn(c, x16[e], bf16_sel(wr, 16 * bk + e));
-                                bam = fmaxf(bam, fabsf(x16[e]));
-                            }
-                            uint32_t sc = 0;
-                            if (d > 0.0f) sc = cvt_e4m3(__fdiv_rn(bam, d));
-                            const float dn = __fmul_rn(e4m3_value(sc), s);
-                            uint32_t c0 = 0u, c1 = 0u;
-                            if (dn > 0.0f) {
-#pragma unroll
-                                for (int e = 0; e < 16; ++e) x16[e] = __fdiv_rn(x16[e], dn);
-                                c0 = cvt_e2m1x8(x16[0], x16[1], x16[2], x16[3], x16[4], x16[5], x16[6], x16[7]);
-                                c1 = cvt_e2m1x8(x16[8], x16[9], x16[10], x16[11], x16[12], x16[13], x16[14], x16[15]);
-                            }
-                            if (bk == 0) {
-                                cw[0] = c0; cw[1] = c1; sfc[0] = sc;
-                            } else {
-                                cw[2] = c0; cw[3] = c1; sfc[1] = sc;
-                            }
-                        }
-                        // Elements whose two ends disagree (in blocks with a certain scale).
-                        uint32_t um = 0u;
-#pragma unroll
-                        for (int w = 0; w < 4; ++w)
-#pragma unroll
-                            for (int j = 0; j < 8; ++j)
-                                um |= (((diff[w] >> (4 * j)) & 0xFu) != 0u ? 1u : 0u) << (8 * w + j);
-                        if (!cert[0]) um &= 0xFFFF0000u;
-                        if (!cert[1]) um &= 0x0000FFFFu;
-#pragma unroll 1
-                        while (um != 0u) {
-                            const int e = __ffs((int)um) - 1;
-                            um &= um - 1u;
-                            const float x = exact_value(bq, af, kt0 + e, c, bf16_sel(wr, e));
-                            const uint32_t code =
-                                cvt_e2m1x8(__fdiv_rn(x, e < 16 ? den[0] : den[1]), 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 0xFu;
-                            const uint32_t sh = 4u * (uint32_t)(e & 7), keep = ~(0xFu << sh);
-                            const int wi = e >> 3;
-                            if (wi == 0) cw[0] = (cw[0] & keep) | (code << sh);
-                            else if (wi == 1) cw[1] = (cw[1] & keep) | (code << sh);
-                            else if (wi == 2) cw[2] = (cw[2] & keep) | (code << sh);
-                            else cw[3] = (cw[3] & keep) | (code << sh);
-                        }
-                    }
+                    Codes32 r;
+                    r.cw[0] = cw[0]; r.cw[1] = cw[1]; r.cw[2] = cw[2]; r.cw[3] = cw[3];
+                    r.sfc[0] = sfc[0]; r.sfc[1] = sfc[1];
+                    r = quant_fix(tbrow, af, kt0, c, s, d, r, make_uint4(diff[0], diff[1], diff[2], diff[3]),
+                                  den[0], den[1], cert[0], cert[1], slow, wr[0], wr[1], wr[2], wr[3]);
+                    cw[0] = r.cw[0]; cw[1] = r.cw[1]; cw[2] = r.cw[2]; cw[3] = r.cw[3];
+                    sfc[0] = r.sfc[0]; sfc[1] = r.sfc[1];
                 }
                 if (col_ok) {
                     if (row_ok)
@@ -754,7 +845,7 @@ cudaError_t run_merge_tc(const LaunchCtx& ctx, const RequantTcMaps& m, const TcA
     if (e != cudaSuccess) return e;
     const int clusters = a.tiles < max_clusters ? a.tiles : max_clusters;
     cfg.gridDim = dim3((unsigned)(clusters * kPair), 1, 1);
-    return cudaLaunchKernelEx(&cfg, merge_tc_kernel<kMode>, m.w, m.bp, m.ap, m.af, a);
+    return cudaLaunchKernelEx(&cfg, merge_tc_kernel<kMode>, m.w, m.ap, m.af, a);
 }
 
 }  // namespace
@@ -789,7 +880,7 @@ cudaError_t launch_requant_tc(const LaunchCtx& ctx, const RequantTcMaps& maps, c
     const int nb_rows = (rows_pad256 + kSplitRows - 1) / kSplitRows;
     const int nb_cols = (int)((K + kSplitCols - 1) / kSplitCols);
     merge_split_kernel<<<(unsigned)(nb_rows + nb_cols), kSplitThreads, 0, ctx.stream>>>(
-        A, B, (int)N, (int)K, rows_pad256, nb_rows, ws.bp, ws.ap, ws.rnorm, ws.cnorm, s_t);
+        A, B, (int)N, (int)K, rows_pad256, nb_rows, ws.ap, ws.rnorm, ws.cnorm, s_t);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if ((e = run_merge_tc<kModeAmax>(ctx, maps, a)) != cudaSuccess) return e;
