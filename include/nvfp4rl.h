@@ -193,6 +193,29 @@ nvfp4_status bf16_gemm(const void* X, const void* W, const void* bias, void* Y, 
 nvfp4_status select_contrastive(const float* rewards, int P, int N, int K, int global_std,
                                 int32_t* idx, float* r_out, void* stream);
 
+/*
+ * nvfp4_requant_noalloc — nvfp4_requant without a caller workspace.  The Sol-RL
+ * pages have no counterpart: this is a library convenience for callers that
+ * cannot hand over scratch memory.  Same arguments, results and errors as
+ * nvfp4_requant; where the tensor-core merge applies, its workspace is a fixed
+ * scratch array that the library reserves in device memory when it is loaded
+ * (NVFP4_NOALLOC_SCRATCH_BYTES per device), instead of caller memory.  The call
+ * itself allocates and frees nothing.
+ *   - Size limit: returns NVFP4_ERR_SHAPE when nvfp4_requant_workspace_bytes(...)
+ *     (256 K + 4 N + 16 K / 128 bytes, N rounded up to 256, each piece rounded up
+ *     to 256 bytes) exceeds NVFP4_NOALLOC_SCRATCH_BYTES: e.g. K = 16384 fits up to
+ *     N = 2^20 rows, K = 32768 up to 15360 rows, K = 65536 never.
+ *   - One scratch per device, shared by every call: two calls whose work can
+ *     overlap on the device (different streams without ordering between them)
+ *     race on it.  Order them (one stream, or events).
+ *   - The first call on each device looks up the scratch's address (a runtime
+ *     query, cached afterwards); make that first call outside any stream capture.
+ */
+#define NVFP4_NOALLOC_SCRATCH_BYTES ((size_t)8 * 1024 * 1024 + (size_t)64 * 1024)
+nvfp4_status nvfp4_requant_noalloc(const void* W, int w_dtype, const float* A, const float* B,
+                                   int r, float alpha, int64_t N, int64_t K, uint8_t* codes,
+                                   uint8_t* sf, float* s_t, void* stream);
+
 /* ---------------------------------------------------------------- diagnostics */
 
 /* Human-readable name of a status code (static storage). */

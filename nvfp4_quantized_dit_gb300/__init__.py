@@ -19,7 +19,7 @@ import torch
 
 __all__ = [
     "NVFP4Error", "library", "sf_bytes", "sf_offset",
-    "nvfp4_requant", "requant_workspace_bytes", "nvfp4_act_quant", "nvfp4_gemm", "bf16_gemm", "select_contrastive",
+    "nvfp4_requant", "requant_workspace_bytes", "nvfp4_requant_noalloc", "nvfp4_act_quant", "nvfp4_gemm", "bf16_gemm", "select_contrastive",
     "nvfp4_device_status", "nvfp4_status_string", "nvfp4_version",
     "nvfp4_test_e2m1", "nvfp4_test_e4m3", "nvfp4_test_e2m1_quotient", "nvfp4_test_e4m3_quotient",
     "nvfp4_test_e4m3_decode", "nvfp4_test_merge", "nvfp4_test_wait_timeout",
@@ -53,6 +53,7 @@ def library() -> ctypes.CDLL:
             P, I64, I, F = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_float
             sig = {
                 "nvfp4_requant": [P, I, P, P, I, F, I64, I64, P, P, P, P, ctypes.c_size_t, P],
+                "nvfp4_requant_noalloc": [P, I, P, P, I, F, I64, I64, P, P, P, P],
                 "nvfp4_act_quant": [P, I64, I64, P, P, P, P],
                 "nvfp4_gemm": [P, P, P, P, P, P, P, P, I64, I64, I64, P],
                 "bf16_gemm": [P, P, P, P, I64, I64, I64, P],
@@ -158,6 +159,29 @@ def nvfp4_requant(W, A=None, B=None, alpha: float = 32.0, codes=None, sf=None, s
     _call("nvfp4_requant", _dev(W, "W"), w_dtype, _opt(A, "A", torch.float32), _opt(B, "B", torch.float32),
           r, ctypes.c_float(alpha), N, K, _dev(codes, "codes", torch.uint8), _dev(sf, "sf", torch.uint8),
           _dev(s_t, "s_t", torch.float32), ws_ptr, ws_bytes, _stream(stream))
+    return codes, sf, s_t
+
+
+def nvfp4_requant_noalloc(W, A=None, B=None, alpha: float = 32.0, codes=None, sf=None, s_t=None,
+                          stream=None):
+    """nvfp4_requant with the library's fixed device scratch instead of a workspace
+    (outputs are still allocated here when the caller does not pass them)."""
+    if W.dim() != 2:
+        raise ValueError("W must be [N, K]")
+    N, K = W.shape
+    w_dtype = {torch.bfloat16: W_BF16, torch.float32: W_FP32}.get(W.dtype)
+    if w_dtype is None:
+        raise TypeError("W must be bfloat16 or float32")
+    r = 0 if (A is None or B is None) else A.shape[0]
+    if r and (tuple(A.shape) != (r, K) or tuple(B.shape) != (N, r)):
+        raise ValueError(f"LoRA shapes A {tuple(A.shape)} / B {tuple(B.shape)} do not match W {tuple(W.shape)}")
+    dev = W.device
+    codes = torch.empty(N, K // 2, dtype=torch.uint8, device=dev) if codes is None else codes
+    sf = torch.empty(sf_bytes(N, K), dtype=torch.uint8, device=dev) if sf is None else sf
+    s_t = torch.empty(1, dtype=torch.float32, device=dev) if s_t is None else s_t
+    _call("nvfp4_requant_noalloc", _dev(W, "W"), w_dtype, _opt(A, "A", torch.float32),
+          _opt(B, "B", torch.float32), r, ctypes.c_float(alpha), N, K, _dev(codes, "codes", torch.uint8),
+          _dev(sf, "sf", torch.uint8), _dev(s_t, "s_t", torch.float32), _stream(stream))
     return codes, sf, s_t
 
 

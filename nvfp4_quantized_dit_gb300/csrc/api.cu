@@ -16,6 +16,9 @@ namespace nvfp4rl {
 // Device status word: 0, or the first failure a kernel recorded (NVFP4_ERR_TIMEOUT).
 __device__ int g_status_word = 0;
 
+// Scratch of nvfp4_requant_noalloc (reserved with the module; one per device).
+__device__ __align__(256) uint8_t g_noalloc_scratch[NVFP4_NOALLOC_SCRATCH_BYTES];
+
 namespace {
 
 struct DeviceInfo {
@@ -26,6 +29,7 @@ struct DeviceInfo {
 };
 
 DeviceInfo g_devices[kMaxDevices];
+void* g_noalloc_addr[kMaxDevices];  // address of g_noalloc_scratch per device, once looked up
 std::mutex g_mutex;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -187,6 +191,34 @@ nvfp4_status nvfp4_requant(const void* W, int w_dtype, const float* A, const flo
     }
     return from_cuda(launch_requant(ctx, W, w_dtype, merge ? A : nullptr, merge ? B : nullptr,
                                     merge ? r : 0, c, N, K, codes, sf, s_t));
+}
+
+nvfp4_status nvfp4_requant_noalloc(const void* W, int w_dtype, const float* A, const float* B,
+                                   int r, float alpha, int64_t N, int64_t K, uint8_t* codes,
+                                   uint8_t* sf, float* s_t, void* stream) {
+    const bool merge = r > 0 && A != nullptr && B != nullptr;
+    const size_t need = merge ? nvfp4_requant_workspace_bytes(w_dtype, r, N, K) : 0;
+    if (need > NVFP4_NOALLOC_SCRATCH_BYTES) return NVFP4_ERR_SHAPE;
+    void* scratch = nullptr;
+    if (need > 0) {
+        int dev = -1;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+            cudaGetLastError();
+            return NVFP4_ERR_CUDA;
+        }
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (g_noalloc_addr[dev] == nullptr) {
+            void* p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+                cudaGetLastError();
+                return NVFP4_ERR_CUDA;
+            }
+            g_noalloc_addr[dev] = p;
+        }
+        scratch = g_noalloc_addr[dev];
+    }
+    return nvfp4_requant(W, w_dtype, A, B, r, alpha, N, K, codes, sf, s_t, scratch,
+                         scratch != nullptr ? NVFP4_NOALLOC_SCRATCH_BYTES : 0, stream);
 }
 
 nvfp4_status nvfp4_act_quant(const void* X, int64_t M, int64_t K, uint8_t* codes, uint8_t* sf,
