@@ -89,11 +89,12 @@ cudaError_t launch_requant(const LaunchCtx&, const void* W, int w_dtype, const f
 // Tensor-core merge (merge_tc.cu): bf16 W, rank 32, 16-byte aligned A and B, and a
 // workspace of requant_tc_workspace_bytes (0 when the path does not apply) laid out by
 // requant_tc_layout: A' [K, 128] bf16, rnorm [N rounded up to 256], cnorm [K / 128
-// rounded up][4].
+// rounded up][4], a CTA counter (finishing the per-tensor scale).
 struct RequantTcLayout {
     uint8_t* ap;
     float* rnorm;
     float* cnorm;
+    unsigned int* counter;
     size_t bytes;
 };
 inline RequantTcLayout requant_tc_layout(void* base, int64_t N, int64_t K) {
@@ -107,6 +108,8 @@ inline RequantTcLayout requant_tc_layout(void* base, int64_t N, int64_t K) {
     off += up((size_t)((N + 255) / 256 * 256) * 4);
     l.cnorm = reinterpret_cast<float*>(p + off);
     off += up((size_t)((K + 127) / 128) * 16);
+    l.counter = reinterpret_cast<unsigned int*>(p + off);
+    off += 256;
     l.bytes = off;
     return l;
 }
@@ -573,6 +576,16 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
             "r"(smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel on the stream (launched with the
+// programmatic-serialization attribute) start, and wait until the previous one has
+// completed with its memory visible.
+__device__ __forceinline__ void grid_dep_launch() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap* map) {

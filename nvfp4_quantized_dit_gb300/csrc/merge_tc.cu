@@ -43,9 +43,8 @@
 // clusters of two CTAs; a pair tile is 256 weight rows (128 per CTA) x 128 columns,
 // walked k-strip first, so the rows of B usually stay the same from one tile to the
 // next.  Per CTA, 20 warps:
-//   warp 0      TMA: W tiles (128 x 128 bf16; 4 slots, freed as soon as every epilogue
-//               warp has copied its rows into registers) and the fp32 strip of A for the
-//               exact chain (3 slots);
+//   warp 0      TMA: W tiles (128 x 128 bf16; 4 slots) and the fp32 strip of A for the
+//               exact chain (3 slots), each freed when the epilogue is done with the tile;
 //   warp 1      tensor-memory allocation; lane 0 of the even CTA issues the 8 pair MMAs
 //               (kind::f16, M = 256, N = 128, A from tensor memory) into a
 //               double-buffered accumulator;
@@ -97,7 +96,7 @@ constexpr int kSplitCols = kSplitThreads / 4;  // columns of A per split block (
 // Registers: launched at 96 per thread (20 warps, 5 per scheduler); the control warp
 // group drops to 32 and the epilogue warp groups rise to 112 (4 x 32 + 16 x 112 <=
 // 20 x 96).
-constexpr uint32_t kRegsCtl = 32, kRegsEpi = 112;
+constexpr uint32_t kRegsCtl = 56, kRegsEpi = 104;
 static_assert(4 * kRegsCtl + kEpiWarps * kRegsEpi <= (uint32_t)(kThreads / 32) * 96, "register split");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 static_assert(kRowBuf0 + 2 * kRowBufCols <= kTmemCols, "tensor memory budget");
@@ -118,6 +117,7 @@ struct TcArgs {
     const float* B;      // [N, 32] fp32
     const float* cnorm;  // [K/128][4]: per 128-column strip, the largest ||A[:,k]||_2
                          // of each 64-column half (upper bounds), then 2 unused
+    unsigned int* counter;  // CTAs of the quantize pass that are done (zeroed by the split)
     int* status;
     int zero;    // 0 (a value the compiler cannot see; used for data dependencies)
     int nks;     // 128-column strips
@@ -158,16 +158,20 @@ __device__ __forceinline__ void split8(const float* v, uint4& p0, uint4& p1) {
 // Four threads per row of B or column of A (8 values each).  Blocks [0, nb_rows) take
 // 64 rows of B: rnorm[n] (0 for the padding rows up to rows_pad256).  The other blocks
 // take 64 columns of A: A'[k] = [a0 a1 a0 a1] and the block's largest column norm.
-// Block 0 also clears the amax accumulator s_t.
+// Block 0 also clears the amax accumulator s_t and the quantize pass's CTA counter.
 __global__ void __launch_bounds__(kSplitThreads)
     merge_split_kernel(const float* __restrict__ A, const float* __restrict__ B, int N, int K,
                        int rows_pad256, int nb_rows, uint8_t* __restrict__ Ap,
                        float* __restrict__ rnorm, float* __restrict__ cnorm,
-                       float* __restrict__ s_t) {
+                       float* __restrict__ s_t, unsigned int* __restrict__ counter) {
     __shared__ float red[kSplitThreads];
     __shared__ float red2[kSplitCols / 32];
     const int tid = (int)threadIdx.x;
-    if (blockIdx.x == 0 && tid == 0) *s_t = 0.0f;
+    grid_dep_launch();  // the amax pass may start streaming W at once
+    if (blockIdx.x == 0 && tid == 0) {
+        *s_t = 0.0f;
+        *counter = 0u;
+    }
     float v[8];
     if ((int)blockIdx.x < nb_rows) {
         const int n = (int)blockIdx.x * kSplitRows + (tid >> 2), g = tid & 3;
@@ -218,12 +222,13 @@ __global__ void __launch_bounds__(kSplitThreads)
     }
 }
 
-// Element e (0..31) of 32 bf16 held as 16 packed pairs, as fp32.
-__device__ __forceinline__ float bf16_sel(const uint4 (&w)[4], int e) {
-    const uint4 v = (e >> 3) == 0 ? w[0] : (e >> 3) == 1 ? w[1] : (e >> 3) == 2 ? w[2] : w[3];
-    const int p = (e >> 1) & 3;
-    const uint32_t pr = p == 0 ? v.x : p == 1 ? v.y : p == 2 ? v.z : v.w;
-    return __uint_as_float((e & 1) ? (pr & 0xFFFF0000u) : (pr << 16));
+// W[row, kt] of a W tile in shared memory (bf16, two 64-column boxes with the 128-byte
+// swizzle: the 16-byte chunk u of a row sits at chunk u ^ (row % 8)).
+__device__ __forceinline__ float w_at(const uint8_t* wt, int row, int kt) {
+    const int u = (kt & 63) >> 3;
+    const uint16_t h = *reinterpret_cast<const uint16_t*>(
+        wt + (kt >> 6) * kWBox + row * 128 + ((u ^ (row & 7)) << 4) + (kt & 7) * 2);
+    return __uint_as_float((uint32_t)h << 16);
 }
 
 // The library's merged value of one element (the fp32 fma chain, in order): b = the
@@ -244,20 +249,18 @@ __device__ __forceinline__ float exact_value(const uint32_t (&b)[kRank], const f
 // values from the exact chain (16 chains side by side), then the scale and codes by
 // true divisions; elements whose interval ends disagree (diff) get their code from
 // the exact chain.  tbrow is the tensor-memory address of the fp32 rows of B, af the
-// fp32 strip of A, w the 32 weights.
+// fp32 strip of A, wt the W tile in shared memory and row this thread's row in it.
 struct Codes32 {
     uint32_t cw[4];
     uint32_t sfc[2];
 };
-__device__ __noinline__ Codes32 quant_fix(uint32_t tbrow, const float* af, int kt0, float c, float s,
+__device__ __forceinline__ Codes32 quant_fix(uint32_t tbrow, const float* af, int kt0, float c, float s,
                                           float d, Codes32 r, uint4 diff, float den0, float den1,
-                                          bool cert0, bool cert1, bool slow, uint4 w0, uint4 w1, uint4 w2,
-                                          uint4 w3) {
+                                          bool cert0, bool cert1, bool slow, const uint8_t* wt, int row) {
     uint32_t bq[kRank];
     tmem_ld_32x32b_x32(tbrow, bq);
     tmem_ld_wait();
     if (!slow) return r;
-    const uint4 wr[4] = {w0, w1, w2, w3};
 #pragma unroll 1
     for (int bk = 0; bk < 2; ++bk) {
         if (bk == 0 ? cert0 : cert1) continue;
@@ -281,7 +284,7 @@ __device__ __noinline__ Codes32 quant_fix(uint32_t tbrow, const float* af, int k
         float bam = 0.0f;
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-            x16[e] = __fmaf_rn(c, x16[e], bf16_sel(wr, 16 * bk + e));
+            x16[e] = __fmaf_rn(c, x16[e], w_at(wt, row, kt + e));
             bam = fmaxf(bam, fabsf(x16[e]));
         }
         uint32_t sc = 0;
@@ -313,7 +316,7 @@ __device__ __noinline__ Codes32 quant_fix(uint32_t tbrow, const float* af, int k
     while (um != 0u) {
         const int e = __ffs((int)um) - 1;
         um &= um - 1u;
-        const float x = exact_value(bq, af, kt0 + e, c, bf16_sel(wr, e));
+        const float x = exact_value(bq, af, kt0 + e, c, w_at(wt, row, kt0 + e));
         const uint32_t code = cvt_e2m1x8(__fdiv_rn(x, e < 16 ? den0 : den1), 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 0xFu;
         const uint32_t sh = 4u * (uint32_t)(e & 7), keep = ~(0xFu << sh);
         const int wi = e >> 3;
@@ -377,6 +380,23 @@ __device__ __forceinline__ bool write_rows(const TcArgs& args, uint32_t tmem_bas
     return true;
 }
 
+// Pass 1's candidate path (called by the whole warp): the largest |W'| over the
+// elements of `mask` (this thread's columns kt0 + e), by the exact chain.
+__device__ __forceinline__ float amax_exact(uint32_t tbrow, const float* af, int kt0, float c, uint32_t mask,
+                                         const uint8_t* wt, int row) {
+    uint32_t bq[kRank];
+    tmem_ld_32x32b_x32(tbrow, bq);
+    tmem_ld_wait();
+    float em = 0.0f;
+#pragma unroll 1
+    while (mask != 0u) {
+        const int e = __ffs((int)mask) - 1;
+        mask &= mask - 1u;
+        em = fmaxf(em, fabsf(exact_value(bq, af, kt0 + e, c, w_at(wt, row, kt0 + e))));
+    }
+    return em;
+}
+
 template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
     merge_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
@@ -412,6 +432,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Tile t of the pair's range: row block t / nks, strip t % nks (walked strip first).
     const int nks = args.nks;
     const int nb_begin = t_begin / nks, ks_begin = t_begin - nb_begin * nks;
+    // The next pass may start as SMs free up: W does not depend on this one.  What
+    // depends on the previous kernel (A', the norms, s_t) is read after grid_dep_wait.
+    if (kMode == kModeAmax) grid_dep_launch();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kWSlots; ++i) {
@@ -497,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 2) {
         if (lane == 0) {
             // ------------------------------------------------ TMA: A' (the MMA's B operand)
+            grid_dep_wait();  // A' is written by the split kernel
             const uint32_t op_full_even = map_to_rank(smem_u32(op_full), 0);
             int ks = ks_begin, i = 0;
             for (int t = t_begin; t < t_end; ++t, ++i) {
@@ -584,6 +608,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float c = args.c, ac = fabsf(args.c);
         float s = 0.0f, d = 0.0f, idlo = 0.0f, idhi = 0.0f;
         bool d_fast = false;
+        int nrb = 0, nqb = 0;  // row buffers written, quarter_bar phases
+        // The first row block's rows (B is an input: no wait), then the previous kernel's
+        // results (norms, s_t).
+        bool alive = t_begin >= t_end ||
+                     write_rows(args, tmem_base, tlane, quarter_bar + q, rows_ready_even, nb_begin, rank, rloc,
+                                chunk, lane, nrb, nqb, abort_flag);
+        grid_dep_wait();
         if (kMode == kModeQuant) {
             const float amax = *reinterpret_cast<volatile const float*>(args.s_t);
             s = __fdiv_rn(amax, kAmaxDiv);
@@ -593,11 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             idlo = __fmul_rd(rd, 1.0f - 0x1p-19f);
             idhi = __fmul_ru(rd, 1.0f + 0x1p-19f);
         }
-        int nrb = 0, nqb = 0;  // row buffers written, quarter_bar phases
         int nb = nb_begin, ks = ks_begin;
-        bool alive = t_begin >= t_end ||
-                     write_rows(args, tmem_base, tlane, quarter_bar + q, rows_ready_even, nb_begin, rank, rloc,
-                                chunk, lane, nrb, nqb, abort_flag);
         // The norms for E (global, read one tile ahead) and, in pass 1, the running lower
         // bound of the tensor amax (any value s_t has held is one), read at the end of a
         // tile for use in the next.
@@ -639,11 +666,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 kWaitLimitNs);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
             tc_fence_after_sync();
+            const uint8_t* wt = wring + ws * kWBytes;  // this tile's W, held until the tile's end
             uint32_t acc[32];
             tmem_ld_32x32b_x32(tmem_base + tlane + (uint32_t)(b * kTK + kt0), acc);
             uint4 wr[4];
             {
-                const uint8_t* wb = wring + ws * kWBytes + (kt0 >> 6) * kWBox + rloc * 128;
+                const uint8_t* wb = wt + (kt0 >> 6) * kWBox + rloc * 128;
                 const int u0 = (kt0 & 63) >> 3;
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
@@ -670,18 +698,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                         wv[e + 1] = y.y;
                     }
                 }
-            }
-            // The W slot goes back to the producer only after every lane's shared-memory
-            // reads of it have returned: the vote reads a value computed from all four
-            // loads in every lane, and the arrival's address depends on the vote (its
-            // offset is 0: args.zero == 0).  A proxy fence here would also wait for the
-            // previous tile's global stores.
-            {
-                const uint32_t dep = (__float_as_uint(wv[7]) ^ __float_as_uint(wv[15]) ^
-                                      __float_as_uint(wv[23]) ^ __float_as_uint(wv[31])) &
-                                     (uint32_t)args.zero;
-                const uint32_t off = __any_sync(0xFFFFFFFFu, dep != 0u) ? 1u : 0u;
-                if (lane == 0) mbar_arrive(&w_empty[ws] + off);
             }
             // E for this row and these columns, every step rounded up.
             float E;
@@ -715,16 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ok = mbar_wait(&x_full[xs], xph, args.status, abort_flag, kWaitLimitNs);
                     if (!__all_sync(0xFFFFFFFFu, ok)) break;
                     x_read = true;
-                    uint32_t bq[kRank];
-                    tmem_ld_32x32b_x32(tbrow, bq);
-                    tmem_ld_wait();
-#pragma unroll 1
-                    while (mask != 0u) {
-                        const int e = __ffs((int)mask) - 1;
-                        mask &= mask - 1u;
-                        em = fmaxf(em, fabsf(exact_value(bq, af, kt0 + e, c, bf16_sel(wr, e))));
-                    }
-                    em = warp_max_f(em);
+                    em = warp_max_f(amax_exact(tbrow, af, kt0, c, mask, wt, rloc));
                 }
                 const float best = fmaxf(em, lo);
                 // |W'| >= 0: the fp32 bit patterns order like the values.
@@ -735,8 +742,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint32_t cw[4], diff[4], sfc[2];
                 float den[2];
                 bool cert[2];
+                float Eb = E;
 #pragma unroll
                 for (int bk = 0; bk < 2; ++bk) {
+                    if (bk == 1) {
+                        // Block 1 after block 0 (an empty asm that "reads" block 0's results
+                        // and "writes" E): keeps the two blocks' temporaries from being
+                        // live at once.
+                        asm volatile("" : "+f"(Eb) : "r"(cw[0]), "r"(cw[1]), "r"(diff[0]), "r"(diff[1]));
+                    }
+                    const float E = Eb;
                     const float* x = wv + 16 * bk;
                     float bam = 0.0f;
 #pragma unroll
@@ -754,27 +769,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const float rr = fast ? recip_approx(den[bk]) : 0.0f;
                     const float2 rlo = make_float2(__fmul_rd(rr, 1.0f - 0x1p-19f), __fmul_rd(rr, 1.0f - 0x1p-19f));
                     const float2 rhi = make_float2(__fmul_ru(rr, 1.0f + 0x1p-19f), __fmul_ru(rr, 1.0f + 0x1p-19f));
-                    // Element codes: both ends of [|w~| - E, |w~| + E], with w~'s sign.
-                    float lo16[16], hi16[16];
+                    // Element codes: both ends of [|w~| - E, |w~| + E], with w~'s sign, 8
+                    // elements at a time.
 #pragma unroll
-                    for (int e = 0; e < 16; e += 2) {
-                        const float2 xv = make_float2(x[e], x[e + 1]);
-                        const float2 sE = make_float2(copysignf(E, x[e]), copysignf(E, x[e + 1]));
-                        const float2 l = __fmul2_rn(__ffma2_rn(make_float2(-1.0f, -1.0f), sE, xv), rlo);
-                        const float2 h = __fmul2_rn(__fadd2_rn(xv, sE), rhi);
-                        lo16[e] = l.x;
-                        lo16[e + 1] = l.y;
-                        hi16[e] = h.x;
-                        hi16[e + 1] = h.y;
+                    for (int g = 0; g < 2; ++g) {
+                        float lo8[8], hi8[8];
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) {
+                            const float2 xv = make_float2(x[8 * g + e], x[8 * g + e + 1]);
+                            const float2 sE = make_float2(copysignf(E, xv.x), copysignf(E, xv.y));
+                            const float2 l = __fmul2_rn(__ffma2_rn(make_float2(-1.0f, -1.0f), sE, xv), rlo);
+                            const float2 h = __fmul2_rn(__fadd2_rn(xv, sE), rhi);
+                            lo8[e] = l.x;
+                            lo8[e + 1] = l.y;
+                            hi8[e] = h.x;
+                            hi8[e + 1] = h.y;
+                        }
+                        const uint32_t lw = cvt_e2m1x8(lo8[0], lo8[1], lo8[2], lo8[3], lo8[4], lo8[5], lo8[6], lo8[7]);
+                        const uint32_t hw = cvt_e2m1x8(hi8[0], hi8[1], hi8[2], hi8[3], hi8[4], hi8[5], hi8[6], hi8[7]);
+                        cw[2 * bk + g] = live ? hw : 0u;
+                        diff[2 * bk + g] = !live ? 0u : fast ? (lw ^ hw) : 0xFFFFFFFFu;
                     }
-                    const uint32_t l0 = cvt_e2m1x8(lo16[0], lo16[1], lo16[2], lo16[3], lo16[4], lo16[5], lo16[6], lo16[7]);
-                    const uint32_t l1 = cvt_e2m1x8(lo16[8], lo16[9], lo16[10], lo16[11], lo16[12], lo16[13], lo16[14], lo16[15]);
-                    const uint32_t h0 = cvt_e2m1x8(hi16[0], hi16[1], hi16[2], hi16[3], hi16[4], hi16[5], hi16[6], hi16[7]);
-                    const uint32_t h1 = cvt_e2m1x8(hi16[8], hi16[9], hi16[10], hi16[11], hi16[12], hi16[13], hi16[14], hi16[15]);
-                    cw[2 * bk] = live ? h0 : 0u;
-                    cw[2 * bk + 1] = live ? h1 : 0u;
-                    diff[2 * bk] = !live ? 0u : fast ? (l0 ^ h0) : 0xFFFFFFFFu;
-                    diff[2 * bk + 1] = !live ? 0u : fast ? (l1 ^ h1) : 0xFFFFFFFFu;
                 }
                 const bool slow = row_ok && col_ok &&
                                   (!cert[0] || !cert[1] || (diff[0] | diff[1] | diff[2] | diff[3]) != 0u);
@@ -786,7 +801,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     r.cw[0] = cw[0]; r.cw[1] = cw[1]; r.cw[2] = cw[2]; r.cw[3] = cw[3];
                     r.sfc[0] = sfc[0]; r.sfc[1] = sfc[1];
                     r = quant_fix(tbrow, af, kt0, c, s, d, r, make_uint4(diff[0], diff[1], diff[2], diff[3]),
-                                  den[0], den[1], cert[0], cert[1], slow, wr[0], wr[1], wr[2], wr[3]);
+                                  den[0], den[1], cert[0], cert[1], slow, wt, rloc);
                     cw[0] = r.cw[0]; cw[1] = r.cw[1]; cw[2] = r.cw[2]; cw[3] = r.cw[3];
                     sfc[0] = r.sfc[0]; sfc[1] = r.sfc[1];
                 }
@@ -801,11 +816,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             (uint16_t)(sfc[0] | (sfc[1] << 8));
                 }
             }
-            // Done with this tile's strip of A (reads, if any, were consumed by the exact
-            // chain, and fenced against the TMA that will overwrite the slot).
+            // Done with this tile's W and strip of A: every shared-memory read of them has
+            // returned (its value was used), and, where the exact chain read them, is
+            // fenced against the TMA that will overwrite the slots.
             if (x_read) fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&x_empty[xs]);
+            if (lane == 0) {
+                mbar_arrive(&w_empty[ws]);
+                mbar_arrive(&x_empty[xs]);
+            }
             nb = nb1;
             ks = ks1;
         }
@@ -814,6 +833,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     tc_fence_before_sync();
     __syncthreads();
+    if (kMode == kModeQuant && threadIdx.x == 0) {
+        // The last CTA to finish (every CTA has read s_t by now) turns the tensor amax
+        // into the per-tensor scale.
+        __threadfence();
+        if (atomicAdd(args.counter, 1u) == gridDim.x - 1) {
+            volatile float* st = args.s_t;
+            *st = __fdiv_rn(*st, kAmaxDiv);
+        }
+    }
     cluster_sync_all();
     if (warp == 1) {
         tc_fence_after_sync();
@@ -821,19 +849,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-__global__ void merge_tc_finalize_kernel(float* s_t) {
-    if (threadIdx.x == 0 && blockIdx.x == 0) *s_t = __fdiv_rn(*s_t, kAmaxDiv);
-}
-
 template <int kMode>
 cudaError_t run_merge_tc(const LaunchCtx& ctx, const RequantTcMaps& m, const TcArgs& a) {
     static OccupancyCache occupancy;
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = kPair;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    // May start before the previous kernel on the stream ends (programmatic dependent
+    // launch); the kernel waits (griddepcontrol.wait) before reading its results.
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(kThreads, 1, 1);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = ctx.stream;
@@ -845,6 +873,7 @@ cudaError_t run_merge_tc(const LaunchCtx& ctx, const RequantTcMaps& m, const TcA
     if (e != cudaSuccess) return e;
     const int clusters = a.tiles < max_clusters ? a.tiles : max_clusters;
     cfg.gridDim = dim3((unsigned)(clusters * kPair), 1, 1);
+    cfg.numAttrs = 2;
     return cudaLaunchKernelEx(&cfg, merge_tc_kernel<kMode>, m.w, m.ap, m.af, a);
 }
 
@@ -870,6 +899,7 @@ cudaError_t launch_requant_tc(const LaunchCtx& ctx, const RequantTcMaps& maps, c
     a.sf = sf;
     a.s_t = s_t;
     a.rnorm = ws.rnorm;
+    a.counter = ws.counter;
     a.B = B;
     a.cnorm = ws.cnorm;
     a.status = ctx.status;
@@ -880,13 +910,11 @@ cudaError_t launch_requant_tc(const LaunchCtx& ctx, const RequantTcMaps& maps, c
     const int nb_rows = (rows_pad256 + kSplitRows - 1) / kSplitRows;
     const int nb_cols = (int)((K + kSplitCols - 1) / kSplitCols);
     merge_split_kernel<<<(unsigned)(nb_rows + nb_cols), kSplitThreads, 0, ctx.stream>>>(
-        A, B, (int)N, (int)K, rows_pad256, nb_rows, ws.ap, ws.rnorm, ws.cnorm, s_t);
+        A, B, (int)N, (int)K, rows_pad256, nb_rows, ws.ap, ws.rnorm, ws.cnorm, s_t, ws.counter);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if ((e = run_merge_tc<kModeAmax>(ctx, maps, a)) != cudaSuccess) return e;
-    if ((e = run_merge_tc<kModeQuant>(ctx, maps, a)) != cudaSuccess) return e;
-    merge_tc_finalize_kernel<<<1, 32, 0, ctx.stream>>>(s_t);
-    return cudaGetLastError();
+    return run_merge_tc<kModeQuant>(ctx, maps, a);
 }
 
 }  // namespace nvfp4rl

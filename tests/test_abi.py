@@ -94,14 +94,14 @@ def test_requant_validation(lib):
 
 def test_requant_workspace_bytes(lib):
     """The tensor-core merge's workspace: A' (256 bytes per column of A), the row
-    norms (rows padded to 256) and 16 bytes of column norms per 128 columns, each
-    piece rounded up to 256 bytes; 0 where that path does not apply."""
+    norms (rows padded to 256), 16 bytes of column norms per 128 columns and a
+    counter, each piece rounded up to 256 bytes; 0 where that path does not apply."""
     ws = lib.nvfp4_requant_workspace_bytes
     ws.restype = ctypes.c_size_t
     ws.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int64, ctypes.c_int64]
     up = lambda x: (x + 255) // 256 * 256
-    assert ws(0, 32, 300, 192) == up(192 * 256) + up(512 * 4) + up(2 * 16)
-    assert ws(0, 32, 12288, 3072) == 3072 * 256 + 12288 * 4 + 512
+    assert ws(0, 32, 300, 192) == up(192 * 256) + up(512 * 4) + up(2 * 16) + 256
+    assert ws(0, 32, 12288, 3072) == 3072 * 256 + 12288 * 4 + 512 + 256
     assert ws(1, 32, 300, 192) == 0     # fp32 W: CUDA-core merge
     assert ws(0, 16, 300, 192) == 0     # rank other than 32
     assert ws(0, 32, 300, 100) == 0     # K % 64
