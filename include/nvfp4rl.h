@@ -144,7 +144,8 @@ size_t nvfp4_requant_workspace_bytes(int w_dtype, int r, int64_t N, int64_t K);
  *   codes  device, [M, K/2] bytes (out).
  *   sf     device, nvfp4_sf_bytes(M, K) bytes (out, padding rows written 0).
  *   s_row  device, [M] fp32 (out): amax(|X[m,:]|) / 2688.
- *   K % 64 == 0, K <= 32768, M < 2^31.  One kernel, one pass over X.
+ *   K % 64 == 0, K <= 32768, M < 2^31.  X must be finite.  One kernel, one
+ *   pass over X.
  */
 nvfp4_status nvfp4_act_quant(const void* X, int64_t M, int64_t K, uint8_t* codes, uint8_t* sf,
                              float* s_row, void* stream);

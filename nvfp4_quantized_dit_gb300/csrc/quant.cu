@@ -85,23 +85,39 @@ __device__ __forceinline__ uint32_t gather_sf_word(uint32_t sfc) {
 // ------------------------------------------------------------------ act_quant
 
 // Persistent, several 8-warp CTAs per SM.  Warps form groups of G (32 G threads per
-// row); each group owns a ring of kAqRing row buffers in shared memory that one lane
-// fills with bulk copies (kAqRing rows ahead; a shallow ring keeps more CTAs per SM,
-// which measured faster than a deeper one), so HBM streams while the group
-// quantizes earlier rows from shared memory.  One lane per 16-element block:
+// row, G as small as 8 blocks per thread allows); each group owns kAqRing row buffers
+// in shared memory that one lane fills with bulk copies.  A single buffer per group
+// measured fastest: shared memory then holds the most groups per SM, and HBM streams
+// while the other groups quantize their rows.  One lane per 16-element block:
 //   pass 1: block maxima on packed bf16 pairs (kept in registers), row amax (warp
 //           shuffles, then shared memory across the group's warps);
 //   pass 2: the block's E4M3 scale, its 16 E2M1 codes (8 bytes), and one scale
 //           word per 4 blocks.
 // Rows M..rows_pad-1 are scale padding: their scale words are written as 0.
 constexpr int kAqWarps = 8;
-constexpr int kAqRing = 2;
+constexpr int kAqRing = 1;
 constexpr int kAqMaxBpt = 8;  // 16-element blocks per thread (K <= 4096 * G)
 
 __device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t m, uint32_t w) {
     // Max of magnitudes, lane-wise on two bf16 values: clearing the sign bits makes the
     // bit patterns order like the magnitudes, so an unsigned 16-bit max is exact.
     return __vmaxu2(m, w & 0x7FFF7FFFu);
+}
+
+// Lane-wise magnitudes of two bf16 values.
+__device__ __forceinline__ __nv_bfloat162 bf16x2_abs(uint32_t w) {
+    return __habs2(*reinterpret_cast<const __nv_bfloat162*>(&w));
+}
+
+// Largest magnitude in each half of 16 bf16 values (8 words), as a bf16 pair; exact
+// for finite inputs.
+__device__ __forceinline__ uint32_t bf16x16_absmax(const uint4& u0, const uint4& u1) {
+    const __nv_bfloat162 m01 = __hmax2(bf16x2_abs(u0.x), bf16x2_abs(u0.y));
+    const __nv_bfloat162 m23 = __hmax2(bf16x2_abs(u0.z), bf16x2_abs(u0.w));
+    const __nv_bfloat162 m45 = __hmax2(bf16x2_abs(u1.x), bf16x2_abs(u1.y));
+    const __nv_bfloat162 m67 = __hmax2(bf16x2_abs(u1.z), bf16x2_abs(u1.w));
+    const __nv_bfloat162 m = __hmax2(__hmax2(m01, m23), __hmax2(m45, m67));
+    return *reinterpret_cast<const uint32_t*>(&m);
 }
 
 template <int G>
@@ -161,15 +177,7 @@ __global__ void __launch_bounds__(kAqWarps * 32)
             const int b = t + i * kThreadsPerRow;
             float bm = 0.0f;
             if (valid && b < nblk) {
-                const uint4 u0 = srow[2 * b], u1 = srow[2 * b + 1];
-                uint32_t mm = bf16x2_absmax(0u, u0.x);
-                mm = bf16x2_absmax(mm, u0.y);
-                mm = bf16x2_absmax(mm, u0.z);
-                mm = bf16x2_absmax(mm, u0.w);
-                mm = bf16x2_absmax(mm, u1.x);
-                mm = bf16x2_absmax(mm, u1.y);
-                mm = bf16x2_absmax(mm, u1.z);
-                mm = bf16x2_absmax(mm, u1.w);
+                const uint32_t mm = bf16x16_absmax(srow[2 * b], srow[2 * b + 1]);
                 bm = fmaxf(bf16_lo(mm), bf16_hi(mm));
             }
             bmax[i] = bm;
@@ -207,15 +215,10 @@ __global__ void __launch_bounds__(kAqWarps * 32)
                 unpack8(srow[2 * b + 1], x);
                 packed.y = e2m1_quotient8(x, den, rc);
             }
-            // Scale codes of blocks b..b+3 (lanes l..l+3, l % 4 == 0) -> one word.
-            const uint32_t s1 = __shfl_down_sync(kFull, sfc, 1);
-            const uint32_t s2 = __shfl_down_sync(kFull, sfc, 2);
-            const uint32_t s3 = __shfl_down_sync(kFull, sfc, 3);
+            // One scale byte per lane: lanes l..l+3 (l % 4 == 0) fill one 4-byte word.
             if (have) {
                 if (valid) crow[b] = packed;
-                if ((b & 3) == 0)
-                    *reinterpret_cast<uint32_t*>(sf + sf_word_offset(m, b, K)) =
-                        sfc | (s1 << 8) | (s2 << 16) | (s3 << 24);
+                sf[sf_word_offset(m, b, K) + (b & 3)] = (uint8_t)sfc;
             }
         }
 
@@ -1056,11 +1059,10 @@ unsigned grid_for(int64_t n, const LaunchCtx& ctx) {
 cudaError_t launch_act_quant(const LaunchCtx& ctx, const __nv_bfloat16* X, int64_t M, int64_t K,
                              uint8_t* codes, uint8_t* sf, float* s_row) {
     const int64_t rows_pad = (M + 127) / 128 * 128;
-    // G warps per row: at most 4 blocks of 16 elements per thread up to K = 16384 (a
-    // smaller ring footprint per CTA, so more CTAs per SM), 8 beyond.
-    if (K <= 2048) return run_act_quant<1>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-    if (K <= 4096) return run_act_quant<2>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-    if (K <= 8192) return run_act_quant<4>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+    // G warps per row: the fewest that keep a thread at kAqMaxBpt blocks of 16 or less.
+    if (K <= 4096) return run_act_quant<1>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+    if (K <= 8192) return run_act_quant<2>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+    if (K <= 16384) return run_act_quant<4>(ctx, X, M, K, rows_pad, codes, sf, s_row);
     return run_act_quant<8>(ctx, X, M, K, rows_pad, codes, sf, s_row);
 }
 
