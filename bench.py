@@ -233,7 +233,7 @@ def run_ours(args):
     launches_per_step = {"nvfp4_requant": 3, "nvfp4_act_quant": 1, "nvfp4_gemm": 1, "bf16_gemm": 1,
                          "select_contrastive": 1}
 
-    def step(d, events=None):
+    def step(d, events=None, y4=Y4, sel=(idx, rr)):
         def mark(i):
             if events is not None:
                 events[i].record()
@@ -243,11 +243,11 @@ def run_ours(args):
         mark(1)
         nv.nvfp4_act_quant(d["X"], a_codes, a_sf, a_s)
         mark(2)
-        nv.nvfp4_gemm((a_codes, a_sf, a_s), (w_codes, w_sf, w_st), d["bias"], out=Y4)
+        nv.nvfp4_gemm((a_codes, a_sf, a_s), (w_codes, w_sf, w_st), d["bias"], out=y4)
         mark(3)
         nv.bf16_gemm(d["X"], d["W"], d["bias"], out=Y16)
         mark(4)
-        nv.select_contrastive(d["rewards"], Kr, True, True, idx, rr)
+        nv.select_contrastive(d["rewards"], Kr, True, True, sel[0], sel[1])
         mark(5)
 
     # ---- device-resident timing
@@ -285,33 +285,65 @@ def run_ours(args):
 
 
 def run_e2e(args, host, dev, step, Y4, idx, rr, M, N, rcfg, Kr, world, device):
+    """End to end through the public calls with host buffers: every step copies its
+    inputs from pinned host memory and its results (Y of the NVFP4 GEMM and the
+    selection) back to pinned host memory, all inside the timed region.  The copies
+    run on their own streams with two sets of device buffers, so step i's kernels
+    overlap step i+1's input copy and step i-1's result copy, as a serving loop would
+    run them."""
     import torch
+    nbuf = 2
     pinned = {k: v.pin_memory() for k, v in host.items()}
-    y_host = torch.empty(M, N, dtype=torch.bfloat16, pin_memory=True)
-    idx_host = torch.empty(rcfg.P, Kr, dtype=torch.int32, pin_memory=True)
-    r_host = torch.empty(rcfg.P, Kr, dtype=torch.float32, pin_memory=True)
-    dev2 = {k: torch.empty_like(v) for k, v in dev.items()}
+    dev_in = [{k: torch.empty_like(v) for k, v in dev.items()} for _ in range(nbuf)]
+    y_dev = [Y4] + [torch.empty_like(Y4) for _ in range(nbuf - 1)]
+    sel_dev = [(idx, rr)] + [(torch.empty_like(idx), torch.empty_like(rr)) for _ in range(nbuf - 1)]
+    y_host = [torch.empty(M, N, dtype=torch.bfloat16, pin_memory=True) for _ in range(nbuf)]
+    sel_host = [(torch.empty(rcfg.P, Kr, dtype=torch.int32, pin_memory=True),
+                 torch.empty(rcfg.P, Kr, dtype=torch.float32, pin_memory=True)) for _ in range(nbuf)]
     h2d = sum(v.numel() * v.element_size() for v in pinned.values())
-    d2h = y_host.numel() * 2 + idx_host.numel() * 4 + r_host.numel() * 4
+    d2h = y_host[0].numel() * 2 + sel_host[0][0].numel() * 4 + sel_host[0][1].numel() * 4
+    s_in, s_run, s_out = (torch.cuda.Stream(device) for _ in range(3))
+    ev_in = [torch.cuda.Event() for _ in range(nbuf)]    # inputs of buffer b landed
+    ev_run = [torch.cuda.Event() for _ in range(nbuf)]   # kernels done with buffer b
+    ev_out = [torch.cuda.Event() for _ in range(nbuf)]   # results of buffer b copied out
 
-    def e2e_step():
-        for k, v in pinned.items():
-            dev2[k].copy_(v, non_blocking=True)
-        step(dev2)
-        y_host.copy_(Y4, non_blocking=True)
-        idx_host.copy_(idx, non_blocking=True)
-        r_host.copy_(rr, non_blocking=True)
+    def e2e_step(i):
+        b = i % nbuf
+        with torch.cuda.stream(s_in):
+            s_in.wait_event(ev_run[b])       # the step two back no longer reads these inputs
+            for k, v in pinned.items():
+                dev_in[b][k].copy_(v, non_blocking=True)
+            ev_in[b].record(s_in)
+        with torch.cuda.stream(s_run):
+            s_run.wait_event(ev_in[b])
+            s_run.wait_event(ev_out[b])      # the step two back has been read out
+            step(dev_in[b], y4=y_dev[b], sel=sel_dev[b])
+            ev_run[b].record(s_run)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_run[b])
+            y_host[b].copy_(y_dev[b], non_blocking=True)
+            sel_host[b][0].copy_(sel_dev[b][0], non_blocking=True)
+            sel_host[b][1].copy_(sel_dev[b][1], non_blocking=True)
+            ev_out[b].record(s_out)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    def run(n):
+        cur = torch.cuda.current_stream()
+        start = torch.cuda.Event(enable_timing=True)
+        stop = torch.cuda.Event(enable_timing=True)
+        start.record(cur)
+        for s in (s_in, s_run, s_out):
+            s.wait_event(start)
+        for i in range(n):
+            e2e_step(i)
+        for s in (s_in, s_run, s_out):
+            cur.wait_stream(s)
+        stop.record(cur)
+        return start, stop
+
+    run(args.warmup)
     torch.cuda.synchronize()
     barrier(world, device)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record()
+    e0, e1 = run(args.steps)
     torch.cuda.synchronize()
     barrier(world, device)
     return max_over_ranks(e0.elapsed_time(e1), world, device), h2d, d2h
