@@ -231,7 +231,7 @@ def run_ours(args):
     # requant: split kernel, amax pass, quantize pass (tensor-core merge); or amax pass,
     # quantize pass, finalize (CUDA-core merge)
     launches_per_step = {"nvfp4_requant": 3, "nvfp4_act_quant": 1, "nvfp4_gemm": 1, "bf16_gemm": 1,
-                         "select_contrastive": 1}
+                         "select_contrastive": 2}
 
     def step(d, events=None, y4=Y4, sel=(idx, rr)):
         def mark(i):
