@@ -225,12 +225,20 @@ struct F8 {
     float v[8];
 };
 
-// Slow path of e2m1_quotient8 (rare): the 8 codes from true IEEE divisions.
-static __device__ __noinline__ uint32_t e2m1_exact8(F8 x, float den) {
-    F8 q;
+// Slow path of e2m1_quotient8: the codes of the elements flagged in `redo` (a nonzero
+// nibble each) from true IEEE divisions, the others kept from `codes`.  bf16 inputs
+// make it common for one element of a block to sit on a rounding boundary (the
+// quotient is then close to a ratio of small integers), so it recomputes only those.
+static __device__ __noinline__ uint32_t e2m1_exact8(F8 x, float den, uint32_t codes, uint32_t redo) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) q.v[i] = __fdiv_rn(x.v[i], den);
-    return cvt_e2m1x8(q.v[0], q.v[1], q.v[2], q.v[3], q.v[4], q.v[5], q.v[6], q.v[7]);
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t sh = 4u * (uint32_t)i;
+        if ((redo >> sh) & 0xFu) {
+            const uint32_t c = cvt_e2m1x8(__fdiv_rn(x.v[i], den), 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 0xFu;
+            codes = (codes & ~(0xFu << sh)) | (c << sh);
+        }
+    }
+    return codes;
 }
 
 static __device__ __noinline__ float exact_quotient(float v, float d) { return __fdiv_rn(v, d); }
@@ -259,9 +267,10 @@ __device__ __forceinline__ Recip make_recip(float den) {
 // product and the quotient round by at most 2^-24 relatively; every E2M1 boundary is
 // a normal number, and below the smallest one all three give code 0 or 0x8).  E2M1
 // rounding is monotone in the magnitude, so if lo and hi give the same 8 codes so
-// does fl(x / den).  Otherwise (a quotient within about 2^-20 of a rounding boundary,
-// or an exact tie) and whenever den or 1/den is not a normal number, the 8 codes come
-// from true IEEE divisions.  Zero stays zero with its sign in both products.
+// does fl(x / den).  Otherwise the codes that differ (a quotient within about 2^-20 of
+// a rounding boundary, or an exact tie), and all 8 whenever den or 1/den is not a
+// normal number, come from true IEEE divisions.  Zero stays zero with its sign in
+// both products.
 __device__ __forceinline__ uint32_t e2m1_quotient8(const float (&x)[8], float den, const Recip& rc) {
     float lo[8], hi[8];
     const float2 rl = make_float2(rc.lo, rc.lo), rh = make_float2(rc.hi, rc.hi);
@@ -280,7 +289,7 @@ __device__ __forceinline__ uint32_t e2m1_quotient8(const float (&x)[8], float de
         F8 xv;
 #pragma unroll
         for (int i = 0; i < 8; ++i) xv.v[i] = x[i];
-        return e2m1_exact8(xv, den);
+        return e2m1_exact8(xv, den, c_hi, rc.fast ? c_lo ^ c_hi : 0xFFFFFFFFu);
     }
     return c_hi;
 }

@@ -131,9 +131,12 @@ struct GemmArgs {
 // flight at any time share a few m-pairs (their A rows are read from DRAM once) and
 // sweep B band by band (B is re-read once per band), instead of re-reading A for
 // every n-block.  Tile t covers m-blocks 2 mp + {0, 1} (one per CTA) and n-block nb.
-constexpr int kBandMp = 16;
-
+// FLUX.1 up-projection: NVFP4 with bands of 4 ~2% faster than 8, 16 or 32 (its B,
+// 21 MB, stays in L2; DRAM reads 119 MB against 254 MB with 16); BF16 with 16 (its
+// 75.5 MB B does not stay in L2 over narrow bands: 2.8 GB of DRAM reads with 4).
+template <bool kFP4>
 struct Sched {
+    static constexpr int kBandMp = kFP4 ? 4 : 16;
     int num_m, num_mp, num_n, total, first, step;
     __device__ Sched(int M, int N) {
         num_m = (M + BM - 1) / BM;
@@ -180,7 +183,7 @@ __global__ void __launch_bounds__(Cfg<kFP4>::kThreads, 1)
     const uint32_t rank = cluster_ctarank();  // 0 (even, issues the MMAs) or 1
     const bool leader = rank == 0;
     const int M = args.M, N = args.N, K = args.K;
-    const Sched sch(M, N);
+    const Sched<kFP4> sch(M, N);
     // MMA steps along K: 64 E2M1 (32 bytes) or 16 BF16 (32 bytes) each; 4 per stage.
     const int k_steps = kFP4 ? K / 64 : (K + 15) / 16;
     const int num_kb = (k_steps + 3) / 4;
