@@ -190,8 +190,8 @@ nvfp4_status bf16_gemm(const void* X, const void* W, const void* bias, void* Y, 
  *            (global_std = 1, the default of the page) or of prompt p's K
  *            (global_std = 0); Z == 0 gives r = 1/2.  Accumulated in fp64.
  *   0 < K <= N, K even, N <= 1024, 0 <= P < 2^31.  Two kernels: the ranks (one
- *   CTA per prompt) and, with r_out, the transform (one CTA per prompt, up to
- *   1024, started by programmatic dependent launch).
+ *   CTA per prompt) and, with r_out, the transform (one CTA per prompt, at most
+ *   one per SM, started by programmatic dependent launch).
  */
 nvfp4_status select_contrastive(const float* rewards, int P, int N, int K, int global_std,
                                 int32_t* idx, float* r_out, void* stream);

@@ -14,13 +14,13 @@
 //   rank_top(i) = #{j : v_j > v_i or (v_j == v_i and j < i)}
 //   rank_bot(i) = #{j : v_j < v_i or (v_j == v_i and j < i)}
 // and seed i goes to slot rank_top(i) (if < K/2) and K/2 + rank_bot(i) (if < K/2).
-// select_transform_kernel (only with r_out): one CTA per prompt (up to kXformCtas),
-// started early by programmatic dependent launch and waiting for the ranks, reads the
-// selected raw rewards through idx; means and standard deviations in fp64 (two
-// passes), then per element (x - mean) * (1 / Z) in fp64, clipped and rounded to
-// fp32.  fp64 is slow on this part: the CTAs spread it over the SMs (each computes
-// the global statistics itself rather than waiting for one that does), and each group
-// takes one division, not one per element.
+// select_transform_kernel (only with r_out): one CTA per prompt (at most one per SM,
+// each CTA then taking several), started early by programmatic dependent launch and
+// waiting for the ranks, reads the selected raw rewards through idx; means and
+// standard deviations in fp64 (two passes), then per element (x - mean) * (1 / Z) in
+// fp64, clipped and rounded to fp32.  fp64 is slow on this part: the CTAs spread it
+// over the SMs (each computes the global statistics itself rather than waiting for
+// one that does), and each group takes one division, not one per element.
 #include "common.cuh"
 
 namespace nvfp4rl {
@@ -29,7 +29,6 @@ namespace {
 constexpr unsigned kFull = 0xFFFFFFFFu;
 constexpr int kMaxN = 1024;
 constexpr int kRankThreads = 256;   // upper bound of the ranking CTA
-constexpr int kXformCtas = 1024;    // upper bound of the transform's grid
 constexpr int kXformThreads = 256;
 constexpr int kKeep = 4;            // selected rewards per thread kept between the two passes
 
@@ -169,7 +168,9 @@ cudaError_t launch_select(const LaunchCtx& ctx, const float* rewards, int P, int
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.gridDim = dim3((unsigned)(P < kXformCtas ? P : kXformCtas));
+    // Every CTA gathers all P * K selected rewards for the global statistics: at most
+    // one CTA per SM keeps that redundant work to one pass per SM.
+    cfg.gridDim = dim3((unsigned)(P < ctx.num_sms ? P : ctx.num_sms));
     cfg.blockDim = dim3(kXformThreads);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = ctx.stream;

@@ -38,6 +38,8 @@ def test_select_configs(orc, name):
 @pytest.mark.parametrize("P,N,K,global_std", [
     (1, 96, 24, False), (32, 96, 24, False), (33, 96, 24, True), (5, 10, 10, True),
     (3, 17, 2, False), (70, 1024, 64, True), (64, 96, 96, True),
+    # more prompts than SMs: transform CTAs take several prompts each
+    (400, 96, 24, True), (300, 128, 40, False),
 ])
 def test_select_shapes(orc, P, N, K, global_std):
     require_gpu()
