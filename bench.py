@@ -176,6 +176,8 @@ def algorithmic_bytes(cfg, rcfg):
         "nvfp4_requant": N * K * 2 + 32 * K * 4 + N * 32 * 4 + N * K // 2 + sf_w + 4,
         # read X once; write codes, scales, one fp32 per row
         "nvfp4_act_quant": M * K * 2 + M * K // 2 + sf_a + 4 * M,
+        # the same with one per-tensor scale
+        "act_quant_per_tensor": M * K * 2 + M * K // 2 + sf_a + 4,
     }
 
 
@@ -273,6 +275,28 @@ def run_ours(args):
            for i, n in enumerate(names)}
     per = {n: max_over_ranks(v, world, device) for n, v in per.items()}
 
+    # ---- a variant outside the step: NVFP4 of X with one per-tensor scale (nvfp4_requant
+    # with no LoRA factors on the bf16 activations: two passes over X)
+    xq_codes = torch.empty_like(a_codes)
+    xq_sf = torch.empty_like(a_sf)
+    xq_st = torch.empty(1, dtype=torch.float32, device=device)
+
+    def per_tensor():
+        nv.nvfp4_requant(dev["X"], None, None, workloads.LORA_ALPHA, xq_codes, xq_sf, xq_st)
+
+    for _ in range(3):
+        per_tensor()
+    torch.cuda.synchronize()
+    vt = []
+    for _ in range(10):
+        v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        v0.record()
+        per_tensor()
+        v1.record()
+        v1.synchronize()
+        vt.append(v0.elapsed_time(v1))
+    per_tensor_ms = max_over_ranks(statistics.median(vt), world, device)
+
     # ---- end to end: pinned host inputs in, result out, every step
     if args.no_e2e:
         e2e_ms = float("nan")
@@ -281,7 +305,7 @@ def run_ours(args):
         e2e_ms, h2d, d2h = run_e2e(args, host, dev, step, Y4, idx, rr, M, N, rcfg, Kr, world, device)
     status = nv.nvfp4_device_status()
     return report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk, world, rank,
-                  launches_per_step)
+                  launches_per_step, per_tensor_ms)
 
 
 def run_e2e(args, host, dev, step, Y4, idx, rr, M, N, rcfg, Kr, world, device):
@@ -350,7 +374,7 @@ def run_e2e(args, host, dev, step, Y4, idx, rr, M, N, rcfg, Kr, world, device):
 
 
 def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk, world, rank,
-           launches_per_step):
+           launches_per_step, per_tensor_ms):
     if rank != 0:
         return None
     M, K, N = cfg.M, cfg.K, cfg.N
@@ -408,6 +432,11 @@ def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk
         "e2e": None if args.no_e2e else {
             "value": round(gemm_flops / (e2e_ms_step * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
             "ms_per_step": round(e2e_ms_step, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "variants": {"act_quant_per_tensor": {
+            "call": "nvfp4_requant on X with no LoRA factors (one per-tensor scale, two passes over X)",
+            "ms": round(per_tensor_ms, 4),
+            "gbs": round(ab["act_quant_per_tensor"] / (per_tensor_ms * 1e-3) / 1e9, 1),
+            "frac": round(ab["act_quant_per_tensor"] / (per_tensor_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}},
         "gpu_launches": sum(launches_per_step.values()) * args.steps,
         "device_status": status,
         "clocks": clk,

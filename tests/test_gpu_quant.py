@@ -127,6 +127,14 @@ def test_requant_iteration_down_projection(orc):
     _check_requant(orc, W, A, B, workloads.LORA_ALPHA)
 
 
+def test_act_quant_per_tensor_variant(orc):
+    """One per-tensor scale for activations: nvfp4_requant with no LoRA factors on
+    FLUX-shaped bf16 activations (outlier channels included), 2048 rows."""
+    require_gpu()
+    X = workloads.activations(workloads.LINEARS["flux_up"], rows=2048)
+    _check_requant(orc, X, None, None, workloads.LORA_ALPHA)
+
+
 @pytest.mark.parametrize("r", [0, 1, 7, 64])
 def test_requant_ranks(orc, r):
     require_gpu()
