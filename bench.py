@@ -275,14 +275,14 @@ def run_ours(args):
            for i, n in enumerate(names)}
     per = {n: max_over_ranks(v, world, device) for n, v in per.items()}
 
-    # ---- a variant outside the step: NVFP4 of X with one per-tensor scale (nvfp4_requant
-    # with no LoRA factors on the bf16 activations: two passes over X)
+    # ---- a variant outside the step: NVFP4 of X with one per-tensor scale (two passes
+    # over X)
     xq_codes = torch.empty_like(a_codes)
     xq_sf = torch.empty_like(a_sf)
     xq_st = torch.empty(1, dtype=torch.float32, device=device)
 
     def per_tensor():
-        nv.nvfp4_requant(dev["X"], None, None, workloads.LORA_ALPHA, xq_codes, xq_sf, xq_st)
+        nv.nvfp4_act_quant_tensor(dev["X"], xq_codes, xq_sf, xq_st)
 
     for _ in range(3):
         per_tensor()
@@ -433,7 +433,7 @@ def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk
             "value": round(gemm_flops / (e2e_ms_step * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
             "ms_per_step": round(e2e_ms_step, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "variants": {"act_quant_per_tensor": {
-            "call": "nvfp4_requant on X with no LoRA factors (one per-tensor scale, two passes over X)",
+            "call": "nvfp4_act_quant_tensor (one per-tensor scale, two passes over X)",
             "ms": round(per_tensor_ms, 4),
             "gbs": round(ab["act_quant_per_tensor"] / (per_tensor_ms * 1e-3) / 1e9, 1),
             "frac": round(ab["act_quant_per_tensor"] / (per_tensor_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}},

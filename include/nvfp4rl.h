@@ -151,6 +151,21 @@ nvfp4_status nvfp4_act_quant(const void* X, int64_t M, int64_t K, uint8_t* codes
                              float* s_row, void* stream);
 
 /*
+ * nvfp4_act_quant_tensor — NVFP4 of BF16 activations with one scale for the whole
+ * tensor instead of one per row (a variant of the per-token reading; the same
+ * convention as the weights: s = amax(|X|) / 2688).
+ *   X      device, [M, K] bf16, finite.
+ *   codes  device, [M, K/2] bytes (out).
+ *   sf     device, nvfp4_sf_bytes(M, K) bytes (out, padding rows written 0).
+ *   s_t    device, one fp32 (out); also the amax accumulator while the call runs.
+ *   K % 64 == 0, K <= 32768, M < 2^31.  Two passes over X: a memset, an amax kernel,
+ *   the quantize kernel and a one-thread kernel that turns amax into s_t.  Gives the
+ *   same codes, scales and s_t as nvfp4_requant with no LoRA factors on X.
+ */
+nvfp4_status nvfp4_act_quant_tensor(const void* X, int64_t M, int64_t K, uint8_t* codes, uint8_t* sf,
+                                    float* s_t, void* stream);
+
+/*
  * nvfp4_gemm — Y = bf16_RNE( s_a[m] * s_w * sum_k a_hat[m,k] * w_hat[n,k] + bias[n] ),
  * where a_hat = e2m1(code) * e4m3(sf) of the activations and w_hat likewise of
  * the weights; the sum runs on the tensor cores (tcgen05 block-scaled FP4 MMA)

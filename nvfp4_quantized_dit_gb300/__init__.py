@@ -19,7 +19,8 @@ import torch
 
 __all__ = [
     "NVFP4Error", "library", "sf_bytes", "sf_offset",
-    "nvfp4_requant", "requant_workspace_bytes", "nvfp4_requant_noalloc", "nvfp4_act_quant", "nvfp4_gemm", "bf16_gemm", "select_contrastive",
+    "nvfp4_requant", "requant_workspace_bytes", "nvfp4_requant_noalloc", "nvfp4_act_quant",
+    "nvfp4_act_quant_tensor", "nvfp4_gemm", "bf16_gemm", "select_contrastive",
     "nvfp4_device_status", "nvfp4_status_string", "nvfp4_version",
     "nvfp4_test_e2m1", "nvfp4_test_e4m3", "nvfp4_test_e2m1_quotient", "nvfp4_test_e4m3_quotient",
     "nvfp4_test_e4m3_decode", "nvfp4_test_merge", "nvfp4_test_wait_timeout",
@@ -55,6 +56,7 @@ def library() -> ctypes.CDLL:
                 "nvfp4_requant": [P, I, P, P, I, F, I64, I64, P, P, P, P, ctypes.c_size_t, P],
                 "nvfp4_requant_noalloc": [P, I, P, P, I, F, I64, I64, P, P, P, P],
                 "nvfp4_act_quant": [P, I64, I64, P, P, P, P],
+                "nvfp4_act_quant_tensor": [P, I64, I64, P, P, P, P],
                 "nvfp4_gemm": [P, P, P, P, P, P, P, P, I64, I64, I64, P],
                 "bf16_gemm": [P, P, P, P, I64, I64, I64, P],
                 "select_contrastive": [P, I, I, I, I, P, P, P],
@@ -197,6 +199,21 @@ def nvfp4_act_quant(X, codes=None, sf=None, s_row=None, stream=None):
     _call("nvfp4_act_quant", _dev(X, "X", torch.bfloat16), M, K, _dev(codes, "codes", torch.uint8),
           _dev(sf, "sf", torch.uint8), _dev(s_row, "s_row", torch.float32), _stream(stream))
     return codes, sf, s_row
+
+
+def nvfp4_act_quant_tensor(X, codes=None, sf=None, s_t=None, stream=None):
+    """NVFP4 of bf16 activations X [M, K] with one per-tensor scale.  Returns
+    (codes, sf, s_t)."""
+    if X.dim() != 2:
+        raise ValueError("X must be [M, K]")
+    M, K = X.shape
+    dev = X.device
+    codes = torch.empty(M, K // 2, dtype=torch.uint8, device=dev) if codes is None else codes
+    sf = torch.empty(sf_bytes(M, K), dtype=torch.uint8, device=dev) if sf is None else sf
+    s_t = torch.empty(1, dtype=torch.float32, device=dev) if s_t is None else s_t
+    _call("nvfp4_act_quant_tensor", _dev(X, "X", torch.bfloat16), M, K, _dev(codes, "codes", torch.uint8),
+          _dev(sf, "sf", torch.uint8), _dev(s_t, "s_t", torch.float32), _stream(stream))
+    return codes, sf, s_t
 
 
 def nvfp4_gemm(a, w, bias=None, out=None, stream=None):

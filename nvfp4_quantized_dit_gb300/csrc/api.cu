@@ -133,6 +133,12 @@ constexpr int64_t kMaxRows = (int64_t(1) << 31) - 1;
 }  // namespace
 }  // namespace nvfp4rl
 
+namespace nvfp4rl {
+// Defined in quant.cu (the per-tensor activation variant).
+cudaError_t launch_act_quant_tensor(const LaunchCtx& ctx, const __nv_bfloat16* X, int64_t M, int64_t K,
+                                    uint8_t* codes, uint8_t* sf, float* s_t);
+}  // namespace nvfp4rl
+
 using namespace nvfp4rl;
 
 extern "C" {
@@ -233,6 +239,19 @@ nvfp4_status nvfp4_act_quant(const void* X, int64_t M, int64_t K, uint8_t* codes
     if (st != NVFP4_OK) return st;
     return from_cuda(launch_act_quant(ctx, static_cast<const __nv_bfloat16*>(X), M, K, codes, sf,
                                       s_row));
+}
+
+nvfp4_status nvfp4_act_quant_tensor(const void* X, int64_t M, int64_t K, uint8_t* codes, uint8_t* sf,
+                                    float* s_t, void* stream) {
+    if (M < 0 || M > kMaxRows || K <= 0 || K % 64 != 0 || K > 32768) return NVFP4_ERR_SHAPE;
+    if (X == nullptr || codes == nullptr || sf == nullptr || s_t == nullptr) return NVFP4_ERR_NULL;
+    if (misaligned(X, 16) || misaligned(codes, 16) || misaligned(sf, 16) || misaligned(s_t, 4))
+        return NVFP4_ERR_ALIGN;
+    LaunchCtx ctx;
+    nvfp4_status st = resolve(stream, &ctx);
+    if (st != NVFP4_OK) return st;
+    if (M == 0) return from_cuda(cudaMemsetAsync(s_t, 0, sizeof(float), ctx.stream));
+    return from_cuda(launch_act_quant_tensor(ctx, static_cast<const __nv_bfloat16*>(X), M, K, codes, sf, s_t));
 }
 
 nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_srow,

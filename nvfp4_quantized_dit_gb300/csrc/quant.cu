@@ -120,7 +120,9 @@ __device__ __forceinline__ uint32_t bf16x16_absmax(const uint4& u0, const uint4&
     return *reinterpret_cast<const uint32_t*>(&m);
 }
 
-template <int G>
+// kTensor: one scale for the whole tensor, s = amax / 2688 with amax read from
+// *s_row (written by act_amax_kernel); nothing is written to s_row.
+template <int G, bool kTensor>
 __global__ void __launch_bounds__(kAqWarps * 32)
     act_quant_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t K, int64_t rows_pad,
                      uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
@@ -159,6 +161,9 @@ __global__ void __launch_bounds__(kAqWarps * 32)
         }
     }
 
+    float s_all = 0.0f;
+    if (kTensor) s_all = __fdiv_rn(*reinterpret_cast<volatile const float*>(s_row), kAmaxDiv);
+
     int slot = 0;
     uint32_t phase = 0;
     for (int64_t m = first; m < rows_pad; m += step) {
@@ -183,15 +188,18 @@ __global__ void __launch_bounds__(kAqWarps * 32)
             bmax[i] = bm;
             amax = fmaxf(amax, bm);
         }
-        amax = warp_max(amax);
-        if (G > 1) {
-            if (lane == 0) red[warp] = amax;
-            named_barrier_sync(1 + group, kThreadsPerRow);
+        float s = s_all;
+        if (!kTensor) {
+            amax = warp_max(amax);
+            if (G > 1) {
+                if (lane == 0) red[warp] = amax;
+                named_barrier_sync(1 + group, kThreadsPerRow);
 #pragma unroll
-            for (int w = 0; w < G; ++w) amax = fmaxf(amax, red[group * G + w]);
+                for (int w = 0; w < G; ++w) amax = fmaxf(amax, red[group * G + w]);
+            }
+            s = __fdiv_rn(amax, kAmaxDiv);
+            if (valid && t == 0) s_row[m] = s;
         }
-        const float s = __fdiv_rn(amax, kAmaxDiv);
-        if (valid && t == 0) s_row[m] = s;
         const float d = __fmul_rn(6.0f, s);
         const bool d_fast = fast_recip_ok(d);
         const float inv_d = d_fast ? recip_approx(d) : 0.0f;
@@ -246,20 +254,52 @@ __global__ void __launch_bounds__(kAqWarps * 32)
     }
 }
 
-template <int G>
+template <int G, bool kTensor>
 cudaError_t run_act_quant(const LaunchCtx& ctx, const __nv_bfloat16* X, int64_t M, int64_t K,
                           int64_t rows_pad, uint8_t* codes, uint8_t* sf, float* s_row) {
     const size_t smem = (size_t)(kAqWarps / G) * kAqRing * (size_t)K * 2;
     static OccupancyCache occupancy;
     int per_sm = 0;
-    const cudaError_t e = blocks_per_sm(occupancy, ctx, act_quant_kernel<G>, kAqWarps * 32, smem, &per_sm);
+    const cudaError_t e =
+        blocks_per_sm(occupancy, ctx, act_quant_kernel<G, kTensor>, kAqWarps * 32, smem, &per_sm);
     if (e != cudaSuccess) return e;
     int64_t grid = (rows_pad + (kAqWarps / G) - 1) / (kAqWarps / G);
     if (grid > (int64_t)ctx.num_sms * per_sm) grid = (int64_t)ctx.num_sms * per_sm;
-    act_quant_kernel<G><<<(unsigned)grid, kAqWarps * 32, smem, ctx.stream>>>(X, M, K, rows_pad, codes,
-                                                                          sf, s_row, ctx.status);
+    act_quant_kernel<G, kTensor><<<(unsigned)grid, kAqWarps * 32, smem, ctx.stream>>>(
+        X, M, K, rows_pad, codes, sf, s_row, ctx.status);
     return cudaGetLastError();
 }
+
+// Per-tensor activation scale, pass 1: amax|X| over the whole tensor into *amax (fp32
+// bits, atomicMax: every value is >= 0, so the bit patterns order like the values;
+// zeroed before the launch).  Streaming loads, 4 in flight per thread.
+constexpr int kAmaxThreads = 256;
+__global__ void __launch_bounds__(kAmaxThreads) act_amax_kernel(const uint4* __restrict__ X, int64_t n_vec,
+                                                                float* __restrict__ amax) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    __nv_bfloat162 m = __float2bfloat162_rn(0.0f);
+    for (; i + 3 * stride < n_vec; i += 4 * stride) {
+        uint4 v[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v[u] = ld_stream_v4(X + i + u * stride);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+            m = __hmax2(m, __hmax2(__hmax2(bf16x2_abs(v[u].x), bf16x2_abs(v[u].y)),
+                                   __hmax2(bf16x2_abs(v[u].z), bf16x2_abs(v[u].w))));
+    }
+    for (; i < n_vec; i += stride) {
+        const uint4 v = ld_stream_v4(X + i);
+        m = __hmax2(m, __hmax2(__hmax2(bf16x2_abs(v.x), bf16x2_abs(v.y)),
+                               __hmax2(bf16x2_abs(v.z), bf16x2_abs(v.w))));
+    }
+    const uint32_t mm = *reinterpret_cast<const uint32_t*>(&m);
+    const float f = warp_max(fmaxf(bf16_lo(mm), bf16_hi(mm)));
+    if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned int*>(amax), __float_as_uint(f));
+}
+
+// Per-tensor activation scale, last step: *s_t = amax / 2688 (fp32).
+__global__ void act_scale_kernel(float* s_t) { *s_t = __fdiv_rn(*s_t, kAmaxDiv); }
 
 // ------------------------------------------------------------------ requant
 //
@@ -1060,10 +1100,30 @@ cudaError_t launch_act_quant(const LaunchCtx& ctx, const __nv_bfloat16* X, int64
                              uint8_t* codes, uint8_t* sf, float* s_row) {
     const int64_t rows_pad = (M + 127) / 128 * 128;
     // G warps per row: the fewest that keep a thread at kAqMaxBpt blocks of 16 or less.
-    if (K <= 4096) return run_act_quant<1>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-    if (K <= 8192) return run_act_quant<2>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-    if (K <= 16384) return run_act_quant<4>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-    return run_act_quant<8>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+    if (K <= 4096) return run_act_quant<1, false>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+    if (K <= 8192) return run_act_quant<2, false>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+    if (K <= 16384) return run_act_quant<4, false>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+    return run_act_quant<8, false>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+}
+
+cudaError_t launch_act_quant_tensor(const LaunchCtx& ctx, const __nv_bfloat16* X, int64_t M, int64_t K,
+                                    uint8_t* codes, uint8_t* sf, float* s_t) {
+    cudaError_t e = cudaMemsetAsync(s_t, 0, sizeof(float), ctx.stream);
+    if (e != cudaSuccess) return e;
+    const int64_t n_vec = M * K / 8;
+    int64_t grid = (n_vec + kAmaxThreads - 1) / kAmaxThreads;
+    if (grid > (int64_t)ctx.num_sms * 8) grid = (int64_t)ctx.num_sms * 8;
+    act_amax_kernel<<<(unsigned)grid, kAmaxThreads, 0, ctx.stream>>>(reinterpret_cast<const uint4*>(X), n_vec,
+                                                                     s_t);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int64_t rows_pad = (M + 127) / 128 * 128;
+    if (K <= 4096) e = run_act_quant<1, true>(ctx, X, M, K, rows_pad, codes, sf, s_t);
+    else if (K <= 8192) e = run_act_quant<2, true>(ctx, X, M, K, rows_pad, codes, sf, s_t);
+    else if (K <= 16384) e = run_act_quant<4, true>(ctx, X, M, K, rows_pad, codes, sf, s_t);
+    else e = run_act_quant<8, true>(ctx, X, M, K, rows_pad, codes, sf, s_t);
+    if (e != cudaSuccess) return e;
+    act_scale_kernel<<<1, 1, 0, ctx.stream>>>(s_t);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_requant(const LaunchCtx& ctx, const void* W, int w_dtype, const float* A,

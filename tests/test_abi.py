@@ -80,6 +80,15 @@ def test_act_quant_validation(lib):
     assert lib.nvfp4_act_quant(None, 0, 64, None, None, None, None) == 0  # empty: no-op
 
 
+def test_act_quant_tensor_validation(lib):
+    P = ctypes.c_void_p
+    assert lib.nvfp4_act_quant_tensor(P(A16), 4, 100, P(A16), P(A16), P(A16), None) == 2  # K % 64
+    assert lib.nvfp4_act_quant_tensor(P(A16), -1, 64, P(A16), P(A16), P(A16), None) == 2
+    assert lib.nvfp4_act_quant_tensor(None, 4, 64, P(A16), P(A16), P(A16), None) == 1
+    assert lib.nvfp4_act_quant_tensor(P(A16), 4, 64, P(A16), P(A16), None, None) == 1  # s_t
+    assert lib.nvfp4_act_quant_tensor(P(BAD), 4, 64, P(A16), P(A16), P(A16), None) == 3
+
+
 def test_requant_validation(lib):
     P = ctypes.c_void_p
     f = ctypes.c_float(32.0)

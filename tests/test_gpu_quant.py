@@ -135,6 +135,42 @@ def test_act_quant_per_tensor_variant(orc):
     _check_requant(orc, X, None, None, workloads.LORA_ALPHA)
 
 
+def _check_act_tensor(orc, X):
+    M, K = X.shape
+    codes, sf, s_t = nv.nvfp4_act_quant_tensor(X.cuda())
+    torch.cuda.synchronize()
+    codes, sf, s_t = np_(codes), np_(sf), np_(s_t)
+    sf_rm, sf_pad = unswizzle_sf(sf, M, K)
+    assert not sf_pad.any(), "scale padding rows must be zero"
+    oc, osf, os_ = orc.requant(workloads.bf16_bits(X), None, None, workloads.LORA_ALPHA)
+    assert s_t.view(np.uint32)[0] == os_.view(np.uint32)[0], f"s_t {s_t[0]!r} vs {os_[0]!r}"
+    assert np.array_equal(sf_rm, osf), f"block scales differ at {np.argwhere(sf_rm != osf)[:3]}"
+    assert np.array_equal(codes, oc), f"codes differ at {np.argwhere(codes != oc)[:3]}"
+
+
+@pytest.mark.parametrize("M,K", [(2048, 3072), (1, 64), (300, 12288), (77, 32768), (129, 2240)])
+def test_act_quant_tensor(orc, M, K):
+    """nvfp4_act_quant_tensor (per-tensor scale, two passes) against the oracle's
+    per-tensor quantization; FLUX-shaped activations for the first case."""
+    require_gpu()
+    if (M, K) == (2048, 3072):
+        X = workloads.activations(workloads.LINEARS["flux_up"], rows=M)
+    else:
+        g = torch.Generator().manual_seed(M * 13 + K)
+        X = (torch.randn(M, K, generator=g) * torch.exp(torch.randn(M, 1, generator=g) * 3)).to(torch.bfloat16)
+    _check_act_tensor(orc, X)
+
+
+def test_act_quant_tensor_edge_values(orc):
+    require_gpu()
+    g = torch.Generator().manual_seed(9)
+    _check_act_tensor(orc, torch.zeros(130, 128, dtype=torch.bfloat16))   # zero tensor: s_t = 0
+    X = torch.randn(64, 256, generator=g)
+    X[5, 17] = -3e38                                                      # amax from a negative value
+    X[7] = 2.0 ** -133
+    _check_act_tensor(orc, X.to(torch.bfloat16))
+
+
 @pytest.mark.parametrize("r", [0, 1, 7, 64])
 def test_requant_ranks(orc, r):
     require_gpu()
