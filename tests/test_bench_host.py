@@ -1,0 +1,59 @@
+"""Host-side bookkeeping of bench.py (no GPU): the DRAM traffic lookup, which must
+only report a captured figure while the kernel's sources are unchanged, and the
+algorithmic byte counts the HBM rooflines divide by."""
+
+import dataclasses
+
+import bench
+import workloads
+
+
+def test_traffic_lookup_follows_the_source_hash(tmp_path, monkeypatch):
+    cur = bench.source_hash(*bench.KERNEL_SOURCES["nvfp4_requant"])
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    (prof / "dram_traffic.txt").write_text(
+        "# comment line nvfp4_requant flux_up x 1\n"
+        f"nvfp4_requant flux_up {cur} 12345\n"
+        "nvfp4_act_quant flux_up 0000000000000000 999\n")
+    hashes = {k: bench.source_hash(*v) for k, v in bench.KERNEL_SOURCES.items()}
+    by_files = {tuple(v): hashes[k] for k, v in bench.KERNEL_SOURCES.items()}
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_hash", lambda *rel: by_files[tuple(rel)])
+    assert bench.dram_traffic("nvfp4_requant", "flux_up") == 12345.0
+    assert bench.dram_traffic("nvfp4_act_quant", "flux_up") is None  # stale capture
+    assert bench.dram_traffic("nvfp4_gemm", "flux_up") is None       # none captured
+    assert bench.dram_traffic("nvfp4_requant", "sana") is None        # other workload
+
+
+def test_source_hash_changes_with_the_sources(tmp_path):
+    a = tmp_path / "a.cu"
+    a.write_text("x")
+    h1 = bench.source_hash(str(a))
+    a.write_text("y")
+    assert bench.source_hash(str(a)) != h1
+
+
+def test_algorithmic_bytes_flux():
+    cfg = workloads.LINEARS["flux_up"]
+    rcfg = workloads.REWARDS[bench.REWARD_CFG]
+    ab = bench.algorithmic_bytes(cfg, rcfg)
+    M, K, N = cfg.M, cfg.K, cfg.N
+    sf_w = (N + 127) // 128 * 128 * (K // 16)
+    sf_a = (M + 127) // 128 * 128 * (K // 16)
+    # W once (bf16), A and B (fp32, rank 32), codes, scales, s_t
+    assert ab["nvfp4_requant"] == 2 * N * K + 4 * 32 * K + 4 * N * 32 + N * K // 2 + sf_w + 4
+    # X once (bf16), codes, scales, one fp32 per row
+    assert ab["nvfp4_act_quant"] == 2 * M * K + M * K // 2 + sf_a + 4 * M
+    assert ab["act_quant_per_tensor"] == ab["nvfp4_act_quant"] - 4 * M + 4
+    # 2.5625 bytes per element of W (N is a multiple of 128), plus the LoRA factors and s_t
+    assert ab["nvfp4_requant"] - (4 * 32 * K + 4 * N * 32 + 4) == 2.5625 * N * K
+
+
+def test_algorithmic_bytes_scale_with_rows():
+    cfg = workloads.LINEARS["flux_up"]
+    rcfg = workloads.REWARDS[bench.REWARD_CFG]
+    small = dataclasses.replace(cfg, M=8192)
+    a, b = bench.algorithmic_bytes(cfg, rcfg), bench.algorithmic_bytes(small, rcfg)
+    assert a["nvfp4_requant"] == b["nvfp4_requant"]  # independent of the activations
+    assert a["nvfp4_act_quant"] > 4 * b["nvfp4_act_quant"]
