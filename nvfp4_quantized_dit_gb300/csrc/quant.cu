@@ -122,7 +122,10 @@ __device__ __forceinline__ uint32_t bf16x16_absmax(const uint4& u0, const uint4&
 
 // kTensor: one scale for the whole tensor, s = amax / 2688 with amax read from
 // *s_row (written by act_amax_kernel); nothing is written to s_row.
-template <int G, bool kTensor>
+// kBpt > 0: every thread has exactly kBpt blocks (K == 512 G kBpt), so the block
+// loops have fixed trip counts (no per-block bounds or exit tests, chains of
+// consecutive blocks interleaved); 0: any K, blocks counted at run time.
+template <int G, bool kTensor, int kBpt>
 __global__ void __launch_bounds__(kAqWarps * 32)
     act_quant_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t K, int64_t rows_pad,
                      uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
@@ -175,13 +178,14 @@ __global__ void __launch_bounds__(kAqWarps * 32)
             if (!ok) break;
         }
         // Pass 1: block maxima and the row amax.
-        float bmax[kAqMaxBpt];
+        constexpr int kB = kBpt > 0 ? kBpt : kAqMaxBpt;
+        float bmax[kB];
         float amax = 0.0f;
 #pragma unroll
-        for (int i = 0; i < kAqMaxBpt; ++i) {
+        for (int i = 0; i < kB; ++i) {
             const int b = t + i * kThreadsPerRow;
             float bm = 0.0f;
-            if (valid && b < nblk) {
+            if (valid && (kBpt > 0 || b < nblk)) {
                 const uint32_t mm = bf16x16_absmax(srow[2 * b], srow[2 * b + 1]);
                 bm = fmaxf(bf16_lo(mm), bf16_hi(mm));
             }
@@ -207,10 +211,10 @@ __global__ void __launch_bounds__(kAqWarps * 32)
         // Pass 2: one block per lane.
         uint2* crow = reinterpret_cast<uint2*>(codes + (valid ? m : 0) * (K >> 1));
 #pragma unroll
-        for (int i = 0; i < kAqMaxBpt; ++i) {
-            if (i * kThreadsPerRow >= nblk) break;  // uniform across the warp
+        for (int i = 0; i < kB; ++i) {
+            if (kBpt == 0 && i * kThreadsPerRow >= nblk) break;  // uniform across the warp
             const int b = t + i * kThreadsPerRow;
-            const bool have = b < nblk;
+            const bool have = kBpt > 0 || b < nblk;
             uint32_t sfc = 0;
             if (d > 0.0f) sfc = e4m3_quotient(bmax[i], d, inv_d, d_fast);
             const float den = __fmul_rn(e4m3_value(sfc), s);
@@ -254,18 +258,18 @@ __global__ void __launch_bounds__(kAqWarps * 32)
     }
 }
 
-template <int G, bool kTensor>
+template <int G, bool kTensor, int kBpt = 0>
 cudaError_t run_act_quant(const LaunchCtx& ctx, const __nv_bfloat16* X, int64_t M, int64_t K,
                           int64_t rows_pad, uint8_t* codes, uint8_t* sf, float* s_row) {
     const size_t smem = (size_t)(kAqWarps / G) * kAqRing * (size_t)K * 2;
     static OccupancyCache occupancy;
     int per_sm = 0;
     const cudaError_t e =
-        blocks_per_sm(occupancy, ctx, act_quant_kernel<G, kTensor>, kAqWarps * 32, smem, &per_sm);
+        blocks_per_sm(occupancy, ctx, act_quant_kernel<G, kTensor, kBpt>, kAqWarps * 32, smem, &per_sm);
     if (e != cudaSuccess) return e;
     int64_t grid = (rows_pad + (kAqWarps / G) - 1) / (kAqWarps / G);
     if (grid > (int64_t)ctx.num_sms * per_sm) grid = (int64_t)ctx.num_sms * per_sm;
-    act_quant_kernel<G, kTensor><<<(unsigned)grid, kAqWarps * 32, smem, ctx.stream>>>(
+    act_quant_kernel<G, kTensor, kBpt><<<(unsigned)grid, kAqWarps * 32, smem, ctx.stream>>>(
         X, M, K, rows_pad, codes, sf, s_row, ctx.status);
     return cudaGetLastError();
 }
@@ -1100,6 +1104,18 @@ cudaError_t launch_act_quant(const LaunchCtx& ctx, const __nv_bfloat16* X, int64
                              uint8_t* codes, uint8_t* sf, float* s_row) {
     const int64_t rows_pad = (M + 127) / 128 * 128;
     // G warps per row: the fewest that keep a thread at kAqMaxBpt blocks of 16 or less.
+    if (K <= 4096 && K % 512 == 0) {
+        switch (K / 512) {  // one warp per row, a fixed number of blocks per thread
+            case 1: return run_act_quant<1, false, 1>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+            case 2: return run_act_quant<1, false, 2>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+            case 3: return run_act_quant<1, false, 3>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+            case 4: return run_act_quant<1, false, 4>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+            case 5: return run_act_quant<1, false, 5>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+            case 6: return run_act_quant<1, false, 6>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+            case 7: return run_act_quant<1, false, 7>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+            default: return run_act_quant<1, false, 8>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+        }
+    }
     if (K <= 4096) return run_act_quant<1, false>(ctx, X, M, K, rows_pad, codes, sf, s_row);
     if (K <= 8192) return run_act_quant<2, false>(ctx, X, M, K, rows_pad, codes, sf, s_row);
     if (K <= 16384) return run_act_quant<4, false>(ctx, X, M, K, rows_pad, codes, sf, s_row);

@@ -56,7 +56,8 @@ def test_act_quant_iteration_batch_sampled_rows(orc):
     _check_act(orc, X, rows)
 
 
-@pytest.mark.parametrize("M,K", [(1, 64), (129, 128), (300, 12288), (77, 32768), (1000, 2240)])
+@pytest.mark.parametrize("M,K", [(1, 64), (129, 128), (300, 12288), (77, 32768), (1000, 2240),
+                                 (64, 512), (33, 4096), (130, 1536)])
 def test_act_quant_shapes(orc, M, K):
     require_gpu()
     g = torch.Generator().manual_seed(M * 7 + K)
