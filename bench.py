@@ -391,9 +391,12 @@ def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk
     ms_per_step = elapsed_ms / args.steps
     e2e_ms_step = e2e_ms / args.steps
 
+    # The captured traffic is of the full workload: a --rows run has none.
+    workload = WORKLOAD if not args.rows else f"{WORKLOAD}@{args.rows}"
+
     def roof(bound, achieved, peak, unit, kernel):
         return {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
-                "frac": round(achieved / peak, 4), "traffic": dram_traffic(kernel, WORKLOAD)}
+                "frac": round(achieved / peak, 4), "traffic": dram_traffic(kernel, workload)}
 
     out = {
         "metric": "NVFP4 GEMM TFLOP/s (FLUX.1-shaped linears) & re-quant GB/s, % of roofline",
