@@ -11,7 +11,8 @@
  *                       no compile step).
  *   nvfp4_act_quant     quantize BF16 activations to NVFP4, one scale per token,
  *                       for the NVFP4-quantized solver (Sol-RL project page,
- *                       "Two-Stage Pipeline", Stage 1).
+ *                       "Two-Stage Pipeline", Stage 1); nvfp4_act_quant_tensor is
+ *                       the variant with one scale for the whole tensor.
  *   nvfp4_gemm          the block-scaled FP4 linear layer of that solver (same
  *                       section: "up to 4x TFLOPs vs. BF16").
  *   bf16_gemm           the BF16 linear layer of Stage 2 (regeneration of the
