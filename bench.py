@@ -119,9 +119,15 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=5)
+        return self.summarize(self.lines)
+
+    @staticmethod
+    def summarize(lines):
+        """Median SM clock, the maximum, and the throttle reasons seen as Active, from
+        nvidia-smi's CSV lines (FIELDS order, no header, no units)."""
         sm, mx, reasons = [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in lines:
             f = [x.strip() for x in ln.split(",")]
             if len(f) < 9:
                 continue

@@ -57,3 +57,18 @@ def test_algorithmic_bytes_scale_with_rows():
     a, b = bench.algorithmic_bytes(cfg, rcfg), bench.algorithmic_bytes(small, rcfg)
     assert a["nvfp4_requant"] == b["nvfp4_requant"]  # independent of the activations
     assert a["nvfp4_act_quant"] > 4 * b["nvfp4_act_quant"]
+
+
+def test_clock_summary_from_nvidia_smi_lines():
+    lines = [
+        "0, 2070, 2070, 950.1, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 1980, 2070, 1390.0, 0x0000000000000004, Not Active, Not Active, Not Active, Active",
+        "0, 2070, 2070, 1200.5, 0x0000000000000000, Not Active, Not Active, Not Active, Not Active",
+        "garbage line",
+        "0, [N/A], 2070, 0, 0x0, Not Active, Not Active, Not Active, Not Active",
+    ]
+    got = bench.ClockSampler.summarize(lines)
+    assert got == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "samples": 3, "reasons": ["sw_power_cap"]}
+    hot = lines[:1] + ["0, 1500, 2070, 900, 0x8, Active, Not Active, Active, Not Active"]
+    assert bench.ClockSampler.summarize(hot)["reasons"] == ["hw_slowdown", "sw_power_cap", "sw_thermal_slowdown"]
+    assert bench.ClockSampler.summarize([]) is None
