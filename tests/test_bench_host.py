@@ -72,3 +72,32 @@ def test_clock_summary_from_nvidia_smi_lines():
     hot = lines[:1] + ["0, 1500, 2070, 900, 0x8, Active, Not Active, Active, Not Active"]
     assert bench.ClockSampler.summarize(hot)["reasons"] == ["hw_slowdown", "sw_power_cap", "sw_thermal_slowdown"]
     assert bench.ClockSampler.summarize([]) is None
+
+
+def test_report_line_has_the_contract_keys():
+    """The JSON line bench.py prints, from made-up timings (no GPU): every key of the
+    contract is there and the derived numbers follow from the timings."""
+    import argparse
+    cfg = workloads.LINEARS["flux_up"]
+    rcfg = workloads.REWARDS[bench.REWARD_CFG]
+    args = argparse.Namespace(steps=10, warmup=3, rows=None, no_e2e=False, no_cpu_baseline=True)
+    per = {"nvfp4_requant": 0.1, "nvfp4_act_quant": 0.08, "nvfp4_gemm": 0.5, "bf16_gemm": 1.5,
+           "select_contrastive": 0.016}
+    clk = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "samples": 5, "reasons": []}
+    out = bench.report(args, cfg, rcfg, None, per, 22.0, 50.0, 304, 906, 0, clk, 1, 0,
+                       {"nvfp4_requant": 3, "nvfp4_act_quant": 1, "nvfp4_gemm": 1, "bf16_gemm": 1,
+                        "select_contrastive": 2}, 0.12)
+    for k in ["metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks"]:
+        assert k in out, k
+    flops = 2.0 * cfg.M * cfg.N * cfg.K
+    assert abs(out["value"] - flops / 0.5e-3 / 1e12) < 0.01
+    assert out["ms_per_step"] == 2.2 and out["gpu_launches"] == 80
+    assert out["config"]["workload"].startswith("FLUX.1-shaped MLP up-projection")
+    assert set(out["roofline"]) == {"bound", "achieved", "peak", "unit", "frac", "traffic"}
+    assert abs(out["roofline"]["frac"] - out["roofline"]["achieved"] / out["roofline"]["peak"]) < 1e-3
+    assert out["e2e"]["h2d_bytes_per_step"] == 304 and out["e2e"]["ms_per_step"] == 5.0
+    assert out["variants"]["act_quant_per_tensor"]["ms"] == 0.12
+    small = argparse.Namespace(**{**vars(args), "rows": 8192})
+    out2 = bench.report(small, cfg, rcfg, None, per, 22.0, 50.0, 304, 906, 0, clk, 1, 0, {}, 0.12)
+    assert all(r["traffic"] is None for r in out2["rooflines"].values())  # no capture of that workload
