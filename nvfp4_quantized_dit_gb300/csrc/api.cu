@@ -251,7 +251,8 @@ nvfp4_status nvfp4_act_quant_tensor(const void* X, int64_t M, int64_t K, uint8_t
     nvfp4_status st = resolve(stream, &ctx);
     if (st != NVFP4_OK) return st;
     if (M == 0) return from_cuda(cudaMemsetAsync(s_t, 0, sizeof(float), ctx.stream));
-    return from_cuda(launch_act_quant_tensor(ctx, static_cast<const __nv_bfloat16*>(X), M, K, codes, sf, s_t));
+    return from_cuda(
+        launch_act_quant_tensor(ctx, static_cast<const __nv_bfloat16*>(X), M, K, codes, sf, s_t));
 }
 
 nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_srow,

@@ -178,8 +178,8 @@ cudaError_t launch_select(const LaunchCtx& ctx, const float* rewards, int P, int
     cfg.numAttrs = 1;
     // The reciprocals of the means' divisors, for div_by (fp64 divisions on the host).
     const double inv_k = 1.0 / (double)K, inv_total = 1.0 / ((double)P * (double)K);
-    return cudaLaunchKernelEx(&cfg, select_transform_kernel, rewards, N, static_cast<const int32_t*>(idx), P, K,
-                              global_std, inv_k, inv_total, r_out);
+    return cudaLaunchKernelEx(&cfg, select_transform_kernel, rewards, N, static_cast<const int32_t*>(idx),
+                              P, K, global_std, inv_k, inv_total, r_out);
 }
 
 }  // namespace nvfp4rl

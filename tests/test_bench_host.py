@@ -70,7 +70,8 @@ def test_clock_summary_from_nvidia_smi_lines():
     got = bench.ClockSampler.summarize(lines)
     assert got == {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "samples": 3, "reasons": ["sw_power_cap"]}
     hot = lines[:1] + ["0, 1500, 2070, 900, 0x8, Active, Not Active, Active, Not Active"]
-    assert bench.ClockSampler.summarize(hot)["reasons"] == ["hw_slowdown", "sw_power_cap", "sw_thermal_slowdown"]
+    reasons = bench.ClockSampler.summarize(hot)["reasons"]
+    assert reasons == ["hw_slowdown", "sw_power_cap", "sw_thermal_slowdown"]
     assert bench.ClockSampler.summarize([]) is None
 
 
@@ -88,7 +89,8 @@ def test_report_line_has_the_contract_keys():
                        {"nvfp4_requant": 3, "nvfp4_act_quant": 1, "nvfp4_gemm": 1, "bf16_gemm": 1,
                         "select_contrastive": 2}, 0.12)
     for k in ["metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
-              "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches", "clocks"]:
+              "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches",
+              "clocks"]:
         assert k in out, k
     flops = 2.0 * cfg.M * cfg.N * cfg.K
     assert abs(out["value"] - flops / 0.5e-3 / 1e12) < 0.01
