@@ -159,6 +159,7 @@ nvfp4_status nvfp4_act_quant(const void* X, int64_t M, int64_t K, uint8_t* codes
  *   codes  device, [M, K/2] bytes (out).
  *   sf     device, nvfp4_sf_bytes(M, K) bytes (out, padding rows written 0).
  *   s_t    device, one fp32 (out); also the amax accumulator while the call runs.
+ *          Required even when M == 0 (it is then set to 0; X, codes, sf may be NULL).
  *   K % 64 == 0, K <= 32768, M < 2^31.  Two passes over X: a memset, an amax kernel,
  *   the quantize kernel and a one-thread kernel that turns amax into s_t.  Gives the
  *   same codes, scales and s_t as nvfp4_requant with no LoRA factors on X.

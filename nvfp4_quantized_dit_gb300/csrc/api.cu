@@ -244,9 +244,12 @@ nvfp4_status nvfp4_act_quant(const void* X, int64_t M, int64_t K, uint8_t* codes
 nvfp4_status nvfp4_act_quant_tensor(const void* X, int64_t M, int64_t K, uint8_t* codes, uint8_t* sf,
                                     float* s_t, void* stream) {
     if (M < 0 || M > kMaxRows || K <= 0 || K % 64 != 0 || K > 32768) return NVFP4_ERR_SHAPE;
-    if (X == nullptr || codes == nullptr || sf == nullptr || s_t == nullptr) return NVFP4_ERR_NULL;
-    if (misaligned(X, 16) || misaligned(codes, 16) || misaligned(sf, 16) || misaligned(s_t, 4))
-        return NVFP4_ERR_ALIGN;
+    if (s_t == nullptr) return NVFP4_ERR_NULL;  // written even for an empty tensor (s_t = 0)
+    if (misaligned(s_t, 4)) return NVFP4_ERR_ALIGN;
+    if (M > 0) {
+        if (X == nullptr || codes == nullptr || sf == nullptr) return NVFP4_ERR_NULL;
+        if (misaligned(X, 16) || misaligned(codes, 16) || misaligned(sf, 16)) return NVFP4_ERR_ALIGN;
+    }
     LaunchCtx ctx;
     nvfp4_status st = resolve(stream, &ctx);
     if (st != NVFP4_OK) return st;

@@ -87,6 +87,8 @@ def test_act_quant_tensor_validation(lib):
     assert lib.nvfp4_act_quant_tensor(None, 4, 64, P(A16), P(A16), P(A16), None) == 1
     assert lib.nvfp4_act_quant_tensor(P(A16), 4, 64, P(A16), P(A16), None, None) == 1  # s_t
     assert lib.nvfp4_act_quant_tensor(P(BAD), 4, 64, P(A16), P(A16), P(A16), None) == 3
+    assert lib.nvfp4_act_quant_tensor(None, 0, 64, None, None, None, None) == 1  # s_t always written
+    assert lib.nvfp4_act_quant_tensor(None, 0, 64, None, None, P(BAD), None) == 3
 
 
 def test_requant_validation(lib):
