@@ -163,6 +163,9 @@ nvfp4_status nvfp4_act_quant(const void* X, int64_t M, int64_t K, uint8_t* codes
  *   K % 64 == 0, K <= 32768, M < 2^31.  Two passes over X: a memset, an amax kernel,
  *   the quantize kernel and a one-thread kernel that turns amax into s_t.  Gives the
  *   same codes, scales and s_t as nvfp4_requant with no LoRA factors on X.
+ *   To use the result as nvfp4_gemm's activations, pass an [M] fp32 vector holding s_t
+ *   in every entry as a_srow (the GEMM reads one scale per row; s_t alone is a single
+ *   float and must not be passed there).
  */
 nvfp4_status nvfp4_act_quant_tensor(const void* X, int64_t M, int64_t K, uint8_t* codes, uint8_t* sf,
                                     float* s_t, void* stream);
@@ -228,8 +231,10 @@ nvfp4_status select_contrastive(const float* rewards, int P, int N, int K, int g
  *   - One scratch per device, shared by every call: two calls whose work can
  *     overlap on the device (different streams without ordering between them)
  *     race on it.  Order them (one stream, or events).
- *   - The first call on each device looks up the scratch's address (a runtime
- *     query, cached afterwards); make that first call outside any stream capture.
+ *   - Arguments are checked first, then the device's architecture, exactly as in
+ *     nvfp4_requant; only then does the first call on each device look up the
+ *     scratch's address (a runtime query, cached afterwards), so make that first
+ *     call outside any stream capture.
  */
 #define NVFP4_NOALLOC_SCRATCH_BYTES ((size_t)8 * 1024 * 1024 + (size_t)64 * 1024)
 nvfp4_status nvfp4_requant_noalloc(const void* W, int w_dtype, const float* A, const float* B,

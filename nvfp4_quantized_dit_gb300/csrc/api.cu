@@ -163,9 +163,11 @@ size_t nvfp4_requant_workspace_bytes(int w_dtype, int r, int64_t N, int64_t K) {
     return requant_tc_workspace_bytes(w_dtype, r, N, K);
 }
 
-nvfp4_status nvfp4_requant(const void* W, int w_dtype, const float* A, const float* B, int r,
-                           float alpha, int64_t N, int64_t K, uint8_t* codes, uint8_t* sf,
-                           float* s_t, void* workspace, size_t workspace_bytes, void* stream) {
+// nvfp4_requant's argument checks (no CUDA call); both requant entry points run them
+// before resolving the device.
+static nvfp4_status check_requant(const void* W, int w_dtype, const float* A, const float* B, int r,
+                                  int64_t N, int64_t K, const uint8_t* codes, const uint8_t* sf,
+                                  const float* s_t) {
     if (w_dtype != NVFP4_W_BF16 && w_dtype != NVFP4_W_FP32) return NVFP4_ERR_SHAPE;
     if (r < 0 || r > 64 || N < 0 || N > kMaxRows || K <= 0 || K % 64 != 0 || K > (1 << 20))
         return NVFP4_ERR_SHAPE;
@@ -177,8 +179,17 @@ nvfp4_status nvfp4_requant(const void* W, int w_dtype, const float* A, const flo
         if (misaligned(W, 16) || misaligned(codes, 16) || misaligned(sf, 16)) return NVFP4_ERR_ALIGN;
         if (merge && (misaligned(A, 16) || misaligned(B, 4))) return NVFP4_ERR_ALIGN;
     }
+    return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_requant(const void* W, int w_dtype, const float* A, const float* B, int r,
+                           float alpha, int64_t N, int64_t K, uint8_t* codes, uint8_t* sf,
+                           float* s_t, void* workspace, size_t workspace_bytes, void* stream) {
+    nvfp4_status st = check_requant(W, w_dtype, A, B, r, N, K, codes, sf, s_t);
+    if (st != NVFP4_OK) return st;
+    const bool merge = r > 0 && A != nullptr && B != nullptr;
     LaunchCtx ctx;
-    nvfp4_status st = resolve(stream, &ctx);
+    st = resolve(stream, &ctx);
     if (st != NVFP4_OK) return st;
     if (N == 0) return from_cuda(cudaMemsetAsync(s_t, 0, sizeof(float), ctx.stream));
     const float c = merge ? alpha / static_cast<float>(r) : 0.0f;
@@ -202,26 +213,28 @@ nvfp4_status nvfp4_requant(const void* W, int w_dtype, const float* A, const flo
 nvfp4_status nvfp4_requant_noalloc(const void* W, int w_dtype, const float* A, const float* B,
                                    int r, float alpha, int64_t N, int64_t K, uint8_t* codes,
                                    uint8_t* sf, float* s_t, void* stream) {
+    // The same checks, in the same order, as nvfp4_requant (arguments, then the device's
+    // architecture) before the scratch's address is looked up.
+    nvfp4_status st = check_requant(W, w_dtype, A, B, r, N, K, codes, sf, s_t);
+    if (st != NVFP4_OK) return st;
     const bool merge = r > 0 && A != nullptr && B != nullptr;
     const size_t need = merge ? nvfp4_requant_workspace_bytes(w_dtype, r, N, K) : 0;
     if (need > NVFP4_NOALLOC_SCRATCH_BYTES) return NVFP4_ERR_SHAPE;
+    LaunchCtx ctx;
+    st = resolve(stream, &ctx);
+    if (st != NVFP4_OK) return st;
     void* scratch = nullptr;
-    if (need > 0) {
-        int dev = -1;
-        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-            cudaGetLastError();
-            return NVFP4_ERR_CUDA;
-        }
+    if (need > 0 && N > 0) {
         std::lock_guard<std::mutex> lock(g_mutex);
-        if (g_noalloc_addr[dev] == nullptr) {
+        if (g_noalloc_addr[ctx.device] == nullptr) {
             void* p = nullptr;
             if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
                 cudaGetLastError();
                 return NVFP4_ERR_CUDA;
             }
-            g_noalloc_addr[dev] = p;
+            g_noalloc_addr[ctx.device] = p;
         }
-        scratch = g_noalloc_addr[dev];
+        scratch = g_noalloc_addr[ctx.device];
     }
     return nvfp4_requant(W, w_dtype, A, B, r, alpha, N, K, codes, sf, s_t, scratch,
                          scratch != nullptr ? NVFP4_NOALLOC_SCRATCH_BYTES : 0, stream);

@@ -180,3 +180,56 @@ def test_act_quant_reads_bf16_bits(orc):
     qc, sf, s = orc.act_quant(xb)
     qc2, sf2, s2 = orc.quantize(((xb.astype(np.uint32)) << 16).view(np.float32), "row")
     assert np.array_equal(qc, qc2) and np.array_equal(sf, sf2) and np.array_equal(s, s2)
+
+
+def _rn32(fr):
+    """Round a non-negative exact rational to the nearest fp32 value, ties to even
+    (normal range only), by integer arithmetic on the rational itself."""
+    assert fr > 0
+    e = fr.numerator.bit_length() - fr.denominator.bit_length()
+    if Fraction(2) ** e > fr:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= fr:
+        e += 1
+    ulp = Fraction(2) ** (e - 23)
+    q, rem = divmod(fr, ulp)
+    q = int(q)
+    if rem * 2 > ulp or (rem * 2 == ulp and q % 2 == 1):
+        q += 1
+    return q * ulp
+
+
+def test_quotient_is_one_division_at_e2m1_ties(orc):
+    """Reading R1 (q = x / (sf * s), one IEEE division) decides exact ties that the
+    reciprocal-multiply and two-step forms resolve the other way
+    (tests/golden/quotient_ties.txt).  Exact rationals establish, independently of
+    the oracle, that each quotient is exactly the boundary and that the other forms
+    are above it; the oracle must return the tie's even code."""
+    from conftest import golden_lines
+    rows = golden_lines("quotient_ties.txt")
+    amax = float(rows[0][1])
+    elems = [(float(r[1]), float(r[2]), int(r[3], 16), int(r[4], 16)) for r in rows[1:]]
+    a = Fraction(np.float32(amax).item())
+    s = _rn32(a / 2688)
+    d6 = _rn32(6 * s)
+    assert _rn32(a / d6) == 448  # block scale exactly 448: code 0x7E
+    den = _rn32(448 * s)
+    rec = _rn32(1 / den)
+    for x, b, _, _ in elems:
+        xf = Fraction(np.float32(x).item())
+        assert _rn32(xf / den) == Fraction(b)            # exactly the boundary
+        assert _rn32(xf * rec) > Fraction(b)             # reciprocal form: above it
+        assert _rn32(_rn32(xf / s) / 448) > Fraction(b)  # two-step form: above it
+    x = np.zeros((1, 16), np.float32)
+    x[0, 0] = amax
+    for i, (v, _, _, _) in enumerate(elems):
+        x[0, 1 + i] = v
+    codes, sf, st = orc.quantize(x, "tensor")
+    assert sf[0, 0] == 0x7E
+    assert st[0] == np.float32(float(s))
+    nib = [(codes[0, i // 2] >> (4 * (i % 2))) & 0xF for i in range(16)]
+    assert nib[0] == 0x7  # the amax element: 6.0
+    for i, (_, _, by_div, by_rec) in enumerate(elems):
+        assert by_div != by_rec
+        assert nib[1 + i] == by_div, f"element {1 + i}: code {nib[1 + i]:#x}, want {by_div:#x}"
+    assert all(n == 0 for n in nib[4:])
