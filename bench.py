@@ -1,10 +1,10 @@
 """Benchmark of the NVFP4 FP4-explore hot path on one GB300 (or N replicas).
 
-One step = one pass of the whole hot path over one batch of synthetic input of
-the FLUX.1-shaped MLP up-projection (M = 8 images x 4608 tokens = 36864, K = 3072,
-N = 12288), all calls through the library's C ABI:
-  1. nvfp4_requant       LoRA (r = 32) merge of W [12288, 3072] bf16 + per-tensor NVFP4
-  2. nvfp4_act_quant     per-row NVFP4 of X [36864, 3072] bf16
+One step = one pass of the whole hot path over one batch of synthetic input of a
+rollout linear (default: the FLUX.1-shaped MLP up-projection, M = 8 images x 4608
+tokens = 36864, K = 3072, N = 12288), all calls through the library's C ABI:
+  1. nvfp4_requant       LoRA (r = 32) merge of W [N, K] bf16 + per-tensor NVFP4
+  2. nvfp4_act_quant     per-row NVFP4 of X [M, K] bf16
   3. nvfp4_gemm          Y = X W'^T + bias, block-scaled FP4 on the tensor cores
   4. bf16_gemm           the BF16 counterpart (Stage 2), for the FP4 / BF16 ratio
   5. select_contrastive  32 prompts x 96 proxy rewards -> top/bottom 12 + reward transform
@@ -12,8 +12,13 @@ N = 12288), all calls through the library's C ABI:
 Prints one JSON line.  `value` is the NVFP4 GEMM throughput in TFLOP/s (2MNK per
 launch / mean CUDA-event duration of the launch over the timed steps, summed over
 ranks); the re-quantization GB/s and every other kernel's roofline are reported
-beside it.  `--impl reference` times the CPU oracle on a bounded sample of the
-same workload instead (no GPU work).
+beside it.  Outside the timed steps it also measures, on rank 0: the same calls on
+the SANA- and SD3.5-L-shaped linears (`per_config`), the iteration-shaped batch
+(57 weight re-quantizations and the 442368-row 3072 -> 12288 -> 3072 chain,
+`iteration`), cuBLAS's NVFP4 GEMM at 8192^3 as a reference point for the FP4 peak,
+and the spread of the selected rewards against N (`evt_spread`).  `--impl reference`
+times the CPU oracle on a bounded sample of the same workload instead (no GPU work).
+`--gpus N` without a launcher starts N local replicas itself (torchrun).
 """
 
 from __future__ import annotations
@@ -21,7 +26,9 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
+import socket
 import statistics
 import subprocess
 import sys
@@ -32,10 +39,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-WORKLOAD = "flux_up"
+HEADLINE = "flux_up"
+SWEEP_CONFIGS = ["sana", "sd35_qkv", "sd35_mlp"]
 REWARD_CFG = "iter"
+ITER_MATRICES = 57          # weights re-quantized per iteration, alternating up / down
+EVT_DELTA = 0.1             # bounded proxy perturbation used by the EVT spread report
 NOMINAL_FP4_OVER_BF16 = 13.5 / 2.25  # dense NVFP4 / dense BF16 tensor rates, GB300 nominal
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20  # written between timed repetitions of the sweeps (L2 is 129 MB)
 
 
 # ----------------------------------------------------------------------------- helpers
@@ -171,9 +182,23 @@ def barrier(world: int, device=None):
             dist.barrier()
 
 
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def replica_command(n: int, argv) -> list:
+    """The command that runs this script as n local replicas, one process per GPU
+    (torchrun on this node, rendezvous on 127.0.0.1)."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+            "--master-addr", "127.0.0.1", "--master-port", str(_free_port()),
+            os.path.abspath(__file__), *argv]
+
+
 # ----------------------------------------------------------------------------- workload
 
-def algorithmic_bytes(cfg, rcfg):
+def algorithmic_bytes(cfg):
     M, K, N = cfg.M, cfg.K, cfg.N
     sf_w = (N + 127) // 128 * 128 * (K // 16)
     sf_a = (M + 127) // 128 * 128 * (K // 16)
@@ -187,23 +212,249 @@ def algorithmic_bytes(cfg, rcfg):
     }
 
 
-def make_inputs(device, seed=0, rows=None):
+def host_inputs(name, seed=0, rows=None):
     import dataclasses
     import workloads
-    cfg = workloads.LINEARS[WORKLOAD]
+    cfg = workloads.LINEARS[name]
     if rows:
         cfg = dataclasses.replace(cfg, M=int(rows))
-    rcfg = workloads.REWARDS[REWARD_CFG]
-    host = {
-        "X": workloads.activations(cfg, seed),
-        "W": workloads.weight(cfg, seed),
-        "bias": workloads.bias(cfg, seed),
-        "rewards": workloads.rewards(rcfg, seed),
-    }
+    host = {"X": workloads.activations(cfg, seed), "W": workloads.weight(cfg, seed),
+            "bias": workloads.bias(cfg, seed)}
     host["A"], host["B"] = workloads.lora(cfg, seed)
-    dev = {k: v.to(device) for k, v in host.items()}
-    return cfg, rcfg, host, dev
+    return cfg, host
 
+
+class L2Flush:
+    """Writes a buffer larger than L2 between timed repetitions."""
+
+    def __init__(self, device):
+        import torch
+        self.buf = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.buf.fill_(1.0)
+
+
+def time_call(fn, reps, flush, warm=3):
+    """Median CUDA-event duration (ms) of fn() on the current stream, L2 flushed
+    before every repetition (outside the events)."""
+    import torch
+    for _ in range(warm):
+        fn()
+    ts = []
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def linear_sweep(name, device, flush, pk, fp4_peak, reps=10):
+    """requant, act_quant, nvfp4_gemm and bf16_gemm of one configuration, each timed
+    alone (median of `reps`, L2 flushed before each)."""
+    import torch
+    import nvfp4_quantized_dit_gb300 as nv
+    import workloads
+    cfg, host = host_inputs(name)
+    d = {k: v.to(device) for k, v in host.items()}
+    M, K, N = cfg.M, cfg.K, cfg.N
+    wq = (torch.empty(N, K // 2, dtype=torch.uint8, device=device),
+          torch.empty(nv.sf_bytes(N, K), dtype=torch.uint8, device=device),
+          torch.empty(1, dtype=torch.float32, device=device))
+    aq = (torch.empty(M, K // 2, dtype=torch.uint8, device=device),
+          torch.empty(nv.sf_bytes(M, K), dtype=torch.uint8, device=device),
+          torch.empty(M, dtype=torch.float32, device=device))
+    ws = torch.empty(max(nv.requant_workspace_bytes(nv.W_BF16, 32, N, K), 1), dtype=torch.uint8, device=device)
+    y4 = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+    y16 = torch.empty(M, N, dtype=torch.bfloat16, device=device)
+    ms = {
+        "nvfp4_requant": time_call(lambda: nv.nvfp4_requant(d["W"], d["A"], d["B"], workloads.LORA_ALPHA,
+                                                            *wq, workspace=ws), reps, flush),
+        "nvfp4_act_quant": time_call(lambda: nv.nvfp4_act_quant(d["X"], *aq), reps, flush),
+        "nvfp4_gemm": time_call(lambda: nv.nvfp4_gemm(aq, wq, d["bias"], out=y4), reps, flush),
+        "bf16_gemm": time_call(lambda: nv.bf16_gemm(d["X"], d["W"], d["bias"], out=y16), reps, flush),
+    }
+    ab = algorithmic_bytes(cfg)
+    flop = 2.0 * M * N * K
+    t4 = flop / (ms["nvfp4_gemm"] * 1e-3) / 1e12
+    t16 = flop / (ms["bf16_gemm"] * 1e-3) / 1e12
+    rq = ab["nvfp4_requant"] / (ms["nvfp4_requant"] * 1e-3) / 1e9
+    aqg = ab["nvfp4_act_quant"] / (ms["nvfp4_act_quant"] * 1e-3) / 1e9
+    out = {"workload": cfg.description, "M": M, "K": K, "N": N,
+           "kernel_ms": {k: round(v, 4) for k, v in ms.items()},
+           "nvfp4_gemm_tflops": round(t4, 1), "nvfp4_gemm_frac": round(t4 / fp4_peak, 4),
+           "bf16_gemm_tflops": round(t16, 1), "bf16_gemm_frac": round(t16 / pk["bf16_tflops"], 4),
+           "fp4_over_bf16": round(t4 / t16, 3),
+           "requant_gbs": round(rq, 1), "requant_frac": round(rq / pk["hbm_gbs"], 4),
+           "act_quant_gbs": round(aqg, 1), "act_quant_frac": round(aqg / pk["hbm_gbs"], 4)}
+    del d, wq, aq, ws, y4, y16
+    torch.cuda.empty_cache()
+    return out
+
+
+def iteration_sweep(device, pk, fp4_peak, reps=3):
+    """The iteration-shaped batch: ITER_MATRICES LoRA merges + re-quantizations of
+    [12288, 3072] / [3072, 12288] weights back to back (each its own buffer in HBM,
+    4.3 GB in all, so nothing is served from L2), then the 442368-row chain
+    act_quant -> nvfp4_gemm -> act_quant -> nvfp4_gemm (3072 -> 12288 -> 3072)."""
+    import torch
+    import nvfp4_quantized_dit_gb300 as nv
+    import workloads
+    up, dn = workloads.LINEARS["iter_up"], workloads.LINEARS["iter_down"]
+    shapes = [up, dn]
+    base = [workloads.weight(c, 0).to(device) for c in shapes]
+    lora = [tuple(t.to(device) for t in workloads.lora(c, 0)) for c in shapes]
+    Ws = [base[i % 2].clone() for i in range(ITER_MATRICES)]
+    outs = []
+    for i in range(ITER_MATRICES):
+        c = shapes[i % 2]
+        outs.append((torch.empty(c.N, c.K // 2, dtype=torch.uint8, device=device),
+                     torch.empty(nv.sf_bytes(c.N, c.K), dtype=torch.uint8, device=device),
+                     torch.empty(1, dtype=torch.float32, device=device)))
+    wss = [torch.empty(nv.requant_workspace_bytes(nv.W_BF16, 32, c.N, c.K), dtype=torch.uint8, device=device)
+           for c in shapes]
+
+    def sweep():
+        for i in range(ITER_MATRICES):
+            A, B = lora[i % 2]
+            nv.nvfp4_requant(Ws[i], A, B, workloads.LORA_ALPHA, *outs[i], workspace=wss[i % 2])
+
+    sweep()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        sweep()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    sweep_ms = statistics.median(ts)
+    rq_bytes = sum(algorithmic_bytes(shapes[i % 2])["nvfp4_requant"] for i in range(ITER_MATRICES))
+    rq_gbs = rq_bytes / (sweep_ms * 1e-3) / 1e9
+    requant = {"matrices": ITER_MATRICES, "ms": round(sweep_ms, 4),
+               "us_per_matrix": round(sweep_ms * 1e3 / ITER_MATRICES, 2), "gbs": round(rq_gbs, 1),
+               "frac": round(rq_gbs / pk["hbm_gbs"], 4),
+               "floor_ms": round(rq_bytes / (pk["hbm_gbs"] * 1e9) * 1e3, 4)}
+    w_up, w_dn = outs[0], outs[1]
+    del Ws, wss
+    torch.cuda.empty_cache()
+
+    # the chain over the whole batch (inputs drawn on the device: timing only)
+    M = up.M
+    X = workloads.activations_on_device(up, device, 0)
+    bias_up, bias_dn = workloads.bias(up, 0).to(device), workloads.bias(dn, 0).to(device)
+    xq = (torch.empty(M, up.K // 2, dtype=torch.uint8, device=device),
+          torch.empty(nv.sf_bytes(M, up.K), dtype=torch.uint8, device=device),
+          torch.empty(M, dtype=torch.float32, device=device))
+    H = torch.empty(M, up.N, dtype=torch.bfloat16, device=device)
+    hq = (torch.empty(M, dn.K // 2, dtype=torch.uint8, device=device),
+          torch.empty(nv.sf_bytes(M, dn.K), dtype=torch.uint8, device=device),
+          torch.empty(M, dtype=torch.float32, device=device))
+    Y = torch.empty(M, dn.N, dtype=torch.bfloat16, device=device)
+    calls = [("act_quant_x", lambda: nv.nvfp4_act_quant(X, *xq)),
+             ("gemm_up", lambda: nv.nvfp4_gemm(xq, w_up, bias_up, out=H)),
+             ("act_quant_hidden", lambda: nv.nvfp4_act_quant(H, *hq)),
+             ("gemm_down", lambda: nv.nvfp4_gemm(hq, w_dn, bias_dn, out=Y))]
+    for _, fn in calls:
+        fn()
+    torch.cuda.synchronize()
+    per = {n: [] for n, _ in calls}
+    total = []
+    for _ in range(reps):
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)]
+        ev[0].record()
+        for i, (_, fn) in enumerate(calls):
+            fn()
+            ev[i + 1].record()
+        ev[-1].synchronize()
+        for i, (n, _) in enumerate(calls):
+            per[n].append(ev[i].elapsed_time(ev[i + 1]))
+        total.append(ev[0].elapsed_time(ev[-1]))
+    per = {n: statistics.median(v) for n, v in per.items()}
+    chain_ms = statistics.median(total)
+    flop = 2.0 * M * up.N * up.K
+    by_x = algorithmic_bytes(up)["nvfp4_act_quant"]
+    by_h = algorithmic_bytes(dn)["nvfp4_act_quant"]
+    chain = {"rows": M, "kernel_ms": {n: round(v, 4) for n, v in per.items()}, "ms": round(chain_ms, 4),
+             "gemm_up_tflops": round(flop / (per["gemm_up"] * 1e-3) / 1e12, 1),
+             "gemm_down_tflops": round(flop / (per["gemm_down"] * 1e-3) / 1e12, 1),
+             "gemm_frac": round(2 * flop / ((per["gemm_up"] + per["gemm_down"]) * 1e-3) / 1e12 / fp4_peak, 4),
+             "act_quant_hidden_gbs": round(by_h / (per["act_quant_hidden"] * 1e-3) / 1e9, 1),
+             "act_quant_x_gbs": round(by_x / (per["act_quant_x"] * 1e-3) / 1e9, 1),
+             "chain_tflops": round(2 * flop / (chain_ms * 1e-3) / 1e12, 1)}
+    del X, xq, H, hq, Y
+    torch.cuda.empty_cache()
+    return {"requant_sweep": requant, "chain": chain}
+
+
+def cublas_nvfp4_peak(device, size=8192, reps=10):
+    """cuBLAS's NVFP4 GEMM (torch._scaled_mm) at size^3 on random operand bytes, best of
+    `reps`: a measured reference point for the FP4 tensor rate.  None if torch cannot
+    run it."""
+    import torch
+    try:
+        g = torch.Generator(device=device)
+        g.manual_seed(0)
+        a = torch.randint(0, 256, (size, size // 2), dtype=torch.uint8, device=device, generator=g)
+        w = torch.randint(0, 256, (size, size // 2), dtype=torch.uint8, device=device, generator=g)
+        nsf = size * size // 16
+        sa = torch.randint(0x30, 0x40, (nsf,), dtype=torch.uint8, device=device, generator=g)
+        sw = torch.randint(0x30, 0x40, (nsf,), dtype=torch.uint8, device=device, generator=g)
+        A4, W4 = a.view(torch.float4_e2m1fn_x2), w.view(torch.float4_e2m1fn_x2)
+        SA, SW = sa.view(torch.float8_e4m3fn), sw.view(torch.float8_e4m3fn)
+
+        def fn():
+            return torch._scaled_mm(A4, W4.t(), SA, SW, out_dtype=torch.bfloat16)
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        best = float("inf")
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        return {"tflops": round(2.0 * size ** 3 / (best * 1e-3) / 1e12, 1), "size": size, "reps": reps,
+                "how": "torch._scaled_mm float4_e2m1fn_x2 x float4_e2m1fn_x2, float8_e4m3fn block scales, "
+                       "bf16 out, best of reps (CUDA events)"}
+    except Exception as e:  # noqa: BLE001 - a reference point only
+        return {"tflops": None, "unavailable": repr(e)[:200]}
+
+
+def evt_report(device, P=2048, K=24, delta=EVT_DELTA, seed=0):
+    """Spread of the selected rewards against N (AI Trends summary, the paragraph on
+    extreme value theory: the expected reward range W of the explored group grows like
+    2 sigma sqrt(2 log N), less 4 Delta for a perturbation bounded by Delta).  True
+    rewards ~ N(0, 1) for P prompts x N seeds; the proxy (standing in for the FP4
+    rollout's reward) adds noise uniform in [-Delta, Delta]; select_contrastive picks
+    on the proxy.  Reported per N: the mean true-reward gap between the best and worst
+    proxy-selected seeds, the mean true range max - min, and the page's expression."""
+    import torch
+    import nvfp4_quantized_dit_gb300 as nv
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    rows = []
+    for N in (24, 48, 96, 192, 384, 768, 1024):
+        r = torch.randn(P, N, generator=g, device=device)
+        proxy = r + (torch.rand(P, N, generator=g, device=device) * 2 - 1) * delta
+        idx, _ = nv.select_contrastive(proxy, K, with_transform=False)
+        top, bot = idx[:, 0].long(), idx[:, K // 2].long()
+        ar = torch.arange(P, device=device)
+        gap = (r[ar, top] - r[ar, bot]).mean().item()
+        rng = (r.max(dim=1).values - r.min(dim=1).values).mean().item()
+        rows.append({"N": N, "selected_gap": round(gap, 4), "true_range": round(rng, 4),
+                     "page_expression": round(2 * math.sqrt(2 * math.log(N)) - 4 * delta, 4)})
+    return {"prompts": P, "K": K, "delta": delta, "rows": rows}
+
+
+# ----------------------------------------------------------------------------- our arm
 
 def run_ours(args):
     import torch
@@ -218,7 +469,10 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=device)
     nv.library()
 
-    cfg, rcfg, host, dev = make_inputs(device, rows=args.rows)
+    cfg, host = host_inputs(args.config, rows=args.rows)
+    rcfg = workloads.REWARDS[REWARD_CFG]
+    host["rewards"] = workloads.rewards(rcfg, 0)
+    dev = {k: v.to(device) for k, v in host.items()}
     M, K, N = cfg.M, cfg.K, cfg.N
     Kr = rcfg.K
     # outputs, allocated once
@@ -236,8 +490,7 @@ def run_ours(args):
     ws_bytes = nv.requant_workspace_bytes(nv.W_BF16, 32, N, K)
     rq_ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
     names = ["nvfp4_requant", "nvfp4_act_quant", "nvfp4_gemm", "bf16_gemm", "select_contrastive"]
-    # requant: split kernel, amax pass, quantize pass (tensor-core merge); or amax pass,
-    # quantize pass, finalize (CUDA-core merge)
+    # requant: split kernel, amax pass, quantize pass (tensor-core merge)
     launches_per_step = {"nvfp4_requant": 3, "nvfp4_act_quant": 1, "nvfp4_gemm": 1, "bf16_gemm": 1,
                          "select_contrastive": 2}
 
@@ -302,6 +555,7 @@ def run_ours(args):
         v1.synchronize()
         vt.append(v0.elapsed_time(v1))
     per_tensor_ms = max_over_ranks(statistics.median(vt), world, device)
+    del xq_codes, xq_sf
 
     # ---- end to end: pinned host inputs in, result out, every step
     if args.no_e2e:
@@ -310,8 +564,24 @@ def run_ours(args):
     else:
         e2e_ms, h2d, d2h = run_e2e(args, host, dev, step, Y4, idx, rr, M, N, rcfg, Kr, world, device)
     status = nv.nvfp4_device_status()
+
+    # ---- measurements outside the step (rank 0)
+    extras = {}
+    if rank == 0:
+        pk, _ = peaks()
+        fp4_peak = pk["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
+        flush = L2Flush(device)
+        if not args.no_per_config:
+            extras["per_config"] = {n: linear_sweep(n, device, flush, pk, fp4_peak)
+                                    for n in SWEEP_CONFIGS if n != args.config}
+        if not args.no_iteration:
+            extras["iteration"] = iteration_sweep(device, pk, fp4_peak)
+        if not args.no_peak_probe:
+            extras["cublas_nvfp4_8192"] = cublas_nvfp4_peak(device)
+        extras["evt_spread"] = evt_report(device)
+        extras["device_status_after_extras"] = nv.nvfp4_device_status()
     return report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk, world, rank,
-                  launches_per_step, per_tensor_ms)
+                  launches_per_step, per_tensor_ms, extras)
 
 
 def run_e2e(args, host, dev, step, Y4, idx, rr, M, N, rcfg, Kr, world, device):
@@ -379,8 +649,13 @@ def run_e2e(args, host, dev, step, Y4, idx, rr, M, N, rcfg, Kr, world, device):
     return max_over_ranks(e0.elapsed_time(e1), world, device), h2d, d2h
 
 
+def workload_name(cfg, rcfg):
+    return (f"{cfg.description}: M={cfg.M} K={cfg.K} N={cfg.N} + LoRA r=32 requant + "
+            f"{rcfg.P}x{rcfg.N} reward selection (K={rcfg.K})")
+
+
 def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk, world, rank,
-           launches_per_step, per_tensor_ms):
+           launches_per_step, per_tensor_ms, extras):
     if rank != 0:
         return None
     M, K, N = cfg.M, cfg.K, cfg.N
@@ -389,7 +664,7 @@ def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk
     pk, pk_kind = peaks()
     fp4_peak = pk["bf16_tflops"] * NOMINAL_FP4_OVER_BF16
     gemm_flops = 2.0 * M * N * K
-    ab = algorithmic_bytes(cfg, rcfg)
+    ab = algorithmic_bytes(cfg)
     tflops4 = gemm_flops / (per["nvfp4_gemm"] * 1e-3) / 1e12
     tflops16 = gemm_flops / (per["bf16_gemm"] * 1e-3) / 1e12
     rq_gbs = ab["nvfp4_requant"] / (per["nvfp4_requant"] * 1e-3) / 1e9
@@ -398,12 +673,15 @@ def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk
     e2e_ms_step = e2e_ms / args.steps
 
     # The captured traffic is of the full workload: a --rows run has none.
-    workload = WORKLOAD if not args.rows else f"{WORKLOAD}@{args.rows}"
+    workload = args.config if not args.rows else f"{args.config}@{args.rows}"
+    x_mb = M * K * 2 / 1e6
+    y_mb = M * N * 2 / 1e6
 
     def roof(bound, achieved, peak, unit, kernel):
         return {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
                 "frac": round(achieved / peak, 4), "traffic": dram_traffic(kernel, workload)}
 
+    cub = extras.get("cublas_nvfp4_8192") or {}
     out = {
         "metric": "NVFP4 GEMM TFLOP/s (FLUX.1-shaped linears) & re-quant GB/s, % of roofline",
         "value": round(tflops4 * world, 2),
@@ -416,12 +694,12 @@ def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "nvfp4 (e2m1 x e4m3 block scale) -> fp32 accumulate -> bf16",
-        "data": "synthetic (seeded; FLUX.1-shaped weights, activations, LoRA r=32, rewards)",
-        "config": {"workload": f"FLUX.1-shaped MLP up-projection M={M} K={K} N={N} + LoRA r=32 "
-                               "requant + 32x96 reward selection (K=24)",
+        "data": "synthetic (seeded; model-shaped weights, activations, LoRA r=32, rewards)",
+        "config": {"workload": workload_name(cfg, rcfg),
                    "M": M, "K": K, "N": N, "lora_rank": 32, "prompts": rcfg.P, "seeds": rcfg.N,
                    "selected": Kr, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (X 226 MB read, Y 906 MB written per step)"},
+                   "l2": f"inputs larger than L2 within a step (X {x_mb:.0f} MB read, Y {y_mb:.0f} MB "
+                         "written twice per step)"},
         "value_basis": "mean CUDA-event duration of the nvfp4_gemm launch inside the timed steps",
         "requant_gbs": round(rq_gbs, 1),
         "act_quant_gbs": round(aq_gbs, 1),
@@ -438,6 +716,8 @@ def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk
         },
         "peak_source": f"{pk_kind}: bf16 {pk['bf16_tflops']} TFLOP/s x {NOMINAL_FP4_OVER_BF16:g} "
                        f"(nominal dense NVFP4/BF16) for NVFP4; HBM {pk['hbm_gbs']} GB/s",
+        "nvfp4_vs_cublas_peak": None if not cub.get("tflops") else {
+            "cublas_8192_tflops": cub["tflops"], "frac": round(tflops4 / cub["tflops"], 4), "how": cub["how"]},
         "e2e": None if args.no_e2e else {
             "value": round(gemm_flops / (e2e_ms_step * 1e-3) / 1e12 * world, 2), "unit": "TFLOP/s",
             "ms_per_step": round(e2e_ms_step, 3), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
@@ -450,29 +730,56 @@ def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk
         "device_status": status,
         "clocks": clk,
     }
+    for k in ("per_config", "iteration", "evt_spread", "device_status_after_extras"):
+        if k in extras:
+            out[k] = extras[k]
     if world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(cfg, host, budget_s=args.cpu_budget)
+        out["cpu_baseline"] = cpu_baseline(cfg, host, rcfg, budget_s=args.cpu_budget)
     return out
 
 
 # ----------------------------------------------------------------------------- oracle legs
 
-def _oracle_inputs(cfg, host, rows):
-    import workloads
-    xb = workloads.bf16_bits(host["X"])[rows]
-    wb = workloads.bf16_bits(host["W"])
-    return xb, wb
+def _timed(fn):
+    t = time.perf_counter()
+    fn()
+    return time.perf_counter() - t
 
 
-def cpu_baseline(cfg, host, budget_s=12.0):
+def cpu_baseline(cfg, host, rcfg, budget_s=12.0):
     """The oracle, as it stands, on the host cores: NVFP4 GEMM over a row sample
-    sized to about `budget_s` seconds (the weights quantized by the oracle)."""
+    sized to about `budget_s` seconds (the weights quantized by the oracle), plus the
+    quantizers (all cores and one core) and the selection (one core)."""
     import numpy as np
     import oracle
     import workloads
     oracle.build()
+    cores = oracle.num_threads()
     wb = workloads.bf16_bits(host["W"])
-    wc, wsf, ws = oracle.requant(wb, host["A"].numpy(), host["B"].numpy(), workloads.LORA_ALPHA)
+    A, B = host["A"].numpy(), host["B"].numpy()
+    ab = algorithmic_bytes(cfg)
+    legs = {}
+    t_all = _timed(lambda: oracle.requant(wb, A, B, workloads.LORA_ALPHA))
+    oracle.set_num_threads(1)
+    try:
+        t_one = _timed(lambda: oracle.requant(wb, A, B, workloads.LORA_ALPHA))
+        xs = workloads.bf16_bits(host["X"][:2048])
+        aq_bytes = ab["nvfp4_act_quant"] * 2048 / cfg.M
+        t_aq1 = _timed(lambda: oracle.act_quant(xs))
+        rw = workloads.rewards(rcfg, 0).numpy()
+        t_sel = min(_timed(lambda: oracle.select_contrastive(rw, rcfg.K)) for _ in range(5))
+    finally:
+        oracle.set_num_threads(cores)
+    t_aqn = _timed(lambda: oracle.act_quant(xs))
+    legs["requant_gbs"] = {"all_cores": round(ab["nvfp4_requant"] / t_all / 1e9, 4),
+                           "one_core": round(ab["nvfp4_requant"] / t_one / 1e9, 4),
+                           "sample": f"full weight [{cfg.N}, {cfg.K}], LoRA r=32 merge + quantize"}
+    legs["act_quant_gbs"] = {"all_cores": round(aq_bytes / t_aqn / 1e9, 4),
+                             "one_core": round(aq_bytes / t_aq1 / 1e9, 4),
+                             "sample": f"2048 rows x K={cfg.K}"}
+    legs["select_us_one_core"] = round(t_sel * 1e6, 1)
+
+    wc, wsf, ws = oracle.requant(wb, A, B, workloads.LORA_ALPHA)
     rng = np.random.default_rng(0)
     probe = np.sort(rng.choice(cfg.M, 16, replace=False))
     ac, asf, a_s = oracle.act_quant(workloads.bf16_bits(host["X"])[probe])
@@ -486,28 +793,26 @@ def cpu_baseline(cfg, host, budget_s=12.0):
     oracle.gemm_nvfp4(ac, asf, a_s, wc, wsf, ws, workloads.bf16_bits(host["bias"]))
     dt = time.perf_counter() - t
     flops = 2.0 * nrows * cfg.N * cfg.K
-    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": cores,
             "kind": "oracle",
             "sample": f"fp64 NVFP4 GEMM oracle on {nrows} sampled rows x N={cfg.N} x K={cfg.K} "
-                      f"({dt:.1f} s), weights re-quantized by the oracle"}
+                      f"({dt:.1f} s), weights re-quantized by the oracle",
+            "legs": legs}
 
 
 def run_reference(args):
     """The oracle as the reference arm: each step is a bounded sample of the
     workload (requant of the full weight, act_quant + GEMM of 32 rows, selection)."""
     import numpy as np
-    import torch
     import oracle
     import workloads
     world, rank, _ = dist_setup()
     if rank != 0:
         return None
     oracle.build()
-    cfg = workloads.LINEARS[WORKLOAD]
+    cfg, host = host_inputs(args.config, rows=args.rows)
     rcfg = workloads.REWARDS[REWARD_CFG]
-    host = {"X": workloads.activations(cfg), "W": workloads.weight(cfg), "bias": workloads.bias(cfg),
-            "rewards": workloads.rewards(rcfg)}
-    host["A"], host["B"] = workloads.lora(cfg)
+    host["rewards"] = workloads.rewards(rcfg)
     wb = workloads.bf16_bits(host["W"])
     xb_all = workloads.bf16_bits(host["X"])
     bias = workloads.bf16_bits(host["bias"])
@@ -538,9 +843,8 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp64 over NVFP4 values (oracle)", "data": "synthetic (seeded)",
-        "config": {"workload": "FLUX.1-shaped MLP up-projection M=36864 K=3072 N=12288 + LoRA r=32 "
-                               "requant + 32x96 reward selection (K=24)",
-                   "parallelism": "replicas x1 (oracle on host cores)"},
+        "config": {"workload": workload_name(cfg, rcfg),
+                   "parallelism": f"oracle on host cores (rank 0 of {world})"},
         "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
                          "kind": "oracle",
                          "sample": f"per step: full-weight requant, act_quant + fp64 GEMM of "
@@ -549,19 +853,36 @@ def run_reference(args):
     }
 
 
-def main(argv=None):
+def parse_args(argv=None):
+    import workloads
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", choices=[HEADLINE, *SWEEP_CONFIGS], default=HEADLINE,
+                    help="the rollout linear of the timed step (default: the FLUX.1 up-projection)")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end phase")
+    ap.add_argument("--no-per-config", action="store_true", help="skip the SANA / SD3.5-L sweeps")
+    ap.add_argument("--no-iteration", action="store_true", help="skip the iteration-shaped batch")
+    ap.add_argument("--no-peak-probe", action="store_true", help="skip cuBLAS's NVFP4 8192^3 reference")
     ap.add_argument("--rows", type=int, default=None,
-                    help="override M (a smaller case for profiling; the default is the full 36864)")
+                    help="override M (a smaller case for profiling; the default is the config's)")
     args = ap.parse_args(argv)
+    assert args.config in workloads.LINEARS
     args.warmup = max(args.warmup, 3)  # at least 3 untimed warm-up steps
+    return args
+
+
+def main(argv=None):
+    argv = sys.argv[1:] if argv is None else list(argv)
+    args = parse_args(argv)
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        # no launcher: start the replicas here, one process per GPU, and pass on
+        # their exit status (rank 0 prints the line)
+        return subprocess.call(replica_command(args.gpus, argv))
     out = run_reference(args) if args.impl == "reference" else run_ours(args)
     if out is not None:
         print(json.dumps(out), flush=True)
@@ -569,7 +890,8 @@ def main(argv=None):
     if world > 1 and args.impl == "ours":
         import torch.distributed as dist
         dist.destroy_process_group()
+    return 0
 
 
 if __name__ == "__main__":
-    main()
+    sys.exit(main())

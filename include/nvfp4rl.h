@@ -301,6 +301,21 @@ nvfp4_status nvfp4_test_merge(const void* W, int w_dtype, const float* A, const 
  */
 nvfp4_status nvfp4_test_wait_timeout(int64_t timeout_ns, void* stream);
 
+/*
+ * nvfp4_gemm (no bias) with one K-stage (256 K-elements) of one CTA pair left
+ * unloaded on purpose: the pair's even CTA skips the copies of stage withhold_kb
+ * (0 <= withhold_kb < K / 256) on its first tile and never announces them, and every
+ * wait of the kernel is bounded by timeout_ns (1e6 .. 1e9) instead of the usual 4 s.
+ * The pair's MMA issuer, scale writers and epilogue must all give up, record
+ * NVFP4_ERR_TIMEOUT, let their own copies and MMAs land, free tensor memory and
+ * exit; Y is then incomplete.  Nothing is read or written out of bounds.  Exists to
+ * exercise the GEMM's abort path without faulting anything.
+ */
+nvfp4_status nvfp4_test_gemm_withhold(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_srow,
+                                      const uint8_t* w_codes, const uint8_t* w_sf, const float* w_st,
+                                      void* Y, int64_t M, int64_t N, int64_t K, int withhold_kb,
+                                      int64_t timeout_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

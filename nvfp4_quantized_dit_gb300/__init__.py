@@ -23,7 +23,7 @@ __all__ = [
     "nvfp4_act_quant_tensor", "nvfp4_gemm", "bf16_gemm", "select_contrastive",
     "nvfp4_device_status", "nvfp4_status_string", "nvfp4_version",
     "nvfp4_test_e2m1", "nvfp4_test_e4m3", "nvfp4_test_e2m1_quotient", "nvfp4_test_e4m3_quotient",
-    "nvfp4_test_e4m3_decode", "nvfp4_test_merge", "nvfp4_test_wait_timeout",
+    "nvfp4_test_e4m3_decode", "nvfp4_test_merge", "nvfp4_test_wait_timeout", "nvfp4_test_gemm_withhold",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnvfp4rl.so")
@@ -68,6 +68,7 @@ def library() -> ctypes.CDLL:
                 "nvfp4_test_e4m3_decode": [P, P, I64, P],
                 "nvfp4_test_merge": [P, I, P, P, I, F, I64, I64, P, P],
                 "nvfp4_test_wait_timeout": [I64, P],
+                "nvfp4_test_gemm_withhold": [P, P, P, P, P, P, P, I64, I64, I64, I, I64, P],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -319,3 +320,18 @@ def nvfp4_test_merge(W, A=None, B=None, alpha: float = 32.0, out=None, stream=No
 
 def nvfp4_test_wait_timeout(timeout_ns: int, stream=None) -> None:
     _call("nvfp4_test_wait_timeout", int(timeout_ns), _stream(stream))
+
+
+def nvfp4_test_gemm_withhold(a, w, withhold_kb: int, timeout_ns: int, out=None, stream=None):
+    """nvfp4_gemm with one K-stage of the first CTA pair never loaded (test hook of the
+    GEMM's abort path); returns the (incomplete) output."""
+    a_codes, a_sf, a_s = a
+    w_codes, w_sf, w_s = w
+    M, K = a_codes.shape[0], a_codes.shape[1] * 2
+    N = w_codes.shape[0]
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=a_codes.device) if out is None else out
+    _call("nvfp4_test_gemm_withhold", _dev(a_codes, "a_codes", torch.uint8), _dev(a_sf, "a_sf", torch.uint8),
+          _dev(a_s, "a_srow", torch.float32), _dev(w_codes, "w_codes", torch.uint8),
+          _dev(w_sf, "w_sf", torch.uint8), _dev(w_s, "w_st", torch.float32), _dev(out, "Y", torch.bfloat16),
+          M, N, K, int(withhold_kb), int(timeout_ns), _stream(stream))
+    return out

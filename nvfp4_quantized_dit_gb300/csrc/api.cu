@@ -271,9 +271,10 @@ nvfp4_status nvfp4_act_quant_tensor(const void* X, int64_t M, int64_t K, uint8_t
         launch_act_quant_tensor(ctx, static_cast<const __nv_bfloat16*>(X), M, K, codes, sf, s_t));
 }
 
-nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_srow,
-                        const uint8_t* w_codes, const uint8_t* w_sf, const float* w_st,
-                        const void* bias, void* Y, int64_t M, int64_t N, int64_t K, void* stream) {
+static nvfp4_status gemm_nvfp4_call(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_srow,
+                                    const uint8_t* w_codes, const uint8_t* w_sf, const float* w_st,
+                                    const void* bias, void* Y, int64_t M, int64_t N, int64_t K,
+                                    void* stream, int withhold_kb, int64_t wait_limit_ns) {
     if (M < 0 || N < 0 || M > kMaxRows || N > kMaxRows || K <= 0 || K % 64 != 0 ||
         K > (1 << 24) || N % 8 != 0)
         return NVFP4_ERR_SHAPE;
@@ -294,7 +295,25 @@ nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const float
         !encode_sf(&tsa, a_sf, M, K) || !encode_sf(&tsb, w_sf, N, K) || !encode_out(&ty, Y, M, N))
         return NVFP4_ERR_CUDA;
     return from_cuda(launch_gemm_nvfp4(ctx, ta, tb, tsa, tsb, ty, a_srow, w_st,
-                                       static_cast<const __nv_bfloat16*>(bias), M, N, K));
+                                       static_cast<const __nv_bfloat16*>(bias), M, N, K, withhold_kb,
+                                       wait_limit_ns));
+}
+
+nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_srow,
+                        const uint8_t* w_codes, const uint8_t* w_sf, const float* w_st,
+                        const void* bias, void* Y, int64_t M, int64_t N, int64_t K, void* stream) {
+    return gemm_nvfp4_call(a_codes, a_sf, a_srow, w_codes, w_sf, w_st, bias, Y, M, N, K, stream, -1, 0);
+}
+
+nvfp4_status nvfp4_test_gemm_withhold(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_srow,
+                                      const uint8_t* w_codes, const uint8_t* w_sf, const float* w_st,
+                                      void* Y, int64_t M, int64_t N, int64_t K, int withhold_kb,
+                                      int64_t timeout_ns, void* stream) {
+    if (withhold_kb < 0 || (int64_t)withhold_kb * 256 >= K || timeout_ns < 1000000 ||
+        timeout_ns > 1000000000LL)
+        return NVFP4_ERR_SHAPE;
+    return gemm_nvfp4_call(a_codes, a_sf, a_srow, w_codes, w_sf, w_st, nullptr, Y, M, N, K, stream,
+                           withhold_kb, timeout_ns);
 }
 
 nvfp4_status bf16_gemm(const void* X, const void* W, const void* bias, void* Y, int64_t M,

@@ -138,7 +138,8 @@ cudaError_t launch_gemm_nvfp4(const LaunchCtx&, const CUtensorMap& tmap_a,
                               const CUtensorMap& tmap_b, const CUtensorMap& tmap_sfa,
                               const CUtensorMap& tmap_sfb, const CUtensorMap& tmap_y,
                               const float* a_srow, const float* w_st, const __nv_bfloat16* bias,
-                              int64_t M, int64_t N, int64_t K);
+                              int64_t M, int64_t N, int64_t K, int withhold_kb = -1,
+                              int64_t wait_limit_ns = 0);
 cudaError_t launch_gemm_bf16(const LaunchCtx&, const CUtensorMap& tmap_a,
                              const CUtensorMap& tmap_b, const CUtensorMap& tmap_y,
                              const __nv_bfloat16* bias, int64_t M, int64_t N, int64_t K);

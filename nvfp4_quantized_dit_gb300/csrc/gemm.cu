@@ -123,6 +123,9 @@ struct GemmArgs {
     const __nv_bfloat16* bias;
     int M, N, K;
     int* status;
+    uint64_t wait_limit_ns;  // bound of every wait (kWaitLimitNs; shorter in the test hook)
+    int withhold_kb;         // test hook only: K-stage whose loads the first pair's even CTA
+                             // never issues (on its first tile), or -1
 };
 
 // Pair tiles, grouped for L2 reuse: tiles are ordered in bands of kBandMp m-pairs
@@ -235,9 +238,20 @@ __global__ void __launch_bounds__(Cfg<kFP4>::kThreads, 1)
                 const int m_blk = mp * kPair + (int)rank;
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, args.status, abort_flag,
-                                   kWaitLimitNs)) {
+                                   args.wait_limit_ns)) {
                         ok = false;
                         break;
+                    }
+                    if (kb == args.withhold_kb && leader && t == (int)(blockIdx.x / kPair) &&
+                        blockIdx.x < kPair) {
+                        // Test hook: this stage's copies are never issued (nor announced), so
+                        // the pair's MMA issuer, scale writers and epilogue all run into their
+                        // bounded waits.  Nothing is read or written out of place.
+                        if (++stage == S) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
                     }
                     const uint32_t bar = full_even + 8u * (uint32_t)stage;
                     uint8_t* sa = smem + stage * C::kStageBytes;
@@ -269,7 +283,7 @@ __global__ void __launch_bounds__(Cfg<kFP4>::kThreads, 1)
                 // release from the pair's MMAs is still in flight towards this CTA at exit.
                 for (int i = 0; i < S; ++i) {
                     if (!mbar_wait(&empty[stage], phase ^ 1u, args.status, abort_flag,
-                                   kWaitLimitNs))
+                                   args.wait_limit_ns))
                         break;
                     if (++stage == S) {
                         stage = 0;
@@ -299,15 +313,15 @@ __global__ void __launch_bounds__(Cfg<kFP4>::kThreads, 1)
             for (int t = sch.first; ok && t < sch.total; t += sch.step) {
                 // The accumulator must have been drained by the epilogue of both CTAs.
                 if (!mbar_wait<true>(tmem_empty, acc_phase ^ 1u, args.status, abort_flag,
-                                     kWaitLimitNs)) {
+                                     args.wait_limit_ns)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
                 for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&full[stage], phase, args.status, abort_flag, kWaitLimitNs) ||
+                    if (!mbar_wait(&full[stage], phase, args.status, abort_flag, args.wait_limit_ns) ||
                         (kFP4 && !mbar_wait<true>(&sfready[stage], phase, args.status, abort_flag,
-                                                  kWaitLimitNs))) {
+                                                  args.wait_limit_ns))) {
                         ok = false;
                         break;
                     }
@@ -361,7 +375,7 @@ __global__ void __launch_bounds__(Cfg<kFP4>::kThreads, 1)
         for (int t = sch.first; t < sch.total; t += sch.step) {
             bool ok = true;
             for (int kb = 0; kb < num_kb; ++kb) {
-                ok = mbar_wait(&sf_full[stage], phase, args.status, abort_flag, kWaitLimitNs);
+                ok = mbar_wait(&sf_full[stage], phase, args.status, abort_flag, args.wait_limit_ns);
                 ok = __all_sync(0xFFFFFFFFu, ok);  // tcgen05.st is .sync.aligned
                 if (!ok) break;
                 const uint8_t* sfa = smem + stage * C::kStageBytes + kATileBytes + kBHalfBytes;
@@ -429,7 +443,7 @@ __global__ void __launch_bounds__(Cfg<kFP4>::kThreads, 1)
                 *reinterpret_cast<uint2*>(sbias + lane * 8) = b2;
             }
             __syncwarp();
-            bool ok = mbar_wait(tmem_full, acc_phase, args.status, abort_flag, kWaitLimitNs);
+            bool ok = mbar_wait(tmem_full, acc_phase, args.status, abort_flag, args.wait_limit_ns);
             // tcgen05.ld is .sync.aligned: reconverge the warp and agree on the outcome.
             ok = __all_sync(0xFFFFFFFFu, ok);
             if (!ok) break;
@@ -549,15 +563,17 @@ cudaError_t launch_gemm_nvfp4(const LaunchCtx& ctx, const CUtensorMap& tmap_a,
                               const CUtensorMap& tmap_b, const CUtensorMap& tmap_sfa,
                               const CUtensorMap& tmap_sfb, const CUtensorMap& tmap_y,
                               const float* a_srow, const float* w_st, const __nv_bfloat16* bias,
-                              int64_t M, int64_t N, int64_t K) {
-    GemmArgs a{a_srow, w_st, bias, (int)M, (int)N, (int)K, ctx.status};
+                              int64_t M, int64_t N, int64_t K, int withhold_kb,
+                              int64_t wait_limit_ns) {
+    GemmArgs a{a_srow, w_st, bias, (int)M, (int)N, (int)K, ctx.status,
+               wait_limit_ns > 0 ? (uint64_t)wait_limit_ns : kWaitLimitNs, withhold_kb};
     return run_gemm<true>(ctx, tmap_a, tmap_b, tmap_sfa, tmap_sfb, tmap_y, a);
 }
 
 cudaError_t launch_gemm_bf16(const LaunchCtx& ctx, const CUtensorMap& tmap_a,
                              const CUtensorMap& tmap_b, const CUtensorMap& tmap_y,
                              const __nv_bfloat16* bias, int64_t M, int64_t N, int64_t K) {
-    GemmArgs a{nullptr, nullptr, bias, (int)M, (int)N, (int)K, ctx.status};
+    GemmArgs a{nullptr, nullptr, bias, (int)M, (int)N, (int)K, ctx.status, kWaitLimitNs, -1};
     return run_gemm<false>(ctx, tmap_a, tmap_b, tmap_a, tmap_b, tmap_y, a);
 }
 

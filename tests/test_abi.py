@@ -159,3 +159,33 @@ def test_binding_refuses_cpu_tensors(lib):
                             codes=torch.zeros(4, 32, dtype=torch.uint8),
                             sf=torch.zeros(pkg.sf_bytes(4, 64), dtype=torch.uint8),
                             s_row=torch.zeros(4))
+
+
+def test_requant_noalloc_checks_arguments_before_anything_else(lib):
+    """nvfp4_requant_noalloc runs nvfp4_requant's argument checks first (before its
+    size limit, the device's architecture and the scratch lookup)."""
+    P, F = ctypes.c_void_p, ctypes.c_float
+    f = lib.nvfp4_requant_noalloc
+    # misaligned codes on a shape whose workspace would also exceed the scratch
+    assert f(P(A16), 0, P(A16), P(A16), 32, F(32.0), 64, 65536, P(BAD), P(A16), P(A16), None) == 3
+    assert f(P(A16), 0, P(A16), P(A16), 32, F(32.0), 64, 65536, P(A16), P(A16), None, None) == 1
+    assert f(P(A16), 7, P(A16), P(A16), 32, F(32.0), 64, 128, P(A16), P(A16), P(A16), None) == 2
+    # the same codes as nvfp4_requant for the same bad arguments
+    g = lib.nvfp4_requant
+    for args in [(P(A16), 0, P(A16), P(A16), 32, F(32.0), 64, 100, P(A16), P(A16), P(A16)),
+                 (P(A16), 0, P(BAD), P(A16), 32, F(32.0), 64, 128, P(A16), P(A16), P(A16)),
+                 (None, 0, P(A16), P(A16), 32, F(32.0), 64, 128, P(A16), P(A16), P(A16))]:
+        assert f(*args, None) == g(*args, None, 0, None)
+
+
+def test_gemm_withhold_hook_validation(lib):
+    P = ctypes.c_void_p
+    f = lib.nvfp4_test_gemm_withhold
+    ok = [P(A16)] * 7
+    assert f(*ok, 256, 256, 512, 2, 50_000_000, None) == 2   # stage 2 of a 2-stage K
+    assert f(*ok, 256, 256, 512, -1, 50_000_000, None) == 2
+    assert f(*ok, 256, 256, 512, 1, 10, None) == 2           # limit below 1 ms
+    assert f(*ok, 256, 256, 100, 0, 50_000_000, None) == 2   # K % 64
+    bad = list(ok)
+    bad[6] = P(BAD)
+    assert f(*bad, 256, 256, 512, 1, 50_000_000, None) == 3

@@ -36,8 +36,7 @@ def test_source_hash_changes_with_the_sources(tmp_path):
 
 def test_algorithmic_bytes_flux():
     cfg = workloads.LINEARS["flux_up"]
-    rcfg = workloads.REWARDS[bench.REWARD_CFG]
-    ab = bench.algorithmic_bytes(cfg, rcfg)
+    ab = bench.algorithmic_bytes(cfg)
     M, K, N = cfg.M, cfg.K, cfg.N
     sf_w = (N + 127) // 128 * 128 * (K // 16)
     sf_a = (M + 127) // 128 * 128 * (K // 16)
@@ -52,9 +51,8 @@ def test_algorithmic_bytes_flux():
 
 def test_algorithmic_bytes_scale_with_rows():
     cfg = workloads.LINEARS["flux_up"]
-    rcfg = workloads.REWARDS[bench.REWARD_CFG]
     small = dataclasses.replace(cfg, M=8192)
-    a, b = bench.algorithmic_bytes(cfg, rcfg), bench.algorithmic_bytes(small, rcfg)
+    a, b = bench.algorithmic_bytes(cfg), bench.algorithmic_bytes(small)
     assert a["nvfp4_requant"] == b["nvfp4_requant"]  # independent of the activations
     assert a["nvfp4_act_quant"] > 4 * b["nvfp4_act_quant"]
 
@@ -81,13 +79,14 @@ def test_report_line_has_the_contract_keys():
     import argparse
     cfg = workloads.LINEARS["flux_up"]
     rcfg = workloads.REWARDS[bench.REWARD_CFG]
-    args = argparse.Namespace(steps=10, warmup=3, rows=None, no_e2e=False, no_cpu_baseline=True)
+    args = argparse.Namespace(steps=10, warmup=3, rows=None, no_e2e=False, no_cpu_baseline=True,
+                              config="flux_up")
     per = {"nvfp4_requant": 0.1, "nvfp4_act_quant": 0.08, "nvfp4_gemm": 0.5, "bf16_gemm": 1.5,
            "select_contrastive": 0.016}
     clk = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "samples": 5, "reasons": []}
     out = bench.report(args, cfg, rcfg, None, per, 22.0, 50.0, 304, 906, 0, clk, 1, 0,
                        {"nvfp4_requant": 3, "nvfp4_act_quant": 1, "nvfp4_gemm": 1, "bf16_gemm": 1,
-                        "select_contrastive": 2}, 0.12)
+                        "select_contrastive": 2}, 0.12, {})
     for k in ["metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
               "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches",
               "clocks"]:
@@ -101,5 +100,18 @@ def test_report_line_has_the_contract_keys():
     assert out["e2e"]["h2d_bytes_per_step"] == 304 and out["e2e"]["ms_per_step"] == 5.0
     assert out["variants"]["act_quant_per_tensor"]["ms"] == 0.12
     small = argparse.Namespace(**{**vars(args), "rows": 8192})
-    out2 = bench.report(small, cfg, rcfg, None, per, 22.0, 50.0, 304, 906, 0, clk, 1, 0, {}, 0.12)
+    out2 = bench.report(small, cfg, rcfg, None, per, 22.0, 50.0, 304, 906, 0, clk, 1, 0, {}, 0.12, {})
     assert all(r["traffic"] is None for r in out2["rooflines"].values())  # no capture of that workload
+
+
+def test_parse_args_defaults_and_config():
+    a = bench.parse_args([])
+    assert (a.gpus, a.config, a.impl) == (1, "flux_up", "ours") and a.warmup >= 3
+    assert bench.parse_args(["--config", "sd35_qkv", "--warmup", "1"]).warmup == 3
+
+
+def test_replica_command_is_a_local_torchrun():
+    cmd = bench.replica_command(4, ["--gpus", "4", "--steps", "5"])
+    assert cmd[1:4] == ["-m", "torch.distributed.run", "--nnodes=1"]
+    assert "--nproc-per-node=4" in cmd and cmd[cmd.index("--master-addr") + 1] == "127.0.0.1"
+    assert cmd[-3:] == ["--gpus", "4", "--steps", "5"][-3:] and cmd[-5].endswith("bench.py")

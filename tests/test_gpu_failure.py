@@ -27,3 +27,44 @@ def test_bounded_wait_reports_timeout_and_context_survives():
     ref = (X.float() @ W.float().T)
     assert torch.allclose(y.float(), ref, rtol=2e-2, atol=2e-2)
     assert nv.nvfp4_device_status(clear=False) == 0
+
+
+def test_gemm_abort_path_frees_everything_and_the_next_call_is_clean(orc):
+    """The NVFP4 GEMM's own abort path: the first CTA pair's even CTA never loads one
+    K-stage (test hook), so its MMA issuer, scale writers and epilogue, and the odd
+    CTA's roles, all run into their bounded waits (50 ms here).  The status must read
+    NVFP4_ERR_TIMEOUT; afterwards the same GEMM, and a larger one that uses every SM
+    (each allocates tensor memory again), must match the oracle with a clean status."""
+    require_gpu()
+    import numpy as np
+
+    import workloads
+    from gpu_util import assert_gemm_close, np_, swizzle_sf
+
+    def operand(rows, K, seed, stream):
+        c, sf, s = [t.numpy() for t in workloads.random_nvfp4_operand(rows, K, seed, stream)]
+        return c, sf, s
+
+    def gpu(c, sf, s, K):
+        return (torch.from_numpy(c).cuda(), torch.from_numpy(swizzle_sf(sf, K)).cuda(),
+                torch.from_numpy(np.ascontiguousarray(s, np.float32)).cuda())
+
+    assert nv.nvfp4_device_status(clear=True) in (0, 6)
+    M, N, K = 256, 256, 1024
+    ac, asf, a_s = operand(M, K, 21, 0)
+    wc, wsf, w_s = operand(N, K, 22, 1)
+    a, w = gpu(ac, asf, a_s, K), gpu(wc, wsf, w_s[:1], K)
+    nv.nvfp4_test_gemm_withhold(a, w, withhold_kb=1, timeout_ns=50_000_000)
+    assert nv.nvfp4_device_status(clear=True) == 6
+    y = nv.nvfp4_gemm(a, w)
+    assert nv.nvfp4_device_status(clear=True) == 0
+    y_ref, S = orc.gemm_nvfp4(ac, asf, a_s, wc, wsf, w_s[:1])
+    assert_gemm_close(np_(y), y_ref, S, "after abort")
+    M2, N2 = 8192, 4096
+    ac2, asf2, a_s2 = operand(M2, K, 23, 0)
+    wc2, wsf2, w_s2 = operand(N2, K, 24, 1)
+    y2 = nv.nvfp4_gemm(gpu(ac2, asf2, a_s2, K), gpu(wc2, wsf2, w_s2[:1], K))
+    assert nv.nvfp4_device_status(clear=True) == 0
+    rows = np.concatenate([np.arange(0, 8192, 61), np.arange(M2 - 8, M2)])
+    y_ref2, S2 = orc.gemm_nvfp4(ac2, asf2, a_s2, wc2, wsf2, w_s2[:1], rows=rows)
+    assert_gemm_close(np_(y2)[rows], y_ref2, S2, "every SM after abort")

@@ -54,3 +54,23 @@ def test_single_rank_is_identity():
     import bench
     assert bench.max_over_ranks(2.25, 1) == 2.25
     bench.barrier(1)
+
+
+def test_bench_starts_its_own_replicas(tmp_path):
+    """`bench.py --gpus 2` with no launcher starts two local ranks itself (torchrun);
+    exactly one line comes out (rank 0), and it reports both ranks.  The reference arm
+    is used: it needs no GPU (rank 0 times the oracle, rank 1 exits without work)."""
+    import json
+    import subprocess
+    import sys
+
+    import bench
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    p = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--steps", "1", "--warmup", "3", "--config", "sana", "--rows", "256"],
+                       capture_output=True, text=True, timeout=600, env=env, cwd=str(tmp_path))
+    assert p.returncode == 0, p.stderr[-2000:]
+    lines = [ln for ln in p.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, p.stdout
+    out = json.loads(lines[0])
+    assert out["impl"] == "reference" and out["n_gpus"] == 2

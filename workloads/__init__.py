@@ -173,3 +173,18 @@ def bf16_bits(t: torch.Tensor):
     import numpy as np
     assert t.dtype == torch.bfloat16
     return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def activations_on_device(cfg: LinearConfig, device, seed: int = 0, rows: int | None = None) -> torch.Tensor:
+    """Activations with the recipe of activations() (N(0, 1), the config's outlier
+    channels scaled) drawn by a seeded generator on `device` instead of the CPU: for
+    timing runs at sizes where drawing on the host would take long.  The values differ
+    from activations(cfg, seed); nothing compares them with the oracle."""
+    M = cfg.M if rows is None else rows
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed) * 1_000_003 + 5)
+    x = torch.randn(M, cfg.K, generator=g, dtype=torch.float32, device=device)
+    if cfg.x_outlier_frac > 0:
+        ch = _outlier_channels(cfg.K, cfg.x_outlier_frac, _gen(seed, 6)).to(device)
+        x[:, ch] *= cfg.x_outlier_gain
+    return x.to(torch.bfloat16)
