@@ -490,8 +490,8 @@ def run_ours(args):
     ws_bytes = nv.requant_workspace_bytes(nv.W_BF16, 32, N, K)
     rq_ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=device)
     names = ["nvfp4_requant", "nvfp4_act_quant", "nvfp4_gemm", "bf16_gemm", "select_contrastive"]
-    # requant: split kernel, amax pass, quantize pass (tensor-core merge)
-    launches_per_step = {"nvfp4_requant": 3, "nvfp4_act_quant": 1, "nvfp4_gemm": 1, "bf16_gemm": 1,
+    # requant: split kernel, then the fused amax + quantize kernel (tensor-core merge)
+    launches_per_step = {"nvfp4_requant": 2, "nvfp4_act_quant": 1, "nvfp4_gemm": 1, "bf16_gemm": 1,
                          "select_contrastive": 2}
 
     def step(d, events=None, y4=Y4, sel=(idx, rr)):

@@ -124,9 +124,11 @@ static inline size_t nvfp4_sf_offset(int64_t row, int64_t kblk, int64_t K) {
  * elements whose |W| a Cauchy-Schwarz bound on the LoRA term leaves in reach of the
  * maximum are merged), merge + quantize (every element merged once), and a
  * one-thread finalize of s_t.  Tensor-core path: a kernel that splits A and B into
- * bf16 pairs (into the workspace), a memset, the merge as a bf16 GEMM with every
- * decision certified against a rigorous bound or recomputed by the fp32 chain
- * (amax pass, quantize pass), and the finalize.  Inputs must be finite.
+ * bf16 pairs (into the workspace), then one persistent kernel with the merge as a
+ * bf16 GEMM and every decision certified against a rigorous bound or recomputed by
+ * the fp32 chain: an amax phase over W, a grid-wide barrier (every CTA resident; a
+ * bounded wait), a quantize phase over W again (from L2), and the finalize.  Inputs
+ * must be finite.
  */
 nvfp4_status nvfp4_requant(const void* W, int w_dtype, const float* A, const float* B, int r,
                            float alpha, int64_t N, int64_t K, uint8_t* codes, uint8_t* sf,

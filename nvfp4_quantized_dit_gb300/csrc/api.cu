@@ -200,11 +200,9 @@ nvfp4_status nvfp4_requant(const void* W, int w_dtype, const float* A, const flo
         RequantTcMaps m;
         if (!encode_2d(&m.w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, W, (uint64_t)K, (uint64_t)N,
                        (uint64_t)K * 2, 64, 128) ||
-            !encode_2d(&m.ap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.ap, 128, (uint64_t)K, 256, 64, 64) ||
-            !encode_2d(&m.af, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, A, (uint64_t)K, (uint64_t)r,
-                       (uint64_t)K * 4, 128, 32, CU_TENSOR_MAP_SWIZZLE_NONE))
+            !encode_2d(&m.ap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, ws.ap, 128, (uint64_t)K, 256, 64, 64))
             return NVFP4_ERR_CUDA;
-        return from_cuda(launch_requant_tc(ctx, m, A, B, workspace, c, N, K, codes, sf, s_t));
+        return from_cuda(launch_requant_tc(ctx, m, W, A, B, workspace, c, N, K, codes, sf, s_t));
     }
     return from_cuda(launch_requant(ctx, W, w_dtype, merge ? A : nullptr, merge ? B : nullptr,
                                     merge ? r : 0, c, N, K, codes, sf, s_t));

@@ -89,7 +89,8 @@ cudaError_t launch_requant(const LaunchCtx&, const void* W, int w_dtype, const f
 // Tensor-core merge (merge_tc.cu): bf16 W, rank 32, 16-byte aligned A and B, and a
 // workspace of requant_tc_workspace_bytes (0 when the path does not apply) laid out by
 // requant_tc_layout: A' [K, 128] bf16, rnorm [N rounded up to 256], cnorm [K / 128
-// rounded up][4], a CTA counter (finishing the per-tensor scale).
+// rounded up][4], two CTA counters (the grid barrier between the amax and quantize
+// phases; the last CTA, which finishes the per-tensor scale).
 struct RequantTcLayout {
     uint8_t* ap;
     float* rnorm;
@@ -113,15 +114,15 @@ inline RequantTcLayout requant_tc_layout(void* base, int64_t N, int64_t K) {
     l.bytes = off;
     return l;
 }
-// Tensor maps of the merge kernels: W [N, K] bf16 (64 x 128 boxes) and A' [K, 128] bf16
-// (64 x 64 boxes), both with the 128-byte swizzle; A [32, K] fp32 (128 x 32 boxes).
+// Tensor maps of the merge kernel: W [N, K] bf16 (64 x 128 boxes) and A' [K, 128] bf16
+// (64 x 64 boxes), both with the 128-byte swizzle.
 struct RequantTcMaps {
-    CUtensorMap w, ap, af;
+    CUtensorMap w, ap;
 };
 size_t requant_tc_workspace_bytes(int w_dtype, int r, int64_t N, int64_t K);
-cudaError_t launch_requant_tc(const LaunchCtx&, const RequantTcMaps& maps, const float* A,
-                              const float* B, void* workspace, float c, int64_t N, int64_t K,
-                              uint8_t* codes, uint8_t* sf, float* s_t);
+cudaError_t launch_requant_tc(const LaunchCtx&, const RequantTcMaps& maps, const void* W,
+                              const float* A, const float* B, void* workspace, float c, int64_t N,
+                              int64_t K, uint8_t* codes, uint8_t* sf, float* s_t);
 cudaError_t launch_test_merge(const LaunchCtx&, const void* W, int w_dtype, const float* A,
                               const float* B, int r, float c, int64_t N, int64_t K, float* out);
 cudaError_t launch_select(const LaunchCtx&, const float* rewards, int P, int N, int K,
@@ -364,11 +365,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return done != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep in the instruction until the phase
+// completes or about kSuspendNs have passed (the hint bounds the sleep; completion
+// wakes it), instead of spinning and taking issue slots from the warps that work.
+constexpr uint32_t kSuspendNs = 20000;
+template <bool kCluster = false>
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    if (kCluster)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity), "r"(kSuspendNs)
+            : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done)
+            : "r"(bar), "r"(parity), "r"(kSuspendNs)
+            : "memory");
+    return done != 0;
+}
+
 // Waits for the phase of `bar` with the given parity to complete, for at most
 // limit_ns of device time.  On expiry it records NVFP4_ERR_TIMEOUT in *status,
 // raises the CTA's abort flag (so the CTA's other waits give up at once) and
 // returns false.  It also returns false as soon as another thread of the CTA
-// has raised the abort flag.  An iteration cap backs up the clock.
+// has raised the abort flag (checked at least every kSuspendNs).  An iteration cap
+// backs up the clock.
 template <bool kCluster = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* status,
                                           volatile int* abort_flag, uint64_t limit_ns) {
@@ -376,11 +404,9 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
     if (mbar_try_wait<kCluster>(a, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 1; it < (1u << 30); ++it) {
-        if (mbar_try_wait<kCluster>(a, parity)) return true;
-        if ((it & 31u) == 0u) {
-            if (*abort_flag) return false;
-            if (globaltimer_ns() - t0 > limit_ns) break;
-        }
+        if (mbar_try_wait_sleep<kCluster>(a, parity)) return true;
+        if (*abort_flag) return false;
+        if (globaltimer_ns() - t0 > limit_ns) break;
     }
     atomicCAS(status, 0, (int)NVFP4_ERR_TIMEOUT);
     *abort_flag = 1;
@@ -396,6 +422,36 @@ __device__ __forceinline__ void tma_load_2d(const CUtensorMap* map, uint64_t* ba
         " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
         : "memory");
+}
+
+// L2 eviction policies for TMA loads: evict_last keeps a tile in L2 for a second read
+// soon after (a later pass over the same data), evict_first lets a last read go.
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// tma_load_2d with an L2 cache policy (from l2_policy_*).
+__device__ __forceinline__ void tma_load_2d_hint(const CUtensorMap* map, uint64_t* bar, void* dst,
+                                                 int32_t x, int32_t y, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+        : "memory");
+}
+
+// Loads with acquire semantics at GPU scope (a flag or counter written by other CTAs).
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const unsigned int* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
 }
 
 // --- CTA pairs (two CTAs of a cluster sharing one 2-CTA MMA)
@@ -557,6 +613,16 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
             "r"(smem_u32(dst)),
         "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// bulk_load with an L2 cache policy (from l2_policy_*).
+__device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                               uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 

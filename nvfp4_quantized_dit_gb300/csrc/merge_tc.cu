@@ -24,27 +24,35 @@
 // a flushed split part (below 2^-126) loses at most 2^-124 sum_j |a_j| <= 2^-121.5 a
 // (or b), flushed products and partial sums at most 128 x 2^-126.  The chain's own
 // subnormal roundings are far below 2^-117.  Every decision is taken on the interval
-// [|w~| - E, |w~| + E] (with the final fma's own rounding covered by 2^-19 / 2^-21
-// nudges of the reciprocals and factors):
-//   * tensor amax (pass 1): a warp's maximum is among its elements whose upper bound
-//     reaches the largest lower bound of the warp; those are recomputed with the exact
-//     chain and the warp's maximum of them goes to the tensor amax;
-//   * block scale (pass 2): the E4M3 codes of both ends of [bam - E, bam + E] must agree,
-//     else the block's 16 values are recomputed exactly;
-//   * element code (pass 2): the E2M1 codes of both ends must agree (an interval that
-//     holds zero gives codes of both signs and never agrees), else that element alone
-//     is recomputed.
+// [w~ - E, w~ + E], widened for the final fma's own rounding:
+//   * tensor amax (amax phase, no MMA): with Ecs = |c| ||B[n,:]|| max ||A[:,k]|| (Cauchy-
+//     Schwarz, plus the roundings) every |w'| lies within Ecs of |W|; a warp's maximum is
+//     among its elements whose |W| + Ecs reaches the largest |W| - Ecs of the warp (or the
+//     running tensor amax); those few are merged exactly and the warp's maximum of them
+//     goes to the tensor amax;
+//   * block scale (quantize phase): the E4M3 codes of both ends of [bam - E, bam + E]
+//     must agree, else the block's 16 values are recomputed exactly;
+//   * element code (quantize phase): with r ~ 1/den, the two ends x r -+ dl of an
+//     interval that holds w'/den (dl per block, from E, the block's largest magnitude
+//     and the reciprocal's error) must give the same E2M1 code, else that element alone
+//     is recomputed (an interval that holds zero gives codes of both signs and never
+//     agrees).
 // So codes, scales and s_t are bit-identical to the fp32 chain's.  The exact chain
-// reads the fp32 factors from shared memory.
+// reads the fp32 factors and W from global memory (L2).
 //
 // Kernels.  A split kernel writes A' = [a0 a1 a0 a1] per column of A (bf16, 256 bytes
 // per row) into the caller's workspace, with upper bounds of every row norm of B and,
-// per 64 columns, of the largest column norm of A.  Then both passes run as persistent
-// clusters of two CTAs; a pair tile is 256 weight rows (128 per CTA) x 128 columns,
-// walked k-strip first, so the rows of B usually stay the same from one tile to the
-// next.  Per CTA, 20 warps:
-//   warp 0      TMA: W tiles (128 x 128 bf16; 4 slots) and the fp32 strip of A for the
-//               exact chain (3 slots), each freed when the epilogue is done with the tile;
+// per 64 columns, of the largest column norm of A.  Then one persistent kernel on
+// clusters of two CTAs (one per SM, every CTA resident) runs both phases over the same
+// tiles: the amax phase reads W from HBM, keeping it in L2; a grid-wide barrier (a
+// counter in the workspace, bounded wait) gathers every CTA's contribution to the
+// tensor amax; the quantize phase walks the tiles in reverse order, reading W back from
+// L2.  Only the epilogue waits at the barrier: the copies and MMAs of the first
+// quantize-phase tiles run ahead.  A pair tile is 256 weight rows (128 per CTA) x 128
+// columns, walked k-strip first, so the rows of B usually stay the same from one tile
+// to the next.  Per CTA, 20 warps:
+//   warp 0      TMA: W tiles (128 x 128 bf16; 5 slots), each freed when the epilogue is
+//               done with the tile;
 //   warp 1      tensor-memory allocation; lane 0 of the even CTA issues the 8 pair MMAs
 //               (kind::f16, M = 256, N = 128, A from tensor memory) into a
 //               double-buffered accumulator;
@@ -52,14 +60,17 @@
 //               completing on the even CTA's barrier, freed by the MMAs;
 //   warp 3      idle;
 //   warps 4-19  epilogue: four warps per tensor-memory lane quarter, 32 columns each (a
-//               thread owns one weight row): accumulator + W -> w~ -> pass 1 amax or
-//               pass 2 codes and scales, stored straight to global memory.
+//               thread owns one weight row): W (amax phase) or accumulator + W -> w~
+//               (quantize phase) -> the amax bound or codes and scales, stored straight
+//               to global memory.
 // The rows of B live in tensor memory next to the accumulators (lane = row), in two
-// buffers for consecutive row blocks: [b0 b0 b1 b1] as bf16 pairs (the MMA's A
-// operand) and the fp32 values (for the exact chain).  The epilogue warps write the
-// next row block's buffer one tile ahead; only the rare uncertain elements read the
-// fp32 rows and the strip of A.
-// Every mbarrier wait is bounded (mbar_wait).
+// buffers for consecutive row blocks, as [b0 b0 b1 b1] bf16 pairs (the MMA's A
+// operand); the epilogue warps write the next row block's buffer one tile ahead.  The
+// rare undecided elements of the quantize phase are queued (two tiles per thread, in
+// shared memory) and merged exactly after the last tile, so that the exact chain's
+// latency stays out of the pair's tile pipeline; their provisional codes are then
+// overwritten.
+// Every wait, the grid barrier's included, is bounded (mbar_wait).
 #include "common.cuh"
 
 namespace nvfp4rl {
@@ -73,23 +84,28 @@ constexpr int kJp = 4 * kRank;  // K' of the merge GEMM
 constexpr int kEpiWarp0 = 4, kEpiWarps = 16;  // warp groups: 0 control, 1-4 epilogue
 constexpr int kCols = 32;       // columns per epilogue warp
 constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
-constexpr int kWSlots = 4, kXSlots = 3, kOpSlots = 3;
+constexpr int kWSlots = 5, kOpSlots = 3;
 constexpr uint32_t kOpBBytes = (kTK / kPair) * kJp * 2;  // 16 KB: A' rows, two 64-column atoms
 constexpr uint32_t kWBox = kTM * 128;                    // 16 KB: 128 rows x 64 bf16
 constexpr uint32_t kWBytes = 2 * kWBox;                  // 32 KB: 128 rows x 128 bf16
-constexpr uint32_t kAfBytes = kRank * kTK * 4;           // 16 KB: fp32 strip of A
 constexpr uint32_t kMiscBytes = 512;
+constexpr int kDefer = 512;  // deferred (thread, tile) entries per CTA, exact work after the tile loop
+constexpr uint32_t kDeferBytes = kDefer * 16;  // (tile, element mask, row | chunk | flags, task base)
+constexpr int kTasks = 1024;  // exact values computed for the deferred entries (one per element)
+constexpr uint32_t kTaskBytes = kTasks * (2 + 4);  // task (entry << 5 | column) and its exact value
+// Per W slot, the tile's bounds: the 128 row norms of this CTA's rows of B and the 4
+// column-norm entries of the tile's 128-column strip (bulk copies beside the W tile).
+constexpr uint32_t kSideBytes = kTM * 4 + 16;
 constexpr uint32_t kSmemBytes =
-    1024 + kOpSlots * kOpBBytes + kWSlots * kWBytes + kXSlots * kAfBytes + kMiscBytes;
-// Tensor memory: two accumulators of 128 columns, then two row buffers of 96 columns:
-// 64 columns of [b0 b0 b1 b1] (bf16 pairs) and 32 columns of fp32 B.
+    1024 + kOpSlots * kOpBBytes + kWSlots * kWBytes + kWSlots * kSideBytes + kDeferBytes + kTaskBytes + kMiscBytes;
+// Tensor memory: two accumulators of 128 columns, then two row buffers of 64 columns of
+// [b0 b0 b1 b1] (bf16 pairs).
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kRowBuf0 = 2 * kTK, kRowBufCols = 96, kRowBufF32 = 64;
+constexpr uint32_t kRowBuf0 = 2 * kTK, kRowBufCols = 64;
 constexpr uint16_t kBothCtas = 0x3;
 constexpr uint16_t kEvenCta = 0x1;
 constexpr uint64_t kWaitLimitNs = 4000000000ull;
 constexpr uint64_t kDrainLimitNs = 200000000ull;
-constexpr int kModeAmax = 0, kModeQuant = 1;
 constexpr int kSplitThreads = 256;
 constexpr int kSplitRows = kSplitThreads / 4;  // rows of B per split block (4 threads a row)
 constexpr int kSplitCols = kSplitThreads / 4;  // columns of A per split block (4 threads a column)
@@ -99,6 +115,7 @@ constexpr int kSplitCols = kSplitThreads / 4;  // columns of A per split block (
 constexpr uint32_t kRegsCtl = 56, kRegsEpi = 104;
 static_assert(4 * kRegsCtl + kEpiWarps * kRegsEpi <= (uint32_t)(kThreads / 32) * 96, "register split");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
+static_assert(kDefer <= 2048, "a task names its entry in 11 bits");
 static_assert(kRowBuf0 + 2 * kRowBufCols <= kTmemCols, "tensor memory budget");
 
 // kind::f16, bf16 A and B, fp32 accumulator, K-major, N = 128, M = 256 (pair).
@@ -112,12 +129,15 @@ struct TcArgs {
     int N, K, rows_pad;
     uint8_t* codes;
     uint8_t* sf;
-    float* s_t;  // pass 1: amax accumulator (fp32 bits, atomicMax); pass 2: reads it
+    float* s_t;  // amax phase: amax accumulator (fp32 bits, atomicMax); quantize phase: reads it
     const float* rnorm;  // [N padded to 256] upper bounds of ||B[n,:]||_2 (0 past N)
     const float* B;      // [N, 32] fp32
+    const float* A;      // [32, K] fp32
+    const uint16_t* W;   // [N, K] bf16 bits
     const float* cnorm;  // [K/128][4]: per 128-column strip, the largest ||A[:,k]||_2
                          // of each 64-column half (upper bounds), then 2 unused
-    unsigned int* counter;  // CTAs of the quantize pass that are done (zeroed by the split)
+    unsigned int* counter;  // CTAs that are done (zeroed by the split)
+    unsigned int* arrive;   // CTAs past the amax phase: the grid barrier (zeroed by the split)
     int* status;
     int zero;    // 0 (a value the compiler cannot see; used for data dependencies)
     int nks;     // 128-column strips
@@ -158,7 +178,8 @@ __device__ __forceinline__ void split8(const float* v, uint4& p0, uint4& p1) {
 // Four threads per row of B or column of A (8 values each).  Blocks [0, nb_rows) take
 // 64 rows of B: rnorm[n] (0 for the padding rows up to rows_pad256).  The other blocks
 // take 64 columns of A: A'[k] = [a0 a1 a0 a1] and the block's largest column norm.
-// Block 0 also clears the amax accumulator s_t and the quantize pass's CTA counter.
+// Block 0 also clears the amax accumulator s_t and the fused kernel's two CTA counters
+// (counter[0]: CTAs done; counter[1]: CTAs past the amax phase).
 __global__ void __launch_bounds__(kSplitThreads)
     merge_split_kernel(const float* __restrict__ A, const float* __restrict__ B, int N, int K,
                        int rows_pad256, int nb_rows, uint8_t* __restrict__ Ap,
@@ -170,7 +191,8 @@ __global__ void __launch_bounds__(kSplitThreads)
     grid_dep_launch();  // the amax pass may start streaming W at once
     if (blockIdx.x == 0 && tid == 0) {
         *s_t = 0.0f;
-        *counter = 0u;
+        counter[0] = 0u;
+        counter[1] = 0u;
     }
     float v[8];
     if ((int)blockIdx.x < nb_rows) {
@@ -222,69 +244,59 @@ __global__ void __launch_bounds__(kSplitThreads)
     }
 }
 
-// W[row, kt] of a W tile in shared memory (bf16, two 64-column boxes with the 128-byte
-// swizzle: the 16-byte chunk u of a row sits at chunk u ^ (row % 8)).
-__device__ __forceinline__ float w_at(const uint8_t* wt, int row, int kt) {
-    const int u = (kt & 63) >> 3;
-    const uint16_t h = *reinterpret_cast<const uint16_t*>(
-        wt + (kt >> 6) * kWBox + row * 128 + ((u ^ (row & 7)) << 4) + (kt & 7) * 2);
-    return __uint_as_float((uint32_t)h << 16);
-}
-
-// The library's merged value of one element (the fp32 fma chain, in order): b = the
-// element's row of B (fp32 bits), column kt of the fp32 strip of A (32 x kTK), weight w.
-__device__ __forceinline__ float exact_value(const uint32_t (&b)[kRank], const float* af, int kt,
-                                             float c, float w) {
-    float a[kRank];
-#pragma unroll
-    for (int j = 0; j < kRank; ++j) a[j] = af[j * kTK + kt];
-    float acc = 0.0f;
-#pragma unroll
-    for (int j = 0; j < kRank; ++j) acc = __fmaf_rn(__uint_as_float(b[j]), a[j], acc);
-    return __fmaf_rn(c, acc, w);
-}
-
-// Pass 2's rare path for one thread's 32 columns (called by the whole warp; `slow`
-// says whether this thread has work): blocks whose scale is uncertain get their 16
-// values from the exact chain (16 chains side by side), then the scale and codes by
-// true divisions; elements whose interval ends disagree (diff) get their code from
-// the exact chain.  tbrow is the tensor-memory address of the fp32 rows of B, af the
-// fp32 strip of A, wt the W tile in shared memory and row this thread's row in it.
+// The quantize phase's exact path for one thread's 32 weights W[n, k0 .. k0 + 31],
+// everything read from global memory (the row of B, the columns of A, the bf16 W):
+// blocks whose scale is undecided (fix0, fix1) get their 16 values from the exact chain
+// (16 chains side by side), then the scale and codes by true divisions; the elements
+// marked in um (one bit per column, in blocks with a decided scale) get their code from
+// the exact chain and a true division.  r holds the codes and scale codes decided so far.
 struct Codes32 {
     uint32_t cw[4];
     uint32_t sfc[2];
 };
-__device__ __forceinline__ Codes32 quant_fix(uint32_t tbrow, const float* af, int kt0, float c, float s,
-                                          float d, Codes32 r, uint4 diff, float den0, float den1,
-                                          bool cert0, bool cert1, bool slow, const uint8_t* wt, int row) {
+__device__ __noinline__ Codes32 quant_fix(const float* brow, const float* A, int K, int k0, const uint16_t* wrow,
+                                         float c, float s, float d, Codes32 r, uint32_t um, bool fix0, bool fix1) {
     uint32_t bq[kRank];
-    tmem_ld_32x32b_x32(tbrow, bq);
-    tmem_ld_wait();
-    if (!slow) return r;
+#pragma unroll
+    for (int j = 0; j < kRank; j += 4) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(brow + j));
+        bq[j] = v.x;
+        bq[j + 1] = v.y;
+        bq[j + 2] = v.z;
+        bq[j + 3] = v.w;
+    }
 #pragma unroll 1
     for (int bk = 0; bk < 2; ++bk) {
-        if (bk == 0 ? cert0 : cert1) continue;
-        const int kt = kt0 + 16 * bk;
+        if (!(bk == 0 ? fix0 : fix1)) continue;
+        const int kk = k0 + 16 * bk;
         float x16[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) x16[e] = 0.0f;
-#pragma unroll 2
-        for (int j = 0; j < kRank; ++j) {
-            const float bj = __uint_as_float(bq[j]);
-            const float4* ar = reinterpret_cast<const float4*>(af + j * kTK + kt);
+#pragma unroll 1
+        for (int j0 = 0; j0 < kRank; j0 += 4) {
+            // 4 rows of A's 16 columns in flight at once, then their FMAs in chain order.
+            float4 v[4][4];
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-                const float4 v = ar[q4];
-                x16[4 * q4] = __fmaf_rn(bj, v.x, x16[4 * q4]);
-                x16[4 * q4 + 1] = __fmaf_rn(bj, v.y, x16[4 * q4 + 1]);
-                x16[4 * q4 + 2] = __fmaf_rn(bj, v.z, x16[4 * q4 + 2]);
-                x16[4 * q4 + 3] = __fmaf_rn(bj, v.w, x16[4 * q4 + 3]);
+            for (int jj = 0; jj < 4; ++jj)
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    v[jj][q4] = __ldg(reinterpret_cast<const float4*>(A + (int64_t)(j0 + jj) * K + kk) + q4);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+                const float bj = __uint_as_float(bq[j0 + jj]);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) {
+                    x16[4 * q4] = __fmaf_rn(bj, v[jj][q4].x, x16[4 * q4]);
+                    x16[4 * q4 + 1] = __fmaf_rn(bj, v[jj][q4].y, x16[4 * q4 + 1]);
+                    x16[4 * q4 + 2] = __fmaf_rn(bj, v[jj][q4].z, x16[4 * q4 + 2]);
+                    x16[4 * q4 + 3] = __fmaf_rn(bj, v[jj][q4].w, x16[4 * q4 + 3]);
+                }
             }
         }
         float bam = 0.0f;
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-            x16[e] = __fmaf_rn(c, x16[e], w_at(wt, row, kt + e));
+            x16[e] = __fmaf_rn(c, x16[e], __uint_as_float((uint32_t)wrow[16 * bk + e] << 16));
             bam = fmaxf(bam, fabsf(x16[e]));
         }
         uint32_t sc = 0;
@@ -303,21 +315,21 @@ __device__ __forceinline__ Codes32 quant_fix(uint32_t tbrow, const float* af, in
             r.cw[2] = c0; r.cw[3] = c1; r.sfc[1] = sc;
         }
     }
-    // Elements whose two ends disagree (in blocks with a certain scale).
-    const uint32_t dw[4] = {diff.x, diff.y, diff.z, diff.w};
-    uint32_t um = 0u;
-#pragma unroll
-    for (int w = 0; w < 4; ++w)
-#pragma unroll
-        for (int j = 0; j < 8; ++j) um |= (((dw[w] >> (4 * j)) & 0xFu) != 0u ? 1u : 0u) << (8 * w + j);
-    if (!cert0) um &= 0xFFFF0000u;
-    if (!cert1) um &= 0x0000FFFFu;
+    if (fix0) um &= 0xFFFF0000u;
+    if (fix1) um &= 0x0000FFFFu;
+    const float den0 = __fmul_rn(e4m3_value(r.sfc[0]), s), den1 = __fmul_rn(e4m3_value(r.sfc[1]), s);
 #pragma unroll 1
     while (um != 0u) {
         const int e = __ffs((int)um) - 1;
         um &= um - 1u;
-        const float x = exact_value(bq, af, kt0 + e, c, w_at(wt, row, kt0 + e));
-        const uint32_t code = cvt_e2m1x8(__fdiv_rn(x, e < 16 ? den0 : den1), 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 0xFu;
+        float acc = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kRank; ++j)
+            acc = __fmaf_rn(__uint_as_float(bq[j]), __ldg(A + (int64_t)j * K + k0 + e), acc);
+        const float x = __fmaf_rn(c, acc, __uint_as_float((uint32_t)wrow[e] << 16));
+        const float den = e < 16 ? den0 : den1;
+        const uint32_t code =
+            den > 0.0f ? cvt_e2m1x8(__fdiv_rn(x, den), 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 0xFu : 0u;
         const uint32_t sh = 4u * (uint32_t)(e & 7), keep = ~(0xFu << sh);
         const int wi = e >> 3;
         if (wi == 0) r.cw[0] = (r.cw[0] & keep) | (code << sh);
@@ -328,28 +340,32 @@ __device__ __forceinline__ Codes32 quant_fix(uint32_t tbrow, const float* af, in
     return r;
 }
 
-// Writes the rows of row block nbw into row buffer nrb & 1 of tensor memory (this
-// warp's 8 of the 32 columns of B for its 32 rows: the bf16 parts for the MMA, fp32
-// for the exact chain), once the lane quarter's 4 warps are all past the tiles that
-// used the buffer, and publishes them to the quarter (qbar) and to the MMA (rows_ready,
-// on the even CTA).  Returns false if a wait gave up.
-__device__ __forceinline__ bool write_rows(const TcArgs& args, uint32_t tmem_base, uint32_t tlane,
-                                           uint64_t* qbar, uint32_t rows_ready_even, int nbw,
-                                           uint32_t rank, int rloc, int chunk, int lane, int& nrb,
-                                           int& nqb, volatile int* abort_flag) {
-    if (lane == 0) mbar_arrive(qbar);
-    bool ok = mbar_wait(qbar, (uint32_t)(nqb & 1), args.status, abort_flag, kWaitLimitNs);
-    ++nqb;
-    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
-    tc_fence_after_sync();
-    const int n = nbw * (kTM * kPair) + (int)rank * kTM + rloc;
-    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+// The byte address of the two scale bytes of row n, columns k0 .. k0 + 31 (k0 % 32 == 0)
+// in the 128x4 blocked layout.
+__device__ __forceinline__ int64_t sf_pair_offset(int n, int k0, int K) {
+    return ((int64_t)(n >> 7) * (K >> 6) + (k0 >> 6)) * 512 + (n & 31) * 16 + ((n >> 5) & 3) * 4 +
+           ((k0 >> 5) & 1) * 2;
+}
+
+// Loads this thread's 8 of the 32 values of B's row n (8 chunk .. 8 chunk + 7; zeros past N).
+__device__ __forceinline__ void load_brow8(const TcArgs& args, int n, int chunk, float (&v)[8]) {
     if (n < args.N) {
         const float4* src = reinterpret_cast<const float4*>(args.B + (int64_t)n * kRank + 8 * chunk);
         const float4 x0 = __ldg(src), x1 = __ldg(src + 1);
         v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
         v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+    } else {
+#pragma unroll
+        for (int z = 0; z < 8; ++z) v[z] = 0.0f;
     }
+}
+
+// Writes a row block's rows of B into row buffer nrb & 1 of tensor memory (this warp's 8
+// of the 32 columns, v, for its 32 rows, as the bf16 parts the MMA reads) and reports it
+// to the MMA issuer (rows_ready, on the even CTA).  The buffer's previous row block was
+// used only by MMAs of tiles this warp has already waited for, so no other wait is needed.
+__device__ __forceinline__ void write_rows(uint32_t tmem_base, uint32_t tlane, uint32_t rows_ready_even, int chunk,
+                                           int lane, int& nrb, const float (&v)[8]) {
     uint4 p0, p1;
     split8(v, p0, p1);
     const uint32_t base = tmem_base + tlane + kRowBuf0 + kRowBufCols * (uint32_t)(nrb & 1);
@@ -361,80 +377,141 @@ __device__ __forceinline__ bool write_rows(const TcArgs& args, uint32_t tmem_bas
     tmem_st_32x32b_x4(base + 16u + col, r0);
     tmem_st_32x32b_x4(base + 32u + col, r1);
     tmem_st_32x32b_x4(base + 48u + col, r1);
-    uint32_t f[8];
-#pragma unroll
-    for (int z = 0; z < 8; ++z) f[z] = __float_as_uint(v[z]);
-    tmem_st_32x32b_x8(base + kRowBufF32 + 8u * (uint32_t)chunk, f);
     tmem_st_wait();
     tc_fence_before_sync();
     __syncwarp();
-    if (lane == 0) {
-        mbar_arrive_cluster(rows_ready_even + 8u * (uint32_t)(nrb & 1));
-        mbar_arrive(qbar);
-    }
-    ok = mbar_wait(qbar, (uint32_t)(nqb & 1), args.status, abort_flag, kWaitLimitNs);
-    ++nqb;
+    if (lane == 0) mbar_arrive_cluster(rows_ready_even + 8u * (uint32_t)(nrb & 1));
     ++nrb;
-    if (!__all_sync(0xFFFFFFFFu, ok)) return false;
-    tc_fence_after_sync();
-    return true;
 }
 
-// Pass 1's candidate path (called by the whole warp): the largest |W'| over the
-// elements of `mask` (this thread's columns kt0 + e), by the exact chain.
-__device__ __forceinline__ float amax_exact(uint32_t tbrow, const float* af, int kt0, float c, uint32_t mask,
-                                         const uint8_t* wt, int row) {
-    uint32_t bq[kRank];
-    tmem_ld_32x32b_x32(tbrow, bq);
-    tmem_ld_wait();
+// The library's merged value W'[n, k] (the fp32 fma chain, in order), everything from
+// global memory: one round of loads (the row of B, the column of A, W).  Out of line:
+// its 64 loaded values stay out of the callers' register budget.
+__device__ __noinline__ float exact_element(const TcArgs& args, int n, int k, float c) {
+    float bv[kRank], av[kRank];
+#pragma unroll
+    for (int j = 0; j < kRank; j += 4) {
+        const float4 v = __ldg(reinterpret_cast<const float4*>(args.B + (int64_t)n * kRank + j));
+        bv[j] = v.x;
+        bv[j + 1] = v.y;
+        bv[j + 2] = v.z;
+        bv[j + 3] = v.w;
+    }
+#pragma unroll
+    for (int j = 0; j < kRank; ++j) av[j] = __ldg(args.A + (int64_t)j * args.K + k);
+    const float w = __uint_as_float((uint32_t)__ldg(args.W + (int64_t)n * args.K + k) << 16);
+    float acc = 0.0f;
+#pragma unroll
+    for (int j = 0; j < kRank; ++j) acc = __fmaf_rn(bv[j], av[j], acc);
+    return __fmaf_rn(c, acc, w);
+}
+
+// The pair's tiles, in the order every role of the fused kernel visits them: the amax
+// phase walks the pair's range [t_begin, t_end) forwards, the quantize phase walks it
+// backwards (its first tiles are the ones the amax phase read last, the likeliest to
+// still be in L2).  Tile t is row block t / nks, 128-column strip t % nks.
+struct TileSeq {
+    int t_begin, t_end, T;
+    __device__ __forceinline__ int tile(int i) const { return i < T ? t_begin + i : t_end - 1 - (i - T); }
+};
+
+// This thread's 32 weights W[n, k0 .. k0 + 31] (read from global memory, all four 16-byte
+// loads in flight at once): the largest |W'| of those whose bound |W| + Ecs reaches thr.
+__device__ __forceinline__ float amax_recheck(const TcArgs& args, int n, int k0, float Ecs, float c, float thr) {
+    uint4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) v[u] = __ldg(reinterpret_cast<const uint4*>(args.W + (int64_t)n * args.K + k0) + u);
     float em = 0.0f;
 #pragma unroll 1
-    while (mask != 0u) {
-        const int e = __ffs((int)mask) - 1;
-        mask &= mask - 1u;
-        em = fmaxf(em, fabsf(exact_value(bq, af, kt0 + e, c, w_at(wt, row, kt0 + e))));
+    for (int e = 0; e < 32; ++e) {
+        const uint4 q = e < 8 ? v[0] : e < 16 ? v[1] : e < 24 ? v[2] : v[3];
+        const int h = (e & 7) >> 1;
+        const uint32_t wd = h == 0 ? q.x : h == 1 ? q.y : h == 2 ? q.z : q.w;
+        const float a = __uint_as_float(((e & 1) ? wd : wd << 16) & 0x7FFF0000u);
+        if (__fadd_ru(__fmul_ru(a, 1.0f + 0x1p-23f), Ecs) < thr) continue;
+        em = fmaxf(em, fabsf(exact_element(args, n, k0 + e, c)));
     }
     return em;
 }
 
-template <int kMode>
+// The end of the amax phase for one epilogue thread: the largest |W'| among the
+// elements that can still be the tensor amax, i.e. whose bound reaches s_t now: this
+// thread's 32 weights of the CTA's seed tile (its first, whose candidates were not
+// queued), or of all its tiles if the queue overflowed, and the queued candidates
+// (entries et, et + 512, ...).
+__device__ __noinline__ float amax_candidates(const TcArgs& args, const uint4* defq, const unsigned int* defn,
+                                              int n0, int k00, bool seed_in, float Ecs, float c, int et,
+                                              bool overflow, TileSeq seq, int nks, uint32_t rank, int rloc, int kt0) {
+    const float st_seen = *reinterpret_cast<volatile const float*>(args.s_t);
+    float em = 0.0f;
+    if (!overflow) {
+        if (seed_in) em = amax_recheck(args, n0, k00, Ecs, c, st_seen);
+        const unsigned int nc = min(*reinterpret_cast<volatile const unsigned int*>(defn), (unsigned int)kDefer);
+        for (unsigned int z = (unsigned int)et; z < nc; z += kEpiWarps * 32) {
+            const uint4 dq = defq[z];
+            if (__uint_as_float(dq.z) >= st_seen) em = fmaxf(em, fabsf(exact_element(args, (int)dq.x, (int)dq.y, c)));
+        }
+    } else {
+#pragma unroll 1
+        for (int i = 0; i < seq.T; ++i) {
+            const int t = seq.tile(i), nb = t / nks;
+            const int n = nb * (kTM * kPair) + (int)rank * kTM + rloc, k0 = (t - nb * nks) * kTK + kt0;
+            if (n < args.N && k0 < args.K) em = fmaxf(em, amax_recheck(args, n, k0, Ecs, c, st_seen));
+        }
+    }
+    return em;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
-    merge_tc_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                    const __grid_constant__ CUtensorMap tmap_ap,
-                    const __grid_constant__ CUtensorMap tmap_af, const TcArgs args) {
+    merge_fused_kernel(const __grid_constant__ CUtensorMap tmap_w,
+                       const __grid_constant__ CUtensorMap tmap_ap, const TcArgs args) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* opB = smem;                          // [kOpSlots]: A' rows of this CTA's 64 columns
     uint8_t* wring = opB + kOpSlots * kOpBBytes;  // [kWSlots]: W tiles
-    uint8_t* xring = wring + kWSlots * kWBytes;   // [kXSlots]: fp32 strips of A
-    uint64_t* bars = reinterpret_cast<uint64_t*>(xring + kXSlots * kAfBytes);
+    uint8_t* side = wring + kWSlots * kWBytes;                           // [kWSlots]: tile bounds
+    uint4* defq = reinterpret_cast<uint4*>(side + kWSlots * kSideBytes);  // [kDefer] the CTA's deferred work
+    float* task_val = reinterpret_cast<float*>(defq + kDefer);           // [kTasks]
+    uint16_t* task_id = reinterpret_cast<uint16_t*>(task_val + kTasks);  // [kTasks]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(task_id + kTasks);
     uint64_t* w_full = bars;                         // [kWSlots]
     uint64_t* w_empty = w_full + kWSlots;            // [kWSlots] the 16 epilogue warps
     uint64_t* op_full = w_empty + kWSlots;           // [kOpSlots] even CTA: both CTAs' A'
     uint64_t* op_empty = op_full + kOpSlots;         // [kOpSlots] the pair's MMAs are done
-    uint64_t* x_full = op_empty + kOpSlots;          // [kXSlots]
-    uint64_t* x_empty = x_full + kXSlots;            // [kXSlots] the 16 epilogue warps
-    uint64_t* tmem_full = x_empty + kXSlots;         // [2]
+    uint64_t* tmem_full = op_empty + kOpSlots;       // [2]
     uint64_t* tmem_empty = tmem_full + 2;            // [2] even CTA
     uint64_t* rows_ready = tmem_empty + 2;           // [2] even CTA: a row buffer is written
-    uint64_t* quarter_bar = rows_ready + 2;          // [4] the 4 warps of a lane quarter
-    uint64_t* drain = quarter_bar + 4;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* drain = rows_ready + 2;
+    uint64_t* epi_done = drain + 1;                  // the 16 epilogue warps finished the amax phase
+    uint64_t* amax_ready = epi_done + 1;             // the tensor amax is in amax_smem
+    uint64_t* loop_done = amax_ready + 1;            // the 16 epilogue warps left the tile loop
+    uint64_t* tasks_ready = loop_done + 1;           // ... listed the deferred elements
+    uint64_t* vals_ready = tasks_ready + 1;          // ... computed their exact values
+    uint64_t* bounds_ready = vals_ready + 1;         // ... contributed to bound_max
+    uint64_t* cand_done = bounds_ready + 1;          // ... queued their amax candidates
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cand_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile float* amax_smem = reinterpret_cast<volatile float*>(tmem_slot + 2);
+    unsigned int* defn = tmem_slot + 3;              // entries pushed to defq
+    unsigned int* ntask = tmem_slot + 4;             // tasks listed in task_id
+    unsigned int* bound_max = tmem_slot + 5;         // [2] largest row norm of B, column norm of A
+    unsigned int* p0_overflow = tmem_slot + 7;       // the amax phase's queue overflowed
+    unsigned int* p1_overflow = tmem_slot + 8;       // the quantize phase's queue overflowed
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
     const int pair = (int)(blockIdx.x / kPair), npairs = (int)(gridDim.x / kPair);
-    const int t_begin = (int)((int64_t)pair * args.tiles / npairs);
-    const int t_end = (int)((int64_t)(pair + 1) * args.tiles / npairs);
-    // Tile t of the pair's range: row block t / nks, strip t % nks (walked strip first).
+    TileSeq seq;
+    seq.t_begin = (int)((int64_t)pair * args.tiles / npairs);
+    seq.t_end = (int)((int64_t)(pair + 1) * args.tiles / npairs);
+    seq.T = seq.t_end - seq.t_begin;
     const int nks = args.nks;
-    const int nb_begin = t_begin / nks, ks_begin = t_begin - nb_begin * nks;
-    // The next pass may start as SMs free up: W does not depend on this one.  What
-    // depends on the previous kernel (A', the norms, s_t) is read after grid_dep_wait.
-    if (kMode == kModeAmax) grid_dep_launch();
+    // Iterations 0 .. T - 1: the amax phase over the pair's tiles (forwards); T .. 2T - 1:
+    // the quantize phase over the same tiles (backwards).
+    const int F = seq.T;
+    const int n_iter = 2 * seq.T;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kWSlots; ++i) {
@@ -445,24 +522,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&op_full[i], 1);
             mbar_init(&op_empty[i], 1);
         }
-        for (int i = 0; i < kXSlots; ++i) {
-            mbar_init(&x_full[i], 1);
-            mbar_init(&x_empty[i], kEpiWarps);
-        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&tmem_full[i], 1);
             mbar_init(&tmem_empty[i], kEpiWarps * kPair);
             mbar_init(&rows_ready[i], kEpiWarps * kPair);
         }
-        for (int i = 0; i < 4; ++i) mbar_init(&quarter_bar[i], kEpiWarps / 4);
         mbar_init(drain, 1);
+        mbar_init(epi_done, kEpiWarps);
+        mbar_init(amax_ready, 1);
+        mbar_init(loop_done, kEpiWarps);
+        mbar_init(tasks_ready, kEpiWarps);
+        mbar_init(vals_ready, kEpiWarps);
+        mbar_init(bounds_ready, kEpiWarps);
+        mbar_init(cand_done, kEpiWarps);
         *abort_flag = 0;
+        *amax_smem = 0.0f;
+        *defn = 0u;
+        *ntask = 0u;
+        bound_max[0] = 0u;
+        bound_max[1] = 0u;
+        *p0_overflow = 0u;
+        *p1_overflow = 0u;
         fence_barrier_init();
     }
-    if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmap_w);
-        prefetch_tmap(&tmap_af);
-    }
+    if (warp == 0 && lane == 0) prefetch_tmap(&tmap_w);
     if (warp == 2 && lane == 0) prefetch_tmap(&tmap_ap);
     if (warp == 1) {
         tmem_alloc_pair(tmem_slot, kTmemCols);
@@ -478,36 +561,44 @@ __global__ void __launch_bounds__(kThreads, 1)
         regs_decrease<kRegsCtl>();
     if (warp == 0) {
         if (lane == 0) {
-            // ------------------------------------------------ TMA: W and strips of A
-            int nb = nb_begin, ks = ks_begin, i = 0;
-            for (int t = t_begin; t < t_end; ++t, ++i) {
-                const int ws = i % kWSlots, xs = i % kXSlots;
-                const int row0 = nb * (kTM * kPair) + (int)rank * kTM;
-                // W (the stream from HBM).
+            // ------------------------------------------------ TMA: W
+            // The amax phase's tiles are kept in L2 (evict_last) for the quantize phase,
+            // which lets them go (evict_first).
+            const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
+            int i = 0;
+            for (; i < n_iter; ++i) {
+                const int ws = i % kWSlots;
                 if (!mbar_wait(&w_empty[ws], (uint32_t)((i / kWSlots) & 1) ^ 1u, args.status,
                                abort_flag, kWaitLimitNs))
                     break;
                 uint8_t* wt = wring + ws * kWBytes;
-                mbar_arrive_expect_tx(&w_full[ws], kWBytes);
-                tma_load_2d(&tmap_w, &w_full[ws], wt, ks * kTK, row0);
-                tma_load_2d(&tmap_w, &w_full[ws], wt + kWBox, ks * kTK + 64, row0);
-                // The fp32 strip of A: the slot's previous strip has landed (its phase is
-                // complete) and the epilogue is done with it.
-                const uint32_t xph = (uint32_t)((i / kXSlots) & 1) ^ 1u;
-                if (!mbar_wait(&x_full[xs], xph, args.status, abort_flag, kWaitLimitNs) ||
-                    !mbar_wait(&x_empty[xs], xph, args.status, abort_flag, kWaitLimitNs))
-                    break;
-                mbar_arrive_expect_tx(&x_full[xs], kAfBytes);
-                tma_load_2d(&tmap_af, &x_full[xs], xring + xs * kAfBytes, ks * kTK, 0);
-                if (++ks == nks) {
-                    ks = 0;
-                    ++nb;
+                if (i < F) {
+                    // An amax-phase tile (the stream from HBM).
+                    const int t = seq.tile(i);
+                    const int nb = t / nks, ks = t - nb * nks;
+                    const int row0 = nb * (kTM * kPair) + (int)rank * kTM;
+                    mbar_arrive_expect_tx(&w_full[ws], kWBytes);
+                    tma_load_2d_hint(&tmap_w, &w_full[ws], wt, ks * kTK, row0, keep);
+                    tma_load_2d_hint(&tmap_w, &w_full[ws], wt + kWBox, ks * kTK + 64, row0, keep);
+                    continue;
                 }
+                if (i == F) grid_dep_wait();  // the norms are written by the split kernel
+                const int t = seq.tile(seq.T + (i - F));
+                const int nb = t / nks, ks = t - nb * nks;
+                const int row0 = nb * (kTM * kPair) + (int)rank * kTM;
+                // A tile of W (from L2), and its bounds: rnorm of the CTA's 128 rows and
+                // cnorm of the strip.
+                mbar_arrive_expect_tx(&w_full[ws], kWBytes + kSideBytes);
+                tma_load_2d_hint(&tmap_w, &w_full[ws], wt, ks * kTK, row0, drop);
+                tma_load_2d_hint(&tmap_w, &w_full[ws], wt + kWBox, ks * kTK + 64, row0, drop);
+                uint8_t* sd = side + ws * kSideBytes;
+                bulk_load(sd, args.rnorm + row0, kTM * 4, &w_full[ws]);
+                bulk_load(sd + kTM * 4, args.cnorm + ks * 4, 16, &w_full[ws]);
             }
             if (!*abort_flag) {
-                // Tail: the last strips of A land before exit.
-                for (int j = (i >= kXSlots ? i - kXSlots : 0); j < i; ++j)
-                    if (!mbar_wait(&x_full[j % kXSlots], (uint32_t)((j / kXSlots) & 1), args.status,
+                // Tail: the last tiles of W land before exit.
+                for (int j = (i >= kWSlots ? i - kWSlots : 0); j < i; ++j)
+                    if (!mbar_wait(&w_full[j % kWSlots], (uint32_t)((j / kWSlots) & 1), args.status,
                                    abort_flag, kWaitLimitNs))
                         break;
             }
@@ -520,10 +611,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 2) {
         if (lane == 0) {
             // ------------------------------------------------ TMA: A' (the MMA's B operand)
+            // The quantize phase's tiles only (the amax phase takes no MMA).
             grid_dep_wait();  // A' is written by the split kernel
             const uint32_t op_full_even = map_to_rank(smem_u32(op_full), 0);
-            int ks = ks_begin, i = 0;
-            for (int t = t_begin; t < t_end; ++t, ++i) {
+            int i = 0;
+            for (; i < seq.T; ++i) {
+                const int t = seq.tile(seq.T + i);
+                const int ks = t - (t / nks) * nks;
                 const int os = i % kOpSlots;
                 if (!mbar_wait(&op_empty[os], (uint32_t)((i / kOpSlots) & 1) ^ 1u, args.status,
                                abort_flag, kWaitLimitNs))
@@ -534,7 +628,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t* ob = opB + os * kOpBBytes;
                 tma_load_2d_pair(&tmap_ap, bar, ob, 0, arow);
                 tma_load_2d_pair(&tmap_ap, bar, ob + kOpBBytes / 2, 64, arow);
-                if (++ks == nks) ks = 0;
             }
             if (!*abort_flag) {
                 // Tail: the last MMAs' releases of the operand slots land before exit.
@@ -553,8 +646,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ------------------------------------------------ MMA issuer (even CTA)
             const uint32_t idesc = idesc_merge();
             bool any = false;
-            int nb = nb_begin, ks = ks_begin, rb = -1, nrb = 0;  // row block in use, buffers filled
-            for (int t = t_begin, i = 0; t < t_end; ++t, ++i) {
+            int rb = -1, nrb = 0;  // row block in use, row buffers filled
+            for (int i = 0; i < seq.T; ++i) {  // the quantize phase's tiles
+                const int t = seq.tile(seq.T + i);
+                const int nb = t / nks;
                 const int b = i & 1, os = i % kOpSlots;
                 if (nb != rb) {
                     // A new row block: its [b0 b0 b1 b1] rows are written by the epilogue.
@@ -583,10 +678,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 any = true;
                 mma_commit_pair_multicast(&op_empty[os], kBothCtas);
                 mma_commit_pair_multicast(&tmem_full[b], kBothCtas);
-                if (++ks == nks) {
-                    ks = 0;
-                    ++nb;
-                }
             }
             if (*abort_flag && any) {
                 mma_commit_pair_multicast(drain, kEvenCta);
@@ -602,73 +693,65 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int chunk = (warp - kEpiWarp0) >> 2;          // 0..3
         const int kt0 = chunk * kCols;                      // this warp's columns in the tile
         const int rloc = q * 32 + lane;                     // this thread's row in the CTA's 128
+        const int et = (int)threadIdx.x - kEpiWarp0 * 32;   // 0..511
+        const int ew = et >> 5;                             // 0..15
         const uint32_t tlane = (uint32_t)(q * 32) << 16;
         const uint32_t rows_ready_even = map_to_rank(smem_u32(rows_ready), 0);
         const uint32_t tmem_empty_even = map_to_rank(smem_u32(tmem_empty), 0);
         const float c = args.c, ac = fabsf(args.c);
         float s = 0.0f, d = 0.0f, idlo = 0.0f, idhi = 0.0f;
         bool d_fast = false;
-        int nrb = 0, nqb = 0;  // row buffers written, quarter_bar phases
-        // The first row block's rows (B is an input: no wait), then the previous kernel's
-        // results (norms, s_t).
-        bool alive = t_begin >= t_end ||
-                     write_rows(args, tmem_base, tlane, quarter_bar + q, rows_ready_even, nb_begin, rank, rloc,
-                                chunk, lane, nrb, nqb, abort_flag);
-        grid_dep_wait();
-        if (kMode == kModeQuant) {
-            const float amax = *reinterpret_cast<volatile const float*>(args.s_t);
-            s = __fdiv_rn(amax, kAmaxDiv);
-            d = __fmul_rn(6.0f, s);
-            d_fast = fast_recip_ok(d);
-            const float rd = d_fast ? recip_approx(d) : 0.0f;
-            idlo = __fmul_rd(rd, 1.0f - 0x1p-19f);
-            idhi = __fmul_ru(rd, 1.0f + 0x1p-19f);
+        int nrb = 0;           // row buffers written
+        grid_dep_wait();       // the split kernel's results (norms, s_t, the counters)
+        // The amax phase's bound on |W' - W| for this CTA's tiles, with the largest norm of
+        // the rows of B they touch and of the columns of A: every |w'| lies within
+        //   Ecs = |c| max ||B[n,:]|| max ||A[:,k]|| (1 + 2^-17) + 2^-126
+        // of |W| (Cauchy-Schwarz; the slack covers the chain's rounding, the final fma's
+        // beyond 2^-23 |W|, and subnormal roundings).
+        float Ecs = 0.0f;
+        {
+            float rmx = 0.0f, cmx = 0.0f;
+            if (F > 0) {
+                // The CTA's 128 rows of each row block from the first tile's to the last's.
+                const int nb_lo = seq.t_begin / nks, nb_hi = (seq.t_end - 1) / nks;
+                for (int r = et; r < (nb_hi - nb_lo + 1) * kTM; r += kEpiWarps * 32)
+                    rmx = fmaxf(rmx, __ldg(args.rnorm + (nb_lo + r / kTM) * (kTM * kPair) + (int)rank * kTM + r % kTM));
+                for (int h = et; h < (args.K >> 6); h += kEpiWarps * 32)
+                    cmx = fmaxf(cmx, __ldg(args.cnorm + (h >> 1) * 4 + (h & 1)));
+            }
+            rmx = warp_max_f(rmx);
+            cmx = warp_max_f(cmx);
+            if (lane == 0) {
+                atomicMax(bound_max, __float_as_uint(rmx));  // non-negative: bits order like values
+                atomicMax(bound_max + 1, __float_as_uint(cmx));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bounds_ready);
+            if (!mbar_wait(bounds_ready, 0, args.status, abort_flag, kWaitLimitNs)) {
+                // leave with the rest (the loop below sees the abort flag at once)
+            }
+            const float rm = __uint_as_float(*reinterpret_cast<volatile unsigned int*>(bound_max));
+            const float cm = __uint_as_float(*reinterpret_cast<volatile unsigned int*>(bound_max + 1));
+            Ecs = __fadd_ru(__fmul_ru(__fmul_ru(ac, __fmul_ru(rm, cm)), 1.0f + 0x1p-17f), 0x1p-126f);
         }
-        int nb = nb_begin, ks = ks_begin;
-        // The norms for E (global, read one tile ahead) and, in pass 1, the running lower
-        // bound of the tensor amax (any value s_t has held is one), read at the end of a
-        // tile for use in the next.
-        float rb_next = 0.0f, ra_next = 0.0f;
-        if (t_begin < t_end) {
-            const int k = ks * kTK + kt0;
-            rb_next = __ldg(args.rnorm + nb * (kTM * kPair) + (int)rank * kTM + rloc);
-            ra_next = k < args.K ? __ldg(args.cnorm + (k >> 7) * 4 + ((k >> 6) & 1)) : 0.0f;
-        }
+        // In the amax phase, the running lower bound of the tensor amax (any value s_t has
+        // held is one), read at the end of a tile for use in the next.
         float st_now = 0.0f, st_next = 0.0f;
-        int cur_buf = 0;  // row buffer of the current tile's row block
-        for (int t = t_begin, i = 0; alive && t < t_end; ++t, ++i) {
-            const int b = i & 1, ws = i % kWSlots, xs = i % kXSlots;
-            const uint32_t ph = (uint32_t)((i >> 1) & 1);
-            const int n = nb * (kTM * kPair) + (int)rank * kTM + rloc;
-            const int k0 = ks * kTK + kt0;        // this warp's first column in W
-            const bool row_ok = n < args.N;
-            const bool col_ok = k0 < args.K;      // K is a multiple of 64: all 32 columns or none
-            const float rb = rb_next, ra = ra_next;
-            int nb1 = nb, ks1 = ks + 1;
-            if (ks1 == nks) {
-                ks1 = 0;
-                ++nb1;
-            }
-            if (t + 1 < t_end) {
-                const int k = ks1 * kTK + kt0;
-                rb_next = __ldg(args.rnorm + nb1 * (kTM * kPair) + (int)rank * kTM + rloc);
-                ra_next = k < args.K ? __ldg(args.cnorm + (k >> 7) * 4 + ((k >> 6) & 1)) : 0.0f;
-                // The next tile starts a new row block: write its rows one tile ahead.
-                if (nb1 != nb && !write_rows(args, tmem_base, tlane, quarter_bar + q, rows_ready_even, nb1, rank,
-                                             rloc, chunk, lane, nrb, nqb, abort_flag))
-                    break;
-            }
-            const uint32_t tbrow = tmem_base + tlane + kRowBuf0 + kRowBufCols * (uint32_t)cur_buf + kRowBufF32;
-            if (t + 1 < t_end && nb1 != nb) cur_buf ^= 1;  // from the next tile on
-            // The accumulator's 32 columns (released at once) and this thread's 32 weights.
-            bool ok = mbar_wait(&tmem_full[b], ph, args.status, abort_flag, kWaitLimitNs) &&
-                      mbar_wait(&w_full[ws], (uint32_t)((i / kWSlots) & 1), args.status, abort_flag,
+        int cur_buf = 0;  // row buffer of the current tile's row block (quantize phase)
+        bool alive = true;
+        // ---- amax phase: tile i of the pair (forwards)
+        for (int i = 0; i < F && !*abort_flag; ++i) {
+            const int ws = i % kWSlots;
+            const uint8_t* wt = wring + ws * kWBytes;  // this tile's W, held until its end
+            // ---- amax phase: this thread's 32 weights of tile i (row n, columns k0 ..).
+            bool ok = mbar_wait(&w_full[ws], (uint32_t)((i / kWSlots) & 1), args.status, abort_flag,
                                 kWaitLimitNs);
             if (!__all_sync(0xFFFFFFFFu, ok)) break;
-            tc_fence_after_sync();
-            const uint8_t* wt = wring + ws * kWBytes;  // this tile's W, held until the tile's end
-            uint32_t acc[32];
-            tmem_ld_32x32b_x32(tmem_base + tlane + (uint32_t)(b * kTK + kt0), acc);
+            const int t = seq.tile(i);
+            const int nb = t / nks, ks = t - nb * nks;
+            const int n = nb * (kTM * kPair) + (int)rank * kTM + rloc;
+            const int k0 = ks * kTK + kt0;
+            const bool in = n < args.N && k0 < args.K;
             uint4 wr[4];
             {
                 const uint8_t* wb = wt + (kt0 >> 6) * kWBox + rloc * 128;
@@ -677,68 +760,185 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int u = 0; u < 4; ++u)
                     wr[u] = *reinterpret_cast<const uint4*>(wb + (((u0 + u) ^ (rloc & 7)) << 4));
             }
-            tmem_ld_wait();
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(tmem_empty_even + 8u * (uint32_t)b);
-            // w~ = fma(c, P~, W) for the 32 columns.
-            float wv[kCols];
-            {
-                const float2 cc = make_float2(c, c);
+            uint32_t mx = 0u;  // bf16 magnitudes order like their bit patterns
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                mx = __vmaxu2(mx, wr[u].x & 0x7FFF7FFFu);
+                mx = __vmaxu2(mx, wr[u].y & 0x7FFF7FFFu);
+                mx = __vmaxu2(mx, wr[u].z & 0x7FFF7FFFu);
+                mx = __vmaxu2(mx, wr[u].w & 0x7FFF7FFFu);
+            }
+            const float mW = in ? __uint_as_float(max(mx & 0xFFFFu, mx >> 16) << 16) : 0.0f;
+            // A lower bound of the tensor amax from this warp's weights.
+            const float lo = warp_max_f(fmaxf(__fsub_rd(__fmul_rd(mW, 1.0f - 0x1p-23f), Ecs), 0.0f));
+            st_now = fmaxf(st_now, st_next);
+            const float thr = fmaxf(lo, st_now);
+            // Only weights with |W| + Ecs at the threshold can be the maximum: queued for
+            // the end of the phase (when the threshold is higher still).  The CTA's first
+            // tile only publishes its bound (the threshold is low then); it is checked
+            // again at the end.
+            const bool cand = in && i > 0 && __fadd_ru(__fmul_ru(mW, 1.0f + 0x1p-23f), Ecs) >= thr;
+            if (__any_sync(0xFFFFFFFFu, cand) && cand) {
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const uint32_t rw[4] = {wr[u].x, wr[u].y, wr[u].z, wr[u].w};
 #pragma unroll
-                    for (int p = 0; p < 4; ++p) {
-                        const int e = 8 * u + 2 * p;
-                        const float2 y = __ffma2_rn(
-                            cc, make_float2(__uint_as_float(acc[e]), __uint_as_float(acc[e + 1])),
-                            make_float2(__uint_as_float(rw[p] << 16), __uint_as_float(rw[p] & 0xFFFF0000u)));
-                        wv[e] = y.x;
-                        wv[e + 1] = y.y;
+                    for (int e = 0; e < 8; ++e) {
+                        const float a = __uint_as_float(((e & 1) ? rw[e >> 1] : rw[e >> 1] << 16) & 0x7FFF0000u);
+                        const float U = __fadd_ru(__fmul_ru(a, 1.0f + 0x1p-23f), Ecs);
+                        if (U < thr) continue;
+                        const int k = k0 + 8 * u + e;
+                        const unsigned int slot = atomicAdd(defn, 1u);
+                        if (slot < (unsigned int)kDefer)
+                            defq[slot] = make_uint4((uint32_t)n, (uint32_t)k, __float_as_uint(U), 0u);
+                        else  // queue full: every tile of the CTA is checked again at the end
+                            *p0_overflow = 1u;
                     }
                 }
             }
-            // E for this row and these columns, every step rounded up.
-            float E;
+            // |W'| >= 0: the fp32 bit patterns order like the values.
+            if (lane == 0 && lo > st_now) atomicMax(reinterpret_cast<unsigned int*>(args.s_t), __float_as_uint(lo));
+            st_next = *reinterpret_cast<volatile const float*>(args.s_t);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&w_empty[ws]);
+        }
+        if (*abort_flag) alive = false;
+        if (alive) {
+            // ---- between the phases.  First the queued amax candidates (elements
+            // whose bound reached the running threshold when their chunk was read):
+            // those whose bound still reaches the current tensor amax bound are merged
+            // exactly (one round of loads each) and their maximum goes to s_t.
+            __syncwarp();
+            if (lane == 0) mbar_arrive(cand_done);
+            if (!mbar_wait(cand_done, 0, args.status, abort_flag, kWaitLimitNs)) alive = false;
             {
-                const float rel = __fmul_ru(__fmul_ru(ac, 0x1p-14f), __fmul_ru(rb, ra));
-                const float abs_ = __fmul_ru(ac, __fmaf_ru(0x1p-120f, __fadd_ru(rb, ra), 0x1p-117f));
-                E = fmaxf(__fadd_ru(rel, abs_), 0x1p-149f);
+                const int t0 = seq.tile(0), nb0 = t0 / nks;
+                const int n0 = nb0 * (kTM * kPair) + (int)rank * kTM + rloc, k00 = (t0 - nb0 * nks) * kTK + kt0;
+                const float em = warp_max_f(amax_candidates(args, defq, defn, n0, k00, n0 < args.N && k00 < args.K,
+                                                            Ecs, c, et, *p0_overflow != 0u, seq, nks, rank,
+                                                            rloc, kt0));
+                if (lane == 0 && em > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(args.s_t), __float_as_uint(em));
             }
-            const float* af = reinterpret_cast<const float*>(xring + xs * kAfBytes);
-            const uint32_t xph = (uint32_t)((i / kXSlots) & 1);
-            bool x_read = false;  // warp-uniform: the exact chain read the strip of A
-
-            if (kMode == kModeAmax) {
-                float m = 0.0f;
-#pragma unroll
-                for (int e = 0; e < kCols; ++e) m = fmaxf(m, fabsf(wv[e]));
-                const bool in = row_ok && col_ok;
-                // A lower bound of the tensor amax from this warp's elements.
-                const float lo = warp_max_f(in ? __fsub_rd(__fmul_rd(m, 1.0f - 0x1p-21f), E) : 0.0f);
-                st_now = fmaxf(st_now, st_next);
-                const float thr = fmaxf(lo, st_now);
-                // Only elements whose upper bound reaches thr can be the maximum.
-                const bool cand = in && __fadd_ru(__fmul_ru(m, 1.0f + 0x1p-21f), E) >= thr;
-                float em = 0.0f;
-                if (__any_sync(0xFFFFFFFFu, cand)) {
-                    uint32_t mask = 0u;
-#pragma unroll
-                    for (int e = 0; e < kCols; ++e)
-                        mask |= (__fadd_ru(__fmul_ru(fabsf(wv[e]), 1.0f + 0x1p-21f), E) >= thr ? 1u : 0u) << e;
-                    if (!cand) mask = 0u;
-                    ok = mbar_wait(&x_full[xs], xph, args.status, abort_flag, kWaitLimitNs);
-                    if (!__all_sync(0xFFFFFFFFu, ok)) break;
-                    x_read = true;
-                    em = warp_max_f(amax_exact(tbrow, af, kt0, c, mask, wt, rloc));
+            // Then every CTA's contributions are in s_t: each warp's atomics are fenced,
+            // the warp reports to epi_done, one thread joins the grid-wide count
+            // (bounded wait) and reads the amax.
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(epi_done);
+            if (warp == kEpiWarp0 && lane == 0) {
+                bool ok = mbar_wait(epi_done, 0, args.status, abort_flag, kWaitLimitNs);
+                float amax = 0.0f;
+                if (ok) {
+                    *defn = 0u;  // the queue now collects the quantize phase's deferred work
+                    __threadfence();
+                    atomicAdd(args.arrive, 1u);
+                    const uint64_t t0 = globaltimer_ns();
+                    while (ld_acquire_gpu(args.arrive) < gridDim.x) {
+                        if (*abort_flag) {
+                            ok = false;
+                            break;
+                        }
+                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                            atomicCAS(args.status, 0, (int)NVFP4_ERR_TIMEOUT);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        __nanosleep(64);
+                    }
+                    if (ok) amax = __uint_as_float(ld_acquire_gpu(reinterpret_cast<const unsigned int*>(args.s_t)));
                 }
-                const float best = fmaxf(em, lo);
-                // |W'| >= 0: the fp32 bit patterns order like the values.
-                if (lane == 0 && best > st_now)
-                    atomicMax(reinterpret_cast<unsigned int*>(args.s_t), __float_as_uint(best));
-                st_next = *reinterpret_cast<volatile const float*>(args.s_t);
-            } else {
+                *amax_smem = amax;
+                mbar_arrive(amax_ready);
+            }
+            const bool ok = mbar_wait(amax_ready, 0, args.status, abort_flag, kWaitLimitNs);
+            if (!__all_sync(0xFFFFFFFFu, ok) || *abort_flag) alive = false;
+            const float amax = *amax_smem;
+            s = __fdiv_rn(amax, kAmaxDiv);
+            d = __fmul_rn(6.0f, s);
+            d_fast = fast_recip_ok(d);
+            const float rd = d_fast ? recip_approx(d) : 0.0f;
+            idlo = __fmul_rd(rd, 1.0f - 0x1p-19f);
+            idhi = __fmul_ru(rd, 1.0f + 0x1p-19f);
+            // The first quantize-phase tile's rows of B (buffer 0), for the MMAs.
+            if (alive) {
+                float bfirst[8];
+                load_brow8(args, (seq.tile(seq.T) / nks) * (kTM * kPair) + (int)rank * kTM + rloc, chunk, bfirst);
+                write_rows(tmem_base, tlane, rows_ready_even, chunk, lane, nrb, bfirst);
+            }
+        }
+        // ---- quantize phase: tile j of the pair (walked backwards)
+        for (int j = 0; alive && j < seq.T && !*abort_flag; ++j) {
+            const int i = F + j;
+            const int ws = i % kWSlots;
+            const uint8_t* wt = wring + ws * kWBytes;  // this tile's W, held until its end
+            const int t = seq.tile(seq.T + j);
+            const int nb = t / nks, ks = t - nb * nks;
+            const int n = nb * (kTM * kPair) + (int)rank * kTM + rloc;
+            const int k0 = ks * kTK + kt0;        // this warp's first column in W
+            const bool row_ok = n < args.N;
+            const bool col_ok = k0 < args.K;      // K is a multiple of 64: all 32 columns or none
+            int nb1 = nb;
+            if (j + 1 < seq.T) {
+                nb1 = seq.tile(seq.T + j + 1) / nks;
+                // The next tile starts a new row block: write its rows one tile ahead.
+                if (nb1 != nb) {
+                    float b1[8];
+                    load_brow8(args, nb1 * (kTM * kPair) + (int)rank * kTM + rloc, chunk, b1);
+                    write_rows(tmem_base, tlane, rows_ready_even, chunk, lane, nrb, b1);
+                }
+            }
+            uint4 wr[4];  // this thread's 32 weights (bf16)
+            {
+                const int b = j & 1;
+                const uint32_t ph = (uint32_t)((j >> 1) & 1);
+                if (nb1 != nb) cur_buf ^= 1;  // from the next tile on
+                // The accumulator's 32 columns (released at once) and this thread's 32 weights.
+                bool ok = mbar_wait(&tmem_full[b], ph, args.status, abort_flag, kWaitLimitNs) &&
+                          mbar_wait(&w_full[ws], (uint32_t)((i / kWSlots) & 1), args.status, abort_flag,
+                                    kWaitLimitNs);
+                if (!__all_sync(0xFFFFFFFFu, ok)) break;
+                tc_fence_after_sync();
+                uint32_t acc[32];
+                tmem_ld_32x32b_x32(tmem_base + tlane + (uint32_t)(b * kTK + kt0), acc);
+                {
+                    const uint8_t* wb = wt + (kt0 >> 6) * kWBox + rloc * 128;
+                    const int u0 = (kt0 & 63) >> 3;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u)
+                        wr[u] = *reinterpret_cast<const uint4*>(wb + (((u0 + u) ^ (rloc & 7)) << 4));
+                }
+                tmem_ld_wait();
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(tmem_empty_even + 8u * (uint32_t)b);
+                // w~ = fma(c, P~, W) for the 32 columns.
+                float wv[kCols];
+                {
+                    const float2 cc = make_float2(c, c);
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const uint32_t rw[4] = {wr[u].x, wr[u].y, wr[u].z, wr[u].w};
+#pragma unroll
+                        for (int p = 0; p < 4; ++p) {
+                            const int e = 8 * u + 2 * p;
+                            const float2 y = __ffma2_rn(
+                                cc, make_float2(__uint_as_float(acc[e]), __uint_as_float(acc[e + 1])),
+                                make_float2(__uint_as_float(rw[p] << 16), __uint_as_float(rw[p] & 0xFFFF0000u)));
+                            wv[e] = y.x;
+                            wv[e + 1] = y.y;
+                        }
+                    }
+                }
+                // E for this row and these columns, every step rounded up.
+                const float rb = reinterpret_cast<const float*>(side + ws * kSideBytes)[rloc];
+                const float ra = reinterpret_cast<const float*>(side + ws * kSideBytes + kTM * 4)[(k0 >> 6) & 1];
+                float E;
+                {
+                    const float rel = __fmul_ru(__fmul_ru(ac, 0x1p-14f), __fmul_ru(rb, ra));
+                    const float abs_ = __fmul_ru(ac, __fmaf_ru(0x1p-120f, __fadd_ru(rb, ra), 0x1p-117f));
+                    E = fmaxf(__fadd_ru(rel, abs_), 0x1p-149f);
+                }
                 uint32_t cw[4], diff[4], sfc[2];
                 float den[2];
                 bool cert[2];
@@ -751,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // live at once.
                         asm volatile("" : "+f"(Eb) : "r"(cw[0]), "r"(cw[1]), "r"(diff[0]), "r"(diff[1]));
                     }
-                    const float E = Eb;
+                    const float Ek = Eb;
                     const float* x = wv + 16 * bk;
                     float bam = 0.0f;
 #pragma unroll
@@ -759,27 +959,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // Block scale: both ends of [bam - E, bam + E] must give the same code.
                     // Rows past N are scale padding (not part of W): scale 0, no codes.
                     const bool scaled = d > 0.0f && row_ok;
-                    const uint32_t slo = cvt_e4m3(__fmul_rn(fmaxf(__fsub_rd(bam, E), 0.0f), idlo));
-                    const uint32_t shi = cvt_e4m3(__fmul_rn(__fadd_ru(bam, E), idhi));
+                    const float X = __fadd_ru(bam, Ek);  // >= |w'| and |w~| of every element
+                    const uint32_t slo = cvt_e4m3(__fmul_rn(fmaxf(__fsub_rd(bam, Ek), 0.0f), idlo));
+                    const uint32_t shi = cvt_e4m3(__fmul_rn(X, idhi));
                     cert[bk] = !scaled || (d_fast && slo == shi);
                     sfc[bk] = scaled ? shi : 0u;
                     den[bk] = __fmul_rn(e4m3_value(sfc[bk]), s);
                     const bool live = den[bk] > 0.0f;
                     const bool fast = fast_recip_ok(den[bk]);
-                    const float rr = fast ? recip_approx(den[bk]) : 0.0f;
-                    const float2 rlo = make_float2(__fmul_rd(rr, 1.0f - 0x1p-19f), __fmul_rd(rr, 1.0f - 0x1p-19f));
-                    const float2 rhi = make_float2(__fmul_ru(rr, 1.0f + 0x1p-19f), __fmul_ru(rr, 1.0f + 0x1p-19f));
-                    // Element codes: both ends of [|w~| - E, |w~| + E], with w~'s sign, 8
-                    // elements at a time.
+                    const float r = fast ? recip_approx(den[bk]) : 0.0f;
+                    // Element codes from one product per element: with r within 2^-23 of
+                    // 1/den (relative), w'/den lies within
+                    //   dl >= E r (1 + 2^-19) + X r 2^-20
+                    // of x r, and so do the rounded ends fl(x r -+ dl) (the slack covers the
+                    // reciprocal's error on |x| <= X, w~'s and w''s own roundings, and the
+                    // rounding of the ends).  fl(w'/den) is then between the two ends, and
+                    // where both ends give the same E2M1 code (sign included) so does it.
+                    const float dl = __fadd_ru(__fmul_ru(__fmul_ru(Ek, r), 1.0f + 0x1p-19f),
+                                               __fmul_ru(__fmul_ru(X, r), 0x1p-20f));
+                    const float2 r2 = make_float2(r, r), dp = make_float2(dl, dl), dn = make_float2(-dl, -dl);
 #pragma unroll
                     for (int g = 0; g < 2; ++g) {
                         float lo8[8], hi8[8];
 #pragma unroll
                         for (int e = 0; e < 8; e += 2) {
                             const float2 xv = make_float2(x[8 * g + e], x[8 * g + e + 1]);
-                            const float2 sE = make_float2(copysignf(E, xv.x), copysignf(E, xv.y));
-                            const float2 l = __fmul2_rn(__ffma2_rn(make_float2(-1.0f, -1.0f), sE, xv), rlo);
-                            const float2 h = __fmul2_rn(__fadd2_rn(xv, sE), rhi);
+                            const float2 l = __ffma2_rn(xv, r2, dn);
+                            const float2 h = __ffma2_rn(xv, r2, dp);
                             lo8[e] = l.x;
                             lo8[e + 1] = l.y;
                             hi8[e] = h.x;
@@ -793,49 +999,195 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const bool slow = row_ok && col_ok &&
                                   (!cert[0] || !cert[1] || (diff[0] | diff[1] | diff[2] | diff[3]) != 0u);
-                if (__any_sync(0xFFFFFFFFu, slow)) {
-                    ok = mbar_wait(&x_full[xs], xph, args.status, abort_flag, kWaitLimitNs);
-                    if (!__all_sync(0xFFFFFFFFu, ok)) break;
-                    x_read = true;
-                    Codes32 r;
-                    r.cw[0] = cw[0]; r.cw[1] = cw[1]; r.cw[2] = cw[2]; r.cw[3] = cw[3];
-                    r.sfc[0] = sfc[0]; r.sfc[1] = sfc[1];
-                    r = quant_fix(tbrow, af, kt0, c, s, d, r, make_uint4(diff[0], diff[1], diff[2], diff[3]),
-                                  den[0], den[1], cert[0], cert[1], slow, wt, rloc);
-                    cw[0] = r.cw[0]; cw[1] = r.cw[1]; cw[2] = r.cw[2]; cw[3] = r.cw[3];
-                    sfc[0] = r.sfc[0]; sfc[1] = r.sfc[1];
+                if (slow) {
+                    // Undecided elements (and blocks): their exact values come from the
+                    // chain, out of this loop, after the last tile: queued for the whole
+                    // CTA in shared memory (kDefer entries; beyond that, the blocks are
+                    // marked and recomputed whole).  The codes stored below are then
+                    // provisional for them.
+                    uint32_t um = 0u;
+#pragma unroll
+                    for (int w = 0; w < 4; ++w)
+#pragma unroll
+                        for (int z = 0; z < 8; ++z)
+                            um |= (((diff[w] >> (4 * z)) & 0xFu) != 0u ? 1u : 0u) << (8 * w + z);
+                    const unsigned int slot = atomicAdd(defn, 1u);
+                    if (slot < (unsigned int)kDefer) {
+                        defq[slot] = make_uint4((uint32_t)j, um,
+                                                (uint32_t)rloc | ((uint32_t)chunk << 8) | (cert[0] ? 0u : 1u << 16) |
+                                                    (cert[1] ? 0u : 1u << 17),
+                                                0u);
+                    } else {
+                        // Queue full: bit 7 of a block's scale byte (never set in an E4M3 scale)
+                        // marks the block for a full exact recomputation after the loop.
+                        if (!cert[0] || (um & 0x0000FFFFu) != 0u) sfc[0] |= 0x80u;
+                        if (!cert[1] || (um & 0xFFFF0000u) != 0u) sfc[1] |= 0x80u;
+                        *p1_overflow = 1u;
+                    }
                 }
                 if (col_ok) {
                     if (row_ok)
                         *reinterpret_cast<uint4*>(args.codes + (int64_t)n * (args.K >> 1) + (k0 >> 1)) =
                             make_uint4(cw[0], cw[1], cw[2], cw[3]);
                     if (n < args.rows_pad)
-                        *reinterpret_cast<uint16_t*>(
-                            args.sf + ((int64_t)(n >> 7) * (args.K >> 6) + (k0 >> 6)) * 512 +
-                            (n & 31) * 16 + ((n >> 5) & 3) * 4 + ((k0 >> 5) & 1) * 2) =
+                        *reinterpret_cast<uint16_t*>(args.sf + sf_pair_offset(n, k0, args.K)) =
                             (uint16_t)(sfc[0] | (sfc[1] << 8));
                 }
             }
-            // Done with this tile's W and strip of A: every shared-memory read of them has
-            // returned (its value was used), and, where the exact chain read them, is
-            // fenced against the TMA that will overwrite the slots.
-            if (x_read) fence_proxy_async_smem();
+            // Done with this tile's W: every shared-memory read of it has returned (its
+            // value was used) before the slot is handed back to the TMA.
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&w_empty[ws]);
-                mbar_arrive(&x_empty[xs]);
+            if (lane == 0) mbar_arrive(&w_empty[ws]);
+        }
+        // The deferred elements, once all 16 warps have left the tile loop, in three steps
+        // spread over the CTA's 512 epilogue threads (one bounded CTA barrier between
+        // steps):
+        //   1. each queued entry (one thread's 32 weights of one tile) lists its elements
+        //      with an undecided code, or all 16 of a block with an undecided scale;
+        //   2. every listed element's exact value: the fp32 chain from global memory (the
+        //      row of B, the column of A, W), one round of loads per element;
+        //   3. each entry's codes (and, for blocks whose scale was undecided, the scale
+        //      byte) from those values by true divisions, written over the provisional
+        //      ones.  An entry whose elements did not fit the task list (kTasks) does its
+        //      own exact work in step 3.
+        __syncwarp();
+        if (lane == 0) mbar_arrive(loop_done);
+        bool go = mbar_wait(loop_done, 0, args.status, abort_flag, kWaitLimitNs);
+        const unsigned int nq = min(*reinterpret_cast<volatile unsigned int*>(defn), (unsigned int)kDefer);
+        if (go) {
+            for (unsigned int z = (unsigned int)et; z < nq; z += kEpiWarps * 32) {
+                const uint4 dq = defq[z];
+                uint32_t em = dq.y;
+                if ((dq.z >> 16) & 1u) em |= 0x0000FFFFu;
+                if ((dq.z >> 17) & 1u) em |= 0xFFFF0000u;
+                const unsigned int cnt = (unsigned int)__popc(em);
+                const unsigned int base = atomicAdd(ntask, cnt);
+                if (base + cnt <= (unsigned int)kTasks) {
+                    unsigned int u = base;
+                    for (uint32_t m = em; m != 0u; m &= m - 1u) task_id[u++] = (uint16_t)((z << 5) | (uint32_t)(__ffs((int)m) - 1));
+                    defq[z].w = base;
+                } else {
+                    defq[z].w = 0xFFFFFFFFu;
+                }
             }
-            nb = nb1;
-            ks = ks1;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tasks_ready);
+        go = go && mbar_wait(tasks_ready, 0, args.status, abort_flag, kWaitLimitNs);
+        if (go) {
+            const unsigned int nt = min(*reinterpret_cast<volatile unsigned int*>(ntask), (unsigned int)kTasks);
+            for (unsigned int u = (unsigned int)et; u < nt; u += kEpiWarps * 32) {
+                const uint32_t id = task_id[u];
+                const uint4 dq = defq[id >> 5];
+                const int t = seq.tile(seq.T + (int)dq.x);
+                const int nb = t / nks;
+                const int n = nb * (kTM * kPair) + (int)rank * kTM + (int)(dq.z & 0xFFu);
+                const int k = (t - nb * nks) * kTK + (int)((dq.z >> 8) & 3u) * kCols + (int)(id & 31u);
+                task_val[u] = exact_element(args, n, k, c);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(vals_ready);
+        go = go && mbar_wait(vals_ready, 0, args.status, abort_flag, kWaitLimitNs);
+        if (go) {
+            for (unsigned int z = (unsigned int)et; z < nq && !*abort_flag; z += kEpiWarps * 32) {
+                const uint4 dq = defq[z];
+                const int t = seq.tile(seq.T + (int)dq.x);
+                const int nb = t / nks;
+                const int n = nb * (kTM * kPair) + (int)rank * kTM + (int)(dq.z & 0xFFu);
+                const int k0 = (t - nb * nks) * kTK + (int)((dq.z >> 8) & 3u) * kCols;
+                const bool fix0 = (dq.z >> 16) & 1u, fix1 = (dq.z >> 17) & 1u;
+                uint4* cp = reinterpret_cast<uint4*>(args.codes + (int64_t)n * (args.K >> 1) + (k0 >> 1));
+                uint16_t* sp = reinterpret_cast<uint16_t*>(args.sf + sf_pair_offset(n, k0, args.K));
+                const uint4 cv = *cp;
+                const uint32_t sv = *sp;
+                Codes32 r;
+                r.cw[0] = cv.x; r.cw[1] = cv.y; r.cw[2] = cv.z; r.cw[3] = cv.w;
+                r.sfc[0] = sv & 0xFFu;
+                r.sfc[1] = sv >> 8;
+                if (dq.w == 0xFFFFFFFFu) {
+                    r = quant_fix(args.B + (int64_t)n * kRank, args.A, args.K, k0, args.W + (int64_t)n * args.K + k0,
+                                  c, s, d, r, dq.y, fix0, fix1);
+                } else {
+                    uint32_t em = dq.y;
+                    if (fix0) em |= 0x0000FFFFu;
+                    if (fix1) em |= 0xFFFF0000u;
+                    const float* xv = task_val + dq.w;  // exact values, in column order of em's bits
+#pragma unroll 1
+                    for (int bk = 0; bk < 2; ++bk) {
+                        if (!(bk == 0 ? fix0 : fix1)) continue;
+                        // The block's 16 exact values: the first 16 (block 0) or the last 16
+                        // of its listed elements.
+                        const float* x16 = xv + (bk == 0 ? 0 : __popc(em & 0x0000FFFFu));
+                        float bam = 0.0f;
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) bam = fmaxf(bam, fabsf(x16[e]));
+                        uint32_t sc = 0;
+                        if (d > 0.0f) sc = cvt_e4m3(__fdiv_rn(bam, d));
+                        const float dn = __fmul_rn(e4m3_value(sc), s);
+                        float q[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) q[e] = dn > 0.0f ? __fdiv_rn(x16[e], dn) : 0.0f;
+                        const uint32_t c0 = dn > 0.0f ? cvt_e2m1x8(q[0], q[1], q[2], q[3], q[4], q[5], q[6], q[7]) : 0u;
+                        const uint32_t c1 = dn > 0.0f ? cvt_e2m1x8(q[8], q[9], q[10], q[11], q[12], q[13], q[14], q[15]) : 0u;
+                        r.cw[2 * bk] = c0;
+                        r.cw[2 * bk + 1] = c1;
+                        r.sfc[bk] = sc;
+                    }
+                    // Elements of blocks whose scale was decided.
+                    const float den0 = __fmul_rn(e4m3_value(r.sfc[0]), s), den1 = __fmul_rn(e4m3_value(r.sfc[1]), s);
+                    int u = 0;
+#pragma unroll 1
+                    for (uint32_t m = em; m != 0u; m &= m - 1u, ++u) {
+                        const int e = __ffs((int)m) - 1;
+                        if ((e < 16 && fix0) || (e >= 16 && fix1)) continue;
+                        const float den = e < 16 ? den0 : den1;
+                        const uint32_t code =
+                            den > 0.0f ? cvt_e2m1x8(__fdiv_rn(xv[u], den), 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f) & 0xFu : 0u;
+                        const uint32_t sh = 4u * (uint32_t)(e & 7), keep = ~(0xFu << sh);
+                        const int wi = e >> 3;
+                        if (wi == 0) r.cw[0] = (r.cw[0] & keep) | (code << sh);
+                        else if (wi == 1) r.cw[1] = (r.cw[1] & keep) | (code << sh);
+                        else if (wi == 2) r.cw[2] = (r.cw[2] & keep) | (code << sh);
+                        else r.cw[3] = (r.cw[3] & keep) | (code << sh);
+                    }
+                }
+                *cp = make_uint4(r.cw[0], r.cw[1], r.cw[2], r.cw[3]);
+                *sp = (uint16_t)(r.sfc[0] | (r.sfc[1] << 8));
+            }
+            // 4. If the queue overflowed: this thread's blocks marked in bit 7 of their scale
+            // byte, each recomputed whole by the exact chain.
+            if (*reinterpret_cast<volatile unsigned int*>(p1_overflow) != 0u) {
+                for (int j = 0; j < seq.T && !*abort_flag; ++j) {
+                    const int t = seq.tile(seq.T + j);
+                    const int nb = t / nks;
+                    const int n = nb * (kTM * kPair) + (int)rank * kTM + rloc;
+                    const int k0 = (t - nb * nks) * kTK + kt0;
+                    if (n >= args.N || k0 >= args.K) continue;
+                    uint16_t* sp = reinterpret_cast<uint16_t*>(args.sf + sf_pair_offset(n, k0, args.K));
+                    const uint32_t sv = *sp;
+                    if ((sv & 0x8080u) == 0u) continue;
+                    uint4* cp = reinterpret_cast<uint4*>(args.codes + (int64_t)n * (args.K >> 1) + (k0 >> 1));
+                    const uint4 cv = *cp;
+                    Codes32 r;
+                    r.cw[0] = cv.x; r.cw[1] = cv.y; r.cw[2] = cv.z; r.cw[3] = cv.w;
+                    r.sfc[0] = sv & 0x7Fu;
+                    r.sfc[1] = (sv >> 8) & 0x7Fu;
+                    r = quant_fix(args.B + (int64_t)n * kRank, args.A, args.K, k0, args.W + (int64_t)n * args.K + k0, c,
+                                  s, d, r, 0u, (sv & 0x80u) != 0u, (sv & 0x8000u) != 0u);
+                    *cp = make_uint4(r.cw[0], r.cw[1], r.cw[2], r.cw[3]);
+                    *sp = (uint16_t)(r.sfc[0] | (r.sfc[1] << 8));
+                }
+            }
         }
     }
 
     __syncwarp();
     tc_fence_before_sync();
     __syncthreads();
-    if (kMode == kModeQuant && threadIdx.x == 0) {
-        // The last CTA to finish (every CTA has read s_t by now) turns the tensor amax
-        // into the per-tensor scale.
+    if (threadIdx.x == 0) {
+        // The last CTA to finish (every CTA has read the amax by now) turns it into the
+        // per-tensor scale.
         __threadfence();
         if (atomicAdd(args.counter, 1u) == gridDim.x - 1) {
             volatile float* st = args.s_t;
@@ -849,8 +1201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int kMode>
-cudaError_t run_merge_tc(const LaunchCtx& ctx, const RequantTcMaps& m, const TcArgs& a) {
+cudaError_t run_merge_fused(const LaunchCtx& ctx, const RequantTcMaps& m, const TcArgs& a) {
     static OccupancyCache occupancy;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[2];
@@ -858,8 +1209,8 @@ cudaError_t run_merge_tc(const LaunchCtx& ctx, const RequantTcMaps& m, const TcA
     attr[0].val.clusterDim.x = kPair;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    // May start before the previous kernel on the stream ends (programmatic dependent
-    // launch); the kernel waits (griddepcontrol.wait) before reading its results.
+    // May start before the split kernel ends (programmatic dependent launch); the kernel
+    // waits (griddepcontrol.wait) before reading its results.
     attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -868,13 +1219,15 @@ cudaError_t run_merge_tc(const LaunchCtx& ctx, const RequantTcMaps& m, const TcA
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3((unsigned)(ctx.num_sms / kPair * kPair), 1, 1);
+    // The grid barrier between the phases needs every CTA resident at once: the grid is
+    // at most the number of clusters the device holds together (one CTA per SM).
     int max_clusters = 0;
-    const cudaError_t e = clusters_per_device(occupancy, ctx, merge_tc_kernel<kMode>, cfg, &max_clusters);
+    const cudaError_t e = clusters_per_device(occupancy, ctx, merge_fused_kernel, cfg, &max_clusters);
     if (e != cudaSuccess) return e;
     const int clusters = a.tiles < max_clusters ? a.tiles : max_clusters;
     cfg.gridDim = dim3((unsigned)(clusters * kPair), 1, 1);
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, merge_tc_kernel<kMode>, m.w, m.ap, m.af, a);
+    return cudaLaunchKernelEx(&cfg, merge_fused_kernel, m.w, m.ap, a);
 }
 
 }  // namespace
@@ -886,9 +1239,9 @@ size_t requant_tc_workspace_bytes(int w_dtype, int r, int64_t N, int64_t K) {
     return requant_tc_layout(nullptr, N, K).bytes;
 }
 
-cudaError_t launch_requant_tc(const LaunchCtx& ctx, const RequantTcMaps& maps, const float* A,
-                              const float* B, void* workspace, float c, int64_t N, int64_t K,
-                              uint8_t* codes, uint8_t* sf, float* s_t) {
+cudaError_t launch_requant_tc(const LaunchCtx& ctx, const RequantTcMaps& maps, const void* W,
+                              const float* A, const float* B, void* workspace, float c, int64_t N,
+                              int64_t K, uint8_t* codes, uint8_t* sf, float* s_t) {
     const RequantTcLayout ws = requant_tc_layout(workspace, N, K);
     TcArgs a;
     a.c = c;
@@ -900,7 +1253,10 @@ cudaError_t launch_requant_tc(const LaunchCtx& ctx, const RequantTcMaps& maps, c
     a.s_t = s_t;
     a.rnorm = ws.rnorm;
     a.counter = ws.counter;
+    a.arrive = ws.counter + 1;
     a.B = B;
+    a.A = A;
+    a.W = static_cast<const uint16_t*>(W);
     a.cnorm = ws.cnorm;
     a.status = ctx.status;
     a.zero = 0;
@@ -913,8 +1269,7 @@ cudaError_t launch_requant_tc(const LaunchCtx& ctx, const RequantTcMaps& maps, c
         A, B, (int)N, (int)K, rows_pad256, nb_rows, ws.ap, ws.rnorm, ws.cnorm, s_t, ws.counter);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if ((e = run_merge_tc<kModeAmax>(ctx, maps, a)) != cudaSuccess) return e;
-    return run_merge_tc<kModeQuant>(ctx, maps, a);
+    return run_merge_fused(ctx, maps, a);
 }
 
 }  // namespace nvfp4rl

@@ -343,3 +343,32 @@ def test_merge_subnormal_accumulator(orc):
     _check_merge(orc, W, A, B, 32.0)
     _check_merge(orc, W * 0, A, B, 0.5)
     _check_requant(orc, W, A, B, 32.0)
+
+
+def test_requant_back_to_back_calls_are_stable(orc):
+    """Forty back-to-back requants of the FLUX.1-shaped weight on one stream (each one
+    kernel with a grid-wide barrier between its amax and quantize phases), every
+    result bit-identical to the oracle's: a barrier that let a CTA read the amax early,
+    or a stale tile, would show up as a mismatch in some call."""
+    require_gpu()
+    cfg = workloads.LINEARS["flux_up"]
+    W = workloads.weight(cfg, seed=3)
+    A, B = workloads.lora(cfg, seed=3)
+    Wd, Ad, Bd = W.cuda(), A.cuda(), B.cuda()
+    N, K = cfg.N, cfg.K
+    outs = [(torch.empty(N, K // 2, dtype=torch.uint8, device="cuda"),
+             torch.empty(nv.sf_bytes(N, K), dtype=torch.uint8, device="cuda"),
+             torch.empty(1, dtype=torch.float32, device="cuda")) for _ in range(40)]
+    ws = torch.empty(nv.requant_workspace_bytes(nv.W_BF16, 32, N, K), dtype=torch.uint8, device="cuda")
+    for o in outs:
+        nv.nvfp4_requant(Wd, Ad, Bd, workloads.LORA_ALPHA, *o, workspace=ws)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_device_status() == 0
+    oc, osf, os_ = orc.requant(workloads.bf16_bits(W), A.numpy(), B.numpy(), workloads.LORA_ALPHA)
+    first = [np_(t) for t in outs[0]]
+    sf_rm, _ = unswizzle_sf(first[1], N, K)
+    assert first[2].view(np.uint32)[0] == os_.view(np.uint32)[0]
+    assert np.array_equal(sf_rm, osf) and np.array_equal(first[0], oc)
+    for j, o in enumerate(outs[1:], 1):
+        for a, b in zip(first, (np_(t) for t in o)):
+            assert np.array_equal(a.view(np.uint8), b.view(np.uint8)), f"call {j} differs from call 0"
