@@ -90,6 +90,7 @@ constexpr uint32_t kWBox = kTM * 128;                    // 16 KB: 128 rows x 64
 constexpr uint32_t kWBytes = 2 * kWBox;                  // 32 KB: 128 rows x 128 bf16
 constexpr uint32_t kMiscBytes = 512;
 constexpr int kDefer = 512;  // deferred (thread, tile) entries per CTA, exact work after the tile loop
+constexpr int kStatic = kWSlots;  // amax tiles a CTA takes by index (the rest from a counter)
 constexpr uint32_t kDeferBytes = kDefer * 16;  // (tile, element mask, row | chunk | flags, task base)
 constexpr int kTasks = 1024;  // exact values computed for the deferred entries (one per element)
 constexpr uint32_t kTaskBytes = kTasks * (2 + 4);  // task (entry << 5 | column) and its exact value
@@ -138,6 +139,8 @@ struct TcArgs {
                          // of each 64-column half (upper bounds), then 2 unused
     unsigned int* counter;  // CTAs that are done (zeroed by the split)
     unsigned int* arrive;   // CTAs past the amax phase: the grid barrier (zeroed by the split)
+    unsigned int* next;     // the amax phase's next dynamically taken tile (zeroed by the split)
+    int units;              // amax-phase tiles: ceil(N / 128) x nks (128 rows x 128 columns)
     int* status;
     int zero;    // 0 (a value the compiler cannot see; used for data dependencies)
     int nks;     // 128-column strips
@@ -178,8 +181,9 @@ __device__ __forceinline__ void split8(const float* v, uint4& p0, uint4& p1) {
 // Four threads per row of B or column of A (8 values each).  Blocks [0, nb_rows) take
 // 64 rows of B: rnorm[n] (0 for the padding rows up to rows_pad256).  The other blocks
 // take 64 columns of A: A'[k] = [a0 a1 a0 a1] and the block's largest column norm.
-// Block 0 also clears the amax accumulator s_t and the fused kernel's two CTA counters
-// (counter[0]: CTAs done; counter[1]: CTAs past the amax phase).
+// Block 0 also clears the amax accumulator s_t and the fused kernel's counters
+// (counter[0]: CTAs done; counter[1]: CTAs past the amax phase; counter[2]: the amax
+// phase's next dynamic tile).
 __global__ void __launch_bounds__(kSplitThreads)
     merge_split_kernel(const float* __restrict__ A, const float* __restrict__ B, int N, int K,
                        int rows_pad256, int nb_rows, uint8_t* __restrict__ Ap,
@@ -193,6 +197,7 @@ __global__ void __launch_bounds__(kSplitThreads)
         *s_t = 0.0f;
         counter[0] = 0u;
         counter[1] = 0u;
+        counter[2] = 0u;
     }
     float v[8];
     if ((int)blockIdx.x < nb_rows) {
@@ -406,10 +411,9 @@ __device__ __noinline__ float exact_element(const TcArgs& args, int n, int k, fl
     return __fmaf_rn(c, acc, w);
 }
 
-// The pair's tiles, in the order every role of the fused kernel visits them: the amax
-// phase walks the pair's range [t_begin, t_end) forwards, the quantize phase walks it
-// backwards (its first tiles are the ones the amax phase read last, the likeliest to
-// still be in L2).  Tile t is row block t / nks, 128-column strip t % nks.
+// The pair's quantize-phase tiles: the range [t_begin, t_end), walked backwards
+// (tile(T + j) for j = 0 .. T - 1).  Tile t is row block t / nks (256 rows, the pair's),
+// 128-column strip t % nks.
 struct TileSeq {
     int t_begin, t_end, T;
     __device__ __forceinline__ int tile(int i) const { return i < T ? t_begin + i : t_end - 1 - (i - T); }
@@ -437,27 +441,17 @@ __device__ __forceinline__ float amax_recheck(const TcArgs& args, int n, int k0,
 // The end of the amax phase for one epilogue thread: the largest |W'| among the
 // elements that can still be the tensor amax, i.e. whose bound reaches s_t now: this
 // thread's 32 weights of the CTA's seed tile (its first, whose candidates were not
-// queued), or of all its tiles if the queue overflowed, and the queued candidates
-// (entries et, et + 512, ...).
+// queued; bound U0, slack E0, skipped when U0 < 0), and the queued candidates (entries
+// et, et + 512, ...; what did not fit in the queue was merged in place).
 __device__ __noinline__ float amax_candidates(const TcArgs& args, const uint4* defq, const unsigned int* defn,
-                                              int n0, int k00, bool seed_in, float Ecs, float c, int et,
-                                              bool overflow, TileSeq seq, int nks, uint32_t rank, int rloc, int kt0) {
+                                              int n0, int k00, float U0, float E0, float c, int et) {
     const float st_seen = *reinterpret_cast<volatile const float*>(args.s_t);
     float em = 0.0f;
-    if (!overflow) {
-        if (seed_in) em = amax_recheck(args, n0, k00, Ecs, c, st_seen);
-        const unsigned int nc = min(*reinterpret_cast<volatile const unsigned int*>(defn), (unsigned int)kDefer);
-        for (unsigned int z = (unsigned int)et; z < nc; z += kEpiWarps * 32) {
-            const uint4 dq = defq[z];
-            if (__uint_as_float(dq.z) >= st_seen) em = fmaxf(em, fabsf(exact_element(args, (int)dq.x, (int)dq.y, c)));
-        }
-    } else {
-#pragma unroll 1
-        for (int i = 0; i < seq.T; ++i) {
-            const int t = seq.tile(i), nb = t / nks;
-            const int n = nb * (kTM * kPair) + (int)rank * kTM + rloc, k0 = (t - nb * nks) * kTK + kt0;
-            if (n < args.N && k0 < args.K) em = fmaxf(em, amax_recheck(args, n, k0, Ecs, c, st_seen));
-        }
+    if (U0 >= st_seen) em = amax_recheck(args, n0, k00, E0, c, st_seen);
+    const unsigned int nc = min(*reinterpret_cast<volatile const unsigned int*>(defn), (unsigned int)kDefer);
+    for (unsigned int z = (unsigned int)et; z < nc; z += kEpiWarps * 32) {
+        const uint4 dq = defq[z];
+        if (__uint_as_float(dq.z) >= st_seen) em = fmaxf(em, fabsf(exact_element(args, (int)dq.x, (int)dq.y, c)));
     }
     return em;
 }
@@ -488,16 +482,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* loop_done = amax_ready + 1;            // the 16 epilogue warps left the tile loop
     uint64_t* tasks_ready = loop_done + 1;           // ... listed the deferred elements
     uint64_t* vals_ready = tasks_ready + 1;          // ... computed their exact values
-    uint64_t* bounds_ready = vals_ready + 1;         // ... contributed to bound_max
-    uint64_t* cand_done = bounds_ready + 1;          // ... queued their amax candidates
+    uint64_t* cand_done = vals_ready + 1;            // ... queued their amax candidates
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cand_done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile float* amax_smem = reinterpret_cast<volatile float*>(tmem_slot + 2);
     unsigned int* defn = tmem_slot + 3;              // entries pushed to defq
     unsigned int* ntask = tmem_slot + 4;             // tasks listed in task_id
-    unsigned int* bound_max = tmem_slot + 5;         // [2] largest row norm of B, column norm of A
-    unsigned int* p0_overflow = tmem_slot + 7;       // the amax phase's queue overflowed
-    unsigned int* p1_overflow = tmem_slot + 8;       // the quantize phase's queue overflowed
+    unsigned int* p0_overflow = tmem_slot + 5;       // the amax phase's queue overflowed
+    unsigned int* p1_overflow = tmem_slot + 6;       // the quantize phase's queue overflowed
+    volatile int* slot_unit = reinterpret_cast<volatile int*>(tmem_slot + 7);  // [kWSlots] amax tile per slot
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -508,10 +501,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     seq.t_end = (int)((int64_t)(pair + 1) * args.tiles / npairs);
     seq.T = seq.t_end - seq.t_begin;
     const int nks = args.nks;
-    // Iterations 0 .. T - 1: the amax phase over the pair's tiles (forwards); T .. 2T - 1:
-    // the quantize phase over the same tiles (backwards).
-    const int F = seq.T;
-    const int n_iter = 2 * seq.T;
+    // The W ring's iterations: first the amax phase's tiles (128 rows x 128 columns: this
+    // CTA's kStatic tiles blockIdx.x + m gridDim.x, then tiles taken from a counter; a
+    // sentinel slot, unit -1, ends the phase), then the quantize phase's T tiles of the
+    // pair.  Producer and epilogue count the amax iterations (F) the same way.
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kWSlots; ++i) {
@@ -533,14 +526,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(loop_done, kEpiWarps);
         mbar_init(tasks_ready, kEpiWarps);
         mbar_init(vals_ready, kEpiWarps);
-        mbar_init(bounds_ready, kEpiWarps);
         mbar_init(cand_done, kEpiWarps);
         *abort_flag = 0;
         *amax_smem = 0.0f;
         *defn = 0u;
         *ntask = 0u;
-        bound_max[0] = 0u;
-        bound_max[1] = 0u;
         *p0_overflow = 0u;
         *p1_overflow = 0u;
         fence_barrier_init();
@@ -563,37 +553,80 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             // ------------------------------------------------ TMA: W
             // The amax phase's tiles are kept in L2 (evict_last) for the quantize phase,
-            // which lets them go (evict_first).
+            // which lets them go (evict_first).  Each W slot also receives the tile's
+            // bounds (row and column norms, written by the split kernel): the first
+            // kStatic tiles' W is requested at once, their bounds once the split kernel is
+            // done.
             const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
-            int i = 0;
-            for (; i < n_iter; ++i) {
-                const int ws = i % kWSlots;
-                if (!mbar_wait(&w_empty[ws], (uint32_t)((i / kWSlots) & 1) ^ 1u, args.status,
-                               abort_flag, kWaitLimitNs))
-                    break;
+            const int G = (int)gridDim.x;
+            int i = 0, nstatic = 0;
+            bool ended = false;
+            auto issue_w = [&](int ws, int u, uint64_t pol) {
                 uint8_t* wt = wring + ws * kWBytes;
-                if (i < F) {
-                    // An amax-phase tile (the stream from HBM).
-                    const int t = seq.tile(i);
-                    const int nb = t / nks, ks = t - nb * nks;
-                    const int row0 = nb * (kTM * kPair) + (int)rank * kTM;
-                    mbar_arrive_expect_tx(&w_full[ws], kWBytes);
-                    tma_load_2d_hint(&tmap_w, &w_full[ws], wt, ks * kTK, row0, keep);
-                    tma_load_2d_hint(&tmap_w, &w_full[ws], wt + kWBox, ks * kTK + 64, row0, keep);
-                    continue;
-                }
-                if (i == F) grid_dep_wait();  // the norms are written by the split kernel
-                const int t = seq.tile(seq.T + (i - F));
-                const int nb = t / nks, ks = t - nb * nks;
-                const int row0 = nb * (kTM * kPair) + (int)rank * kTM;
-                // A tile of W (from L2), and its bounds: rnorm of the CTA's 128 rows and
-                // cnorm of the strip.
-                mbar_arrive_expect_tx(&w_full[ws], kWBytes + kSideBytes);
-                tma_load_2d_hint(&tmap_w, &w_full[ws], wt, ks * kTK, row0, drop);
-                tma_load_2d_hint(&tmap_w, &w_full[ws], wt + kWBox, ks * kTK + 64, row0, drop);
+                const int row0 = (u / nks) * kTM, x0 = (u - (u / nks) * nks) * kTK;
+                tma_load_2d_hint(&tmap_w, &w_full[ws], wt, x0, row0, pol);
+                tma_load_2d_hint(&tmap_w, &w_full[ws], wt + kWBox, x0 + 64, row0, pol);
+            };
+            auto issue_side = [&](int ws, int row0, int ks) {
                 uint8_t* sd = side + ws * kSideBytes;
                 bulk_load(sd, args.rnorm + row0, kTM * 4, &w_full[ws]);
                 bulk_load(sd + kTM * 4, args.cnorm + ks * 4, 16, &w_full[ws]);
+            };
+            for (; i < kStatic && !ended; ++i) {
+                if (!mbar_wait(&w_empty[i], 1u, args.status, abort_flag, kWaitLimitNs)) break;
+                const int u = (int)blockIdx.x + i * G;
+                if (u >= args.units) {
+                    slot_unit[i] = -1;
+                    mbar_arrive(&w_full[i]);
+                    ended = true;
+                } else {
+                    slot_unit[i] = u;
+                    mbar_arrive_expect_tx(&w_full[i], kWBytes + kSideBytes);
+                    issue_w(i, u, keep);
+                    ++nstatic;
+                }
+            }
+            grid_dep_wait();  // the norms and the tile counter are written by the split kernel
+            for (int z = 0; z < nstatic; ++z) {
+                const int u = (int)blockIdx.x + z * G;
+                issue_side(z, (u / nks) * kTM, u - (u / nks) * nks);
+            }
+            // Each unit is claimed before its slot is free (the claim's round trip overlaps
+            // the wait).
+            int u_next = ended ? args.units : kStatic * G + (int)atomicAdd(args.next, 1u);
+            for (; !ended && !*abort_flag; ++i) {
+                const int ws = i % kWSlots;
+                const int u = u_next;
+                if (u < args.units) u_next = kStatic * G + (int)atomicAdd(args.next, 1u);
+                if (!mbar_wait(&w_empty[ws], (uint32_t)((i / kWSlots) & 1) ^ 1u, args.status, abort_flag,
+                               kWaitLimitNs))
+                    break;
+                if (u >= args.units) {
+                    slot_unit[ws] = -1;
+                    mbar_arrive(&w_full[ws]);
+                    ended = true;
+                } else {
+                    slot_unit[ws] = u;
+                    mbar_arrive_expect_tx(&w_full[ws], kWBytes + kSideBytes);
+                    issue_w(ws, u, keep);
+                    issue_side(ws, (u / nks) * kTM, u - (u / nks) * nks);
+                }
+            }
+            // i = the amax iterations, the sentinel's included; the quantize phase's
+            // tiles follow in the ring.
+            for (int j = 0; ended && j < seq.T && !*abort_flag; ++j, ++i) {
+                const int ws = i % kWSlots;
+                if (!mbar_wait(&w_empty[ws], (uint32_t)((i / kWSlots) & 1) ^ 1u, args.status, abort_flag,
+                               kWaitLimitNs))
+                    break;
+                const int t = seq.tile(seq.T + j);
+                const int nb = t / nks, ks = t - nb * nks;
+                const int row0 = nb * (kTM * kPair) + (int)rank * kTM;
+                // A quantize-phase tile of W (from L2), and its bounds.
+                mbar_arrive_expect_tx(&w_full[ws], kWBytes + kSideBytes);
+                tma_load_2d_hint(&tmap_w, &w_full[ws], wring + ws * kWBytes, ks * kTK, row0, drop);
+                tma_load_2d_hint(&tmap_w, &w_full[ws], wring + ws * kWBytes + kWBox, ks * kTK + 64, row0, drop);
+                issue_side(ws, row0, ks);
             }
             if (!*abort_flag) {
                 // Tail: the last tiles of W land before exit.
@@ -694,7 +727,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int kt0 = chunk * kCols;                      // this warp's columns in the tile
         const int rloc = q * 32 + lane;                     // this thread's row in the CTA's 128
         const int et = (int)threadIdx.x - kEpiWarp0 * 32;   // 0..511
-        const int ew = et >> 5;                             // 0..15
         const uint32_t tlane = (uint32_t)(q * 32) << 16;
         const uint32_t rows_ready_even = map_to_rank(smem_u32(rows_ready), 0);
         const uint32_t tmem_empty_even = map_to_rank(smem_u32(tmem_empty), 0);
@@ -703,104 +735,124 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool d_fast = false;
         int nrb = 0;           // row buffers written
         grid_dep_wait();       // the split kernel's results (norms, s_t, the counters)
-        // The amax phase's bound on |W' - W| for this CTA's tiles, with the largest norm of
-        // the rows of B they touch and of the columns of A: every |w'| lies within
-        //   Ecs = |c| max ||B[n,:]|| max ||A[:,k]|| (1 + 2^-17) + 2^-126
-        // of |W| (Cauchy-Schwarz; the slack covers the chain's rounding, the final fma's
-        // beyond 2^-23 |W|, and subnormal roundings).
-        float Ecs = 0.0f;
-        {
-            float rmx = 0.0f, cmx = 0.0f;
-            if (F > 0) {
-                // The CTA's 128 rows of each row block from the first tile's to the last's.
-                const int nb_lo = seq.t_begin / nks, nb_hi = (seq.t_end - 1) / nks;
-                for (int r = et; r < (nb_hi - nb_lo + 1) * kTM; r += kEpiWarps * 32)
-                    rmx = fmaxf(rmx, __ldg(args.rnorm + (nb_lo + r / kTM) * (kTM * kPair) + (int)rank * kTM + r % kTM));
-                for (int h = et; h < (args.K >> 6); h += kEpiWarps * 32)
-                    cmx = fmaxf(cmx, __ldg(args.cnorm + (h >> 1) * 4 + (h & 1)));
-            }
-            rmx = warp_max_f(rmx);
-            cmx = warp_max_f(cmx);
-            if (lane == 0) {
-                atomicMax(bound_max, __float_as_uint(rmx));  // non-negative: bits order like values
-                atomicMax(bound_max + 1, __float_as_uint(cmx));
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(bounds_ready);
-            if (!mbar_wait(bounds_ready, 0, args.status, abort_flag, kWaitLimitNs)) {
-                // leave with the rest (the loop below sees the abort flag at once)
-            }
-            const float rm = __uint_as_float(*reinterpret_cast<volatile unsigned int*>(bound_max));
-            const float cm = __uint_as_float(*reinterpret_cast<volatile unsigned int*>(bound_max + 1));
-            Ecs = __fadd_ru(__fmul_ru(__fmul_ru(ac, __fmul_ru(rm, cm)), 1.0f + 0x1p-17f), 0x1p-126f);
-        }
         // In the amax phase, the running lower bound of the tensor amax (any value s_t has
         // held is one), read at the end of a tile for use in the next.
         float st_now = 0.0f, st_next = 0.0f;
         int cur_buf = 0;  // row buffer of the current tile's row block (quantize phase)
         bool alive = true;
-        // ---- amax phase: tile i of the pair (forwards)
-        for (int i = 0; i < F && !*abort_flag; ++i) {
+        // ---- amax phase: one tile per W slot until the sentinel (unit -1).  Thread (q,
+        // chunk, lane) takes its 32 weights of the tile (row n, columns k0 ..).  With the
+        // tile's bounds rb >= ||B[n,:]|| and ra >= max ||A[:,k]|| every |w'| lies within
+        //   Ecs = |c| rb ra (1 + 2^-17) + 2^-126
+        // of |W| (Cauchy-Schwarz; the slack covers the chain's rounding, the final fma's
+        // beyond 2^-23 |W|, and subnormal roundings).
+        int F = 0;                            // amax iterations, the sentinel's included
+        float seed_U = -1.0f, seed_E = 0.0f;  // the first tile's largest bound and Ecs
+        int seed_n = 0, seed_k0 = 0;
+        auto amax_tile = [&](int i, bool slow_mode) -> int {  // 0: phase over, 1: done, 2: redo
             const int ws = i % kWSlots;
             const uint8_t* wt = wring + ws * kWBytes;  // this tile's W, held until its end
-            // ---- amax phase: this thread's 32 weights of tile i (row n, columns k0 ..).
-            bool ok = mbar_wait(&w_full[ws], (uint32_t)((i / kWSlots) & 1), args.status, abort_flag,
-                                kWaitLimitNs);
-            if (!__all_sync(0xFFFFFFFFu, ok)) break;
-            const int t = seq.tile(i);
-            const int nb = t / nks, ks = t - nb * nks;
-            const int n = nb * (kTM * kPair) + (int)rank * kTM + rloc;
-            const int k0 = ks * kTK + kt0;
+            bool ok = mbar_wait(&w_full[ws], (uint32_t)((i / kWSlots) & 1), args.status, abort_flag, kWaitLimitNs);
+            if (!__all_sync(0xFFFFFFFFu, ok)) return 0;
+            const int u = slot_unit[ws];
+            if (u < 0) {  // the sentinel: the phase ends here
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&w_empty[ws]);
+                F = i + 1;
+                return 0;
+            }
+            const int n = (u / nks) * kTM + rloc;
+            const int k0 = (u - (u / nks) * nks) * kTK + kt0;
             const bool in = n < args.N && k0 < args.K;
+            const float rb = reinterpret_cast<const float*>(side + ws * kSideBytes)[rloc];
+            const float ra = reinterpret_cast<const float*>(side + ws * kSideBytes + kTM * 4)[(k0 >> 6) & 1];
+            const float Ecs = __fadd_ru(__fmul_ru(__fmul_ru(ac, __fmul_ru(rb, ra)), 1.0f + 0x1p-17f), 0x1p-126f);
             uint4 wr[4];
             {
                 const uint8_t* wb = wt + (kt0 >> 6) * kWBox + rloc * 128;
                 const int u0 = (kt0 & 63) >> 3;
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    wr[u] = *reinterpret_cast<const uint4*>(wb + (((u0 + u) ^ (rloc & 7)) << 4));
+                for (int z = 0; z < 4; ++z) wr[z] = *reinterpret_cast<const uint4*>(wb + (((u0 + z) ^ (rloc & 7)) << 4));
             }
             uint32_t mx = 0u;  // bf16 magnitudes order like their bit patterns
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                mx = __vmaxu2(mx, wr[u].x & 0x7FFF7FFFu);
-                mx = __vmaxu2(mx, wr[u].y & 0x7FFF7FFFu);
-                mx = __vmaxu2(mx, wr[u].z & 0x7FFF7FFFu);
-                mx = __vmaxu2(mx, wr[u].w & 0x7FFF7FFFu);
+            for (int z = 0; z < 4; ++z) {
+                mx = __vmaxu2(mx, wr[z].x & 0x7FFF7FFFu);
+                mx = __vmaxu2(mx, wr[z].y & 0x7FFF7FFFu);
+                mx = __vmaxu2(mx, wr[z].z & 0x7FFF7FFFu);
+                mx = __vmaxu2(mx, wr[z].w & 0x7FFF7FFFu);
             }
             const float mW = in ? __uint_as_float(max(mx & 0xFFFFu, mx >> 16) << 16) : 0.0f;
             // A lower bound of the tensor amax from this warp's weights.
             const float lo = warp_max_f(fmaxf(__fsub_rd(__fmul_rd(mW, 1.0f - 0x1p-23f), Ecs), 0.0f));
             st_now = fmaxf(st_now, st_next);
             const float thr = fmaxf(lo, st_now);
+            const float U_t = __fadd_ru(__fmul_ru(mW, 1.0f + 0x1p-23f), Ecs);
             // Only weights with |W| + Ecs at the threshold can be the maximum: queued for
-            // the end of the phase (when the threshold is higher still).  The CTA's first
-            // tile only publishes its bound (the threshold is low then); it is checked
-            // again at the end.
-            const bool cand = in && i > 0 && __fadd_ru(__fmul_ru(mW, 1.0f + 0x1p-23f), Ecs) >= thr;
+            // the end of the phase (when the threshold is higher still), or, in slow mode,
+            // merged here.  The CTA's first tile only publishes its bound (the threshold is
+            // low then); it is checked again at the end.
+            if (i == 0 && in) {
+                seed_U = U_t;
+                seed_E = Ecs;
+                seed_n = n;
+                seed_k0 = k0;
+            }
+            const bool cand = in && i > 0 && U_t >= thr;
+            bool full = false;
             if (__any_sync(0xFFFFFFFFu, cand) && cand) {
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const uint32_t rw[4] = {wr[u].x, wr[u].y, wr[u].z, wr[u].w};
-#pragma unroll
+                float em = 0.0f;
+#pragma unroll 1
+                for (int z = 0; z < 4; ++z) {
+                    const uint32_t rw[4] = {wr[z].x, wr[z].y, wr[z].z, wr[z].w};
+#pragma unroll 1
                     for (int e = 0; e < 8; ++e) {
-                        const float a = __uint_as_float(((e & 1) ? rw[e >> 1] : rw[e >> 1] << 16) & 0x7FFF0000u);
+                        const uint32_t wd = (e >> 1) == 0 ? rw[0] : (e >> 1) == 1 ? rw[1] : (e >> 1) == 2 ? rw[2] : rw[3];
+                        const float a = __uint_as_float(((e & 1) ? wd : wd << 16) & 0x7FFF0000u);
                         const float U = __fadd_ru(__fmul_ru(a, 1.0f + 0x1p-23f), Ecs);
                         if (U < thr) continue;
-                        const int k = k0 + 8 * u + e;
-                        const unsigned int slot = atomicAdd(defn, 1u);
-                        if (slot < (unsigned int)kDefer)
-                            defq[slot] = make_uint4((uint32_t)n, (uint32_t)k, __float_as_uint(U), 0u);
-                        else  // queue full: every tile of the CTA is checked again at the end
-                            *p0_overflow = 1u;
+                        const int k = k0 + 8 * z + e;
+                        if (slow_mode) {
+                            em = fmaxf(em, fabsf(exact_element(args, n, k, c)));
+                        } else {
+                            const unsigned int slot = atomicAdd(defn, 1u);
+                            if (slot < (unsigned int)kDefer)
+                                defq[slot] = make_uint4((uint32_t)n, (uint32_t)k, __float_as_uint(U), 0u);
+                            else
+                                full = true;
+                        }
                     }
                 }
+                if (em > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(args.s_t), __float_as_uint(em));
+            }
+            if (__any_sync(0xFFFFFFFFu, full)) {
+                // The queue is full: this tile is done again, and the rest of the phase, in
+                // slow mode (the slot is not released yet).
+                if (lane == 0) *p0_overflow = 1u;
+                return 2;
             }
             // |W'| >= 0: the fp32 bit patterns order like the values.
             if (lane == 0 && lo > st_now) atomicMax(reinterpret_cast<unsigned int*>(args.s_t), __float_as_uint(lo));
             st_next = *reinterpret_cast<volatile const float*>(args.s_t);
             __syncwarp();
             if (lane == 0) mbar_arrive(&w_empty[ws]);
+            return 1;
+        };
+        int resume = -1;
+        for (int i = 0; !*abort_flag; ++i) {
+            const int r = amax_tile(i, false);
+            if (r == 0) break;
+            if (r == 2 || *reinterpret_cast<volatile unsigned int*>(p0_overflow) != 0u) {
+                resume = r == 2 ? i : i + 1;
+                break;
+            }
+        }
+        if (resume >= 0) {
+            // Slow mode (the queue filled, in this warp or another): from the tile that
+            // overflowed (or the next one), candidates are merged in place.
+            __syncwarp();
+            for (int i = resume; !*abort_flag; ++i)
+                if (amax_tile(i, true) == 0) break;
         }
         if (*abort_flag) alive = false;
         if (alive) {
@@ -812,11 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(cand_done);
             if (!mbar_wait(cand_done, 0, args.status, abort_flag, kWaitLimitNs)) alive = false;
             {
-                const int t0 = seq.tile(0), nb0 = t0 / nks;
-                const int n0 = nb0 * (kTM * kPair) + (int)rank * kTM + rloc, k00 = (t0 - nb0 * nks) * kTK + kt0;
-                const float em = warp_max_f(amax_candidates(args, defq, defn, n0, k00, n0 < args.N && k00 < args.K,
-                                                            Ecs, c, et, *p0_overflow != 0u, seq, nks, rank,
-                                                            rloc, kt0));
+                const float em = warp_max_f(amax_candidates(args, defq, defn, seed_n, seed_k0, seed_U, seed_E, c, et));
                 if (lane == 0 && em > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(args.s_t), __float_as_uint(em));
             }
             // Then every CTA's contributions are in s_t: each warp's atomics are fenced,
@@ -1254,6 +1302,7 @@ cudaError_t launch_requant_tc(const LaunchCtx& ctx, const RequantTcMaps& maps, c
     a.rnorm = ws.rnorm;
     a.counter = ws.counter;
     a.arrive = ws.counter + 1;
+    a.next = ws.counter + 2;
     a.B = B;
     a.A = A;
     a.W = static_cast<const uint16_t*>(W);
@@ -1262,6 +1311,7 @@ cudaError_t launch_requant_tc(const LaunchCtx& ctx, const RequantTcMaps& maps, c
     a.zero = 0;
     a.nks = (int)((K + kTK - 1) / kTK);
     a.tiles = (int)((N + kTM * kPair - 1) / (kTM * kPair)) * a.nks;
+    a.units = (int)((N + kTM - 1) / kTM) * a.nks;
     const int rows_pad256 = (int)((N + 255) / 256 * 256);
     const int nb_rows = (rows_pad256 + kSplitRows - 1) / kSplitRows;
     const int nb_cols = (int)((K + kSplitCols - 1) / kSplitCols);
