@@ -245,6 +245,23 @@ nvfp4_status nvfp4_requant_noalloc(const void* W, int w_dtype, const float* A, c
 
 /* ---------------------------------------------------------------- diagnostics */
 
+/*
+ * nvfp4_requant_exact_counts — how much of the last tensor-core nvfp4_requant that
+ * used this workspace went through the exact fp32 chain instead of a certified
+ * tensor-core decision (a diagnostic; the Sol-RL pages have no counterpart).
+ *   workspace, workspace_bytes, N, K  as passed to that nvfp4_requant call (the
+ *            counts live in the workspace; 256-byte aligned, at least
+ *            nvfp4_requant_workspace_bytes(NVFP4_W_BF16, 32, N, K) bytes).
+ *   counts   host, 2 x uint32 (out): [0] quantize-phase elements merged by the chain
+ *            (listed elements, plus 16 per block recomputed whole); [1] amax-phase
+ *            candidates merged by the chain.
+ * Reads the counts with a device-to-host copy ordered after the work already on
+ * `stream`, and waits for it.  Meaningless after a call that took the CUDA-core
+ * path or failed.  NVFP4_ERR_NULL / _ALIGN / _SHAPE for bad arguments.
+ */
+nvfp4_status nvfp4_requant_exact_counts(const void* workspace, size_t workspace_bytes, int64_t N,
+                                        int64_t K, uint32_t* counts, void* stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* nvfp4_status_string(nvfp4_status s);
 

@@ -55,6 +55,7 @@ def library() -> ctypes.CDLL:
             sig = {
                 "nvfp4_requant": [P, I, P, P, I, F, I64, I64, P, P, P, P, ctypes.c_size_t, P],
                 "nvfp4_requant_noalloc": [P, I, P, P, I, F, I64, I64, P, P, P, P],
+                "nvfp4_requant_exact_counts": [P, ctypes.c_size_t, I64, I64, P, P],
                 "nvfp4_act_quant": [P, I64, I64, P, P, P, P],
                 "nvfp4_act_quant_tensor": [P, I64, I64, P, P, P, P],
                 "nvfp4_gemm": [P, P, P, P, P, P, P, P, I64, I64, I64, P],
@@ -186,6 +187,15 @@ def nvfp4_requant_noalloc(W, A=None, B=None, alpha: float = 32.0, codes=None, sf
           _opt(B, "B", torch.float32), r, ctypes.c_float(alpha), N, K, _dev(codes, "codes", torch.uint8),
           _dev(sf, "sf", torch.uint8), _dev(s_t, "s_t", torch.float32), _stream(stream))
     return codes, sf, s_t
+
+
+def nvfp4_requant_exact_counts(workspace, N: int, K: int, stream=None):
+    """(quantize-phase, amax-phase) element counts that the last tensor-core
+    nvfp4_requant with this workspace merged by the exact fp32 chain."""
+    out = (ctypes.c_uint32 * 2)()
+    _call("nvfp4_requant_exact_counts", _dev(workspace, "workspace", torch.uint8), workspace.numel(),
+          N, K, out, _stream(stream))
+    return int(out[0]), int(out[1])
 
 
 def nvfp4_act_quant(X, codes=None, sf=None, s_row=None, stream=None):

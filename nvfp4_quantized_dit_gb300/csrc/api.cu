@@ -158,6 +158,22 @@ const char* nvfp4_status_string(nvfp4_status s) {
 
 int nvfp4_version(void) { return 100; }
 
+nvfp4_status nvfp4_requant_exact_counts(const void* workspace, size_t workspace_bytes, int64_t N,
+                                        int64_t K, uint32_t* counts, void* stream) {
+    if (workspace == nullptr || counts == nullptr) return NVFP4_ERR_NULL;
+    if (misaligned(workspace, 256)) return NVFP4_ERR_ALIGN;
+    if (N <= 0 || N > kMaxRows || K <= 0 || K % 64 != 0 || K > (1 << 20)) return NVFP4_ERR_SHAPE;
+    const size_t need = requant_tc_workspace_bytes(NVFP4_W_BF16, 32, N, K);
+    if (need == 0 || workspace_bytes < need) return NVFP4_ERR_SHAPE;
+    LaunchCtx ctx;
+    const nvfp4_status st = resolve(stream, &ctx);
+    if (st != NVFP4_OK) return st;
+    const RequantTcLayout ws = requant_tc_layout(const_cast<void*>(workspace), N, K);
+    cudaError_t e = cudaMemcpyAsync(counts, ws.counter + 3, 2 * sizeof(uint32_t), cudaMemcpyDeviceToHost, ctx.stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(ctx.stream);
+    return from_cuda(e);
+}
+
 size_t nvfp4_requant_workspace_bytes(int w_dtype, int r, int64_t N, int64_t K) {
     if (N < 0 || N > kMaxRows || K <= 0 || K % 64 != 0 || K > (1 << 20)) return 0;
     return requant_tc_workspace_bytes(w_dtype, r, N, K);

@@ -183,7 +183,8 @@ __device__ __forceinline__ void split8(const float* v, uint4& p0, uint4& p1) {
 // take 64 columns of A: A'[k] = [a0 a1 a0 a1] and the block's largest column norm.
 // Block 0 also clears the amax accumulator s_t and the fused kernel's counters
 // (counter[0]: CTAs done; counter[1]: CTAs past the amax phase; counter[2]: the amax
-// phase's next dynamic tile).
+// phase's next dynamic tile; counter[3], counter[4]: elements merged by the exact chain
+// in the quantize and the amax phase, a diagnostic).
 __global__ void __launch_bounds__(kSplitThreads)
     merge_split_kernel(const float* __restrict__ A, const float* __restrict__ B, int N, int K,
                        int rows_pad256, int nb_rows, uint8_t* __restrict__ Ap,
@@ -198,6 +199,8 @@ __global__ void __launch_bounds__(kSplitThreads)
         counter[0] = 0u;
         counter[1] = 0u;
         counter[2] = 0u;
+        counter[3] = 0u;
+        counter[4] = 0u;
     }
     float v[8];
     if ((int)blockIdx.x < nb_rows) {
@@ -421,7 +424,8 @@ struct TileSeq {
 
 // This thread's 32 weights W[n, k0 .. k0 + 31] (read from global memory, all four 16-byte
 // loads in flight at once): the largest |W'| of those whose bound |W| + Ecs reaches thr.
-__device__ __forceinline__ float amax_recheck(const TcArgs& args, int n, int k0, float Ecs, float c, float thr) {
+__device__ __forceinline__ float amax_recheck(const TcArgs& args, int n, int k0, float Ecs, float c, float thr,
+                                              unsigned int* xcnt) {
     uint4 v[4];
 #pragma unroll
     for (int u = 0; u < 4; ++u) v[u] = __ldg(reinterpret_cast<const uint4*>(args.W + (int64_t)n * args.K + k0) + u);
@@ -433,6 +437,7 @@ __device__ __forceinline__ float amax_recheck(const TcArgs& args, int n, int k0,
         const uint32_t wd = h == 0 ? q.x : h == 1 ? q.y : h == 2 ? q.z : q.w;
         const float a = __uint_as_float(((e & 1) ? wd : wd << 16) & 0x7FFF0000u);
         if (__fadd_ru(__fmul_ru(a, 1.0f + 0x1p-23f), Ecs) < thr) continue;
+        atomicAdd(xcnt, 1u);
         em = fmaxf(em, fabsf(exact_element(args, n, k0 + e, c)));
     }
     return em;
@@ -444,14 +449,18 @@ __device__ __forceinline__ float amax_recheck(const TcArgs& args, int n, int k0,
 // queued; bound U0, slack E0, skipped when U0 < 0), and the queued candidates (entries
 // et, et + 512, ...; what did not fit in the queue was merged in place).
 __device__ __noinline__ float amax_candidates(const TcArgs& args, const uint4* defq, const unsigned int* defn,
-                                              int n0, int k00, float U0, float E0, float c, int et) {
+                                              int n0, int k00, float U0, float E0, float c, int et,
+                                              unsigned int* xcnt) {
     const float st_seen = *reinterpret_cast<volatile const float*>(args.s_t);
     float em = 0.0f;
-    if (U0 >= st_seen) em = amax_recheck(args, n0, k00, E0, c, st_seen);
+    if (U0 >= st_seen) em = amax_recheck(args, n0, k00, E0, c, st_seen, xcnt);
     const unsigned int nc = min(*reinterpret_cast<volatile const unsigned int*>(defn), (unsigned int)kDefer);
     for (unsigned int z = (unsigned int)et; z < nc; z += kEpiWarps * 32) {
         const uint4 dq = defq[z];
-        if (__uint_as_float(dq.z) >= st_seen) em = fmaxf(em, fabsf(exact_element(args, (int)dq.x, (int)dq.y, c)));
+        if (__uint_as_float(dq.z) >= st_seen) {
+            atomicAdd(xcnt, 1u);
+            em = fmaxf(em, fabsf(exact_element(args, (int)dq.x, (int)dq.y, c)));
+        }
     }
     return em;
 }
@@ -487,10 +496,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile float* amax_smem = reinterpret_cast<volatile float*>(tmem_slot + 2);
     unsigned int* defn = tmem_slot + 3;              // entries pushed to defq
-    unsigned int* ntask = tmem_slot + 4;             // tasks listed in task_id
+    unsigned int* ntask = tmem_slot + 4;             // elements claimed in task_id (may pass kTasks)
     unsigned int* p0_overflow = tmem_slot + 5;       // the amax phase's queue overflowed
     unsigned int* p1_overflow = tmem_slot + 6;       // the quantize phase's queue overflowed
     volatile int* slot_unit = reinterpret_cast<volatile int*>(tmem_slot + 7);  // [kWSlots] amax tile per slot
+    unsigned int* xcount = tmem_slot + 7 + kWSlots;  // [2] exact merges: quantize (whole blocks), amax
+    // The end of the listed tasks: the entries that fit occupy task_id[0, nfill) (the
+    // first entry that does not fit, and every later one, claims past kTasks).
+    unsigned int* nfill = tmem_slot + 9 + kWSlots;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -533,6 +546,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         *ntask = 0u;
         *p0_overflow = 0u;
         *p1_overflow = 0u;
+        xcount[0] = 0u;
+        xcount[1] = 0u;
+        *nfill = 0u;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) prefetch_tmap(&tmap_w);
@@ -813,6 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (U < thr) continue;
                         const int k = k0 + 8 * z + e;
                         if (slow_mode) {
+                            atomicAdd(&xcount[1], 1u);
                             em = fmaxf(em, fabsf(exact_element(args, n, k, c)));
                         } else {
                             const unsigned int slot = atomicAdd(defn, 1u);
@@ -864,7 +881,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(cand_done);
             if (!mbar_wait(cand_done, 0, args.status, abort_flag, kWaitLimitNs)) alive = false;
             {
-                const float em = warp_max_f(amax_candidates(args, defq, defn, seed_n, seed_k0, seed_U, seed_E, c, et));
+                const float em = warp_max_f(amax_candidates(args, defq, defn, seed_n, seed_k0, seed_U, seed_E, c, et,
+                                                                        &xcount[1]));
                 if (lane == 0 && em > 0.0f) atomicMax(reinterpret_cast<unsigned int*>(args.s_t), __float_as_uint(em));
             }
             // Then every CTA's contributions are in s_t: each warp's atomics are fenced,
@@ -1111,6 +1129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const unsigned int cnt = (unsigned int)__popc(em);
                 const unsigned int base = atomicAdd(ntask, cnt);
                 if (base + cnt <= (unsigned int)kTasks) {
+                    atomicMax(nfill, base + cnt);
                     unsigned int u = base;
                     for (uint32_t m = em; m != 0u; m &= m - 1u) task_id[u++] = (uint16_t)((z << 5) | (uint32_t)(__ffs((int)m) - 1));
                     defq[z].w = base;
@@ -1123,9 +1142,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(tasks_ready);
         go = go && mbar_wait(tasks_ready, 0, args.status, abort_flag, kWaitLimitNs);
         if (go) {
-            const unsigned int nt = min(*reinterpret_cast<volatile unsigned int*>(ntask), (unsigned int)kTasks);
+            const unsigned int nt = *reinterpret_cast<volatile unsigned int*>(nfill);
             for (unsigned int u = (unsigned int)et; u < nt; u += kEpiWarps * 32) {
                 const uint32_t id = task_id[u];
+                if ((id >> 5) >= nq) continue;  // never: every listed task names a queued entry
                 const uint4 dq = defq[id >> 5];
                 const int t = seq.tile(seq.T + (int)dq.x);
                 const int nb = t / nks;
@@ -1215,6 +1235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint16_t* sp = reinterpret_cast<uint16_t*>(args.sf + sf_pair_offset(n, k0, args.K));
                     const uint32_t sv = *sp;
                     if ((sv & 0x8080u) == 0u) continue;
+                    atomicAdd(&xcount[0], ((sv & 0x80u) ? 16u : 0u) + ((sv & 0x8000u) ? 16u : 0u));
                     uint4* cp = reinterpret_cast<uint4*>(args.codes + (int64_t)n * (args.K >> 1) + (k0 >> 1));
                     const uint4 cv = *cp;
                     Codes32 r;
@@ -1237,6 +1258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The last CTA to finish (every CTA has read the amax by now) turns it into the
         // per-tensor scale.
         __threadfence();
+        // The exact chain's share (elements listed for it, blocks recomputed whole).
+        const unsigned int xq = *reinterpret_cast<volatile unsigned int*>(ntask) + xcount[0];
+        if (xq != 0u) atomicAdd(args.counter + 3, xq);
+        if (xcount[1] != 0u) atomicAdd(args.counter + 4, xcount[1]);
         if (atomicAdd(args.counter, 1u) == gridDim.x - 1) {
             volatile float* st = args.s_t;
             *st = __fdiv_rn(*st, kAmaxDiv);

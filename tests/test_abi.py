@@ -189,3 +189,17 @@ def test_gemm_withhold_hook_validation(lib):
     bad = list(ok)
     bad[6] = P(BAD)
     assert f(*bad, 256, 256, 512, 1, 50_000_000, None) == 3
+
+
+def test_requant_exact_counts_validation(lib):
+    """The diagnostic checks its arguments before any CUDA call."""
+    P = ctypes.c_void_p
+    f = lib.nvfp4_requant_exact_counts
+    need = lib.nvfp4_requant_workspace_bytes(0, 32, 256, 1024)
+    out = (ctypes.c_uint32 * 2)()
+    assert f(None, need, 256, 1024, out, None) == 1
+    assert f(P(A16), need, 256, 1024, None, None) == 1
+    assert f(P(A16 + 16), need, 256, 1024, out, None) == 3       # workspace not 256-aligned
+    assert f(P(A16), need - 1, 256, 1024, out, None) == 2        # too small
+    assert f(P(A16), need, 256, 100, out, None) == 2             # K % 64
+    assert f(P(A16), need, 0, 1024, out, None) == 2
