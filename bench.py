@@ -73,6 +73,8 @@ KERNEL_SOURCES = {
     "nvfp4_gemm": ["nvfp4_quantized_dit_gb300/csrc/gemm.cu", "nvfp4_quantized_dit_gb300/csrc/common.cuh"],
     "bf16_gemm": ["nvfp4_quantized_dit_gb300/csrc/gemm.cu", "nvfp4_quantized_dit_gb300/csrc/common.cuh"],
     "nvfp4_act_quant": ["nvfp4_quantized_dit_gb300/csrc/quant.cu", "nvfp4_quantized_dit_gb300/csrc/common.cuh"],
+    "nvfp4_act_quant_prescaled": ["nvfp4_quantized_dit_gb300/csrc/quant.cu",
+                                  "nvfp4_quantized_dit_gb300/csrc/common.cuh"],
     "nvfp4_requant": ["nvfp4_quantized_dit_gb300/csrc/merge_tc.cu", "nvfp4_quantized_dit_gb300/csrc/common.cuh"],
 }
 
@@ -209,6 +211,8 @@ def algorithmic_bytes(cfg):
         "nvfp4_act_quant": M * K * 2 + M * K // 2 + sf_a + 4 * M,
         # the same with one per-tensor scale
         "act_quant_per_tensor": M * K * 2 + M * K // 2 + sf_a + 4,
+        # the same with the row amax read instead of found
+        "act_quant_prescaled": M * K * 2 + M * K // 2 + sf_a + 8 * M,
     }
 
 
@@ -356,9 +360,12 @@ def iteration_sweep(device, pk, fp4_peak, reps=3):
           torch.empty(nv.sf_bytes(M, dn.K), dtype=torch.uint8, device=device),
           torch.empty(M, dtype=torch.float32, device=device))
     Y = torch.empty(M, dn.N, dtype=torch.bfloat16, device=device)
+    h_amax = torch.empty(M, dtype=torch.float32, device=device)
+    # The up-projection hands its output's row amax to the hidden state's quantization,
+    # which then streams H once (nvfp4_gemm_rowamax -> nvfp4_act_quant_prescaled).
     calls = [("act_quant_x", lambda: nv.nvfp4_act_quant(X, *xq)),
-             ("gemm_up", lambda: nv.nvfp4_gemm(xq, w_up, bias_up, out=H)),
-             ("act_quant_hidden", lambda: nv.nvfp4_act_quant(H, *hq)),
+             ("gemm_up", lambda: nv.nvfp4_gemm_rowamax(xq, w_up, bias_up, out=H, row_amax=h_amax)),
+             ("act_quant_hidden", lambda: nv.nvfp4_act_quant_prescaled(H, h_amax, *hq)),
              ("gemm_down", lambda: nv.nvfp4_gemm(hq, w_dn, bias_dn, out=Y))]
     for _, fn in calls:
         fn()
@@ -377,6 +384,23 @@ def iteration_sweep(device, pk, fp4_peak, reps=3):
         total.append(ev[0].elapsed_time(ev[-1]))
     per = {n: statistics.median(v) for n, v in per.items()}
     chain_ms = statistics.median(total)
+    # For comparison: the hidden state's quantization without the handed-over row amax
+    # (nvfp4_act_quant, which finds each row's amax itself), and the up-projection
+    # without the row-amax epilogue.
+    alt = {"act_quant_hidden_row_buffered": lambda: nv.nvfp4_act_quant(H, *hq),
+           "gemm_up_plain": lambda: nv.nvfp4_gemm(xq, w_up, bias_up, out=H)}
+    alt_ms = {}
+    for n, fn in alt.items():
+        fn()
+        vs = []
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            fn()
+            b.record()
+            b.synchronize()
+            vs.append(a.elapsed_time(b))
+        alt_ms[n] = statistics.median(vs)
     flop = 2.0 * M * up.N * up.K
     by_x = algorithmic_bytes(up)["nvfp4_act_quant"]
     by_h = algorithmic_bytes(dn)["nvfp4_act_quant"]
@@ -385,9 +409,12 @@ def iteration_sweep(device, pk, fp4_peak, reps=3):
              "gemm_down_tflops": round(flop / (per["gemm_down"] * 1e-3) / 1e12, 1),
              "gemm_frac": round(2 * flop / ((per["gemm_up"] + per["gemm_down"]) * 1e-3) / 1e12 / fp4_peak, 4),
              "act_quant_hidden_gbs": round(by_h / (per["act_quant_hidden"] * 1e-3) / 1e9, 1),
+             "act_quant_hidden_frac": round(by_h / (per["act_quant_hidden"] * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+             "act_quant_hidden_calls": "nvfp4_gemm_rowamax (up) -> nvfp4_act_quant_prescaled",
+             "compare_ms": {n: round(v, 4) for n, v in alt_ms.items()},
              "act_quant_x_gbs": round(by_x / (per["act_quant_x"] * 1e-3) / 1e9, 1),
              "chain_tflops": round(2 * flop / (chain_ms * 1e-3) / 1e12, 1)}
-    del X, xq, H, hq, Y
+    del X, xq, H, hq, Y, h_amax
     torch.cuda.empty_cache()
     return {"requant_sweep": requant, "chain": chain}
 
@@ -555,7 +582,33 @@ def run_ours(args):
         v1.synchronize()
         vt.append(v0.elapsed_time(v1))
     per_tensor_ms = max_over_ranks(statistics.median(vt), world, device)
-    del xq_codes, xq_sf
+
+    # ---- variants of the step's act_quant and GEMM with the row amax handed over: the
+    # GEMM's epilogue reduces its output rows' amax (nvfp4_gemm_rowamax), and a
+    # streaming quantizer takes it (nvfp4_act_quant_prescaled, here on X with its own
+    # row amax, as if X came from such a GEMM)
+    x_amax = dev["X"].float().abs().amax(dim=1)
+    y_amax = torch.empty(M, dtype=torch.float32, device=device)
+    variant_ms = {}
+    for n, fn in {"act_quant_prescaled": lambda: nv.nvfp4_act_quant_prescaled(dev["X"], x_amax, xq_codes, xq_sf,
+                                                                                a_s),
+                  "nvfp4_gemm_rowamax": lambda: nv.nvfp4_gemm_rowamax((a_codes, a_sf, a_s),
+                                                                      (w_codes, w_sf, w_st), dev["bias"],
+                                                                      out=Y4, row_amax=y_amax)}.items():
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        vt = []
+        for _ in range(10):
+            v0, v1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            v0.record()
+            fn()
+            v1.record()
+            v1.synchronize()
+            vt.append(v0.elapsed_time(v1))
+        variant_ms[n] = max_over_ranks(statistics.median(vt), world, device)
+    # a_s is act_quant's own output again (the prescaled call above rewrote it identically)
+    del xq_codes, xq_sf, x_amax, y_amax
 
     # ---- end to end: pinned host inputs in, result out, every step
     if args.no_e2e:
@@ -581,7 +634,7 @@ def run_ours(args):
         extras["evt_spread"] = evt_report(device)
         extras["device_status_after_extras"] = nv.nvfp4_device_status()
     return report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk, world, rank,
-                  launches_per_step, per_tensor_ms, extras)
+                  launches_per_step, per_tensor_ms, extras, variant_ms)
 
 
 def run_e2e(args, host, dev, step, Y4, idx, rr, M, N, rcfg, Kr, world, device):
@@ -655,7 +708,7 @@ def workload_name(cfg, rcfg):
 
 
 def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk, world, rank,
-           launches_per_step, per_tensor_ms, extras):
+           launches_per_step, per_tensor_ms, extras, variant_ms):
     if rank != 0:
         return None
     M, K, N = cfg.M, cfg.K, cfg.N
@@ -669,6 +722,7 @@ def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk
     tflops16 = gemm_flops / (per["bf16_gemm"] * 1e-3) / 1e12
     rq_gbs = ab["nvfp4_requant"] / (per["nvfp4_requant"] * 1e-3) / 1e9
     aq_gbs = ab["nvfp4_act_quant"] / (per["nvfp4_act_quant"] * 1e-3) / 1e9
+    aqp_gbs = ab["act_quant_prescaled"] / (variant_ms["act_quant_prescaled"] * 1e-3) / 1e9
     ms_per_step = elapsed_ms / args.steps
     e2e_ms_step = e2e_ms / args.steps
 
@@ -725,7 +779,18 @@ def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk
             "call": "nvfp4_act_quant_tensor (one per-tensor scale, two passes over X)",
             "ms": round(per_tensor_ms, 4),
             "gbs": round(ab["act_quant_per_tensor"] / (per_tensor_ms * 1e-3) / 1e9, 1),
-            "frac": round(ab["act_quant_per_tensor"] / (per_tensor_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)}},
+            "frac": round(ab["act_quant_per_tensor"] / (per_tensor_ms * 1e-3) / 1e9 / pk["hbm_gbs"], 4)},
+            "act_quant_prescaled": {
+                "call": "nvfp4_act_quant_prescaled (row amax handed over, e.g. by nvfp4_gemm_rowamax, "
+                        "instead of reduced over the row)",
+                "ms": round(variant_ms["act_quant_prescaled"], 4),
+                "gbs": round(aqp_gbs, 1),
+                "frac": round(aqp_gbs / pk["hbm_gbs"], 4),
+                "roofline": roof("hbm", aqp_gbs, pk["hbm_gbs"], "GB/s", "nvfp4_act_quant_prescaled")},
+            "nvfp4_gemm_rowamax": {
+                "call": "nvfp4_gemm_rowamax (nvfp4_gemm plus the output rows' amax from the epilogue)",
+                "ms": round(variant_ms["nvfp4_gemm_rowamax"], 4),
+                "tflops": round(gemm_flops / (variant_ms["nvfp4_gemm_rowamax"] * 1e-3) / 1e12, 1)}},
         "gpu_launches": sum(launches_per_step.values()) * args.steps,
         "device_status": status,
         "clocks": clk,

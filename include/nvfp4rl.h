@@ -163,7 +163,8 @@ nvfp4_status nvfp4_act_quant(const void* X, int64_t M, int64_t K, uint8_t* codes
  *   s_t    device, one fp32 (out); also the amax accumulator while the call runs.
  *          Required even when M == 0 (it is then set to 0; X, codes, sf may be NULL).
  *   K % 64 == 0, K <= 32768, M < 2^31.  Two passes over X: a memset, an amax kernel,
- *   the quantize kernel and a one-thread kernel that turns amax into s_t.  Gives the
+ *   nvfp4_act_quant's kernel with the tensor's amax given for every row, and a
+ *   one-thread kernel that turns amax into s_t.  Gives the
  *   same codes, scales and s_t as nvfp4_requant with no LoRA factors on X.
  *   To use the result as nvfp4_gemm's activations, pass an [M] fp32 vector holding s_t
  *   in every entry as a_srow (the GEMM reads one scale per row; s_t alone is a single
@@ -171,6 +172,24 @@ nvfp4_status nvfp4_act_quant(const void* X, int64_t M, int64_t K, uint8_t* codes
  */
 nvfp4_status nvfp4_act_quant_tensor(const void* X, int64_t M, int64_t K, uint8_t* codes, uint8_t* sf,
                                     float* s_t, void* stream);
+
+/*
+ * nvfp4_act_quant_prescaled — nvfp4_act_quant for activations whose per-row amax is
+ * already known, e.g. written by nvfp4_gemm_rowamax when it produced X (the per-token
+ * quantization of the NVFP4-quantized solver's next linear, Sol-RL project page,
+ * "Two-Stage Pipeline", Stage 1).  With row_amax[m] == max_k |X[m,k]| the codes, scales
+ * and s_row are identical to nvfp4_act_quant(X); a row_amax below a row's true amax
+ * makes its largest elements saturate (E4M3 scale and E2M1 code clamp).
+ *   X         device, [M, K] bf16, finite.
+ *   row_amax  device, [M] fp32 (in), each >= 0.
+ *   codes     device, [M, K/2] bytes (out).
+ *   sf        device, nvfp4_sf_bytes(M, K) bytes (out, padding rows written 0).
+ *   s_row     device, [M] fp32 (out): row_amax[m] / 2688.
+ *   K % 64 == 0, K <= 32768, M < 2^31.  One kernel: nvfp4_act_quant's, with each row's
+ *   scale from row_amax instead of a reduction over the row (X is still read once).
+ */
+nvfp4_status nvfp4_act_quant_prescaled(const void* X, int64_t M, int64_t K, const float* row_amax,
+                                       uint8_t* codes, uint8_t* sf, float* s_row, void* stream);
 
 /*
  * nvfp4_gemm — Y = bf16_RNE( s_a[m] * s_w * sum_k a_hat[m,k] * w_hat[n,k] + bias[n] ),
@@ -188,6 +207,22 @@ nvfp4_status nvfp4_act_quant_tensor(const void* X, int64_t M, int64_t K, uint8_t
 nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_srow,
                         const uint8_t* w_codes, const uint8_t* w_sf, const float* w_st,
                         const void* bias, void* Y, int64_t M, int64_t N, int64_t K, void* stream);
+
+/*
+ * nvfp4_gemm_rowamax — nvfp4_gemm that also writes each output row's amax,
+ *   y_row_amax[m] = max_n |Y[m,n]| (of the bf16 values, exactly; 0 when N == 0),
+ * for the per-token quantization of the next linear (nvfp4_act_quant_prescaled), so
+ * that it needs no pass of its own over Y to find the row scales.  The epilogue of
+ * every output tile max-reduces its rows into y_row_amax (atomicMax on the fp32 bits;
+ * every value is >= 0, so the result is exact and order-free), which the call first
+ * zeroes (a memset on `stream`).
+ *   y_row_amax  device, [M] fp32 (out), 4-byte aligned.
+ *   Other arguments, limits and errors as nvfp4_gemm; Y is bit-identical to its Y.
+ */
+nvfp4_status nvfp4_gemm_rowamax(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_srow,
+                                const uint8_t* w_codes, const uint8_t* w_sf, const float* w_st,
+                                const void* bias, void* Y, float* y_row_amax, int64_t M, int64_t N,
+                                int64_t K, void* stream);
 
 /*
  * bf16_gemm — Y = bf16_RNE( X * W^T + bias ), bf16 operands, fp32 accumulation on

@@ -59,6 +59,8 @@ def library() -> ctypes.CDLL:
                 "nvfp4_act_quant": [P, I64, I64, P, P, P, P],
                 "nvfp4_act_quant_tensor": [P, I64, I64, P, P, P, P],
                 "nvfp4_gemm": [P, P, P, P, P, P, P, P, I64, I64, I64, P],
+                "nvfp4_gemm_rowamax": [P, P, P, P, P, P, P, P, P, I64, I64, I64, P],
+                "nvfp4_act_quant_prescaled": [P, I64, I64, P, P, P, P, P],
                 "bf16_gemm": [P, P, P, P, I64, I64, I64, P],
                 "select_contrastive": [P, I, I, I, I, P, P, P],
                 "nvfp4_device_status": [ctypes.POINTER(ctypes.c_int), I],
@@ -242,6 +244,43 @@ def nvfp4_gemm(a, w, bias=None, out=None, stream=None):
           _dev(w_sf, "w_sf", torch.uint8), _dev(w_s, "w_st", torch.float32),
           _opt(bias, "bias", torch.bfloat16), _dev(out, "Y", torch.bfloat16), M, N, K, _stream(stream))
     return out
+
+
+def nvfp4_gemm_rowamax(a, w, bias=None, out=None, row_amax=None, stream=None):
+    """nvfp4_gemm that also returns amax|Y[m, :]| per row (fp32 [M]): (Y, row_amax)."""
+    a_codes, a_sf, a_s = a
+    w_codes, w_sf, w_s = w
+    M, K = a_codes.shape[0], a_codes.shape[1] * 2
+    N = w_codes.shape[0]
+    if w_codes.shape[1] * 2 != K:
+        raise ValueError("activation and weight K differ")
+    dev = a_codes.device
+    out = torch.empty(M, N, dtype=torch.bfloat16, device=dev) if out is None else out
+    row_amax = torch.empty(M, dtype=torch.float32, device=dev) if row_amax is None else row_amax
+    _call("nvfp4_gemm_rowamax", _dev(a_codes, "a_codes", torch.uint8), _dev(a_sf, "a_sf", torch.uint8),
+          _dev(a_s, "a_srow", torch.float32), _dev(w_codes, "w_codes", torch.uint8),
+          _dev(w_sf, "w_sf", torch.uint8), _dev(w_s, "w_st", torch.float32),
+          _opt(bias, "bias", torch.bfloat16), _dev(out, "Y", torch.bfloat16),
+          _dev(row_amax, "row_amax", torch.float32), M, N, K, _stream(stream))
+    return out, row_amax
+
+
+def nvfp4_act_quant_prescaled(X, row_amax, codes=None, sf=None, s_row=None, stream=None):
+    """nvfp4_act_quant of X [M, K] given amax|X[m, :]| per row (fp32 [M]), e.g. from
+    nvfp4_gemm_rowamax.  Returns (codes, sf, s_row)."""
+    if X.dim() != 2:
+        raise ValueError("X must be [M, K]")
+    M, K = X.shape
+    if row_amax.numel() != M:
+        raise ValueError("row_amax must hold one value per row of X")
+    dev = X.device
+    codes = torch.empty(M, K // 2, dtype=torch.uint8, device=dev) if codes is None else codes
+    sf = torch.empty(sf_bytes(M, K), dtype=torch.uint8, device=dev) if sf is None else sf
+    s_row = torch.empty(M, dtype=torch.float32, device=dev) if s_row is None else s_row
+    _call("nvfp4_act_quant_prescaled", _dev(X, "X", torch.bfloat16), M, K,
+          _dev(row_amax, "row_amax", torch.float32), _dev(codes, "codes", torch.uint8),
+          _dev(sf, "sf", torch.uint8), _dev(s_row, "s_row", torch.float32), _stream(stream))
+    return codes, sf, s_row
 
 
 def bf16_gemm(X, W, bias=None, out=None, stream=None):

@@ -268,6 +268,21 @@ nvfp4_status nvfp4_act_quant(const void* X, int64_t M, int64_t K, uint8_t* codes
                                       s_row));
 }
 
+nvfp4_status nvfp4_act_quant_prescaled(const void* X, int64_t M, int64_t K, const float* row_amax,
+                                       uint8_t* codes, uint8_t* sf, float* s_row, void* stream) {
+    if (M < 0 || M > kMaxRows || K <= 0 || K % 64 != 0 || K > 32768) return NVFP4_ERR_SHAPE;
+    if (M == 0) return NVFP4_OK;
+    if (!X || !row_amax || !codes || !sf || !s_row) return NVFP4_ERR_NULL;
+    if (misaligned(X, 16) || misaligned(codes, 16) || misaligned(sf, 16) || misaligned(row_amax, 4) ||
+        misaligned(s_row, 4))
+        return NVFP4_ERR_ALIGN;
+    LaunchCtx ctx;
+    const nvfp4_status st = resolve(stream, &ctx);
+    if (st != NVFP4_OK) return st;
+    return from_cuda(launch_act_quant_prescaled(ctx, static_cast<const __nv_bfloat16*>(X), M, K, row_amax,
+                                                codes, sf, s_row));
+}
+
 nvfp4_status nvfp4_act_quant_tensor(const void* X, int64_t M, int64_t K, uint8_t* codes, uint8_t* sf,
                                     float* s_t, void* stream) {
     if (M < 0 || M > kMaxRows || K <= 0 || K % 64 != 0 || K > 32768) return NVFP4_ERR_SHAPE;
@@ -288,19 +303,32 @@ nvfp4_status nvfp4_act_quant_tensor(const void* X, int64_t M, int64_t K, uint8_t
 static nvfp4_status gemm_nvfp4_call(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_srow,
                                     const uint8_t* w_codes, const uint8_t* w_sf, const float* w_st,
                                     const void* bias, void* Y, int64_t M, int64_t N, int64_t K,
-                                    void* stream, int withhold_kb, int64_t wait_limit_ns) {
+                                    void* stream, int withhold_kb, int64_t wait_limit_ns,
+                                    float* row_amax = nullptr, bool want_amax = false) {
     if (M < 0 || N < 0 || M > kMaxRows || N > kMaxRows || K <= 0 || K % 64 != 0 ||
         K > (1 << 24) || N % 8 != 0)
         return NVFP4_ERR_SHAPE;
-    if (M == 0 || N == 0) return NVFP4_OK;
-    if (!a_codes || !a_sf || !a_srow || !w_codes || !w_sf || !w_st || !Y) return NVFP4_ERR_NULL;
-    if (misaligned(a_codes, 16) || misaligned(a_sf, 16) || misaligned(w_codes, 16) ||
-        misaligned(w_sf, 16) || misaligned(Y, 16) || misaligned(a_srow, 4) ||
-        misaligned(w_st, 4) || (bias && misaligned(bias, 16)))
-        return NVFP4_ERR_ALIGN;
+    if (want_amax) {
+        if (M > 0 && row_amax == nullptr) return NVFP4_ERR_NULL;
+        if (misaligned(row_amax, 4)) return NVFP4_ERR_ALIGN;
+    }
+    if (M == 0) return NVFP4_OK;
+    if (N > 0) {
+        if (!a_codes || !a_sf || !a_srow || !w_codes || !w_sf || !w_st || !Y) return NVFP4_ERR_NULL;
+        if (misaligned(a_codes, 16) || misaligned(a_sf, 16) || misaligned(w_codes, 16) ||
+            misaligned(w_sf, 16) || misaligned(Y, 16) || misaligned(a_srow, 4) ||
+            misaligned(w_st, 4) || (bias && misaligned(bias, 16)))
+            return NVFP4_ERR_ALIGN;
+    }
     LaunchCtx ctx;
     nvfp4_status st = resolve(stream, &ctx);
     if (st != NVFP4_OK) return st;
+    if (want_amax) {
+        // The epilogue max-reduces into zeros (an empty row's amax is 0).
+        const cudaError_t e = cudaMemsetAsync(row_amax, 0, (size_t)M * sizeof(float), ctx.stream);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    if (N == 0) return NVFP4_OK;
     CUtensorMap ta, tb, tsa, tsb, ty;
     if (!encode_2d(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, a_codes, (uint64_t)K / 2, (uint64_t)M,
                    (uint64_t)K / 2, 128, 128) ||
@@ -310,7 +338,15 @@ static nvfp4_status gemm_nvfp4_call(const uint8_t* a_codes, const uint8_t* a_sf,
         return NVFP4_ERR_CUDA;
     return from_cuda(launch_gemm_nvfp4(ctx, ta, tb, tsa, tsb, ty, a_srow, w_st,
                                        static_cast<const __nv_bfloat16*>(bias), M, N, K, withhold_kb,
-                                       wait_limit_ns));
+                                       wait_limit_ns, want_amax ? row_amax : nullptr));
+}
+
+nvfp4_status nvfp4_gemm_rowamax(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_srow,
+                                const uint8_t* w_codes, const uint8_t* w_sf, const float* w_st,
+                                const void* bias, void* Y, float* y_row_amax, int64_t M, int64_t N,
+                                int64_t K, void* stream) {
+    return gemm_nvfp4_call(a_codes, a_sf, a_srow, w_codes, w_sf, w_st, bias, Y, M, N, K, stream, -1, 0,
+                           y_row_amax, true);
 }
 
 nvfp4_status nvfp4_gemm(const uint8_t* a_codes, const uint8_t* a_sf, const float* a_srow,

@@ -83,6 +83,8 @@ cudaError_t clusters_per_device(OccupancyCache& cache, const LaunchCtx& ctx, Ker
 // Implemented per translation unit; each returns cudaSuccess or the launch error.
 cudaError_t launch_act_quant(const LaunchCtx&, const __nv_bfloat16* X, int64_t M, int64_t K,
                              uint8_t* codes, uint8_t* sf, float* s_row);
+cudaError_t launch_act_quant_prescaled(const LaunchCtx&, const __nv_bfloat16* X, int64_t M, int64_t K,
+                                       const float* row_amax, uint8_t* codes, uint8_t* sf, float* s_row);
 cudaError_t launch_requant(const LaunchCtx&, const void* W, int w_dtype, const float* A,
                            const float* B, int r, float c, int64_t N, int64_t K, uint8_t* codes,
                            uint8_t* sf, float* s_t);
@@ -140,7 +142,7 @@ cudaError_t launch_gemm_nvfp4(const LaunchCtx&, const CUtensorMap& tmap_a,
                               const CUtensorMap& tmap_sfb, const CUtensorMap& tmap_y,
                               const float* a_srow, const float* w_st, const __nv_bfloat16* bias,
                               int64_t M, int64_t N, int64_t K, int withhold_kb = -1,
-                              int64_t wait_limit_ns = 0);
+                              int64_t wait_limit_ns = 0, float* row_amax = nullptr);
 cudaError_t launch_gemm_bf16(const LaunchCtx&, const CUtensorMap& tmap_a,
                              const CUtensorMap& tmap_b, const CUtensorMap& tmap_y,
                              const __nv_bfloat16* bias, int64_t M, int64_t N, int64_t K);

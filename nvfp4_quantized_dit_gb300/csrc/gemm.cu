@@ -126,6 +126,8 @@ struct GemmArgs {
     uint64_t wait_limit_ns;  // bound of every wait (kWaitLimitNs; shorter in the test hook)
     int withhold_kb;         // test hook only: K-stage whose loads the first pair's even CTA
                              // never issues (on its first tile), or -1
+    float* row_amax;         // optional: max |Y[m, :]| (of the bf16 values), atomicMax on the
+                             // fp32 bits into a zeroed [M] array; nullptr: not computed
 };
 
 // Pair tiles, grouped for L2 reuse: tiles are ordered in bands of kBandMp m-pairs
@@ -457,6 +459,7 @@ __global__ void __launch_bounds__(Cfg<kFP4>::kThreads, 1)
             tc_fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tmem_empty_even);
+            uint32_t ymax = 0u;  // largest bf16 magnitude of this row's 128 columns (bit pattern)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t packed[16];
@@ -473,6 +476,11 @@ __global__ void __launch_bounds__(Cfg<kFP4>::kThreads, 1)
                             fmaf(__uint_as_float(v[c][2 * i + 1]), scale,
                                  __uint_as_float(bw[u] & 0xFFFF0000u)));
                     }
+                }
+                if (args.row_amax != nullptr) {
+                    // Columns past N hold 0 (their accumulators and bias are 0).
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) ymax = __vmaxu2(ymax, packed[i] & 0x7FFF7FFFu);
                 }
                 // Row `lane` of the 32x32 bf16 chunk -> staging chunk, 16-byte pieces placed
                 // by the 64-byte swizzle of the Y tensor map (piece j of row r at
@@ -498,6 +506,11 @@ __global__ void __launch_bounds__(Cfg<kFP4>::kThreads, 1)
                     bulk_commit_group();
                 }
                 ++chunk_seq;
+            }
+            if (args.row_amax != nullptr && row < M) {
+                // |bf16| bit patterns order like the values; as fp32 (<< 16) too.
+                const uint32_t mx = max(ymax & 0xFFFFu, ymax >> 16);
+                if (mx != 0u) atomicMax(reinterpret_cast<unsigned int*>(args.row_amax + row), mx << 16);
             }
             acc_phase ^= 1u;
         }
@@ -564,16 +577,16 @@ cudaError_t launch_gemm_nvfp4(const LaunchCtx& ctx, const CUtensorMap& tmap_a,
                               const CUtensorMap& tmap_sfb, const CUtensorMap& tmap_y,
                               const float* a_srow, const float* w_st, const __nv_bfloat16* bias,
                               int64_t M, int64_t N, int64_t K, int withhold_kb,
-                              int64_t wait_limit_ns) {
+                              int64_t wait_limit_ns, float* row_amax) {
     GemmArgs a{a_srow, w_st, bias, (int)M, (int)N, (int)K, ctx.status,
-               wait_limit_ns > 0 ? (uint64_t)wait_limit_ns : kWaitLimitNs, withhold_kb};
+               wait_limit_ns > 0 ? (uint64_t)wait_limit_ns : kWaitLimitNs, withhold_kb, row_amax};
     return run_gemm<true>(ctx, tmap_a, tmap_b, tmap_sfa, tmap_sfb, tmap_y, a);
 }
 
 cudaError_t launch_gemm_bf16(const LaunchCtx& ctx, const CUtensorMap& tmap_a,
                              const CUtensorMap& tmap_b, const CUtensorMap& tmap_y,
                              const __nv_bfloat16* bias, int64_t M, int64_t N, int64_t K) {
-    GemmArgs a{nullptr, nullptr, bias, (int)M, (int)N, (int)K, ctx.status, kWaitLimitNs, -1};
+    GemmArgs a{nullptr, nullptr, bias, (int)M, (int)N, (int)K, ctx.status, kWaitLimitNs, -1, nullptr};
     return run_gemm<false>(ctx, tmap_a, tmap_b, tmap_a, tmap_b, tmap_y, a);
 }
 

@@ -120,15 +120,19 @@ __device__ __forceinline__ uint32_t bf16x16_absmax(const uint4& u0, const uint4&
     return *reinterpret_cast<const uint32_t*>(&m);
 }
 
-// kTensor: one scale for the whole tensor, s = amax / 2688 with amax read from
-// *s_row (written by act_amax_kernel); nothing is written to s_row.
+// kMode: how s is found.  kAqReduce: s = amax(|X[m,:]|) / 2688 from the row itself
+// (pass 1 below), written to s_row[m].  kAqGivenRow: the row's amax is read from
+// amax_in[m] (e.g. reduced by the epilogue of the GEMM that produced X), s written to
+// s_row[m].  kAqGivenTensor: one amax for the whole tensor, amax_in[0]; nothing is
+// written to s_row.
 // kBpt > 0: every thread has exactly kBpt blocks (K == 512 G kBpt), so the block
 // loops have fixed trip counts (no per-block bounds or exit tests, chains of
 // consecutive blocks interleaved); 0: any K, blocks counted at run time.
-template <int G, bool kTensor, int kBpt>
+enum { kAqReduce = 0, kAqGivenRow = 1, kAqGivenTensor = 2 };
+template <int G, int kMode, int kBpt>
 __global__ void __launch_bounds__(kAqWarps * 32)
     act_quant_kernel(const __nv_bfloat16* __restrict__ X, int64_t M, int64_t K, int64_t rows_pad,
-                     uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
+                     const float* __restrict__ amax_in, uint8_t* __restrict__ codes, uint8_t* __restrict__ sf,
                      float* __restrict__ s_row, int* status) {
     constexpr int kGroups = kAqWarps / G;
     constexpr int kThreadsPerRow = 32 * G;
@@ -164,9 +168,7 @@ __global__ void __launch_bounds__(kAqWarps * 32)
         }
     }
 
-    float s_all = 0.0f;
-    if (kTensor) s_all = __fdiv_rn(*reinterpret_cast<volatile const float*>(s_row), kAmaxDiv);
-
+    const float s_all = kMode == kAqGivenTensor ? __fdiv_rn(__ldg(amax_in), kAmaxDiv) : 0.0f;
     int slot = 0;
     uint32_t phase = 0;
     for (int64_t m = first; m < rows_pad; m += step) {
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(kAqWarps * 32)
             amax = fmaxf(amax, bm);
         }
         float s = s_all;
-        if (!kTensor) {
+        if (kMode == kAqReduce) {
             amax = warp_max(amax);
             if (G > 1) {
                 if (lane == 0) red[warp] = amax;
@@ -202,8 +204,10 @@ __global__ void __launch_bounds__(kAqWarps * 32)
                 for (int w = 0; w < G; ++w) amax = fmaxf(amax, red[group * G + w]);
             }
             s = __fdiv_rn(amax, kAmaxDiv);
-            if (valid && t == 0) s_row[m] = s;
+        } else if (kMode == kAqGivenRow) {
+            s = valid ? __fdiv_rn(__ldg(amax_in + m), kAmaxDiv) : 0.0f;
         }
+        if (kMode != kAqGivenTensor && valid && t == 0) s_row[m] = s;
         const float d = __fmul_rn(6.0f, s);
         const bool d_fast = fast_recip_ok(d);
         const float inv_d = d_fast ? recip_approx(d) : 0.0f;
@@ -258,19 +262,19 @@ __global__ void __launch_bounds__(kAqWarps * 32)
     }
 }
 
-template <int G, bool kTensor, int kBpt = 0>
+template <int G, int kMode, int kBpt = 0>
 cudaError_t run_act_quant(const LaunchCtx& ctx, const __nv_bfloat16* X, int64_t M, int64_t K,
-                          int64_t rows_pad, uint8_t* codes, uint8_t* sf, float* s_row) {
+                          int64_t rows_pad, const float* amax_in, uint8_t* codes, uint8_t* sf, float* s_row) {
     const size_t smem = (size_t)(kAqWarps / G) * kAqRing * (size_t)K * 2;
     static OccupancyCache occupancy;
     int per_sm = 0;
     const cudaError_t e =
-        blocks_per_sm(occupancy, ctx, act_quant_kernel<G, kTensor, kBpt>, kAqWarps * 32, smem, &per_sm);
+        blocks_per_sm(occupancy, ctx, act_quant_kernel<G, kMode, kBpt>, kAqWarps * 32, smem, &per_sm);
     if (e != cudaSuccess) return e;
     int64_t grid = (rows_pad + (kAqWarps / G) - 1) / (kAqWarps / G);
     if (grid > (int64_t)ctx.num_sms * per_sm) grid = (int64_t)ctx.num_sms * per_sm;
-    act_quant_kernel<G, kTensor, kBpt><<<(unsigned)grid, kAqWarps * 32, smem, ctx.stream>>>(
-        X, M, K, rows_pad, codes, sf, s_row, ctx.status);
+    act_quant_kernel<G, kMode, kBpt><<<(unsigned)grid, kAqWarps * 32, smem, ctx.stream>>>(
+        X, M, K, rows_pad, amax_in, codes, sf, s_row, ctx.status);
     return cudaGetLastError();
 }
 
@@ -456,20 +460,6 @@ __device__ __forceinline__ void rq_copy_b(const RqArgs& a, int lane, int64_t row
         }
     }
     asm volatile("cp.async.commit_group;" ::: "memory");
-}
-
-// Bs (row-major) -> Bt[j][row].  Lane l moves row l % 16, steps j = 8 t + 4 (l / 16)
-// .. +3: one 16-byte load and four 4-byte stores, the stores of a warp instruction
-// covering 32 distinct banks.  Entries past r hold copies of the row padding.
-__device__ __forceinline__ void rq_transpose_b(const RqArgs& a, int lane, const float* Bs, float* Bt) {
-    const int rl = lane & 15, jq = (lane >> 4) * 4;
-    for (int j4 = jq; j4 < a.r; j4 += 8) {
-        const float4 v = *reinterpret_cast<const float4*>(Bs + rl * a.rs + j4);
-        Bt[(j4 + 0) * kRqBtStride + rl] = v.x;
-        Bt[(j4 + 1) * kRqBtStride + rl] = v.y;
-        Bt[(j4 + 2) * kRqBtStride + rl] = v.z;
-        Bt[(j4 + 3) * kRqBtStride + rl] = v.w;
-    }
 }
 
 __device__ __forceinline__ void rq_commit_empty() { asm volatile("cp.async.commit_group;" ::: "memory"); }
@@ -1098,28 +1088,40 @@ unsigned grid_for(int64_t n, const LaunchCtx& ctx) {
     return (unsigned)(g < 1 ? 1 : (g > cap ? cap : g));
 }
 
+// G warps per row: the fewest that keep a thread at kAqMaxBpt blocks of 16 or less;
+// for K a multiple of 512 up to 4096, one warp per row with a fixed block count.
+template <int kMode>
+cudaError_t dispatch_act_quant(const LaunchCtx& ctx, const __nv_bfloat16* X, int64_t M, int64_t K,
+                               const float* amax_in, uint8_t* codes, uint8_t* sf, float* s_row) {
+    const int64_t rows_pad = (M + 127) / 128 * 128;
+    if (K <= 4096 && K % 512 == 0) {
+        switch (K / 512) {
+            case 1: return run_act_quant<1, kMode, 1>(ctx, X, M, K, rows_pad, amax_in, codes, sf, s_row);
+            case 2: return run_act_quant<1, kMode, 2>(ctx, X, M, K, rows_pad, amax_in, codes, sf, s_row);
+            case 3: return run_act_quant<1, kMode, 3>(ctx, X, M, K, rows_pad, amax_in, codes, sf, s_row);
+            case 4: return run_act_quant<1, kMode, 4>(ctx, X, M, K, rows_pad, amax_in, codes, sf, s_row);
+            case 5: return run_act_quant<1, kMode, 5>(ctx, X, M, K, rows_pad, amax_in, codes, sf, s_row);
+            case 6: return run_act_quant<1, kMode, 6>(ctx, X, M, K, rows_pad, amax_in, codes, sf, s_row);
+            case 7: return run_act_quant<1, kMode, 7>(ctx, X, M, K, rows_pad, amax_in, codes, sf, s_row);
+            default: return run_act_quant<1, kMode, 8>(ctx, X, M, K, rows_pad, amax_in, codes, sf, s_row);
+        }
+    }
+    if (K <= 4096) return run_act_quant<1, kMode>(ctx, X, M, K, rows_pad, amax_in, codes, sf, s_row);
+    if (K <= 8192) return run_act_quant<2, kMode>(ctx, X, M, K, rows_pad, amax_in, codes, sf, s_row);
+    if (K <= 16384) return run_act_quant<4, kMode>(ctx, X, M, K, rows_pad, amax_in, codes, sf, s_row);
+    return run_act_quant<8, kMode>(ctx, X, M, K, rows_pad, amax_in, codes, sf, s_row);
+}
+
 }  // namespace
 
 cudaError_t launch_act_quant(const LaunchCtx& ctx, const __nv_bfloat16* X, int64_t M, int64_t K,
                              uint8_t* codes, uint8_t* sf, float* s_row) {
-    const int64_t rows_pad = (M + 127) / 128 * 128;
-    // G warps per row: the fewest that keep a thread at kAqMaxBpt blocks of 16 or less.
-    if (K <= 4096 && K % 512 == 0) {
-        switch (K / 512) {  // one warp per row, a fixed number of blocks per thread
-            case 1: return run_act_quant<1, false, 1>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-            case 2: return run_act_quant<1, false, 2>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-            case 3: return run_act_quant<1, false, 3>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-            case 4: return run_act_quant<1, false, 4>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-            case 5: return run_act_quant<1, false, 5>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-            case 6: return run_act_quant<1, false, 6>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-            case 7: return run_act_quant<1, false, 7>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-            default: return run_act_quant<1, false, 8>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-        }
-    }
-    if (K <= 4096) return run_act_quant<1, false>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-    if (K <= 8192) return run_act_quant<2, false>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-    if (K <= 16384) return run_act_quant<4, false>(ctx, X, M, K, rows_pad, codes, sf, s_row);
-    return run_act_quant<8, false>(ctx, X, M, K, rows_pad, codes, sf, s_row);
+    return dispatch_act_quant<kAqReduce>(ctx, X, M, K, nullptr, codes, sf, s_row);
+}
+
+cudaError_t launch_act_quant_prescaled(const LaunchCtx& ctx, const __nv_bfloat16* X, int64_t M, int64_t K,
+                                       const float* row_amax, uint8_t* codes, uint8_t* sf, float* s_row) {
+    return dispatch_act_quant<kAqGivenRow>(ctx, X, M, K, row_amax, codes, sf, s_row);
 }
 
 cudaError_t launch_act_quant_tensor(const LaunchCtx& ctx, const __nv_bfloat16* X, int64_t M, int64_t K,
@@ -1132,11 +1134,8 @@ cudaError_t launch_act_quant_tensor(const LaunchCtx& ctx, const __nv_bfloat16* X
     act_amax_kernel<<<(unsigned)grid, kAmaxThreads, 0, ctx.stream>>>(reinterpret_cast<const uint4*>(X), n_vec,
                                                                      s_t);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const int64_t rows_pad = (M + 127) / 128 * 128;
-    if (K <= 4096) e = run_act_quant<1, true>(ctx, X, M, K, rows_pad, codes, sf, s_t);
-    else if (K <= 8192) e = run_act_quant<2, true>(ctx, X, M, K, rows_pad, codes, sf, s_t);
-    else if (K <= 16384) e = run_act_quant<4, true>(ctx, X, M, K, rows_pad, codes, sf, s_t);
-    else e = run_act_quant<8, true>(ctx, X, M, K, rows_pad, codes, sf, s_t);
+    // Pass 2 with the tensor's amax (still in *s_t); then s_t = amax / 2688.
+    e = dispatch_act_quant<kAqGivenTensor>(ctx, X, M, K, s_t, codes, sf, nullptr);
     if (e != cudaSuccess) return e;
     act_scale_kernel<<<1, 1, 0, ctx.stream>>>(s_t);
     return cudaGetLastError();

@@ -203,3 +203,18 @@ def test_requant_exact_counts_validation(lib):
     assert f(P(A16), need - 1, 256, 1024, out, None) == 2        # too small
     assert f(P(A16), need, 256, 100, out, None) == 2             # K % 64
     assert f(P(A16), need, 0, 1024, out, None) == 2
+
+
+def test_prescaled_and_rowamax_validation(lib):
+    P = ctypes.c_void_p
+    f = lib.nvfp4_act_quant_prescaled
+    assert f(P(A16), 4, 100, P(A16), P(A16), P(A16), P(A16), None) == 2     # K % 64
+    assert f(P(A16), 4, 64, None, P(A16), P(A16), P(A16), None) == 1        # row_amax
+    assert f(P(A16), 4, 64, P(BAD), P(A16), P(A16), P(A16), None) == 3
+    assert f(None, 0, 64, None, None, None, None, None) == 0                # nothing to do
+    g = lib.nvfp4_gemm_rowamax
+    ok = [P(A16)] * 8
+    assert g(*ok, None, 4, 256, 256, None) == 1                              # y_row_amax
+    assert g(*ok, P(BAD), 4, 256, 256, None) == 3
+    assert g(*ok, P(A16), 4, 256, 100, None) == 2
+    assert g(*ok, None, 0, 256, 256, None) == 0                              # M == 0

@@ -86,7 +86,8 @@ def test_report_line_has_the_contract_keys():
     clk = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "samples": 5, "reasons": []}
     out = bench.report(args, cfg, rcfg, None, per, 22.0, 50.0, 304, 906, 0, clk, 1, 0,
                        {"nvfp4_requant": 3, "nvfp4_act_quant": 1, "nvfp4_gemm": 1, "bf16_gemm": 1,
-                        "select_contrastive": 2}, 0.12, {})
+                        "select_contrastive": 2}, 0.12, {},
+                       {"act_quant_prescaled": 0.05, "nvfp4_gemm_rowamax": 0.51})
     for k in ["metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
               "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "e2e", "gpu_launches",
               "clocks"]:
@@ -99,8 +100,11 @@ def test_report_line_has_the_contract_keys():
     assert abs(out["roofline"]["frac"] - out["roofline"]["achieved"] / out["roofline"]["peak"]) < 1e-3
     assert out["e2e"]["h2d_bytes_per_step"] == 304 and out["e2e"]["ms_per_step"] == 5.0
     assert out["variants"]["act_quant_per_tensor"]["ms"] == 0.12
+    ab = bench.algorithmic_bytes(cfg)["act_quant_prescaled"]
+    assert abs(out["variants"]["act_quant_prescaled"]["gbs"] - ab / 0.05e-3 / 1e9) < 0.1
     small = argparse.Namespace(**{**vars(args), "rows": 8192})
-    out2 = bench.report(small, cfg, rcfg, None, per, 22.0, 50.0, 304, 906, 0, clk, 1, 0, {}, 0.12, {})
+    out2 = bench.report(small, cfg, rcfg, None, per, 22.0, 50.0, 304, 906, 0, clk, 1, 0, {}, 0.12, {},
+                        {"act_quant_prescaled": 0.05, "nvfp4_gemm_rowamax": 0.51})
     assert all(r["traffic"] is None for r in out2["rooflines"].values())  # no capture of that workload
 
 
