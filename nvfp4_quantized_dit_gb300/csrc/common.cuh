@@ -393,6 +393,15 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parit
     return done != 0;
 }
 
+// A flag that another thread may raise at any time, read so that the whole warp agrees
+// (set if any lane saw it set).  Per-lane reads of such a flag must never steer a warp's
+// lanes down different paths ahead of a warp-collective operation (__all_sync, a
+// shuffle, tcgen05.ld/st): the lanes would then wait at different collectives.
+__device__ __forceinline__ bool warp_flag(const volatile int* f) { return __any_sync(0xFFFFFFFFu, *f != 0); }
+__device__ __forceinline__ bool warp_flag(const volatile unsigned int* f) {
+    return __any_sync(0xFFFFFFFFu, *f != 0u);
+}
+
 // Waits for the phase of `bar` with the given parity to complete, for at most
 // limit_ns of device time.  On expiry it records NVFP4_ERR_TIMEOUT in *status,
 // raises the CTA's abort flag (so the CTA's other waits give up at once) and

@@ -856,10 +856,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             return 1;
         };
         int resume = -1;
-        for (int i = 0; !*abort_flag; ++i) {
+        // Loop conditions are voted on by the warp (warp_flag): amax_tile is collective.
+        for (int i = 0; !warp_flag(abort_flag); ++i) {
             const int r = amax_tile(i, false);
             if (r == 0) break;
-            if (r == 2 || *reinterpret_cast<volatile unsigned int*>(p0_overflow) != 0u) {
+            if (r == 2 || warp_flag(reinterpret_cast<volatile unsigned int*>(p0_overflow))) {
                 resume = r == 2 ? i : i + 1;
                 break;
             }
@@ -868,10 +869,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Slow mode (the queue filled, in this warp or another): from the tile that
             // overflowed (or the next one), candidates are merged in place.
             __syncwarp();
-            for (int i = resume; !*abort_flag; ++i)
+            for (int i = resume; !warp_flag(abort_flag); ++i)
                 if (amax_tile(i, true) == 0) break;
         }
-        if (*abort_flag) alive = false;
+        if (warp_flag(abort_flag)) alive = false;
         if (alive) {
             // ---- between the phases.  First the queued amax candidates (elements
             // whose bound reached the running threshold when their chunk was read):
@@ -918,7 +919,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(amax_ready);
             }
             const bool ok = mbar_wait(amax_ready, 0, args.status, abort_flag, kWaitLimitNs);
-            if (!__all_sync(0xFFFFFFFFu, ok) || *abort_flag) alive = false;
+            if (!__all_sync(0xFFFFFFFFu, ok) || warp_flag(abort_flag)) alive = false;
             const float amax = *amax_smem;
             s = __fdiv_rn(amax, kAmaxDiv);
             d = __fmul_rn(6.0f, s);
@@ -934,7 +935,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         // ---- quantize phase: tile j of the pair (walked backwards)
-        for (int j = 0; alive && j < seq.T && !*abort_flag; ++j) {
+        for (int j = 0; alive && j < seq.T && !warp_flag(abort_flag); ++j) {
             const int i = F + j;
             const int ws = i % kWSlots;
             const uint8_t* wt = wring + ws * kWBytes;  // this tile's W, held until its end

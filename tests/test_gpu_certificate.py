@@ -131,6 +131,21 @@ def build_amax_case(N, K, seed):
     return Wb, torch.from_numpy(A.astype(np.float32)), torch.from_numpy(B.astype(np.float32))
 
 
+def build_amax_flood_case(N, K, seed):
+    """Every |W| within 3 bf16 steps of the top (0.5 - j 2^-9, j = 0..3) and a LoRA
+    term whose bound spans about two of those steps: most elements stay candidates for
+    the tensor amax to the end, so every CTA's candidate queue overflows and the amax
+    phase finishes in its slow mode (candidates merged where they are found)."""
+    rng = np.random.default_rng(seed)
+    j = rng.integers(0, 4, (N, K))
+    W = (0.5 - j * 2.0 ** -9) * rng.choice([-1.0, 1.0], (N, K))
+    A = rng.standard_normal((R, K)) / 32
+    B = rng.standard_normal((N, R)) * (2.0 ** -8 / 1.4)
+    c = workloads.LORA_ALPHA / R
+    B /= c
+    return _bf16(W), torch.from_numpy(A.astype(np.float32)), torch.from_numpy(B.astype(np.float32))
+
+
 def _ulps(x, target):
     """|x - target| in fp32 ulps of x (x float32, target float64)."""
     return np.abs(x.astype(np.float64) - target) / np.spacing(np.abs(x)).astype(np.float64)
@@ -218,3 +233,13 @@ def test_certificate_amax_competitors(orc, seed):
           f"exact chain: {xa} amax candidates, {xq} quantize-phase elements")
     assert spread <= 1024, spread
     assert xa > 0, "the amax candidates must have been merged exactly"
+
+
+@pytest.mark.parametrize("N,K,seed", [(1024, 3072, 0), (520, 2240, 1), (256, 12288, 2)])
+def test_certificate_amax_queue_overflow(orc, N, K, seed):
+    """The amax phase's slow mode: thousands of candidates per CTA."""
+    require_gpu()
+    W, A, B = build_amax_flood_case(N, K, seed)
+    (xq, xa), wp, osf, os_ = _run(orc, W, A, B)
+    print(f"\n[amax flood N={N} K={K} seed={seed}] exact chain: {xa} amax candidates, {xq} quantize-phase elements")
+    assert xa > 512 * 4, "the candidate queues must have overflowed"
