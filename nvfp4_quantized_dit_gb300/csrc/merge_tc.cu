@@ -43,16 +43,18 @@
 // Kernels.  A split kernel writes A' = [a0 a1 a0 a1] per column of A (bf16, 256 bytes
 // per row) into the caller's workspace, with upper bounds of every row norm of B and,
 // per 64 columns, of the largest column norm of A.  Then one persistent kernel on
-// clusters of two CTAs (one per SM, every CTA resident) runs both phases over the same
-// tiles: the amax phase reads W from HBM, keeping it in L2; a grid-wide barrier (a
+// clusters of two CTAs (one per SM, every CTA resident) runs both phases: the amax phase
+// streams W from HBM in contiguous chunks of up to 32 KB (each CTA its first five by
+// index, the rest claimed from a counter), keeping it in L2; a grid-wide barrier (a
 // counter in the workspace, bounded wait) gathers every CTA's contribution to the
-// tensor amax; the quantize phase walks the tiles in reverse order, reading W back from
-// L2.  Only the epilogue waits at the barrier: the copies and MMAs of the first
+// tensor amax; the quantize phase walks its pair's 256 x 128 tiles, reading W back
+// from L2.  Only the epilogue waits at the barrier: the copies and MMAs of the first
 // quantize-phase tiles run ahead.  A pair tile is 256 weight rows (128 per CTA) x 128
 // columns, walked k-strip first, so the rows of B usually stay the same from one tile
 // to the next.  Per CTA, 20 warps:
-//   warp 0      TMA: W tiles (128 x 128 bf16; 5 slots), each freed when the epilogue is
-//               done with the tile;
+//   warp 0      copies of W into 5 slots of 32 KB, each freed when the epilogue is done
+//               with it: amax-phase chunks (bulk copies, with the row norms of the rows
+//               they touch), then quantize-phase tiles (128 x 128 bf16, tensor copies);
 //   warp 1      tensor-memory allocation; lane 0 of the even CTA issues the 8 pair MMAs
 //               (kind::f16, M = 256, N = 128, A from tensor memory) into a
 //               double-buffered accumulator;
@@ -60,7 +62,8 @@
 //               completing on the even CTA's barrier, freed by the MMAs;
 //   warp 3      idle;
 //   warps 4-19  epilogue: four warps per tensor-memory lane quarter, 32 columns each (a
-//               thread owns one weight row): W (amax phase) or accumulator + W -> w~
+//               thread owns one weight row in the quantize phase, 32 consecutive weights
+//               of a chunk in the amax phase): W (amax phase) or accumulator + W -> w~
 //               (quantize phase) -> the amax bound or codes and scales, stored straight
 //               to global memory.
 // The rows of B live in tensor memory next to the accumulators (lane = row), in two
@@ -94,9 +97,14 @@ constexpr int kStatic = kWSlots;  // amax tiles a CTA takes by index (the rest f
 constexpr uint32_t kDeferBytes = kDefer * 16;  // (tile, element mask, row | chunk | flags, task base)
 constexpr int kTasks = 1024;  // exact values computed for the deferred entries (one per element)
 constexpr uint32_t kTaskBytes = kTasks * (2 + 4);  // task (entry << 5 | column) and its exact value
-// Per W slot, the tile's bounds: the 128 row norms of this CTA's rows of B and the 4
-// column-norm entries of the tile's 128-column strip (bulk copies beside the W tile).
-constexpr uint32_t kSideBytes = kTM * 4 + 16;
+// Per W slot, the tile's bounds (bulk copies beside the W tile).  Quantize phase: the
+// 128 row norms of this CTA's rows of B and the 4 column-norm entries of the tile's
+// 128-column strip (kSideQBytes).  Amax phase: the row norms of the rows the chunk
+// touches (at most kChunkRows + 2, from a 16-byte aligned row on).
+constexpr uint32_t kSideQBytes = kTM * 4 + 16;
+constexpr int kChunkRows = 128;  // a chunk spans at most this many whole rows
+constexpr uint32_t kSideBytes = (kChunkRows + 2 + 3 + 3) / 4 * 16;  // 544
+static_assert(kSideBytes >= kSideQBytes && kSideBytes % 16 == 0, "side area");
 constexpr uint32_t kSmemBytes =
     1024 + kOpSlots * kOpBBytes + kWSlots * kWBytes + kWSlots * kSideBytes + kDeferBytes + kTaskBytes + kMiscBytes;
 // Tensor memory: two accumulators of 128 columns, then two row buffers of 64 columns of
@@ -140,7 +148,8 @@ struct TcArgs {
     unsigned int* counter;  // CTAs that are done (zeroed by the split)
     unsigned int* arrive;   // CTAs past the amax phase: the grid barrier (zeroed by the split)
     unsigned int* next;     // the amax phase's next dynamically taken tile (zeroed by the split)
-    int units;              // amax-phase tiles: ceil(N / 128) x nks (128 rows x 128 columns)
+    int units;              // amax-phase chunks: ceil(N K / chunk) contiguous pieces of W
+    int chunk;              // elements per amax chunk: min(16384, 128 K) (at most 32 KB)
     int* status;
     int zero;    // 0 (a value the compiler cannot see; used for data dependencies)
     int nks;     // 128-column strips
@@ -492,18 +501,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* tasks_ready = loop_done + 1;           // ... listed the deferred elements
     uint64_t* vals_ready = tasks_ready + 1;          // ... computed their exact values
     uint64_t* cand_done = vals_ready + 1;            // ... queued their amax candidates
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(cand_done + 1);
+    uint64_t* ra_ready = cand_done + 1;              // ... contributed to ra_all
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ra_ready + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile float* amax_smem = reinterpret_cast<volatile float*>(tmem_slot + 2);
     unsigned int* defn = tmem_slot + 3;              // entries pushed to defq
     unsigned int* ntask = tmem_slot + 4;             // elements claimed in task_id (may pass kTasks)
     unsigned int* p0_overflow = tmem_slot + 5;       // the amax phase's queue overflowed
     unsigned int* p1_overflow = tmem_slot + 6;       // the quantize phase's queue overflowed
-    volatile int* slot_unit = reinterpret_cast<volatile int*>(tmem_slot + 7);  // [kWSlots] amax tile per slot
+    volatile int* slot_unit = reinterpret_cast<volatile int*>(tmem_slot + 7);  // [kWSlots] amax chunk per slot
     unsigned int* xcount = tmem_slot + 7 + kWSlots;  // [2] exact merges: quantize (whole blocks), amax
     // The end of the listed tasks: the entries that fit occupy task_id[0, nfill) (the
     // first entry that does not fit, and every later one, claims past kTasks).
     unsigned int* nfill = tmem_slot + 9 + kWSlots;
+    volatile int* slot_n0 = reinterpret_cast<volatile int*>(tmem_slot + 10 + kWSlots);  // [kWSlots] chunk's row
+    volatile int* slot_r0 = slot_n0 + kWSlots;  // [kWSlots] and column of its first element
+    float* ra_all = reinterpret_cast<float*>(tmem_slot + 10 + 3 * kWSlots);  // max_k ||A[:,k]|| bound
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -540,6 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(tasks_ready, kEpiWarps);
         mbar_init(vals_ready, kEpiWarps);
         mbar_init(cand_done, kEpiWarps);
+        mbar_init(ra_ready, kEpiWarps);
         *abort_flag = 0;
         *amax_smem = 0.0f;
         *defn = 0u;
@@ -549,6 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         xcount[0] = 0u;
         xcount[1] = 0u;
         *nfill = 0u;
+        *ra_all = 0.0f;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) prefetch_tmap(&tmap_w);
@@ -568,20 +583,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         if (lane == 0) {
             // ------------------------------------------------ TMA: W
-            // The amax phase's tiles are kept in L2 (evict_last) for the quantize phase,
-            // which lets them go (evict_first).  Each W slot also receives the tile's
-            // bounds (row and column norms, written by the split kernel): the first
-            // kStatic tiles' W is requested at once, their bounds once the split kernel is
+            // Amax phase: contiguous chunks of W (args.chunk elements, one bulk copy each),
+            // kept in L2 (evict_last) for the quantize phase, whose 128 x 128 tiles (tensor
+            // copies) let them go (evict_first).  Each W slot also receives bounds written by
+            // the split kernel: for a chunk, the row norms of the rows it touches; the first
+            // kStatic chunks are requested at once, their bounds once the split kernel is
             // done.
             const uint64_t keep = l2_policy_evict_last(), drop = l2_policy_evict_first();
             const int G = (int)gridDim.x;
+            const int64_t NK = (int64_t)args.N * args.K;
+            const int rows_pad256 = (args.N + 255) / 256 * 256;
             int i = 0, nstatic = 0;
             bool ended = false;
-            auto issue_w = [&](int ws, int u, uint64_t pol) {
-                uint8_t* wt = wring + ws * kWBytes;
-                const int row0 = (u / nks) * kTM, x0 = (u - (u / nks) * nks) * kTK;
-                tma_load_2d_hint(&tmap_w, &w_full[ws], wt, x0, row0, pol);
-                tma_load_2d_hint(&tmap_w, &w_full[ws], wt + kWBox, x0 + 64, row0, pol);
+            uint32_t side_bytes[kStatic];
+            // Requests chunk u into slot ws; returns the bytes of its row-norm slice.
+            auto issue_w = [&](int ws, int u) -> uint32_t {
+                const int64_t e0 = (int64_t)u * args.chunk;
+                const uint32_t bytes = (uint32_t)min((int64_t)args.chunk, NK - e0) * 2u;
+                const int n0 = (int)(e0 / args.K);
+                const int n_last = (int)((e0 + bytes / 2 - 1) / args.K);
+                const int n0a = n0 & ~3;
+                const uint32_t sb = (uint32_t)min((n_last - n0a + 4) & ~3, rows_pad256 - n0a) * 4u;
+                slot_unit[ws] = u;
+                slot_n0[ws] = n0;
+                slot_r0[ws] = (int)(e0 - (int64_t)n0 * args.K);
+                mbar_arrive_expect_tx(&w_full[ws], bytes + sb);
+                bulk_load_hint(wring + ws * kWBytes, args.W + e0, bytes, &w_full[ws], keep);
+                return sb;
+            };
+            auto issue_side_rows = [&](int ws, uint32_t sb) {
+                bulk_load(side + ws * kSideBytes, args.rnorm + (slot_n0[ws] & ~3), sb, &w_full[ws]);
             };
             auto issue_side = [&](int ws, int row0, int ks) {
                 uint8_t* sd = side + ws * kSideBytes;
@@ -596,17 +627,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(&w_full[i]);
                     ended = true;
                 } else {
-                    slot_unit[i] = u;
-                    mbar_arrive_expect_tx(&w_full[i], kWBytes + kSideBytes);
-                    issue_w(i, u, keep);
+                    side_bytes[i] = issue_w(i, u);
                     ++nstatic;
                 }
             }
-            grid_dep_wait();  // the norms and the tile counter are written by the split kernel
-            for (int z = 0; z < nstatic; ++z) {
-                const int u = (int)blockIdx.x + z * G;
-                issue_side(z, (u / nks) * kTM, u - (u / nks) * nks);
-            }
+            grid_dep_wait();  // the norms and the chunk counter are written by the split kernel
+            for (int z = 0; z < nstatic; ++z) issue_side_rows(z, side_bytes[z]);
             // Each unit is claimed before its slot is free (the claim's round trip overlaps
             // the wait).
             int u_next = ended ? args.units : kStatic * G + (int)atomicAdd(args.next, 1u);
@@ -622,10 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(&w_full[ws]);
                     ended = true;
                 } else {
-                    slot_unit[ws] = u;
-                    mbar_arrive_expect_tx(&w_full[ws], kWBytes + kSideBytes);
-                    issue_w(ws, u, keep);
-                    issue_side(ws, (u / nks) * kTM, u - (u / nks) * nks);
+                    issue_side_rows(ws, issue_w(ws, u));
                 }
             }
             // i = the amax iterations, the sentinel's included; the quantize phase's
@@ -639,7 +662,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nb = t / nks, ks = t - nb * nks;
                 const int row0 = nb * (kTM * kPair) + (int)rank * kTM;
                 // A quantize-phase tile of W (from L2), and its bounds.
-                mbar_arrive_expect_tx(&w_full[ws], kWBytes + kSideBytes);
+                mbar_arrive_expect_tx(&w_full[ws], kWBytes + kSideQBytes);
                 tma_load_2d_hint(&tmap_w, &w_full[ws], wring + ws * kWBytes, ks * kTK, row0, drop);
                 tma_load_2d_hint(&tmap_w, &w_full[ws], wring + ws * kWBytes + kWBox, ks * kTK + 64, row0, drop);
                 issue_side(ws, row0, ks);
@@ -752,22 +775,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         int nrb = 0;           // row buffers written
         grid_dep_wait();       // the split kernel's results (norms, s_t, the counters)
         // In the amax phase, the running lower bound of the tensor amax (any value s_t has
-        // held is one), read at the end of a tile for use in the next.
-        float st_now = 0.0f, st_next = 0.0f;
+        // held is one), read before each tile's wait for its data (the load's round trip
+        // overlaps the wait).
+        float st_now = 0.0f;
         int cur_buf = 0;  // row buffer of the current tile's row block (quantize phase)
         bool alive = true;
-        // ---- amax phase: one tile per W slot until the sentinel (unit -1).  Thread (q,
-        // chunk, lane) takes its 32 weights of the tile (row n, columns k0 ..).  With the
-        // tile's bounds rb >= ||B[n,:]|| and ra >= max ||A[:,k]|| every |w'| lies within
+        // ---- amax phase: one chunk of W per slot until the sentinel (unit -1).  Thread
+        // et takes the chunk's elements 32 et .. 32 et + 31 (row n, columns k0 ..; K is a
+        // multiple of 64, so they never straddle a row).  With rb >= ||B[n,:]|| (the
+        // slot's row norms) and ra >= max_k ||A[:,k]|| every |w'| lies within
         //   Ecs = |c| rb ra (1 + 2^-17) + 2^-126
         // of |W| (Cauchy-Schwarz; the slack covers the chain's rounding, the final fma's
         // beyond 2^-23 |W|, and subnormal roundings).
+        {
+            // ra: the largest column-norm entry (the split kernel wrote one per 64 columns).
+            float m = 0.0f;
+            for (int i = et; i < args.K / 64; i += kEpiWarps * 32) m = fmaxf(m, args.cnorm[(i >> 1) * 4 + (i & 1)]);
+            m = warp_max_f(m);
+            if (lane == 0) {
+                atomicMax(reinterpret_cast<unsigned int*>(ra_all), __float_as_uint(m));
+                mbar_arrive(ra_ready);
+            }
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait(ra_ready, 0, args.status, abort_flag, kWaitLimitNs))) alive = false;
+        }
+        const float ra = *reinterpret_cast<volatile float*>(ra_all);
         int F = 0;                            // amax iterations, the sentinel's included
         float seed_U = -1.0f, seed_E = 0.0f;  // the first tile's largest bound and Ecs
         int seed_n = 0, seed_k0 = 0;
         auto amax_tile = [&](int i, bool slow_mode) -> int {  // 0: phase over, 1: done, 2: redo
             const int ws = i % kWSlots;
             const uint8_t* wt = wring + ws * kWBytes;  // this tile's W, held until its end
+            const float st_pre = *reinterpret_cast<volatile const float*>(args.s_t);
             bool ok = mbar_wait(&w_full[ws], (uint32_t)((i / kWSlots) & 1), args.status, abort_flag, kWaitLimitNs);
             if (!__all_sync(0xFFFFFFFFu, ok)) return 0;
             const int u = slot_unit[ws];
@@ -777,18 +815,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 F = i + 1;
                 return 0;
             }
-            const int n = (u / nks) * kTM + rloc;
-            const int k0 = (u - (u / nks) * nks) * kTK + kt0;
-            const bool in = n < args.N && k0 < args.K;
-            const float rb = reinterpret_cast<const float*>(side + ws * kSideBytes)[rloc];
-            const float ra = reinterpret_cast<const float*>(side + ws * kSideBytes + kTM * 4)[(k0 >> 6) & 1];
+            const int n0 = slot_n0[ws];
+            const int off = slot_r0[ws] + 32 * et;  // < K + chunk
+            const int q = off / args.K;
+            const int n = n0 + q;
+            const int k0 = off - q * args.K;
+            const bool in = 32 * et < args.chunk && (int64_t)u * args.chunk + 32 * et < (int64_t)args.N * args.K;
+            const float rb = in ? reinterpret_cast<const float*>(side + ws * kSideBytes)[n - (n0 & ~3)] : 0.0f;
             const float Ecs = __fadd_ru(__fmul_ru(__fmul_ru(ac, __fmul_ru(rb, ra)), 1.0f + 0x1p-17f), 0x1p-126f);
             uint4 wr[4];
             {
-                const uint8_t* wb = wt + (kt0 >> 6) * kWBox + rloc * 128;
-                const int u0 = (kt0 & 63) >> 3;
+                const uint4* wb = reinterpret_cast<const uint4*>(wt) + 4 * et;
 #pragma unroll
-                for (int z = 0; z < 4; ++z) wr[z] = *reinterpret_cast<const uint4*>(wb + (((u0 + z) ^ (rloc & 7)) << 4));
+                for (int z = 0; z < 4; ++z) wr[z] = wb[z];
             }
             uint32_t mx = 0u;  // bf16 magnitudes order like their bit patterns
 #pragma unroll
@@ -801,7 +840,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float mW = in ? __uint_as_float(max(mx & 0xFFFFu, mx >> 16) << 16) : 0.0f;
             // A lower bound of the tensor amax from this warp's weights.
             const float lo = warp_max_f(fmaxf(__fsub_rd(__fmul_rd(mW, 1.0f - 0x1p-23f), Ecs), 0.0f));
-            st_now = fmaxf(st_now, st_next);
+            st_now = fmaxf(st_now, st_pre);
             const float thr = fmaxf(lo, st_now);
             const float U_t = __fadd_ru(__fmul_ru(mW, 1.0f + 0x1p-23f), Ecs);
             // Only weights with |W| + Ecs at the threshold can be the maximum: queued for
@@ -850,14 +889,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // |W'| >= 0: the fp32 bit patterns order like the values.
             if (lane == 0 && lo > st_now) atomicMax(reinterpret_cast<unsigned int*>(args.s_t), __float_as_uint(lo));
-            st_next = *reinterpret_cast<volatile const float*>(args.s_t);
             __syncwarp();
             if (lane == 0) mbar_arrive(&w_empty[ws]);
             return 1;
         };
         int resume = -1;
         // Loop conditions are voted on by the warp (warp_flag): amax_tile is collective.
-        for (int i = 0; !warp_flag(abort_flag); ++i) {
+        for (int i = 0; alive && !warp_flag(abort_flag); ++i) {
             const int r = amax_tile(i, false);
             if (r == 0) break;
             if (r == 2 || warp_flag(reinterpret_cast<volatile unsigned int*>(p0_overflow))) {
@@ -1337,7 +1375,8 @@ cudaError_t launch_requant_tc(const LaunchCtx& ctx, const RequantTcMaps& maps, c
     a.zero = 0;
     a.nks = (int)((K + kTK - 1) / kTK);
     a.tiles = (int)((N + kTM * kPair - 1) / (kTM * kPair)) * a.nks;
-    a.units = (int)((N + kTM - 1) / kTM) * a.nks;
+    a.chunk = (int)(K >= 128 ? (int64_t)kWBytes / 2 : K * kChunkRows);
+    a.units = (int)((N * K + a.chunk - 1) / a.chunk);
     const int rows_pad256 = (int)((N + 255) / 256 * 256);
     const int nb_rows = (rows_pad256 + kSplitRows - 1) / kSplitRows;
     const int nb_cols = (int)((K + kSplitCols - 1) / kSplitCols);
