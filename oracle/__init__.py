@@ -67,6 +67,13 @@ def lib():
             L.orc_gemm_bf16.argtypes = [P, P, P, I64, I64, I64, P, I64, P, P]
             L.orc_select_contrastive.restype = I
             L.orc_select_contrastive.argtypes = [P, I, I, I, I, P, P]
+            L.orc_bf16_rne.restype = ctypes.c_uint16
+            L.orc_bf16_rne.argtypes = [ctypes.c_double]
+            L.orc_bf16_rne_array.argtypes = [P, I64, P]
+            L.orc_softmax_bf16.argtypes = [P, I64, I64, ctypes.c_double, P]
+            L.orc_gelu_f64.argtypes = [P, I64, P]
+            L.orc_gelu_bf16.argtypes = [P, I64, P]
+            L.orc_add_bf16.argtypes = [P, P, I64, P]
             _lib = L
     return _lib
 
@@ -246,3 +253,104 @@ def select_contrastive(rewards, K: int, global_std: bool = True, with_transform:
     if rc != 0:
         raise ValueError(f"select_contrastive: bad shape P={P} N={N} K={K}")
     return idx, r
+
+
+# ---------------------------------------------------------------- DiT block (reading R11)
+
+def bf16_rne(x) -> np.ndarray:
+    """Nearest bf16 (ties to even) of float64 values, as uint16 bits (same shape)."""
+    x = np.asarray(x, np.float64)
+    flat = _c(x, np.float64).reshape(-1)
+    out = np.empty(flat.size, np.uint16)
+    lib().orc_bf16_rne_array(_p(flat), flat.size, _p(out))
+    return out.reshape(x.shape)
+
+
+def bf16_value(bits) -> np.ndarray:
+    """float64 values of bf16 bit patterns."""
+    return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def softmax_bf16(L_bits, scale: float) -> np.ndarray:
+    """bf16(softmax(scale * L)) per row of bf16 logits [rows, cols] (exact in double)."""
+    L_bits = _c(L_bits, np.uint16)
+    rows, cols = L_bits.shape
+    out = np.empty((rows, cols), np.uint16)
+    lib().orc_softmax_bf16(_p(L_bits), rows, cols, ctypes.c_double(scale), _p(out))
+    return out
+
+
+def gelu_f64(x) -> np.ndarray:
+    x = _c(x, np.float64)
+    y = np.empty_like(x)
+    lib().orc_gelu_f64(_p(x), x.size, _p(y))
+    return y
+
+
+def gelu_bf16(x_bits) -> np.ndarray:
+    x_bits = _c(x_bits, np.uint16)
+    y = np.empty_like(x_bits)
+    lib().orc_gelu_bf16(_p(x_bits), x_bits.size, _p(y))
+    return y
+
+
+def add_bf16(a_bits, b_bits) -> np.ndarray:
+    a_bits = _c(a_bits, np.uint16)
+    b_bits = _c(b_bits, np.uint16)
+    assert a_bits.shape == b_bits.shape
+    y = np.empty_like(a_bits)
+    lib().orc_add_bf16(_p(a_bits), _p(b_bits), a_bits.size, _p(y))
+    return y
+
+
+def attention_head(q_bits, k_bits, v_bits) -> np.ndarray:
+    """One head: O = bf16(P V) with P = bf16(softmax(bf16(q k^T) / sqrt(dh))); q, k, v
+    [S, dh] bf16 bits.  Returns O [S, dh] bits."""
+    q_bits, k_bits, v_bits = (_c(t, np.uint16) for t in (q_bits, k_bits, v_bits))
+    dh = q_bits.shape[1]
+    logits, _ = gemm_bf16(q_bits, k_bits)
+    P = softmax_bf16(bf16_rne(logits), 1.0 / np.sqrt(dh))
+    o, _ = gemm_bf16(P, np.ascontiguousarray(v_bits.T))
+    return bf16_rne(o)
+
+
+def attention(qkv_bits, B: int, S: int, H: int) -> np.ndarray:
+    """Multi-head attention of the block: qkv [B*S, 3D] bf16 bits (q, k, v side by
+    side, head h in columns h*dh .. of each); returns o [B*S, D] bits."""
+    qkv_bits = _c(qkv_bits, np.uint16)
+    T, D3 = qkv_bits.shape
+    D = D3 // 3
+    dh = D // H
+    o = np.empty((T, D), np.uint16)
+    for b in range(B):
+        rs = slice(b * S, (b + 1) * S)
+        for h in range(H):
+            c = slice(h * dh, (h + 1) * dh)
+            o[rs, c] = attention_head(qkv_bits[rs, c], qkv_bits[rs, D + h * dh:D + (h + 1) * dh],
+                                      qkv_bits[rs, 2 * D + h * dh:2 * D + (h + 1) * dh])
+    return o
+
+
+def nvfp4_linear(x_bits, w, bias_bits=None) -> np.ndarray:
+    """bf16(NVFP4 GEMM) of bf16 activations x [T, K] (quantized per row) with weights
+    w = (codes, sf row-major, s_t) from requant; returns [T, N] bits."""
+    ac, asf, a_s = act_quant(x_bits)
+    y, _ = gemm_nvfp4(ac, asf, a_s, *w, bias_bits)
+    return bf16_rne(y)
+
+
+def dit_block(x_bits, w, bias, B: int, S: int, H: int) -> dict:
+    """The synthetic DiT block of reading R11 on bf16 x [B*S, D]:
+    qkv = lin(x, qkv); o = attention(qkv); h1 = bf16(lin(o, o) + x);
+    out = bf16(lin(gelu(lin(h1, up)), dn) + h1), every lin an NVFP4 linear (per-row
+    activation quantization) with bias.  w and bias: dicts keyed 'qkv', 'o', 'up',
+    'dn' (weights as returned by requant, bias as bf16 bits or None).  Returns every
+    intermediate (bits)."""
+    r = {}
+    r["qkv"] = nvfp4_linear(x_bits, w["qkv"], bias.get("qkv"))
+    r["o"] = attention(r["qkv"], B, S, H)
+    r["h1"] = add_bf16(nvfp4_linear(r["o"], w["o"], bias.get("o")), x_bits)
+    r["u"] = nvfp4_linear(r["h1"], w["up"], bias.get("up"))
+    r["g"] = gelu_bf16(r["u"])
+    r["out"] = add_bf16(nvfp4_linear(r["g"], w["dn"], bias.get("dn")), r["h1"])
+    return r

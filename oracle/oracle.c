@@ -47,6 +47,13 @@
  *       population standard deviation of all P*K selected rewards (global) or of
  *       the prompt's K (per prompt); Z == 0 gives r = 1/2.  Accumulation in fp64,
  *       r rounded to fp32 once.
+ *   R11 The synthetic DiT block ([SOL] Stage 1 runs the NVFP4-quantized solver
+ *       over the DiT's linears; the block below is a FLUX-shaped stand-in):
+ *       tensors between the steps are bf16, each rounded once to nearest-even
+ *       from the exact value of its step: the NVFP4 and BF16 products (exact
+ *       sums), the attention logits, the softmax probabilities, the GELU
+ *       (tanh form) and the residual sums.  See orc_bf16_rne and the block
+ *       functions at the end.
  *
  * Every function is pinned by tests/test_oracle_*.py against closed forms,
  * brute force or a library routine; none is "parity unpinned".
@@ -475,4 +482,80 @@ int orc_select_contrastive(const float* rewards, int P, int N, int K, int global
     free(mu);
     free(z);
     return ORC_OK;
+}
+
+/* ------------------------------------------------------------------ DiT block (R11) */
+
+/* Nearest bf16 to x, ties to even: 8 significant bits over the fp32 exponent
+ * range (below 2^-126 a fixed quantum of 2^-133, the bf16 subnormals); values
+ * that round above the largest finite bf16, (2 - 2^-7) 2^127, give infinity.
+ * Returns the bf16 bit pattern.  The rounding is one operation on the exact
+ * double: x / quantum is exact (a power of two), nearbyint rounds it to an
+ * integer with ties to even (the default rounding mode). */
+uint16_t orc_bf16_rne(double x) {
+    if (x != x) return 0x7FC0;
+    const uint16_t sign = signbit(x) ? 0x8000 : 0;
+    const double a = fabs(x);
+    if (a == 0.0) return sign;
+    if (isinf(a)) return sign | 0x7F80;
+    int e;
+    (void)frexp(a, &e); /* a = f 2^e, f in [0.5, 1): the leading bit is 2^(e-1) */
+    int lead = e - 1;
+    if (lead < -126) lead = -126;
+    const double quantum = ldexp(1.0, lead - 7);
+    const double v = nearbyint(a / quantum) * quantum;
+    if (v > 3.3895313892515355e38) return sign | 0x7F80;
+    const float f = (float)v; /* exact: at most 8 significant bits in range */
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return sign | (uint16_t)(u >> 16);
+}
+
+void orc_bf16_rne_array(const double* x, int64_t n, uint16_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_bf16_rne(x[i]);
+}
+
+/* Attention probabilities: per row of bf16 logits L [rows, cols],
+ * P = bf16(softmax(scale * L)), the softmax exact in double (the maximum
+ * subtracted first, which leaves it unchanged). */
+void orc_softmax_bf16(const uint16_t* L, int64_t rows, int64_t cols, double scale, uint16_t* P) {
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t i = 0; i < rows; ++i) {
+        const uint16_t* l = L + i * cols;
+        double m = -INFINITY;
+        for (int64_t j = 0; j < cols; ++j) m = fmax(m, (double)bf16_bits_to_float(l[j]));
+        double sum = 0.0;
+        for (int64_t j = 0; j < cols; ++j) sum += exp(scale * ((double)bf16_bits_to_float(l[j]) - m));
+        for (int64_t j = 0; j < cols; ++j)
+            P[i * cols + j] = orc_bf16_rne(exp(scale * ((double)bf16_bits_to_float(l[j]) - m)) / sum);
+    }
+}
+
+/* GELU in its tanh form, g(x) = x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), in
+ * double; and its bf16 version on bf16 inputs. */
+void orc_gelu_f64(const double* x, int64_t n, double* y) {
+    const double k = sqrt(2.0 / (4.0 * atan(1.0)));
+    for (int64_t i = 0; i < n; ++i) {
+        const double v = x[i];
+        y[i] = 0.5 * v * (1.0 + tanh(k * (v + 0.044715 * v * v * v)));
+    }
+}
+
+void orc_gelu_bf16(const uint16_t* x, int64_t n, uint16_t* y) {
+    const double k = sqrt(2.0 / (4.0 * atan(1.0)));
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t i = 0; i < n; ++i) {
+        const double v = (double)bf16_bits_to_float(x[i]);
+        y[i] = orc_bf16_rne(0.5 * v * (1.0 + tanh(k * (v + 0.044715 * v * v * v))));
+    }
+}
+
+/* Residual sum of two bf16 tensors, bf16(a + b) (the sum is exact in double). */
+void orc_add_bf16(const uint16_t* a, const uint16_t* b, int64_t n, uint16_t* y) {
+    for (int64_t i = 0; i < n; ++i)
+        y[i] = orc_bf16_rne((double)bf16_bits_to_float(a[i]) + (double)bf16_bits_to_float(b[i]));
 }
