@@ -503,6 +503,65 @@ def evt_report(device, P=2048, K=24, delta=EVT_DELTA, seed=0):
 
 # ----------------------------------------------------------------------------- our arm
 
+def dit_block_report(device, pk, fp4_peak, reps=5):
+    """The FLUX.1-shaped synthetic DiT block (8 images x 4608 tokens, D 3072, 24 heads):
+    one nvfp4_dit_block call on resident inputs, median of `reps` (CUDA events on the
+    launching stream; the activations, 226 MB, exceed L2), and its attention alone.
+    FLOPs: the four linears 24 T D^2 (NVFP4), the attention 4 B S^2 D (bf16).  `frac` is
+    the time both would take at the measured peaks (FP4 = bf16 x the nominal ratio) over
+    the measured time."""
+    import torch
+    import nvfp4_quantized_dit_gb300 as nv
+    import workloads
+    cfg = workloads.BLOCKS["flux"]
+    B, S, D, H = cfg.B, cfg.S, cfg.D, cfg.H
+    T = B * S
+    x = workloads.block_input(cfg, seed=0).to(device)
+    wts = workloads.block_weights(cfg, seed=0)
+    weights = []
+    for name in workloads.BLOCK_LINEARS:
+        W, b = wts[name]
+        weights.append((*nv.nvfp4_requant(W.to(device)), b.to(device)))
+    out = torch.empty_like(x)
+    ws = torch.empty(nv.dit_block_workspace_bytes(B, S, D, H), dtype=torch.uint8, device=device)
+    g = torch.Generator(device=device)
+    g.manual_seed(1)
+    qkv = torch.randn(T, 3 * D, generator=g, device=device).to(torch.bfloat16)
+    o = torch.empty(T, D, dtype=torch.bfloat16, device=device)
+    wsa = torch.empty(nv.dit_attention_workspace_bytes(B, S, D, H), dtype=torch.uint8, device=device)
+
+    def med(fn):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        vs = []
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            vs.append(e0.elapsed_time(e1))
+        return statistics.median(vs)
+    block_ms = med(lambda: nv.nvfp4_dit_block(x, B, S, H, weights, out=out, workspace=ws))
+    attn_ms = med(lambda: nv.nvfp4_dit_attention(qkv, B, S, H, o=o, workspace=wsa))
+    lin_flop = 24.0 * T * D * D
+    attn_flop = 4.0 * B * S * S * D
+    ideal_ms = (lin_flop / (fp4_peak * 1e12) + attn_flop / (pk["bf16_tflops"] * 1e12)) * 1e3
+    res = {"workload": cfg.description, "ms": round(block_ms, 3),
+           "tflops": round((lin_flop + attn_flop) / (block_ms * 1e-3) / 1e12, 1),
+           "attention_ms": round(attn_ms, 3),
+           "attention_tflops": round(attn_flop / (attn_ms * 1e-3) / 1e12, 1),
+           "rest_ms": round(block_ms - attn_ms, 3),
+           "rest_linear_tflops": round(lin_flop / ((block_ms - attn_ms) * 1e-3) / 1e12, 1),
+           "flop": {"linears_nvfp4": lin_flop, "attention_bf16": attn_flop},
+           "frac": round(ideal_ms / block_ms, 4), "reps": reps,
+           "device_status": nv.nvfp4_device_status()}
+    del x, weights, out, ws, qkv, o, wsa
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_ours(args):
     import torch
     import nvfp4_quantized_dit_gb300 as nv
@@ -653,6 +712,8 @@ def run_ours(args):
         if not args.no_peak_probe:
             extras["cublas_nvfp4_8192"] = cublas_nvfp4_peak(device)
         extras["evt_spread"] = evt_report(device)
+        if not args.no_block:
+            extras["dit_block"] = dit_block_report(device, pk, fp4_peak)
         extras["device_status_after_extras"] = nv.nvfp4_device_status()
     return report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk, world, rank,
                   launches_per_step, per_tensor_ms, extras, variant_ms)
@@ -835,7 +896,7 @@ def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk
         "device_status": status,
         "clocks": clk,
     }
-    for k in ("per_config", "iteration", "evt_spread", "device_status_after_extras"):
+    for k in ("per_config", "iteration", "dit_block", "evt_spread", "device_status_after_extras"):
         if k in extras:
             out[k] = extras[k]
     if world == 1 and not args.no_cpu_baseline:
@@ -973,6 +1034,7 @@ def parse_args(argv=None):
     ap.add_argument("--no-per-config", action="store_true", help="skip the SANA / SD3.5-L sweeps")
     ap.add_argument("--no-iteration", action="store_true", help="skip the iteration-shaped batch")
     ap.add_argument("--no-peak-probe", action="store_true", help="skip cuBLAS's NVFP4 8192^3 reference")
+    ap.add_argument("--no-block", action="store_true", help="skip the FLUX.1-shaped DiT block timing")
     ap.add_argument("--rows", type=int, default=None,
                     help="override M (a smaller case for profiling; the default is the config's)")
     args = ap.parse_args(argv)

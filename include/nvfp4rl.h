@@ -278,6 +278,67 @@ nvfp4_status nvfp4_requant_noalloc(const void* W, int w_dtype, const float* A, c
                                    int r, float alpha, int64_t N, int64_t K, uint8_t* codes,
                                    uint8_t* sf, float* s_t, void* stream);
 
+/* ---------------------------------------------------------------- synthetic DiT block
+ *
+ * A FLUX-shaped transformer block with NVFP4 linears, standing in for one block of the
+ * NVFP4-quantized solver that explores the seeds (Sol-RL project page, "Two-Stage
+ * Pipeline", Stage 1; the pages give no block layout, so this is the plain reading):
+ * with x [T, D] bf16, T = B*S tokens (B images of S tokens), H heads of dh = D/H,
+ *   qkv = lin(x, qkv)                                 [T, 3D]: q | k | v, head h in
+ *                                                     columns h*dh .. of each part
+ *   o   = attention(qkv): per image and head, P = bf16(softmax(bf16(q k^T) / sqrt(dh)))
+ *         over the image's S keys, O = bf16(P v)      [T, D]
+ *   h1  = bf16(lin(o, o) + x)
+ *   out = bf16(lin(gelu(lin(h1, up)), dn) + h1)       gelu: tanh form, bf16 out
+ * where lin(a, w) = nvfp4_gemm(nvfp4_act_quant(a), w) + bias (bf16 out), and w are
+ * weights as written by nvfp4_requant: qkv [3D, D], o [D, D], up [4D, D], dn [D, 4D].
+ * Every intermediate is bf16, rounded once to nearest-even; the attention's products
+ * run on the BF16 GEMM (bf16_gemm), one image-head at a time.
+ * Shapes: D % 64 == 0, H divides D with dh % 64 == 0, S % 64 == 0, T < 2^31.
+ */
+typedef struct {
+    const uint8_t* codes; /* [N, K/2] E2M1 codes (nvfp4_requant) */
+    const uint8_t* sf;    /* nvfp4_sf_bytes(N, K) bytes, blocked layout */
+    const float* s_t;     /* one fp32 */
+    const void* bias;     /* [N] bf16, or NULL */
+} nvfp4_linear_weights;
+
+/* Bytes of device workspace nvfp4_dit_block needs (host only; 0 for invalid shapes). */
+size_t nvfp4_dit_block_workspace_bytes(int64_t B, int64_t S, int64_t D, int64_t H);
+
+/*
+ * nvfp4_dit_block — the block above.
+ *   x          device, [B*S, D] bf16.
+ *   w          host array of 4 nvfp4_linear_weights (device pointers): qkv, o, up, dn.
+ *   out        device, [B*S, D] bf16 (out); may not alias x.
+ *   workspace  device, >= nvfp4_dit_block_workspace_bytes(...) bytes, 256-byte aligned;
+ *              owned by the caller, not used by anything else until the call's work on
+ *              `stream` is done.
+ * Errors as the calls it makes (NVFP4_ERR_SHAPE for the shape rules above, _NULL,
+ * _ALIGN, _ARCH, _CUDA).  Enqueues about 3 B H + 14 kernels; allocates nothing.
+ */
+nvfp4_status nvfp4_dit_block(const void* x, int64_t B, int64_t S, int64_t D, int64_t H,
+                             const nvfp4_linear_weights* w, void* out, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* The block's attention alone: qkv [B*S, 3D] bf16 -> o [B*S, D] bf16, with a workspace of
+ * nvfp4_dit_attention_workspace_bytes(B, S, D, H) bytes (shape rules as the block). */
+size_t nvfp4_dit_attention_workspace_bytes(int64_t B, int64_t S, int64_t D, int64_t H);
+nvfp4_status nvfp4_dit_attention(const void* qkv, int64_t B, int64_t S, int64_t D, int64_t H, void* o,
+                                 void* workspace, size_t workspace_bytes, void* stream);
+
+/* The block's streaming steps on bf16 tensors (n % 8 == 0, cols % 8 == 0, 16-byte
+ * aligned; results rounded to nearest-even):
+ *   bf16_softmax_rows  P = softmax(scale * L) per row of L [rows, cols] (fp32 exp);
+ *                      P may alias L.
+ *   bf16_gelu          y = x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))) (fp32); y may
+ *                      alias x.
+ *   bf16_add           y = a + b (fp32 sum); y may alias a or b. */
+nvfp4_status bf16_softmax_rows(const void* L, int64_t rows, int64_t cols, float scale, void* P,
+                               void* stream);
+nvfp4_status bf16_gelu(const void* x, int64_t n, void* y, void* stream);
+nvfp4_status bf16_add(const void* a, const void* b, int64_t n, void* y, void* stream);
+
 /* ---------------------------------------------------------------- diagnostics */
 
 /*

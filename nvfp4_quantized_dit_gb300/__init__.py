@@ -61,6 +61,11 @@ def library() -> ctypes.CDLL:
                 "nvfp4_gemm": [P, P, P, P, P, P, P, P, I64, I64, I64, P],
                 "nvfp4_gemm_rowamax": [P, P, P, P, P, P, P, P, P, I64, I64, I64, P],
                 "nvfp4_act_quant_prescaled": [P, I64, I64, P, P, P, P, P],
+                "nvfp4_dit_block": [P, I64, I64, I64, I64, P, P, P, ctypes.c_size_t, P],
+                "nvfp4_dit_attention": [P, I64, I64, I64, I64, P, P, ctypes.c_size_t, P],
+                "bf16_softmax_rows": [P, I64, I64, F, P, P],
+                "bf16_gelu": [P, I64, P, P],
+                "bf16_add": [P, P, I64, P, P],
                 "bf16_gemm": [P, P, P, P, I64, I64, I64, P],
                 "select_contrastive": [P, I, I, I, I, P, P, P],
                 "nvfp4_device_status": [ctypes.POINTER(ctypes.c_int), I],
@@ -79,6 +84,9 @@ def library() -> ctypes.CDLL:
                 fn.restype = I
             L.nvfp4_requant_workspace_bytes.argtypes = [I, I, I64, I64]
             L.nvfp4_requant_workspace_bytes.restype = ctypes.c_size_t
+            for name in ("nvfp4_dit_block_workspace_bytes", "nvfp4_dit_attention_workspace_bytes"):
+                getattr(L, name).argtypes = [I64, I64, I64, I64]
+                getattr(L, name).restype = ctypes.c_size_t
             L.nvfp4_status_string.argtypes = [I]
             L.nvfp4_status_string.restype = ctypes.c_char_p
             L.nvfp4_version.argtypes = []
@@ -384,3 +392,80 @@ def nvfp4_test_gemm_withhold(a, w, withhold_kb: int, timeout_ns: int, out=None, 
           _dev(w_sf, "w_sf", torch.uint8), _dev(w_s, "w_st", torch.float32), _dev(out, "Y", torch.bfloat16),
           M, N, K, int(withhold_kb), int(timeout_ns), _stream(stream))
     return out
+
+
+# ---------------------------------------------------------------- synthetic DiT block
+
+class _LinearWeights(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("sf", ctypes.c_void_p), ("s_t", ctypes.c_void_p),
+                ("bias", ctypes.c_void_p)]
+
+
+def dit_block_workspace_bytes(B: int, S: int, D: int, H: int) -> int:
+    return int(library().nvfp4_dit_block_workspace_bytes(B, S, D, H))
+
+
+def dit_attention_workspace_bytes(B: int, S: int, D: int, H: int) -> int:
+    return int(library().nvfp4_dit_attention_workspace_bytes(B, S, D, H))
+
+
+def _workspace(nbytes: int, dev, workspace):
+    if nbytes == 0:
+        raise NVFP4Error("workspace size", 2)  # NVFP4_ERR_SHAPE: the shape rules of the block
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    return workspace
+
+
+def nvfp4_dit_block(x, B: int, S: int, H: int, weights, out=None, workspace=None, stream=None):
+    """The synthetic DiT block on bf16 x [B*S, D]; weights: 4 tuples (codes, sf, s_t,
+    bias or None) for qkv, o, up, dn, as nvfp4_requant returns them.  Returns out."""
+    T, D = x.shape
+    if T != B * S:
+        raise ValueError("x must be [B*S, D]")
+    if len(weights) != 4:
+        raise ValueError("weights: qkv, o, up, dn")
+    arr = (_LinearWeights * 4)()
+    for i, wt in enumerate(weights):
+        codes, sf, s_t, bias = wt
+        arr[i] = _LinearWeights(_dev(codes, "codes", torch.uint8), _dev(sf, "sf", torch.uint8),
+                                _dev(s_t, "s_t", torch.float32), _opt(bias, "bias", torch.bfloat16))
+    out = torch.empty_like(x) if out is None else out
+    workspace = _workspace(dit_block_workspace_bytes(B, S, D, H), x.device, workspace)
+    _call("nvfp4_dit_block", _dev(x, "x", torch.bfloat16), B, S, D, H, arr, _dev(out, "out", torch.bfloat16),
+          _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    return out
+
+
+def nvfp4_dit_attention(qkv, B: int, S: int, H: int, o=None, workspace=None, stream=None):
+    """The block's attention: qkv [B*S, 3D] bf16 -> o [B*S, D] bf16."""
+    T, D3 = qkv.shape
+    D = D3 // 3
+    o = torch.empty(T, D, dtype=torch.bfloat16, device=qkv.device) if o is None else o
+    workspace = _workspace(dit_attention_workspace_bytes(B, S, D, H), qkv.device, workspace)
+    _call("nvfp4_dit_attention", _dev(qkv, "qkv", torch.bfloat16), B, S, D, H, _dev(o, "o", torch.bfloat16),
+          _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    return o
+
+
+def bf16_softmax_rows(L, scale: float, P=None, stream=None):
+    rows, cols = L.shape
+    P = torch.empty_like(L) if P is None else P
+    _call("bf16_softmax_rows", _dev(L, "L", torch.bfloat16), rows, cols, ctypes.c_float(scale),
+          _dev(P, "P", torch.bfloat16), _stream(stream))
+    return P
+
+
+def bf16_gelu(x, y=None, stream=None):
+    y = torch.empty_like(x) if y is None else y
+    _call("bf16_gelu", _dev(x, "x", torch.bfloat16), x.numel(), _dev(y, "y", torch.bfloat16), _stream(stream))
+    return y
+
+
+def bf16_add(a, b, y=None, stream=None):
+    if a.shape != b.shape:
+        raise ValueError("a and b differ in shape")
+    y = torch.empty_like(a) if y is None else y
+    _call("bf16_add", _dev(a, "a", torch.bfloat16), _dev(b, "b", torch.bfloat16), a.numel(),
+          _dev(y, "y", torch.bfloat16), _stream(stream))
+    return y

@@ -9,6 +9,7 @@
 
 #include <mutex>
 
+#include "block.cuh"
 #include "common.cuh"
 
 namespace nvfp4rl {
@@ -387,6 +388,189 @@ nvfp4_status bf16_gemm(const void* X, const void* W, const void* bias, void* Y, 
         return NVFP4_ERR_CUDA;
     return from_cuda(launch_gemm_bf16(ctx, ta, tb, ty, static_cast<const __nv_bfloat16*>(bias), M,
                                       N, K));
+}
+
+// ------------------------------------------------------------------ synthetic DiT block
+
+static size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+static bool block_shape_ok(int64_t B, int64_t S, int64_t D, int64_t H) {
+    if (B <= 0 || S <= 0 || D <= 0 || H <= 0) return false;
+    if (D % 64 != 0 || D % H != 0 || (D / H) % 64 != 0 || S % 64 != 0) return false;
+    if (B * S > kMaxRows || B * H > 65535 || S > (1 << 20) || 4 * D > (1 << 20)) return false;
+    return true;
+}
+
+// Attention scratch: per-head Q, K, V^T and O ([B*H, S, dh] each) and one head's logits.
+struct AttnLayout {
+    uint16_t *Q, *K, *Vt, *O, *L;
+    size_t bytes;
+};
+static AttnLayout attn_layout(void* base, int64_t B, int64_t S, int64_t D) {
+    AttnLayout l;
+    const size_t td = up256((size_t)B * S * D * 2);
+    uint8_t* p = static_cast<uint8_t*>(base);
+    l.Q = reinterpret_cast<uint16_t*>(p);
+    l.K = reinterpret_cast<uint16_t*>(p + td);
+    l.Vt = reinterpret_cast<uint16_t*>(p + 2 * td);
+    l.O = reinterpret_cast<uint16_t*>(p + 3 * td);
+    l.L = reinterpret_cast<uint16_t*>(p + 4 * td);
+    l.bytes = 4 * td + up256((size_t)S * S * 2);
+    return l;
+}
+
+size_t nvfp4_dit_attention_workspace_bytes(int64_t B, int64_t S, int64_t D, int64_t H) {
+    if (!block_shape_ok(B, S, D, H)) return 0;
+    return attn_layout(nullptr, B, S, D).bytes;
+}
+
+// The attention of the block: heads split, per image-head L = Q K^T (BF16 GEMM),
+// P = softmax in place, O = P V (BF16 GEMM against V^T), heads merged into o.
+static nvfp4_status attention_run(const LaunchCtx& ctx, const uint16_t* qkv, int64_t B, int64_t S, int64_t D,
+                                  int64_t H, uint16_t* o, const AttnLayout& l, void* stream) {
+    const int64_t dh = D / H;
+    cudaError_t e = launch_heads_split(ctx, qkv, B, S, D, H, l.Q, l.K, l.Vt);
+    if (e != cudaSuccess) return from_cuda(e);
+    const float scale = 1.0f / sqrtf((float)dh);
+    for (int64_t z = 0; z < B * H; ++z) {
+        nvfp4_status st = bf16_gemm(l.Q + z * S * dh, l.K + z * S * dh, nullptr, l.L, S, S, dh, stream);
+        if (st != NVFP4_OK) return st;
+        if ((e = launch_softmax_rows(ctx, l.L, S, S, scale, l.L)) != cudaSuccess) return from_cuda(e);
+        st = bf16_gemm(l.L, l.Vt + z * dh * S, nullptr, l.O + z * S * dh, S, dh, S, stream);
+        if (st != NVFP4_OK) return st;
+    }
+    return from_cuda(launch_heads_merge(ctx, l.O, B, S, D, H, o));
+}
+
+nvfp4_status nvfp4_dit_attention(const void* qkv, int64_t B, int64_t S, int64_t D, int64_t H, void* o,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+    if (!block_shape_ok(B, S, D, H)) return NVFP4_ERR_SHAPE;
+    if (!qkv || !o || !workspace) return NVFP4_ERR_NULL;
+    if (misaligned(qkv, 16) || misaligned(o, 16) || misaligned(workspace, 256)) return NVFP4_ERR_ALIGN;
+    const AttnLayout l = attn_layout(workspace, B, S, D);
+    if (workspace_bytes < l.bytes) return NVFP4_ERR_SHAPE;
+    LaunchCtx ctx;
+    const nvfp4_status st = resolve(stream, &ctx);
+    if (st != NVFP4_OK) return st;
+    return attention_run(ctx, static_cast<const uint16_t*>(qkv), B, S, D, H, static_cast<uint16_t*>(o), l,
+                         stream);
+}
+
+// Block scratch: R1 [3 T D] holds qkv, then o | a | d; R2 [4 T D] holds the attention's
+// Q | K | V^T | O, then u; h1 [T D]; L [S S]; the activation quantization of a D-wide
+// tensor (x, o, h1 in turn) and of the 4D-wide GELU output.
+struct BlockLayout {
+    uint16_t *r1, *r2, *h1, *L;
+    uint8_t *qa_codes, *qa_sf, *qb_codes, *qb_sf;
+    float *qa_s, *qb_s;
+    size_t bytes;
+};
+static BlockLayout block_layout(void* base, int64_t B, int64_t S, int64_t D) {
+    BlockLayout l;
+    const int64_t T = B * S;
+    const size_t td = up256((size_t)T * D * 2);
+    size_t off = 0;
+    uint8_t* p = static_cast<uint8_t*>(base);
+    auto take = [&](size_t n) {
+        uint8_t* q = p + off;
+        off += up256(n);
+        return q;
+    };
+    l.r1 = reinterpret_cast<uint16_t*>(take(3 * td));
+    l.r2 = reinterpret_cast<uint16_t*>(take(4 * td));
+    l.h1 = reinterpret_cast<uint16_t*>(take(td));
+    l.L = reinterpret_cast<uint16_t*>(take((size_t)S * S * 2));
+    l.qa_codes = take((size_t)T * D / 2);
+    l.qa_sf = take(nvfp4_sf_bytes(T, D));
+    l.qa_s = reinterpret_cast<float*>(take((size_t)T * 4));
+    l.qb_codes = take((size_t)T * 4 * D / 2);
+    l.qb_sf = take(nvfp4_sf_bytes(T, 4 * D));
+    l.qb_s = reinterpret_cast<float*>(take((size_t)T * 4));
+    l.bytes = off;
+    return l;
+}
+
+size_t nvfp4_dit_block_workspace_bytes(int64_t B, int64_t S, int64_t D, int64_t H) {
+    if (!block_shape_ok(B, S, D, H)) return 0;
+    return block_layout(nullptr, B, S, D).bytes;
+}
+
+nvfp4_status nvfp4_dit_block(const void* x, int64_t B, int64_t S, int64_t D, int64_t H,
+                             const nvfp4_linear_weights* w, void* out, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    if (!block_shape_ok(B, S, D, H)) return NVFP4_ERR_SHAPE;
+    if (!x || !w || !out || !workspace) return NVFP4_ERR_NULL;
+    for (int i = 0; i < 4; ++i)
+        if (!w[i].codes || !w[i].sf || !w[i].s_t) return NVFP4_ERR_NULL;
+    if (misaligned(x, 16) || misaligned(out, 16) || misaligned(workspace, 256)) return NVFP4_ERR_ALIGN;
+    const BlockLayout l = block_layout(workspace, B, S, D);
+    if (workspace_bytes < l.bytes) return NVFP4_ERR_SHAPE;
+    LaunchCtx ctx;
+    nvfp4_status st = resolve(stream, &ctx);
+    if (st != NVFP4_OK) return st;
+    const int64_t T = B * S, TD = T * D;
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    uint16_t *qkv = l.r1, *o = l.r1, *a = l.r1 + TD, *d = l.r1 + 2 * TD, *u = l.r2;
+    auto lin = [&](const uint16_t* in, int64_t K, uint8_t* c, uint8_t* sf, float* s, const nvfp4_linear_weights& wi,
+                   int64_t N, uint16_t* y) {
+        nvfp4_status r = nvfp4_act_quant(in, T, K, c, sf, s, stream);
+        if (r != NVFP4_OK) return r;
+        return nvfp4_gemm(c, sf, s, wi.codes, wi.sf, wi.s_t, wi.bias, y, T, N, K, stream);
+    };
+    if ((st = lin(xb, D, l.qa_codes, l.qa_sf, l.qa_s, w[0], 3 * D, qkv)) != NVFP4_OK) return st;
+    AttnLayout al;
+    const size_t td = up256((size_t)TD * 2);
+    uint8_t* r2b = reinterpret_cast<uint8_t*>(l.r2);
+    al.Q = reinterpret_cast<uint16_t*>(r2b);
+    al.K = reinterpret_cast<uint16_t*>(r2b + td);
+    al.Vt = reinterpret_cast<uint16_t*>(r2b + 2 * td);
+    al.O = reinterpret_cast<uint16_t*>(r2b + 3 * td);
+    al.L = l.L;
+    al.bytes = 0;
+    if ((st = attention_run(ctx, qkv, B, S, D, H, o, al, stream)) != NVFP4_OK) return st;
+    if ((st = lin(o, D, l.qa_codes, l.qa_sf, l.qa_s, w[1], D, a)) != NVFP4_OK) return st;
+    cudaError_t e = launch_add(ctx, a, xb, TD, l.h1);
+    if (e != cudaSuccess) return from_cuda(e);
+    if ((st = lin(l.h1, D, l.qa_codes, l.qa_sf, l.qa_s, w[2], 4 * D, u)) != NVFP4_OK) return st;
+    if ((e = launch_gelu(ctx, u, 4 * TD, u)) != cudaSuccess) return from_cuda(e);
+    if ((st = lin(u, 4 * D, l.qb_codes, l.qb_sf, l.qb_s, w[3], D, d)) != NVFP4_OK) return st;
+    return from_cuda(launch_add(ctx, d, l.h1, TD, static_cast<uint16_t*>(out)));
+}
+
+nvfp4_status bf16_softmax_rows(const void* L, int64_t rows, int64_t cols, float scale, void* P,
+                               void* stream) {
+    if (rows < 0 || cols <= 0 || cols % 8 != 0 || rows > kMaxRows || cols > (1 << 24)) return NVFP4_ERR_SHAPE;
+    if (rows == 0) return NVFP4_OK;
+    if (!L || !P) return NVFP4_ERR_NULL;
+    if (misaligned(L, 16) || misaligned(P, 16)) return NVFP4_ERR_ALIGN;
+    LaunchCtx ctx;
+    const nvfp4_status st = resolve(stream, &ctx);
+    if (st != NVFP4_OK) return st;
+    return from_cuda(launch_softmax_rows(ctx, static_cast<const uint16_t*>(L), rows, cols, scale,
+                                         static_cast<uint16_t*>(P)));
+}
+
+nvfp4_status bf16_gelu(const void* x, int64_t n, void* y, void* stream) {
+    if (n < 0 || n % 8 != 0) return NVFP4_ERR_SHAPE;
+    if (n == 0) return NVFP4_OK;
+    if (!x || !y) return NVFP4_ERR_NULL;
+    if (misaligned(x, 16) || misaligned(y, 16)) return NVFP4_ERR_ALIGN;
+    LaunchCtx ctx;
+    const nvfp4_status st = resolve(stream, &ctx);
+    if (st != NVFP4_OK) return st;
+    return from_cuda(launch_gelu(ctx, static_cast<const uint16_t*>(x), n, static_cast<uint16_t*>(y)));
+}
+
+nvfp4_status bf16_add(const void* a, const void* b, int64_t n, void* y, void* stream) {
+    if (n < 0 || n % 8 != 0) return NVFP4_ERR_SHAPE;
+    if (n == 0) return NVFP4_OK;
+    if (!a || !b || !y) return NVFP4_ERR_NULL;
+    if (misaligned(a, 16) || misaligned(b, 16) || misaligned(y, 16)) return NVFP4_ERR_ALIGN;
+    LaunchCtx ctx;
+    const nvfp4_status st = resolve(stream, &ctx);
+    if (st != NVFP4_OK) return st;
+    return from_cuda(launch_add(ctx, static_cast<const uint16_t*>(a), static_cast<const uint16_t*>(b), n,
+                                static_cast<uint16_t*>(y)));
 }
 
 nvfp4_status select_contrastive(const float* rewards, int P, int N, int K, int global_std,

@@ -255,7 +255,7 @@ def select_contrastive(rewards, K: int, global_std: bool = True, with_transform:
     return idx, r
 
 
-# ---------------------------------------------------------------- DiT block (reading R11)
+# ---------------------------------------------------------------- DiT block (reading R11 of oracle.c's header)
 
 def bf16_rne(x) -> np.ndarray:
     """Nearest bf16 (ties to even) of float64 values, as uint16 bits (same shape)."""
@@ -304,12 +304,14 @@ def add_bf16(a_bits, b_bits) -> np.ndarray:
 
 
 def attention_head(q_bits, k_bits, v_bits) -> np.ndarray:
-    """One head: O = bf16(P V) with P = bf16(softmax(bf16(q k^T) / sqrt(dh))); q, k, v
-    [S, dh] bf16 bits.  Returns O [S, dh] bits."""
+    """One head: O = bf16(P V) with P = bf16(softmax(bf16(q k^T) * scale)), scale the
+    fp32 value of 1 / sqrt(dh); q, k, v [S, dh] bf16 bits.  Returns O [S, dh] bits."""
     q_bits, k_bits, v_bits = (_c(t, np.uint16) for t in (q_bits, k_bits, v_bits))
     dh = q_bits.shape[1]
     logits, _ = gemm_bf16(q_bits, k_bits)
-    P = softmax_bf16(bf16_rne(logits), 1.0 / np.sqrt(dh))
+    # The scale is the fp32 value 1 / sqrt(dh) (two fp32 operations, IEEE rounding).
+    scale = float(np.float32(1.0) / np.sqrt(np.float32(dh)))
+    P = softmax_bf16(bf16_rne(logits), scale)
     o, _ = gemm_bf16(P, np.ascontiguousarray(v_bits.T))
     return bf16_rne(o)
 
@@ -340,7 +342,7 @@ def nvfp4_linear(x_bits, w, bias_bits=None) -> np.ndarray:
 
 
 def dit_block(x_bits, w, bias, B: int, S: int, H: int) -> dict:
-    """The synthetic DiT block of reading R11 on bf16 x [B*S, D]:
+    """The synthetic DiT block (reading R11 of oracle.c's header) on bf16 x [B*S, D]:
     qkv = lin(x, qkv); o = attention(qkv); h1 = bf16(lin(o, o) + x);
     out = bf16(lin(gelu(lin(h1, up)), dn) + h1), every lin an NVFP4 linear (per-row
     activation quantization) with bias.  w and bias: dicts keyed 'qkv', 'o', 'up',
@@ -354,3 +356,59 @@ def dit_block(x_bits, w, bias, B: int, S: int, H: int) -> dict:
     r["g"] = gelu_bf16(r["u"])
     r["out"] = add_bf16(nvfp4_linear(r["g"], w["dn"], bias.get("dn")), r["h1"])
     return r
+
+
+def linear_unquantized(x_bits, w, bias_bits=None) -> np.ndarray:
+    """bf16(x W^T + bias) with the NVFP4 weights w = (codes, sf row-major, s_t)
+    dequantized and the bf16 activations x [T, K] used as they are (no activation
+    quantization), the product in fp64 (a library matmul).  Returns [T, N] bits.  The
+    distance of a block built on it from the NVFP4 block measures what the activation
+    quantizer's decisions do to the result."""
+    codes, sf, s_t = w
+    W = dequantize(codes, sf, np.asarray(s_t, np.float32).reshape(-1)[:1], "tensor")
+    y = bf16_value(_c(x_bits, np.uint16)) @ W.T
+    if bias_bits is not None:
+        y = y + bf16_value(_c(bias_bits, np.uint16))[None, :]
+    return bf16_rne(y)
+
+
+def dit_block_rows(x_bits, w, bias, B: int, S: int, H: int, rows,
+                   quantize_activations: bool = True) -> np.ndarray:
+    """dit_block's output at the token rows `rows` only, for inputs too large to run
+    whole.  Every step of the block but the attention maps a row to the same row (the
+    activation quantization is per row), so those steps run on the chosen rows alone;
+    the attention of a row reads the keys and values of every token of its image, so
+    those (columns D..3D of the qkv linear) are formed for each image that holds a
+    chosen row.  With quantize_activations=False every linear is linear_unquantized
+    instead (the same weights, activations not quantized).  Returns out[rows]
+    [len(rows), D] bits."""
+    x_bits = _c(x_bits, np.uint16)
+    T, D = x_bits.shape
+    dh = D // H
+    rows = np.asarray(rows, np.int64).reshape(-1)
+    lin = nvfp4_linear if quantize_activations else linear_unquantized
+    codes, sf, s_t = w["qkv"]
+    bq = bias.get("qkv")
+    bq = None if bq is None else _c(bq, np.uint16)
+    if quantize_activations:
+        ac, asf, a_s = act_quant(x_bits)
+    o = np.empty((rows.size, D), np.uint16)
+    for b in np.unique(rows // S):
+        sel = np.nonzero(rows // S == b)[0]
+        img = slice(int(b) * S, (int(b) + 1) * S)
+        w_kv = (codes[D:3 * D], sf[D:3 * D], s_t)
+        w_q = (codes[:D], sf[:D], s_t)
+        b_kv = None if bq is None else bq[D:3 * D]
+        b_q = None if bq is None else bq[:D]
+        if quantize_activations:
+            kv = bf16_rne(gemm_nvfp4(ac[img], asf[img], a_s[img], *w_kv, b_kv)[0])
+            q = bf16_rne(gemm_nvfp4(ac, asf, a_s, *w_q, b_q, rows=rows[sel])[0])
+        else:
+            kv = linear_unquantized(x_bits[img], w_kv, b_kv)
+            q = linear_unquantized(x_bits[rows[sel]], w_q, b_q)
+        for h in range(H):
+            c = slice(h * dh, (h + 1) * dh)
+            o[sel, c] = attention_head(q[:, c], kv[:, c], kv[:, D + h * dh:D + (h + 1) * dh])
+    h1 = add_bf16(lin(o, w["o"], bias.get("o")), x_bits[rows])
+    g = gelu_bf16(lin(h1, w["up"], bias.get("up")))
+    return add_bf16(lin(g, w["dn"], bias.get("dn")), h1)

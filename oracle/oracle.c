@@ -533,25 +533,27 @@ void orc_softmax_bf16(const uint16_t* L, int64_t rows, int64_t cols, double scal
     }
 }
 
-/* GELU in its tanh form, g(x) = x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3))), in
- * double; and its bf16 version on bf16 inputs. */
-void orc_gelu_f64(const double* x, int64_t n, double* y) {
+/* GELU in its tanh form, g(x) = x/2 (1 + tanh(t)), t = sqrt(2/pi) (x + 0.044715 x^3),
+ * in double; and its bf16 version on bf16 inputs.  It is evaluated through the exact
+ * identity (1 + tanh(t)) / 2 = 1 / (1 + e^(-2t)), with the exponential taken of a
+ * non-positive argument: 1 + tanh(t) itself cancels for t << 0 (x below about -5),
+ * where g is small but not zero. */
+static double gelu_f64_one(double v) {
     const double k = sqrt(2.0 / (4.0 * atan(1.0)));
-    for (int64_t i = 0; i < n; ++i) {
-        const double v = x[i];
-        y[i] = 0.5 * v * (1.0 + tanh(k * (v + 0.044715 * v * v * v)));
-    }
+    const double t2 = 2.0 * k * (v + 0.044715 * v * v * v);
+    const double sig = t2 >= 0.0 ? 1.0 / (1.0 + exp(-t2)) : exp(t2) / (1.0 + exp(t2));
+    return v * sig;
+}
+
+void orc_gelu_f64(const double* x, int64_t n, double* y) {
+    for (int64_t i = 0; i < n; ++i) y[i] = gelu_f64_one(x[i]);
 }
 
 void orc_gelu_bf16(const uint16_t* x, int64_t n, uint16_t* y) {
-    const double k = sqrt(2.0 / (4.0 * atan(1.0)));
 #ifdef _OPENMP
 #pragma omp parallel for schedule(static)
 #endif
-    for (int64_t i = 0; i < n; ++i) {
-        const double v = (double)bf16_bits_to_float(x[i]);
-        y[i] = orc_bf16_rne(0.5 * v * (1.0 + tanh(k * (v + 0.044715 * v * v * v))));
-    }
+    for (int64_t i = 0; i < n; ++i) y[i] = orc_bf16_rne(gelu_f64_one((double)bf16_bits_to_float(x[i])));
 }
 
 /* Residual sum of two bf16 tensors, bf16(a + b) (the sum is exact in double). */

@@ -1,4 +1,4 @@
-"""Pins of the oracle's synthetic DiT block (reading R11 in oracle/oracle.c): bf16
+"""Pins of the oracle's synthetic DiT block (reading R11 in oracle/oracle.c's header): bf16
 rounding, the attention softmax, the GELU (tanh form), the residual add, one
 attention head and the block's wiring.  Each is checked against a library routine
 (torch's float32 -> bf16 conversion and bf16 addition, scipy's softmax and erf), a
@@ -89,6 +89,28 @@ def test_gelu_identity_and_erf_form():
     assert np.array_equal(orc.gelu_bf16(xb), orc.bf16_rne(orc.gelu_f64(orc.bf16_value(xb))))
 
 
+def test_gelu_tail_against_high_precision():
+    """The tanh form evaluated at 60 digits by mpmath, across the range where 1 + tanh(t)
+    cancels (x down to -11, where g(x) is about -1e-48): the double result keeps its
+    relative accuracy there, and the bf16 result is the high-precision value rounded
+    (subnormal bf16 values included)."""
+    mpmath = pytest.importorskip("mpmath")
+    mpmath.mp.dps = 60
+    k = mpmath.sqrt(2 / mpmath.pi)
+    x = np.concatenate([np.linspace(-11, -3, 801), np.linspace(-3, 3, 301), np.array([5.0, 9.0])])
+    hp = [0.5 * mpmath.mpf(v) * (1 + mpmath.tanh(k * (mpmath.mpf(v) + mpmath.mpf("0.044715") * mpmath.mpf(v) ** 3)))
+          for v in x]
+    g = orc.gelu_f64(x)
+    rel = np.array([abs((mpmath.mpf(gi) - h) / h) if h != 0 else abs(gi) for gi, h in zip(g, hp)], np.float64)
+    assert rel.max() < 1e-13
+    xb = orc.bf16_rne(x)
+    xv = orc.bf16_value(xb)
+    hb = np.array([float(0.5 * mpmath.mpf(v) * (1 + mpmath.tanh(k * (mpmath.mpf(v) + mpmath.mpf("0.044715") * mpmath.mpf(v) ** 3))))
+                   for v in xv])
+    assert np.array_equal(orc.gelu_bf16(xb), orc.bf16_rne(hb))
+    assert (orc.bf16_value(orc.gelu_bf16(xb)) < 0).sum() > 700  # the negative tail does not flush to zero
+
+
 def test_add_matches_torch_bf16_addition():
     rng = np.random.default_rng(2)
     a = torch.from_numpy((rng.standard_normal(200000) * 10.0 ** rng.integers(-6, 6, 200000)).astype(np.float32)).to(torch.bfloat16)
@@ -131,3 +153,73 @@ def test_block_residual_wiring():
     wz = {"qkv": zero(3 * D, D), "o": zero(D, D), "up": zero(4 * D, D), "dn": zero(D, 4 * D)}
     rz = orc.dit_block(x, wz, {}, B, S, H)
     assert not orc.bf16_value(rz["o"]).any() and np.array_equal(rz["out"], x)
+
+
+def test_block_rows_equals_whole_block():
+    """The row-restricted block (for inputs too large to run whole) reproduces the whole
+    block's output bit for bit on the chosen rows, rows of the first and last image
+    included, with biases on every linear."""
+    rng = np.random.default_rng(6)
+    B, S, H, dh = 3, 64, 2, 64
+    D = H * dh
+    x = orc.bf16_rne(rng.standard_normal((B * S, D)))
+    shapes = {"qkv": (3 * D, D), "o": (D, D), "up": (4 * D, D), "dn": (D, 4 * D)}
+    w = {k: orc.requant(orc.bf16_rne(rng.standard_normal(sh) * 0.05), None, None, 32.0) for k, sh in shapes.items()}
+    bias = {k: orc.bf16_rne(rng.standard_normal(sh[0]) * 0.02) for k, sh in shapes.items()}
+    full = orc.dit_block(x, w, bias, B, S, H)["out"]
+    rows = np.array([0, 5, 63, 2 * S, 2 * S + 17, 3 * S - 1])
+    assert np.array_equal(orc.dit_block_rows(x, w, bias, B, S, H, rows), full[rows])
+
+
+def _grid_weight(rng, N, K):
+    """A bf16 weight that per-tensor NVFP4 represents exactly: tensor amax 2688 * 2^-12
+    (so s = 2^-12), every 16-block c * sf * s with c on the E2M1 grid and sf an E4M3
+    value, one element of each block at |c| = 6 (so the block scale is sf itself)."""
+    grid = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+    sfs = np.array([448.0, 224.0, 112.0, 96.0, 56.0, 40.0, 13.0, 1.5, 0.25])
+    c = grid[rng.integers(0, 8, (N, K))] * rng.choice([-1.0, 1.0], (N, K))
+    c.reshape(N, K // 16, 16)[:, :, 0] = 6.0 * rng.choice([-1.0, 1.0], (N, K // 16))
+    sf = sfs[rng.integers(0, len(sfs), (N, K // 16))]
+    sf[0, 0] = 448.0
+    W = c * np.repeat(sf, 16, axis=1) * 2.0 ** -12
+    bits = orc.bf16_rne(W)
+    assert np.array_equal(orc.bf16_value(bits), W)
+    return bits
+
+
+def test_linear_unquantized_is_the_bf16_product_on_grid_weights():
+    """On a weight that NVFP4 represents exactly, the unquantized-activation linear is
+    the plain product of the bf16 activations with that weight: it must equal the
+    oracle's bf16 GEMM (rounded to bf16), bias included, bit for bit."""
+    rng = np.random.default_rng(8)
+    N, K, T = 96, 256, 40
+    w_bits = _grid_weight(rng, N, K)
+    w = orc.requant(w_bits, None, None, 32.0)
+    assert np.float32(np.asarray(w[2]).reshape(-1)[0]) == np.float32(2.0 ** -12)
+    assert np.array_equal(orc.dequantize(w[0], w[1], w[2], "tensor"), orc.bf16_value(w_bits))
+    x = orc.bf16_rne(rng.standard_normal((T, K)))
+    b = orc.bf16_rne(rng.standard_normal(N) * 0.1)
+    ref = orc.bf16_rne(orc.gemm_bf16(x, w_bits, b)[0])
+    assert np.array_equal(orc.linear_unquantized(x, w, b), ref)
+    # The quantized linear on the same weight differs (the activations are quantized).
+    assert not np.array_equal(orc.nvfp4_linear(x, w, b), ref)
+
+
+def test_block_rows_unquantized_mode():
+    """quantize_activations=False changes only the linears: with zero output
+    projections the block is still the identity, and otherwise it stays close to the
+    NVFP4 block (their gap is the activation quantization's, a few percent)."""
+    rng = np.random.default_rng(9)
+    B, S, H, dh = 2, 64, 2, 64
+    D = H * dh
+    x = orc.bf16_rne(rng.standard_normal((B * S, D)))
+    shapes = {"qkv": (3 * D, D), "o": (D, D), "up": (4 * D, D), "dn": (D, 4 * D)}
+    w = {k: orc.requant(orc.bf16_rne(rng.standard_normal(sh) * 0.05), None, None, 32.0) for k, sh in shapes.items()}
+    rows = np.array([1, 70, 127])
+    wz = dict(w, o=orc.requant(np.zeros(shapes["o"], np.uint16), None, None, 32.0),
+              dn=orc.requant(np.zeros(shapes["dn"], np.uint16), None, None, 32.0))
+    assert np.array_equal(orc.dit_block_rows(x, wz, {}, B, S, H, rows, quantize_activations=False), x[rows])
+    q = orc.bf16_value(orc.dit_block_rows(x, w, {}, B, S, H, rows))
+    u = orc.bf16_value(orc.dit_block_rows(x, w, {}, B, S, H, rows, quantize_activations=False))
+    gap = np.linalg.norm(q - u) / np.linalg.norm(u)
+    assert 1e-3 < gap < 0.2

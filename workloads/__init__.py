@@ -188,3 +188,51 @@ def activations_on_device(cfg: LinearConfig, device, seed: int = 0, rows: int | 
         ch = _outlier_channels(cfg.K, cfg.x_outlier_frac, _gen(seed, 6)).to(device)
         x[:, ch] *= cfg.x_outlier_gain
     return x.to(torch.bfloat16)
+
+
+@dataclass(frozen=True)
+class BlockConfig:
+    """A synthetic DiT block: B images of S tokens of width D, H attention heads of
+    D/H channels; linears qkv [3D, D], o [D, D], up [4D, D] and dn [D, 4D], each
+    with a bias."""
+
+    name: str
+    B: int
+    S: int
+    D: int
+    H: int
+    description: str = ""
+
+
+BLOCKS = {
+    "tiny": BlockConfig("tiny", B=2, S=128, D=256, H=2,
+                        description="tiny DiT block: 2 x 128 tokens, D 256, 2 heads"),
+    "flux": BlockConfig("flux", B=8, S=4608, D=3072, H=24,
+                        description="FLUX.1-shaped DiT block: 8 images x 4608 tokens (4096 latent + "
+                                    "512 text), D 3072, 24 heads of 128, MLP 4D"),
+}
+
+BLOCK_LINEARS = ("qkv", "o", "up", "dn")
+
+
+def block_linear_shape(cfg: BlockConfig, name: str):
+    """(N, K) of one of the block's linears."""
+    D = cfg.D
+    return {"qkv": (3 * D, D), "o": (D, D), "up": (4 * D, D), "dn": (D, 4 * D)}[name]
+
+
+def block_weights(cfg: BlockConfig, seed: int = 0) -> dict:
+    """{name: (W [N, K] bf16 ~ N(0, 0.02^2), bias [N] bf16 ~ N(0, 0.02^2))} for the
+    block's four linears."""
+    out = {}
+    for i, name in enumerate(BLOCK_LINEARS):
+        N, K = block_linear_shape(cfg, name)
+        w = torch.randn(N, K, generator=_gen(seed, 200 + 2 * i), dtype=torch.float32) * 0.02
+        b = torch.randn(N, generator=_gen(seed, 201 + 2 * i), dtype=torch.float32) * 0.02
+        out[name] = (w.to(torch.bfloat16), b.to(torch.bfloat16))
+    return out
+
+
+def block_input(cfg: BlockConfig, seed: int = 0) -> torch.Tensor:
+    """The block's input x [B*S, D] bf16 ~ N(0, 1)."""
+    return torch.randn(cfg.B * cfg.S, cfg.D, generator=_gen(seed, 210), dtype=torch.float32).to(torch.bfloat16)
