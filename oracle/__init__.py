@@ -255,7 +255,7 @@ def select_contrastive(rewards, K: int, global_std: bool = True, with_transform:
     return idx, r
 
 
-# ---------------------------------------------------------------- DiT block (reading R11 of oracle.c's header)
+# ---------------------------------------------------------------- DiT block (reading R15 of oracle.c's header)
 
 def bf16_rne(x) -> np.ndarray:
     """Nearest bf16 (ties to even) of float64 values, as uint16 bits (same shape)."""
@@ -342,7 +342,7 @@ def nvfp4_linear(x_bits, w, bias_bits=None) -> np.ndarray:
 
 
 def dit_block(x_bits, w, bias, B: int, S: int, H: int) -> dict:
-    """The synthetic DiT block (reading R11 of oracle.c's header) on bf16 x [B*S, D]:
+    """The synthetic DiT block (reading R15 of oracle.c's header) on bf16 x [B*S, D]:
     qkv = lin(x, qkv); o = attention(qkv); h1 = bf16(lin(o, o) + x);
     out = bf16(lin(gelu(lin(h1, up)), dn) + h1), every lin an NVFP4 linear (per-row
     activation quantization) with bias.  w and bias: dicts keyed 'qkv', 'o', 'up',

@@ -32,28 +32,32 @@
  *   sf  = RNE_E4M3_sat(block_amax / (6 s))   one per 16 consecutive K-elements
  *   q   = RNE_E2M1_sat(x / (sf s))           sign kept, saturating at 6
  *
- * Readings where the pages are silent:
+ * Readings where the pages are silent (numbered as in the project's list of readings):
  *   R1  Scale arithmetic is IEEE fp32: d = 6*s, v = bamax / d (a division, not a
  *       reciprocal multiply), den = sff * s formed first, then q = x / den.
  *   R2  Merge: c = alpha / r (fp32); acc = fmaf chain over j = 0..r-1 of
  *       B[n,j]*A[j,k] starting from +0; w' = fmaf(c, acc, W[n,k]).
  *   R3  s = 0 gives sf = 0 for every block; a block whose den = sff*s is 0 emits
  *       code 0x0 for all its elements.
- *   R4  Code nibbles: byte k/2 holds code(k even) in bits 0..3, code(k odd) in
+ *   R7  Code nibbles: byte k/2 holds code(k even) in bits 0..3, code(k odd) in
  *       bits 4..7.  Scales are emitted row-major [rows, K/16] here.
- *   R5  Selection: top K/2 by (value desc, index asc), then bottom K/2 by
+ *   R9  Selection: top K/2 by (value desc, index asc), then bottom K/2 by
  *       (value asc, index asc); -0 == +0.
- *   R6  Transform: mean over the K selected rewards of the prompt; Z is the
+ *   R10 Transform: mean over the K selected rewards of the prompt; Z is the
  *       population standard deviation of all P*K selected rewards (global) or of
  *       the prompt's K (per prompt); Z == 0 gives r = 1/2.  Accumulation in fp64,
  *       r rounded to fp32 once.
- *   R11 The synthetic DiT block ([SOL] Stage 1 runs the NVFP4-quantized solver
+ *   R15 The synthetic DiT block ([SOL] Stage 1 runs the NVFP4-quantized solver
  *       over the DiT's linears; the block below is a FLUX-shaped stand-in):
  *       tensors between the steps are bf16, each rounded once to nearest-even
  *       from the exact value of its step: the NVFP4 and BF16 products (exact
  *       sums), the attention logits, the softmax probabilities, the GELU
- *       (tanh form) and the residual sums.  See orc_bf16_rne and the block
+ *       (tanh form) and the residual sums.  The softmax scale is the fp32 value of
+ *       1/sqrt(dh), applied to the bf16 logits.  See orc_bf16_rne and the block
  *       functions at the end.
+ *   R16 The GELU's tanh form is evaluated through the exact identity
+ *       (1 + tanh t)/2 = 1/(1 + e^(-2t)), the exponential of a non-positive
+ *       argument (the direct form cancels below x = -7).
  *
  * Every function is pinned by tests/test_oracle_*.py against closed forms,
  * brute force or a library routine; none is "parity unpinned".
@@ -211,7 +215,7 @@ void orc_merge(const void* W, int w_dtype, const float* A, const float* B, int r
 
 /* ------------------------------------------------------------------ quantize */
 
-/* Quantize rows [r0, r1) of x [rows,K] with second-level scale s, reading R1/R3/R4. */
+/* Quantize rows [r0, r1) of x [rows,K] with second-level scale s, readings R1/R3/R7. */
 static void quantize_rows(const float* x, int64_t r0, int64_t r1, int64_t K, float s,
                           uint8_t* codes, uint8_t* sf) {
     const int64_t nblk = K / 16;
@@ -418,7 +422,7 @@ static int by_value_asc(const void* pa, const void* pb) {
 }
 
 /* Contrastive filter ([SOL] Stage 1, [AIT] top K/2 and bottom K/2) and the
- * reward transform ([NFT] "Algorithm"), readings R5/R6.
+ * reward transform ([NFT] "Algorithm"), readings R9/R10.
  * rewards [P,N]; idx [P,K]: slots 0..K/2-1 the top seeds in descending order,
  * slots K/2..K-1 the bottom seeds in ascending order; r_out [P,K] or NULL. */
 int orc_select_contrastive(const float* rewards, int P, int N, int K, int global_std,
@@ -484,7 +488,7 @@ int orc_select_contrastive(const float* rewards, int P, int N, int K, int global
     return ORC_OK;
 }
 
-/* ------------------------------------------------------------------ DiT block (R11) */
+/* ------------------------------------------------------------------ DiT block (R15) */
 
 /* Nearest bf16 to x, ties to even: 8 significant bits over the fp32 exponent
  * range (below 2^-126 a fixed quantum of 2^-133, the bf16 subnormals); values

@@ -1,6 +1,6 @@
-"""The synthetic DiT block (reading R11 of oracle/oracle.c's header; Sol-RL project page, "Two-Stage Pipeline",
-Stage 1: the NVFP4-quantized solver runs the DiT's linears in NVFP4): its streaming
-steps, its attention and the whole block against the oracle.
+"""The synthetic DiT block (reading R15 of oracle/oracle.c's header; Sol-RL project
+page, "Two-Stage Pipeline", Stage 1: the NVFP4-quantized solver runs the DiT's linears
+in NVFP4): its streaming steps, its attention and the whole block against the oracle.
 
 The softmax and the GELU run in fp32 on the GPU and in double in the oracle, and the
 attention's logits and products accumulate in fp32 on the tensor cores against exact

@@ -1,4 +1,4 @@
-"""Pins of the oracle's synthetic DiT block (reading R11 in oracle/oracle.c's header): bf16
+"""Pins of the oracle's synthetic DiT block (reading R15 in oracle/oracle.c's header): bf16
 rounding, the attention softmax, the GELU (tanh form), the residual add, one
 attention head and the block's wiring.  Each is checked against a library routine
 (torch's float32 -> bf16 conversion and bf16 addition, scipy's softmax and erf), a
