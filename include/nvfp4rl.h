@@ -292,9 +292,12 @@ nvfp4_status nvfp4_requant_noalloc(const void* W, int w_dtype, const float* A, c
  *   out = bf16(lin(gelu(lin(h1, up)), dn) + h1)       gelu: tanh form, bf16 out
  * where lin(a, w) = nvfp4_gemm(nvfp4_act_quant(a), w) + bias (bf16 out), and w are
  * weights as written by nvfp4_requant: qkv [3D, D], o [D, D], up [4D, D], dn [D, 4D].
- * Every intermediate is bf16, rounded once to nearest-even; the attention's products
- * run on the BF16 GEMM (bf16_gemm), one image-head at a time.
- * Shapes: D % 64 == 0, H divides D with dh % 64 == 0, S % 64 == 0, T < 2^31.
+ * Every intermediate is bf16, rounded once to nearest-even.  The softmax scale is the
+ * fp32 value of 1/sqrt(dh); P is normalised before it is rounded.  The attention runs
+ * as one fused tensor-core kernel per call (two passes over the keys: the row maxima
+ * and sums, then P and P v), after a per-head transpose of v.
+ * Shapes: D % 64 == 0, H divides D with dh = D/H equal to 64 or 128, S % 64 == 0,
+ * B*H <= 65535, T < 2^31.
  */
 typedef struct {
     const uint8_t* codes; /* [N, K/2] E2M1 codes (nvfp4_requant) */
@@ -315,14 +318,16 @@ size_t nvfp4_dit_block_workspace_bytes(int64_t B, int64_t S, int64_t D, int64_t 
  *              owned by the caller, not used by anything else until the call's work on
  *              `stream` is done.
  * Errors as the calls it makes (NVFP4_ERR_SHAPE for the shape rules above, _NULL,
- * _ALIGN, _ARCH, _CUDA).  Enqueues about 3 B H + 14 kernels; allocates nothing.
+ * _ALIGN, _ARCH, _CUDA).  Enqueues 13 kernels; allocates nothing.
  */
 nvfp4_status nvfp4_dit_block(const void* x, int64_t B, int64_t S, int64_t D, int64_t H,
                              const nvfp4_linear_weights* w, void* out, void* workspace,
                              size_t workspace_bytes, void* stream);
 
-/* The block's attention alone: qkv [B*S, 3D] bf16 -> o [B*S, D] bf16, with a workspace of
- * nvfp4_dit_attention_workspace_bytes(B, S, D, H) bytes (shape rules as the block). */
+/* The block's attention alone: qkv [B*S, 3D] bf16 -> o [B*S, D] bf16 (o may not alias
+ * qkv), with a device workspace of nvfp4_dit_attention_workspace_bytes(B, S, D, H)
+ * bytes (256-byte aligned; it holds v transposed per head), shape rules as the block.
+ * Enqueues two kernels; allocates nothing. */
 size_t nvfp4_dit_attention_workspace_bytes(int64_t B, int64_t S, int64_t D, int64_t H);
 nvfp4_status nvfp4_dit_attention(const void* qkv, int64_t B, int64_t S, int64_t D, int64_t H, void* o,
                                  void* workspace, size_t workspace_bytes, void* stream);

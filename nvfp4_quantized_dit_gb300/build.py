@@ -21,7 +21,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libnvfp4rl.so")
-SOURCES = ["api.cu", "quant.cu", "select.cu", "gemm.cu", "merge_tc.cu", "block.cu"]
+SOURCES = ["api.cu", "quant.cu", "select.cu", "gemm.cu", "merge_tc.cu", "block.cu", "attn.cu"]
 HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "block.cuh"), os.path.join(INCLUDE, "nvfp4rl.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

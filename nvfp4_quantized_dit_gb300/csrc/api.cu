@@ -396,50 +396,39 @@ static size_t up256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 
 static bool block_shape_ok(int64_t B, int64_t S, int64_t D, int64_t H) {
     if (B <= 0 || S <= 0 || D <= 0 || H <= 0) return false;
-    if (D % 64 != 0 || D % H != 0 || (D / H) % 64 != 0 || S % 64 != 0) return false;
+    if (D % 64 != 0 || D % H != 0 || S % 64 != 0) return false;
+    const int64_t dh = D / H;
+    if (dh != 64 && dh != 128) return false;
     if (B * S > kMaxRows || B * H > 65535 || S > (1 << 20) || 4 * D > (1 << 20)) return false;
     return true;
 }
 
-// Attention scratch: per-head Q, K, V^T and O ([B*H, S, dh] each) and one head's logits.
-struct AttnLayout {
-    uint16_t *Q, *K, *Vt, *O, *L;
-    size_t bytes;
-};
-static AttnLayout attn_layout(void* base, int64_t B, int64_t S, int64_t D) {
-    AttnLayout l;
-    const size_t td = up256((size_t)B * S * D * 2);
-    uint8_t* p = static_cast<uint8_t*>(base);
-    l.Q = reinterpret_cast<uint16_t*>(p);
-    l.K = reinterpret_cast<uint16_t*>(p + td);
-    l.Vt = reinterpret_cast<uint16_t*>(p + 2 * td);
-    l.O = reinterpret_cast<uint16_t*>(p + 3 * td);
-    l.L = reinterpret_cast<uint16_t*>(p + 4 * td);
-    l.bytes = 4 * td + up256((size_t)S * S * 2);
-    return l;
-}
+// Attention scratch: V^T [B*H, dh, S] (the only operand the fused kernel does not read
+// from qkv directly).
+static size_t attn_bytes(int64_t B, int64_t S, int64_t D) { return up256((size_t)B * S * D * 2); }
 
 size_t nvfp4_dit_attention_workspace_bytes(int64_t B, int64_t S, int64_t D, int64_t H) {
     if (!block_shape_ok(B, S, D, H)) return 0;
-    return attn_layout(nullptr, B, S, D).bytes;
+    return attn_bytes(B, S, D);
 }
 
-// The attention of the block: heads split, per image-head L = Q K^T (BF16 GEMM),
-// P = softmax in place, O = P V (BF16 GEMM against V^T), heads merged into o.
+// The attention of the block: v transposed per head, then the fused two-pass kernel
+// (attn.cu), which reads q and k from qkv and writes o in the [B*S, D] layout.
 static nvfp4_status attention_run(const LaunchCtx& ctx, const uint16_t* qkv, int64_t B, int64_t S, int64_t D,
-                                  int64_t H, uint16_t* o, const AttnLayout& l, void* stream) {
-    const int64_t dh = D / H;
-    cudaError_t e = launch_heads_split(ctx, qkv, B, S, D, H, l.Q, l.K, l.Vt);
+                                  int64_t H, uint16_t* o, uint16_t* Vt) {
+    const int64_t dh = D / H, T = B * S;
+    CUtensorMap tq, tk, tv;
+    if (!encode_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qkv, (uint64_t)(3 * D), (uint64_t)T, (uint64_t)(3 * D) * 2,
+                   64, 128) ||
+        !encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qkv, (uint64_t)(3 * D), (uint64_t)T, (uint64_t)(3 * D) * 2,
+                   64, 64) ||
+        !encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Vt, (uint64_t)S, (uint64_t)(B * H * dh), (uint64_t)S * 2,
+                   64, (uint32_t)(dh / 2)))
+        return NVFP4_ERR_CUDA;
+    cudaError_t e = launch_heads_vt(ctx, qkv, B, S, D, H, Vt);
     if (e != cudaSuccess) return from_cuda(e);
     const float scale = 1.0f / sqrtf((float)dh);
-    for (int64_t z = 0; z < B * H; ++z) {
-        nvfp4_status st = bf16_gemm(l.Q + z * S * dh, l.K + z * S * dh, nullptr, l.L, S, S, dh, stream);
-        if (st != NVFP4_OK) return st;
-        if ((e = launch_softmax_rows(ctx, l.L, S, S, scale, l.L)) != cudaSuccess) return from_cuda(e);
-        st = bf16_gemm(l.L, l.Vt + z * dh * S, nullptr, l.O + z * S * dh, S, dh, S, stream);
-        if (st != NVFP4_OK) return st;
-    }
-    return from_cuda(launch_heads_merge(ctx, l.O, B, S, D, H, o));
+    return from_cuda(launch_attention(ctx, tq, tk, tv, o, B, S, D, H, scale));
 }
 
 nvfp4_status nvfp4_dit_attention(const void* qkv, int64_t B, int64_t S, int64_t D, int64_t H, void* o,
@@ -447,20 +436,19 @@ nvfp4_status nvfp4_dit_attention(const void* qkv, int64_t B, int64_t S, int64_t 
     if (!block_shape_ok(B, S, D, H)) return NVFP4_ERR_SHAPE;
     if (!qkv || !o || !workspace) return NVFP4_ERR_NULL;
     if (misaligned(qkv, 16) || misaligned(o, 16) || misaligned(workspace, 256)) return NVFP4_ERR_ALIGN;
-    const AttnLayout l = attn_layout(workspace, B, S, D);
-    if (workspace_bytes < l.bytes) return NVFP4_ERR_SHAPE;
+    if (workspace_bytes < attn_bytes(B, S, D)) return NVFP4_ERR_SHAPE;
     LaunchCtx ctx;
     const nvfp4_status st = resolve(stream, &ctx);
     if (st != NVFP4_OK) return st;
-    return attention_run(ctx, static_cast<const uint16_t*>(qkv), B, S, D, H, static_cast<uint16_t*>(o), l,
-                         stream);
+    return attention_run(ctx, static_cast<const uint16_t*>(qkv), B, S, D, H, static_cast<uint16_t*>(o),
+                         static_cast<uint16_t*>(workspace));
 }
 
 // Block scratch: R1 [3 T D] holds qkv, then o | a | d; R2 [4 T D] holds the attention's
-// Q | K | V^T | O, then u; h1 [T D]; L [S S]; the activation quantization of a D-wide
-// tensor (x, o, h1 in turn) and of the 4D-wide GELU output.
+// V^T, then u; h1 [T D]; the activation quantization of a D-wide tensor (x, o, h1 in
+// turn) and of the 4D-wide GELU output.
 struct BlockLayout {
-    uint16_t *r1, *r2, *h1, *L;
+    uint16_t *r1, *r2, *h1;
     uint8_t *qa_codes, *qa_sf, *qb_codes, *qb_sf;
     float *qa_s, *qb_s;
     size_t bytes;
@@ -479,7 +467,6 @@ static BlockLayout block_layout(void* base, int64_t B, int64_t S, int64_t D) {
     l.r1 = reinterpret_cast<uint16_t*>(take(3 * td));
     l.r2 = reinterpret_cast<uint16_t*>(take(4 * td));
     l.h1 = reinterpret_cast<uint16_t*>(take(td));
-    l.L = reinterpret_cast<uint16_t*>(take((size_t)S * S * 2));
     l.qa_codes = take((size_t)T * D / 2);
     l.qa_sf = take(nvfp4_sf_bytes(T, D));
     l.qa_s = reinterpret_cast<float*>(take((size_t)T * 4));
@@ -518,16 +505,7 @@ nvfp4_status nvfp4_dit_block(const void* x, int64_t B, int64_t S, int64_t D, int
         return nvfp4_gemm(c, sf, s, wi.codes, wi.sf, wi.s_t, wi.bias, y, T, N, K, stream);
     };
     if ((st = lin(xb, D, l.qa_codes, l.qa_sf, l.qa_s, w[0], 3 * D, qkv)) != NVFP4_OK) return st;
-    AttnLayout al;
-    const size_t td = up256((size_t)TD * 2);
-    uint8_t* r2b = reinterpret_cast<uint8_t*>(l.r2);
-    al.Q = reinterpret_cast<uint16_t*>(r2b);
-    al.K = reinterpret_cast<uint16_t*>(r2b + td);
-    al.Vt = reinterpret_cast<uint16_t*>(r2b + 2 * td);
-    al.O = reinterpret_cast<uint16_t*>(r2b + 3 * td);
-    al.L = l.L;
-    al.bytes = 0;
-    if ((st = attention_run(ctx, qkv, B, S, D, H, o, al, stream)) != NVFP4_OK) return st;
+    if ((st = attention_run(ctx, qkv, B, S, D, H, o, l.r2)) != NVFP4_OK) return st;
     if ((st = lin(o, D, l.qa_codes, l.qa_sf, l.qa_s, w[1], D, a)) != NVFP4_OK) return st;
     cudaError_t e = launch_add(ctx, a, xb, TD, l.h1);
     if (e != cudaSuccess) return from_cuda(e);

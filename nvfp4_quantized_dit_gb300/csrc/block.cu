@@ -1,11 +1,11 @@
-// The non-GEMM kernels of the synthetic DiT block (a FLUX-shaped stand-in for the
+// The streaming kernels of the synthetic DiT block (a FLUX-shaped stand-in for the
 // linears of the NVFP4-quantized solver, Sol-RL project page, "Two-Stage Pipeline",
-// Stage 1): head split and merge, the attention softmax, the GELU and the residual
-// add.  Every one is a streaming pass over bf16 data (HBM- or L2-bound); each rounds
-// its result to bf16 once, to nearest-even.
+// Stage 1): the per-head transpose of v for the fused attention (attn.cu), a row
+// softmax (the attention's softmax step as an entry point of its own), the GELU and
+// the residual add.  Every one is a streaming pass over bf16 data (HBM- or L2-bound);
+// each rounds its result to bf16 once, to nearest-even.
 //
-//   heads_split   qkv [B*S, 3D] -> Q, K [B*H, S, dh] and V^T [B*H, dh, S]
-//   heads_merge   O [B*H, S, dh] -> o [B*S, D]
+//   heads_vt      qkv [B*S, 3D] -> V^T [B*H, dh, S]
 //   softmax_rows  P = bf16(softmax(scale * L)) per row, in place allowed
 //   gelu          y = bf16(x/2 (1 + tanh(sqrt(2/pi) (x + 0.044715 x^3)))), fp32 (through
 //                 the logistic form of the same function)
@@ -21,25 +21,6 @@ __device__ __forceinline__ float bf(uint16_t h) { return __uint_as_float((uint32
 __device__ __forceinline__ uint16_t to_bf(float v) {
     const __nv_bfloat16 b = __float2bfloat16_rn(v);
     return *reinterpret_cast<const uint16_t*>(&b);
-}
-
-// Q and K rows: one thread per 16 bytes (8 bf16) of a head's row segment.
-__global__ void __launch_bounds__(kBlkThreads)
-    heads_split_qk_kernel(const uint16_t* __restrict__ qkv, int64_t B, int64_t S, int64_t D, int64_t H,
-                          uint16_t* __restrict__ Q, uint16_t* __restrict__ Kh) {
-    const int64_t dh = D / H, per_row = D / 8;  // 16-byte pieces per token for q (and k)
-    const int64_t total = B * S * per_row * 2;
-    for (int64_t i = (int64_t)blockIdx.x * kBlkThreads + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * kBlkThreads) {
-        const int64_t which = i / (B * S * per_row);  // 0: q, 1: k
-        const int64_t r = i - which * (B * S * per_row);
-        const int64_t t = r / per_row, p = r - t * per_row;
-        const int64_t b = t / S, s = t - b * S;
-        const int64_t h = (p * 8) / dh, c = p * 8 - h * dh;
-        const uint4 v = *reinterpret_cast<const uint4*>(qkv + t * 3 * D + which * D + p * 8);
-        uint16_t* dst = (which == 0 ? Q : Kh) + ((b * H + h) * S + s) * dh + c;
-        *reinterpret_cast<uint4*>(dst) = v;
-    }
 }
 
 // V transposed per head, through a 64 x 64 shared-memory tile: block (tile of S, tile of
@@ -62,21 +43,6 @@ __global__ void __launch_bounds__(kBlkThreads)
         const int rc = i / kTr, rs = i % kTr;
         const int64_t s = s0 + rs, c = c0 + rc;
         if (s < S && c < dh) Vt[(z * dh + c) * S + s] = tile[rs][rc];
-    }
-}
-
-__global__ void __launch_bounds__(kBlkThreads)
-    heads_merge_kernel(const uint16_t* __restrict__ O, int64_t B, int64_t S, int64_t D, int64_t H,
-                       uint16_t* __restrict__ o) {
-    const int64_t dh = D / H, per_row = D / 8;
-    const int64_t total = B * S * per_row;
-    for (int64_t i = (int64_t)blockIdx.x * kBlkThreads + threadIdx.x; i < total;
-         i += (int64_t)gridDim.x * kBlkThreads) {
-        const int64_t t = i / per_row, p = i - t * per_row;
-        const int64_t b = t / S, s = t - b * S;
-        const int64_t h = (p * 8) / dh, c = p * 8 - h * dh;
-        *reinterpret_cast<uint4*>(o + t * D + p * 8) =
-            *reinterpret_cast<const uint4*>(O + ((b * H + h) * S + s) * dh + c);
     }
 }
 
@@ -181,20 +147,11 @@ unsigned stream_grid(int64_t work, const LaunchCtx& ctx) {
 
 }  // namespace
 
-cudaError_t launch_heads_split(const LaunchCtx& ctx, const uint16_t* qkv, int64_t B, int64_t S, int64_t D,
-                               int64_t H, uint16_t* Q, uint16_t* K, uint16_t* Vt) {
-    heads_split_qk_kernel<<<stream_grid(B * S * D / 4, ctx), kBlkThreads, 0, ctx.stream>>>(qkv, B, S, D, H, Q, K);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
+cudaError_t launch_heads_vt(const LaunchCtx& ctx, const uint16_t* qkv, int64_t B, int64_t S, int64_t D, int64_t H,
+                            uint16_t* Vt) {
     const int64_t dh = D / H;
     const dim3 grid((unsigned)((S + kTr - 1) / kTr), (unsigned)((dh + kTr - 1) / kTr), (unsigned)(B * H));
     heads_split_vt_kernel<<<grid, kBlkThreads, 0, ctx.stream>>>(qkv, S, D, H, Vt);
-    return cudaGetLastError();
-}
-
-cudaError_t launch_heads_merge(const LaunchCtx& ctx, const uint16_t* O, int64_t B, int64_t S, int64_t D,
-                               int64_t H, uint16_t* o) {
-    heads_merge_kernel<<<stream_grid(B * S * D / 8, ctx), kBlkThreads, 0, ctx.stream>>>(O, B, S, D, H, o);
     return cudaGetLastError();
 }
 

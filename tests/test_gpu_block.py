@@ -72,8 +72,12 @@ def test_gelu_and_add():
     assert np.array_equal(s, orc.add_bf16(np_(xd), np_(yd)))
 
 
-@pytest.mark.parametrize("B,S,D,H", [(2, 256, 256, 2), (1, 512, 384, 3)])
+@pytest.mark.parametrize("B,S,D,H", [(2, 256, 256, 2), (1, 512, 384, 3), (2, 320, 256, 4), (3, 192, 128, 1),
+                                     (1, 4608, 256, 2)])
 def test_attention(B, S, D, H):
+    """The fused attention kernel: head widths 128 and 64, several 256-row query blocks,
+    S % 256 != 0 (a query block with rows past S in one or both CTAs) and S % 128 == 64
+    (a last key tile of 64 keys), and 4608 keys (36 tiles, both passes over the ring)."""
     require_gpu()
     rng = np.random.default_rng(B * S + D)
     qkv = _bf16(rng.standard_normal((B * S, 3 * D)) * 0.5)
@@ -192,4 +196,6 @@ def test_block_shape_rules():
     require_gpu()
     assert nv.dit_block_workspace_bytes(1, 100, 256, 2) == 0      # S % 64
     assert nv.dit_block_workspace_bytes(1, 128, 256, 3) == 0      # H does not divide D into 64s
+    assert nv.dit_block_workspace_bytes(1, 128, 384, 2) == 0      # dh = 192: the attention takes 64 or 128
+    assert nv.dit_attention_workspace_bytes(2, 320, 256, 4) == 2 * 320 * 256 * 2  # v transposed
     assert nv.dit_block_workspace_bytes(8, 4608, 3072, 24) > 0
