@@ -24,6 +24,7 @@ times the CPU oracle on a bounded sample of the same workload instead (no GPU wo
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
 import math
@@ -503,7 +504,7 @@ def evt_report(device, P=2048, K=24, delta=EVT_DELTA, seed=0):
 
 # ----------------------------------------------------------------------------- our arm
 
-def dit_block_report(device, pk, fp4_peak, reps=5):
+def dit_block_report(device, pk, fp4_peak, reps=5, images=None):
     """The FLUX.1-shaped synthetic DiT block (8 images x 4608 tokens, D 3072, 24 heads):
     one nvfp4_dit_block call on resident inputs, median of `reps` (CUDA events on the
     launching stream; the activations, 226 MB, exceed L2), and its attention alone.
@@ -514,6 +515,8 @@ def dit_block_report(device, pk, fp4_peak, reps=5):
     import nvfp4_quantized_dit_gb300 as nv
     import workloads
     cfg = workloads.BLOCKS["flux"]
+    if images is not None:
+        cfg = dataclasses.replace(cfg, B=images, description=f"{cfg.description}; {images} image(s)")
     B, S, D, H = cfg.B, cfg.S, cfg.D, cfg.H
     T = B * S
     x = workloads.block_input(cfg, seed=0).to(device)
@@ -1035,6 +1038,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-iteration", action="store_true", help="skip the iteration-shaped batch")
     ap.add_argument("--no-peak-probe", action="store_true", help="skip cuBLAS's NVFP4 8192^3 reference")
     ap.add_argument("--no-block", action="store_true", help="skip the FLUX.1-shaped DiT block timing")
+    ap.add_argument("--block-only", action="store_true",
+                    help="time only the DiT block (one JSON object; for profiling the block's kernels)")
+    ap.add_argument("--block-images", type=int, default=None,
+                    help="images of the block-only run (default: the workload's 8)")
     ap.add_argument("--rows", type=int, default=None,
                     help="override M (a smaller case for profiling; the default is the config's)")
     args = ap.parse_args(argv)
@@ -1050,6 +1057,13 @@ def main(argv=None):
         # no launcher: start the replicas here, one process per GPU, and pass on
         # their exit status (rank 0 prints the line)
         return subprocess.call(replica_command(args.gpus, argv))
+    if args.block_only:
+        import torch
+        pk, _ = peaks()
+        out = {"dit_block": dit_block_report(torch.device("cuda", 0), pk, pk["bf16_tflops"] * NOMINAL_FP4_OVER_BF16,
+                                             images=args.block_images)}
+        print(json.dumps(out), flush=True)
+        return 0
     out = run_reference(args) if args.impl == "reference" else run_ours(args)
     if out is not None:
         print(json.dumps(out), flush=True)

@@ -417,18 +417,16 @@ size_t nvfp4_dit_attention_workspace_bytes(int64_t B, int64_t S, int64_t D, int6
 static nvfp4_status attention_run(const LaunchCtx& ctx, const uint16_t* qkv, int64_t B, int64_t S, int64_t D,
                                   int64_t H, uint16_t* o, uint16_t* Vt) {
     const int64_t dh = D / H, T = B * S;
-    CUtensorMap tq, tk, tv;
-    if (!encode_2d(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qkv, (uint64_t)(3 * D), (uint64_t)T, (uint64_t)(3 * D) * 2,
+    CUtensorMap tqk, tv;
+    if (!encode_2d(&tqk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qkv, (uint64_t)(3 * D), (uint64_t)T, (uint64_t)(3 * D) * 2,
                    64, 128) ||
-        !encode_2d(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qkv, (uint64_t)(3 * D), (uint64_t)T, (uint64_t)(3 * D) * 2,
-                   64, 64) ||
         !encode_2d(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, Vt, (uint64_t)S, (uint64_t)(B * H * dh), (uint64_t)S * 2,
                    64, (uint32_t)(dh / 2)))
         return NVFP4_ERR_CUDA;
     cudaError_t e = launch_heads_vt(ctx, qkv, B, S, D, H, Vt);
     if (e != cudaSuccess) return from_cuda(e);
     const float scale = 1.0f / sqrtf((float)dh);
-    return from_cuda(launch_attention(ctx, tq, tk, tv, o, B, S, D, H, scale));
+    return from_cuda(launch_attention(ctx, tqk, tv, o, B, S, D, H, scale));
 }
 
 nvfp4_status nvfp4_dit_attention(const void* qkv, int64_t B, int64_t S, int64_t D, int64_t H, void* o,

@@ -12,21 +12,24 @@
 //
 // One cluster of two CTAs per (image-head, 256 query rows); every MMA is a 2-CTA
 // `cta_group::2` MMA (M = 256: each CTA's 128 query rows):
-//   L tile   M = 256, N = 128 keys (64 per CTA), K = dh;   A = Q (shared memory),
+//   L tile   M = 256, N = 256 keys (128 per CTA), K = dh;  A = Q (shared memory),
 //            B = K rows (shared memory)
-//   O       M = 256, N = dh (dh/2 per CTA), K = 128 keys; A = P (tensor memory),
+//   O       M = 256, N = dh (dh/2 per CTA), K = 256 keys; A = P (tensor memory),
 //            B = V^T rows (shared memory)
 // Q and K tiles come from qkv by TMA (128-byte swizzle); V^T [B*H*dh, S] is written
 // beforehand by the block's transpose kernel.  Keys past S (the last tile when
-// S % 128 == 64) are masked: their logits count as -inf, their P as 0.
+// S % 256 != 0) are masked: their logits count as -inf, their P as 0.
 //
-// Tensor memory per CTA (512 columns): L tiles in 0..127 and 128..255 (double
-// buffer), P tiles in 256..319 and 320..383 (64 columns of bf16 pairs each), O in
-// 384 .. 384 + dh - 1.
+// Tensor memory per CTA (512 columns): the L tile in 0..255, P in 256..383 (bf16
+// pairs), O in 384 .. 384 + dh - 1.  The L tile is read into registers at once, so
+// the next tile's MMAs run while the softmax works on the last one.
 //
 // Warps: 0 TMA producer (both CTAs: Q once, then K tiles for pass 1 and K, V tiles
 // for pass 2); 1 tensor-memory allocation and, in the even CTA, the MMA issuer;
-// 2..5 softmax and output (one row per thread: tensor-memory lane quarter = warp % 4).
+// 2..17 softmax and output: one query row per thread (tensor-memory lane quarter =
+// warp % 4), four warps per quarter, each with a quarter of the columns of every L
+// tile and of O; the four partial maxima and sums of a row are combined once,
+// between the passes.
 // Every wait is bounded (mbar_wait); on expiry the kernel records NVFP4_ERR_TIMEOUT,
 // lets its copies and MMAs land, frees tensor memory and returns.
 #include "block.cuh"
@@ -36,11 +39,14 @@ namespace {
 
 constexpr int kPairCtas = 2;
 constexpr int kRowsCta = 128;    // query rows per CTA
-constexpr int kTileKeys = 128;   // keys per L tile (64 per CTA)
-constexpr int kStagesK = 4;
-constexpr int kStagesV = 4;
+constexpr int kTileKeys = 256;   // keys per L tile (128 per CTA)
+constexpr int kStagesK = 3;
+constexpr int kStagesV = 2;
 constexpr int kSoftWarp0 = 2;
-constexpr int kSoftWarps = 4;
+constexpr int kSoftWarps = 16;                   // four per tensor-memory lane quarter
+constexpr int kSlices = kSoftWarps / 4;          // column slices of a tile, one per warp of a quarter
+constexpr int kSliceCols = kTileKeys / kSlices;  // 64 logits of a row per warp and tile
+constexpr int kChunk = 32;                       // columns per tensor-memory load
 constexpr int kAttnThreads = (kSoftWarp0 + kSoftWarps) * 32;
 constexpr uint32_t kTmemColsAttn = 512;
 constexpr uint32_t kColL = 0, kColP = 256, kColO = 384;
@@ -53,11 +59,11 @@ struct AttnCfg {
     static_assert(kDh == 64 || kDh == 128, "head width");
     static constexpr uint32_t kQSub = kRowsCta * 128;                 // one 64-column atom of Q
     static constexpr uint32_t kQBytes = kQSub * (kDh / 64);
-    static constexpr uint32_t kKSub = (kTileKeys / kPairCtas) * 128;   // 64 keys x 64 columns
+    static constexpr uint32_t kKSub = (kTileKeys / kPairCtas) * 128;   // 128 keys x 64 columns
     static constexpr uint32_t kKBytes = kKSub * (kDh / 64);
     static constexpr uint32_t kVSub = (kDh / kPairCtas) * 128;         // dh/2 rows x 64 keys
     static constexpr uint32_t kVBytes = kVSub * (kTileKeys / 64);
-    static constexpr uint32_t kBarBytes = 512;
+    static constexpr uint32_t kBarBytes = 512 + kSlices * 2 * kRowsCta * 4;  // barriers; (m, sum) per slice and row
     static constexpr uint32_t kSmemBytes =
         1024 + kQBytes + kStagesK * kKBytes + kStagesV * kVBytes + kBarBytes;
     // kind::f16, bf16 A and B, fp32 accumulator, both K-major, M = 256.
@@ -67,6 +73,7 @@ struct AttnCfg {
 };
 static_assert(AttnCfg<128>::kSmemBytes <= 232448, "shared memory budget");
 static_assert(kColO + 128 <= kTmemColsAttn, "tensor memory budget");
+static_assert(30 * 8 + 8 <= 512, "barrier area");
 
 struct AttnArgs {
     uint16_t* o;
@@ -75,9 +82,12 @@ struct AttnArgs {
     int* status;
 };
 
+// 2^x (hardware approximation; results below 2^-126 flush to zero, which changes no
+// sum of exponentials that includes the row maximum's 1, nor any P that bf16 keeps
+// above the products' rounding).
 __device__ __forceinline__ float ex2(float x) {
     float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
 
@@ -94,25 +104,42 @@ __device__ __forceinline__ uint32_t bmax2(uint32_t a, uint32_t b) {
     return r;
 }
 
-// The 128 logits of this thread's row in one L tile, rounded to bf16 (pairs), with
-// the columns at and past `valid` set to -inf.
-__device__ __forceinline__ void round_tile(const uint32_t (&v)[4][32], int valid, uint32_t (&lb)[64]) {
+__device__ __forceinline__ float lg2(float x) {
+    float y;
+    asm("lg2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ void tmem_ld_32x32b_x16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32"
+        " {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+// kChunk logits of this thread's row (columns col .. col + kChunk - 1 of an L tile),
+// rounded to bf16 (pairs) into lb, with the columns at and past `valid` set to -inf.
+__device__ __forceinline__ void round_chunk(const uint32_t (&v)[kChunk], int col, int valid, uint32_t* lb) {
 #pragma unroll
-    for (int c = 0; c < 4; ++c)
+    for (int i = 0; i < kChunk / 2; ++i) lb[i] = bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+    if (col + kChunk > valid) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-            lb[c * 16 + i] = bf16x2(__uint_as_float(v[c][2 * i]), __uint_as_float(v[c][2 * i + 1]));
-    if (valid < kTileKeys) {
-#pragma unroll
-        for (int i = 0; i < 64; ++i)
-            if (2 * i >= valid) lb[i] = 0xFF80FF80u;  // both halves -inf (valid is even)
+        for (int i = 0; i < kChunk / 2; ++i)
+            if (col + 2 * i >= valid) lb[i] = 0xFF80FF80u;  // both halves -inf (valid is even)
     }
+}
+
+// The two fp32 values of a bf16 pair.
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
 }
 
 template <int kDh>
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    attn_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                const __grid_constant__ CUtensorMap tmap_v, const AttnArgs args) {
+    attn_kernel(const __grid_constant__ CUtensorMap tmap_qk, const __grid_constant__ CUtensorMap tmap_v,
+                const AttnArgs args) {
     using C = AttnCfg<kDh>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -126,14 +153,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint64_t* k_empty = k_full + kStagesK;
     uint64_t* v_full = k_empty + kStagesK;
     uint64_t* v_empty = v_full + kStagesV;
-    uint64_t* s_full = v_empty + kStagesV;   // [2]
-    uint64_t* s_empty = s_full + 2;          // [2], even CTA
-    uint64_t* p_full = s_empty + 2;          // [2], even CTA
-    uint64_t* p_free = p_full + 2;           // [2]
-    uint64_t* o_full = p_free + 2;
+    uint64_t* s_full = v_empty + kStagesV;   // the L tile is in tensor memory
+    uint64_t* s_empty = s_full + 1;          // ... and has been read (even CTA)
+    uint64_t* p_full = s_empty + 1;          // P is in tensor memory (even CTA)
+    uint64_t* p_free = p_full + 1;           // ... and has been read by the P v MMAs
+    uint64_t* o_full = p_free + 1;
     uint64_t* drain = o_full + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* stats_ready = drain + 1;       // every softmax thread has written its (m, sum)
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stats_ready + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    float* row_stats = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 512);  // [slice][m|sum][row]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
@@ -154,20 +183,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mbar_init(&v_full[s], 1);
             mbar_init(&v_empty[s], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&s_full[i], 1);
-            mbar_init(&s_empty[i], kSoftWarps * kPairCtas);
-            mbar_init(&p_full[i], kSoftWarps * kPairCtas);
-            mbar_init(&p_free[i], 1);
-        }
+        mbar_init(s_full, 1);
+        mbar_init(s_empty, kSoftWarps * kPairCtas);
+        mbar_init(p_full, kSoftWarps * kPairCtas);
+        mbar_init(p_free, 1);
         mbar_init(o_full, 1);
         mbar_init(drain, 1);
+        mbar_init(stats_ready, kSoftWarps * 32);
         *abort_flag = 0;
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmap_q);
-        prefetch_tmap(&tmap_k);
+        prefetch_tmap(&tmap_qk);
         prefetch_tmap(&tmap_v);
     }
     if (warp == 1) {
@@ -192,7 +219,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (leader) mbar_arrive_expect_tx(q_full, kPairCtas * C::kQBytes);
 #pragma unroll
             for (int i = 0; i < kDh / 64; ++i)
-                tma_load_2d_pair(&tmap_q, q_full_e, sq + i * C::kQSub, qcol + 64 * i,
+                tma_load_2d_pair(&tmap_qk, q_full_e, sq + i * C::kQSub, qcol + 64 * i,
                                  row0 + qb * (kRowsCta * kPairCtas) + (int)rank * kRowsCta);
             int kc = 0, vc = 0;
             for (int pass = 0; ok && pass < 2; ++pass) {
@@ -208,7 +235,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         uint8_t* dst = sk + s * C::kKBytes;
 #pragma unroll
                         for (int i = 0; i < kDh / 64; ++i)
-                            tma_load_2d_pair(&tmap_k, k_full_e + 8u * (uint32_t)s, dst + i * C::kKSub, kcol + 64 * i,
+                            tma_load_2d_pair(&tmap_qk, k_full_e + 8u * (uint32_t)s, dst + i * C::kKSub, kcol + 64 * i,
                                              row0 + j * kTileKeys + (int)rank * (kTileKeys / kPairCtas));
                         ++kc;
                     }
@@ -255,36 +282,35 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             bool ok = mbar_wait(q_full, 0, args.status, abort_flag, kAttnWaitNs);
             bool any = false;
             int kc = 0, g = 0;
-            // One L tile: wait for its K stage and a free L buffer, dh/16 MMAs, release.
+            // One L tile: wait for its K stage and for the previous tile to have been read,
+            // dh/16 MMAs, release the stage, announce the tile.
             auto issue_l = [&]() -> bool {
-                const int s = kc % kStagesK, lb = g & 1;
+                const int s = kc % kStagesK;
                 if (!mbar_wait(&k_full[s], (uint32_t)((kc / kStagesK) & 1), args.status, abort_flag, kAttnWaitNs) ||
-                    !mbar_wait<true>(&s_empty[lb], (uint32_t)(((g >> 1) & 1) ^ 1), args.status, abort_flag,
-                                     kAttnWaitNs))
+                    !mbar_wait<true>(s_empty, (uint32_t)((g & 1) ^ 1), args.status, abort_flag, kAttnWaitNs))
                     return false;
                 tc_fence_after_sync();
                 const uint64_t kd = k_desc0 + (uint64_t)((s * C::kKBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < kDh / 16; ++kk) {
-                    const uint64_t off = (uint64_t)((kk >> 2) * 0 + (kk & 3) * 2);
-                    mma_bf16_pair(tmem_base + kColL + (uint32_t)(lb * kTileKeys),
-                                  q_desc + (uint64_t)((kk >> 2) * (C::kQSub >> 4)) + off,
-                                  kd + (uint64_t)((kk >> 2) * (C::kKSub >> 4)) + off, idesc_l, kk > 0 ? 1u : 0u);
-                }
+                for (int kk = 0; kk < kDh / 16; ++kk)
+                    mma_bf16_pair(tmem_base + kColL,
+                                  q_desc + (uint64_t)((kk >> 2) * (C::kQSub >> 4) + (kk & 3) * 2),
+                                  kd + (uint64_t)((kk >> 2) * (C::kKSub >> 4) + (kk & 3) * 2), idesc_l, kk > 0 ? 1u : 0u);
                 any = true;
                 mma_commit_pair_multicast(&k_empty[s], kBoth);
-                mma_commit_pair_multicast(&s_full[lb], kBoth);
+                mma_commit_pair_multicast(s_full, kBoth);
                 ++kc;
                 ++g;
                 return true;
             };
-            for (int j = 0; ok && j < n_tiles; ++j) ok = issue_l();  // pass 1
-            if (ok) ok = issue_l();                                  // pass 2, tile 0
+            // L tiles g = 0 .. 2n-1 in order (pass 1, then pass 2); in pass 2 tile j + 1
+            // is queued before the P v of tile j, so it is ready when the softmax is.
+            for (int j = 0; ok && j < n_tiles + 1; ++j) ok = issue_l();
             for (int j = 0; ok && j < n_tiles; ++j) {
                 if (j + 1 < n_tiles && !(ok = issue_l())) break;
-                const int s = j % kStagesV, pb = j & 1;
+                const int s = j % kStagesV;
                 if (!mbar_wait(&v_full[s], (uint32_t)((j / kStagesV) & 1), args.status, abort_flag, kAttnWaitNs) ||
-                    !mbar_wait<true>(&p_full[pb], (uint32_t)((j >> 1) & 1), args.status, abort_flag, kAttnWaitNs)) {
+                    !mbar_wait<true>(p_full, (uint32_t)(j & 1), args.status, abort_flag, kAttnWaitNs)) {
                     ok = false;
                     break;
                 }
@@ -292,11 +318,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const uint64_t vd = v_desc0 + (uint64_t)((s * C::kVBytes) >> 4);
 #pragma unroll
                 for (int kk = 0; kk < kTileKeys / 16; ++kk)
-                    mma_bf16_pair_ta(tmem_base + kColO, tmem_base + kColP + (uint32_t)(pb * 64) + 8u * (uint32_t)kk,
+                    mma_bf16_pair_ta(tmem_base + kColO, tmem_base + kColP + 8u * (uint32_t)kk,
                                      vd + (uint64_t)((kk >> 2) * (C::kVSub >> 4) + (kk & 3) * 2), idesc_o,
                                      (j > 0 || kk > 0) ? 1u : 0u);
                 mma_commit_pair_multicast(&v_empty[s], kBoth);
-                mma_commit_pair_multicast(&p_free[pb], kBoth);
+                mma_commit_pair_multicast(p_free, kBoth);
             }
             if (ok) mma_commit_pair_multicast(o_full, kBoth);
             if (*abort_flag && any) {
@@ -307,68 +333,98 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
     } else {
         // ------------------------------------------------ softmax and output (both CTAs)
-        const int quarter = warp & 3;
+        // Warp w: tensor-memory lanes 32 (w % 4) .. +31 (one query row per thread) and
+        // column slice (w - 2) / 4 of every L tile and of O.
+        const int quarter = warp & 3, slice = (warp - kSoftWarp0) / 4;
+        const int row = quarter * 32 + lane;
         const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
         const uint32_t s_empty_e = map_to_rank(smem_u32(s_empty), 0);
         const uint32_t p_full_e = map_to_rank(smem_u32(p_full), 0);
         const float c = args.c;
-        float m = -INFINITY, sum = 0.0f, inv = 0.0f;
+        const float2 c2 = make_float2(c, c);
+        const int col0 = slice * kSliceCols;
+        float m = -INFINITY, sum = 0.0f, mc2 = 0.0f;
         bool ok = true;
         for (int g = 0; ok && g < 2 * n_tiles; ++g) {
             const int j = g < n_tiles ? g : g - n_tiles;
-            const int lb = g & 1;
             const int valid = min(kTileKeys, S - j * kTileKeys);
-            ok = mbar_wait(&s_full[lb], (uint32_t)((g >> 1) & 1), args.status, abort_flag, kAttnWaitNs);
+            ok = mbar_wait(s_full, (uint32_t)(g & 1), args.status, abort_flag, kAttnWaitNs);
             ok = __all_sync(0xFFFFFFFFu, ok);  // tcgen05.ld is .sync.aligned
             if (!ok) break;
             tc_fence_after_sync();
-            uint32_t v[4][32];
+            uint32_t lbits[kSliceCols / 2];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) tmem_ld_32x32b_x32(lane_base + kColL + (uint32_t)(lb * kTileKeys + q * 32), v[q]);
-            tmem_ld_wait();
+            for (int ch = 0; ch < kSliceCols / kChunk; ++ch) {
+                uint32_t v[kChunk];
+                tmem_ld_32x32b_x32(lane_base + kColL + (uint32_t)(col0 + ch * kChunk), v);
+                tmem_ld_wait();
+                round_chunk(v, col0 + ch * kChunk, valid, lbits + ch * (kChunk / 2));
+            }
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(s_empty_e + 8u * (uint32_t)lb);
-            uint32_t lbits[64];
-            round_tile(v, valid, lbits);
+            if (lane == 0) mbar_arrive_cluster(s_empty_e);
             if (g < n_tiles) {
-                // Pass 1: running maximum and rescaled sum of exponentials.
+                // Pass 1: running maximum and rescaled sum of exponentials (packed pairs,
+                // four partial sums, so that the additions do not form one chain).
                 uint32_t mx2 = lbits[0];
 #pragma unroll
-                for (int i = 1; i < 64; ++i) mx2 = bmax2(mx2, lbits[i]);
+                for (int i = 1; i < kSliceCols / 2; ++i) mx2 = bmax2(mx2, lbits[i]);
                 const float tmax = fmaxf(__uint_as_float(mx2 << 16), __uint_as_float(mx2 & 0xFFFF0000u));
                 const float m_new = fmaxf(m, tmax);
-                const float mc = m_new * c;
-                float acc = sum * ex2(fmaf(m, c, -mc));
+                // A slice whose columns so far were all masked (m_new = -inf) keeps sum = 0:
+                // with the offset 0 every term is 2^-inf = 0 (no inf - inf).
+                const float mc = m_new == -INFINITY ? 0.0f : m_new * c;
+                const float2 nmc = make_float2(-mc, -mc);
+                float2 acc[4] = {make_float2(sum * ex2(fmaf(m, c, -mc)), 0.0f), make_float2(0.0f, 0.0f),
+                                 make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    acc += ex2(fmaf(__uint_as_float(lbits[i] << 16), c, -mc));
-                    acc += ex2(fmaf(__uint_as_float(lbits[i] & 0xFFFF0000u), c, -mc));
+                for (int i = 0; i < kSliceCols / 2; ++i) {
+                    const float2 a = __ffma2_rn(unpack_bf16x2(lbits[i]), c2, nmc);
+                    acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(ex2(a.x), ex2(a.y)));
                 }
-                sum = acc;
+                const float2 s01 = __fadd2_rn(acc[0], acc[1]), s23 = __fadd2_rn(acc[2], acc[3]);
+                const float2 s4 = __fadd2_rn(s01, s23);
+                sum = s4.x + s4.y;
                 m = m_new;
-                if (g == n_tiles - 1) inv = 1.0f / sum;
+                if (g == n_tiles - 1) {
+                    // The row's slices: combine their (m, sum) through shared memory.
+                    row_stats[(slice * 2 + 0) * kRowsCta + row] = m;
+                    row_stats[(slice * 2 + 1) * kRowsCta + row] = sum;
+                    mbar_arrive(stats_ready);
+                    ok = mbar_wait(stats_ready, 0, args.status, abort_flag, kAttnWaitNs);
+                    ok = __all_sync(0xFFFFFFFFu, ok);
+                    if (!ok) break;
+                    float ms[kSlices], ss[kSlices], mm = -INFINITY;
+#pragma unroll
+                    for (int k = 0; k < kSlices; ++k) {
+                        ms[k] = row_stats[(k * 2 + 0) * kRowsCta + row];
+                        ss[k] = row_stats[(k * 2 + 1) * kRowsCta + row];
+                        mm = fmaxf(mm, ms[k]);
+                    }
+                    float total = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < kSlices; ++k) total += ss[k] * ex2(fmaf(ms[k], c, -mm * c));
+                    // P = exp(scale (l - m)) / sum = 2^(l c - (m c + log2(sum))).
+                    mc2 = fmaf(mm, c, lg2(total));
+                }
             } else {
                 // Pass 2: P = bf16(exp(scale (l - m)) / sum) into tensor memory.
-                const float mc = m * c;
-                uint32_t p[2][32];
+                const float2 nmc = make_float2(-mc2, -mc2);
+                uint32_t p[kSliceCols / 2];
 #pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    const float e0 = ex2(fmaf(__uint_as_float(lbits[i] << 16), c, -mc)) * inv;
-                    const float e1 = ex2(fmaf(__uint_as_float(lbits[i] & 0xFFFF0000u), c, -mc)) * inv;
-                    p[i >> 5][i & 31] = bf16x2(e0, e1);
+                for (int i = 0; i < kSliceCols / 2; ++i) {
+                    const float2 a = __ffma2_rn(unpack_bf16x2(lbits[i]), c2, nmc);
+                    p[i] = bf16x2(ex2(a.x), ex2(a.y));
                 }
-                const int pb = j & 1;
-                ok = mbar_wait(&p_free[pb], (uint32_t)(((j >> 1) & 1) ^ 1), args.status, abort_flag, kAttnWaitNs);
+                ok = mbar_wait(p_free, (uint32_t)((j & 1) ^ 1), args.status, abort_flag, kAttnWaitNs);
                 ok = __all_sync(0xFFFFFFFFu, ok);  // tcgen05.st is .sync.aligned
                 if (!ok) break;
                 tc_fence_after_sync();
-                tmem_st_32x32b_x32(lane_base + kColP + (uint32_t)(pb * 64), p[0]);
-                tmem_st_32x32b_x32(lane_base + kColP + (uint32_t)(pb * 64 + 32), p[1]);
+                tmem_st_32x32b_x32(lane_base + kColP + (uint32_t)(slice * (kSliceCols / 2)), p);
                 tmem_st_wait();
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(p_full_e + 8u * (uint32_t)pb);
+                if (lane == 0) mbar_arrive_cluster(p_full_e);
             }
         }
         if (ok) {
@@ -376,23 +432,27 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             ok = __all_sync(0xFFFFFFFFu, ok);
         }
         if (ok) {
+            // O: this warp's dh / 4 columns of its 32 rows.
+            constexpr int kOCols = kDh / kSlices;
             tc_fence_after_sync();
-            uint32_t v[kDh / 32][32];
-#pragma unroll
-            for (int q = 0; q < kDh / 32; ++q) tmem_ld_32x32b_x32(lane_base + kColO + (uint32_t)(q * 32), v[q]);
+            uint32_t v[kOCols];
+            const uint32_t oaddr = lane_base + kColO + (uint32_t)(slice * kOCols);
+            if constexpr (kOCols == 32) {
+                tmem_ld_32x32b_x32(oaddr, v);
+            } else {
+                tmem_ld_32x32b_x16(oaddr, v);
+            }
             tmem_ld_wait();
-            const int s = qb * (kRowsCta * kPairCtas) + (int)rank * kRowsCta + quarter * 32 + lane;
+            const int s = qb * (kRowsCta * kPairCtas) + (int)rank * kRowsCta + row;
             if (s < S) {
-                uint4* dst = reinterpret_cast<uint4*>(args.o + ((int64_t)b * S + s) * D + (int64_t)h * kDh);
+                uint4* dst = reinterpret_cast<uint4*>(args.o + ((int64_t)b * S + s) * D + (int64_t)h * kDh +
+                                                      slice * kOCols);
 #pragma unroll
-                for (int q = 0; q < kDh / 32; ++q)
-#pragma unroll
-                    for (int i = 0; i < 4; ++i)
-                        dst[q * 4 + i] = make_uint4(
-                            bf16x2(__uint_as_float(v[q][8 * i + 0]), __uint_as_float(v[q][8 * i + 1])),
-                            bf16x2(__uint_as_float(v[q][8 * i + 2]), __uint_as_float(v[q][8 * i + 3])),
-                            bf16x2(__uint_as_float(v[q][8 * i + 4]), __uint_as_float(v[q][8 * i + 5])),
-                            bf16x2(__uint_as_float(v[q][8 * i + 6]), __uint_as_float(v[q][8 * i + 7])));
+                for (int i = 0; i < kOCols / 8; ++i)
+                    dst[i] = make_uint4(bf16x2(__uint_as_float(v[8 * i + 0]), __uint_as_float(v[8 * i + 1])),
+                                        bf16x2(__uint_as_float(v[8 * i + 2]), __uint_as_float(v[8 * i + 3])),
+                                        bf16x2(__uint_as_float(v[8 * i + 4]), __uint_as_float(v[8 * i + 5])),
+                                        bf16x2(__uint_as_float(v[8 * i + 6]), __uint_as_float(v[8 * i + 7])));
             }
         }
     }
@@ -409,8 +469,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 template <int kDh>
-cudaError_t run_attn(const LaunchCtx& ctx, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                     const AttnArgs& args, int64_t items) {
+cudaError_t run_attn(const LaunchCtx& ctx, const CUtensorMap& tqk, const CUtensorMap& tv, const AttnArgs& args,
+                     int64_t items) {
     static bool configured[kMaxDevices] = {};
     if (!configured[ctx.device]) {
         const cudaError_t e = cudaFuncSetAttribute(attn_kernel<kDh>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -430,21 +490,20 @@ cudaError_t run_attn(const LaunchCtx& ctx, const CUtensorMap& tq, const CUtensor
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     cfg.gridDim = dim3((unsigned)(items * kPairCtas), 1, 1);
-    return cudaLaunchKernelEx(&cfg, attn_kernel<kDh>, tq, tk, tv, args);
+    return cudaLaunchKernelEx(&cfg, attn_kernel<kDh>, tqk, tv, args);
 }
 
 }  // namespace
 
-cudaError_t launch_attention(const LaunchCtx& ctx, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
-                             const CUtensorMap& tmap_vt, uint16_t* o, int64_t B, int64_t S, int64_t D, int64_t H,
-                             float scale) {
+cudaError_t launch_attention(const LaunchCtx& ctx, const CUtensorMap& tmap_qk, const CUtensorMap& tmap_vt,
+                             uint16_t* o, int64_t B, int64_t S, int64_t D, int64_t H, float scale) {
     const int64_t dh = D / H;
     const int64_t nqb = (S + kRowsCta * kPairCtas - 1) / (kRowsCta * kPairCtas);
     const int64_t items = B * H * nqb;
     if (items <= 0 || items * kPairCtas > 0x7FFFFFFF) return cudaErrorInvalidValue;
     AttnArgs a{o, (int)S, (int)D, (int)H, (int)nqb, scale * 1.4426950408889634f, ctx.status};
-    if (dh == 128) return run_attn<128>(ctx, tmap_q, tmap_k, tmap_vt, a, items);
-    if (dh == 64) return run_attn<64>(ctx, tmap_q, tmap_k, tmap_vt, a, items);
+    if (dh == 128) return run_attn<128>(ctx, tmap_qk, tmap_vt, a, items);
+    if (dh == 64) return run_attn<64>(ctx, tmap_qk, tmap_vt, a, items);
     return cudaErrorInvalidValue;
 }
 

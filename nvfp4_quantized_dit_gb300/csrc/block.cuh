@@ -9,12 +9,11 @@ namespace nvfp4rl {
 
 cudaError_t launch_heads_vt(const LaunchCtx&, const uint16_t* qkv, int64_t B, int64_t S, int64_t D, int64_t H,
                             uint16_t* Vt);
-// The fused attention (attn.cu): Q and K tiles from qkv [B*S, 3D] (tmap_q: 64 x 128
-// boxes, tmap_k: 64 x 64 boxes, 128-byte swizzle), V^T [B*H*dh, S] (tmap_vt: 64 x dh/2
-// boxes), o [B*S, D] written at columns h*dh; dh = D/H is 64 or 128.
-cudaError_t launch_attention(const LaunchCtx&, const CUtensorMap& tmap_q, const CUtensorMap& tmap_k,
-                             const CUtensorMap& tmap_vt, uint16_t* o, int64_t B, int64_t S, int64_t D, int64_t H,
-                             float scale);
+// The fused attention (attn.cu): Q and K tiles from qkv [B*S, 3D] (tmap_qk: 64 x 128
+// boxes, 128-byte swizzle), V^T [B*H*dh, S] (tmap_vt: 64 x dh/2 boxes), o [B*S, D]
+// written at columns h*dh; dh = D/H is 64 or 128.
+cudaError_t launch_attention(const LaunchCtx&, const CUtensorMap& tmap_qk, const CUtensorMap& tmap_vt, uint16_t* o,
+                             int64_t B, int64_t S, int64_t D, int64_t H, float scale);
 cudaError_t launch_softmax_rows(const LaunchCtx&, const uint16_t* L, int64_t rows, int64_t cols, float scale,
                                 uint16_t* P);
 cudaError_t launch_gelu(const LaunchCtx&, const uint16_t* x, int64_t n, uint16_t* y);

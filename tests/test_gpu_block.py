@@ -72,12 +72,13 @@ def test_gelu_and_add():
     assert np.array_equal(s, orc.add_bf16(np_(xd), np_(yd)))
 
 
-@pytest.mark.parametrize("B,S,D,H", [(2, 256, 256, 2), (1, 512, 384, 3), (2, 320, 256, 4), (3, 192, 128, 1),
+@pytest.mark.parametrize("B,S,D,H", [(2, 256, 256, 2), (1, 512, 384, 3), (2, 320, 256, 4), (3, 192, 128, 1), (2, 64, 128, 2),
                                      (1, 4608, 256, 2)])
 def test_attention(B, S, D, H):
     """The fused attention kernel: head widths 128 and 64, several 256-row query blocks,
-    S % 256 != 0 (a query block with rows past S in one or both CTAs) and S % 128 == 64
-    (a last key tile of 64 keys), and 4608 keys (36 tiles, both passes over the ring)."""
+    S % 256 != 0 (a query block with rows past S in one or both CTAs, and a last key
+    tile of 64, 128 or 192 valid keys, some column slices wholly masked), and 4608 keys
+    (18 tiles, both passes around the rings)."""
     require_gpu()
     rng = np.random.default_rng(B * S + D)
     qkv = _bf16(rng.standard_normal((B * S, 3 * D)) * 0.5)
