@@ -24,25 +24,31 @@ __device__ __forceinline__ uint16_t to_bf(float v) {
 }
 
 // V transposed per head, through a 64 x 64 shared-memory tile: block (tile of S, tile of
-// dh, head z) reads 64 tokens x 64 channels and writes 64 channels x 64 tokens.
+// dh, head z) reads 64 tokens x 64 channels (16-byte loads, 8 threads per token row) and
+// writes 64 channels x 64 tokens (16-byte stores, 8 threads per channel row).  S and dh
+// are multiples of 64.
 constexpr int kTr = 64;
+constexpr int kTrPad = kTr + 8;  // row stride 144 bytes: the 8 rows a store gathers sit in distinct banks
 __global__ void __launch_bounds__(kBlkThreads)
     heads_split_vt_kernel(const uint16_t* __restrict__ qkv, int64_t S, int64_t D, int64_t H,
                           uint16_t* __restrict__ Vt) {
-    __shared__ uint16_t tile[kTr][kTr + 2];
+    __shared__ __align__(16) uint16_t tile[kTr][kTrPad];
     const int64_t dh = D / H;
     const int64_t z = blockIdx.z, b = z / H, h = z - b * H;
     const int64_t s0 = (int64_t)blockIdx.x * kTr, c0 = (int64_t)blockIdx.y * kTr;
-    for (int i = threadIdx.x; i < kTr * kTr; i += kBlkThreads) {
-        const int rs = i / kTr, rc = i % kTr;
-        const int64_t s = s0 + rs, c = c0 + rc;
-        tile[rs][rc] = (s < S && c < dh) ? qkv[(b * S + s) * 3 * D + 2 * D + h * dh + c] : (uint16_t)0;
+    for (int i = threadIdx.x; i < kTr * (kTr / 8); i += kBlkThreads) {
+        const int rs = i >> 3, piece = i & 7;
+        const uint4 v = *reinterpret_cast<const uint4*>(qkv + (b * S + s0 + rs) * 3 * D + 2 * D + h * dh + c0 + piece * 8);
+        *reinterpret_cast<uint4*>(&tile[rs][piece * 8]) = v;
     }
     __syncthreads();
-    for (int i = threadIdx.x; i < kTr * kTr; i += kBlkThreads) {
-        const int rc = i / kTr, rs = i % kTr;
-        const int64_t s = s0 + rs, c = c0 + rc;
-        if (s < S && c < dh) Vt[(z * dh + c) * S + s] = tile[rs][rc];
+    for (int i = threadIdx.x; i < kTr * (kTr / 8); i += kBlkThreads) {
+        const int rc = i >> 3, tg = i & 7;
+        uint32_t w[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+            w[q] = (uint32_t)tile[tg * 8 + 2 * q][rc] | ((uint32_t)tile[tg * 8 + 2 * q + 1][rc] << 16);
+        *reinterpret_cast<uint4*>(Vt + (z * dh + c0 + rc) * S + s0 + tg * 8) = make_uint4(w[0], w[1], w[2], w[3]);
     }
 }
 
@@ -93,17 +99,26 @@ __global__ void __launch_bounds__(kBlkThreads)
 }
 
 // g(x) = x (1 + tanh(t)) / 2 through the identity (1 + tanh(t)) / 2 = 1 / (1 + e^(-2t)),
-// the exponential taken of a non-positive argument (1 + tanh(t) cancels for t << 0).
+// evaluated without cancellation: u = e^(-2|t|) in (0, 1], r = 1 / (1 + u), and the
+// logistic value is r for t >= 0 and u r for t < 0.  ex2.approx (no flush to zero: the
+// function's tail reaches bf16's subnormal range near x = -10) and rcp.approx each err
+// by a few ulps of fp32, far below bf16's rounding step.
+__device__ __forceinline__ float ex2_full(float x) {
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_full(float x) {
+    float y;
+    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ float gelu_one(float v) {
-    const float t2 = 1.5957691216057308f * (v + 0.044715f * v * v * v);  // 2 sqrt(2 / pi) (...)
-    float sig;
-    if (t2 >= 0.0f) {
-        sig = 1.0f / (1.0f + expf(-t2));
-    } else {
-        const float e = expf(t2);
-        sig = e / (1.0f + e);
-    }
-    return v * sig;
+    // 2t log2(e) = 2 sqrt(2/pi) log2(e) (v + 0.044715 v^3)
+    const float t2 = 2.3022082f * fmaf(0.044715f * v, v * v, v);
+    const float u = ex2_full(-fabsf(t2));
+    const float r = rcp_full(1.0f + u);
+    return v * (t2 >= 0.0f ? r : u * r);
 }
 
 // 8 values per thread and step (n % 8 == 0).
