@@ -318,7 +318,8 @@ size_t nvfp4_dit_block_workspace_bytes(int64_t B, int64_t S, int64_t D, int64_t 
  *              owned by the caller, not used by anything else until the call's work on
  *              `stream` is done.
  * Errors as the calls it makes (NVFP4_ERR_SHAPE for the shape rules above, _NULL,
- * _ALIGN, _ARCH, _CUDA).  Enqueues 13 kernels; allocates nothing.
+ * _ALIGN, _ARCH, _CUDA).  Enqueues 10 kernels (the GELU and both residual adds run in
+ * the epilogues of the GEMMs that produce their inputs); allocates nothing.
  */
 nvfp4_status nvfp4_dit_block(const void* x, int64_t B, int64_t S, int64_t D, int64_t H,
                              const nvfp4_linear_weights* w, void* out, void* workspace,

@@ -305,7 +305,8 @@ static nvfp4_status gemm_nvfp4_call(const uint8_t* a_codes, const uint8_t* a_sf,
                                     const uint8_t* w_codes, const uint8_t* w_sf, const float* w_st,
                                     const void* bias, void* Y, int64_t M, int64_t N, int64_t K,
                                     void* stream, int withhold_kb, int64_t wait_limit_ns,
-                                    float* row_amax = nullptr, bool want_amax = false) {
+                                    float* row_amax = nullptr, bool want_amax = false, int epi = 0,
+                                    const uint16_t* residual = nullptr) {
     if (M < 0 || N < 0 || M > kMaxRows || N > kMaxRows || K <= 0 || K % 64 != 0 ||
         K > (1 << 24) || N % 8 != 0)
         return NVFP4_ERR_SHAPE;
@@ -320,6 +321,8 @@ static nvfp4_status gemm_nvfp4_call(const uint8_t* a_codes, const uint8_t* a_sf,
             misaligned(w_sf, 16) || misaligned(Y, 16) || misaligned(a_srow, 4) ||
             misaligned(w_st, 4) || (bias && misaligned(bias, 16)))
             return NVFP4_ERR_ALIGN;
+        if (epi == kGemmEpiResidual && (!residual || misaligned(residual, 16) || N % 32 != 0))
+            return NVFP4_ERR_SHAPE;
     }
     LaunchCtx ctx;
     nvfp4_status st = resolve(stream, &ctx);
@@ -337,6 +340,9 @@ static nvfp4_status gemm_nvfp4_call(const uint8_t* a_codes, const uint8_t* a_sf,
                    (uint64_t)K / 2, 128, 128) ||
         !encode_sf(&tsa, a_sf, M, K) || !encode_sf(&tsb, w_sf, N, K) || !encode_out(&ty, Y, M, N))
         return NVFP4_ERR_CUDA;
+    if (epi != 0)
+        return from_cuda(launch_gemm_nvfp4_epi(ctx, ta, tb, tsa, tsb, ty, a_srow, w_st,
+                                               static_cast<const __nv_bfloat16*>(bias), M, N, K, epi, residual));
     return from_cuda(launch_gemm_nvfp4(ctx, ta, tb, tsa, tsb, ty, a_srow, w_st,
                                        static_cast<const __nv_bfloat16*>(bias), M, N, K, withhold_kb,
                                        wait_limit_ns, want_amax ? row_amax : nullptr));
@@ -442,9 +448,9 @@ nvfp4_status nvfp4_dit_attention(const void* qkv, int64_t B, int64_t S, int64_t 
                          static_cast<uint16_t*>(workspace));
 }
 
-// Block scratch: R1 [3 T D] holds qkv, then o | a | d; R2 [4 T D] holds the attention's
-// V^T, then u; h1 [T D]; the activation quantization of a D-wide tensor (x, o, h1 in
-// turn) and of the 4D-wide GELU output.
+// Block scratch: R1 [3 T D] holds qkv, then o; R2 [4 T D] holds the attention's V^T,
+// then the GELU output of the up-projection; h1 [T D]; the activation quantization of a
+// D-wide tensor (x, o, h1 in turn) and of the 4D-wide GELU output.
 struct BlockLayout {
     uint16_t *r1, *r2, *h1;
     uint8_t *qa_codes, *qa_sf, *qb_codes, *qb_sf;
@@ -493,24 +499,25 @@ nvfp4_status nvfp4_dit_block(const void* x, int64_t B, int64_t S, int64_t D, int
     LaunchCtx ctx;
     nvfp4_status st = resolve(stream, &ctx);
     if (st != NVFP4_OK) return st;
-    const int64_t T = B * S, TD = T * D;
+    const int64_t T = B * S;
     const uint16_t* xb = static_cast<const uint16_t*>(x);
-    uint16_t *qkv = l.r1, *o = l.r1, *a = l.r1 + TD, *d = l.r1 + 2 * TD, *u = l.r2;
+    uint16_t *qkv = l.r1, *o = l.r1, *u = l.r2;
+    // lin(in) = nvfp4_gemm(nvfp4_act_quant(in)) + bias, with the GEMM epilogue's GELU or
+    // residual add where the block applies one to the linear's output (the same bits as
+    // the separate passes: bf16 output first, then the operation, then bf16).
     auto lin = [&](const uint16_t* in, int64_t K, uint8_t* c, uint8_t* sf, float* s, const nvfp4_linear_weights& wi,
-                   int64_t N, uint16_t* y) {
+                   int64_t N, uint16_t* y, int epi, const uint16_t* residual) {
         nvfp4_status r = nvfp4_act_quant(in, T, K, c, sf, s, stream);
         if (r != NVFP4_OK) return r;
-        return nvfp4_gemm(c, sf, s, wi.codes, wi.sf, wi.s_t, wi.bias, y, T, N, K, stream);
+        return gemm_nvfp4_call(c, sf, s, wi.codes, wi.sf, wi.s_t, wi.bias, y, T, N, K, stream, -1, 0, nullptr,
+                               false, epi, residual);
     };
-    if ((st = lin(xb, D, l.qa_codes, l.qa_sf, l.qa_s, w[0], 3 * D, qkv)) != NVFP4_OK) return st;
+    if ((st = lin(xb, D, l.qa_codes, l.qa_sf, l.qa_s, w[0], 3 * D, qkv, 0, nullptr)) != NVFP4_OK) return st;
     if ((st = attention_run(ctx, qkv, B, S, D, H, o, l.r2)) != NVFP4_OK) return st;
-    if ((st = lin(o, D, l.qa_codes, l.qa_sf, l.qa_s, w[1], D, a)) != NVFP4_OK) return st;
-    cudaError_t e = launch_add(ctx, a, xb, TD, l.h1);
-    if (e != cudaSuccess) return from_cuda(e);
-    if ((st = lin(l.h1, D, l.qa_codes, l.qa_sf, l.qa_s, w[2], 4 * D, u)) != NVFP4_OK) return st;
-    if ((e = launch_gelu(ctx, u, 4 * TD, u)) != cudaSuccess) return from_cuda(e);
-    if ((st = lin(u, 4 * D, l.qb_codes, l.qb_sf, l.qb_s, w[3], D, d)) != NVFP4_OK) return st;
-    return from_cuda(launch_add(ctx, d, l.h1, TD, static_cast<uint16_t*>(out)));
+    if ((st = lin(o, D, l.qa_codes, l.qa_sf, l.qa_s, w[1], D, l.h1, kGemmEpiResidual, xb)) != NVFP4_OK) return st;
+    if ((st = lin(l.h1, D, l.qa_codes, l.qa_sf, l.qa_s, w[2], 4 * D, u, kGemmEpiGelu, nullptr)) != NVFP4_OK)
+        return st;
+    return lin(u, 4 * D, l.qb_codes, l.qb_sf, l.qb_s, w[3], D, static_cast<uint16_t*>(out), kGemmEpiResidual, l.h1);
 }
 
 nvfp4_status bf16_softmax_rows(const void* L, int64_t rows, int64_t cols, float scale, void* P,

@@ -98,29 +98,6 @@ __global__ void __launch_bounds__(kBlkThreads)
     }
 }
 
-// g(x) = x (1 + tanh(t)) / 2 through the identity (1 + tanh(t)) / 2 = 1 / (1 + e^(-2t)),
-// evaluated without cancellation: u = e^(-2|t|) in (0, 1], r = 1 / (1 + u), and the
-// logistic value is r for t >= 0 and u r for t < 0.  ex2.approx (no flush to zero: the
-// function's tail reaches bf16's subnormal range near x = -10) and rcp.approx each err
-// by a few ulps of fp32, far below bf16's rounding step.
-__device__ __forceinline__ float ex2_full(float x) {
-    float y;
-    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float rcp_full(float x) {
-    float y;
-    asm("rcp.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-__device__ __forceinline__ float gelu_one(float v) {
-    // 2t log2(e) = 2 sqrt(2/pi) log2(e) (v + 0.044715 v^3)
-    const float t2 = 2.3022082f * fmaf(0.044715f * v, v * v, v);
-    const float u = ex2_full(-fabsf(t2));
-    const float r = rcp_full(1.0f + u);
-    return v * (t2 >= 0.0f ? r : u * r);
-}
-
 // 8 values per thread and step (n % 8 == 0).
 __global__ void __launch_bounds__(kBlkThreads)
     gelu_kernel(const uint16_t* x, int64_t n, uint16_t* y) {
@@ -131,7 +108,7 @@ __global__ void __launch_bounds__(kBlkThreads)
         uint32_t o[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q)
-            o[q] = (uint32_t)to_bf(gelu_one(bf((uint16_t)w[q]))) | ((uint32_t)to_bf(gelu_one(bf((uint16_t)(w[q] >> 16)))) << 16);
+            o[q] = (uint32_t)to_bf(gelu_f32(bf((uint16_t)w[q]))) | ((uint32_t)to_bf(gelu_f32(bf((uint16_t)(w[q] >> 16)))) << 16);
         reinterpret_cast<uint4*>(y)[i] = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }

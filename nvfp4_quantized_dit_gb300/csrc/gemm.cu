@@ -46,6 +46,7 @@
 // Every mbarrier wait is bounded (common.cuh: mbar_wait); on expiry the kernel
 // records NVFP4_ERR_TIMEOUT, drains its own copies and MMAs (again bounded),
 // frees tensor memory and returns.
+#include "block.cuh"
 #include "common.cuh"
 
 namespace nvfp4rl {
@@ -128,6 +129,7 @@ struct GemmArgs {
                              // never issues (on its first tile), or -1
     float* row_amax;         // optional: max |Y[m, :]| (of the bf16 values), atomicMax on the
                              // fp32 bits into a zeroed [M] array; nullptr: not computed
+    const uint16_t* residual;  // kGemmEpiResidual only: [M, N] bf16 added to the bf16 output
 };
 
 // Pair tiles, grouped for L2 reuse: tiles are ordered in bands of kBandMp m-pairs
@@ -160,7 +162,8 @@ struct Sched {
     }
 };
 
-template <bool kFP4>
+// kEpi: 0, or kGemmEpiGelu / kGemmEpiResidual (the DiT block's epilogues, block.cuh).
+template <bool kFP4, int kEpi = 0>
 __global__ void __launch_bounds__(Cfg<kFP4>::kThreads, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmap_a,
                 const __grid_constant__ CUtensorMap tmap_b,
@@ -463,6 +466,19 @@ __global__ void __launch_bounds__(Cfg<kFP4>::kThreads, 1)
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
                 uint32_t packed[16];
+                uint32_t rw[16];  // kGemmEpiResidual: this row's 32 residual values of the chunk
+                if constexpr (kEpi == kGemmEpiResidual) {
+                    const bool in = row < M && n0 + c * 32 < N;  // N % 32 == 0: whole chunks
+                    const uint4* rp = reinterpret_cast<const uint4*>(args.residual + (int64_t)row * N + n0 + c * 32);
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const uint4 r4 = in ? __ldg(rp + q) : make_uint4(0, 0, 0, 0);
+                        rw[4 * q] = r4.x;
+                        rw[4 * q + 1] = r4.y;
+                        rw[4 * q + 2] = r4.z;
+                        rw[4 * q + 3] = r4.w;
+                    }
+                }
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     // 8 bias values per 8 columns (shared memory, broadcast to the warp).
@@ -471,10 +487,22 @@ __global__ void __launch_bounds__(Cfg<kFP4>::kThreads, 1)
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
                         const int i = q * 4 + u;
-                        packed[i] = pack_bf16x2(
-                            fmaf(__uint_as_float(v[c][2 * i]), scale, __uint_as_float(bw[u] << 16)),
-                            fmaf(__uint_as_float(v[c][2 * i + 1]), scale,
-                                 __uint_as_float(bw[u] & 0xFFFF0000u)));
+                        float lo = fmaf(__uint_as_float(v[c][2 * i]), scale, __uint_as_float(bw[u] << 16));
+                        float hi = fmaf(__uint_as_float(v[c][2 * i + 1]), scale, __uint_as_float(bw[u] & 0xFFFF0000u));
+                        if constexpr (kEpi != 0) {
+                            // The plain output's bf16 value first, as the separate pass reads it.
+                            const uint32_t yb = pack_bf16x2(lo, hi);
+                            lo = __uint_as_float(yb << 16);
+                            hi = __uint_as_float(yb & 0xFFFF0000u);
+                            if constexpr (kEpi == kGemmEpiGelu) {
+                                lo = gelu_f32(lo);
+                                hi = gelu_f32(hi);
+                            } else {
+                                lo += __uint_as_float(rw[i] << 16);
+                                hi += __uint_as_float(rw[i] & 0xFFFF0000u);
+                            }
+                        }
+                        packed[i] = pack_bf16x2(lo, hi);
                     }
                 }
                 if (args.row_amax != nullptr) {
@@ -542,7 +570,7 @@ __global__ void wait_timeout_kernel(int* status, uint64_t limit_ns) {
     __syncthreads();
 }
 
-template <bool kFP4>
+template <bool kFP4, int kEpi = 0>
 cudaError_t run_gemm(const LaunchCtx& ctx, const CUtensorMap& ta, const CUtensorMap& tb,
                      const CUtensorMap& tsfa, const CUtensorMap& tsfb, const CUtensorMap& ty,
                      const GemmArgs& args) {
@@ -561,13 +589,13 @@ cudaError_t run_gemm(const LaunchCtx& ctx, const CUtensorMap& ta, const CUtensor
     // Co-resident pairs (one CTA per SM), capped by the work available.
     cfg.gridDim = dim3((unsigned)(ctx.num_sms / kPair * kPair), 1, 1);
     int max_clusters = 0;
-    const cudaError_t e = clusters_per_device(occupancy, ctx, gemm_kernel<kFP4>, cfg, &max_clusters);
+    const cudaError_t e = clusters_per_device(occupancy, ctx, gemm_kernel<kFP4, kEpi>, cfg, &max_clusters);
     if (e != cudaSuccess) return e;
     const int64_t num_m = (args.M + BM - 1) / BM;
     const int64_t pairs = (num_m + kPair - 1) / kPair * ((args.N + BN - 1) / BN);
     const int64_t clusters = pairs < max_clusters ? pairs : max_clusters;
     cfg.gridDim = dim3((unsigned)(clusters * kPair), 1, 1);
-    return cudaLaunchKernelEx(&cfg, gemm_kernel<kFP4>, ta, tb, tsfa, tsfb, ty, args);
+    return cudaLaunchKernelEx(&cfg, gemm_kernel<kFP4, kEpi>, ta, tb, tsfa, tsfb, ty, args);
 }
 
 }  // namespace
@@ -588,6 +616,18 @@ cudaError_t launch_gemm_bf16(const LaunchCtx& ctx, const CUtensorMap& tmap_a,
                              const __nv_bfloat16* bias, int64_t M, int64_t N, int64_t K) {
     GemmArgs a{nullptr, nullptr, bias, (int)M, (int)N, (int)K, ctx.status, kWaitLimitNs, -1, nullptr};
     return run_gemm<false>(ctx, tmap_a, tmap_b, tmap_a, tmap_b, tmap_y, a);
+}
+
+cudaError_t launch_gemm_nvfp4_epi(const LaunchCtx& ctx, const CUtensorMap& tmap_a, const CUtensorMap& tmap_b,
+                                  const CUtensorMap& tmap_sfa, const CUtensorMap& tmap_sfb,
+                                  const CUtensorMap& tmap_y, const float* a_srow, const float* w_st,
+                                  const __nv_bfloat16* bias, int64_t M, int64_t N, int64_t K, int epi,
+                                  const uint16_t* residual) {
+    GemmArgs a{a_srow, w_st, bias, (int)M, (int)N, (int)K, ctx.status, kWaitLimitNs, -1, nullptr, residual};
+    if (epi == kGemmEpiGelu) return run_gemm<true, kGemmEpiGelu>(ctx, tmap_a, tmap_b, tmap_sfa, tmap_sfb, tmap_y, a);
+    if (epi == kGemmEpiResidual && residual != nullptr && N % 32 == 0)
+        return run_gemm<true, kGemmEpiResidual>(ctx, tmap_a, tmap_b, tmap_sfa, tmap_sfb, tmap_y, a);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_test_wait_timeout(const LaunchCtx& ctx, int64_t timeout_ns) {

@@ -182,6 +182,27 @@ def test_block_flux_shape_sampled_rows():
     assert np.linalg.norm(vg - vr) <= 2.0 ** -4 * np.linalg.norm(vr), info
 
 
+@pytest.mark.parametrize("B,S,D,H", [(2, 128, 256, 2), (1, 320, 512, 4)])
+def test_block_equals_its_public_steps(B, S, D, H):
+    """The block fuses the GELU and both residual adds into the GEMM epilogues; the result
+    must equal, bit for bit, the same block composed from the library's public calls
+    (act_quant, nvfp4_gemm, the attention, bf16_gelu, bf16_add)."""
+    require_gpu()
+    rng = np.random.default_rng(3 * B + S)
+    x = _bf16(rng.standard_normal((B * S, D)))
+    w_bits, b_bits = _weights(rng, D)
+    w = _gpu_weights(w_bits, b_bits)
+
+    def lin(a, wi):
+        return nv.nvfp4_gemm(nv.nvfp4_act_quant(a), wi[:3], bias=wi[3])
+    qkv = lin(x, w[0])
+    h1 = nv.bf16_add(lin(nv.nvfp4_dit_attention(qkv, B, S, H), w[1]), x)
+    ref = nv.bf16_add(lin(nv.bf16_gelu(lin(h1, w[2])), w[3]), h1)
+    out = nv.nvfp4_dit_block(x, B, S, H, w)
+    assert torch.equal(out.view(torch.int16), ref.view(torch.int16))
+    assert nv.nvfp4_device_status() == 0
+
+
 def test_block_residual_wiring_is_exact():
     """Zero output projections: the GPU block returns its input bit for bit."""
     require_gpu()
