@@ -107,8 +107,10 @@ __global__ void __launch_bounds__(kBlkThreads)
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
         uint32_t o[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-            o[q] = (uint32_t)to_bf(gelu_f32(bf((uint16_t)w[q]))) | ((uint32_t)to_bf(gelu_f32(bf((uint16_t)(w[q] >> 16)))) << 16);
+        for (int q = 0; q < 4; ++q) {
+            const float2 g = gelu_f32x2(make_float2(bf((uint16_t)w[q]), bf((uint16_t)(w[q] >> 16))));
+            o[q] = (uint32_t)to_bf(g.x) | ((uint32_t)to_bf(g.y) << 16);
+        }
         reinterpret_cast<uint4*>(y)[i] = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }

@@ -495,8 +495,9 @@ __global__ void __launch_bounds__(Cfg<kFP4>::kThreads, 1)
                             lo = __uint_as_float(yb << 16);
                             hi = __uint_as_float(yb & 0xFFFF0000u);
                             if constexpr (kEpi == kGemmEpiGelu) {
-                                lo = gelu_f32(lo);
-                                hi = gelu_f32(hi);
+                                const float2 g = gelu_f32x2(make_float2(lo, hi));
+                                lo = g.x;
+                                hi = g.y;
                             } else {
                                 lo += __uint_as_float(rw[i] << 16);
                                 hi += __uint_as_float(rw[i] & 0xFFFF0000u);
