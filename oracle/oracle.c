@@ -32,7 +32,8 @@
  *   sf  = RNE_E4M3_sat(block_amax / (6 s))   one per 16 consecutive K-elements
  *   q   = RNE_E2M1_sat(x / (sf s))           sign kept, saturating at 6
  *
- * Readings where the pages are silent (numbered as in the project's list of readings):
+ * Readings where the pages are silent (the numbers skip readings that concern only
+ * the CUDA library or the synthetic inputs):
  *   R1  Scale arithmetic is IEEE fp32: d = 6*s, v = bamax / d (a division, not a
  *       reciprocal multiply), den = sff * s formed first, then q = x / den.
  *   R2  Merge: c = alpha / r (fp32); acc = fmaf chain over j = 0..r-1 of
