@@ -10,8 +10,10 @@
 // (rescaled when m grows), pass 2 forms the tiles of L again (the same MMAs, so the
 // same bits), turns them into P with the final m and 1/sum, and accumulates P v.
 //
-// One cluster of two CTAs per (image-head, 256 query rows); every MMA is a 2-CTA
-// `cta_group::2` MMA (M = 256: each CTA's 128 query rows):
+// Persistent clusters of two CTAs (one per SM), each walking items (image-head, 256
+// query rows); every MMA is a 2-CTA `cta_group::2` MMA (M = 256: each CTA's 128 query
+// rows).  The next item's Q loads once the current item's last L tile is formed, and
+// its first P v waits until the current item's O has been read out of tensor memory:
 //   L tile   M = 256, N = 256 keys (128 per CTA), K = dh;  A = Q (shared memory),
 //            B = K rows (shared memory)
 //   O       M = 256, N = dh (dh/2 per CTA), K = 256 keys; A = P (tensor memory),
@@ -63,7 +65,8 @@ struct AttnCfg {
     static constexpr uint32_t kKBytes = kKSub * (kDh / 64);
     static constexpr uint32_t kVSub = (kDh / kPairCtas) * 128;         // dh/2 rows x 64 keys
     static constexpr uint32_t kVBytes = kVSub * (kTileKeys / 64);
-    static constexpr uint32_t kBarBytes = 512 + kSlices * 2 * kRowsCta * 4;  // barriers; (m, sum) per slice and row
+    // barriers; (m, sum) per item parity, slice and row
+    static constexpr uint32_t kBarBytes = 512 + 2 * kSlices * 2 * kRowsCta * 4;
     static constexpr uint32_t kSmemBytes =
         1024 + kQBytes + kStagesK * kKBytes + kStagesV * kVBytes + kBarBytes;
     // kind::f16, bf16 A and B, fp32 accumulator, both K-major, M = 256.
@@ -73,11 +76,12 @@ struct AttnCfg {
 };
 static_assert(AttnCfg<128>::kSmemBytes <= 232448, "shared memory budget");
 static_assert(kColO + 128 <= kTmemColsAttn, "tensor memory budget");
-static_assert(30 * 8 + 8 <= 512, "barrier area");
+static_assert(32 * 8 + 8 <= 512, "barrier area");
 
 struct AttnArgs {
     uint16_t* o;
     int S, D, H, nqb;   // nqb: 256-row query blocks per head
+    int items;          // B * H * nqb
     float c;            // scale * log2(e)
     int* status;
 };
@@ -148,8 +152,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint8_t* sk = sq + C::kQBytes;
     uint8_t* sv = sk + kStagesK * C::kKBytes;
     uint64_t* bars = reinterpret_cast<uint64_t*>(sv + kStagesV * C::kVBytes);
-    uint64_t* q_full = bars;
-    uint64_t* k_full = q_full + 1;
+    uint64_t* q_full = bars;                 // Q of the pair's current item has landed (even CTA)
+    uint64_t* q_empty = q_full + 1;          // ... and its last L tile's MMAs have read it
+    uint64_t* k_full = q_empty + 1;
     uint64_t* k_empty = k_full + kStagesK;
     uint64_t* v_full = k_empty + kStagesK;
     uint64_t* v_empty = v_full + kStagesV;
@@ -157,24 +162,26 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint64_t* s_empty = s_full + 1;          // ... and has been read (even CTA)
     uint64_t* p_full = s_empty + 1;          // P is in tensor memory (even CTA)
     uint64_t* p_free = p_full + 1;           // ... and has been read by the P v MMAs
-    uint64_t* o_full = p_free + 1;
-    uint64_t* drain = o_full + 1;
+    uint64_t* o_full = p_free + 1;           // the item's O is complete in tensor memory
+    uint64_t* o_free = o_full + 1;           // ... and has been read out (even CTA)
+    uint64_t* drain = o_free + 1;
     uint64_t* stats_ready = drain + 1;       // every softmax thread has written its (m, sum)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(stats_ready + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    float* row_stats = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 512);  // [slice][m|sum][row]
+    // [item parity][slice][m|sum][row]
+    float* row_stats = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(bars) + 512);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t rank = cluster_ctarank();
     const bool leader = rank == 0;
     const int S = args.S, D = args.D, H = args.H;
-    const int item = (int)(blockIdx.x / kPairCtas);
-    const int z = item / args.nqb, qb = item - z * args.nqb;
-    const int b = z / H, h = z - b * H;
     const int n_tiles = (S + kTileKeys - 1) / kTileKeys;
+    // Items (image-head, 256 query rows) of this pair: first, first + step, ...
+    const int first = (int)(blockIdx.x / kPairCtas), step = (int)(gridDim.x / kPairCtas);
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
+        mbar_init(q_empty, 1);
         for (int s = 0; s < kStagesK; ++s) {
             mbar_init(&k_full[s], 1);
             mbar_init(&k_empty[s], 1);
@@ -188,6 +195,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_init(p_full, kSoftWarps * kPairCtas);
         mbar_init(p_free, 1);
         mbar_init(o_full, 1);
+        mbar_init(o_free, kSoftWarps * kPairCtas);
         mbar_init(drain, 1);
         mbar_init(stats_ready, kSoftWarps * 32);
         *abort_flag = 0;
@@ -213,46 +221,53 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const uint32_t q_full_e = map_to_rank(smem_u32(q_full), 0);
             const uint32_t k_full_e = map_to_rank(smem_u32(k_full), 0);
             const uint32_t v_full_e = map_to_rank(smem_u32(v_full), 0);
-            const int row0 = b * S;
-            const int qcol = h * kDh, kcol = D + h * kDh;
             bool ok = true;
-            if (leader) mbar_arrive_expect_tx(q_full, kPairCtas * C::kQBytes);
+            int kc = 0, vc = 0, it = 0;
+            for (int item = first; ok && item < args.items; item += step, ++it) {
+                const int z = item / args.nqb, qb = item - z * args.nqb;
+                const int b = z / H, h = z - b * H;
+                const int row0 = b * S;
+                const int qcol = h * kDh, kcol = D + h * kDh;
+                // Q: once the previous item's last L tile has been formed.
+                if (!mbar_wait(q_empty, (uint32_t)((it & 1) ^ 1), args.status, abort_flag, kAttnWaitNs)) break;
+                if (leader) mbar_arrive_expect_tx(q_full, kPairCtas * C::kQBytes);
 #pragma unroll
-            for (int i = 0; i < kDh / 64; ++i)
-                tma_load_2d_pair(&tmap_qk, q_full_e, sq + i * C::kQSub, qcol + 64 * i,
-                                 row0 + qb * (kRowsCta * kPairCtas) + (int)rank * kRowsCta);
-            int kc = 0, vc = 0;
-            for (int pass = 0; ok && pass < 2; ++pass) {
-                for (int j = 0; j < n_tiles; ++j) {
-                    {
-                        const int s = kc % kStagesK;
-                        if (!mbar_wait(&k_empty[s], (uint32_t)(((kc / kStagesK) & 1) ^ 1), args.status, abort_flag,
-                                       kAttnWaitNs)) {
-                            ok = false;
-                            break;
+                for (int i = 0; i < kDh / 64; ++i)
+                    tma_load_2d_pair(&tmap_qk, q_full_e, sq + i * C::kQSub, qcol + 64 * i,
+                                     row0 + qb * (kRowsCta * kPairCtas) + (int)rank * kRowsCta);
+                for (int pass = 0; ok && pass < 2; ++pass) {
+                    for (int j = 0; j < n_tiles; ++j) {
+                        {
+                            const int s = kc % kStagesK;
+                            if (!mbar_wait(&k_empty[s], (uint32_t)(((kc / kStagesK) & 1) ^ 1), args.status,
+                                           abort_flag, kAttnWaitNs)) {
+                                ok = false;
+                                break;
+                            }
+                            if (leader) mbar_arrive_expect_tx(&k_full[s], kPairCtas * C::kKBytes);
+                            uint8_t* dst = sk + s * C::kKBytes;
+#pragma unroll
+                            for (int i = 0; i < kDh / 64; ++i)
+                                tma_load_2d_pair(&tmap_qk, k_full_e + 8u * (uint32_t)s, dst + i * C::kKSub,
+                                                 kcol + 64 * i,
+                                                 row0 + j * kTileKeys + (int)rank * (kTileKeys / kPairCtas));
+                            ++kc;
                         }
-                        if (leader) mbar_arrive_expect_tx(&k_full[s], kPairCtas * C::kKBytes);
-                        uint8_t* dst = sk + s * C::kKBytes;
+                        if (pass == 1) {
+                            const int s = vc % kStagesV;
+                            if (!mbar_wait(&v_empty[s], (uint32_t)(((vc / kStagesV) & 1) ^ 1), args.status,
+                                           abort_flag, kAttnWaitNs)) {
+                                ok = false;
+                                break;
+                            }
+                            if (leader) mbar_arrive_expect_tx(&v_full[s], kPairCtas * C::kVBytes);
+                            uint8_t* dst = sv + s * C::kVBytes;
 #pragma unroll
-                        for (int i = 0; i < kDh / 64; ++i)
-                            tma_load_2d_pair(&tmap_qk, k_full_e + 8u * (uint32_t)s, dst + i * C::kKSub, kcol + 64 * i,
-                                             row0 + j * kTileKeys + (int)rank * (kTileKeys / kPairCtas));
-                        ++kc;
-                    }
-                    if (pass == 1) {
-                        const int s = vc % kStagesV;
-                        if (!mbar_wait(&v_empty[s], (uint32_t)(((vc / kStagesV) & 1) ^ 1), args.status, abort_flag,
-                                       kAttnWaitNs)) {
-                            ok = false;
-                            break;
+                            for (int i = 0; i < kTileKeys / 64; ++i)
+                                tma_load_2d_pair(&tmap_v, v_full_e + 8u * (uint32_t)s, dst + i * C::kVSub,
+                                                 j * kTileKeys + 64 * i, z * kDh + (int)rank * (kDh / kPairCtas));
+                            ++vc;
                         }
-                        if (leader) mbar_arrive_expect_tx(&v_full[s], kPairCtas * C::kVBytes);
-                        uint8_t* dst = sv + s * C::kVBytes;
-#pragma unroll
-                        for (int i = 0; i < kTileKeys / 64; ++i)
-                            tma_load_2d_pair(&tmap_v, v_full_e + 8u * (uint32_t)s, dst + i * C::kVSub,
-                                             j * kTileKeys + 64 * i, z * kDh + (int)rank * (kDh / kPairCtas));
-                        ++vc;
                     }
                 }
             }
@@ -279,9 +294,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             const uint64_t q_desc = smem_desc(smem_u32(sq), 16, 1024, kLayoutSw128);
             const uint64_t k_desc0 = smem_desc(smem_u32(sk), 16, 1024, kLayoutSw128);
             const uint64_t v_desc0 = smem_desc(smem_u32(sv), 16, 1024, kLayoutSw128);
-            bool ok = mbar_wait(q_full, 0, args.status, abort_flag, kAttnWaitNs);
-            bool any = false;
-            int kc = 0, g = 0;
+            bool ok = true, any = false;
+            // Running counts over the pair's items: K stages, L tiles, P tiles, V stages.
+            int kc = 0, g = 0, pj = 0, vc = 0, it = 0;
             // One L tile: wait for its K stage and for the previous tile to have been read,
             // dh/16 MMAs, release the stage, announce the tile.
             auto issue_l = [&]() -> bool {
@@ -303,28 +318,40 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 ++g;
                 return true;
             };
-            // L tiles g = 0 .. 2n-1 in order (pass 1, then pass 2); in pass 2 tile j + 1
-            // is queued before the P v of tile j, so it is ready when the softmax is.
-            for (int j = 0; ok && j < n_tiles + 1; ++j) ok = issue_l();
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                if (j + 1 < n_tiles && !(ok = issue_l())) break;
-                const int s = j % kStagesV;
-                if (!mbar_wait(&v_full[s], (uint32_t)((j / kStagesV) & 1), args.status, abort_flag, kAttnWaitNs) ||
-                    !mbar_wait<true>(p_full, (uint32_t)(j & 1), args.status, abort_flag, kAttnWaitNs)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after_sync();
-                const uint64_t vd = v_desc0 + (uint64_t)((s * C::kVBytes) >> 4);
+            for (int item = first; ok && item < args.items; item += step, ++it) {
+                if (!(ok = mbar_wait(q_full, (uint32_t)(it & 1), args.status, abort_flag, kAttnWaitNs))) break;
+                // L tiles of both passes in order; in pass 2 tile j + 1 is queued before the
+                // P v of tile j, so it is ready when the softmax is.  After the item's last L
+                // tile Q is released to the producer (the next item's Q loads meanwhile).
+                for (int j = 0; ok && j < n_tiles + 1; ++j) ok = issue_l();
+                if (ok && n_tiles == 1) mma_commit_pair_multicast(q_empty, kBoth);
+                for (int j = 0; ok && j < n_tiles; ++j, ++pj, ++vc) {
+                    if (j + 1 < n_tiles) {
+                        if (!(ok = issue_l())) break;
+                        if (j + 2 == n_tiles) mma_commit_pair_multicast(q_empty, kBoth);
+                    }
+                    const int s = vc % kStagesV;
+                    if (!mbar_wait(&v_full[s], (uint32_t)((vc / kStagesV) & 1), args.status, abort_flag, kAttnWaitNs) ||
+                        !mbar_wait<true>(p_full, (uint32_t)(pj & 1), args.status, abort_flag, kAttnWaitNs) ||
+                        // The first P v of an item overwrites O: the previous item's O must
+                        // have been read out.
+                        (j == 0 && !mbar_wait<true>(o_free, (uint32_t)((it & 1) ^ 1), args.status, abort_flag,
+                                                    kAttnWaitNs))) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint64_t vd = v_desc0 + (uint64_t)((s * C::kVBytes) >> 4);
 #pragma unroll
-                for (int kk = 0; kk < kTileKeys / 16; ++kk)
-                    mma_bf16_pair_ta(tmem_base + kColO, tmem_base + kColP + 8u * (uint32_t)kk,
-                                     vd + (uint64_t)((kk >> 2) * (C::kVSub >> 4) + (kk & 3) * 2), idesc_o,
-                                     (j > 0 || kk > 0) ? 1u : 0u);
-                mma_commit_pair_multicast(&v_empty[s], kBoth);
-                mma_commit_pair_multicast(p_free, kBoth);
+                    for (int kk = 0; kk < kTileKeys / 16; ++kk)
+                        mma_bf16_pair_ta(tmem_base + kColO, tmem_base + kColP + 8u * (uint32_t)kk,
+                                         vd + (uint64_t)((kk >> 2) * (C::kVSub >> 4) + (kk & 3) * 2), idesc_o,
+                                         (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_commit_pair_multicast(&v_empty[s], kBoth);
+                    mma_commit_pair_multicast(p_free, kBoth);
+                }
+                if (ok) mma_commit_pair_multicast(o_full, kBoth);
             }
-            if (ok) mma_commit_pair_multicast(o_full, kBoth);
             if (*abort_flag && any) {
                 mma_commit_pair_multicast(drain, kEven);
                 int dummy = 0;
@@ -340,99 +367,109 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
         const uint32_t s_empty_e = map_to_rank(smem_u32(s_empty), 0);
         const uint32_t p_full_e = map_to_rank(smem_u32(p_full), 0);
+        const uint32_t o_free_e = map_to_rank(smem_u32(o_free), 0);
         const float c = args.c;
         const float2 c2 = make_float2(c, c);
         const int col0 = slice * kSliceCols;
-        float m = -INFINITY, sum = 0.0f, mc2 = 0.0f;
         bool ok = true;
-        for (int g = 0; ok && g < 2 * n_tiles; ++g) {
-            const int j = g < n_tiles ? g : g - n_tiles;
-            const int valid = min(kTileKeys, S - j * kTileKeys);
-            ok = mbar_wait(s_full, (uint32_t)(g & 1), args.status, abort_flag, kAttnWaitNs);
-            ok = __all_sync(0xFFFFFFFFu, ok);  // tcgen05.ld is .sync.aligned
-            if (!ok) break;
-            tc_fence_after_sync();
-            uint32_t lbits[kSliceCols / 2];
-#pragma unroll
-            for (int ch = 0; ch < kSliceCols / kChunk; ++ch) {
-                uint32_t v[kChunk];
-                tmem_ld_32x32b_x32(lane_base + kColL + (uint32_t)(col0 + ch * kChunk), v);
-                tmem_ld_wait();
-                round_chunk(v, col0 + ch * kChunk, valid, lbits + ch * (kChunk / 2));
-            }
-            tc_fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(s_empty_e);
-            if (g < n_tiles) {
-                // Pass 1: running maximum and rescaled sum of exponentials (packed pairs,
-                // four partial sums, so that the additions do not form one chain).
-                uint32_t mx2 = lbits[0];
-#pragma unroll
-                for (int i = 1; i < kSliceCols / 2; ++i) mx2 = bmax2(mx2, lbits[i]);
-                const float tmax = fmaxf(__uint_as_float(mx2 << 16), __uint_as_float(mx2 & 0xFFFF0000u));
-                const float m_new = fmaxf(m, tmax);
-                // A slice whose columns so far were all masked (m_new = -inf) keeps sum = 0:
-                // with the offset 0 every term is 2^-inf = 0 (no inf - inf).
-                const float mc = m_new == -INFINITY ? 0.0f : m_new * c;
-                const float2 nmc = make_float2(-mc, -mc);
-                float2 acc[4] = {make_float2(sum * ex2(fmaf(m, c, -mc)), 0.0f), make_float2(0.0f, 0.0f),
-                                 make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-#pragma unroll
-                for (int i = 0; i < kSliceCols / 2; ++i) {
-                    const float2 a = __ffma2_rn(unpack_bf16x2(lbits[i]), c2, nmc);
-                    acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(ex2(a.x), ex2(a.y)));
-                }
-                const float2 s01 = __fadd2_rn(acc[0], acc[1]), s23 = __fadd2_rn(acc[2], acc[3]);
-                const float2 s4 = __fadd2_rn(s01, s23);
-                sum = s4.x + s4.y;
-                m = m_new;
-                if (g == n_tiles - 1) {
-                    // The row's slices: combine their (m, sum) through shared memory.
-                    row_stats[(slice * 2 + 0) * kRowsCta + row] = m;
-                    row_stats[(slice * 2 + 1) * kRowsCta + row] = sum;
-                    mbar_arrive(stats_ready);
-                    ok = mbar_wait(stats_ready, 0, args.status, abort_flag, kAttnWaitNs);
-                    ok = __all_sync(0xFFFFFFFFu, ok);
-                    if (!ok) break;
-                    float ms[kSlices], ss[kSlices], mm = -INFINITY;
-#pragma unroll
-                    for (int k = 0; k < kSlices; ++k) {
-                        ms[k] = row_stats[(k * 2 + 0) * kRowsCta + row];
-                        ss[k] = row_stats[(k * 2 + 1) * kRowsCta + row];
-                        mm = fmaxf(mm, ms[k]);
-                    }
-                    float total = 0.0f;
-#pragma unroll
-                    for (int k = 0; k < kSlices; ++k) total += ss[k] * ex2(fmaf(ms[k], c, -mm * c));
-                    // P = exp(scale (l - m)) / sum = 2^(l c - (m c + log2(sum))).
-                    mc2 = fmaf(mm, c, lg2(total));
-                }
-            } else {
-                // Pass 2: P = bf16(exp(scale (l - m)) / sum) into tensor memory.
-                const float2 nmc = make_float2(-mc2, -mc2);
-                uint32_t p[kSliceCols / 2];
-#pragma unroll
-                for (int i = 0; i < kSliceCols / 2; ++i) {
-                    const float2 a = __ffma2_rn(unpack_bf16x2(lbits[i]), c2, nmc);
-                    p[i] = bf16x2(ex2(a.x), ex2(a.y));
-                }
-                ok = mbar_wait(p_free, (uint32_t)((j & 1) ^ 1), args.status, abort_flag, kAttnWaitNs);
-                ok = __all_sync(0xFFFFFFFFu, ok);  // tcgen05.st is .sync.aligned
+        int gg = 0, pj = 0, it = 0;  // running counts: L tiles, P tiles, items
+        for (int item = first; ok && item < args.items; item += step, ++it) {
+            const int z = item / args.nqb, qb = item - z * args.nqb;
+            const int b = z / H, h = z - b * H;
+            float* stats = row_stats + (it & 1) * (kSlices * 2 * kRowsCta);
+            float m = -INFINITY, sum = 0.0f, mc2 = 0.0f;
+            for (int g = 0; ok && g < 2 * n_tiles; ++g, ++gg) {
+                const int j = g < n_tiles ? g : g - n_tiles;
+                const int valid = min(kTileKeys, S - j * kTileKeys);
+                ok = mbar_wait(s_full, (uint32_t)(gg & 1), args.status, abort_flag, kAttnWaitNs);
+                ok = __all_sync(0xFFFFFFFFu, ok);  // tcgen05.ld is .sync.aligned
                 if (!ok) break;
                 tc_fence_after_sync();
-                tmem_st_32x32b_x32(lane_base + kColP + (uint32_t)(slice * (kSliceCols / 2)), p);
-                tmem_st_wait();
+                uint32_t lbits[kSliceCols / 2];
+#pragma unroll
+                for (int ch = 0; ch < kSliceCols / kChunk; ++ch) {
+                    uint32_t v[kChunk];
+                    tmem_ld_32x32b_x32(lane_base + kColL + (uint32_t)(col0 + ch * kChunk), v);
+                    tmem_ld_wait();
+                    round_chunk(v, col0 + ch * kChunk, valid, lbits + ch * (kChunk / 2));
+                }
                 tc_fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(p_full_e);
+                if (lane == 0) mbar_arrive_cluster(s_empty_e);
+                if (g < n_tiles) {
+                    // Pass 1: running maximum and rescaled sum of exponentials (packed pairs,
+                    // four partial sums, so that the additions do not form one chain).
+                    uint32_t mx2 = lbits[0];
+#pragma unroll
+                    for (int i = 1; i < kSliceCols / 2; ++i) mx2 = bmax2(mx2, lbits[i]);
+                    const float tmax = fmaxf(__uint_as_float(mx2 << 16), __uint_as_float(mx2 & 0xFFFF0000u));
+                    const float m_new = fmaxf(m, tmax);
+                    // A slice whose columns so far were all masked (m_new = -inf) keeps sum = 0:
+                    // with the offset 0 every term is 2^-inf = 0 (no inf - inf).
+                    const float mc = m_new == -INFINITY ? 0.0f : m_new * c;
+                    const float2 nmc = make_float2(-mc, -mc);
+                    float2 acc[4] = {make_float2(sum * ex2(fmaf(m, c, -mc)), 0.0f), make_float2(0.0f, 0.0f),
+                                     make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+#pragma unroll
+                    for (int i = 0; i < kSliceCols / 2; ++i) {
+                        const float2 a = __ffma2_rn(unpack_bf16x2(lbits[i]), c2, nmc);
+                        acc[i & 3] = __fadd2_rn(acc[i & 3], make_float2(ex2(a.x), ex2(a.y)));
+                    }
+                    const float2 s01 = __fadd2_rn(acc[0], acc[1]), s23 = __fadd2_rn(acc[2], acc[3]);
+                    const float2 s4 = __fadd2_rn(s01, s23);
+                    sum = s4.x + s4.y;
+                    m = m_new;
+                    if (g == n_tiles - 1) {
+                        // The row's slices: combine their (m, sum) through shared memory (one
+                        // buffer per item parity, so a warp ahead on the next item cannot
+                        // overwrite values another warp still reads).
+                        stats[(slice * 2 + 0) * kRowsCta + row] = m;
+                        stats[(slice * 2 + 1) * kRowsCta + row] = sum;
+                        mbar_arrive(stats_ready);
+                        ok = mbar_wait(stats_ready, (uint32_t)(it & 1), args.status, abort_flag, kAttnWaitNs);
+                        ok = __all_sync(0xFFFFFFFFu, ok);
+                        if (!ok) break;
+                        float ms[kSlices], ss[kSlices], mm = -INFINITY;
+#pragma unroll
+                        for (int k = 0; k < kSlices; ++k) {
+                            ms[k] = stats[(k * 2 + 0) * kRowsCta + row];
+                            ss[k] = stats[(k * 2 + 1) * kRowsCta + row];
+                            mm = fmaxf(mm, ms[k]);
+                        }
+                        float total = 0.0f;
+#pragma unroll
+                        for (int k = 0; k < kSlices; ++k) total += ss[k] * ex2(fmaf(ms[k], c, -mm * c));
+                        // P = exp(scale (l - m)) / sum = 2^(l c - (m c + log2(sum))).
+                        mc2 = fmaf(mm, c, lg2(total));
+                    }
+                } else {
+                    // Pass 2: P = bf16(exp(scale (l - m)) / sum) into tensor memory.
+                    const float2 nmc = make_float2(-mc2, -mc2);
+                    uint32_t p[kSliceCols / 2];
+#pragma unroll
+                    for (int i = 0; i < kSliceCols / 2; ++i) {
+                        const float2 a = __ffma2_rn(unpack_bf16x2(lbits[i]), c2, nmc);
+                        p[i] = bf16x2(ex2(a.x), ex2(a.y));
+                    }
+                    ok = mbar_wait(p_free, (uint32_t)((pj & 1) ^ 1), args.status, abort_flag, kAttnWaitNs);
+                    ok = __all_sync(0xFFFFFFFFu, ok);  // tcgen05.st is .sync.aligned
+                    if (!ok) break;
+                    tc_fence_after_sync();
+                    tmem_st_32x32b_x32(lane_base + kColP + (uint32_t)(slice * (kSliceCols / 2)), p);
+                    tmem_st_wait();
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(p_full_e);
+                    ++pj;
+                }
             }
-        }
-        if (ok) {
-            ok = mbar_wait(o_full, 0, args.status, abort_flag, kAttnWaitNs);
-            ok = __all_sync(0xFFFFFFFFu, ok);
-        }
-        if (ok) {
-            // O: this warp's dh / 4 columns of its 32 rows.
+            if (ok) {
+                ok = mbar_wait(o_full, (uint32_t)(it & 1), args.status, abort_flag, kAttnWaitNs);
+                ok = __all_sync(0xFFFFFFFFu, ok);
+            }
+            if (!ok) break;
+            // O: this warp's dh / 4 columns of its 32 rows; then O's columns are free for
+            // the next item's P v.
             constexpr int kOCols = kDh / kSlices;
             tc_fence_after_sync();
             uint32_t v[kOCols];
@@ -443,6 +480,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 tmem_ld_32x32b_x16(oaddr, v);
             }
             tmem_ld_wait();
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(o_free_e);
             const int s = qb * (kRowsCta * kPairCtas) + (int)rank * kRowsCta + row;
             if (s < S) {
                 uint4* dst = reinterpret_cast<uint4*>(args.o + ((int64_t)b * S + s) * D + (int64_t)h * kDh +
@@ -469,15 +509,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 }
 
 template <int kDh>
-cudaError_t run_attn(const LaunchCtx& ctx, const CUtensorMap& tqk, const CUtensorMap& tv, const AttnArgs& args,
-                     int64_t items) {
-    static bool configured[kMaxDevices] = {};
-    if (!configured[ctx.device]) {
-        const cudaError_t e = cudaFuncSetAttribute(attn_kernel<kDh>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   (int)AttnCfg<kDh>::kSmemBytes);
-        if (e != cudaSuccess) return e;
-        configured[ctx.device] = true;
-    }
+cudaError_t run_attn(const LaunchCtx& ctx, const CUtensorMap& tqk, const CUtensorMap& tv, const AttnArgs& args) {
+    static OccupancyCache occupancy;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -489,7 +522,13 @@ cudaError_t run_attn(const LaunchCtx& ctx, const CUtensorMap& tqk, const CUtenso
     cfg.stream = ctx.stream;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cfg.gridDim = dim3((unsigned)(items * kPairCtas), 1, 1);
+    // Persistent: the co-resident pairs (one CTA per SM), each walking its items.
+    cfg.gridDim = dim3((unsigned)(ctx.num_sms / kPairCtas * kPairCtas), 1, 1);
+    int max_clusters = 0;
+    const cudaError_t e = clusters_per_device(occupancy, ctx, attn_kernel<kDh>, cfg, &max_clusters);
+    if (e != cudaSuccess) return e;
+    const int pairs = args.items < max_clusters ? args.items : max_clusters;
+    cfg.gridDim = dim3((unsigned)(pairs * kPairCtas), 1, 1);
     return cudaLaunchKernelEx(&cfg, attn_kernel<kDh>, tqk, tv, args);
 }
 
@@ -500,10 +539,10 @@ cudaError_t launch_attention(const LaunchCtx& ctx, const CUtensorMap& tmap_qk, c
     const int64_t dh = D / H;
     const int64_t nqb = (S + kRowsCta * kPairCtas - 1) / (kRowsCta * kPairCtas);
     const int64_t items = B * H * nqb;
-    if (items <= 0 || items * kPairCtas > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    AttnArgs a{o, (int)S, (int)D, (int)H, (int)nqb, scale * 1.4426950408889634f, ctx.status};
-    if (dh == 128) return run_attn<128>(ctx, tmap_qk, tmap_vt, a, items);
-    if (dh == 64) return run_attn<64>(ctx, tmap_qk, tmap_vt, a, items);
+    if (items <= 0 || items > 0x7FFFFFFF) return cudaErrorInvalidValue;
+    AttnArgs a{o, (int)S, (int)D, (int)H, (int)nqb, (int)items, scale * 1.4426950408889634f, ctx.status};
+    if (dh == 128) return run_attn<128>(ctx, tmap_qk, tmap_vt, a);
+    if (dh == 64) return run_attn<64>(ctx, tmap_qk, tmap_vt, a);
     return cudaErrorInvalidValue;
 }
 
