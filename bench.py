@@ -811,6 +811,17 @@ def workload_name(cfg, rcfg):
             f"{rcfg.P}x{rcfg.N} reward selection (K={rcfg.K})")
 
 
+def bench_config(cfg, rcfg, world):
+    """The `config` object of the JSON line, the same for both arms."""
+    x_mb = cfg.M * cfg.K * 2 / 1e6
+    y_mb = cfg.M * cfg.N * 2 / 1e6
+    return {"workload": workload_name(cfg, rcfg),
+            "M": cfg.M, "K": cfg.K, "N": cfg.N, "lora_rank": 32, "prompts": rcfg.P, "seeds": rcfg.N,
+            "selected": rcfg.K, "parallelism": f"replicas x{world}",
+            "l2": f"inputs larger than L2 within a step (X {x_mb:.0f} MB read, Y {y_mb:.0f} MB "
+                  "written twice per step)"}
+
+
 def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk, world, rank,
            launches_per_step, per_tensor_ms, extras, variant_ms):
     if rank != 0:
@@ -832,8 +843,6 @@ def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk
 
     # The captured traffic is of the full workload: a --rows run has none.
     workload = args.config if not args.rows else f"{args.config}@{args.rows}"
-    x_mb = M * K * 2 / 1e6
-    y_mb = M * N * 2 / 1e6
 
     def roof(bound, achieved, peak, unit, kernel):
         return {"bound": bound, "achieved": round(achieved, 2), "peak": round(peak, 1), "unit": unit,
@@ -853,11 +862,7 @@ def report(args, cfg, rcfg, host, per, elapsed_ms, e2e_ms, h2d, d2h, status, clk
         "vs_baseline": None,
         "dtype": "nvfp4 (e2m1 x e4m3 block scale) -> fp32 accumulate -> bf16",
         "data": "synthetic (seeded; model-shaped weights, activations, LoRA r=32, rewards)",
-        "config": {"workload": workload_name(cfg, rcfg),
-                   "M": M, "K": K, "N": N, "lora_rank": 32, "prompts": rcfg.P, "seeds": rcfg.N,
-                   "selected": Kr, "parallelism": f"replicas x{world}",
-                   "l2": f"inputs larger than L2 within a step (X {x_mb:.0f} MB read, Y {y_mb:.0f} MB "
-                         "written twice per step)"},
+        "config": bench_config(cfg, rcfg, world),
         "value_basis": "mean CUDA-event duration of the nvfp4_gemm launch inside the timed steps",
         "requant_gbs": round(rq_gbs, 1),
         "act_quant_gbs": round(aq_gbs, 1),
@@ -1014,8 +1019,7 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": round(total / args.steps * 1e3, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp64 over NVFP4 values (oracle)", "data": "synthetic (seeded)",
-        "config": {"workload": workload_name(cfg, rcfg),
-                   "parallelism": f"oracle on host cores (rank 0 of {world})"},
+        "config": bench_config(cfg, rcfg, world),
         "cpu_baseline": {"value": round(v, 6), "unit": "TFLOP/s", "cores": oracle.num_threads(),
                          "kind": "oracle",
                          "sample": f"per step: full-weight requant, act_quant + fp64 GEMM of "
