@@ -218,3 +218,56 @@ def test_prescaled_and_rowamax_validation(lib):
     assert g(*ok, P(BAD), 4, 256, 256, None) == 3
     assert g(*ok, P(A16), 4, 256, 100, None) == 2
     assert g(*ok, None, 0, 256, 256, None) == 0                              # M == 0
+
+
+def test_block_entry_points_validation(lib):
+    """The synthetic DiT block's entry points check shapes, pointers and alignment before
+    any CUDA call (shape rules: D % 64, dh = D/H in {64, 128}, S % 64)."""
+    P = ctypes.c_void_p
+    W = (ctypes.c_void_p * 16)(*([A16] * 16))  # 4 x {codes, sf, s_t, bias}
+    blk, att = lib.nvfp4_dit_block, lib.nvfp4_dit_attention
+    need = lib.nvfp4_dit_block_workspace_bytes(2, 128, 256, 2)
+    # shapes
+    assert blk(P(A16), 2, 100, 256, 2, W, P(A16), P(A16), need, None) == 2      # S % 64
+    assert blk(P(A16), 1, 128, 384, 2, W, P(A16), P(A16), need, None) == 2      # dh = 192
+    assert blk(P(A16), 2, 128, 256, 2, W, P(A16), P(A16), need - 256, None) == 2  # workspace too small
+    # pointers and alignment
+    assert blk(None, 2, 128, 256, 2, W, P(A16), P(A16), need, None) == 1
+    assert blk(P(A16), 2, 128, 256, 2, None, P(A16), P(A16), need, None) == 1
+    W0 = (ctypes.c_void_p * 16)(*([A16] * 16))
+    W0[2] = None  # the first linear's s_t
+    assert blk(P(A16), 2, 128, 256, 2, W0, P(A16), P(A16), need, None) == 1
+    assert blk(P(BAD), 2, 128, 256, 2, W, P(A16), P(A16), need, None) == 3
+    assert blk(P(A16), 2, 128, 256, 2, W, P(A16), P(A16 + 16), need, None) == 3  # workspace 256-aligned
+    need_a = lib.nvfp4_dit_attention_workspace_bytes(2, 128, 256, 2)
+    assert att(P(A16), 2, 100, 256, 2, P(A16), P(A16), need_a, None) == 2
+    assert att(None, 2, 128, 256, 2, P(A16), P(A16), need_a, None) == 1
+    assert att(P(A16), 2, 128, 256, 2, P(BAD), P(A16), need_a, None) == 3
+    assert att(P(A16), 2, 128, 256, 2, P(A16), P(A16), need_a - 1, None) == 2
+    # the streaming steps
+    assert lib.bf16_softmax_rows(P(A16), 4, 12, ctypes.c_float(1.0), P(A16), None) == 2   # cols % 8
+    assert lib.bf16_softmax_rows(None, 0, 16, ctypes.c_float(1.0), None, None) == 0      # empty
+    assert lib.bf16_softmax_rows(None, 4, 16, ctypes.c_float(1.0), P(A16), None) == 1
+    assert lib.bf16_softmax_rows(P(BAD), 4, 16, ctypes.c_float(1.0), P(A16), None) == 3
+    assert lib.bf16_gelu(P(A16), 12, P(A16), None) == 2
+    assert lib.bf16_gelu(None, 0, None, None) == 0
+    assert lib.bf16_gelu(P(A16), 16, None, None) == 1
+    assert lib.bf16_add(P(A16), P(BAD), 16, P(A16), None) == 3
+    assert lib.bf16_add(P(A16), P(A16), -8, P(A16), None) == 2
+
+
+def test_block_workspace_sizes(lib):
+    """0 for shapes outside the rules; otherwise 256-byte multiples that hold at least
+    the block's bf16 intermediates (qkv, the MLP hidden, h1: 8 T D values), growing
+    with the batch; the attention's scratch is V transposed (T D values)."""
+    blk, att = lib.nvfp4_dit_block_workspace_bytes, lib.nvfp4_dit_attention_workspace_bytes
+    for bad in [(1, 100, 256, 2), (1, 128, 256, 3), (1, 128, 384, 2), (0, 128, 256, 2), (1, 128, 96, 1)]:
+        assert blk(*bad) == 0 and att(*bad) == 0
+    prev = 0
+    for B in (1, 2, 8):
+        T, D = B * 4608, 3072
+        n = blk(B, 4608, D, 24)
+        assert n % 256 == 0 and n >= 2 * 8 * T * D and n > prev
+        prev = n
+        assert att(B, 4608, D, 24) == 2 * T * D
+    assert blk(2, 128, 256, 4) > 0  # dh = 64
