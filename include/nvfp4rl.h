@@ -437,6 +437,20 @@ nvfp4_status nvfp4_test_gemm_withhold(const uint8_t* a_codes, const uint8_t* a_s
                                       void* Y, int64_t M, int64_t N, int64_t K, int withhold_kb,
                                       int64_t timeout_ns, void* stream);
 
+/*
+ * nvfp4_dit_attention with one K tile (256 keys) of pass 1 left unloaded on purpose:
+ * both CTAs of the first CTA pair skip the copies of tile withhold_tile
+ * (0 <= withhold_tile < ceil(S / 256)) for their first item and never announce them,
+ * and every wait of the kernel is bounded by timeout_ns (1e6 .. 1e9) instead of the
+ * usual 4 s.  The pair's MMA issuer, producer and softmax warps must all give up,
+ * record NVFP4_ERR_TIMEOUT, let their own copies and MMAs land, free tensor memory and
+ * exit; o is then incomplete.  Nothing is read or written out of bounds.  Exists to
+ * exercise the attention's abort path without faulting anything.
+ */
+nvfp4_status nvfp4_test_attention_withhold(const void* qkv, int64_t B, int64_t S, int64_t D, int64_t H, void* o,
+                                           void* workspace, size_t workspace_bytes, int withhold_tile,
+                                           int64_t timeout_ns, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

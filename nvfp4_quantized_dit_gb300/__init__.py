@@ -23,7 +23,7 @@ __all__ = [
     "nvfp4_act_quant_tensor", "nvfp4_gemm", "bf16_gemm", "select_contrastive",
     "nvfp4_device_status", "nvfp4_status_string", "nvfp4_version",
     "nvfp4_test_e2m1", "nvfp4_test_e4m3", "nvfp4_test_e2m1_quotient", "nvfp4_test_e4m3_quotient",
-    "nvfp4_test_e4m3_decode", "nvfp4_test_merge", "nvfp4_test_wait_timeout", "nvfp4_test_gemm_withhold",
+    "nvfp4_test_e4m3_decode", "nvfp4_test_merge", "nvfp4_test_wait_timeout", "nvfp4_test_gemm_withhold", "nvfp4_test_attention_withhold",
 ]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libnvfp4rl.so")
@@ -77,6 +77,7 @@ def library() -> ctypes.CDLL:
                 "nvfp4_test_merge": [P, I, P, P, I, F, I64, I64, P, P],
                 "nvfp4_test_wait_timeout": [I64, P],
                 "nvfp4_test_gemm_withhold": [P, P, P, P, P, P, P, I64, I64, I64, I, I64, P],
+                "nvfp4_test_attention_withhold": [P, I64, I64, I64, I64, P, P, ctypes.c_size_t, I, I64, P],
             }
             for name, args in sig.items():
                 fn = getattr(L, name)
@@ -445,6 +446,19 @@ def nvfp4_dit_attention(qkv, B: int, S: int, H: int, o=None, workspace=None, str
     workspace = _workspace(dit_attention_workspace_bytes(B, S, D, H), qkv.device, workspace)
     _call("nvfp4_dit_attention", _dev(qkv, "qkv", torch.bfloat16), B, S, D, H, _dev(o, "o", torch.bfloat16),
           _dev(workspace, "workspace", torch.uint8), workspace.numel(), _stream(stream))
+    return o
+
+
+def nvfp4_test_attention_withhold(qkv, B: int, S: int, H: int, withhold_tile: int, timeout_ns: int, stream=None):
+    """nvfp4_dit_attention with one K tile of the first CTA pair never loaded (test hook
+    of the attention's abort path); returns the (incomplete) output."""
+    T, D3 = qkv.shape
+    D = D3 // 3
+    o = torch.empty(T, D, dtype=torch.bfloat16, device=qkv.device)
+    workspace = _workspace(dit_attention_workspace_bytes(B, S, D, H), qkv.device, None)
+    _call("nvfp4_test_attention_withhold", _dev(qkv, "qkv", torch.bfloat16), B, S, D, H, _dev(o, "o", torch.bfloat16),
+          _dev(workspace, "workspace", torch.uint8), workspace.numel(), int(withhold_tile), int(timeout_ns),
+          _stream(stream))
     return o
 
 

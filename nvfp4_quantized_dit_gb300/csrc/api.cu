@@ -421,7 +421,7 @@ size_t nvfp4_dit_attention_workspace_bytes(int64_t B, int64_t S, int64_t D, int6
 // The attention of the block: v transposed per head, then the fused two-pass kernel
 // (attn.cu), which reads q and k from qkv and writes o in the [B*S, D] layout.
 static nvfp4_status attention_run(const LaunchCtx& ctx, const uint16_t* qkv, int64_t B, int64_t S, int64_t D,
-                                  int64_t H, uint16_t* o, uint16_t* Vt) {
+                                  int64_t H, uint16_t* o, uint16_t* Vt, int withhold = -1, int64_t wait_limit_ns = 0) {
     const int64_t dh = D / H, T = B * S;
     CUtensorMap tqk, tv;
     if (!encode_2d(&tqk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, qkv, (uint64_t)(3 * D), (uint64_t)T, (uint64_t)(3 * D) * 2,
@@ -432,11 +432,12 @@ static nvfp4_status attention_run(const LaunchCtx& ctx, const uint16_t* qkv, int
     cudaError_t e = launch_heads_vt(ctx, qkv, B, S, D, H, Vt);
     if (e != cudaSuccess) return from_cuda(e);
     const float scale = 1.0f / sqrtf((float)dh);
-    return from_cuda(launch_attention(ctx, tqk, tv, o, B, S, D, H, scale));
+    return from_cuda(launch_attention(ctx, tqk, tv, o, B, S, D, H, scale, withhold, wait_limit_ns));
 }
 
-nvfp4_status nvfp4_dit_attention(const void* qkv, int64_t B, int64_t S, int64_t D, int64_t H, void* o,
-                                 void* workspace, size_t workspace_bytes, void* stream) {
+static nvfp4_status dit_attention_call(const void* qkv, int64_t B, int64_t S, int64_t D, int64_t H, void* o,
+                                       void* workspace, size_t workspace_bytes, void* stream, int withhold,
+                                       int64_t wait_limit_ns) {
     if (!block_shape_ok(B, S, D, H)) return NVFP4_ERR_SHAPE;
     if (!qkv || !o || !workspace) return NVFP4_ERR_NULL;
     if (misaligned(qkv, 16) || misaligned(o, 16) || misaligned(workspace, 256)) return NVFP4_ERR_ALIGN;
@@ -445,7 +446,21 @@ nvfp4_status nvfp4_dit_attention(const void* qkv, int64_t B, int64_t S, int64_t 
     const nvfp4_status st = resolve(stream, &ctx);
     if (st != NVFP4_OK) return st;
     return attention_run(ctx, static_cast<const uint16_t*>(qkv), B, S, D, H, static_cast<uint16_t*>(o),
-                         static_cast<uint16_t*>(workspace));
+                         static_cast<uint16_t*>(workspace), withhold, wait_limit_ns);
+}
+
+nvfp4_status nvfp4_dit_attention(const void* qkv, int64_t B, int64_t S, int64_t D, int64_t H, void* o,
+                                 void* workspace, size_t workspace_bytes, void* stream) {
+    return dit_attention_call(qkv, B, S, D, H, o, workspace, workspace_bytes, stream, -1, 0);
+}
+
+nvfp4_status nvfp4_test_attention_withhold(const void* qkv, int64_t B, int64_t S, int64_t D, int64_t H, void* o,
+                                           void* workspace, size_t workspace_bytes, int withhold_tile,
+                                           int64_t timeout_ns, void* stream) {
+    const int64_t n_tiles = (S + 255) / 256;
+    if (withhold_tile < 0 || withhold_tile >= n_tiles || timeout_ns < 1000000 || timeout_ns > 1000000000LL)
+        return NVFP4_ERR_SHAPE;
+    return dit_attention_call(qkv, B, S, D, H, o, workspace, workspace_bytes, stream, withhold_tile, timeout_ns);
 }
 
 // Block scratch: R1 [3 T D] holds qkv, then o; R2 [4 T D] holds the attention's V^T,

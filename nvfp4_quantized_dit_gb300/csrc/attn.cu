@@ -84,6 +84,9 @@ struct AttnArgs {
     int items;          // B * H * nqb
     float c;            // scale * log2(e)
     int* status;
+    uint64_t wait_ns;   // bound of every wait (kAttnWaitNs; shorter in the test hook)
+    int withhold;       // test hook only: K tile of pass 1 that the first pair never loads for its
+                        // first item (nothing issued, nothing announced), or -1
 };
 
 // 2^x (hardware approximation; results below 2^-126 flush to zero, which changes no
@@ -229,7 +232,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const int row0 = b * S;
                 const int qcol = h * kDh, kcol = D + h * kDh;
                 // Q: once the previous item's last L tile has been formed.
-                if (!mbar_wait(q_empty, (uint32_t)((it & 1) ^ 1), args.status, abort_flag, kAttnWaitNs)) break;
+                if (!mbar_wait(q_empty, (uint32_t)((it & 1) ^ 1), args.status, abort_flag, args.wait_ns)) break;
                 if (leader) mbar_arrive_expect_tx(q_full, kPairCtas * C::kQBytes);
 #pragma unroll
                 for (int i = 0; i < kDh / 64; ++i)
@@ -237,10 +240,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                      row0 + qb * (kRowsCta * kPairCtas) + (int)rank * kRowsCta);
                 for (int pass = 0; ok && pass < 2; ++pass) {
                     for (int j = 0; j < n_tiles; ++j) {
+                        if (pass == 0 && j == args.withhold && it == 0 && first == 0) {
+                            // Test hook: this K tile is never loaded nor announced, so the pair's
+                            // MMA issuer and softmax warps run into their bounded waits.
+                            ++kc;
+                            continue;
+                        }
                         {
                             const int s = kc % kStagesK;
                             if (!mbar_wait(&k_empty[s], (uint32_t)(((kc / kStagesK) & 1) ^ 1), args.status,
-                                           abort_flag, kAttnWaitNs)) {
+                                           abort_flag, args.wait_ns)) {
                                 ok = false;
                                 break;
                             }
@@ -256,7 +265,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         if (pass == 1) {
                             const int s = vc % kStagesV;
                             if (!mbar_wait(&v_empty[s], (uint32_t)(((vc / kStagesV) & 1) ^ 1), args.status,
-                                           abort_flag, kAttnWaitNs)) {
+                                           abort_flag, args.wait_ns)) {
                                 ok = false;
                                 break;
                             }
@@ -275,11 +284,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 // Tail: the releases of the last fills land before this CTA leaves.
                 for (int i = (kc > kStagesK ? kc - kStagesK : 0); i < kc; ++i)
                     if (!mbar_wait(&k_empty[i % kStagesK], (uint32_t)((i / kStagesK) & 1), args.status, abort_flag,
-                                   kAttnWaitNs))
+                                   args.wait_ns))
                         break;
                 for (int i = (vc > kStagesV ? vc - kStagesV : 0); i < vc; ++i)
                     if (!mbar_wait(&v_empty[i % kStagesV], (uint32_t)((i / kStagesV) & 1), args.status, abort_flag,
-                                   kAttnWaitNs))
+                                   args.wait_ns))
                         break;
             }
             if (*abort_flag) {
@@ -301,8 +310,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // dh/16 MMAs, release the stage, announce the tile.
             auto issue_l = [&]() -> bool {
                 const int s = kc % kStagesK;
-                if (!mbar_wait(&k_full[s], (uint32_t)((kc / kStagesK) & 1), args.status, abort_flag, kAttnWaitNs) ||
-                    !mbar_wait<true>(s_empty, (uint32_t)((g & 1) ^ 1), args.status, abort_flag, kAttnWaitNs))
+                if (!mbar_wait(&k_full[s], (uint32_t)((kc / kStagesK) & 1), args.status, abort_flag, args.wait_ns) ||
+                    !mbar_wait<true>(s_empty, (uint32_t)((g & 1) ^ 1), args.status, abort_flag, args.wait_ns))
                     return false;
                 tc_fence_after_sync();
                 const uint64_t kd = k_desc0 + (uint64_t)((s * C::kKBytes) >> 4);
@@ -319,7 +328,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 return true;
             };
             for (int item = first; ok && item < args.items; item += step, ++it) {
-                if (!(ok = mbar_wait(q_full, (uint32_t)(it & 1), args.status, abort_flag, kAttnWaitNs))) break;
+                if (!(ok = mbar_wait(q_full, (uint32_t)(it & 1), args.status, abort_flag, args.wait_ns))) break;
                 // L tiles of both passes in order; in pass 2 tile j + 1 is queued before the
                 // P v of tile j, so it is ready when the softmax is.  After the item's last L
                 // tile Q is released to the producer (the next item's Q loads meanwhile).
@@ -331,12 +340,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         if (j + 2 == n_tiles) mma_commit_pair_multicast(q_empty, kBoth);
                     }
                     const int s = vc % kStagesV;
-                    if (!mbar_wait(&v_full[s], (uint32_t)((vc / kStagesV) & 1), args.status, abort_flag, kAttnWaitNs) ||
-                        !mbar_wait<true>(p_full, (uint32_t)(pj & 1), args.status, abort_flag, kAttnWaitNs) ||
+                    if (!mbar_wait(&v_full[s], (uint32_t)((vc / kStagesV) & 1), args.status, abort_flag, args.wait_ns) ||
+                        !mbar_wait<true>(p_full, (uint32_t)(pj & 1), args.status, abort_flag, args.wait_ns) ||
                         // The first P v of an item overwrites O: the previous item's O must
                         // have been read out.
                         (j == 0 && !mbar_wait<true>(o_free, (uint32_t)((it & 1) ^ 1), args.status, abort_flag,
-                                                    kAttnWaitNs))) {
+                                                    args.wait_ns))) {
                         ok = false;
                         break;
                     }
@@ -381,7 +390,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int g = 0; ok && g < 2 * n_tiles; ++g, ++gg) {
                 const int j = g < n_tiles ? g : g - n_tiles;
                 const int valid = min(kTileKeys, S - j * kTileKeys);
-                ok = mbar_wait(s_full, (uint32_t)(gg & 1), args.status, abort_flag, kAttnWaitNs);
+                ok = mbar_wait(s_full, (uint32_t)(gg & 1), args.status, abort_flag, args.wait_ns);
                 ok = __all_sync(0xFFFFFFFFu, ok);  // tcgen05.ld is .sync.aligned
                 if (!ok) break;
                 tc_fence_after_sync();
@@ -426,7 +435,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         stats[(slice * 2 + 0) * kRowsCta + row] = m;
                         stats[(slice * 2 + 1) * kRowsCta + row] = sum;
                         mbar_arrive(stats_ready);
-                        ok = mbar_wait(stats_ready, (uint32_t)(it & 1), args.status, abort_flag, kAttnWaitNs);
+                        ok = mbar_wait(stats_ready, (uint32_t)(it & 1), args.status, abort_flag, args.wait_ns);
                         ok = __all_sync(0xFFFFFFFFu, ok);
                         if (!ok) break;
                         float ms[kSlices], ss[kSlices], mm = -INFINITY;
@@ -451,7 +460,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const float2 a = __ffma2_rn(unpack_bf16x2(lbits[i]), c2, nmc);
                         p[i] = bf16x2(ex2(a.x), ex2(a.y));
                     }
-                    ok = mbar_wait(p_free, (uint32_t)((pj & 1) ^ 1), args.status, abort_flag, kAttnWaitNs);
+                    ok = mbar_wait(p_free, (uint32_t)((pj & 1) ^ 1), args.status, abort_flag, args.wait_ns);
                     ok = __all_sync(0xFFFFFFFFu, ok);  // tcgen05.st is .sync.aligned
                     if (!ok) break;
                     tc_fence_after_sync();
@@ -464,7 +473,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
             }
             if (ok) {
-                ok = mbar_wait(o_full, (uint32_t)(it & 1), args.status, abort_flag, kAttnWaitNs);
+                ok = mbar_wait(o_full, (uint32_t)(it & 1), args.status, abort_flag, args.wait_ns);
                 ok = __all_sync(0xFFFFFFFFu, ok);
             }
             if (!ok) break;
@@ -535,12 +544,14 @@ cudaError_t run_attn(const LaunchCtx& ctx, const CUtensorMap& tqk, const CUtenso
 }  // namespace
 
 cudaError_t launch_attention(const LaunchCtx& ctx, const CUtensorMap& tmap_qk, const CUtensorMap& tmap_vt,
-                             uint16_t* o, int64_t B, int64_t S, int64_t D, int64_t H, float scale) {
+                             uint16_t* o, int64_t B, int64_t S, int64_t D, int64_t H, float scale, int withhold,
+                             int64_t wait_limit_ns) {
     const int64_t dh = D / H;
     const int64_t nqb = (S + kRowsCta * kPairCtas - 1) / (kRowsCta * kPairCtas);
     const int64_t items = B * H * nqb;
     if (items <= 0 || items > 0x7FFFFFFF) return cudaErrorInvalidValue;
-    AttnArgs a{o, (int)S, (int)D, (int)H, (int)nqb, (int)items, scale * 1.4426950408889634f, ctx.status};
+    AttnArgs a{o, (int)S, (int)D, (int)H, (int)nqb, (int)items, scale * 1.4426950408889634f, ctx.status,
+               wait_limit_ns > 0 ? (uint64_t)wait_limit_ns : kAttnWaitNs, withhold};
     if (dh == 128) return run_attn<128>(ctx, tmap_qk, tmap_vt, a);
     if (dh == 64) return run_attn<64>(ctx, tmap_qk, tmap_vt, a);
     return cudaErrorInvalidValue;

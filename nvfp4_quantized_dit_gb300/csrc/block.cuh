@@ -12,8 +12,10 @@ cudaError_t launch_heads_vt(const LaunchCtx&, const uint16_t* qkv, int64_t B, in
 // The fused attention (attn.cu): Q and K tiles from qkv [B*S, 3D] (tmap_qk: 64 x 128
 // boxes, 128-byte swizzle), V^T [B*H*dh, S] (tmap_vt: 64 x dh/2 boxes), o [B*S, D]
 // written at columns h*dh; dh = D/H is 64 or 128.
+// withhold >= 0 and wait_limit_ns > 0 only from the test hook (nvfp4_test_attention_withhold).
 cudaError_t launch_attention(const LaunchCtx&, const CUtensorMap& tmap_qk, const CUtensorMap& tmap_vt, uint16_t* o,
-                             int64_t B, int64_t S, int64_t D, int64_t H, float scale);
+                             int64_t B, int64_t S, int64_t D, int64_t H, float scale, int withhold = -1,
+                             int64_t wait_limit_ns = 0);
 cudaError_t launch_softmax_rows(const LaunchCtx&, const uint16_t* L, int64_t rows, int64_t cols, float scale,
                                 uint16_t* P);
 // The NVFP4 GEMM (gemm.cu) with one of the block's epilogues applied to each output

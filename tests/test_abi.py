@@ -271,3 +271,14 @@ def test_block_workspace_sizes(lib):
         prev = n
         assert att(B, 4608, D, 24) == 2 * T * D
     assert blk(2, 128, 256, 4) > 0  # dh = 64
+
+
+def test_attention_withhold_hook_validation(lib):
+    P = ctypes.c_void_p
+    f = lib.nvfp4_test_attention_withhold
+    need = lib.nvfp4_dit_attention_workspace_bytes(2, 512, 256, 2)
+    assert f(P(A16), 2, 512, 256, 2, P(A16), P(A16), need, 2, 50_000_000, None) == 2   # 2 tiles of 256 keys
+    assert f(P(A16), 2, 512, 256, 2, P(A16), P(A16), need, -1, 50_000_000, None) == 2
+    assert f(P(A16), 2, 512, 256, 2, P(A16), P(A16), need, 1, 10, None) == 2           # timeout range
+    assert f(P(A16), 2, 500, 256, 2, P(A16), P(A16), need, 1, 50_000_000, None) == 2   # S % 64
+    assert f(None, 2, 512, 256, 2, P(A16), P(A16), need, 1, 50_000_000, None) == 1

@@ -68,3 +68,44 @@ def test_gemm_abort_path_frees_everything_and_the_next_call_is_clean(orc):
     rows = np.concatenate([np.arange(0, 8192, 61), np.arange(M2 - 8, M2)])
     y_ref2, S2 = orc.gemm_nvfp4(ac2, asf2, a_s2, wc2, wsf2, w_s2[:1], rows=rows)
     assert_gemm_close(np_(y2)[rows], y_ref2, S2, "every SM after abort")
+
+
+def test_attention_abort_path_frees_everything():
+    """The fused attention's own abort path: one K tile of the first CTA pair is never
+    loaded (test hook), every wait is bounded by 50 ms.  The pair must record
+    NVFP4_ERR_TIMEOUT and exit with its tensor memory freed: the same attention then
+    runs correctly, and so does a larger one that puts a CTA pair on every SM."""
+    require_gpu()
+    import numpy as np
+
+    import oracle as orc
+    from gpu_util import np_
+
+    def bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(orc.bf16_rne(a)).view(np.int16)).view(torch.bfloat16).cuda()
+
+    def check(o, qkv, B, S, H, images):
+        o, qkv = np_(o), np_(qkv)
+        D = qkv.shape[1] // 3
+        for b in images:
+            rs = slice(b * S, (b + 1) * S)
+            ref = orc.attention(qkv[rs], 1, S, H)
+            vo, vr = orc.bf16_value(o[rs]), orc.bf16_value(ref)
+            assert (o[rs] == ref).mean() > 0.95
+            assert np.max(np.abs(vo - vr)) <= 2.0 ** -6 * np.max(np.abs(vr))
+        assert o.shape[1] == D
+
+    assert nv.nvfp4_device_status(clear=True) in (0, 6)
+    rng = np.random.default_rng(31)
+    B, S, D, H = 2, 512, 256, 2
+    qkv = bf16(rng.standard_normal((B * S, 3 * D)) * 0.5)
+    nv.nvfp4_test_attention_withhold(qkv, B, S, H, withhold_tile=1, timeout_ns=50_000_000)
+    assert nv.nvfp4_device_status(clear=True) == 6
+    o = nv.nvfp4_dit_attention(qkv, B, S, H)
+    assert nv.nvfp4_device_status(clear=True) == 0
+    check(o, qkv, B, S, H, range(B))
+    B2, S2 = 8, 2048  # 128 items (image-head, 256 query rows): every pair of the persistent grid works
+    qkv2 = bf16(rng.standard_normal((B2 * S2, 3 * D)) * 0.5)
+    o2 = nv.nvfp4_dit_attention(qkv2, B2, S2, H)
+    assert nv.nvfp4_device_status(clear=True) == 0
+    check(o2, qkv2, B2, S2, H, [0, B2 - 1])
