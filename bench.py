@@ -72,9 +72,9 @@ def source_hash(*rel):
 
 KERNEL_SOURCES = {
     "nvfp4_gemm": ["nvfp4_quantized_dit_gb300/csrc/gemm.cu", "nvfp4_quantized_dit_gb300/csrc/common.cuh",
-                   "nvfp4_quantized_dit_gb300/csrc/block.cuh"],
+                   "nvfp4_quantized_dit_gb300/csrc/gemm_epilogue.cuh"],
     "bf16_gemm": ["nvfp4_quantized_dit_gb300/csrc/gemm.cu", "nvfp4_quantized_dit_gb300/csrc/common.cuh",
-                  "nvfp4_quantized_dit_gb300/csrc/block.cuh"],
+                  "nvfp4_quantized_dit_gb300/csrc/gemm_epilogue.cuh"],
     "nvfp4_act_quant": ["nvfp4_quantized_dit_gb300/csrc/quant.cu", "nvfp4_quantized_dit_gb300/csrc/common.cuh"],
     "nvfp4_act_quant_prescaled": ["nvfp4_quantized_dit_gb300/csrc/quant.cu",
                                   "nvfp4_quantized_dit_gb300/csrc/common.cuh"],

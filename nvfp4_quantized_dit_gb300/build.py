@@ -22,7 +22,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "libnvfp4rl.so")
 SOURCES = ["api.cu", "quant.cu", "select.cu", "gemm.cu", "merge_tc.cu", "block.cu", "attn.cu"]
-HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "block.cuh"), os.path.join(INCLUDE, "nvfp4rl.h")]
+HEADERS = [os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "block.cuh"), os.path.join(CSRC, "gemm_epilogue.cuh"), os.path.join(INCLUDE, "nvfp4rl.h")]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

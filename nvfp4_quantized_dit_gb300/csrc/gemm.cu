@@ -46,8 +46,8 @@
 // Every mbarrier wait is bounded (common.cuh: mbar_wait); on expiry the kernel
 // records NVFP4_ERR_TIMEOUT, drains its own copies and MMAs (again bounded),
 // frees tensor memory and returns.
-#include "block.cuh"
 #include "common.cuh"
+#include "gemm_epilogue.cuh"
 
 namespace nvfp4rl {
 namespace {
