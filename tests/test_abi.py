@@ -282,3 +282,25 @@ def test_attention_withhold_hook_validation(lib):
     assert f(P(A16), 2, 512, 256, 2, P(A16), P(A16), need, 1, 10, None) == 2           # timeout range
     assert f(P(A16), 2, 500, 256, 2, P(A16), P(A16), need, 1, 50_000_000, None) == 2   # S % 64
     assert f(None, 2, 512, 256, 2, P(A16), P(A16), need, 1, 50_000_000, None) == 1
+
+
+def test_header_is_plain_c(tmp_path):
+    """The boundary is a C ABI: the header compiles as C99 and C11 (pedantic, all
+    warnings as errors), structs and inline helpers included."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "nvfp4rl.h"\n'
+                   "int main(void) {\n"
+                   "    nvfp4_linear_weights w[4] = {{0}};\n"
+                   "    (void)w;\n"
+                   "    return nvfp4_sf_bytes(128, 64) == 512 && nvfp4_sf_offset(1, 0, 64) == 16 ? 0 : 1;\n"
+                   "}\n")
+    for std in ("c99", "c11"):
+        exe = tmp_path / f"use_header_{std}"
+        subprocess.run([gcc, f"-std={std}", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                        "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+        assert subprocess.run([str(exe)]).returncode == 0
