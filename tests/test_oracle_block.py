@@ -223,3 +223,29 @@ def test_block_rows_unquantized_mode():
     u = orc.bf16_value(orc.dit_block_rows(x, w, {}, B, S, H, rows, quantize_activations=False))
     gap = np.linalg.norm(q - u) / np.linalg.norm(u)
     assert 1e-3 < gap < 0.2
+
+
+def test_attention_head_applies_the_scale():
+    """Two keys whose logits differ by a: P = (1/(1 + e^(-a s)), 1/(1 + e^(a s))) with s =
+    1/sqrt(dh) (dh = 64: s = 1/8 exactly, dh = 128: the fp32 value of 1/sqrt(128)); v
+    picks each probability out into its own column of O.  A missing or different scale
+    (none, 1/dh, sqrt(dh)) changes P by far more than a bf16 step."""
+    for dh in (64, 128):
+        s = float(np.float32(1.0) / np.sqrt(np.float32(dh)))
+        for a in (1.0, 4.0, 10.0, -7.5):
+            q = np.zeros((2, dh), np.uint16)
+            k = np.zeros((2, dh), np.uint16)
+            v = np.zeros((2, dh), np.uint16)
+            q[:, 0] = orc.bf16_rne(a)
+            k[0, 0] = orc.bf16_rne(1.0)  # logits: a for key 0, 0 for key 1 (exact in bf16)
+            v[0, 1] = orc.bf16_rne(1.0)
+            v[1, 2] = orc.bf16_rne(1.0)
+            o = orc.bf16_value(orc.attention_head(q, k, v))
+            p0 = 1.0 / (1.0 + np.exp(-a * s))
+            p1 = 1.0 / (1.0 + np.exp(a * s))
+            for col, p in ((1, p0), (2, p1)):
+                # P is rounded to bf16, then O = bf16(P * 1): two roundings of p
+                assert np.all(o[:, col] == orc.bf16_value(orc.bf16_rne(orc.bf16_value(orc.bf16_rne(p)))))
+            for wrong in (1.0, 1.0 / dh, np.sqrt(dh)):
+                pw = 1.0 / (1.0 + np.exp(-a * wrong))
+                assert abs(pw - p0) > 2.0 ** -7 * max(p0, 1e-30)
