@@ -98,32 +98,50 @@ def dram_traffic(kernel, workload):
 
 
 class ClockSampler:
-    """Samples nvidia-smi clocks and throttle reasons during the timed region."""
+    """Samples nvidia-smi clocks and throttle reasons during the timed region.
+
+    The sampler runs from before the region (start() returns once the first sample has
+    arrived, or after a bounded wait), begin() and end() bracket the region on the
+    host clock, and stop() summarises the samples that arrived inside the bracket (or
+    within one interval after it, for the query's own latency); a region shorter than
+    the interval falls back to the first sample that arrived after its start."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    INTERVAL_MS = 20
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.proc = None
-        self.lines = []
+        self.lines = []  # (host monotonic time of arrival, CSV line)
         self.thread = None
+        self.t_begin = None
+        self.t_end = None
 
-    def start(self):
+    def start(self, wait_s: float = 5.0):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", str(self.INTERVAL_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
             return
         self.thread = threading.Thread(target=self._read, daemon=True)
         self.thread.start()
+        deadline = time.monotonic() + wait_s
+        while not self.lines and self.proc.poll() is None and time.monotonic() < deadline:
+            time.sleep(0.01)
 
     def _read(self):
         for ln in self.proc.stdout:
-            self.lines.append(ln.strip())
+            self.lines.append((time.monotonic(), ln.strip()))
+
+    def begin(self):
+        self.t_begin = time.monotonic()
+
+    def end(self):
+        self.t_end = time.monotonic()
 
     def stop(self):
         if self.proc is None:
@@ -135,7 +153,20 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=5)
-        return self.summarize(self.lines)
+        return self.summarize(self.in_region(self.lines, self.t_begin, self.t_end, self.INTERVAL_MS / 1000.0))
+
+    @staticmethod
+    def in_region(stamped, t_begin, t_end, interval_s):
+        """The CSV lines of (arrival time, line) pairs that belong to the region
+        [t_begin, t_end]: those that arrived from its start to one interval after its end,
+        else the first one that arrived after its start.  Without a bracket, all lines."""
+        if t_begin is None or t_end is None:
+            return [ln for _, ln in stamped]
+        inside = [ln for t, ln in stamped if t_begin <= t <= t_end + interval_s]
+        if inside:
+            return inside
+        after = [ln for t, ln in stamped if t >= t_begin]
+        return after[:1]
 
     @staticmethod
     def summarize(lines):
@@ -633,11 +664,13 @@ def run_ours(args):
     torch.cuda.synchronize()
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
+    clocks.begin()
     t0.record()
     for s in range(args.steps):
         step(dev, ev[s])
     t1.record()
     torch.cuda.synchronize()
+    clocks.end()
     barrier(world, device)
     clk = clocks.stop()
     elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, device)

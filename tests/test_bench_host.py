@@ -3,6 +3,7 @@ only report a captured figure while the kernel's sources are unchanged, and the
 algorithmic byte counts the HBM rooflines divide by."""
 
 import dataclasses
+import os
 
 import bench
 import workloads
@@ -71,6 +72,44 @@ def test_clock_summary_from_nvidia_smi_lines():
     reasons = bench.ClockSampler.summarize(hot)["reasons"]
     assert reasons == ["hw_slowdown", "sw_power_cap", "sw_thermal_slowdown"]
     assert bench.ClockSampler.summarize([]) is None
+
+
+def test_clock_samples_are_taken_from_the_timed_region():
+    """Lines stamped with their arrival time: the region keeps those that arrived from
+    its start to one interval after its end; a region shorter than the interval keeps
+    the first sample after its start; no bracket keeps everything."""
+    stamped = [(0.90, "a"), (1.00, "b"), (1.02, "c"), (1.04, "d"), (1.07, "e"), (1.50, "f")]
+    pick = bench.ClockSampler.in_region
+    assert pick(stamped, 1.00, 1.03, 0.02) == ["b", "c", "d"]
+    assert pick(stamped, 1.045, 1.046, 0.02) == ["e"]   # nothing inside: the next sample
+    assert pick(stamped, 1.60, 1.70, 0.02) == []        # nothing after the start
+    assert pick(stamped, None, None, 0.02) == ["a", "b", "c", "d", "e", "f"]
+
+
+def test_clock_sampler_runs_a_fake_nvidia_smi(tmp_path, monkeypatch):
+    """The sampler end to end against a stand-in nvidia-smi that prints a CSV line every
+    20 ms: start() returns once sampling runs, the bracket keeps the samples of the
+    region, stop() ends the child."""
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\n"
+                    "i=0\n"
+                    "while [ $i -lt 250 ]; do\n"
+                    "  echo '0, 2070, 2070, 1000.0, 0x0, Not Active, Not Active, Not Active, Not Active'\n"
+                    "  i=$((i+1)); sleep 0.02\n"
+                    "done\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}:{os.environ.get('PATH', '')}")
+    import time
+    cs = bench.ClockSampler(0)
+    cs.start()
+    assert cs.lines, "start() returns once the first sample is in"
+    cs.begin()
+    time.sleep(0.2)
+    cs.end()
+    got = cs.stop()
+    assert cs.proc.poll() is not None
+    assert got["sm_mhz"] == 2070.0 and got["reasons"] == []
+    assert 2 <= got["samples"] < len(cs.lines)
 
 
 def test_report_line_has_the_contract_keys():
