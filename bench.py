@@ -104,7 +104,8 @@ class ClockSampler:
     arrived, or after a bounded wait), begin() and end() bracket the region on the
     host clock, and stop() summarises the samples that arrived inside the bracket (or
     within one interval after it, for the query's own latency); a region shorter than
-    the interval falls back to the first sample that arrived after its start."""
+    the interval falls back to the first sample that arrived after its start (stop()
+    waits for it, bounded)."""
 
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -118,20 +119,29 @@ class ClockSampler:
         self.thread = None
         self.t_begin = None
         self.t_end = None
+        self.interval_ms = self.INTERVAL_MS
 
     def start(self, wait_s: float = 5.0):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", str(self.INTERVAL_MS)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except OSError:
-            self.proc = None
-            return
-        self.thread = threading.Thread(target=self._read, daemon=True)
-        self.thread.start()
-        deadline = time.monotonic() + wait_s
-        while not self.lines and self.proc.poll() is None and time.monotonic() < deadline:
-            time.sleep(0.01)
+        # The recipe's 200 ms interval is the fallback should this nvidia-smi refuse a
+        # shorter one (it then exits without a sample).
+        for interval in (self.INTERVAL_MS, 200):
+            self.interval_ms = interval
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", str(interval)],
+                    stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            except OSError:
+                self.proc = None
+                return
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            deadline = time.monotonic() + wait_s
+            while not self.lines and self.proc.poll() is None and time.monotonic() < deadline:
+                time.sleep(0.01)
+            if self.lines or self.proc.poll() is None:
+                return
+            self.thread.join(timeout=5)
 
     def _read(self):
         for ln in self.proc.stdout:
@@ -146,6 +156,12 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return None
+        # A region shorter than the interval may end before its first sample: wait
+        # (bounded) for one that arrives after the region's start.
+        deadline = time.monotonic() + 2 * self.interval_ms / 1000.0 + 0.5
+        while (self.t_begin is not None and not any(t >= self.t_begin for t, _ in self.lines)
+               and self.proc.poll() is None and time.monotonic() < deadline):
+            time.sleep(0.01)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -153,7 +169,7 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=5)
-        return self.summarize(self.in_region(self.lines, self.t_begin, self.t_end, self.INTERVAL_MS / 1000.0))
+        return self.summarize(self.in_region(self.lines, self.t_begin, self.t_end, self.interval_ms / 1000.0))
 
     @staticmethod
     def in_region(stamped, t_begin, t_end, interval_s):

@@ -112,6 +112,28 @@ def test_clock_sampler_runs_a_fake_nvidia_smi(tmp_path, monkeypatch):
     assert 2 <= got["samples"] < len(cs.lines)
 
 
+def test_clock_sampler_falls_back_to_the_longer_interval(tmp_path, monkeypatch):
+    """A stand-in nvidia-smi that refuses -lms 20 (exits at once, no output) and samples
+    at -lms 200: the sampler retries with 200 ms and still summarises."""
+    fake = tmp_path / "nvidia-smi"
+    fake.write_text("#!/bin/sh\n"
+                    "for a in \"$@\"; do [ \"$a\" = 20 ] && exit 1; done\n"
+                    "i=0\n"
+                    "while [ $i -lt 50 ]; do\n"
+                    "  echo '0, 1980, 2070, 1000.0, 0x4, Not Active, Not Active, Not Active, Active'\n"
+                    "  i=$((i+1)); sleep 0.2\n"
+                    "done\n")
+    fake.chmod(0o755)
+    monkeypatch.setenv("PATH", f"{tmp_path}:{os.environ.get('PATH', '')}")
+    cs = bench.ClockSampler(0)
+    cs.start()
+    assert cs.interval_ms == 200 and cs.lines
+    cs.begin()
+    cs.end()
+    got = cs.stop()
+    assert got == {"sm_mhz": 1980.0, "sm_max_mhz": 2070.0, "samples": 1, "reasons": ["sw_power_cap"]}
+
+
 def test_report_line_has_the_contract_keys():
     """The JSON line bench.py prints, from made-up timings (no GPU): every key of the
     contract is there and the derived numbers follow from the timings."""
